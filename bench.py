@@ -1,0 +1,379 @@
+#!/usr/bin/env python
+"""Throughput of one pre-LN tensor-parallel GPT layer, forward + backward, on GB300.
+
+A step is one forward and one backward pass of the whole layer (every kernel of
+the C ABI's mtl_layer_fwd and mtl_layer_bwd) over one batch of seeded synthetic
+input.  Default workload: the 8.3B-model-shaped layer (h=3072, 32 heads, seq
+1024, batch 16, ffn 12288, t=8 partitions laid out on one GPU).  Its inputs and
+activations (several GB) are far larger than L2, so no flush is needed between
+steps.
+
+Prints one JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+on a bounded sample instead.  Under torchrun each rank runs an independent
+replica (the layer is not sharded across GPUs).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synthetic  # noqa: E402
+
+METRIC = "layer fwd+bwd TFLOP/s on 1 GB300 and % of BF16 dense peak; oracle-match"
+KIND_NAMES = {1: "gemm_tc", 2: "gemm_simt", 3: "attn_fwd", 4: "attn_bwd", 5: "ln_fwd",
+              6: "ln_bwd", 7: "colsum", 8: "finalize"}
+
+
+def layer_flops(s, batch=None):
+    b = s.batch if batch is None else batch
+    n = b * s.seq
+    gemm_fwd = 2 * n * (3 * s.h * s.h + s.h * s.h + 2 * s.ffn * s.h)
+    attn_fwd = 2 * b * s.seq * (s.seq + 1) * s.h
+    return 3 * (gemm_fwd + attn_fwd)
+
+
+def megatron_flops(s):
+    n = s.batch * s.seq
+    return 72 * n * s.h * s.h + 12 * s.batch * s.seq * s.seq * s.h
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], 0.0, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def traffic_record(kernel_file):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
+    or None when absent or taken on a different revision of the kernel source."""
+    path = os.path.join(ROOT, "profiles", "gemm_tc_traffic.txt")
+    try:
+        rec = {}
+        for ln in open(path):
+            if ":" in ln:
+                k, v = ln.split(":", 1)
+                rec[k.strip()] = v.strip()
+        src = open(kernel_file, "rb").read()
+        if rec.get("source_sha256") != hashlib.sha256(src).hexdigest():
+            return None
+        return rec
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args, shape, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    sample_batch = 1
+    flops = layer_flops(shape, sample_batch)
+    x, p, dy = synthetic.make_layer(shape, seed=0, batch=sample_batch)
+    for _ in range(max(0, min(args.warmup, 1))):
+        pass  # the oracle has no warm state worth priming; keep the run bounded
+    times = []
+    steps = max(1, min(args.steps, 3))
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        y, cache = oracle.layer_fwd(p, x, shape.heads)
+        oracle.layer_bwd(p, cache, dy)
+        times.append(time.perf_counter() - t0)
+    sec = float(np.mean(times))
+    value = flops / sec / 1e12
+    sample = (f"{shape.name} at batch {sample_batch} (of {shape.batch}), "
+              f"{steps} fwd+bwd passes of the fp64 numpy oracle")
+    out = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+           "steps": steps, "warmup": 0, "ms_per_step": sec * 1e3, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "impl": "reference",
+           "config": {"workload": f"{args.config}: {shape.name}, t={args.t}",
+                      "h": shape.h, "heads": shape.heads, "seq": shape.seq,
+                      "batch": sample_batch, "ffn": shape.ffn, "t": args.t},
+           "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores,
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def cpu_baseline(shape):
+    import oracle
+    x, p, dy = synthetic.make_layer(shape, seed=0, batch=1)
+    t0 = time.perf_counter()
+    y, cache = oracle.layer_fwd(p, x, shape.heads)
+    oracle.layer_bwd(p, cache, dy)
+    sec = time.perf_counter() - t0
+    return {"value": layer_flops(shape, 1) / sec / 1e12, "unit": "TFLOP/s",
+            "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"{shape.name} at batch 1 (of {shape.batch}): one fwd+bwd of the "
+                      f"fp64 numpy oracle, {sec:.1f} s"}
+
+
+# ---------------------------------------------------------------- our arm
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="D", choices=sorted(synthetic.CONFIGS))
+    ap.add_argument("--t", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    shape = synthetic.CONFIGS[args.config]
+    if args.t is None:
+        args.t = shape.t[0]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, shape, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+    from tensor_model_transformer_gb300 import mtl
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    dt = torch.bfloat16 if shape.dtype == "bf16" else torch.float32
+    x, p, dy = synthetic.make_layer(shape, seed=rank)
+    desc = mtl.layer_desc(shape.h, shape.heads, shape.seq, shape.batch, shape.ffn, args.t,
+                          shape.dtype)
+    w = {k: torch.from_numpy(v).cuda().to(dt) for k, v in p.items()}
+    x_h = torch.from_numpy(x).to(dt).pin_memory()
+    dy_h = torch.from_numpy(dy).to(dt).pin_memory()
+    del x, p, dy
+    xd = x_h.cuda()
+    dyd = dy_h.cuda()
+    y = torch.empty_like(xd)
+    dx = torch.empty_like(xd)
+    saved, ws, grads = mtl.alloc_layer_buffers(desc)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        mtl.layer_fwd(desc, w, xd, y, saved, ws, stream)
+        n1 = mtl.last_launch_count()
+        mtl.layer_bwd(desc, w, xd, saved, dyd, dx, grads, ws, stream)
+        return n1 + mtl.last_launch_count()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        launches_per_step = step()
+    mtl.layer_check(ws)
+    torch.cuda.synchronize()
+
+    # ---- timed region: inputs resident in HBM
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    launches = 0
+    for _ in range(args.steps):
+        launches += step()
+    ev1.record(stream)
+    ev1.synchronize()
+    torch.cuda.synchronize()
+    barrier()
+    ms = ev0.elapsed_time(ev1)
+    clk = clocks.stop()
+    mtl.layer_check(ws)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    flops = layer_flops(shape)
+    value = flops * args.steps * world / (ms / 1e3) / 1e12
+
+    # ---- end to end: host buffers in, results out, every step
+    barrier()
+    torch.cuda.synchronize()
+    y_h = torch.empty_like(x_h).pin_memory()
+    dx_h = torch.empty_like(x_h).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        xd.copy_(x_h, non_blocking=True)
+        dyd.copy_(dy_h, non_blocking=True)
+        step()
+        y_h.copy_(y, non_blocking=True)
+        dx_h.copy_(dx, non_blocking=True)
+    e1.record(stream)
+    e1.synchronize()
+    ms_e2e = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms_e2e], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    e2e_value = flops * args.steps * world / (ms_e2e / 1e3) / 1e12
+    nbytes = x_h.numel() * x_h.element_size()
+
+    # ---- per-kernel times: the same steps again with events around every kernel
+    cap = launches_per_step * args.steps + 16
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * cap)]
+    for e in evs:
+        e.record(stream)
+    torch.cuda.synchronize()
+    import ctypes
+    handles = (ctypes.c_void_p * (2 * cap))(*[e.cuda_event for e in evs])
+    kinds = (ctypes.c_int32 * cap)()
+    work = (ctypes.c_double * cap)()
+    mtl.lib().mtl_profile_set(handles, cap, kinds, work)
+    for _ in range(args.steps):
+        step()
+    count = mtl.lib().mtl_profile_count()
+    mtl.lib().mtl_profile_set(None, 0, None, None)
+    torch.cuda.synchronize()
+    per_kind = {}
+    for i in range(count):
+        dur = evs[2 * i].elapsed_time(evs[2 * i + 1])
+        k = KIND_NAMES.get(kinds[i], str(kinds[i]))
+        rec = per_kind.setdefault(k, {"launches": 0, "ms": 0.0, "work": 0.0})
+        rec["launches"] += 1
+        rec["ms"] += dur
+        rec["work"] += work[i]
+    total_ms = sum(r["ms"] for r in per_kind.values()) or 1.0
+    breakdown = {k: {"launches_per_step": r["launches"] // args.steps,
+                     "ms_per_step": r["ms"] / args.steps, "share": r["ms"] / total_ms}
+                 for k, r in sorted(per_kind.items(), key=lambda kv: -kv[1]["ms"])}
+
+    pk, pk_src = peaks()
+    dom = max(per_kind.items(), key=lambda kv: kv[1]["ms"])[0] if per_kind else None
+    roofline = None
+    if dom is not None:
+        r = per_kind[dom]
+        if dom in ("gemm_tc", "gemm_simt", "attn_fwd", "attn_bwd"):
+            achieved = r["work"] / (r["ms"] / 1e3) / 1e12
+            peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+            unit, bound = "TFLOP/s", "tensor"
+        else:
+            achieved = r["work"] / (r["ms"] / 1e3) / 1e9
+            peak = pk["hbm_gbs"]
+            unit, bound = "GB/s", "hbm"
+        tr = traffic_record(os.path.join(ROOT, "tensor_model_transformer_gb300", "csrc",
+                                         "gemm_tc.cu")) if dom == "gemm_tc" else None
+        traffic = None
+        if tr and "dram_bytes_per_launch_full" in tr:
+            traffic = float(tr["dram_bytes_per_launch_full"])
+        roofline = {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak,
+                    "unit": unit, "frac": achieved / peak, "traffic": traffic,
+                    "peak_source": f"{pk_src} bf16 sustained" if bound == "tensor"
+                    else f"{pk_src} hbm"}
+
+    out = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": shape.dtype, "data": "synthetic",
+        "config": {"workload": f"{args.config}: {shape.name}, t={args.t}", "h": shape.h,
+                   "heads": shape.heads, "seq": shape.seq, "batch": shape.batch,
+                   "ffn": shape.ffn, "t": args.t, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (no flush)",
+                   "flops_per_step": flops, "megatron_flops_per_step": megatron_flops(shape)},
+        "pct_of_bf16_peak": 100.0 * value / world / pk["bf16_tflops"],
+        "peak_source": pk_src,
+        "gpu_launches": launches,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 2 * nbytes,
+                "d2h_bytes_per_step": 2 * nbytes},
+        "roofline": roofline,
+        "kernels": breakdown,
+    }
+    if clk:
+        out["clocks"] = clk
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(shape)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

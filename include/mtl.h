@@ -1,0 +1,194 @@
+/*
+ * mtl.h -- C ABI of a GB300-native (sm_103a) pre-LN GPT transformer layer with
+ * Megatron's intra-layer tensor-parallel split laid out inside one GPU.
+ *
+ * The operation (page "Megatron-LM: GPU-Cluster Training Parallelism"):
+ *   * "Paper 1: BERT LayerNorm Rearrangement": Pre-LN, x -> LayerNorm ->
+ *     sublayer -> added back onto x:
+ *         x1 = x  + Attn(LN1(x)),   y = x1 + MLP(LN2(x1)).
+ *   * "Paper 1: The f/g Conjugate Operators": the QKV and fc1 GEMMs are split by
+ *     columns into t partitions (GeLU and softmax stay local to a partition);
+ *     the out-proj and fc2 GEMMs are split by rows and give t partial sums that
+ *     g reduces in the forward pass; f reduces the partial input gradients of
+ *     the column-split GEMMs in the backward pass.  Two reductions forward, two
+ *     backward.
+ *   * "Paper 1: QKV Column-Parallel Splitting in Detail": the fused QKV weight is
+ *     head-interleaved, so partition p owns heads [p*H/t, (p+1)*H/t) whole.
+ *   * "Fused Transformer Kernels": causal scale-mask-softmax, bias+GeLU and
+ *     bias+residual fused into the GEMMs.
+ *
+ * On one GPU the t partitions are a layout: partition p's shard is a view (a
+ * row block of w_qkv / w_fc1, a column block of w_o / w_fc2 and the matching
+ * column blocks of the activations).  The g and f all-reduces become fixed-order
+ * (p = 0 .. t-1) sums of t separately accumulated fp32 partials inside the GEMM
+ * epilogues, so results are bitwise reproducible for a given t and agree across
+ * t within rounding.
+ *
+ * Conventions
+ *   * All pointers are DEVICE pointers unless stated; the caller owns all
+ *     memory.  The library allocates and frees nothing and keeps no state other
+ *     than a once-initialised per-device cache of kernel attributes.
+ *   * Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream).  Functions return after enqueueing.
+ *   * Layouts are row-major.  x, y, dx, dy: [batch, seq, h].  Weights are
+ *     [out, in]: w_qkv [3h][h] with head-interleaved rows
+ *     (row = head*3*d + {0:Q,1:K,2:V}*d + channel, d = h/heads); w_o [h][h];
+ *     w_fc1 [ffn][h]; w_fc2 [h][ffn].  b_qkv [3h] (same interleaved order),
+ *     b_fc1 [ffn]; b_o, b_fc2, ln1_g, ln1_b, ln2_g, ln2_b [h].
+ *   * Element type of x, y, dx, dy, weights and saved activations is desc.dtype
+ *     (fp32 or bf16).  Gradients of the parameters are always fp32 and are
+ *     OVERWRITTEN, not accumulated.  bf16 math accumulates in fp32.
+ *   * GeLU is the exact x*Phi(x) (erf) form; the softmax scale is 1/sqrt(d);
+ *     keys after the query are excluded (probability 0); LayerNorm uses the
+ *     biased variance with desc.ln_eps inside the square root; dropout is 0.
+ *   * Every pointer must be 16-byte aligned.  Validation failures return before
+ *     anything is enqueued.  No C++ exception crosses this boundary.  Calls are
+ *     reentrant; calls on different streams may run concurrently as long as
+ *     they use different workspaces.
+ *   * Errors: MTL_ERR_INVALID_ARG (null / misaligned pointer, bad sizes),
+ *     MTL_ERR_UNSUPPORTED (valid layer outside what the kernels implement),
+ *     MTL_ERR_WORKSPACE (ws_bytes too small), MTL_ERR_CUDA (a CUDA call or launch
+ *     failed; see mtl_last_cuda_error), MTL_ERR_TIMEOUT (a device-side bounded
+ *     wait gave up; reported by mtl_layer_check).
+ */
+#ifndef MTL_H_
+#define MTL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* mtl_stream;  /* == cudaStream_t */
+
+typedef enum {
+  MTL_OK = 0,
+  MTL_ERR_INVALID_ARG = 1,
+  MTL_ERR_UNSUPPORTED = 2,
+  MTL_ERR_WORKSPACE = 3,
+  MTL_ERR_CUDA = 4,
+  MTL_ERR_TIMEOUT = 5
+} mtl_status;
+
+typedef enum { MTL_F32 = 0, MTL_BF16 = 1 } mtl_dtype;
+
+/* One layer.  h = heads * d with d in {64, 96, 128}; t divides heads and ffn;
+ * causal must be 1.  bf16 layers (tensor-core path) additionally need
+ * seq % 128 == 0, h % 64 == 0, ffn % 64 == 0, (h/t) % 64 == 0, (3h/t) % 64 == 0
+ * and (ffn/t) % 64 == 0, else MTL_ERR_UNSUPPORTED.  fp32 layers run exact fp32
+ * CUDA-core kernels and need only h % 4 == 0 and ffn % 4 == 0. */
+typedef struct {
+  int32_t h, heads, seq, batch, ffn, t;
+  int32_t dtype;   /* mtl_dtype */
+  float ln_eps;    /* 1e-5 */
+  int32_t causal;  /* 1 */
+} mtl_layer_desc;
+
+typedef struct {
+  const void *w_qkv, *b_qkv, *w_o, *b_o, *w_fc1, *b_fc1, *w_fc2, *b_fc2;
+  const void *ln1_g, *ln1_b, *ln2_g, *ln2_b;
+} mtl_weights;
+
+typedef struct {
+  void *w_qkv, *b_qkv, *w_o, *b_o, *w_fc1, *b_fc1, *w_fc2, *b_fc2;
+  void *ln1_g, *ln1_b, *ln2_g, *ln2_b;
+} mtl_grads;   /* all fp32 */
+
+/* Byte offsets of the activations the forward saves for the backward, inside
+ * the caller's `saved` buffer (each 256-byte aligned).  Element types: mu*,
+ * rstd*, lse fp32; the rest desc.dtype.  Shapes with n = batch*seq:
+ * mu1, rstd1, mu2, rstd2 [n]; u1, ctx, x1, u2 [n][h]; qkv [n][3h] (columns in
+ * the head-interleaved order of w_qkv); lse [batch][heads][seq] (log of the
+ * softmax normaliser per query row); z (fc1 pre-activation) and a = GeLU(z)
+ * [n][ffn]. */
+typedef struct {
+  size_t mu1, rstd1, u1, qkv, ctx, lse, x1, mu2, rstd2, u2, z, a;
+  size_t total;
+} mtl_saved_layout;
+
+/* Sizes in bytes of the `saved` buffer written by mtl_layer_fwd and read by
+ * mtl_layer_bwd, and of the scratch workspace both calls need (the same value
+ * serves both).  Returns MTL_ERR_INVALID_ARG / MTL_ERR_UNSUPPORTED for a desc
+ * the kernels cannot run. */
+mtl_status mtl_layer_sizes(const mtl_layer_desc* desc, size_t* saved_bytes,
+                           size_t* workspace_bytes);
+
+/* Offsets of each saved activation inside `saved` (see mtl_saved_layout). */
+mtl_status mtl_layer_saved_layout(const mtl_layer_desc* desc, mtl_saved_layout* out);
+
+/* Forward pass: y = layer(x).  x, y [batch][seq][h] of desc.dtype; `saved`
+ * (>= saved_bytes) receives the activations for the backward; `workspace`
+ * (>= workspace_bytes, contents not preserved) is scratch.  y must not alias x
+ * or saved.  Steps, in stream order: LN1; QKV GEMM (column-parallel, bias
+ * epilogue); causal attention per head; out-proj GEMM (row-parallel: t fp32
+ * partials summed in order, + b_o + x); LN2; fc1 GEMM (column-parallel, bias +
+ * GeLU epilogue, saves z and a); fc2 GEMM (row-parallel, + b_fc2 + x1). */
+mtl_status mtl_layer_fwd(const mtl_layer_desc* desc, const mtl_weights* w, const void* x,
+                         void* y, void* saved, void* workspace, size_t ws_bytes,
+                         mtl_stream stream);
+
+/* Backward pass for upstream gradient dy (the gradient of a loss with respect
+ * to y).  Reads x and the `saved` buffer written by mtl_layer_fwd with the same
+ * desc and weights; writes dx [batch][seq][h] (desc.dtype) and every pointer in
+ * `grads` (fp32, overwritten).  The two f reductions (input gradients of the QKV
+ * and fc1 GEMMs) are t fp32 partials summed in partition order. */
+mtl_status mtl_layer_bwd(const mtl_layer_desc* desc, const mtl_weights* w, const void* x,
+                         const void* saved, const void* dy, void* dx, const mtl_grads* grads,
+                         void* workspace, size_t ws_bytes, mtl_stream stream);
+
+/* Waits for `stream`, then reports the device-side status word that the last
+ * call using `workspace` left: MTL_OK, or MTL_ERR_TIMEOUT if a bounded
+ * device wait gave up (the call's outputs are then undefined).  Resets it. */
+mtl_status mtl_layer_check(void* workspace, mtl_stream stream);
+
+/* Utility GEMM on the same kernels, for component tests:
+ *   C[m][n] = sum_{p<k_parts} ( sum_{k in part p} A(m,k) * B(n,k) )
+ * with the k_parts partial sums accumulated separately in fp32 and added in
+ * order p = 0..k_parts-1, then the epilogue:
+ *   epi 0: C = acc                      epi 1: C = acc + bias[n]
+ *   epi 2: C = acc + bias[n] + R[m][n]  epi 3: Z = acc + bias[n], C = GeLU(Z)
+ *   epi 4: C = acc * GeLU'(Z[m][n])
+ * A(m,k) = A[m*lda + k] if a_k_major else A[k*lda + m]; likewise B(n,k) with
+ * b_k_major.  A, B, bias, R, Z are `dtype`; C is fp32 if c_f32 else `dtype`.
+ * Leading dimensions are in elements (C: ldc, R: ldr, Z: ldz).  K must split
+ * into k_parts equal parts; bf16 needs (K/k_parts) % 64 == 0 and lda, ldb,
+ * ldc, ldr, ldz multiples of 8. */
+mtl_status mtl_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, int32_t k_parts,
+                    const void* A, int64_t lda, int32_t a_k_major,
+                    const void* B, int64_t ldb, int32_t b_k_major,
+                    int32_t epi, const void* bias, const void* R, int64_t ldr,
+                    void* Z, int64_t ldz, void* C, int64_t ldc, int32_t c_f32,
+                    void* workspace, size_t ws_bytes, mtl_stream stream);
+
+/* Human-readable name of a status. */
+const char* mtl_status_str(mtl_status s);
+
+/* Text of the last CUDA error seen by this thread's calls (empty if none). */
+const char* mtl_last_cuda_error(void);
+
+/* Number of kernels the last mtl_layer_fwd / mtl_layer_bwd / mtl_gemm call on
+ * this thread enqueued. */
+int32_t mtl_last_launch_count(void);
+
+/* Per-kernel timing for measurement.  `events` points to 2*capacity caller-
+ * created CUDA events (cudaEvent_t); while set, each kernel the calling thread
+ * enqueues records events[2i] before and events[2i+1] after itself on its
+ * stream, and writes its kind to kinds[i] (1 tensor-core GEMM, 2 CUDA-core
+ * GEMM, 3 attention forward, 4 attention backward, 5 LayerNorm forward,
+ * 6 LayerNorm backward, 7 column sum, 8 partial-sum finalise) and its
+ * algorithmic work to work[i] (flops for GEMMs and attention, bytes moved for
+ * the memory-bound kernels).  Launches past `capacity` are not recorded.
+ * Passing events = NULL turns recording off.  The library keeps the pointers
+ * until the next call; the caller owns and frees everything. */
+void mtl_profile_set(void** events, int32_t capacity, int32_t* kinds, double* work);
+
+/* Number of kernels recorded since the last mtl_profile_set. */
+int32_t mtl_profile_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MTL_H_ */

@@ -417,3 +417,41 @@ def layer_flops(h, heads, seq, batch, ffn=None):
     gemm_fwd = 2 * n * (3 * h * h + h * h + 2 * ffn * h)
     attn_fwd = 2 * batch * seq * (seq + 1) * h
     return 3 * (gemm_fwd + attn_fwd)
+
+
+# --------------------------------------------------------------------------
+# One partitioned GEMM with its fused epilogue (the kernels' unit of work)
+# --------------------------------------------------------------------------
+
+def gemm_partitioned(A, B, parts, epi=0, bias=None, R=None, Z=None):
+    """C = epi( sum_{p < parts} A[:, K_p] B[:, K_p]^T ), K split into equal parts.
+
+    A [M, K], B [N, K].  The partial products of the parts are summed in part
+    order: a row-parallel GEMM's partial outputs and their g / f reduction
+    ("Paper 1: The f/g Conjugate Operators").  Epilogues (the fused kernels of
+    "Fused Transformer Kernels"):
+      0: C = acc            1: C = acc + bias            2: C = acc + bias + R
+      3: Z = acc + bias, C = GeLU(Z)                     4: C = acc * GeLU'(Z)
+    Returns C, or (C, Z) for epilogue 3.
+    """
+    A = _f64(A)
+    B = _f64(B)
+    K = A.shape[1]
+    if parts < 1 or K % parts:
+        raise ValueError("parts must divide K")
+    kp = K // parts
+    acc = np.zeros((A.shape[0], B.shape[0]))
+    for p in range(parts):
+        acc = acc + A[:, p * kp:(p + 1) * kp] @ B[:, p * kp:(p + 1) * kp].T
+    if epi == 0:
+        return acc
+    if epi == 1:
+        return acc + _f64(bias)[None, :]
+    if epi == 2:
+        return acc + _f64(bias)[None, :] + _f64(R)
+    if epi == 3:
+        z = acc + _f64(bias)[None, :]
+        return gelu(z), z
+    if epi == 4:
+        return acc * gelu_grad(_f64(Z))
+    raise ValueError(epi)

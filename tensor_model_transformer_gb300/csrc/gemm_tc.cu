@@ -1,0 +1,490 @@
+// Tensor-core GEMM for sm_103a: TMA -> shared memory -> tcgen05.mma -> TMEM ->
+// fused epilogue.  bf16 operands, fp32 accumulation.
+//
+//   C = epi( sum_{p = 0..parts-1} P_p ),  P_p = sum_{k in part p} A(m,k) B(n,k)
+//
+// Row-parallel GEMMs (out-proj and fc2 forward; the fc1 and QKV input-gradient
+// GEMMs backward) split K into t partitions.  Each partition's partial product
+// is accumulated on its own in TMEM and the epilogue adds the partials in
+// partition order in fp32: the g (forward) and f (backward) all-reduces of
+// "Megatron-LM: GPU-Cluster Training Parallelism", section "Paper 1: The f/g
+// Conjugate Operators", done as a fixed-order in-GPU sum.  Column-parallel
+// GEMMs (QKV, fc1) have no reduction; their bias / GeLU ride the epilogue
+// (section "Fused Transformer Kernels").
+//
+// Kernel shape: persistent, one 320-thread CTA per SM, 128x256 output tile,
+// K blocks of 64 in a 4-stage TMA ring (48 KB per stage, 128-byte swizzle).
+//   warp 0      TMA producer (one thread)
+//   warp 1      TMEM allocator and MMA issuer (one thread)
+//   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4).., columns
+//               128*((w-2)/4).. of the tile
+// TMEM holds two 128x256 fp32 accumulators (all 512 columns) so the epilogue
+// of one work unit overlaps the MMAs of the next.  A work unit is one
+// partition of one tile.  Operands may be K-major or MN-major (the backward's
+// data and weight gradients read activations and weights transposed); MN-major
+// tiles are loaded as 64-wide column boxes and described to the MMA with the
+// leading byte offset stepping between them.
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mtl {
+namespace tcg {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int BAR_BYTES = 256;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+constexpr int GROUP_M = 16;   // tile raster: groups of 16 M-blocks sweep all N-blocks
+
+struct Params {
+  int M, N, K, parts, kb_per_unit, units_per_tile;
+  int a_mn, b_mn;
+  int tiles_m, tiles_n, num_tiles;
+  const bf16* bias;
+  const bf16* R;
+  int64_t ldr;
+  bf16* Z;
+  int64_t ldz;
+  void* C;
+  int64_t ldc;
+  unsigned* status;
+};
+
+__device__ __forceinline__ void tile_coords(const Params& p, int tile, int& mb, int& nb) {
+  const int per_group = GROUP_M * p.tiles_n;
+  const int g = tile / per_group;
+  const int first_m = g * GROUP_M;
+  const int gsize = min(GROUP_M, p.tiles_m - first_m);
+  const int r = tile - g * per_group;
+  mb = first_m + r % gsize;
+  nb = r / gsize;
+}
+
+// Applies the epilogue to 32 consecutive columns [col0, col0+32) of one row.
+template <int EPI, bool OUT_F32>
+__device__ __forceinline__ void epi_chunk(const Params& p, int row, int col0, float (&v)[32]) {
+  if (row >= p.M || col0 >= p.N) return;
+  const bool full = col0 + 32 <= p.N;
+  if (full) {
+    if (EPI == EPI_BIAS || EPI == EPI_BIAS_RESID || EPI == EPI_BIAS_GELU) {
+      const uint4* bp = reinterpret_cast<const uint4*>(p.bias + col0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 u = __ldg(bp + q);
+        const bf16* hb = reinterpret_cast<const bf16*>(&u);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[q * 8 + e] += __bfloat162float(hb[e]);
+      }
+    }
+    if (EPI == EPI_BIAS_RESID) {
+      const uint4* rp = reinterpret_cast<const uint4*>(p.R + (size_t)row * p.ldr + col0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 u = rp[q];
+        const bf16* hb = reinterpret_cast<const bf16*>(&u);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[q * 8 + e] += __bfloat162float(hb[e]);
+      }
+    }
+    if (EPI == EPI_DGELU) {
+      const uint4* zp = reinterpret_cast<const uint4*>(p.Z + (size_t)row * p.ldz + col0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 u = zp[q];
+        const bf16* hb = reinterpret_cast<const bf16*>(&u);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[q * 8 + e] *= gelu_grad_f(__bfloat162float(hb[e]));
+      }
+    }
+    if (EPI == EPI_BIAS_GELU) {
+      uint4* zp = reinterpret_cast<uint4*>(p.Z + (size_t)row * p.ldz + col0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 u;
+        bf16* hb = reinterpret_cast<bf16*>(&u);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          hb[e] = __float2bfloat16_rn(v[q * 8 + e]);
+          v[q * 8 + e] = gelu_f(v[q * 8 + e]);
+        }
+        zp[q] = u;
+      }
+    }
+    if (OUT_F32) {
+      float4* cp = reinterpret_cast<float4*>(static_cast<float*>(p.C) + (size_t)row * p.ldc + col0);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        cp[q] = make_float4(v[q * 4], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
+    } else {
+      uint4* cp = reinterpret_cast<uint4*>(static_cast<bf16*>(p.C) + (size_t)row * p.ldc + col0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 u;
+        bf16* hb = reinterpret_cast<bf16*>(&u);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) hb[e] = __float2bfloat16_rn(v[q * 8 + e]);
+        cp[q] = u;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int col = col0 + e;
+      if (col < p.N) {
+        float x = v[e];
+        if (EPI == EPI_BIAS || EPI == EPI_BIAS_RESID || EPI == EPI_BIAS_GELU)
+          x += __bfloat162float(p.bias[col]);
+        if (EPI == EPI_BIAS_RESID) x += __bfloat162float(p.R[(size_t)row * p.ldr + col]);
+        if (EPI == EPI_DGELU) x *= gelu_grad_f(__bfloat162float(p.Z[(size_t)row * p.ldz + col]));
+        if (EPI == EPI_BIAS_GELU) {
+          p.Z[(size_t)row * p.ldz + col] = __float2bfloat16_rn(x);
+          x = gelu_f(x);
+        }
+        if (OUT_F32)
+          static_cast<float*>(p.C)[(size_t)row * p.ldc + col] = x;
+        else
+          static_cast<bf16*>(p.C)[(size_t)row * p.ldc + col] = __float2bfloat16_rn(x);
+      }
+    }
+  }
+}
+
+template <int EPI, bool OUT_F32, bool REDUCE>
+__global__ void __maxnreg__(200)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sA0 = smem_u32(smem);
+  const uint32_t sB0 = sA0 + STAGES * A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  // bars[0..S): full, [S..2S): empty, [2S..2S+2): tmem full, [2S+2..2S+4): tmem empty
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), EPI_WARPS);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_shared();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      const int kb_per_tile = p.kb_per_unit * p.units_per_tile;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+        int mb, nb;
+        tile_coords(p, tile, mb, nb);
+        for (int kb = 0; kb < kb_per_tile; ++kb) {
+          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          const int k0 = kb * BK;
+          const uint32_t sa = sA0 + stage * A_BYTES, sb = sB0 + stage * B_BYTES;
+          if (!p.a_mn) {
+            tma_load_2d(sa, &tmA, fb, k0, mb * BM);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BM / 64; ++j) tma_load_2d(sa + j * (BK * 128), &tmA, fb, mb * BM + 64 * j, k0);
+          }
+          if (!p.b_mn) {
+            tma_load_2d(sb, &tmB, fb, k0, nb * BN);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * (BK * 128), &tmB, fb, nb * BN + 64 * j, k0);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(BM, BN, p.a_mn != 0, p.b_mn != 0);
+      // K-major tiles: rows of 128 bytes, 8-row groups 1024 bytes apart; a
+      // 16-deep K step moves 32 bytes along the row.  MN-major tiles: 64-wide
+      // column boxes of BK rows (8 KB apart, the leading byte offset), 8-row
+      // K groups 1024 bytes apart; a K step moves 16 rows = 2048 bytes.
+      const uint32_t a_lbo = p.a_mn ? BK * 128 : 16, b_lbo = p.b_mn ? BK * 128 : 16;
+      const uint32_t a_kstep = p.a_mn ? 2048 : 32, b_kstep = p.b_mn ? 2048 : 32;
+      int stage = 0;
+      uint32_t phase = 0;
+      int unit = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+        for (int u = 0; u < p.units_per_tile && ok; ++u, ++unit) {
+          const int buf = unit & 1;
+          const uint32_t uphase = (unit >> 1) & 1;
+          if (!mbar_wait_bounded(tempty_bar(buf), uphase ^ 1u, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + buf * BN;
+          for (int kb = 0; kb < p.kb_per_unit; ++kb) {
+            if (!mbar_wait_bounded(full_bar(stage), phase, p.status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = sA0 + stage * A_BYTES, sb = sB0 + stage * B_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t ad = smem_desc_sw128(sa + kk * a_kstep, a_lbo, 1024);
+              const uint64_t bd = smem_desc_sw128(sb + kk * b_kstep, b_lbo, 1024);
+              tc_mma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc_commit(empty_bar(stage));
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (ok) tc_commit(tfull_bar(buf));
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;
+    const int quarter = warp & 3;
+    const int chalf = ew >> 2;
+    int unit = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+      int mb, nb;
+      tile_coords(p, tile, mb, nb);
+      const int row = mb * BM + quarter * 32 + lane;
+      const int colbase = nb * BN + chalf * 128;
+      float sum[REDUCE ? 128 : 1];
+      for (int u = 0; u < p.units_per_tile; ++u, ++unit) {
+        const int buf = unit & 1;
+        const uint32_t uphase = (unit >> 1) & 1;
+        if (!mbar_wait_bounded(tfull_bar(buf), uphase, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tb = tmem_base + buf * BN + chalf * 128 + ((uint32_t)(quarter * 32) << 16);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tb + c * 32, r);
+          tmem_ld_wait();
+          if constexpr (REDUCE) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float x = __uint_as_float(r[i]);
+              sum[c * 32 + i] = (u == 0) ? x : sum[c * 32 + i] + x;
+            }
+          } else {
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+            epi_chunk<EPI, OUT_F32>(p, row, colbase + c * 32, v);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(buf));
+      }
+      if constexpr (REDUCE) {
+        if (ok) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = sum[c * 32 + i];
+            epi_chunk<EPI, OUT_F32>(p, row, colbase + c * 32, v);
+          }
+        }
+      }
+    }
+    __syncwarp();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    if (*abort_flag) {
+      // A role gave up on a wait (after ~2 s).  Copies and MMAs issued before
+      // that finish in microseconds; pause ~1 ms so none is still writing
+      // shared memory or TMEM when they are released.
+      const long long t0 = clock64();
+      while (clock64() - t0 < 2000000LL) {
+      }
+    }
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// 2D bf16 map over a row-major matrix with `rows` rows of `cols` elements
+// (row pitch ld elements), box of box_cols x box_rows, 128-byte swizzle,
+// out-of-range elements read as zero.
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, int64_t ld,
+              uint32_t box_cols, uint32_t box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// K-major operand (rows x K): box 64 (K) x rows_box.  MN-major operand stored
+// [K][MN]: box 64 (MN) x BK (K).
+bool make_operand_map(CUtensorMap* m, const GemmOperand& op, int mn, int K, int box_rows) {
+  if (op.k_major) return make_map(m, op.ptr, (uint64_t)K, (uint64_t)mn, op.ld, BK, box_rows);
+  return make_map(m, op.ptr, (uint64_t)mn, (uint64_t)K, op.ld, 64, BK);
+}
+
+typedef void (*KernelFn)(CUtensorMap, CUtensorMap, Params);
+
+template <int EPI, bool F32, bool RED>
+KernelFn kernel_ptr() {
+  return reinterpret_cast<KernelFn>(gemm_tc_kernel<EPI, F32, RED>);
+}
+
+KernelFn select_kernel(int epi, bool f32, bool red) {
+#define SEL(E)                                                                         \
+  if (epi == E) {                                                                      \
+    if (f32) return red ? kernel_ptr<E, true, true>() : kernel_ptr<E, true, false>();  \
+    return red ? kernel_ptr<E, false, true>() : kernel_ptr<E, false, false>();         \
+  }
+  SEL(EPI_STORE)
+  SEL(EPI_BIAS)
+  SEL(EPI_BIAS_RESID)
+  SEL(EPI_BIAS_GELU)
+  SEL(EPI_DGELU)
+#undef SEL
+  return nullptr;
+}
+
+}  // namespace tcg
+
+bool gemm_tc_supported(const GemmArgs& a) {
+  if (a.parts < 1 || a.K % a.parts) return false;
+  const int kpart = a.K / a.parts;
+  if (a.parts > 1 && kpart % tcg::BK) return false;
+  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  if (!al16(a.A.ptr) || !al16(a.B.ptr) || !al16(a.C)) return false;
+  if ((a.A.ld % 8) || (a.B.ld % 8) || (a.ldc % 8)) return false;
+  if (a.epi == EPI_BIAS_RESID && ((a.ldr % 8) || !al16(a.R))) return false;
+  if ((a.epi == EPI_BIAS_GELU || a.epi == EPI_DGELU) && ((a.ldz % 8) || !al16(a.Z))) return false;
+  if ((a.epi == EPI_BIAS || a.epi == EPI_BIAS_RESID || a.epi == EPI_BIAS_GELU) && !al16(a.bias))
+    return false;
+  return true;
+}
+
+cudaError_t gemm_tc(const GemmArgs& a, const LaunchCtx& c) {
+  using namespace tcg;
+  if (a.M == 0 || a.N == 0) return cudaSuccess;
+  if (!gemm_tc_supported(a)) return cudaErrorInvalidValue;
+  CUtensorMap ma, mb;
+  if (!make_operand_map(&ma, a.A, a.M, a.K, BM) || !make_operand_map(&mb, a.B, a.N, a.K, BN))
+    return cudaErrorInvalidValue;
+  Params p;
+  p.M = a.M;
+  p.N = a.N;
+  p.K = a.K;
+  p.parts = a.parts;
+  const bool reduce = a.parts > 1;
+  const int nkb = (a.K + BK - 1) / BK;
+  p.units_per_tile = reduce ? a.parts : 1;
+  p.kb_per_unit = reduce ? (a.K / a.parts) / BK : nkb;
+  p.a_mn = a.A.k_major ? 0 : 1;
+  p.b_mn = a.B.k_major ? 0 : 1;
+  p.tiles_m = (a.M + BM - 1) / BM;
+  p.tiles_n = (a.N + BN - 1) / BN;
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  p.bias = static_cast<const bf16*>(a.bias);
+  p.R = static_cast<const bf16*>(a.R);
+  p.ldr = a.ldr;
+  p.Z = static_cast<bf16*>(a.Z);
+  p.ldz = a.ldz;
+  p.C = a.C;
+  p.ldc = a.ldc;
+  p.status = a.status;
+  KernelFn fn = select_kernel(a.epi, a.c_f32, reduce);
+  if (!fn) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  if (p.kb_per_unit == 0) {
+    // K == 0: nothing to accumulate; the kernel is not launched
+    return cudaErrorInvalidValue;
+  }
+  const int grid = p.num_tiles < c.num_sms ? p.num_tiles : c.num_sms;
+  c.before(KK_GEMM_TC, 2.0 * a.M * a.N * a.K);
+  fn<<<grid, THREADS, SMEM_BYTES, c.stream>>>(ma, mb, p);
+  c.after();
+  return cudaGetLastError();
+}
+
+}  // namespace mtl

@@ -1,0 +1,110 @@
+// Internal host-side launchers of the layer's kernels (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mtl {
+
+enum DType { kF32 = 0, kBF16 = 1 };
+
+// GEMM epilogues (the numbering is the one mtl_gemm exposes).
+enum Epi { EPI_STORE = 0, EPI_BIAS = 1, EPI_BIAS_RESID = 2, EPI_BIAS_GELU = 3, EPI_DGELU = 4 };
+
+// A(m,k) = ptr[m*ld + k] when k_major, else ptr[k*ld + m].
+struct GemmOperand {
+  const void* ptr;
+  int64_t ld;
+  bool k_major;
+};
+
+// C[m][n] = epi( sum over parts p in order of ( sum_{k in part p} A(m,k) B(n,k) ) )
+struct GemmArgs {
+  int M, N, K, parts;
+  GemmOperand A, B;
+  int epi;
+  const void* bias;       // [N] (EPI_BIAS, EPI_BIAS_RESID, EPI_BIAS_GELU)
+  const void* R;          // residual [M][ldr] (EPI_BIAS_RESID)
+  int64_t ldr;
+  void* Z;                // EPI_BIAS_GELU: pre-activation out; EPI_DGELU: pre-activation in
+  int64_t ldz;
+  void* C;                // output [M][ldc]
+  int64_t ldc;
+  bool c_f32;             // C stored as fp32 (else as the operand dtype)
+  unsigned* status;       // device status word
+};
+
+// Kernel kinds reported through the profiling hooks.
+enum KernelKind {
+  KK_GEMM_TC = 1, KK_GEMM_SIMT = 2, KK_ATTN_FWD = 3, KK_ATTN_BWD = 4, KK_LN_FWD = 5,
+  KK_LN_BWD = 6, KK_COLSUM = 7, KK_FINALIZE = 8
+};
+
+// Optional per-launch timing: when set, events[2i] / events[2i+1] are recorded
+// on the launch stream around the i-th kernel, with its kind and work (flops
+// for contractions, bytes for memory-bound kernels).
+struct Profiler {
+  cudaEvent_t* events;
+  int capacity;
+  int count;
+  int* kinds;
+  double* work;
+};
+
+struct LaunchCtx {
+  cudaStream_t stream;
+  int num_sms;
+  int* launches;          // incremented per kernel enqueued
+  Profiler* prof;         // may be null
+
+  void before(int kind, double work) const {
+    if (prof && prof->events && prof->count < prof->capacity) {
+      cudaEventRecord(prof->events[2 * prof->count], stream);
+      prof->kinds[prof->count] = kind;
+      prof->work[prof->count] = work;
+    }
+  }
+  void after() const {
+    ++*launches;
+    if (prof && prof->events && prof->count < prof->capacity) {
+      cudaEventRecord(prof->events[2 * prof->count + 1], stream);
+      ++prof->count;
+    }
+  }
+};
+
+// CUDA-core GEMM, exact fp32 math; dtype of operands kF32 or kBF16.
+cudaError_t gemm_simt(int dtype, const GemmArgs& a, const LaunchCtx& c);
+// tcgen05 / TMEM / TMA GEMM, bf16 operands, fp32 accumulate.
+cudaError_t gemm_tc(const GemmArgs& a, const LaunchCtx& c);
+// Host check of the shapes gemm_tc accepts.
+bool gemm_tc_supported(const GemmArgs& a);
+
+// LayerNorm forward of x [n][h] -> u [n][h], mean and rstd [n] (fp32).
+cudaError_t ln_fwd(int dtype, const void* x, const void* gamma, const void* beta, void* u,
+                   float* mean, float* rstd, int n, int h, float eps, const LaunchCtx& c);
+// LayerNorm backward plus residual gradient: dx = resid + LN_bwd(du); du fp32.
+// dgamma / dbeta (fp32 [h]) are reduced in a fixed order through `partial`
+// (ln_bwd_partial_floats(n, h) floats).
+cudaError_t ln_bwd(int dtype, const float* du, const void* x, const float* mean,
+                   const float* rstd, const void* gamma, const void* resid, void* dx,
+                   float* dgamma, float* dbeta, float* partial, int n, int h,
+                   const LaunchCtx& c);
+size_t ln_bwd_partial_floats(int n, int h);
+
+// out[j] = sum_i Y[i*ld + j] (fp32, fixed order) for j < N, i < n, through
+// `partial` (colsum_partial_floats(n, N) floats).
+cudaError_t colsum(int dtype, const void* Y, int64_t ld, int n, int N, float* out,
+                   float* partial, const LaunchCtx& c);
+size_t colsum_partial_floats(int n, int N);
+
+// Causal attention over a head-interleaved qkv [batch*seq][3h] -> ctx
+// [batch*seq][h], lse [batch][heads][seq] (CUDA-core reference kernels).
+cudaError_t attn_fwd_simt(int dtype, const void* qkv, void* ctx, float* lse, int batch, int seq,
+                          int heads, int d, const LaunchCtx& c);
+// Backward: dctx -> dqkv [batch*seq][3h]; dsum [batch][heads][seq] is scratch.
+cudaError_t attn_bwd_simt(int dtype, const void* qkv, const void* ctx, const float* lse,
+                          const void* dctx, void* dqkv, float* dsum, int batch, int seq,
+                          int heads, int d, const LaunchCtx& c);
+
+}  // namespace mtl

@@ -1,0 +1,370 @@
+// LayerNorm forward / backward (+ residual gradient) and fixed-order column sums.
+//
+// Pre-LN ("Megatron-LM: GPU-Cluster Training Parallelism", section "Paper 1: BERT
+// LayerNorm Rearrangement"): every sublayer reads LayerNorm(x).  These kernels are
+// HBM-bound: each row is read once into registers as 16-byte vectors, reduced
+// with warp shuffles, and written once.  Parameter gradients (dgamma, dbeta) and
+// bias gradients are reduced deterministically: fixed row blocks write partial
+// column sums, then one pass adds the partials in block order.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mtl {
+namespace {
+
+constexpr int kLnThreadsMax = 512;
+constexpr int kLnBwdBlocks = 512;     // row blocks of the dgamma/dbeta reduction
+constexpr int kColsumBlocks = 128;    // row blocks of the bias-gradient reduction
+
+// Sum of two values over the block; `red` holds 2*32 floats.
+__device__ __forceinline__ float2 block_sum2(float a, float b, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = (blockDim.x + 31) >> 5;
+  a = warp_sum(a);
+  b = warp_sum(b);
+  __syncthreads();  // earlier readers of `red` are done
+  if (lane == 0) {
+    red[warp] = a;
+    red[32 + warp] = b;
+  }
+  __syncthreads();
+  float sa = 0.f, sb = 0.f;
+  for (int w = 0; w < nw; ++w) {  // same order in every thread
+    sa += red[w];
+    sb += red[32 + w];
+  }
+  return make_float2(sa, sb);
+}
+
+template <typename T, int V>
+__global__ void __launch_bounds__(kLnThreadsMax) ln_fwd_kernel(const T* __restrict__ x, const T* __restrict__ gamma,
+                              const T* __restrict__ beta, T* __restrict__ u,
+                              float* __restrict__ mean_out, float* __restrict__ rstd_out, int n,
+                              int h, float eps, int rows_per_block) {
+  constexpr int E = Vec<T>::N;
+  __shared__ float red[64];
+  const int nvec = h / E;
+  float g[V][E], b[V][E];
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int vi = threadIdx.x + i * blockDim.x;
+    if (vi < nvec) {
+      Vec<T> tg, tb;
+      tg.load(gamma + vi * E);
+      tb.load(beta + vi * E);
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        g[i][e] = tg.get(e);
+        b[i][e] = tb.get(e);
+      }
+    }
+  }
+  const int r0 = blockIdx.x * rows_per_block;
+  const int r1 = min(n, r0 + rows_per_block);
+  const float inv_h = 1.0f / (float)h;
+  for (int r = r0; r < r1; ++r) {
+    const T* xr = x + (size_t)r * h;
+    float v[V][E];
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int vi = threadIdx.x + i * blockDim.x;
+      if (vi < nvec) {
+        Vec<T> t;
+        t.load(xr + vi * E);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          v[i][e] = t.get(e);
+          s += v[i][e];
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[i][e] = 0.f;
+      }
+    }
+    const float mean = block_sum2(s, 0.f, red).x * inv_h;
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int vi = threadIdx.x + i * blockDim.x;
+      if (vi < nvec) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const float dlt = v[i][e] - mean;
+          ss += dlt * dlt;
+        }
+      }
+    }
+    const float var = block_sum2(ss, 0.f, red).x * inv_h;
+    const float rs = 1.0f / sqrtf(var + eps);
+    T* ur = u + (size_t)r * h;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int vi = threadIdx.x + i * blockDim.x;
+      if (vi < nvec) {
+        Vec<T> o;
+#pragma unroll
+        for (int e = 0; e < E; ++e) o.set(e, (v[i][e] - mean) * rs * g[i][e] + b[i][e]);
+        o.store(ur + vi * E);
+      }
+    }
+    if (threadIdx.x == 0) {
+      mean_out[r] = mean;
+      rstd_out[r] = rs;
+    }
+  }
+}
+
+// Dynamic shared memory: gamma, and the block's running column sums of
+// du * xhat and du (3 * h floats); thread i owns the same columns in every row,
+// so the sums need no atomics.
+template <typename T, int V>
+__global__ void __launch_bounds__(kLnThreadsMax)
+    ln_bwd_kernel(const float* __restrict__ du, const T* __restrict__ x,
+                  const float* __restrict__ mean_in, const float* __restrict__ rstd_in,
+                  const T* __restrict__ gamma, const T* __restrict__ resid, T* __restrict__ dx,
+                  float* __restrict__ part_g, float* __restrict__ part_b, int n, int h,
+                  int rows_per_block) {
+  constexpr int E = Vec<T>::N;
+  extern __shared__ float lsm[];
+  float* sg = lsm;
+  float* acc_g = lsm + h;
+  float* acc_b = lsm + 2 * h;
+  __shared__ float red[64];
+  const int nvec = h / E;
+  for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+    Vec<T> tg;
+    tg.load(gamma + vi * E);
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      sg[vi * E + e] = tg.get(e);
+      acc_g[vi * E + e] = 0.f;
+      acc_b[vi * E + e] = 0.f;
+    }
+  }
+  // each thread reads back only the columns it wrote: no barrier needed
+  const int r0 = blockIdx.x * rows_per_block;
+  const int r1 = min(n, r0 + rows_per_block);
+  const float inv_h = 1.0f / (float)h;
+  for (int r = r0; r < r1; ++r) {
+    const float mu = mean_in[r], rs = rstd_in[r];
+    Vec<T> xv[V];
+    float dd[V][E];
+    float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int vi = threadIdx.x + i * blockDim.x;
+      if (vi < nvec) {
+        xv[i].load(x + (size_t)r * h + vi * E);
+        const float* dur = du + (size_t)r * h + vi * E;
+#pragma unroll
+        for (int e = 0; e < E; e += 4) {
+          const float4 q = *reinterpret_cast<const float4*>(dur + e);
+          dd[i][e] = q.x;
+          dd[i][e + 1] = q.y;
+          dd[i][e + 2] = q.z;
+          dd[i][e + 3] = q.w;
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int col = vi * E + e;
+          const float xh = (xv[i].get(e) - mu) * rs;
+          const float gd = dd[i][e] * sg[col];
+          s1 += gd;
+          s2 += gd * xh;
+          acc_g[col] += dd[i][e] * xh;
+          acc_b[col] += dd[i][e];
+        }
+      }
+    }
+    const float2 s = block_sum2(s1, s2, red);
+    const float m1 = s.x * inv_h, m2 = s.y * inv_h;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int vi = threadIdx.x + i * blockDim.x;
+      if (vi < nvec) {
+        Vec<T> tr, o;
+        tr.load(resid + (size_t)r * h + vi * E);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int col = vi * E + e;
+          const float xh = (xv[i].get(e) - mu) * rs;
+          const float gd = dd[i][e] * sg[col];
+          o.set(e, tr.get(e) + rs * (gd - m1 - xh * m2));
+        }
+        o.store(dx + (size_t)r * h + vi * E);
+      }
+    }
+  }
+  for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      part_g[(size_t)blockIdx.x * h + vi * E + e] = acc_g[vi * E + e];
+      part_b[(size_t)blockIdx.x * h + vi * E + e] = acc_b[vi * E + e];
+    }
+  }
+}
+
+// out[c] = sum over row blocks b = 0..nblk-1 of part[b*N + c]
+__global__ void finalize_cols_kernel(const float* __restrict__ part, int nblk, int N,
+                                     float* __restrict__ out) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= N) return;
+  float s = 0.f;
+  for (int b = 0; b < nblk; ++b) s += part[(size_t)b * N + c];
+  out[c] = s;
+}
+
+template <typename T>
+__global__ void colsum_partial_kernel(const T* __restrict__ Y, int64_t ld, int n, int N,
+                                      int rows_per_block, float* __restrict__ part) {
+  constexpr int E = Vec<T>::N;
+  const int c0 = (blockIdx.x * blockDim.x + threadIdx.x) * E;
+  if (c0 >= N) return;
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  const int r0 = blockIdx.y * rows_per_block;
+  const int r1 = min(n, r0 + rows_per_block);
+  for (int r = r0; r < r1; ++r) {
+    Vec<T> v;
+    v.load(Y + (size_t)r * ld + c0);
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] += v.get(e);
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) part[(size_t)blockIdx.y * N + c0 + e] = acc[e];
+}
+
+// Vectors per thread and threads per block for a row of h elements.
+template <typename T>
+void row_plan(int h, int* vpt, int* threads) {
+  const int nvec = h / Vec<T>::N;
+  int v = 1;
+  while ((nvec + v - 1) / v > kLnThreadsMax) v *= 2;
+  *vpt = v;
+  *threads = (((nvec + v - 1) / v) + 31) / 32 * 32;
+}
+
+template <typename T>
+cudaError_t ln_fwd_t(const void* x, const void* g, const void* b, void* u, float* mean,
+                     float* rstd, int n, int h, float eps, const LaunchCtx& c) {
+  if (n == 0) return cudaSuccess;
+  int vpt, threads;
+  row_plan<T>(h, &vpt, &threads);
+  const int rows = n >= 4 * c.num_sms * 4 ? 4 : 1;
+  const int grid = (n + rows - 1) / rows;
+#define LN_FWD_CASE(VV)                                                                      \
+  case VV:                                                                                   \
+    ln_fwd_kernel<T, VV><<<grid, threads, 0, c.stream>>>(                                    \
+        (const T*)x, (const T*)g, (const T*)b, (T*)u, mean, rstd, n, h, eps, rows);          \
+    break;
+  c.before(KK_LN_FWD, (double)n * h * (2.0 * sizeof(T)) + 8.0 * n);
+  switch (vpt) {
+    LN_FWD_CASE(1)
+    LN_FWD_CASE(2)
+    LN_FWD_CASE(4)
+    LN_FWD_CASE(8)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef LN_FWD_CASE
+  c.after();
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t ln_bwd_t(const float* du, const void* x, const float* mean, const float* rstd,
+                     const void* g, const void* resid, void* dx, float* dgamma, float* dbeta,
+                     float* partial, int n, int h, const LaunchCtx& c) {
+  int vpt, threads;
+  row_plan<T>(h, &vpt, &threads);
+  const int nblk = n < kLnBwdBlocks ? (n > 0 ? n : 1) : kLnBwdBlocks;
+  const int rows = (n + nblk - 1) / nblk;
+  float* pg = partial;
+  float* pb = partial + (size_t)nblk * h;
+  const size_t smem = 3 * (size_t)h * sizeof(float);
+#define LN_BWD_CASE(VV)                                                                     \
+  case VV:                                                                                  \
+    if (smem > 48 * 1024) {                                                                 \
+      cudaError_t fe = cudaFuncSetAttribute(ln_bwd_kernel<T, VV>,                           \
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,    \
+                                            (int)smem);                                     \
+      if (fe != cudaSuccess) return fe;                                                     \
+    }                                                                                       \
+    ln_bwd_kernel<T, VV><<<nblk, threads, smem, c.stream>>>(du, (const T*)x, mean, rstd,    \
+                                                            (const T*)g, (const T*)resid,   \
+                                                            (T*)dx, pg, pb, n, h, rows);    \
+    break;
+  c.before(KK_LN_BWD, (double)n * h * (3.0 * sizeof(T) + 4.0) + 8.0 * n);
+  switch (vpt) {
+    LN_BWD_CASE(1)
+    LN_BWD_CASE(2)
+    LN_BWD_CASE(4)
+    LN_BWD_CASE(8)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef LN_BWD_CASE
+  c.after();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  c.before(KK_FINALIZE, 4.0 * nblk * h);
+  finalize_cols_kernel<<<(h + 255) / 256, 256, 0, c.stream>>>(pg, nblk, h, dgamma);
+  c.after();
+  c.before(KK_FINALIZE, 4.0 * nblk * h);
+  finalize_cols_kernel<<<(h + 255) / 256, 256, 0, c.stream>>>(pb, nblk, h, dbeta);
+  c.after();
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t colsum_t(const void* Y, int64_t ld, int n, int N, float* out, float* partial,
+                     const LaunchCtx& c) {
+  constexpr int E = Vec<T>::N;
+  const int nblk = n < kColsumBlocks ? (n > 0 ? n : 1) : kColsumBlocks;
+  const int rows = (n + nblk - 1) / nblk;
+  const int threads = 256;
+  dim3 grid((N / E + threads - 1) / threads, nblk);
+  c.before(KK_COLSUM, (double)n * N * sizeof(T));
+  colsum_partial_kernel<T><<<grid, threads, 0, c.stream>>>((const T*)Y, ld, n, N, rows, partial);
+  c.after();
+  c.before(KK_FINALIZE, 4.0 * nblk * N);
+  finalize_cols_kernel<<<(N + 255) / 256, 256, 0, c.stream>>>(partial, nblk, N, out);
+  c.after();
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t ln_bwd_partial_floats(int n, int h) {
+  const size_t nblk = n < kLnBwdBlocks ? (n > 0 ? n : 1) : kLnBwdBlocks;
+  return 2 * nblk * (size_t)h;
+}
+size_t colsum_partial_floats(int n, int N) {
+  const size_t nblk = n < kColsumBlocks ? (n > 0 ? n : 1) : kColsumBlocks;
+  return nblk * (size_t)N;
+}
+
+cudaError_t ln_fwd(int dtype, const void* x, const void* g, const void* b, void* u, float* mean,
+                   float* rstd, int n, int h, float eps, const LaunchCtx& c) {
+  return dtype == kBF16 ? ln_fwd_t<bf16>(x, g, b, u, mean, rstd, n, h, eps, c)
+                        : ln_fwd_t<float>(x, g, b, u, mean, rstd, n, h, eps, c);
+}
+
+cudaError_t ln_bwd(int dtype, const float* du, const void* x, const float* mean,
+                   const float* rstd, const void* g, const void* resid, void* dx,
+                   float* dgamma, float* dbeta, float* partial, int n, int h,
+                   const LaunchCtx& c) {
+  return dtype == kBF16
+             ? ln_bwd_t<bf16>(du, x, mean, rstd, g, resid, dx, dgamma, dbeta, partial, n, h, c)
+             : ln_bwd_t<float>(du, x, mean, rstd, g, resid, dx, dgamma, dbeta, partial, n, h, c);
+}
+
+cudaError_t colsum(int dtype, const void* Y, int64_t ld, int n, int N, float* out,
+                   float* partial, const LaunchCtx& c) {
+  return dtype == kBF16 ? colsum_t<bf16>(Y, ld, n, N, out, partial, c)
+                        : colsum_t<float>(Y, ld, n, N, out, partial, c);
+}
+
+}  // namespace mtl

@@ -1,0 +1,515 @@
+// The C ABI: argument validation, buffer layouts and the stream-ordered launch
+// sequence of one pre-LN GPT layer, forward and backward.
+//
+// Layer ("Megatron-LM: GPU-Cluster Training Parallelism"; sections "Paper 1: BERT
+// LayerNorm Rearrangement", "Paper 1: The f/g Conjugate Operators", "Paper 1: QKV
+// Column-Parallel Splitting in Detail", "Fused Transformer Kernels"):
+//   u1 = LN1(x); qkv = u1 W_qkv^T + b_qkv            (column-parallel, f = identity)
+//   ctx = causal softmax(Q K^T / sqrt d) V per head    (local to a partition)
+//   x1 = x + b_o + g( sum_p ctx[:, P_p] W_o[:, P_p]^T )(row-parallel + g)
+//   u2 = LN2(x1); z = u2 W_fc1^T + b_fc1; a = GeLU(z)  (column-parallel)
+//   y  = x1 + b_fc2 + g( sum_p a[:, F_p] W_fc2[:, F_p]^T )
+// Backward mirrors it; f sums the partitions' partial input gradients of the
+// two column-parallel GEMMs.  g and f are fixed-order sums inside the GEMMs.
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/mtl.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace mtl;
+
+namespace {
+
+thread_local char g_cuda_err[256] = {0};
+thread_local int g_launches = 0;
+thread_local Profiler g_prof = {nullptr, 0, 0, nullptr, nullptr};
+
+constexpr size_t kAlign = 256;
+constexpr size_t kStatusBytes = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+mtl_status cuda_fail(cudaError_t e, const char* where) {
+  snprintf(g_cuda_err, sizeof(g_cuda_err), "%s: %s", where, cudaGetErrorString(e));
+  return MTL_ERR_CUDA;
+}
+
+int device_sm_count() {
+  static int counts[64];
+  static std::once_flag once[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::call_once(once[dev], [dev]() {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    counts[dev] = v;
+  });
+  return counts[dev];
+}
+
+struct Dims {
+  int64_t h, heads, d, seq, batch, n, f, t;
+  int dtype;
+  size_t esz;
+};
+
+mtl_status validate(const mtl_layer_desc* desc, Dims* o) {
+  if (!desc) return MTL_ERR_INVALID_ARG;
+  const mtl_layer_desc& d = *desc;
+  if (d.h <= 0 || d.heads <= 0 || d.seq <= 0 || d.batch < 0 || d.ffn <= 0 || d.t <= 0)
+    return MTL_ERR_INVALID_ARG;
+  if (d.dtype != MTL_F32 && d.dtype != MTL_BF16) return MTL_ERR_INVALID_ARG;
+  if (!(d.ln_eps > 0.f)) return MTL_ERR_INVALID_ARG;
+  if (d.h % d.heads) return MTL_ERR_INVALID_ARG;
+  if (d.heads % d.t || d.ffn % d.t) return MTL_ERR_INVALID_ARG;
+  const int dh = d.h / d.heads;
+  if (dh != 64 && dh != 96 && dh != 128) return MTL_ERR_UNSUPPORTED;
+  if (d.causal != 1) return MTL_ERR_UNSUPPORTED;
+  if ((int64_t)d.batch * d.seq > (int64_t)1 << 30) return MTL_ERR_UNSUPPORTED;
+  if (d.dtype == MTL_BF16) {
+    if (d.seq % 128 || d.h % 64 || d.ffn % 64) return MTL_ERR_UNSUPPORTED;
+    if ((d.h / d.t) % 64 || ((3 * d.h) / d.t) % 64 || (d.ffn / d.t) % 64) return MTL_ERR_UNSUPPORTED;
+  } else {
+    if (d.h % 4 || d.ffn % 4) return MTL_ERR_UNSUPPORTED;
+    if (d.seq > 8192) return MTL_ERR_UNSUPPORTED;
+  }
+  o->h = d.h;
+  o->heads = d.heads;
+  o->d = dh;
+  o->seq = d.seq;
+  o->batch = d.batch;
+  o->n = (int64_t)d.batch * d.seq;
+  o->f = d.ffn;
+  o->t = d.t;
+  o->dtype = d.dtype;
+  o->esz = d.dtype == MTL_BF16 ? 2 : 4;
+  return MTL_OK;
+}
+
+mtl_saved_layout saved_layout(const Dims& D) {
+  mtl_saved_layout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align_up(bytes);
+    return at;
+  };
+  const size_t nh = (size_t)D.n * D.h * D.esz;
+  L.mu1 = take((size_t)D.n * 4);
+  L.rstd1 = take((size_t)D.n * 4);
+  L.u1 = take(nh);
+  L.qkv = take(3 * nh);
+  L.ctx = take(nh);
+  L.lse = take((size_t)D.batch * D.heads * D.seq * 4);
+  L.x1 = take(nh);
+  L.mu2 = take((size_t)D.n * 4);
+  L.rstd2 = take((size_t)D.n * 4);
+  L.u2 = take(nh);
+  L.z = take((size_t)D.n * D.f * D.esz);
+  L.a = take((size_t)D.n * D.f * D.esz);
+  L.total = off;
+  return L;
+}
+
+// Backward scratch, after the status word.
+struct WsLayout {
+  size_t dz, du, dx1, dctx, dqkv, dsum, partial, total;
+};
+
+WsLayout ws_layout(const Dims& D) {
+  WsLayout W;
+  size_t off = kStatusBytes;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align_up(bytes);
+    return at;
+  };
+  const size_t nh = (size_t)D.n * D.h;
+  W.dz = take((size_t)D.n * D.f * D.esz);
+  W.du = take(nh * 4);
+  W.dx1 = take(nh * D.esz);
+  W.dctx = take(nh * D.esz);
+  W.dqkv = take(3 * nh * D.esz);
+  W.dsum = take((size_t)D.batch * D.heads * D.seq * 4);
+  size_t pf = ln_bwd_partial_floats((int)D.n, (int)D.h);
+  const size_t widest = (size_t)(D.f > 3 * D.h ? D.f : 3 * D.h);
+  const size_t pc = colsum_partial_floats((int)D.n, (int)widest);
+  if (pc > pf) pf = pc;
+  W.partial = take(pf * 4);
+  W.total = off;
+  return W;
+}
+
+template <typename T>
+T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(base) + off);
+}
+template <typename T>
+const T* at(const void* base, size_t off) {
+  return reinterpret_cast<const T*>(static_cast<const char*>(base) + off);
+}
+
+bool weights_ok(const mtl_weights* w) {
+  if (!w) return false;
+  const void* ps[] = {w->w_qkv, w->b_qkv, w->w_o,   w->b_o,   w->w_fc1, w->b_fc1,
+                      w->w_fc2, w->b_fc2, w->ln1_g, w->ln1_b, w->ln2_g, w->ln2_b};
+  for (const void* p : ps)
+    if (!aligned16(p)) return false;
+  return true;
+}
+
+bool grads_ok(const mtl_grads* g) {
+  if (!g) return false;
+  const void* ps[] = {g->w_qkv, g->b_qkv, g->w_o,   g->b_o,   g->w_fc1, g->b_fc1,
+                      g->w_fc2, g->b_fc2, g->ln1_g, g->ln1_b, g->ln2_g, g->ln2_b};
+  for (const void* p : ps)
+    if (!aligned16(p)) return false;
+  return true;
+}
+
+// One GEMM on the path of the layer's dtype: tcgen05 for bf16, exact fp32 on
+// CUDA cores for fp32.
+cudaError_t run_gemm(const Dims& D, const GemmArgs& a, const LaunchCtx& c) {
+  if (D.dtype == MTL_BF16) return gemm_tc(a, c);
+  return gemm_simt(kF32, a, c);
+}
+
+GemmArgs gemm_args(int M, int N, int K, int parts, const void* A, int64_t lda, bool ak,
+                   const void* B, int64_t ldb, bool bk, int epi, void* C, int64_t ldc, bool cf32,
+                   unsigned* status) {
+  GemmArgs g;
+  memset(&g, 0, sizeof(g));
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.parts = parts;
+  g.A = {A, lda, ak};
+  g.B = {B, ldb, bk};
+  g.epi = epi;
+  g.C = C;
+  g.ldc = ldc;
+  g.c_f32 = cf32;
+  g.status = status;
+  return g;
+}
+
+#define MTL_TRY(expr, where)                     \
+  do {                                           \
+    cudaError_t _e = (expr);                     \
+    if (_e != cudaSuccess) return cuda_fail(_e, where); \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+const char* mtl_status_str(mtl_status s) {
+  switch (s) {
+    case MTL_OK: return "ok";
+    case MTL_ERR_INVALID_ARG: return "invalid argument";
+    case MTL_ERR_UNSUPPORTED: return "unsupported layer shape";
+    case MTL_ERR_WORKSPACE: return "workspace too small";
+    case MTL_ERR_CUDA: return "CUDA error";
+    case MTL_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+const char* mtl_last_cuda_error(void) { return g_cuda_err; }
+
+int32_t mtl_last_launch_count(void) { return g_launches; }
+
+void mtl_profile_set(void** events, int32_t capacity, int32_t* kinds, double* work) {
+  g_prof.events = reinterpret_cast<cudaEvent_t*>(events);
+  g_prof.capacity = events ? capacity : 0;
+  g_prof.count = 0;
+  g_prof.kinds = kinds;
+  g_prof.work = work;
+}
+
+int32_t mtl_profile_count(void) { return g_prof.count; }
+
+mtl_status mtl_layer_sizes(const mtl_layer_desc* desc, size_t* saved_bytes,
+                           size_t* workspace_bytes) {
+  Dims D;
+  mtl_status st = validate(desc, &D);
+  if (st != MTL_OK) return st;
+  if (saved_bytes) *saved_bytes = saved_layout(D).total;
+  if (workspace_bytes) *workspace_bytes = ws_layout(D).total;
+  return MTL_OK;
+}
+
+mtl_status mtl_layer_saved_layout(const mtl_layer_desc* desc, mtl_saved_layout* out) {
+  Dims D;
+  mtl_status st = validate(desc, &D);
+  if (st != MTL_OK) return st;
+  if (!out) return MTL_ERR_INVALID_ARG;
+  *out = saved_layout(D);
+  return MTL_OK;
+}
+
+mtl_status mtl_layer_fwd(const mtl_layer_desc* desc, const mtl_weights* w, const void* x,
+                         void* y, void* saved, void* workspace, size_t ws_bytes,
+                         mtl_stream stream) {
+  g_launches = 0;
+  g_cuda_err[0] = 0;
+  Dims D;
+  mtl_status st = validate(desc, &D);
+  if (st != MTL_OK) return st;
+  if (!weights_ok(w) || !aligned16(x) || !aligned16(y) || !aligned16(saved) ||
+      !aligned16(workspace) || x == y || y == saved)
+    return MTL_ERR_INVALID_ARG;
+  const WsLayout W = ws_layout(D);
+  if (ws_bytes < W.total) return MTL_ERR_WORKSPACE;
+  const int nsm = device_sm_count();
+  if (nsm <= 0) return cuda_fail(cudaGetLastError(), "device query");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  LaunchCtx c{s, nsm, &g_launches, &g_prof};
+  unsigned* status = static_cast<unsigned*>(workspace);
+  MTL_TRY(cudaMemsetAsync(status, 0, kStatusBytes, s), "status reset");
+  if (D.n == 0) return MTL_OK;
+
+  const mtl_saved_layout L = saved_layout(D);
+  const int n = (int)D.n, h = (int)D.h, f = (int)D.f, t = (int)D.t;
+  void* u1 = at<char>(saved, L.u1);
+  void* qkv = at<char>(saved, L.qkv);
+  void* ctx = at<char>(saved, L.ctx);
+  void* x1 = at<char>(saved, L.x1);
+  void* u2 = at<char>(saved, L.u2);
+  void* z = at<char>(saved, L.z);
+  void* a = at<char>(saved, L.a);
+  const bool bf = D.dtype == MTL_BF16;
+
+  // F1 LN1
+  MTL_TRY(ln_fwd(D.dtype, x, w->ln1_g, w->ln1_b, u1, at<float>(saved, L.mu1),
+                 at<float>(saved, L.rstd1), n, h, desc->ln_eps, c),
+          "ln1 fwd");
+  // F2 QKV, column-parallel: partition p = rows [p*3h/t, (p+1)*3h/t) of w_qkv
+  {
+    GemmArgs g = gemm_args(n, 3 * h, h, 1, u1, h, true, w->w_qkv, h, true, EPI_BIAS, qkv, 3 * h,
+                           false, status);
+    g.bias = w->b_qkv;
+    MTL_TRY(run_gemm(D, g, c), "qkv gemm");
+  }
+  // F3 attention per head
+  MTL_TRY(attn_fwd_simt(D.dtype, qkv, ctx, at<float>(saved, L.lse), (int)D.batch, (int)D.seq,
+                        (int)D.heads, (int)D.d, c),
+          "attention fwd");
+  // F4 out-proj, row-parallel + g: t partials over K = h, + b_o + x
+  {
+    GemmArgs g = gemm_args(n, h, h, t, ctx, h, true, w->w_o, h, true, EPI_BIAS_RESID, x1, h,
+                           false, status);
+    g.bias = w->b_o;
+    g.R = x;
+    g.ldr = h;
+    MTL_TRY(run_gemm(D, g, c), "out-proj gemm");
+  }
+  // F5 LN2
+  MTL_TRY(ln_fwd(D.dtype, x1, w->ln2_g, w->ln2_b, u2, at<float>(saved, L.mu2),
+                 at<float>(saved, L.rstd2), n, h, desc->ln_eps, c),
+          "ln2 fwd");
+  // F6 fc1, column-parallel + bias + GeLU (saves z and a)
+  {
+    GemmArgs g = gemm_args(n, f, h, 1, u2, h, true, w->w_fc1, h, true, EPI_BIAS_GELU, a, f, false,
+                           status);
+    g.bias = w->b_fc1;
+    g.Z = z;
+    g.ldz = f;
+    MTL_TRY(run_gemm(D, g, c), "fc1 gemm");
+  }
+  // F7 fc2, row-parallel + g: t partials over K = ffn, + b_fc2 + x1
+  {
+    GemmArgs g = gemm_args(n, h, f, t, a, f, true, w->w_fc2, f, true, EPI_BIAS_RESID, y, h, false,
+                           status);
+    g.bias = w->b_fc2;
+    g.R = x1;
+    g.ldr = h;
+    MTL_TRY(run_gemm(D, g, c), "fc2 gemm");
+  }
+  (void)bf;
+  return MTL_OK;
+}
+
+mtl_status mtl_layer_bwd(const mtl_layer_desc* desc, const mtl_weights* w, const void* x,
+                         const void* saved, const void* dy, void* dx, const mtl_grads* gr,
+                         void* workspace, size_t ws_bytes, mtl_stream stream) {
+  g_launches = 0;
+  g_cuda_err[0] = 0;
+  Dims D;
+  mtl_status st = validate(desc, &D);
+  if (st != MTL_OK) return st;
+  if (!weights_ok(w) || !grads_ok(gr) || !aligned16(x) || !aligned16(saved) || !aligned16(dy) ||
+      !aligned16(dx) || !aligned16(workspace) || dx == dy)
+    return MTL_ERR_INVALID_ARG;
+  const WsLayout W = ws_layout(D);
+  if (ws_bytes < W.total) return MTL_ERR_WORKSPACE;
+  const int nsm = device_sm_count();
+  if (nsm <= 0) return cuda_fail(cudaGetLastError(), "device query");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  LaunchCtx c{s, nsm, &g_launches, &g_prof};
+  unsigned* status = static_cast<unsigned*>(workspace);
+  MTL_TRY(cudaMemsetAsync(status, 0, kStatusBytes, s), "status reset");
+
+  const mtl_saved_layout L = saved_layout(D);
+  const int n = (int)D.n, h = (int)D.h, f = (int)D.f, t = (int)D.t;
+  const void* u1 = at<char>(saved, L.u1);
+  const void* qkv = at<char>(saved, L.qkv);
+  const void* ctx = at<char>(saved, L.ctx);
+  const void* x1 = at<char>(saved, L.x1);
+  const void* u2 = at<char>(saved, L.u2);
+  const void* z = at<char>(saved, L.z);
+  const void* a = at<char>(saved, L.a);
+  void* dz = at<char>(workspace, W.dz);
+  float* du = at<float>(workspace, W.du);
+  void* dx1 = at<char>(workspace, W.dx1);
+  void* dctx = at<char>(workspace, W.dctx);
+  void* dqkv = at<char>(workspace, W.dqkv);
+  float* dsum = at<float>(workspace, W.dsum);
+  float* partial = at<float>(workspace, W.partial);
+
+  if (D.n == 0) {
+    // no tokens: every gradient is zero
+    void* zs[] = {gr->w_qkv, gr->b_qkv, gr->w_o, gr->b_o, gr->w_fc1, gr->b_fc1,
+                  gr->w_fc2, gr->b_fc2, gr->ln1_g, gr->ln1_b, gr->ln2_g, gr->ln2_b};
+    size_t sz[] = {3 * (size_t)h * h, 3 * (size_t)h, (size_t)h * h, (size_t)h,
+                   (size_t)f * h,     (size_t)f,     (size_t)h * f, (size_t)h,
+                   (size_t)h,         (size_t)h,     (size_t)h,     (size_t)h};
+    for (int i = 0; i < 12; ++i) MTL_TRY(cudaMemsetAsync(zs[i], 0, sz[i] * 4, s), "zero grads");
+    return MTL_OK;
+  }
+
+  // B1 fc2 dgrad + GeLU': dz = (dy W_fc2) * GeLU'(z)  (column-local, no reduction)
+  {
+    GemmArgs g = gemm_args(n, f, h, 1, dy, h, true, w->w_fc2, f, false, EPI_DGELU, dz, f, false,
+                           status);
+    g.Z = const_cast<void*>(z);
+    g.ldz = f;
+    MTL_TRY(run_gemm(D, g, c), "fc2 dgrad");
+  }
+  // B2 fc2 wgrad dW2 = dy^T a, db2 = sum_rows dy
+  MTL_TRY(run_gemm(D, gemm_args(h, f, n, 1, dy, h, false, a, f, false, EPI_STORE, gr->w_fc2, f,
+                                true, status),
+                   c),
+          "fc2 wgrad");
+  MTL_TRY(colsum(D.dtype, dy, h, n, h, static_cast<float*>(gr->b_fc2), partial, c), "db_fc2");
+  // B3 fc1 dgrad with the f reduction: du2 = sum_p dz[:, F_p] W_fc1[F_p, :]
+  MTL_TRY(run_gemm(D, gemm_args(n, h, f, t, dz, f, true, w->w_fc1, h, false, EPI_STORE, du, h,
+                                true, status),
+                   c),
+          "fc1 dgrad");
+  // B4 fc1 wgrad dW1 = dz^T u2, db1 = sum_rows dz
+  MTL_TRY(run_gemm(D, gemm_args(f, h, n, 1, dz, f, false, u2, h, false, EPI_STORE, gr->w_fc1, h,
+                                true, status),
+                   c),
+          "fc1 wgrad");
+  MTL_TRY(colsum(D.dtype, dz, f, n, f, static_cast<float*>(gr->b_fc1), partial, c), "db_fc1");
+  // B5 LN2 backward + residual: dx1 = dy + LN2_bwd(du2)
+  MTL_TRY(ln_bwd(D.dtype, du, x1, at<float>(saved, L.mu2), at<float>(saved, L.rstd2), w->ln2_g, dy,
+                 dx1, static_cast<float*>(gr->ln2_g), static_cast<float*>(gr->ln2_b), partial, n,
+                 h, c),
+          "ln2 bwd");
+  // B6 out-proj dgrad dctx = dx1 W_o, wgrad dW_o = dx1^T ctx, db_o = sum_rows dx1
+  MTL_TRY(run_gemm(D, gemm_args(n, h, h, 1, dx1, h, true, w->w_o, h, false, EPI_STORE, dctx, h,
+                                false, status),
+                   c),
+          "out-proj dgrad");
+  MTL_TRY(run_gemm(D, gemm_args(h, h, n, 1, dx1, h, false, ctx, h, false, EPI_STORE, gr->w_o, h,
+                                true, status),
+                   c),
+          "out-proj wgrad");
+  MTL_TRY(colsum(D.dtype, dx1, h, n, h, static_cast<float*>(gr->b_o), partial, c), "db_o");
+  // B7 attention backward per head
+  MTL_TRY(attn_bwd_simt(D.dtype, qkv, ctx, at<float>(saved, L.lse), dctx, dqkv, dsum,
+                        (int)D.batch, (int)D.seq, (int)D.heads, (int)D.d, c),
+          "attention bwd");
+  // B8 QKV wgrad dW_qkv = dqkv^T u1, db_qkv = sum_rows dqkv
+  MTL_TRY(run_gemm(D, gemm_args(3 * h, h, n, 1, dqkv, 3 * h, false, u1, h, false, EPI_STORE,
+                                gr->w_qkv, h, true, status),
+                   c),
+          "qkv wgrad");
+  MTL_TRY(colsum(D.dtype, dqkv, 3 * h, n, 3 * h, static_cast<float*>(gr->b_qkv), partial, c),
+          "db_qkv");
+  // B9 QKV dgrad with the f reduction: du1 = sum_p dqkv[:, Q_p] W_qkv[Q_p, :]
+  MTL_TRY(run_gemm(D, gemm_args(n, h, 3 * h, t, dqkv, 3 * h, true, w->w_qkv, h, false, EPI_STORE,
+                                du, h, true, status),
+                   c),
+          "qkv dgrad");
+  // B10 LN1 backward + residual: dx = dx1 + LN1_bwd(du1)
+  MTL_TRY(ln_bwd(D.dtype, du, x, at<float>(saved, L.mu1), at<float>(saved, L.rstd1), w->ln1_g,
+                 dx1, dx, static_cast<float*>(gr->ln1_g), static_cast<float*>(gr->ln1_b),
+                 partial, n, h, c),
+          "ln1 bwd");
+  return MTL_OK;
+}
+
+mtl_status mtl_layer_check(void* workspace, mtl_stream stream) {
+  if (!aligned16(workspace)) return MTL_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "stream sync");
+  unsigned word = 0;
+  e = cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  if (word) {
+    unsigned zero = 0;
+    cudaMemcpy(workspace, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+  }
+  if (word & kDevErrTimeout) return MTL_ERR_TIMEOUT;
+  if (word) return MTL_ERR_INVALID_ARG;
+  return MTL_OK;
+}
+
+mtl_status mtl_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, int32_t k_parts,
+                    const void* A, int64_t lda, int32_t a_k_major, const void* B, int64_t ldb,
+                    int32_t b_k_major, int32_t epi, const void* bias, const void* R, int64_t ldr,
+                    void* Z, int64_t ldz, void* C, int64_t ldc, int32_t c_f32, void* workspace,
+                    size_t ws_bytes, mtl_stream stream) {
+  g_launches = 0;
+  g_cuda_err[0] = 0;
+  if (dtype != MTL_F32 && dtype != MTL_BF16) return MTL_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || k_parts < 1 || K % k_parts) return MTL_ERR_INVALID_ARG;
+  if (epi < EPI_STORE || epi > EPI_DGELU) return MTL_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C) || !aligned16(workspace))
+    return MTL_ERR_INVALID_ARG;
+  if (ws_bytes < kStatusBytes) return MTL_ERR_WORKSPACE;
+  const bool need_bias = epi == EPI_BIAS || epi == EPI_BIAS_RESID || epi == EPI_BIAS_GELU;
+  if (need_bias && !aligned16(bias)) return MTL_ERR_INVALID_ARG;
+  if (epi == EPI_BIAS_RESID && !aligned16(R)) return MTL_ERR_INVALID_ARG;
+  if ((epi == EPI_BIAS_GELU || epi == EPI_DGELU) && !aligned16(Z)) return MTL_ERR_INVALID_ARG;
+  const int64_t a_rows = a_k_major ? M : K, b_rows = b_k_major ? N : K;
+  const int64_t a_cols = a_k_major ? K : M, b_cols = b_k_major ? K : N;
+  if ((a_rows > 0 && lda < a_cols) || (b_rows > 0 && ldb < b_cols) || ldc < N)
+    return MTL_ERR_INVALID_ARG;
+  if (epi == EPI_BIAS_RESID && ldr < N) return MTL_ERR_INVALID_ARG;
+  if ((epi == EPI_BIAS_GELU || epi == EPI_DGELU) && ldz < N) return MTL_ERR_INVALID_ARG;
+  unsigned* status = static_cast<unsigned*>(workspace);
+  GemmArgs g = gemm_args(M, N, K, k_parts, A, lda, a_k_major != 0, B, ldb, b_k_major != 0, epi, C,
+                         ldc, c_f32 != 0, status);
+  g.bias = bias;
+  g.R = R;
+  g.ldr = ldr;
+  g.Z = Z;
+  g.ldz = ldz;
+  if (dtype == MTL_BF16) {
+    if (!gemm_tc_supported(g) || K == 0) return MTL_ERR_UNSUPPORTED;
+  }
+  const int nsm = device_sm_count();
+  if (nsm <= 0) return cuda_fail(cudaGetLastError(), "device query");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  LaunchCtx c{s, nsm, &g_launches, &g_prof};
+  MTL_TRY(cudaMemsetAsync(status, 0, kStatusBytes, s), "status reset");
+  if (M == 0 || N == 0) return MTL_OK;
+  if (dtype == MTL_BF16) {
+    MTL_TRY(gemm_tc(g, c), "gemm");
+  } else {
+    MTL_TRY(gemm_simt(kF32, g, c), "gemm");
+  }
+  return MTL_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,209 @@
+"""ctypes binding of the C ABI in include/mtl.h (argument marshalling only).
+
+Every step of the layer runs in the CUDA library libmtl.so; this module only
+turns torch tensors into device pointers, picks the current CUDA stream and
+raises on a non-OK status.  It fails loudly when the library is missing: there
+is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PARAM_NAMES = ("w_qkv", "b_qkv", "w_o", "b_o", "w_fc1", "b_fc1", "w_fc2", "b_fc2",
+               "ln1_g", "ln1_b", "ln2_g", "ln2_b")
+SAVED_NAMES = ("mu1", "rstd1", "u1", "qkv", "ctx", "lse", "x1", "mu2", "rstd2", "u2", "z", "a")
+
+F32, BF16 = 0, 1
+STATUS = {0: "MTL_OK", 1: "MTL_ERR_INVALID_ARG", 2: "MTL_ERR_UNSUPPORTED",
+          3: "MTL_ERR_WORKSPACE", 4: "MTL_ERR_CUDA", 5: "MTL_ERR_TIMEOUT"}
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmtl.so")
+
+
+class MtlError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        msg = f"{where}: {STATUS.get(status, status)}"
+        if detail:
+            msg += f" ({detail})"
+        super().__init__(msg)
+
+
+class LayerDesc(ctypes.Structure):
+    _fields_ = [("h", ctypes.c_int32), ("heads", ctypes.c_int32), ("seq", ctypes.c_int32),
+                ("batch", ctypes.c_int32), ("ffn", ctypes.c_int32), ("t", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("ln_eps", ctypes.c_float), ("causal", ctypes.c_int32)]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in PARAM_NAMES]
+
+
+class Grads(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in PARAM_NAMES]
+
+
+class SavedLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in SAVED_NAMES] + [("total", ctypes.c_size_t)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libmtl.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "tensor_model_transformer_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, sz, i32, i64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_int64
+        pd = ctypes.POINTER(LayerDesc)
+        L.mtl_layer_sizes.argtypes = [pd, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+        L.mtl_layer_saved_layout.argtypes = [pd, ctypes.POINTER(SavedLayout)]
+        L.mtl_layer_fwd.argtypes = [pd, ctypes.POINTER(Weights), vp, vp, vp, vp, sz, vp]
+        L.mtl_layer_bwd.argtypes = [pd, ctypes.POINTER(Weights), vp, vp, vp, vp,
+                                    ctypes.POINTER(Grads), vp, sz, vp]
+        L.mtl_layer_check.argtypes = [vp, vp]
+        L.mtl_gemm.argtypes = [i32, i32, i32, i32, i32, vp, i64, i32, vp, i64, i32, i32, vp, vp,
+                               i64, vp, i64, vp, i64, i32, vp, sz, vp]
+        L.mtl_status_str.argtypes = [ctypes.c_int]
+        L.mtl_status_str.restype = ctypes.c_char_p
+        L.mtl_last_cuda_error.restype = ctypes.c_char_p
+        L.mtl_last_launch_count.restype = ctypes.c_int32
+        for fn in ("mtl_layer_sizes", "mtl_layer_saved_layout", "mtl_layer_fwd", "mtl_layer_bwd",
+                   "mtl_layer_check", "mtl_gemm"):
+            getattr(L, fn).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        detail = lib().mtl_last_cuda_error().decode() if status == 4 else ""
+        raise MtlError(status, where, detail)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def layer_desc(h, heads, seq, batch, ffn, t, dtype, ln_eps=1e-5, causal=1) -> LayerDesc:
+    dt = {"f32": F32, "bf16": BF16, F32: F32, BF16: BF16}[dtype]
+    return LayerDesc(h, heads, seq, batch, ffn, t, dt, ln_eps, causal)
+
+
+def layer_sizes(desc: LayerDesc):
+    """(saved_bytes, workspace_bytes) of mtl_layer_sizes."""
+    s, w = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check(lib().mtl_layer_sizes(ctypes.byref(desc), ctypes.byref(s), ctypes.byref(w)),
+           "mtl_layer_sizes")
+    return s.value, w.value
+
+
+def layer_saved_layout(desc: LayerDesc) -> dict:
+    out = SavedLayout()
+    _check(lib().mtl_layer_saved_layout(ctypes.byref(desc), ctypes.byref(out)),
+           "mtl_layer_saved_layout")
+    return {n: getattr(out, n) for n in SAVED_NAMES + ("total",)}
+
+
+def _weights(w: dict) -> Weights:
+    return Weights(*[_ptr(w[n]) for n in PARAM_NAMES])
+
+
+def _grads(g: dict) -> Grads:
+    return Grads(*[_ptr(g[n]) for n in PARAM_NAMES])
+
+
+def layer_fwd(desc, weights: dict, x, y, saved, workspace, stream=None):
+    """mtl_layer_fwd on torch tensors (device memory)."""
+    wt = _weights(weights)
+    _check(lib().mtl_layer_fwd(ctypes.byref(desc), ctypes.byref(wt), _ptr(x), _ptr(y),
+                               _ptr(saved), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                               _stream(stream)), "mtl_layer_fwd")
+
+
+def layer_bwd(desc, weights: dict, x, saved, dy, dx, grads: dict, workspace, stream=None):
+    """mtl_layer_bwd on torch tensors (device memory)."""
+    wt, gt = _weights(weights), _grads(grads)
+    _check(lib().mtl_layer_bwd(ctypes.byref(desc), ctypes.byref(wt), _ptr(x), _ptr(saved),
+                               _ptr(dy), _ptr(dx), ctypes.byref(gt), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream)),
+           "mtl_layer_bwd")
+
+
+def layer_check(workspace, stream=None):
+    """mtl_layer_check: waits for the stream, raises MtlError on a device timeout."""
+    _check(lib().mtl_layer_check(_ptr(workspace), _stream(stream)), "mtl_layer_check")
+
+
+def last_launch_count() -> int:
+    return lib().mtl_last_launch_count()
+
+
+def gemm(dtype, M, N, K, parts, A, lda, a_k_major, B, ldb, b_k_major, epi, C, ldc, c_f32,
+         workspace, bias=None, R=None, ldr=0, Z=None, ldz=0, stream=None):
+    """mtl_gemm on torch tensors."""
+    dt = {"f32": F32, "bf16": BF16, F32: F32, BF16: BF16}[dtype]
+    _check(lib().mtl_gemm(dt, M, N, K, parts, _ptr(A), lda, int(a_k_major), _ptr(B), ldb,
+                          int(b_k_major), epi, _ptr(bias), _ptr(R), ldr, _ptr(Z), ldz, _ptr(C),
+                          ldc, int(c_f32), _ptr(workspace),
+                          workspace.numel() * workspace.element_size(), _stream(stream)),
+           "mtl_gemm")
+
+
+# ---------------------------------------------------------------- allocation helpers
+
+def torch_dtype(desc: LayerDesc):
+    import torch
+    return torch.bfloat16 if desc.dtype == BF16 else torch.float32
+
+
+def alloc_layer_buffers(desc: LayerDesc, device="cuda"):
+    """Device buffers for one layer: saved, workspace (uint8) and the fp32 grads."""
+    import torch
+    saved_b, ws_b = layer_sizes(desc)
+    h, f = desc.h, desc.ffn
+    shapes = {"w_qkv": (3 * h, h), "b_qkv": (3 * h,), "w_o": (h, h), "b_o": (h,),
+              "w_fc1": (f, h), "b_fc1": (f,), "w_fc2": (h, f), "b_fc2": (h,),
+              "ln1_g": (h,), "ln1_b": (h,), "ln2_g": (h,), "ln2_b": (h,)}
+    saved = torch.empty(max(saved_b, 16), dtype=torch.uint8, device=device)
+    ws = torch.empty(max(ws_b, 256), dtype=torch.uint8, device=device)
+    grads = {k: torch.empty(v, dtype=torch.float32, device=device) for k, v in shapes.items()}
+    return saved, ws, grads
+
+
+def saved_views(desc: LayerDesc, saved):
+    """Typed views of the saved activations inside `saved` (for inspection)."""
+    import torch
+    lay = layer_saved_layout(desc)
+    n, h, f = desc.batch * desc.seq, desc.h, desc.ffn
+    dt = torch_dtype(desc)
+    esz = 2 if desc.dtype == BF16 else 4
+
+    def view(name, shape, dtype, elsize):
+        cnt = 1
+        for s in shape:
+            cnt *= s
+        off = lay[name]
+        return saved[off:off + cnt * elsize].view(dtype).view(*shape)
+
+    return {
+        "mu1": view("mu1", (n,), torch.float32, 4), "rstd1": view("rstd1", (n,), torch.float32, 4),
+        "u1": view("u1", (n, h), dt, esz), "qkv": view("qkv", (n, 3 * h), dt, esz),
+        "ctx": view("ctx", (n, h), dt, esz),
+        "lse": view("lse", (desc.batch, desc.heads, desc.seq), torch.float32, 4),
+        "x1": view("x1", (n, h), dt, esz), "mu2": view("mu2", (n,), torch.float32, 4),
+        "rstd2": view("rstd2", (n,), torch.float32, 4), "u2": view("u2", (n, h), dt, esz),
+        "z": view("z", (n, f), dt, esz), "a": view("a", (n, f), dt, esz),
+    }

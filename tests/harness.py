@@ -1,0 +1,95 @@
+"""Test helpers: run one layer through the C ABI and through the oracle.
+
+Both sides are fed the same seeded inputs from `synthetic`; nothing computed on
+the GPU ever reaches the oracle.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+import synthetic
+
+# Tolerances on max|gpu - ref| / max|ref| per tensor.
+TOL = {
+    "f32": {"fwd": 1e-5, "bwd": 1e-5},
+    "bf16": {"fwd": 1.5e-2, "bwd": 3e-2},
+}
+
+
+def rel_err(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    m = float(np.max(np.abs(b))) if b.size else 0.0
+    d = float(np.max(np.abs(a - b))) if b.size else 0.0
+    return d / m if m > 0 else d
+
+
+def to_device(arr, dtype):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(arr, dtype=np.float32))
+    return t.to(dtype=torch.bfloat16 if dtype == "bf16" else torch.float32).cuda()
+
+
+def to_np(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def run_gpu(shape, x, p, dy, t, runs=1, want_saved=True):
+    """Forward + backward through the C ABI.  Returns a dict of float64 arrays."""
+    import torch
+    from tensor_model_transformer_gb300 import mtl
+    b = x.shape[0]
+    desc = mtl.layer_desc(shape.h, shape.heads, shape.seq, b, shape.ffn, t, shape.dtype)
+    dev_p = {k: to_device(v, shape.dtype) for k, v in p.items()}
+    xd = to_device(x, shape.dtype)
+    dyd = to_device(dy, shape.dtype)
+    saved, ws, grads = mtl.alloc_layer_buffers(desc)
+    y = torch.empty_like(xd)
+    dx = torch.empty_like(xd)
+    outs = []
+    for _ in range(runs):
+        mtl.layer_fwd(desc, dev_p, xd, y, saved, ws)
+        mtl.layer_check(ws)
+        mtl.layer_bwd(desc, dev_p, xd, saved, dyd, dx, grads, ws)
+        mtl.layer_check(ws)
+        torch.cuda.synchronize()
+        out = {"y": to_np(y), "dx": to_np(dx)}
+        out.update({"d_" + k: to_np(v) for k, v in grads.items()})
+        if want_saved:
+            sv = mtl.saved_views(desc, saved)
+            out.update({"s_" + k: to_np(v) for k, v in sv.items()})
+        outs.append(out)
+    return outs if runs > 1 else outs[0]
+
+
+def run_oracle(shape, x, p, dy):
+    """The oracle's outputs and intermediates, keyed like run_gpu."""
+    y, cache = oracle.layer_fwd(p, x, shape.heads)
+    dx, g, _ = oracle.layer_bwd(p, cache, dy)
+    out = {"y": y, "dx": dx}
+    out.update({"d_" + k: v for k, v in g.items()})
+    for k in ("u1", "qkv", "ctx", "lse", "x1", "u2", "z", "a", "mu1", "rstd1", "mu2", "rstd2"):
+        out["s_" + k] = cache[k]
+    return out
+
+
+def compare(gpu, ref, dtype, keys=None):
+    """{key: rel_err} for the outputs present in both."""
+    keys = keys or [k for k in ref if k in gpu]
+    res = {}
+    for k in keys:
+        g = gpu[k].reshape(ref[k].shape)
+        res[k] = rel_err(g, ref[k])
+    return res
+
+
+def tolerance(key, dtype):
+    tol = TOL[dtype]
+    if key == "y" or key.startswith("s_"):
+        return tol["fwd"]
+    return tol["bwd"]
+
+
+def make(shape, seed=0, affine=False, batch=None):
+    return synthetic.make_layer(shape, seed=seed, affine=affine, batch=batch)

@@ -1,0 +1,168 @@
+"""Host-only checks of the C ABI: the library loads, exports every declared
+symbol, and rejects bad arguments before touching the GPU.  No GPU needed."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def mtl():
+    from tensor_model_transformer_gb300 import build, mtl as m
+    if not os.path.exists(m.LIB_PATH):
+        build.build()
+    m.lib()
+    return m
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "mtl.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mtl_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(mtl):
+    names = declared_functions()
+    assert "mtl_layer_fwd" in names and "mtl_layer_bwd" in names
+    lib = ctypes.CDLL(mtl.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(mtl):
+    for s in range(6):
+        assert mtl.lib().mtl_status_str(s)
+
+
+def good_desc(mtl, **kw):
+    d = dict(h=256, heads=4, seq=128, batch=2, ffn=1024, t=2, dtype="bf16")
+    d.update(kw)
+    return mtl.layer_desc(**d)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(h=0), 1), (dict(heads=0), 1), (dict(seq=0), 1), (dict(t=0), 1),
+    (dict(h=250), 1),                     # heads does not divide h
+    (dict(t=3), 1),                       # t does not divide heads
+    (dict(ffn=1000, t=8), 1),             # t does not divide ffn
+    (dict(h=128, heads=4), 2),            # d = 32 unsupported
+    (dict(seq=100), 2),                   # bf16 needs seq % 128 == 0
+    (dict(h=384, heads=4, ffn=1536, t=4), 2),  # h/t = 96 not a multiple of 64
+    (dict(dtype=7), 1),
+])
+def test_layer_sizes_rejects(mtl, kw, status):
+    if "dtype" in kw and kw["dtype"] == 7:
+        d = good_desc(mtl)
+        d.dtype = 7
+    else:
+        d = good_desc(mtl, **kw)
+    s, w = ctypes.c_size_t(), ctypes.c_size_t()
+    assert mtl.lib().mtl_layer_sizes(ctypes.byref(d), ctypes.byref(s), ctypes.byref(w)) == status
+
+
+def test_causal_required(mtl):
+    d = good_desc(mtl)
+    d.causal = 0
+    assert mtl.lib().mtl_layer_sizes(ctypes.byref(d), None, None) == 2
+
+
+def test_fp32_path_accepts_small_shapes(mtl):
+    d = good_desc(mtl, dtype="f32", seq=100, h=192, heads=3, ffn=300, t=3)
+    saved, ws = mtl.layer_sizes(d)
+    assert saved > 0 and ws > 0
+
+
+def test_saved_layout_is_aligned_and_sized(mtl):
+    d = good_desc(mtl)
+    lay = mtl.layer_saved_layout(d)
+    n, h, f = 256, 256, 1024
+    assert all(v % 256 == 0 for v in lay.values())
+    assert lay["qkv"] - lay["u1"] >= n * h * 2
+    assert lay["a"] - lay["z"] >= n * f * 2
+    assert lay["total"] >= lay["a"] + n * f * 2
+    assert lay["total"] == mtl.layer_sizes(d)[0]
+
+
+FAKE = 0x10000  # an aligned, never dereferenced host-side stand-in
+
+
+def _weights(mtl, base=FAKE):
+    return mtl.Weights(*[base + 256 * i for i in range(12)])
+
+
+def _grads(mtl, base=FAKE):
+    return mtl.Grads(*[base + 256 * i for i in range(12)])
+
+
+def test_fwd_rejects_null_and_misaligned_pointers(mtl):
+    d = good_desc(mtl)
+    _, ws_b = mtl.layer_sizes(d)
+    w = _weights(mtl)
+    L = mtl.lib()
+    ok = (FAKE, FAKE + 4096, FAKE + 8192, FAKE + 12288)
+    assert L.mtl_layer_fwd(ctypes.byref(d), ctypes.byref(w), None, ok[1], ok[2], ok[3], ws_b, None) == 1
+    assert L.mtl_layer_fwd(ctypes.byref(d), ctypes.byref(w), ok[0] + 8, ok[1], ok[2], ok[3], ws_b,
+                           None) == 1
+    assert L.mtl_layer_fwd(ctypes.byref(d), None, ok[0], ok[1], ok[2], ok[3], ws_b, None) == 1
+    w.b_o = None
+    assert L.mtl_layer_fwd(ctypes.byref(d), ctypes.byref(w), *ok, ws_b, None) == 1
+    # y aliasing x
+    w = _weights(mtl)
+    assert L.mtl_layer_fwd(ctypes.byref(d), ctypes.byref(w), ok[0], ok[0], ok[2], ok[3], ws_b,
+                           None) == 1
+
+
+def test_fwd_and_bwd_reject_small_workspace(mtl):
+    d = good_desc(mtl)
+    _, ws_b = mtl.layer_sizes(d)
+    w, g = _weights(mtl), _grads(mtl)
+    L = mtl.lib()
+    assert L.mtl_layer_fwd(ctypes.byref(d), ctypes.byref(w), FAKE, FAKE + 4096, FAKE + 8192,
+                           FAKE + 12288, ws_b - 1, None) == 3
+    assert L.mtl_layer_bwd(ctypes.byref(d), ctypes.byref(w), FAKE, FAKE + 4096, FAKE + 8192,
+                           FAKE + 12288, ctypes.byref(g), FAKE + 16384, ws_b - 1, None) == 3
+
+
+def test_bwd_rejects_null_grad(mtl):
+    d = good_desc(mtl)
+    _, ws_b = mtl.layer_sizes(d)
+    w, g = _weights(mtl), _grads(mtl)
+    g.ln2_b = None
+    assert mtl.lib().mtl_layer_bwd(ctypes.byref(d), ctypes.byref(w), FAKE, FAKE + 4096,
+                                   FAKE + 8192, FAKE + 12288, ctypes.byref(g), FAKE + 16384,
+                                   ws_b, None) == 1
+
+
+def test_gemm_rejects_bad_arguments(mtl):
+    L = mtl.lib()
+    args = dict(dtype=1, M=128, N=128, K=128, parts=1, A=FAKE, lda=128, ak=1, B=FAKE, ldb=128,
+                bk=1, epi=0, bias=None, R=None, ldr=0, Z=None, ldz=0, C=FAKE, ldc=128, cf=1,
+                ws=FAKE, wsb=256)
+
+    def call(**kw):
+        a = dict(args)
+        a.update(kw)
+        return L.mtl_gemm(a["dtype"], a["M"], a["N"], a["K"], a["parts"], a["A"], a["lda"],
+                          a["ak"], a["B"], a["ldb"], a["bk"], a["epi"], a["bias"], a["R"],
+                          a["ldr"], a["Z"], a["ldz"], a["C"], a["ldc"], a["cf"], a["ws"],
+                          a["wsb"], None)
+
+    assert call(parts=3) == 1                  # parts must divide K
+    assert call(epi=9) == 1
+    assert call(epi=1) == 1                    # bias missing
+    assert call(A=FAKE + 2) == 1               # misaligned
+    assert call(wsb=16) == 3
+    assert call(lda=64) == 1                   # lda < K
+    assert call(ldc=8) == 1
+    assert call(parts=2, K=192, lda=192, ldb=192) == 2  # bf16: K/parts must be a multiple of 64
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    from tensor_model_transformer_gb300 import mtl as m
+    monkeypatch.setattr(m, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(m, "_lib", None)
+    with pytest.raises(RuntimeError):
+        m.lib()

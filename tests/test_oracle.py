@@ -381,3 +381,30 @@ def test_flop_count():
     assert oracle.layer_flops(3072, 32, 1024, 16) == 3 * (24 * 16384 * 3072 ** 2
                                                          + 2 * 16 * 1024 * 1025 * 3072)
     assert abs(oracle.layer_flops(3072, 32, 1024, 16) - 1.144e13) / 1.144e13 < 1e-3
+
+
+# ---------------------------------------------------------------- the GEMM unit
+
+def test_gemm_partitioned_pins():
+    rng = np.random.default_rng(12)
+    A = rng.standard_normal((7, 12))
+    B = rng.standard_normal((5, 12))
+    full = oracle.gemm_partitioned(A, B, 1)
+    # identity operand: A I^T = A
+    assert np.array_equal(oracle.gemm_partitioned(A, np.eye(12), 3), A)
+    # the split identity: any number of parts sums to the same product
+    for parts in (2, 3, 4, 6, 12):
+        assert rel_err(oracle.gemm_partitioned(A, B, parts), full) < 1e-14
+    # entry (i, j) is the dot product of row i of A with row j of B (not a transpose)
+    assert abs(full[3, 2] - sum(A[3, k] * B[2, k] for k in range(12))) < 1e-12
+    bias = rng.standard_normal(5)
+    R = rng.standard_normal((7, 5))
+    assert rel_err(oracle.gemm_partitioned(A, B, 2, 1, bias=bias), full + bias) < 1e-14
+    assert rel_err(oracle.gemm_partitioned(A, B, 2, 2, bias=bias, R=R), full + bias + R) < 1e-14
+    c, z = oracle.gemm_partitioned(A, B, 3, 3, bias=bias)
+    assert rel_err(z, full + bias) < 1e-14
+    assert np.max(np.abs(c - z * oracle.gelu_grad(0 * z) * 0 - oracle.gelu(z))) == 0.0
+    c4 = oracle.gemm_partitioned(A, B, 4, 4, Z=R)
+    assert rel_err(c4, full * oracle.gelu_grad(R)) < 1e-14
+    with pytest.raises(ValueError):
+        oracle.gemm_partitioned(A, B, 5)
