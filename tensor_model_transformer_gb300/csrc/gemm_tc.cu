@@ -12,12 +12,17 @@
 // GEMMs (QKV, fc1) have no reduction; their bias / GeLU ride the epilogue
 // (section "Fused Transformer Kernels").
 //
-// Kernel shape: persistent, one 320-thread CTA per SM, 128x256 output tile,
+// Kernel shape: persistent, one 384-thread CTA per SM, 128x256 output tile,
 // K blocks of 64 in a 4-stage TMA ring (48 KB per stage, 128-byte swizzle).
-//   warp 0      TMA producer (one thread)
-//   warp 1      TMEM allocator and MMA issuer (one thread)
-//   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4).., columns
-//               128*((w-2)/4).. of the tile
+//   warp 0       TMA producer (one thread)
+//   warp 1       TMEM allocator and MMA issuer (one thread)
+//   warps 2..3   idle
+//   warps 4..11  epilogue: warp w reads TMEM lanes 32*(w%4).., columns
+//                128*((w-4)/4).. of the tile
+// Registers: the launch gives 168 per thread; the producer warpgroup (warps
+// 0..3) drops to 40 and the two epilogue warpgroups rise to 232, which holds
+// the 128 fp32 running partition sums per thread (40*128 + 232*256 = 168*384).
+// The host launches the kernel only if it was compiled to exactly 168.
 // TMEM holds two 128x256 fp32 accumulators (all 512 columns) so the epilogue
 // of one work unit overlaps the MMAs of the next.  A work unit is one
 // partition of one tile.  Operands may be K-major or MN-major (the backward's
@@ -37,7 +42,10 @@ constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int EPI_WARPS = 8;
-constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int THREADS = 128 + 32 * EPI_WARPS;
+constexpr int LAUNCH_REGS = 168, PRODUCER_REGS = 40, EPILOGUE_REGS = 232;
+static_assert(PRODUCER_REGS * 128 + EPILOGUE_REGS * 32 * EPI_WARPS == LAUNCH_REGS * THREADS,
+              "register split must add up to the launch total");
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int BAR_BYTES = 256;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
@@ -156,8 +164,72 @@ __device__ __forceinline__ void epi_chunk(const Params& p, int row, int col0, fl
   }
 }
 
+// Epilogue warps 4..11: wait for an accumulator, read it from TMEM (32 columns
+// at a time), add partition partials in order, apply the epilogue, store.
 template <int EPI, bool OUT_F32, bool REDUCE>
-__global__ void __maxnreg__(200)
+__device__ __forceinline__ void epilogue_role(const Params& p, uint32_t tmem_base, uint32_t bar0,
+                                              volatile int* abort_flag, int warp, int lane) {
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const int ew = warp - 4;
+  const int quarter = warp & 3;
+  const int chalf = ew >> 2;
+  int unit = 0;
+  bool ok = true;
+  for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+    int mb, nb;
+    tile_coords(p, tile, mb, nb);
+    const int row = mb * BM + quarter * 32 + lane;
+    const int colbase = nb * BN + chalf * 128;
+    float sum[REDUCE ? 128 : 1];
+    for (int u = 0; u < p.units_per_tile; ++u, ++unit) {
+      const int buf = unit & 1;
+      const uint32_t uphase = (unit >> 1) & 1;
+      if (!mbar_wait_bounded(tfull_bar(buf), uphase, p.status, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tb = tmem_base + buf * BN + chalf * 128 + ((uint32_t)(quarter * 32) << 16);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tb + c * 32, r);
+        tmem_ld_wait();
+        if constexpr (REDUCE) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float x = __uint_as_float(r[i]);
+            sum[c * 32 + i] = (u == 0) ? x : sum[c * 32 + i] + x;
+          }
+        } else {
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+          epi_chunk<EPI, OUT_F32>(p, row, colbase + c * 32, v);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(buf));
+    }
+    if constexpr (REDUCE) {
+      if (ok) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = sum[c * 32 + i];
+          epi_chunk<EPI, OUT_F32>(p, row, colbase + c * 32, v);
+        }
+      }
+    }
+  }
+  __syncwarp();
+}
+
+template <int EPI, bool OUT_F32, bool REDUCE>
+__global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -199,7 +271,15 @@ __global__ void __maxnreg__(200)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PRODUCER_REGS));
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(EPILOGUE_REGS));
+  }
+
+  if (warp >= 4) {
+    epilogue_role<EPI, OUT_F32, REDUCE>(p, tmem_base, bar0, abort_flag, warp, lane);
+  } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int stage = 0;
@@ -282,63 +362,6 @@ __global__ void __maxnreg__(200)
             }
           }
           if (ok) tc_commit(tfull_bar(buf));
-        }
-      }
-    }
-    __syncwarp();
-  } else {
-    // ------------------------------------------------------------ epilogue
-    const int ew = warp - 2;
-    const int quarter = warp & 3;
-    const int chalf = ew >> 2;
-    int unit = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
-      int mb, nb;
-      tile_coords(p, tile, mb, nb);
-      const int row = mb * BM + quarter * 32 + lane;
-      const int colbase = nb * BN + chalf * 128;
-      float sum[REDUCE ? 128 : 1];
-      for (int u = 0; u < p.units_per_tile; ++u, ++unit) {
-        const int buf = unit & 1;
-        const uint32_t uphase = (unit >> 1) & 1;
-        if (!mbar_wait_bounded(tfull_bar(buf), uphase, p.status, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t tb = tmem_base + buf * BN + chalf * 128 + ((uint32_t)(quarter * 32) << 16);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tb + c * 32, r);
-          tmem_ld_wait();
-          if constexpr (REDUCE) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float x = __uint_as_float(r[i]);
-              sum[c * 32 + i] = (u == 0) ? x : sum[c * 32 + i] + x;
-            }
-          } else {
-            float v[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-            epi_chunk<EPI, OUT_F32>(p, row, colbase + c * 32, v);
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tempty_bar(buf));
-      }
-      if constexpr (REDUCE) {
-        if (ok) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float v[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = sum[c * 32 + i];
-            epi_chunk<EPI, OUT_F32>(p, row, colbase + c * 32, v);
-          }
         }
       }
     }
@@ -476,6 +499,12 @@ cudaError_t gemm_tc(const GemmArgs& a, const LaunchCtx& c) {
   cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  // The warpgroup register split assumes exactly LAUNCH_REGS registers per
+  // thread at launch; with fewer, setmaxnreg.inc could never be satisfied.
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(fn));
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != LAUNCH_REGS) return cudaErrorInvalidConfiguration;
   if (p.kb_per_unit == 0) {
     // K == 0: nothing to accumulate; the kernel is not launched
     return cudaErrorInvalidValue;
