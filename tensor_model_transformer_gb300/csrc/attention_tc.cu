@@ -1,0 +1,800 @@
+// Causal flash attention on tcgen05 tensor cores (bf16 in, fp32 accumulate),
+// forward and a deterministic two-kernel backward.
+//
+// Each head is local to its partition: Q, K and V of head `hd` are the three
+// d-wide column blocks at hd*3d of the head-interleaved qkv activation ("Megatron-
+// LM: GPU-Cluster Training Parallelism", section "Paper 1: QKV Column-Parallel
+// Splitting in Detail"), so the kernels read them straight from qkv with TMA
+// boxes -- no transpose kernel (section "Fused Transformer Kernels": layout
+// change instead of transposes, fused scale-mask-softmax).
+//
+//   S = Q K^T / sqrt(d), keys after the query excluded, P = softmax(S), O = P V,
+//   lse = log sum exp(S) per query row.
+//   Backward: D_i = sum_c dO_ic O_ic;  dS = P * (dO V^T - D);  dQ = dS K / sqrt d;
+//   dK = dS^T Q / sqrt d;  dV = P^T dO.
+//
+// All three kernels: one CTA per 128-row block, 192 threads:
+//   warp 0      TMA producer
+//   warp 1      TMEM allocator, MMA issuer
+//   warps 2..5  row threads: thread (warp%4)*32+lane owns TMEM lane = one row of
+//               the block, so row maxima and sums need no cross-thread reduction.
+// Operand tiles are [atoms][rows][64] 128-byte-swizzled boxes straight from TMA;
+// the same box serves as a K-major operand (rows = M/N) or an MN-major one
+// (rows = K), e.g. dO is the K-major B of dO V^T and the MN-major B of P^T dO.
+// P and dS go from registers to shared memory in the same swizzled layout.
+// Every wait is bounded; a timeout is recorded in the status word.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mtl {
+namespace attn {
+
+constexpr int THREADS = 192;
+constexpr int ATOM128 = 128 * 128;   // [128 rows][64 bf16]
+constexpr int ATOM64 = 64 * 128;     // [64 rows][64 bf16]
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+
+struct Params {
+  int batch, seq, heads, d, h, nqb;
+  float scale_log2;   // log2(e) / sqrt(d)
+  float scale;        // 1 / sqrt(d)
+  bf16* ctx;          // fwd out / bwd in (O)
+  float* lse;
+  const bf16* dctx;   // dO
+  bf16* dqkv;
+  float* dsum;
+  unsigned* status;
+};
+
+struct Smem {
+  uint8_t* base;
+  uint32_t u32;
+};
+
+__device__ __forceinline__ Smem smem_aligned(uint8_t* raw) {
+  uint8_t* p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) &
+                                          ~static_cast<uintptr_t>(1023));
+  return {p, smem_u32(p)};
+}
+
+// Block index -> (row block, head, batch); `heavy_first_desc` puts the row
+// blocks with the most causal work first.
+__device__ __forceinline__ void block_coords(const Params& p, int nblk, bool desc, int& blk,
+                                             int& hd, int& b) {
+  const int hb = p.heads * p.batch;
+  const int i = blockIdx.x / hb;
+  blk = desc ? (nblk - 1 - i) : i;
+  const int r = blockIdx.x % hb;
+  hd = r % p.heads;
+  b = r / p.heads;
+}
+
+// ============================================================================ forward
+// Per CTA: 128 queries; K/V blocks of 128 keys, double-buffered.
+// smem: Q, K[2], V[2] (NA atoms of 16 KB each), P (2 atoms).  TMEM: S cols
+// 0..127, O cols 128..128+d.
+template <int NA>
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const Smem sm = smem_aligned(smem_raw);
+  constexpr uint32_t TILE = NA * ATOM128;
+  const uint32_t sQ = sm.u32, sK0 = sQ + TILE, sV0 = sQ + 3 * TILE, sP = sQ + 5 * TILE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm.base + 5 * TILE + 2 * ATOM128);
+  const uint32_t bar0 = smem_u32(bars);
+  // 0 q_full, 1-2 k_full, 3-4 k_empty, 5-6 v_full, 7-8 v_empty, 9 s_full, 10 p_full, 11 o_done
+  auto B = [&](int i) { return bar0 + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  int qb, hd, b;
+  block_coords(p, p.nqb, true, qb, hd, b);
+  const int nkv = qb + 1;
+  const int row0 = b * p.seq + qb * 128;
+  const int colq = hd * 3 * p.d;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 12; ++i) mbar_init(B(i), i == 10 ? 128 : 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_shared();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem, tO = tmem + 128;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm);
+      mbar_arrive_expect_tx(B(0), TILE);
+      for (int a = 0; a < NA; ++a) tma_load_2d(sQ + a * ATOM128, &tm, B(0), colq + 64 * a, row0);
+      for (int j = 0; j < nkv; ++j) {
+        const int s = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        const int krow = b * p.seq + j * 128;
+        if (!mbar_wait_bounded(B(3 + s), ph ^ 1u, p.status, abort_flag)) break;
+        mbar_arrive_expect_tx(B(1 + s), TILE);
+        for (int a = 0; a < NA; ++a)
+          tma_load_2d(sK0 + s * TILE + a * ATOM128, &tm, B(1 + s), colq + p.d + 64 * a, krow);
+        if (!mbar_wait_bounded(B(7 + s), ph ^ 1u, p.status, abort_flag)) break;
+        mbar_arrive_expect_tx(B(5 + s), TILE);
+        for (int a = 0; a < NA; ++a)
+          tma_load_2d(sV0 + s * TILE + a * ATOM128, &tm, B(5 + s), colq + 2 * p.d + 64 * a, krow);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);
+      const uint32_t id_pv = idesc_bf16_f32(128, p.d, false, true);
+      const int ksteps = p.d / 16;
+      bool ok = mbar_wait_bounded(B(0), 0, p.status, abort_flag) &&
+                mbar_wait_bounded(B(1), 0, p.status, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        for (int kk = 0; kk < ksteps; ++kk)
+          tc_mma_bf16(tS, desc_kmajor(sQ, ATOM128, kk), desc_kmajor(sK0, ATOM128, kk), id_qk,
+                      kk > 0);
+        tc_commit(B(3));
+        tc_commit(B(9));
+      }
+      for (int j = 0; j < nkv && ok; ++j) {
+        if (!mbar_wait_bounded(B(10), j & 1, p.status, abort_flag)) break;
+        tc_fence_after();
+        if (j + 1 < nkv) {
+          const int s1 = (j + 1) & 1;
+          if (!mbar_wait_bounded(B(1 + s1), ((j + 1) >> 1) & 1, p.status, abort_flag)) break;
+          tc_fence_after();
+          for (int kk = 0; kk < ksteps; ++kk)
+            tc_mma_bf16(tS, desc_kmajor(sQ, ATOM128, kk), desc_kmajor(sK0 + s1 * TILE, ATOM128, kk),
+                        id_qk, kk > 0);
+          tc_commit(B(3 + s1));
+          tc_commit(B(9));
+        }
+        const int s = j & 1;
+        if (!mbar_wait_bounded(B(5 + s), (j >> 1) & 1, p.status, abort_flag)) break;
+        tc_fence_after();
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma_bf16(tO, desc_kmajor(sP, ATOM128, kk), desc_mnmajor(sV0 + s * TILE, ATOM128, kk),
+                      id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(B(7 + s));
+        tc_commit(B(11));
+      }
+    }
+    __syncwarp();
+  } else {
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;                       // row in the block = TMEM lane
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      if (!mbar_wait_bounded(B(9), j & 1, p.status, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tS + lane_off + c * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]) * p.scale_log2;
+      }
+      if (j == qb) {
+#pragma unroll
+        for (int k = 0; k < 128; ++k)
+          if (k > r) s[k] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int k = 1; k < 128; ++k) mx = fmaxf(mx, s[k]);
+      const float m_new = fmaxf(m_used, mx);
+      // Rescale only when the running maximum grew by more than 2^8: the
+      // exponentials stay below 256 and the final O / l is exact either way.
+      const bool resc = m_new > m_used + 8.0f;
+      const float alpha = resc ? fast_exp2(m_used - m_new) : 1.0f;
+      if (resc) m_used = m_new;
+      float rs = 0.f;
+#pragma unroll
+      for (int k = 0; k < 128; ++k) {
+        s[k] = fast_exp2(s[k] - m_used);
+        rs += s[k];
+      }
+      l = l * alpha + rs;
+      if (j > 0) {
+        if (!mbar_wait_bounded(B(11), (j - 1) & 1, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, resc)) {
+          for (int c = 0; c < p.d; c += 32) {
+            uint32_t v[32];
+            tmem_ld32(tO + lane_off + c, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            tmem_st32(tO + lane_off + c, v);
+          }
+          tmem_st_wait();
+        }
+      }
+      // P (bf16) -> shared memory, two 64-key boxes
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int k = c * 8;
+        const uint32_t addr = sP + (c >> 3) * ATOM128 + sw128_offset(r, c & 7);
+        st_shared_v4(addr, pack_bf16x2(s[k], s[k + 1]), pack_bf16x2(s[k + 2], s[k + 3]),
+                     pack_bf16x2(s[k + 4], s[k + 5]), pack_bf16x2(s[k + 6], s[k + 7]));
+      }
+      fence_proxy_async_shared();
+      tc_fence_before();
+      mbar_arrive(B(10));
+    }
+    if (ok && mbar_wait_bounded(B(11), (nkv - 1) & 1, p.status, abort_flag)) {
+      tc_fence_after();
+      const float inv = 1.0f / l;
+      bf16* orow = p.ctx + (size_t)(row0 + r) * p.h + (size_t)hd * p.d;
+      for (int c = 0; c < p.d; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(tO + lane_off + c, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 u;
+          u.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]) * inv, __uint_as_float(v[q * 8 + 1]) * inv);
+          u.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]) * inv, __uint_as_float(v[q * 8 + 3]) * inv);
+          u.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]) * inv, __uint_as_float(v[q * 8 + 5]) * inv);
+          u.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]) * inv, __uint_as_float(v[q * 8 + 7]) * inv);
+          *reinterpret_cast<uint4*>(orow + c + q * 8) = u;
+        }
+      }
+      p.lse[((size_t)b * p.heads + hd) * p.seq + qb * 128 + r] = (m_used + __log2f(l)) * LN2;
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  if (warp == 1) {
+    if (*abort_flag) {
+      const long long t0 = clock64();
+      while (clock64() - t0 < 2000000LL) {
+      }
+    }
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+// ============================================================================ dQ
+// Per CTA: 128 queries; K/V blocks of 64 keys, double-buffered.  Also writes
+// D_i = sum_c dO_ic O_ic for the dK/dV kernel.
+// smem: Q, dO (NA atoms of 16 KB), K[2], V[2] (NA atoms of 8 KB), dS (1 atom,
+// 16 KB).  TMEM: S cols 0..63, dP 64..127, dQ 128..128+d.
+template <int NA>
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm128,
+                          const __grid_constant__ CUtensorMap tm64,
+                          const __grid_constant__ CUtensorMap tmdo128, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const Smem sm = smem_aligned(smem_raw);
+  constexpr uint32_t T128 = NA * ATOM128, T64 = NA * ATOM64;
+  const uint32_t sQ = sm.u32, sDO = sQ + T128, sK0 = sQ + 2 * T128, sV0 = sK0 + 2 * T64,
+                 sDS = sV0 + 2 * T64;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm.base + 2 * T128 + 4 * T64 + ATOM128);
+  const uint32_t bar0 = smem_u32(bars);
+  // 0 q/do full, 1-2 kv_full, 3-4 kv_empty, 5 s_full, 6 ds_full, 7 dq_done
+  auto B = [&](int i) { return bar0 + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  int qb, hd, b;
+  block_coords(p, p.nqb, true, qb, hd, b);
+  const int nkv = 2 * qb + 2;   // 64-key blocks up to the diagonal
+  const int row0 = b * p.seq + qb * 128;
+  const int colq = hd * 3 * p.d;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 8; ++i) mbar_init(B(i), i == 6 ? 128 : 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_shared();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem, tDP = tmem + 64, tDQ = tmem + 128;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm128);
+      tma_prefetch_desc(&tm64);
+      tma_prefetch_desc(&tmdo128);
+      mbar_arrive_expect_tx(B(0), 2 * T128);
+      for (int a = 0; a < NA; ++a) {
+        tma_load_2d(sQ + a * ATOM128, &tm128, B(0), colq + 64 * a, row0);
+        tma_load_2d(sDO + a * ATOM128, &tmdo128, B(0), hd * p.d + 64 * a, row0);
+      }
+      for (int j = 0; j < nkv; ++j) {
+        const int s = j & 1;
+        const int krow = b * p.seq + j * 64;
+        if (!mbar_wait_bounded(B(3 + s), ((j >> 1) & 1) ^ 1u, p.status, abort_flag)) break;
+        mbar_arrive_expect_tx(B(1 + s), 2 * T64);
+        for (int a = 0; a < NA; ++a) {
+          tma_load_2d(sK0 + s * T64 + a * ATOM64, &tm64, B(1 + s), colq + p.d + 64 * a, krow);
+          tma_load_2d(sV0 + s * T64 + a * ATOM64, &tm64, B(1 + s), colq + 2 * p.d + 64 * a, krow);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16_f32(128, 64, false, false);
+      const uint32_t id_dq = idesc_bf16_f32(128, p.d, false, true);
+      const int ksteps = p.d / 16;
+      auto issue_s = [&](int j) {
+        const int s = j & 1;
+        for (int kk = 0; kk < ksteps; ++kk)
+          tc_mma_bf16(tS, desc_kmajor(sQ, ATOM128, kk), desc_kmajor(sK0 + s * T64, ATOM64, kk),
+                      id_s, kk > 0);
+        for (int kk = 0; kk < ksteps; ++kk)
+          tc_mma_bf16(tDP, desc_kmajor(sDO, ATOM128, kk), desc_kmajor(sV0 + s * T64, ATOM64, kk),
+                      id_s, kk > 0);
+        tc_commit(B(5));
+      };
+      bool ok = mbar_wait_bounded(B(0), 0, p.status, abort_flag) &&
+                mbar_wait_bounded(B(1), 0, p.status, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+      }
+      for (int j = 0; j < nkv && ok; ++j) {
+        if (!mbar_wait_bounded(B(6), j & 1, p.status, abort_flag)) break;
+        tc_fence_after();
+        if (j + 1 < nkv) {
+          if (!mbar_wait_bounded(B(1 + ((j + 1) & 1)), ((j + 1) >> 1) & 1, p.status, abort_flag))
+            break;
+          tc_fence_after();
+          issue_s(j + 1);
+        }
+        const int s = j & 1;
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma_bf16(tDQ, desc_kmajor(sDS, ATOM128, kk), desc_mnmajor(sK0 + s * T64, ATOM64, kk),
+                      id_dq, (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(B(3 + s));
+        tc_commit(B(7));
+      }
+    }
+    __syncwarp();
+  } else {
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    // D_r = dO_r . O_r and the row's lse (log2 units)
+    const size_t orow = (size_t)(row0 + r) * p.h + (size_t)hd * p.d;
+    float Dr = 0.f;
+    for (int c = 0; c < p.d; c += 8) {
+      const uint4 go = *reinterpret_cast<const uint4*>(p.dctx + orow + c);
+      const uint4 oo = *reinterpret_cast<const uint4*>(p.ctx + orow + c);
+      const bf16* g = reinterpret_cast<const bf16*>(&go);
+      const bf16* o = reinterpret_cast<const bf16*>(&oo);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) Dr = fmaf(__bfloat162float(g[e]), __bfloat162float(o[e]), Dr);
+    }
+    const size_t lrow = ((size_t)b * p.heads + hd) * p.seq + qb * 128 + r;
+    p.dsum[lrow] = Dr;
+    const float lse2 = p.lse[lrow] * LOG2E;
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      if (!mbar_wait_bounded(B(5), j & 1, p.status, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float ds[64];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t sv[32], dv[32];
+        tmem_ld32(tS + lane_off + c * 32, sv);
+        tmem_ld32(tDP + lane_off + c * 32, dv);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int key = j * 64 + c * 32 + i;   // key index within the sequence block origin
+          float pr = fast_exp2(__uint_as_float(sv[i]) * p.scale_log2 - lse2);
+          if (key > qb * 128 + r) pr = 0.f;
+          ds[c * 32 + i] = pr * (__uint_as_float(dv[i]) - Dr);
+        }
+      }
+      if (j > 0) {
+        if (!mbar_wait_bounded(B(7), (j - 1) & 1, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int k = c * 8;
+        st_shared_v4(sDS + sw128_offset(r, c), pack_bf16x2(ds[k], ds[k + 1]),
+                     pack_bf16x2(ds[k + 2], ds[k + 3]), pack_bf16x2(ds[k + 4], ds[k + 5]),
+                     pack_bf16x2(ds[k + 6], ds[k + 7]));
+      }
+      fence_proxy_async_shared();
+      tc_fence_before();
+      mbar_arrive(B(6));
+    }
+    if (ok && mbar_wait_bounded(B(7), (nkv - 1) & 1, p.status, abort_flag)) {
+      tc_fence_after();
+      bf16* dq = p.dqkv + (size_t)(row0 + r) * 3 * p.h + colq;
+      for (int c = 0; c < p.d; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(tDQ + lane_off + c, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 u;
+          u.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]) * p.scale, __uint_as_float(v[q * 8 + 1]) * p.scale);
+          u.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]) * p.scale, __uint_as_float(v[q * 8 + 3]) * p.scale);
+          u.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]) * p.scale, __uint_as_float(v[q * 8 + 5]) * p.scale);
+          u.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]) * p.scale, __uint_as_float(v[q * 8 + 7]) * p.scale);
+          *reinterpret_cast<uint4*>(dq + c + q * 8) = u;
+        }
+      }
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  if (warp == 1) {
+    if (*abort_flag) {
+      const long long t0 = clock64();
+      while (clock64() - t0 < 2000000LL) {
+      }
+    }
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+// ============================================================================ dK, dV
+// Per CTA: 128 keys; query blocks of 64 from the diagonal on, double-buffered.
+// smem: K, V (NA atoms of 16 KB), Q[2], dO[2] (NA atoms of 8 KB), P^T and dS^T
+// (1 atom of 16 KB each).  TMEM: S^T cols 0..63, dP^T 64..127, dV 128..255,
+// dK 256..383.
+template <int NA>
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm128,
+                           const __grid_constant__ CUtensorMap tm64,
+                           const __grid_constant__ CUtensorMap tmdo64, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const Smem sm = smem_aligned(smem_raw);
+  constexpr uint32_t T128 = NA * ATOM128, T64 = NA * ATOM64;
+  const uint32_t sK = sm.u32, sV = sK + T128, sQ0 = sK + 2 * T128, sDO0 = sQ0 + 2 * T64,
+                 sPT = sDO0 + 2 * T64, sDST = sPT + ATOM128;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm.base + 2 * T128 + 4 * T64 + 2 * ATOM128);
+  const uint32_t bar0 = smem_u32(bars);
+  // 0 kv_full, 1-2 qdo_full, 3-4 qdo_empty, 5 st_full, 6 pt_full, 7 mm_done
+  auto B = [&](int i) { return bar0 + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  int kb, hd, b;
+  block_coords(p, p.nqb, false, kb, hd, b);
+  const int first = 2 * kb;               // first 64-query block that sees these keys
+  const int nq = 2 * p.nqb - first;
+  const int krow0 = b * p.seq + kb * 128;
+  const int colq = hd * 3 * p.d;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 8; ++i) mbar_init(B(i), i == 6 ? 128 : 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_shared();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tST = tmem, tDPT = tmem + 64, tDV = tmem + 128, tDK = tmem + 256;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm128);
+      tma_prefetch_desc(&tm64);
+      tma_prefetch_desc(&tmdo64);
+      mbar_arrive_expect_tx(B(0), 2 * T128);
+      for (int a = 0; a < NA; ++a) {
+        tma_load_2d(sK + a * ATOM128, &tm128, B(0), colq + p.d + 64 * a, krow0);
+        tma_load_2d(sV + a * ATOM128, &tm128, B(0), colq + 2 * p.d + 64 * a, krow0);
+      }
+      for (int i = 0; i < nq; ++i) {
+        const int s = i & 1;
+        const int qrow = b * p.seq + (first + i) * 64;
+        if (!mbar_wait_bounded(B(3 + s), ((i >> 1) & 1) ^ 1u, p.status, abort_flag)) break;
+        mbar_arrive_expect_tx(B(1 + s), 2 * T64);
+        for (int a = 0; a < NA; ++a) {
+          tma_load_2d(sQ0 + s * T64 + a * ATOM64, &tm64, B(1 + s), colq + 64 * a, qrow);
+          tma_load_2d(sDO0 + s * T64 + a * ATOM64, &tmdo64, B(1 + s), hd * p.d + 64 * a, qrow);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t id_st = idesc_bf16_f32(128, 64, false, false);
+      const uint32_t id_acc = idesc_bf16_f32(128, p.d, false, true);
+      const int ksteps = p.d / 16;
+      auto issue_st = [&](int i) {
+        const int s = i & 1;
+        for (int kk = 0; kk < ksteps; ++kk)
+          tc_mma_bf16(tST, desc_kmajor(sK, ATOM128, kk), desc_kmajor(sQ0 + s * T64, ATOM64, kk),
+                      id_st, kk > 0);
+        for (int kk = 0; kk < ksteps; ++kk)
+          tc_mma_bf16(tDPT, desc_kmajor(sV, ATOM128, kk), desc_kmajor(sDO0 + s * T64, ATOM64, kk),
+                      id_st, kk > 0);
+        tc_commit(B(5));
+      };
+      bool ok = mbar_wait_bounded(B(0), 0, p.status, abort_flag) &&
+                mbar_wait_bounded(B(1), 0, p.status, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        issue_st(0);
+      }
+      for (int i = 0; i < nq && ok; ++i) {
+        if (!mbar_wait_bounded(B(6), i & 1, p.status, abort_flag)) break;
+        tc_fence_after();
+        if (i + 1 < nq) {
+          if (!mbar_wait_bounded(B(1 + ((i + 1) & 1)), ((i + 1) >> 1) & 1, p.status, abort_flag))
+            break;
+          tc_fence_after();
+          issue_st(i + 1);
+        }
+        const int s = i & 1;
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma_bf16(tDV, desc_kmajor(sPT, ATOM128, kk), desc_mnmajor(sDO0 + s * T64, ATOM64, kk),
+                      id_acc, (i > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma_bf16(tDK, desc_kmajor(sDST, ATOM128, kk), desc_mnmajor(sQ0 + s * T64, ATOM64, kk),
+                      id_acc, (i > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(B(3 + s));
+        tc_commit(B(7));
+      }
+    }
+    __syncwarp();
+  } else {
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;   // key row
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    const int key = kb * 128 + r;
+    const float* lse_bh = p.lse + ((size_t)b * p.heads + hd) * p.seq;
+    const float* d_bh = p.dsum + ((size_t)b * p.heads + hd) * p.seq;
+    bool ok = true;
+    for (int i = 0; i < nq; ++i) {
+      if (!mbar_wait_bounded(B(5), i & 1, p.status, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int q0 = (first + i) * 64;
+      float pt[64], dst[64];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t sv[32], dv[32];
+        tmem_ld32(tST + lane_off + c * 32, sv);
+        tmem_ld32(tDPT + lane_off + c * 32, dv);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int q = q0 + c * 32 + e;
+          float pr = fast_exp2(__uint_as_float(sv[e]) * p.scale_log2 - __ldg(lse_bh + q) * LOG2E);
+          if (q < key) pr = 0.f;
+          pt[c * 32 + e] = pr;
+          dst[c * 32 + e] = pr * (__uint_as_float(dv[e]) - __ldg(d_bh + q));
+        }
+      }
+      if (i > 0) {
+        if (!mbar_wait_bounded(B(7), (i - 1) & 1, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int k = c * 8;
+        st_shared_v4(sPT + sw128_offset(r, c), pack_bf16x2(pt[k], pt[k + 1]),
+                     pack_bf16x2(pt[k + 2], pt[k + 3]), pack_bf16x2(pt[k + 4], pt[k + 5]),
+                     pack_bf16x2(pt[k + 6], pt[k + 7]));
+        st_shared_v4(sDST + sw128_offset(r, c), pack_bf16x2(dst[k], dst[k + 1]),
+                     pack_bf16x2(dst[k + 2], dst[k + 3]), pack_bf16x2(dst[k + 4], dst[k + 5]),
+                     pack_bf16x2(dst[k + 6], dst[k + 7]));
+      }
+      fence_proxy_async_shared();
+      tc_fence_before();
+      mbar_arrive(B(6));
+    }
+    if (ok && mbar_wait_bounded(B(7), (nq - 1) & 1, p.status, abort_flag)) {
+      tc_fence_after();
+      bf16* out = p.dqkv + (size_t)(krow0 + r) * 3 * p.h + colq;
+      for (int which = 0; which < 2; ++which) {   // 0: dK (scaled), 1: dV
+        const uint32_t tsrc = which == 0 ? tDK : tDV;
+        const float sc = which == 0 ? p.scale : 1.0f;
+        bf16* dst_row = out + (which == 0 ? p.d : 2 * p.d);
+        for (int c = 0; c < p.d; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(tsrc + lane_off + c, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 u;
+            u.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]) * sc, __uint_as_float(v[q * 8 + 1]) * sc);
+            u.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]) * sc, __uint_as_float(v[q * 8 + 3]) * sc);
+            u.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]) * sc, __uint_as_float(v[q * 8 + 5]) * sc);
+            u.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]) * sc, __uint_as_float(v[q * 8 + 7]) * sc);
+            *reinterpret_cast<uint4*>(dst_row + c + q * 8) = u;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  if (warp == 1) {
+    if (*abort_flag) {
+      const long long t0 = clock64();
+      while (clock64() - t0 < 2000000LL) {
+      }
+    }
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  static EncodeTiledFn enc = nullptr;
+  if (!enc) {
+    void* fp = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fp, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return false;
+    enc = reinterpret_cast<EncodeTiledFn>(fp);
+  }
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t fwd_smem(int na) { return (size_t)5 * na * ATOM128 + 2 * ATOM128 + 256 + 1024; }
+size_t dq_smem(int na) { return (size_t)2 * na * ATOM128 + 4 * na * ATOM64 + ATOM128 + 256 + 1024; }
+// The dK/dV kernel holds all 512 TMEM columns: its shared memory request keeps
+// it at one CTA per SM so a second CTA never waits in tcgen05.alloc.
+size_t dkv_smem(int na) {
+  const size_t need = (size_t)2 * na * ATOM128 + 4 * na * ATOM64 + 2 * ATOM128 + 256 + 1024;
+  return need < 120 * 1024 ? 120 * 1024 : need;
+}
+
+Params make_params(int batch, int seq, int heads, int d, unsigned* status) {
+  Params p;
+  p.batch = batch;
+  p.seq = seq;
+  p.heads = heads;
+  p.d = d;
+  p.h = heads * d;
+  p.nqb = seq / 128;
+  p.scale = 1.0f / sqrtf((float)d);
+  p.scale_log2 = LOG2E * p.scale;
+  p.ctx = nullptr;
+  p.lse = nullptr;
+  p.dctx = nullptr;
+  p.dqkv = nullptr;
+  p.dsum = nullptr;
+  p.status = status;
+  return p;
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, size_t bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+}  // namespace attn
+
+bool attn_tc_supported(int seq, int d) { return seq % 128 == 0 && (d == 64 || d == 96 || d == 128); }
+
+cudaError_t attn_fwd_tc(const void* qkv, void* ctx, float* lse, int batch, int seq, int heads,
+                        int d, unsigned* status, const LaunchCtx& c) {
+  using namespace attn;
+  if (batch == 0) return cudaSuccess;
+  if (!attn_tc_supported(seq, d)) return cudaErrorInvalidValue;
+  CUtensorMap tm;
+  if (!make_map(&tm, qkv, 3ull * heads * d, (uint64_t)batch * seq, 128)) return cudaErrorInvalidValue;
+  Params p = make_params(batch, seq, heads, d, status);
+  p.ctx = static_cast<bf16*>(ctx);
+  p.lse = lse;
+  const int grid = p.nqb * heads * batch;
+  const double flops = 2.0 * 2.0 * batch * heads * d * ((double)seq * (seq + 1) / 2.0);
+  cudaError_t e;
+  if (d == 64) {
+    const size_t sm = fwd_smem(1);
+    if ((e = set_smem(attn_fwd_tc_kernel<1>, sm)) != cudaSuccess) return e;
+    c.before(KK_ATTN_FWD, flops);
+    attn_fwd_tc_kernel<1><<<grid, THREADS, sm, c.stream>>>(tm, p);
+  } else {
+    const size_t sm = fwd_smem(2);
+    if ((e = set_smem(attn_fwd_tc_kernel<2>, sm)) != cudaSuccess) return e;
+    c.before(KK_ATTN_FWD, flops);
+    attn_fwd_tc_kernel<2><<<grid, THREADS, sm, c.stream>>>(tm, p);
+  }
+  c.after();
+  return cudaGetLastError();
+}
+
+cudaError_t attn_bwd_tc(const void* qkv, const void* ctx, const float* lse, const void* dctx,
+                        void* dqkv, float* dsum, int batch, int seq, int heads, int d,
+                        unsigned* status, const LaunchCtx& c) {
+  using namespace attn;
+  if (batch == 0) return cudaSuccess;
+  if (!attn_tc_supported(seq, d)) return cudaErrorInvalidValue;
+  const uint64_t n = (uint64_t)batch * seq;
+  CUtensorMap tm128, tm64, tmdo128, tmdo64;
+  if (!make_map(&tm128, qkv, 3ull * heads * d, n, 128) || !make_map(&tm64, qkv, 3ull * heads * d, n, 64) ||
+      !make_map(&tmdo128, dctx, (uint64_t)heads * d, n, 128) ||
+      !make_map(&tmdo64, dctx, (uint64_t)heads * d, n, 64))
+    return cudaErrorInvalidValue;
+  Params p = make_params(batch, seq, heads, d, status);
+  p.ctx = static_cast<bf16*>(const_cast<void*>(ctx));
+  p.lse = const_cast<float*>(lse);
+  p.dctx = static_cast<const bf16*>(dctx);
+  p.dqkv = static_cast<bf16*>(dqkv);
+  p.dsum = dsum;
+  const int grid = p.nqb * heads * batch;
+  const double tri = (double)batch * heads * d * ((double)seq * (seq + 1) / 2.0);
+  cudaError_t e;
+  if (d == 64) {
+    if ((e = set_smem(attn_bwd_dq_tc_kernel<1>, dq_smem(1))) != cudaSuccess) return e;
+    if ((e = set_smem(attn_bwd_dkv_tc_kernel<1>, dkv_smem(1))) != cudaSuccess) return e;
+    c.before(KK_ATTN_BWD, 2.0 * 3.0 * tri);
+    attn_bwd_dq_tc_kernel<1><<<grid, THREADS, dq_smem(1), c.stream>>>(tm128, tm64, tmdo128, p);
+    c.after();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    c.before(KK_ATTN_BWD, 2.0 * 4.0 * tri);
+    attn_bwd_dkv_tc_kernel<1><<<grid, THREADS, dkv_smem(1), c.stream>>>(tm128, tm64, tmdo64, p);
+    c.after();
+  } else {
+    if ((e = set_smem(attn_bwd_dq_tc_kernel<2>, dq_smem(2))) != cudaSuccess) return e;
+    if ((e = set_smem(attn_bwd_dkv_tc_kernel<2>, dkv_smem(2))) != cudaSuccess) return e;
+    c.before(KK_ATTN_BWD, 2.0 * 3.0 * tri);
+    attn_bwd_dq_tc_kernel<2><<<grid, THREADS, dq_smem(2), c.stream>>>(tm128, tm64, tmdo128, p);
+    c.after();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    c.before(KK_ATTN_BWD, 2.0 * 4.0 * tri);
+    attn_bwd_dkv_tc_kernel<2><<<grid, THREADS, dkv_smem(2), c.stream>>>(tm128, tm64, tmdo64, p);
+    c.after();
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace mtl

@@ -107,4 +107,14 @@ cudaError_t attn_bwd_simt(int dtype, const void* qkv, const void* ctx, const flo
                           const void* dctx, void* dqkv, float* dsum, int batch, int seq,
                           int heads, int d, const LaunchCtx& c);
 
+// Causal attention on tcgen05 tensor cores (bf16; seq % 128 == 0, d in
+// {64, 96, 128}).  Forward writes ctx and lse; backward writes dqkv and, as
+// scratch, dsum [batch][heads][seq].
+bool attn_tc_supported(int seq, int d);
+cudaError_t attn_fwd_tc(const void* qkv, void* ctx, float* lse, int batch, int seq, int heads,
+                        int d, unsigned* status, const LaunchCtx& c);
+cudaError_t attn_bwd_tc(const void* qkv, const void* ctx, const float* lse, const void* dctx,
+                        void* dqkv, float* dsum, int batch, int seq, int heads, int d,
+                        unsigned* status, const LaunchCtx& c);
+
 }  // namespace mtl

@@ -297,9 +297,15 @@ mtl_status mtl_layer_fwd(const mtl_layer_desc* desc, const mtl_weights* w, const
     MTL_TRY(run_gemm(D, g, c), "qkv gemm");
   }
   // F3 attention per head
-  MTL_TRY(attn_fwd_simt(D.dtype, qkv, ctx, at<float>(saved, L.lse), (int)D.batch, (int)D.seq,
-                        (int)D.heads, (int)D.d, c),
-          "attention fwd");
+  if (bf) {
+    MTL_TRY(attn_fwd_tc(qkv, ctx, at<float>(saved, L.lse), (int)D.batch, (int)D.seq, (int)D.heads,
+                        (int)D.d, status, c),
+            "attention fwd");
+  } else {
+    MTL_TRY(attn_fwd_simt(D.dtype, qkv, ctx, at<float>(saved, L.lse), (int)D.batch, (int)D.seq,
+                          (int)D.heads, (int)D.d, c),
+            "attention fwd");
+  }
   // F4 out-proj, row-parallel + g: t partials over K = h, + b_o + x
   {
     GemmArgs g = gemm_args(n, h, h, t, ctx, h, true, w->w_o, h, true, EPI_BIAS_RESID, x1, h,
@@ -331,7 +337,6 @@ mtl_status mtl_layer_fwd(const mtl_layer_desc* desc, const mtl_weights* w, const
     g.ldr = h;
     MTL_TRY(run_gemm(D, g, c), "fc2 gemm");
   }
-  (void)bf;
   return MTL_OK;
 }
 
@@ -424,9 +429,15 @@ mtl_status mtl_layer_bwd(const mtl_layer_desc* desc, const mtl_weights* w, const
           "out-proj wgrad");
   MTL_TRY(colsum(D.dtype, dx1, h, n, h, static_cast<float*>(gr->b_o), partial, c), "db_o");
   // B7 attention backward per head
-  MTL_TRY(attn_bwd_simt(D.dtype, qkv, ctx, at<float>(saved, L.lse), dctx, dqkv, dsum,
-                        (int)D.batch, (int)D.seq, (int)D.heads, (int)D.d, c),
-          "attention bwd");
+  if (D.dtype == MTL_BF16) {
+    MTL_TRY(attn_bwd_tc(qkv, ctx, at<float>(saved, L.lse), dctx, dqkv, dsum, (int)D.batch,
+                        (int)D.seq, (int)D.heads, (int)D.d, status, c),
+            "attention bwd");
+  } else {
+    MTL_TRY(attn_bwd_simt(D.dtype, qkv, ctx, at<float>(saved, L.lse), dctx, dqkv, dsum,
+                          (int)D.batch, (int)D.seq, (int)D.heads, (int)D.d, c),
+            "attention bwd");
+  }
   // B8 QKV wgrad dW_qkv = dqkv^T u1, db_qkv = sum_rows dqkv
   MTL_TRY(run_gemm(D, gemm_args(3 * h, h, n, 1, dqkv, 3 * h, false, u1, h, false, EPI_STORE,
                                 gr->w_qkv, h, true, status),
