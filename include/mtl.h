@@ -162,6 +162,29 @@ mtl_status mtl_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, int32_t k_pa
                     void* Z, int64_t ldz, void* C, int64_t ldc, int32_t c_f32,
                     void* workspace, size_t ws_bytes, mtl_stream stream);
 
+/* Bias gradient for callers that cannot allocate device memory:
+ *   out[j] = sum_{i < rows} dy[i*ld + j]   (j < cols; fp32, fixed order)
+ * -- the sum mtl_layer_bwd uses for b_fc2, b_o, b_fc1 and b_qkv, with the same
+ * kernels and the same result.  The paper has no counterpart; this exists for
+ * callers whose device memory is planned up front and who may not call the
+ * CUDA allocator (a runtime that hands all of HBM to its own pool at start-up,
+ * a deployment with a fixed memory plan), and so cannot provide a workspace.
+ *   dtype: MTL_F32 or MTL_BF16, the element type of dy; out is fp32.
+ *   dy: device, 16-byte aligned; ld and cols multiples of 8 (bf16) or 4 (fp32),
+ *   ld >= cols; out: device, cols floats.
+ * Scratch: a static device array of 8 MiB (128 x 16384 floats) inside the
+ * library, held by every GPU that loads it until the process exits; cols above
+ * 16384 return MTL_ERR_UNSUPPORTED.  Nothing is allocated or freed: no
+ * cudaMalloc, no cudaFree, no allocating library call.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress, with that
+ * device current); make that first call before any stream capture.  All calls
+ * on a device share the one array, whose contents persist from the last call:
+ * calls that overlap on the GPU (different streams, no ordering) race and give
+ * wrong sums, so order them on one stream.  Returns MTL_ERR_INVALID_ARG for
+ * bad pointers or sizes and MTL_ERR_CUDA if a launch fails. */
+mtl_status mtl_bias_grad_noalloc(int32_t dtype, const void* dy, int64_t ld, int32_t rows,
+                                 int32_t cols, void* out, mtl_stream stream);
+
 /* Human-readable name of a status. */
 const char* mtl_status_str(mtl_status s);
 

@@ -98,6 +98,10 @@ cudaError_t colsum(int dtype, const void* Y, int64_t ld, int n, int N, float* ou
                    float* partial, const LaunchCtx& c);
 size_t colsum_partial_floats(int n, int N);
 
+// Error text for mtl_last_cuda_error, shared by every entry point.
+void record_cuda_error(cudaError_t e, const char* where);
+void clear_cuda_error();
+
 // Causal attention over a head-interleaved qkv [batch*seq][3h] -> ctx
 // [batch*seq][h], lse [batch][heads][seq] (CUDA-core reference kernels).
 cudaError_t attn_fwd_simt(int dtype, const void* qkv, void* ctx, float* lse, int batch, int seq,

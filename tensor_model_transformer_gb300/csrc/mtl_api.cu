@@ -22,8 +22,20 @@
 using namespace mtl;
 
 namespace {
-
 thread_local char g_cuda_err[256] = {0};
+}  // namespace
+
+namespace mtl {
+// Records a CUDA failure for mtl_last_cuda_error (used by entry points that
+// live in other translation units).
+void record_cuda_error(cudaError_t e, const char* where) {
+  snprintf(g_cuda_err, sizeof(g_cuda_err), "%s: %s", where, cudaGetErrorString(e));
+}
+void clear_cuda_error() { g_cuda_err[0] = 0; }
+}  // namespace mtl
+
+namespace {
+
 thread_local int g_launches = 0;
 thread_local Profiler g_prof = {nullptr, 0, 0, nullptr, nullptr};
 

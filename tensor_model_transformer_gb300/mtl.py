@@ -69,6 +69,8 @@ def lib():
         L.mtl_layer_check.argtypes = [vp, vp]
         L.mtl_gemm.argtypes = [i32, i32, i32, i32, i32, vp, i64, i32, vp, i64, i32, i32, vp, vp,
                                i64, vp, i64, vp, i64, i32, vp, sz, vp]
+        L.mtl_bias_grad_noalloc.argtypes = [i32, vp, i64, i32, i32, vp, vp]
+        L.mtl_bias_grad_noalloc.restype = ctypes.c_int
         L.mtl_status_str.argtypes = [ctypes.c_int]
         L.mtl_status_str.restype = ctypes.c_char_p
         L.mtl_last_cuda_error.restype = ctypes.c_char_p
@@ -160,6 +162,16 @@ def gemm(dtype, M, N, K, parts, A, lda, a_k_major, B, ldb, b_k_major, epi, C, ld
                           ldc, int(c_f32), _ptr(workspace),
                           workspace.numel() * workspace.element_size(), _stream(stream)),
            "mtl_gemm")
+
+
+def bias_grad_noalloc(dtype, dy, ld, rows, cols, out, stream=None):
+    """mtl_bias_grad_noalloc: out[j] = sum_i dy[i*ld + j] with no workspace.
+
+    For callers that cannot allocate device memory; its scratch is a static
+    array inside the library (see include/mtl.h)."""
+    dt = {"f32": F32, "bf16": BF16, F32: F32, BF16: BF16}[dtype]
+    _check(lib().mtl_bias_grad_noalloc(dt, _ptr(dy), ld, rows, cols, _ptr(out), _stream(stream)),
+           "mtl_bias_grad_noalloc")
 
 
 # ---------------------------------------------------------------- allocation helpers
