@@ -32,6 +32,7 @@ namespace attn {
 constexpr int THREADS = 192;
 constexpr int ATOM128 = 128 * 128;   // [128 rows][64 bf16]
 constexpr int ATOM64 = 64 * 128;     // [64 rows][64 bf16]
+constexpr int BWD_STAGES = 3;      // TMA ring depth of the backward kernels
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
@@ -58,16 +59,17 @@ __device__ __forceinline__ Smem smem_aligned(uint8_t* raw) {
   return {p, smem_u32(p)};
 }
 
-// Block index -> (row block, head, batch); `heavy_first_desc` puts the row
-// blocks with the most causal work first.
+// Block index -> (row block, head, batch).  Consecutive blocks share a
+// (batch, head) pair, so the CTAs running at once reuse each other's K/V (or
+// Q/dO) tiles from L2; inside a pair the row blocks with the most causal work
+// come first (`desc`: high row blocks are heavy; else low ones are).
 __device__ __forceinline__ void block_coords(const Params& p, int nblk, bool desc, int& blk,
                                              int& hd, int& b) {
-  const int hb = p.heads * p.batch;
-  const int i = blockIdx.x / hb;
+  const int pair = blockIdx.x / nblk;
+  const int i = blockIdx.x % nblk;
   blk = desc ? (nblk - 1 - i) : i;
-  const int r = blockIdx.x % hb;
-  hd = r % p.heads;
-  b = r / p.heads;
+  hd = pair % p.heads;
+  b = pair / p.heads;
 }
 
 // ============================================================================ forward
@@ -193,21 +195,29 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int k = 0; k < 128; ++k)
           if (k > r) s[k] = -INFINITY;
       }
-      float mx = s[0];
+      // 8 independent partial maxima / sums keep the dependent chains short
+      float mxp[8];
 #pragma unroll
-      for (int k = 1; k < 128; ++k) mx = fmaxf(mx, s[k]);
+      for (int q = 0; q < 8; ++q) mxp[q] = s[q];
+#pragma unroll
+      for (int k = 8; k < 128; ++k) mxp[k & 7] = fmaxf(mxp[k & 7], s[k]);
+      const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                             fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
       const float m_new = fmaxf(m_used, mx);
       // Rescale only when the running maximum grew by more than 2^8: the
       // exponentials stay below 256 and the final O / l is exact either way.
       const bool resc = m_new > m_used + 8.0f;
       const float alpha = resc ? fast_exp2(m_used - m_new) : 1.0f;
       if (resc) m_used = m_new;
-      float rs = 0.f;
+      float rsp[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) rsp[q] = 0.f;
 #pragma unroll
       for (int k = 0; k < 128; ++k) {
         s[k] = fast_exp2(s[k] - m_used);
-        rs += s[k];
+        rsp[k & 7] += s[k];
       }
+      const float rs = ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
       l = l * alpha + rs;
       if (j > 0) {
         if (!mbar_wait_bounded(B(11), (j - 1) & 1, p.status, abort_flag)) {
@@ -286,13 +296,16 @@ __global__ void __launch_bounds__(THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   const Smem sm = smem_aligned(smem_raw);
   constexpr uint32_t T128 = NA * ATOM128, T64 = NA * ATOM64;
-  const uint32_t sQ = sm.u32, sDO = sQ + T128, sK0 = sQ + 2 * T128, sV0 = sK0 + 2 * T64,
-                 sDS = sV0 + 2 * T64;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm.base + 2 * T128 + 4 * T64 + ATOM128);
+  constexpr int ST = BWD_STAGES;
+  const uint32_t sQ = sm.u32, sDO = sQ + T128, sK0 = sQ + 2 * T128, sV0 = sK0 + ST * T64,
+                 sDS = sV0 + ST * T64;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm.base + 2 * T128 + 2 * ST * T64 + ATOM128);
   const uint32_t bar0 = smem_u32(bars);
-  // 0 q/do full, 1-2 kv_full, 3-4 kv_empty, 5 s_full, 6 ds_full, 7 dq_done
+  // 0 q/do full, 1..ST kv_full, ST+1..2ST kv_empty, 2ST+1 s_full, 2ST+2 ds_full,
+  // 2ST+3 dq_done
   auto B = [&](int i) { return bar0 + 8u * i; };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
+  const int KVF = 1, KVE = 1 + ST, SF = 1 + 2 * ST, DSF = 2 + 2 * ST, DQD = 3 + 2 * ST;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * ST + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   int qb, hd, b;
@@ -303,7 +316,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 8; ++i) mbar_init(B(i), i == 6 ? 128 : 1);
+    for (int i = 0; i < 2 * ST + 4; ++i) mbar_init(B(i), i == DSF ? 128 : 1);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_shared();
@@ -326,13 +339,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         tma_load_2d(sDO + a * ATOM128, &tmdo128, B(0), hd * p.d + 64 * a, row0);
       }
       for (int j = 0; j < nkv; ++j) {
-        const int s = j & 1;
+        const int s = j % ST;
         const int krow = b * p.seq + j * 64;
-        if (!mbar_wait_bounded(B(3 + s), ((j >> 1) & 1) ^ 1u, p.status, abort_flag)) break;
-        mbar_arrive_expect_tx(B(1 + s), 2 * T64);
+        if (!mbar_wait_bounded(B(KVE + s), ((j / ST) & 1) ^ 1u, p.status, abort_flag)) break;
+        mbar_arrive_expect_tx(B(KVF + s), 2 * T64);
         for (int a = 0; a < NA; ++a) {
-          tma_load_2d(sK0 + s * T64 + a * ATOM64, &tm64, B(1 + s), colq + p.d + 64 * a, krow);
-          tma_load_2d(sV0 + s * T64 + a * ATOM64, &tm64, B(1 + s), colq + 2 * p.d + 64 * a, krow);
+          tma_load_2d(sK0 + s * T64 + a * ATOM64, &tm64, B(KVF + s), colq + p.d + 64 * a, krow);
+          tma_load_2d(sV0 + s * T64 + a * ATOM64, &tm64, B(KVF + s), colq + 2 * p.d + 64 * a,
+                      krow);
         }
       }
     }
@@ -343,36 +357,36 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t id_dq = idesc_bf16_f32(128, p.d, false, true);
       const int ksteps = p.d / 16;
       auto issue_s = [&](int j) {
-        const int s = j & 1;
+        const int s = j % ST;
         for (int kk = 0; kk < ksteps; ++kk)
           tc_mma_bf16(tS, desc_kmajor(sQ, ATOM128, kk), desc_kmajor(sK0 + s * T64, ATOM64, kk),
                       id_s, kk > 0);
         for (int kk = 0; kk < ksteps; ++kk)
           tc_mma_bf16(tDP, desc_kmajor(sDO, ATOM128, kk), desc_kmajor(sV0 + s * T64, ATOM64, kk),
                       id_s, kk > 0);
-        tc_commit(B(5));
+        tc_commit(B(SF));
       };
       bool ok = mbar_wait_bounded(B(0), 0, p.status, abort_flag) &&
-                mbar_wait_bounded(B(1), 0, p.status, abort_flag);
+                mbar_wait_bounded(B(KVF), 0, p.status, abort_flag);
       if (ok) {
         tc_fence_after();
         issue_s(0);
       }
       for (int j = 0; j < nkv && ok; ++j) {
-        if (!mbar_wait_bounded(B(6), j & 1, p.status, abort_flag)) break;
+        if (!mbar_wait_bounded(B(DSF), j & 1, p.status, abort_flag)) break;
         tc_fence_after();
         if (j + 1 < nkv) {
-          if (!mbar_wait_bounded(B(1 + ((j + 1) & 1)), ((j + 1) >> 1) & 1, p.status, abort_flag))
+          if (!mbar_wait_bounded(B(KVF + (j + 1) % ST), ((j + 1) / ST) & 1, p.status, abort_flag))
             break;
           tc_fence_after();
           issue_s(j + 1);
         }
-        const int s = j & 1;
+        const int s = j % ST;
         for (int kk = 0; kk < 4; ++kk)
           tc_mma_bf16(tDQ, desc_kmajor(sDS, ATOM128, kk), desc_mnmajor(sK0 + s * T64, ATOM64, kk),
                       id_dq, (j > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(B(3 + s));
-        tc_commit(B(7));
+        tc_commit(B(KVE + s));
+        tc_commit(B(DQD));
       }
     }
     __syncwarp();
@@ -396,7 +410,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const float lse2 = p.lse[lrow] * LOG2E;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
-      if (!mbar_wait_bounded(B(5), j & 1, p.status, abort_flag)) {
+      if (!mbar_wait_bounded(B(SF), j & 1, p.status, abort_flag)) {
         ok = false;
         break;
       }
@@ -417,7 +431,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       if (j > 0) {
-        if (!mbar_wait_bounded(B(7), (j - 1) & 1, p.status, abort_flag)) {
+        if (!mbar_wait_bounded(B(DQD), (j - 1) & 1, p.status, abort_flag)) {
           ok = false;
           break;
         }
@@ -431,9 +445,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       fence_proxy_async_shared();
       tc_fence_before();
-      mbar_arrive(B(6));
+      mbar_arrive(B(DSF));
     }
-    if (ok && mbar_wait_bounded(B(7), (nkv - 1) & 1, p.status, abort_flag)) {
+    if (ok && mbar_wait_bounded(B(DQD), (nkv - 1) & 1, p.status, abort_flag)) {
       tc_fence_after();
       bf16* dq = p.dqkv + (size_t)(row0 + r) * 3 * p.h + colq;
       for (int c = 0; c < p.d; c += 32) {
@@ -478,13 +492,21 @@ __global__ void __launch_bounds__(THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   const Smem sm = smem_aligned(smem_raw);
   constexpr uint32_t T128 = NA * ATOM128, T64 = NA * ATOM64;
-  const uint32_t sK = sm.u32, sV = sK + T128, sQ0 = sK + 2 * T128, sDO0 = sQ0 + 2 * T64,
-                 sPT = sDO0 + 2 * T64, sDST = sPT + ATOM128;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm.base + 2 * T128 + 4 * T64 + 2 * ATOM128);
+  constexpr int ST = BWD_STAGES;
+  const uint32_t sK = sm.u32, sV = sK + T128, sQ0 = sK + 2 * T128, sDO0 = sQ0 + ST * T64,
+                 sPT = sDO0 + ST * T64, sDST = sPT + ATOM128;
+  // lse and D of the 64-query block of each stage, copied in with its Q / dO
+  float* s_lse0 = reinterpret_cast<float*>(sm.base + 2 * T128 + 2 * ST * T64 + 2 * ATOM128);
+  float* s_d0 = s_lse0 + 64 * ST;
+  const uint32_t s_lse_u32 = smem_u32(s_lse0), s_d_u32 = smem_u32(s_d0);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm.base + 2 * T128 + 2 * ST * T64 + 2 * ATOM128 +
+                                               512 * ST);
   const uint32_t bar0 = smem_u32(bars);
-  // 0 kv_full, 1-2 qdo_full, 3-4 qdo_empty, 5 st_full, 6 pt_full, 7 mm_done
+  // 0 kv_full, 1..ST qdo_full, ST+1..2ST qdo_empty, 2ST+1 st_full, 2ST+2 pt_full,
+  // 2ST+3 mm_done
   auto B = [&](int i) { return bar0 + 8u * i; };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
+  const int QF = 1, QE = 1 + ST, STF = 1 + 2 * ST, PTF = 2 + 2 * ST, MMD = 3 + 2 * ST;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * ST + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   int kb, hd, b;
@@ -496,7 +518,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 8; ++i) mbar_init(B(i), i == 6 ? 128 : 1);
+    for (int i = 0; i < 2 * ST + 4; ++i) mbar_init(B(i), i == PTF ? 128 : 1);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_shared();
@@ -519,14 +541,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         tma_load_2d(sV + a * ATOM128, &tm128, B(0), colq + 2 * p.d + 64 * a, krow0);
       }
       for (int i = 0; i < nq; ++i) {
-        const int s = i & 1;
+        const int s = i % ST;
         const int qrow = b * p.seq + (first + i) * 64;
-        if (!mbar_wait_bounded(B(3 + s), ((i >> 1) & 1) ^ 1u, p.status, abort_flag)) break;
-        mbar_arrive_expect_tx(B(1 + s), 2 * T64);
+        if (!mbar_wait_bounded(B(QE + s), ((i / ST) & 1) ^ 1u, p.status, abort_flag)) break;
+        mbar_arrive_expect_tx(B(QF + s), 2 * T64 + 512);
         for (int a = 0; a < NA; ++a) {
-          tma_load_2d(sQ0 + s * T64 + a * ATOM64, &tm64, B(1 + s), colq + 64 * a, qrow);
-          tma_load_2d(sDO0 + s * T64 + a * ATOM64, &tmdo64, B(1 + s), hd * p.d + 64 * a, qrow);
+          tma_load_2d(sQ0 + s * T64 + a * ATOM64, &tm64, B(QF + s), colq + 64 * a, qrow);
+          tma_load_2d(sDO0 + s * T64 + a * ATOM64, &tmdo64, B(QF + s), hd * p.d + 64 * a, qrow);
         }
+        const size_t lo = ((size_t)b * p.heads + hd) * p.seq + (first + i) * 64;
+        bulk_load(s_lse_u32 + s * 256, p.lse + lo, 256, B(QF + s));
+        bulk_load(s_d_u32 + s * 256, p.dsum + lo, 256, B(QF + s));
       }
     }
     __syncwarp();
@@ -536,39 +561,39 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t id_acc = idesc_bf16_f32(128, p.d, false, true);
       const int ksteps = p.d / 16;
       auto issue_st = [&](int i) {
-        const int s = i & 1;
+        const int s = i % ST;
         for (int kk = 0; kk < ksteps; ++kk)
           tc_mma_bf16(tST, desc_kmajor(sK, ATOM128, kk), desc_kmajor(sQ0 + s * T64, ATOM64, kk),
                       id_st, kk > 0);
         for (int kk = 0; kk < ksteps; ++kk)
           tc_mma_bf16(tDPT, desc_kmajor(sV, ATOM128, kk), desc_kmajor(sDO0 + s * T64, ATOM64, kk),
                       id_st, kk > 0);
-        tc_commit(B(5));
+        tc_commit(B(STF));
       };
       bool ok = mbar_wait_bounded(B(0), 0, p.status, abort_flag) &&
-                mbar_wait_bounded(B(1), 0, p.status, abort_flag);
+                mbar_wait_bounded(B(QF), 0, p.status, abort_flag);
       if (ok) {
         tc_fence_after();
         issue_st(0);
       }
       for (int i = 0; i < nq && ok; ++i) {
-        if (!mbar_wait_bounded(B(6), i & 1, p.status, abort_flag)) break;
+        if (!mbar_wait_bounded(B(PTF), i & 1, p.status, abort_flag)) break;
         tc_fence_after();
         if (i + 1 < nq) {
-          if (!mbar_wait_bounded(B(1 + ((i + 1) & 1)), ((i + 1) >> 1) & 1, p.status, abort_flag))
+          if (!mbar_wait_bounded(B(QF + (i + 1) % ST), ((i + 1) / ST) & 1, p.status, abort_flag))
             break;
           tc_fence_after();
           issue_st(i + 1);
         }
-        const int s = i & 1;
+        const int s = i % ST;
         for (int kk = 0; kk < 4; ++kk)
           tc_mma_bf16(tDV, desc_kmajor(sPT, ATOM128, kk), desc_mnmajor(sDO0 + s * T64, ATOM64, kk),
                       id_acc, (i > 0 || kk > 0) ? 1u : 0u);
         for (int kk = 0; kk < 4; ++kk)
           tc_mma_bf16(tDK, desc_kmajor(sDST, ATOM128, kk), desc_mnmajor(sQ0 + s * T64, ATOM64, kk),
                       id_acc, (i > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(B(3 + s));
-        tc_commit(B(7));
+        tc_commit(B(QE + s));
+        tc_commit(B(MMD));
       }
     }
     __syncwarp();
@@ -577,16 +602,23 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int r = q4 * 32 + lane;   // key row
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const int key = kb * 128 + r;
-    const float* lse_bh = p.lse + ((size_t)b * p.heads + hd) * p.seq;
-    const float* d_bh = p.dsum + ((size_t)b * p.heads + hd) * p.seq;
     bool ok = true;
     for (int i = 0; i < nq; ++i) {
-      if (!mbar_wait_bounded(B(5), i & 1, p.status, abort_flag)) {
+      if (!mbar_wait_bounded(B(STF), i & 1, p.status, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
       const int q0 = (first + i) * 64;
+      // lse / D of this block arrive with its Q / dO tiles: observe that
+      // barrier's phase too (stage i&1 is not refilled before this iteration
+      // ends: its release waits for the MMAs that follow our arrival below)
+      if (!mbar_wait_bounded(B(QF + i % ST), (i / ST) & 1, p.status, abort_flag)) {
+        ok = false;
+        break;
+      }
+      const float* s_lse = s_lse0 + (i % ST) * 64;
+      const float* s_d = s_d0 + (i % ST) * 64;
       float pt[64], dst[64];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -597,14 +629,14 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int q = q0 + c * 32 + e;
-          float pr = fast_exp2(__uint_as_float(sv[e]) * p.scale_log2 - __ldg(lse_bh + q) * LOG2E);
+          float pr = fast_exp2(__uint_as_float(sv[e]) * p.scale_log2 - s_lse[c * 32 + e] * LOG2E);
           if (q < key) pr = 0.f;
           pt[c * 32 + e] = pr;
-          dst[c * 32 + e] = pr * (__uint_as_float(dv[e]) - __ldg(d_bh + q));
+          dst[c * 32 + e] = pr * (__uint_as_float(dv[e]) - s_d[c * 32 + e]);
         }
       }
       if (i > 0) {
-        if (!mbar_wait_bounded(B(7), (i - 1) & 1, p.status, abort_flag)) {
+        if (!mbar_wait_bounded(B(MMD), (i - 1) & 1, p.status, abort_flag)) {
           ok = false;
           break;
         }
@@ -621,9 +653,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       fence_proxy_async_shared();
       tc_fence_before();
-      mbar_arrive(B(6));
+      mbar_arrive(B(PTF));
     }
-    if (ok && mbar_wait_bounded(B(7), (nq - 1) & 1, p.status, abort_flag)) {
+    if (ok && mbar_wait_bounded(B(MMD), (nq - 1) & 1, p.status, abort_flag)) {
       tc_fence_after();
       bf16* out = p.dqkv + (size_t)(krow0 + r) * 3 * p.h + colq;
       for (int which = 0; which < 2; ++which) {   // 0: dK (scaled), 1: dV
@@ -688,11 +720,14 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uin
 }
 
 size_t fwd_smem(int na) { return (size_t)5 * na * ATOM128 + 2 * ATOM128 + 256 + 1024; }
-size_t dq_smem(int na) { return (size_t)2 * na * ATOM128 + 4 * na * ATOM64 + ATOM128 + 256 + 1024; }
+size_t dq_smem(int na) {
+  return (size_t)2 * na * ATOM128 + 2 * BWD_STAGES * na * ATOM64 + ATOM128 + 256 + 1024;
+}
 // The dK/dV kernel holds all 512 TMEM columns: its shared memory request keeps
 // it at one CTA per SM so a second CTA never waits in tcgen05.alloc.
 size_t dkv_smem(int na) {
-  const size_t need = (size_t)2 * na * ATOM128 + 4 * na * ATOM64 + 2 * ATOM128 + 256 + 1024;
+  const size_t need = (size_t)2 * na * ATOM128 + 2 * BWD_STAGES * na * ATOM64 + 2 * ATOM128 +
+                      512 * BWD_STAGES + 256 + 1024;
   return need < 120 * 1024 ? 120 * 1024 : need;
 }
 

@@ -16,109 +16,110 @@ constexpr int kLnThreadsMax = 512;
 constexpr int kLnBwdBlocks = 512;     // row blocks of the dgamma/dbeta reduction
 constexpr int kColsumBlocks = 128;    // row blocks of the bias-gradient reduction
 
-// Sum of two values over the block; `red` holds 2*32 floats.
-__device__ __forceinline__ float2 block_sum2(float a, float b, float* red) {
+// Sums NV values over the block in place; `red` holds NV*32 floats.  Every
+// thread adds the per-warp sums in the same order.
+template <int NV>
+__device__ __forceinline__ void block_sum_n(float (&v)[NV], float* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nw = (blockDim.x + 31) >> 5;
-  a = warp_sum(a);
-  b = warp_sum(b);
+#pragma unroll
+  for (int i = 0; i < NV; ++i) v[i] = warp_sum(v[i]);
   __syncthreads();  // earlier readers of `red` are done
   if (lane == 0) {
-    red[warp] = a;
-    red[32 + warp] = b;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) red[i * 32 + warp] = v[i];
   }
   __syncthreads();
-  float sa = 0.f, sb = 0.f;
-  for (int w = 0; w < nw; ++w) {  // same order in every thread
-    sa += red[w];
-    sb += red[32 + w];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    float s = 0.f;
+    for (int w = 0; w < nw; ++w) s += red[i * 32 + w];
+    v[i] = s;
   }
-  return make_float2(sa, sb);
 }
 
-template <typename T, int V>
-__global__ void __launch_bounds__(kLnThreadsMax) ln_fwd_kernel(const T* __restrict__ x, const T* __restrict__ gamma,
-                              const T* __restrict__ beta, T* __restrict__ u,
-                              float* __restrict__ mean_out, float* __restrict__ rstd_out, int n,
-                              int h, float eps, int rows_per_block) {
+// R rows per iteration: the loads of all R rows are issued before the block
+// reductions, so each thread keeps R*V 16-byte loads in flight.
+template <typename T, int V, int R>
+__global__ void __launch_bounds__(kLnThreadsMax)
+    ln_fwd_kernel(const T* __restrict__ x, const T* __restrict__ gamma, const T* __restrict__ beta,
+                  T* __restrict__ u, float* __restrict__ mean_out, float* __restrict__ rstd_out,
+                  int n, int h, float eps, int rows_per_block) {
   constexpr int E = Vec<T>::N;
-  __shared__ float red[64];
+  __shared__ float red[R * 32];
   const int nvec = h / E;
-  float g[V][E], b[V][E];
+  const int r_begin = blockIdx.x * rows_per_block;
+  const int r_end = min(n, r_begin + rows_per_block);
+  const float inv_h = 1.0f / (float)h;
+  for (int r0 = r_begin; r0 < r_end; r0 += R) {
+    Vec<T> xv[R][V];
+    float s[R];
 #pragma unroll
-  for (int i = 0; i < V; ++i) {
-    const int vi = threadIdx.x + i * blockDim.x;
-    if (vi < nvec) {
+    for (int rr = 0; rr < R; ++rr) {
+      s[rr] = 0.f;
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        const int vi = threadIdx.x + i * blockDim.x;
+        if (r0 + rr < r_end && vi < nvec) {
+          xv[rr][i].load(x + (size_t)(r0 + rr) * h + vi * E);
+#pragma unroll
+          for (int e = 0; e < E; ++e) s[rr] += xv[rr][i].get(e);
+        }
+      }
+    }
+    block_sum_n<R>(s, red);
+    float mean[R], ss[R];
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) {
+      mean[rr] = s[rr] * inv_h;
+      ss[rr] = 0.f;
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        const int vi = threadIdx.x + i * blockDim.x;
+        if (r0 + rr < r_end && vi < nvec) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const float dlt = xv[rr][i].get(e) - mean[rr];
+            ss[rr] += dlt * dlt;
+          }
+        }
+      }
+    }
+    block_sum_n<R>(ss, red);
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int vi = threadIdx.x + i * blockDim.x;
+      if (vi >= nvec) continue;
       Vec<T> tg, tb;
       tg.load(gamma + vi * E);
       tb.load(beta + vi * E);
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        g[i][e] = tg.get(e);
-        b[i][e] = tb.get(e);
-      }
-    }
-  }
-  const int r0 = blockIdx.x * rows_per_block;
-  const int r1 = min(n, r0 + rows_per_block);
-  const float inv_h = 1.0f / (float)h;
-  for (int r = r0; r < r1; ++r) {
-    const T* xr = x + (size_t)r * h;
-    float v[V][E];
-    float s = 0.f;
-#pragma unroll
-    for (int i = 0; i < V; ++i) {
-      const int vi = threadIdx.x + i * blockDim.x;
-      if (vi < nvec) {
-        Vec<T> t;
-        t.load(xr + vi * E);
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          v[i][e] = t.get(e);
-          s += v[i][e];
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < E; ++e) v[i][e] = 0.f;
-      }
-    }
-    const float mean = block_sum2(s, 0.f, red).x * inv_h;
-    float ss = 0.f;
-#pragma unroll
-    for (int i = 0; i < V; ++i) {
-      const int vi = threadIdx.x + i * blockDim.x;
-      if (vi < nvec) {
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const float dlt = v[i][e] - mean;
-          ss += dlt * dlt;
-        }
-      }
-    }
-    const float var = block_sum2(ss, 0.f, red).x * inv_h;
-    const float rs = 1.0f / sqrtf(var + eps);
-    T* ur = u + (size_t)r * h;
-#pragma unroll
-    for (int i = 0; i < V; ++i) {
-      const int vi = threadIdx.x + i * blockDim.x;
-      if (vi < nvec) {
+      for (int rr = 0; rr < R; ++rr) {
+        if (r0 + rr >= r_end) continue;
+        const float rs = 1.0f / sqrtf(ss[rr] * inv_h + eps);
         Vec<T> o;
 #pragma unroll
-        for (int e = 0; e < E; ++e) o.set(e, (v[i][e] - mean) * rs * g[i][e] + b[i][e]);
-        o.store(ur + vi * E);
+        for (int e = 0; e < E; ++e)
+          o.set(e, (xv[rr][i].get(e) - mean[rr]) * rs * tg.get(e) + tb.get(e));
+        o.store(u + (size_t)(r0 + rr) * h + vi * E);
       }
     }
     if (threadIdx.x == 0) {
-      mean_out[r] = mean;
-      rstd_out[r] = rs;
+#pragma unroll
+      for (int rr = 0; rr < R; ++rr) {
+        if (r0 + rr < r_end) {
+          mean_out[r0 + rr] = mean[rr];
+          rstd_out[r0 + rr] = 1.0f / sqrtf(ss[rr] * inv_h + eps);
+        }
+      }
     }
   }
 }
 
-// Dynamic shared memory: gamma, and the block's running column sums of
-// du * xhat and du (3 * h floats); thread i owns the same columns in every row,
-// so the sums need no atomics.
-template <typename T, int V>
+// Dynamic shared memory: the block's running column sums of du * xhat and du
+// (2 * h floats); thread i owns the same columns in every row, so the sums need
+// no atomics.  R rows per iteration, their loads issued before the reduction.
+template <typename T, int V, int R>
 __global__ void __launch_bounds__(kLnThreadsMax)
     ln_bwd_kernel(const float* __restrict__ du, const T* __restrict__ x,
                   const float* __restrict__ mean_in, const float* __restrict__ rstd_in,
@@ -127,80 +128,106 @@ __global__ void __launch_bounds__(kLnThreadsMax)
                   int rows_per_block) {
   constexpr int E = Vec<T>::N;
   extern __shared__ float lsm[];
-  float* sg = lsm;
-  float* acc_g = lsm + h;
-  float* acc_b = lsm + 2 * h;
-  __shared__ float red[64];
+  float* acc_g = lsm;
+  float* acc_b = lsm + h;
+  __shared__ float red[2 * R * 32];
   const int nvec = h / E;
+  // accumulator layout [e][vi]: consecutive threads touch consecutive words
   for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
-    Vec<T> tg;
-    tg.load(gamma + vi * E);
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      sg[vi * E + e] = tg.get(e);
-      acc_g[vi * E + e] = 0.f;
-      acc_b[vi * E + e] = 0.f;
+      acc_g[e * nvec + vi] = 0.f;
+      acc_b[e * nvec + vi] = 0.f;
     }
   }
   // each thread reads back only the columns it wrote: no barrier needed
-  const int r0 = blockIdx.x * rows_per_block;
-  const int r1 = min(n, r0 + rows_per_block);
+  const int r_begin = blockIdx.x * rows_per_block;
+  const int r_end = min(n, r_begin + rows_per_block);
   const float inv_h = 1.0f / (float)h;
-  for (int r = r0; r < r1; ++r) {
-    const float mu = mean_in[r], rs = rstd_in[r];
-    Vec<T> xv[V];
-    float dd[V][E];
-    float s1 = 0.f, s2 = 0.f;
+  for (int r0 = r_begin; r0 < r_end; r0 += R) {
+    Vec<T> xv[R][V], rv[R][V];
+    float dd[R][V][E];
+    float mu[R], rs[R], s[2 * R];
 #pragma unroll
-    for (int i = 0; i < V; ++i) {
-      const int vi = threadIdx.x + i * blockDim.x;
-      if (vi < nvec) {
-        xv[i].load(x + (size_t)r * h + vi * E);
-        const float* dur = du + (size_t)r * h + vi * E;
+    for (int rr = 0; rr < R; ++rr) {
+      const bool live = r0 + rr < r_end;
+      mu[rr] = live ? mean_in[r0 + rr] : 0.f;
+      rs[rr] = live ? rstd_in[r0 + rr] : 0.f;
+      s[2 * rr] = 0.f;
+      s[2 * rr + 1] = 0.f;
 #pragma unroll
-        for (int e = 0; e < E; e += 4) {
-          const float4 q = *reinterpret_cast<const float4*>(dur + e);
-          dd[i][e] = q.x;
-          dd[i][e + 1] = q.y;
-          dd[i][e + 2] = q.z;
-          dd[i][e + 3] = q.w;
-        }
+      for (int i = 0; i < V; ++i) {
+        const int vi = threadIdx.x + i * blockDim.x;
+        if (live && vi < nvec) {
+          const size_t off = (size_t)(r0 + rr) * h + vi * E;
+          xv[rr][i].load(x + off);
+          rv[rr][i].load(resid + off);
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const int col = vi * E + e;
-          const float xh = (xv[i].get(e) - mu) * rs;
-          const float gd = dd[i][e] * sg[col];
-          s1 += gd;
-          s2 += gd * xh;
-          acc_g[col] += dd[i][e] * xh;
-          acc_b[col] += dd[i][e];
+          for (int e = 0; e < E; e += 4) {
+            const float4 q = *reinterpret_cast<const float4*>(du + off + e);
+            dd[rr][i][e] = q.x;
+            dd[rr][i][e + 1] = q.y;
+            dd[rr][i][e + 2] = q.z;
+            dd[rr][i][e + 3] = q.w;
+          }
         }
       }
     }
-    const float2 s = block_sum2(s1, s2, red);
-    const float m1 = s.x * inv_h, m2 = s.y * inv_h;
 #pragma unroll
     for (int i = 0; i < V; ++i) {
       const int vi = threadIdx.x + i * blockDim.x;
-      if (vi < nvec) {
-        Vec<T> tr, o;
-        tr.load(resid + (size_t)r * h + vi * E);
+      if (vi >= nvec) continue;
+      Vec<T> tg;
+      tg.load(gamma + vi * E);
+#pragma unroll
+      for (int rr = 0; rr < R; ++rr) {
+        if (r0 + rr >= r_end) continue;
 #pragma unroll
         for (int e = 0; e < E; ++e) {
-          const int col = vi * E + e;
-          const float xh = (xv[i].get(e) - mu) * rs;
-          const float gd = dd[i][e] * sg[col];
-          o.set(e, tr.get(e) + rs * (gd - m1 - xh * m2));
+          const float xh = (xv[rr][i].get(e) - mu[rr]) * rs[rr];
+          const float gd = dd[rr][i][e] * tg.get(e);
+          s[2 * rr] += gd;
+          s[2 * rr + 1] += gd * xh;
         }
-        o.store(dx + (size_t)r * h + vi * E);
+      }
+    }
+    block_sum_n<2 * R>(s, red);
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int vi = threadIdx.x + i * blockDim.x;
+      if (vi >= nvec) continue;
+      Vec<T> tg;
+      tg.load(gamma + vi * E);
+      float ag[E], ab[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) ag[e] = ab[e] = 0.f;
+#pragma unroll
+      for (int rr = 0; rr < R; ++rr) {
+        if (r0 + rr >= r_end) continue;
+        const float m1 = s[2 * rr] * inv_h, m2 = s[2 * rr + 1] * inv_h;
+        Vec<T> o;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const float xh = (xv[rr][i].get(e) - mu[rr]) * rs[rr];
+          const float gd = dd[rr][i][e] * tg.get(e);
+          o.set(e, rv[rr][i].get(e) + rs[rr] * (gd - m1 - xh * m2));
+          ag[e] += dd[rr][i][e] * xh;
+          ab[e] += dd[rr][i][e];
+        }
+        o.store(dx + (size_t)(r0 + rr) * h + vi * E);
+      }
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        acc_g[e * nvec + vi] += ag[e];
+        acc_b[e * nvec + vi] += ab[e];
       }
     }
   }
   for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      part_g[(size_t)blockIdx.x * h + vi * E + e] = acc_g[vi * E + e];
-      part_b[(size_t)blockIdx.x * h + vi * E + e] = acc_b[vi * E + e];
+      part_g[(size_t)blockIdx.x * h + vi * E + e] = acc_g[e * nvec + vi];
+      part_b[(size_t)blockIdx.x * h + vi * E + e] = acc_b[e * nvec + vi];
     }
   }
 }
@@ -254,17 +281,17 @@ cudaError_t ln_fwd_t(const void* x, const void* g, const void* b, void* u, float
   row_plan<T>(h, &vpt, &threads);
   const int rows = n >= 4 * c.num_sms * 4 ? 4 : 1;
   const int grid = (n + rows - 1) / rows;
-#define LN_FWD_CASE(VV)                                                                      \
+  c.before(KK_LN_FWD, (double)n * h * (2.0 * sizeof(T)) + 8.0 * n);
+#define LN_FWD_CASE(VV, RR)                                                                  \
   case VV:                                                                                   \
-    ln_fwd_kernel<T, VV><<<grid, threads, 0, c.stream>>>(                                    \
+    ln_fwd_kernel<T, VV, RR><<<grid, threads, 0, c.stream>>>(                                \
         (const T*)x, (const T*)g, (const T*)b, (T*)u, mean, rstd, n, h, eps, rows);          \
     break;
-  c.before(KK_LN_FWD, (double)n * h * (2.0 * sizeof(T)) + 8.0 * n);
   switch (vpt) {
-    LN_FWD_CASE(1)
-    LN_FWD_CASE(2)
-    LN_FWD_CASE(4)
-    LN_FWD_CASE(8)
+    LN_FWD_CASE(1, 4)
+    LN_FWD_CASE(2, 2)
+    LN_FWD_CASE(4, 1)
+    LN_FWD_CASE(8, 1)
     default:
       return cudaErrorInvalidValue;
   }
@@ -283,25 +310,25 @@ cudaError_t ln_bwd_t(const float* du, const void* x, const float* mean, const fl
   const int rows = (n + nblk - 1) / nblk;
   float* pg = partial;
   float* pb = partial + (size_t)nblk * h;
-  const size_t smem = 3 * (size_t)h * sizeof(float);
-#define LN_BWD_CASE(VV)                                                                     \
+  const size_t smem = 2 * (size_t)h * sizeof(float);
+  c.before(KK_LN_BWD, (double)n * h * (3.0 * sizeof(T) + 4.0) + 8.0 * n);
+#define LN_BWD_CASE(VV, RR)                                                                 \
   case VV:                                                                                  \
     if (smem > 48 * 1024) {                                                                 \
-      cudaError_t fe = cudaFuncSetAttribute(ln_bwd_kernel<T, VV>,                           \
+      cudaError_t fe = cudaFuncSetAttribute(ln_bwd_kernel<T, VV, RR>,                       \
                                             cudaFuncAttributeMaxDynamicSharedMemorySize,    \
                                             (int)smem);                                     \
       if (fe != cudaSuccess) return fe;                                                     \
     }                                                                                       \
-    ln_bwd_kernel<T, VV><<<nblk, threads, smem, c.stream>>>(du, (const T*)x, mean, rstd,    \
-                                                            (const T*)g, (const T*)resid,   \
-                                                            (T*)dx, pg, pb, n, h, rows);    \
+    ln_bwd_kernel<T, VV, RR><<<nblk, threads, smem, c.stream>>>(                            \
+        du, (const T*)x, mean, rstd, (const T*)g, (const T*)resid, (T*)dx, pg, pb, n, h,    \
+        rows);                                                                              \
     break;
-  c.before(KK_LN_BWD, (double)n * h * (3.0 * sizeof(T) + 4.0) + 8.0 * n);
   switch (vpt) {
-    LN_BWD_CASE(1)
-    LN_BWD_CASE(2)
-    LN_BWD_CASE(4)
-    LN_BWD_CASE(8)
+    LN_BWD_CASE(1, 4)
+    LN_BWD_CASE(2, 2)
+    LN_BWD_CASE(4, 1)
+    LN_BWD_CASE(8, 1)
     default:
       return cudaErrorInvalidValue;
   }
