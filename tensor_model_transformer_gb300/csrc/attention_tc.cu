@@ -29,7 +29,8 @@
 namespace mtl {
 namespace attn {
 
-constexpr int THREADS = 192;
+constexpr int THREADS = 192;       // forward kernel
+constexpr int BWD_THREADS = 384;   // backward kernels: two warpgroups of row threads
 constexpr int ATOM128 = 128 * 128;   // [128 rows][64 bf16]
 constexpr int ATOM64 = 64 * 128;     // [64 rows][64 bf16]
 constexpr int BWD_STAGES = 3;      // TMA ring depth of the backward kernels
@@ -284,12 +285,14 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // ============================================================================ dQ
-// Per CTA: 128 queries; K/V blocks of 64 keys, double-buffered.  Also writes
-// D_i = sum_c dO_ic O_ic for the dK/dV kernel.
-// smem: Q, dO (NA atoms of 16 KB), K[2], V[2] (NA atoms of 8 KB), dS (1 atom,
-// 16 KB).  TMEM: S cols 0..63, dP 64..127, dQ 128..128+d.
+// Per CTA: 128 queries; K/V blocks of 64 keys in a BWD_STAGES-deep ring.  S and
+// dP are double-buffered in TMEM so the MMAs of block j+2 run while the row
+// threads work on block j; two warpgroups of row threads each take 32 of the 64
+// key columns.  Also writes D_i = sum_c dO_ic O_ic for the dK/dV kernel.
+// smem: Q, dO (NA atoms of 16 KB), K[ST], V[ST] (NA atoms of 8 KB), dS (1 atom
+// of 16 KB).  TMEM: S[b] cols 64b, dP[b] cols 128+64b, dQ cols 256..256+d.
 template <int NA>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(BWD_THREADS, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm128,
                           const __grid_constant__ CUtensorMap tm64,
                           const __grid_constant__ CUtensorMap tmdo128, const Params p) {
@@ -299,13 +302,16 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr int ST = BWD_STAGES;
   const uint32_t sQ = sm.u32, sDO = sQ + T128, sK0 = sQ + 2 * T128, sV0 = sK0 + ST * T64,
                  sDS = sV0 + ST * T64;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm.base + 2 * T128 + 2 * ST * T64 + ATOM128);
+  float* s_dpart = reinterpret_cast<float*>(sm.base + 2 * T128 + 2 * ST * T64 + ATOM128);
+  uint64_t* bars =
+      reinterpret_cast<uint64_t*>(sm.base + 2 * T128 + 2 * ST * T64 + ATOM128 + 1024);
   const uint32_t bar0 = smem_u32(bars);
-  // 0 q/do full, 1..ST kv_full, ST+1..2ST kv_empty, 2ST+1 s_full, 2ST+2 ds_full,
-  // 2ST+3 dq_done
+  // 0 q/do full, 1..ST kv_full, ST+1..2ST kv_empty, 2ST+1..2ST+2 s_full[2],
+  // 2ST+3 ds_full, 2ST+4 dq_done
   auto B = [&](int i) { return bar0 + 8u * i; };
-  const int KVF = 1, KVE = 1 + ST, SF = 1 + 2 * ST, DSF = 2 + 2 * ST, DQD = 3 + 2 * ST;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * ST + 4);
+  const int KVF = 1, KVE = 1 + ST, SF = 1 + 2 * ST, DSF = 3 + 2 * ST, DQD = 4 + 2 * ST;
+  const int NBAR = 5 + 2 * ST;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   int qb, hd, b;
@@ -316,17 +322,17 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2 * ST + 4; ++i) mbar_init(B(i), i == DSF ? 128 : 1);
+    for (int i = 0; i < NBAR; ++i) mbar_init(B(i), i == DSF ? 256 : 1);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_shared();
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 256);
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tDP = tmem + 64, tDQ = tmem + 128;
+  const uint32_t tS = tmem, tDP = tmem + 128, tDQ = tmem + 256;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -356,78 +362,81 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t id_s = idesc_bf16_f32(128, 64, false, false);
       const uint32_t id_dq = idesc_bf16_f32(128, p.d, false, true);
       const int ksteps = p.d / 16;
-      auto issue_s = [&](int j) {
+      // S(j), dP(j) into TMEM buffer j % 2
+      auto issue_s = [&](int j) -> bool {
         const int s = j % ST;
-        for (int kk = 0; kk < ksteps; ++kk)
-          tc_mma_bf16(tS, desc_kmajor(sQ, ATOM128, kk), desc_kmajor(sK0 + s * T64, ATOM64, kk),
-                      id_s, kk > 0);
-        for (int kk = 0; kk < ksteps; ++kk)
-          tc_mma_bf16(tDP, desc_kmajor(sDO, ATOM128, kk), desc_kmajor(sV0 + s * T64, ATOM64, kk),
-                      id_s, kk > 0);
-        tc_commit(B(SF));
-      };
-      bool ok = mbar_wait_bounded(B(0), 0, p.status, abort_flag) &&
-                mbar_wait_bounded(B(KVF), 0, p.status, abort_flag);
-      if (ok) {
+        if (!mbar_wait_bounded(B(KVF + s), (j / ST) & 1, p.status, abort_flag)) return false;
         tc_fence_after();
-        issue_s(0);
-      }
+        const uint32_t bo = (j & 1) * 64;
+        for (int kk = 0; kk < ksteps; ++kk)
+          tc_mma_bf16(tS + bo, desc_kmajor(sQ, ATOM128, kk), desc_kmajor(sK0 + s * T64, ATOM64, kk),
+                      id_s, kk > 0);
+        for (int kk = 0; kk < ksteps; ++kk)
+          tc_mma_bf16(tDP + bo, desc_kmajor(sDO, ATOM128, kk),
+                      desc_kmajor(sV0 + s * T64, ATOM64, kk), id_s, kk > 0);
+        tc_commit(B(SF + (j & 1)));
+        return true;
+      };
+      bool ok = mbar_wait_bounded(B(0), 0, p.status, abort_flag);
+      if (ok) ok = issue_s(0);
+      if (ok && nkv > 1) ok = issue_s(1);
       for (int j = 0; j < nkv && ok; ++j) {
+        // row threads wrote dS(j) and are done reading buffer j % 2
         if (!mbar_wait_bounded(B(DSF), j & 1, p.status, abort_flag)) break;
         tc_fence_after();
-        if (j + 1 < nkv) {
-          if (!mbar_wait_bounded(B(KVF + (j + 1) % ST), ((j + 1) / ST) & 1, p.status, abort_flag))
-            break;
-          tc_fence_after();
-          issue_s(j + 1);
-        }
         const int s = j % ST;
         for (int kk = 0; kk < 4; ++kk)
           tc_mma_bf16(tDQ, desc_kmajor(sDS, ATOM128, kk), desc_mnmajor(sK0 + s * T64, ATOM64, kk),
                       id_dq, (j > 0 || kk > 0) ? 1u : 0u);
         tc_commit(B(KVE + s));
         tc_commit(B(DQD));
+        if (j + 2 < nkv && !issue_s(j + 2)) break;
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp >= 4) {
+    const int wg = (warp - 4) >> 2;                 // column half of the 64 keys
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    // D_r = dO_r . O_r and the row's lse (log2 units)
+    // D_r = dO_r . O_r: each warpgroup sums half of the channels
     const size_t orow = (size_t)(row0 + r) * p.h + (size_t)hd * p.d;
-    float Dr = 0.f;
-    for (int c = 0; c < p.d; c += 8) {
+    const int half = p.d / 2;
+    float Dp = 0.f;
+    for (int c = wg * half; c < (wg + 1) * half; c += 8) {
       const uint4 go = *reinterpret_cast<const uint4*>(p.dctx + orow + c);
       const uint4 oo = *reinterpret_cast<const uint4*>(p.ctx + orow + c);
       const bf16* g = reinterpret_cast<const bf16*>(&go);
       const bf16* o = reinterpret_cast<const bf16*>(&oo);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) Dr = fmaf(__bfloat162float(g[e]), __bfloat162float(o[e]), Dr);
+      for (int e = 0; e < 8; ++e) Dp = fmaf(__bfloat162float(g[e]), __bfloat162float(o[e]), Dp);
     }
+    s_dpart[wg * 128 + r] = Dp;
+    named_bar_sync(1, 256);   // all 256 row threads reach this before any wait
+    const float Dr = s_dpart[r] + s_dpart[128 + r];
     const size_t lrow = ((size_t)b * p.heads + hd) * p.seq + qb * 128 + r;
-    p.dsum[lrow] = Dr;
+    if (wg == 0) p.dsum[lrow] = Dr;
     const float lse2 = p.lse[lrow] * LOG2E;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
-      if (!mbar_wait_bounded(B(SF), j & 1, p.status, abort_flag)) {
+      if (!mbar_wait_bounded(B(SF + (j & 1)), (j >> 1) & 1, p.status, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float ds[64];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      const uint32_t col = (j & 1) * 64 + wg * 32;
+      float ds[32];
+      {
         uint32_t sv[32], dv[32];
-        tmem_ld32(tS + lane_off + c * 32, sv);
-        tmem_ld32(tDP + lane_off + c * 32, dv);
+        tmem_ld32(tS + lane_off + col, sv);
+        tmem_ld32(tDP + lane_off + col, dv);
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const int key = j * 64 + c * 32 + i;   // key index within the sequence block origin
+          const int key = j * 64 + wg * 32 + i;
           float pr = fast_exp2(__uint_as_float(sv[i]) * p.scale_log2 - lse2);
           if (key > qb * 128 + r) pr = 0.f;
-          ds[c * 32 + i] = pr * (__uint_as_float(dv[i]) - Dr);
+          ds[i] = pr * (__uint_as_float(dv[i]) - Dr);
         }
       }
       if (j > 0) {
@@ -437,9 +446,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < 4; ++c) {
         const int k = c * 8;
-        st_shared_v4(sDS + sw128_offset(r, c), pack_bf16x2(ds[k], ds[k + 1]),
+        st_shared_v4(sDS + sw128_offset(r, wg * 4 + c), pack_bf16x2(ds[k], ds[k + 1]),
                      pack_bf16x2(ds[k + 2], ds[k + 3]), pack_bf16x2(ds[k + 4], ds[k + 5]),
                      pack_bf16x2(ds[k + 6], ds[k + 7]));
       }
@@ -447,7 +456,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_before();
       mbar_arrive(B(DSF));
     }
-    if (ok && mbar_wait_bounded(B(DQD), (nkv - 1) & 1, p.status, abort_flag)) {
+    if (wg == 0 && ok && mbar_wait_bounded(B(DQD), (nkv - 1) & 1, p.status, abort_flag)) {
       tc_fence_after();
       bf16* dq = p.dqkv + (size_t)(row0 + r) * 3 * p.h + colq;
       for (int c = 0; c < p.d; c += 32) {
@@ -475,17 +484,19 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 
 // ============================================================================ dK, dV
-// Per CTA: 128 keys; query blocks of 64 from the diagonal on, double-buffered.
-// smem: K, V (NA atoms of 16 KB), Q[2], dO[2] (NA atoms of 8 KB), P^T and dS^T
-// (1 atom of 16 KB each).  TMEM: S^T cols 0..63, dP^T 64..127, dV 128..255,
-// dK 256..383.
+// Per CTA: 128 keys; query blocks of 64 from the diagonal on, in a
+// BWD_STAGES-deep ring.  S^T and dP^T are double-buffered in TMEM; two
+// warpgroups of row threads each take 32 of the 64 query columns.
+// smem: K, V (NA atoms of 16 KB), Q[ST], dO[ST] (NA atoms of 8 KB), P^T and dS^T
+// (1 atom of 16 KB each), lse / D per stage.  TMEM: S^T[b] cols 64b, dP^T[b]
+// cols 128+64b, dV 256.., dK 384..
 template <int NA>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(BWD_THREADS, 1)
     attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm128,
                            const __grid_constant__ CUtensorMap tm64,
                            const __grid_constant__ CUtensorMap tmdo64, const Params p) {
@@ -502,11 +513,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm.base + 2 * T128 + 2 * ST * T64 + 2 * ATOM128 +
                                                512 * ST);
   const uint32_t bar0 = smem_u32(bars);
-  // 0 kv_full, 1..ST qdo_full, ST+1..2ST qdo_empty, 2ST+1 st_full, 2ST+2 pt_full,
-  // 2ST+3 mm_done
+  // 0 kv_full, 1..ST qdo_full, ST+1..2ST qdo_empty, 2ST+1..2ST+2 st_full[2],
+  // 2ST+3 pt_full, 2ST+4 mm_done
   auto B = [&](int i) { return bar0 + 8u * i; };
-  const int QF = 1, QE = 1 + ST, STF = 1 + 2 * ST, PTF = 2 + 2 * ST, MMD = 3 + 2 * ST;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * ST + 4);
+  const int QF = 1, QE = 1 + ST, STF = 1 + 2 * ST, PTF = 3 + 2 * ST, MMD = 4 + 2 * ST;
+  const int NBAR = 5 + 2 * ST;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   int kb, hd, b;
@@ -518,7 +530,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2 * ST + 4; ++i) mbar_init(B(i), i == PTF ? 128 : 1);
+    for (int i = 0; i < NBAR; ++i) mbar_init(B(i), i == PTF ? 256 : 1);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_shared();
@@ -528,7 +540,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tST = tmem, tDPT = tmem + 64, tDV = tmem + 128, tDK = tmem + 256;
+  const uint32_t tST = tmem, tDPT = tmem + 128, tDV = tmem + 256, tDK = tmem + 384;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -560,31 +572,28 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t id_st = idesc_bf16_f32(128, 64, false, false);
       const uint32_t id_acc = idesc_bf16_f32(128, p.d, false, true);
       const int ksteps = p.d / 16;
-      auto issue_st = [&](int i) {
+      // S^T(i), dP^T(i) into TMEM buffer i % 2
+      auto issue_st = [&](int i) -> bool {
         const int s = i % ST;
-        for (int kk = 0; kk < ksteps; ++kk)
-          tc_mma_bf16(tST, desc_kmajor(sK, ATOM128, kk), desc_kmajor(sQ0 + s * T64, ATOM64, kk),
-                      id_st, kk > 0);
-        for (int kk = 0; kk < ksteps; ++kk)
-          tc_mma_bf16(tDPT, desc_kmajor(sV, ATOM128, kk), desc_kmajor(sDO0 + s * T64, ATOM64, kk),
-                      id_st, kk > 0);
-        tc_commit(B(STF));
-      };
-      bool ok = mbar_wait_bounded(B(0), 0, p.status, abort_flag) &&
-                mbar_wait_bounded(B(QF), 0, p.status, abort_flag);
-      if (ok) {
+        if (!mbar_wait_bounded(B(QF + s), (i / ST) & 1, p.status, abort_flag)) return false;
         tc_fence_after();
-        issue_st(0);
-      }
+        const uint32_t bo = (i & 1) * 64;
+        for (int kk = 0; kk < ksteps; ++kk)
+          tc_mma_bf16(tST + bo, desc_kmajor(sK, ATOM128, kk),
+                      desc_kmajor(sQ0 + s * T64, ATOM64, kk), id_st, kk > 0);
+        for (int kk = 0; kk < ksteps; ++kk)
+          tc_mma_bf16(tDPT + bo, desc_kmajor(sV, ATOM128, kk),
+                      desc_kmajor(sDO0 + s * T64, ATOM64, kk), id_st, kk > 0);
+        tc_commit(B(STF + (i & 1)));
+        return true;
+      };
+      bool ok = mbar_wait_bounded(B(0), 0, p.status, abort_flag);
+      if (ok) ok = issue_st(0);
+      if (ok && nq > 1) ok = issue_st(1);
       for (int i = 0; i < nq && ok; ++i) {
+        // row threads wrote P^T(i), dS^T(i) and are done reading buffer i % 2
         if (!mbar_wait_bounded(B(PTF), i & 1, p.status, abort_flag)) break;
         tc_fence_after();
-        if (i + 1 < nq) {
-          if (!mbar_wait_bounded(B(QF + (i + 1) % ST), ((i + 1) / ST) & 1, p.status, abort_flag))
-            break;
-          tc_fence_after();
-          issue_st(i + 1);
-        }
         const int s = i % ST;
         for (int kk = 0; kk < 4; ++kk)
           tc_mma_bf16(tDV, desc_kmajor(sPT, ATOM128, kk), desc_mnmajor(sDO0 + s * T64, ATOM64, kk),
@@ -594,45 +603,46 @@ __global__ void __launch_bounds__(THREADS, 1)
                       id_acc, (i > 0 || kk > 0) ? 1u : 0u);
         tc_commit(B(QE + s));
         tc_commit(B(MMD));
+        if (i + 2 < nq && !issue_st(i + 2)) break;
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp >= 4) {
+    const int wg = (warp - 4) >> 2;   // column half of the 64 queries
     const int q4 = warp & 3;
-    const int r = q4 * 32 + lane;   // key row
+    const int r = q4 * 32 + lane;     // key row
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const int key = kb * 128 + r;
     bool ok = true;
     for (int i = 0; i < nq; ++i) {
-      if (!mbar_wait_bounded(B(STF), i & 1, p.status, abort_flag)) {
+      if (!mbar_wait_bounded(B(STF + (i & 1)), (i >> 1) & 1, p.status, abort_flag)) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      const int q0 = (first + i) * 64;
       // lse / D of this block arrive with its Q / dO tiles: observe that
-      // barrier's phase too (stage i&1 is not refilled before this iteration
-      // ends: its release waits for the MMAs that follow our arrival below)
+      // barrier's phase too (stage i % ST is not refilled before this
+      // iteration ends: its release follows our arrival below)
       if (!mbar_wait_bounded(B(QF + i % ST), (i / ST) & 1, p.status, abort_flag)) {
         ok = false;
         break;
       }
-      const float* s_lse = s_lse0 + (i % ST) * 64;
-      const float* s_d = s_d0 + (i % ST) * 64;
-      float pt[64], dst[64];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      tc_fence_after();
+      const int q0 = (first + i) * 64 + wg * 32;
+      const float* s_lse = s_lse0 + (i % ST) * 64 + wg * 32;
+      const float* s_d = s_d0 + (i % ST) * 64 + wg * 32;
+      const uint32_t col = (i & 1) * 64 + wg * 32;
+      float pt[32], dst[32];
+      {
         uint32_t sv[32], dv[32];
-        tmem_ld32(tST + lane_off + c * 32, sv);
-        tmem_ld32(tDPT + lane_off + c * 32, dv);
+        tmem_ld32(tST + lane_off + col, sv);
+        tmem_ld32(tDPT + lane_off + col, dv);
         tmem_ld_wait();
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const int q = q0 + c * 32 + e;
-          float pr = fast_exp2(__uint_as_float(sv[e]) * p.scale_log2 - s_lse[c * 32 + e] * LOG2E);
-          if (q < key) pr = 0.f;
-          pt[c * 32 + e] = pr;
-          dst[c * 32 + e] = pr * (__uint_as_float(dv[e]) - s_d[c * 32 + e]);
+          float pr = fast_exp2(__uint_as_float(sv[e]) * p.scale_log2 - s_lse[e] * LOG2E);
+          if (q0 + e < key) pr = 0.f;
+          pt[e] = pr;
+          dst[e] = pr * (__uint_as_float(dv[e]) - s_d[e]);
         }
       }
       if (i > 0) {
@@ -642,12 +652,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < 4; ++c) {
         const int k = c * 8;
-        st_shared_v4(sPT + sw128_offset(r, c), pack_bf16x2(pt[k], pt[k + 1]),
+        st_shared_v4(sPT + sw128_offset(r, wg * 4 + c), pack_bf16x2(pt[k], pt[k + 1]),
                      pack_bf16x2(pt[k + 2], pt[k + 3]), pack_bf16x2(pt[k + 4], pt[k + 5]),
                      pack_bf16x2(pt[k + 6], pt[k + 7]));
-        st_shared_v4(sDST + sw128_offset(r, c), pack_bf16x2(dst[k], dst[k + 1]),
+        st_shared_v4(sDST + sw128_offset(r, wg * 4 + c), pack_bf16x2(dst[k], dst[k + 1]),
                      pack_bf16x2(dst[k + 2], dst[k + 3]), pack_bf16x2(dst[k + 4], dst[k + 5]),
                      pack_bf16x2(dst[k + 6], dst[k + 7]));
       }
@@ -657,24 +667,23 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     if (ok && mbar_wait_bounded(B(MMD), (nq - 1) & 1, p.status, abort_flag)) {
       tc_fence_after();
+      // warpgroup 0 writes dK (scaled), warpgroup 1 writes dV
       bf16* out = p.dqkv + (size_t)(krow0 + r) * 3 * p.h + colq;
-      for (int which = 0; which < 2; ++which) {   // 0: dK (scaled), 1: dV
-        const uint32_t tsrc = which == 0 ? tDK : tDV;
-        const float sc = which == 0 ? p.scale : 1.0f;
-        bf16* dst_row = out + (which == 0 ? p.d : 2 * p.d);
-        for (int c = 0; c < p.d; c += 32) {
-          uint32_t v[32];
-          tmem_ld32(tsrc + lane_off + c, v);
-          tmem_ld_wait();
+      const uint32_t tsrc = wg == 0 ? tDK : tDV;
+      const float sc = wg == 0 ? p.scale : 1.0f;
+      bf16* dst_row = out + (wg == 0 ? p.d : 2 * p.d);
+      for (int c = 0; c < p.d; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(tsrc + lane_off + c, v);
+        tmem_ld_wait();
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 u;
-            u.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]) * sc, __uint_as_float(v[q * 8 + 1]) * sc);
-            u.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]) * sc, __uint_as_float(v[q * 8 + 3]) * sc);
-            u.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]) * sc, __uint_as_float(v[q * 8 + 5]) * sc);
-            u.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]) * sc, __uint_as_float(v[q * 8 + 7]) * sc);
-            *reinterpret_cast<uint4*>(dst_row + c + q * 8) = u;
-          }
+        for (int q = 0; q < 4; ++q) {
+          uint4 u;
+          u.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]) * sc, __uint_as_float(v[q * 8 + 1]) * sc);
+          u.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]) * sc, __uint_as_float(v[q * 8 + 3]) * sc);
+          u.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]) * sc, __uint_as_float(v[q * 8 + 5]) * sc);
+          u.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]) * sc, __uint_as_float(v[q * 8 + 7]) * sc);
+          *reinterpret_cast<uint4*>(dst_row + c + q * 8) = u;
         }
       }
     }
@@ -720,11 +729,13 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uin
 }
 
 size_t fwd_smem(int na) { return (size_t)5 * na * ATOM128 + 2 * ATOM128 + 256 + 1024; }
+// The backward kernels hold all 512 TMEM columns: their shared memory requests
+// keep them at one CTA per SM so a second CTA never waits in tcgen05.alloc.
 size_t dq_smem(int na) {
-  return (size_t)2 * na * ATOM128 + 2 * BWD_STAGES * na * ATOM64 + ATOM128 + 256 + 1024;
+  const size_t need =
+      (size_t)2 * na * ATOM128 + 2 * BWD_STAGES * na * ATOM64 + ATOM128 + 1024 + 256 + 1024;
+  return need < 120 * 1024 ? 120 * 1024 : need;
 }
-// The dK/dV kernel holds all 512 TMEM columns: its shared memory request keeps
-// it at one CTA per SM so a second CTA never waits in tcgen05.alloc.
 size_t dkv_smem(int na) {
   const size_t need = (size_t)2 * na * ATOM128 + 2 * BWD_STAGES * na * ATOM64 + 2 * ATOM128 +
                       512 * BWD_STAGES + 256 + 1024;
@@ -812,21 +823,21 @@ cudaError_t attn_bwd_tc(const void* qkv, const void* ctx, const float* lse, cons
     if ((e = set_smem(attn_bwd_dq_tc_kernel<1>, dq_smem(1))) != cudaSuccess) return e;
     if ((e = set_smem(attn_bwd_dkv_tc_kernel<1>, dkv_smem(1))) != cudaSuccess) return e;
     c.before(KK_ATTN_BWD, 2.0 * 3.0 * tri);
-    attn_bwd_dq_tc_kernel<1><<<grid, THREADS, dq_smem(1), c.stream>>>(tm128, tm64, tmdo128, p);
+    attn_bwd_dq_tc_kernel<1><<<grid, BWD_THREADS, dq_smem(1), c.stream>>>(tm128, tm64, tmdo128, p);
     c.after();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     c.before(KK_ATTN_BWD, 2.0 * 4.0 * tri);
-    attn_bwd_dkv_tc_kernel<1><<<grid, THREADS, dkv_smem(1), c.stream>>>(tm128, tm64, tmdo64, p);
+    attn_bwd_dkv_tc_kernel<1><<<grid, BWD_THREADS, dkv_smem(1), c.stream>>>(tm128, tm64, tmdo64, p);
     c.after();
   } else {
     if ((e = set_smem(attn_bwd_dq_tc_kernel<2>, dq_smem(2))) != cudaSuccess) return e;
     if ((e = set_smem(attn_bwd_dkv_tc_kernel<2>, dkv_smem(2))) != cudaSuccess) return e;
     c.before(KK_ATTN_BWD, 2.0 * 3.0 * tri);
-    attn_bwd_dq_tc_kernel<2><<<grid, THREADS, dq_smem(2), c.stream>>>(tm128, tm64, tmdo128, p);
+    attn_bwd_dq_tc_kernel<2><<<grid, BWD_THREADS, dq_smem(2), c.stream>>>(tm128, tm64, tmdo128, p);
     c.after();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     c.before(KK_ATTN_BWD, 2.0 * 4.0 * tri);
-    attn_bwd_dkv_tc_kernel<2><<<grid, THREADS, dkv_smem(2), c.stream>>>(tm128, tm64, tmdo64, p);
+    attn_bwd_dkv_tc_kernel<2><<<grid, BWD_THREADS, dkv_smem(2), c.stream>>>(tm128, tm64, tmdo64, p);
     c.after();
   }
   return cudaGetLastError();
