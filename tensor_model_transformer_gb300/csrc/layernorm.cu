@@ -232,14 +232,28 @@ __global__ void __launch_bounds__(kLnThreadsMax)
   }
 }
 
-// out[c] = sum over row blocks b = 0..nblk-1 of part[b*N + c]
-__global__ void finalize_cols_kernel(const float* __restrict__ part, int nblk, int N,
-                                     float* __restrict__ out) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= N) return;
+// out[c] = sum over row blocks b = 0..nblk-1 of part[b*N + c].  One CTA per
+// 32 columns: warp w sums the row blocks w, w+8, w+16, ... (coalesced 128-byte
+// rows), then the 8 warp sums are added in warp order: a fixed order for any
+// launch.
+constexpr int kFinWarps = 8;
+__global__ void __launch_bounds__(kFinWarps * 32)
+    finalize_cols_kernel(const float* __restrict__ part, int nblk, int N,
+                         float* __restrict__ out) {
+  __shared__ float red[kFinWarps][33];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c = blockIdx.x * 32 + lane;
   float s = 0.f;
-  for (int b = 0; b < nblk; ++b) s += part[(size_t)b * N + c];
-  out[c] = s;
+  if (c < N)
+    for (int b = warp; b < nblk; b += kFinWarps) s += part[(size_t)b * N + c];
+  red[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0 && c < N) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < kFinWarps; ++w) t += red[w][lane];
+    out[c] = t;
+  }
 }
 
 template <typename T>
@@ -337,10 +351,10 @@ cudaError_t ln_bwd_t(const float* du, const void* x, const float* mean, const fl
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   c.before(KK_FINALIZE, 4.0 * nblk * h);
-  finalize_cols_kernel<<<(h + 255) / 256, 256, 0, c.stream>>>(pg, nblk, h, dgamma);
+  finalize_cols_kernel<<<(h + 31) / 32, kFinWarps * 32, 0, c.stream>>>(pg, nblk, h, dgamma);
   c.after();
   c.before(KK_FINALIZE, 4.0 * nblk * h);
-  finalize_cols_kernel<<<(h + 255) / 256, 256, 0, c.stream>>>(pb, nblk, h, dbeta);
+  finalize_cols_kernel<<<(h + 31) / 32, kFinWarps * 32, 0, c.stream>>>(pb, nblk, h, dbeta);
   c.after();
   return cudaGetLastError();
 }
@@ -357,7 +371,7 @@ cudaError_t colsum_t(const void* Y, int64_t ld, int n, int N, float* out, float*
   colsum_partial_kernel<T><<<grid, threads, 0, c.stream>>>((const T*)Y, ld, n, N, rows, partial);
   c.after();
   c.before(KK_FINALIZE, 4.0 * nblk * N);
-  finalize_cols_kernel<<<(N + 255) / 256, 256, 0, c.stream>>>(partial, nblk, N, out);
+  finalize_cols_kernel<<<(N + 31) / 32, kFinWarps * 32, 0, c.stream>>>(partial, nblk, N, out);
   c.after();
   return cudaGetLastError();
 }
