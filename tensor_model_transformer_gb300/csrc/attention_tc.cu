@@ -29,7 +29,7 @@
 namespace mtl {
 namespace attn {
 
-constexpr int THREADS = 192;       // forward kernel
+constexpr int FWD_THREADS = 384;   // forward kernel: two warpgroups of row threads
 constexpr int BWD_THREADS = 384;   // backward kernels: two warpgroups of row threads
 constexpr int ATOM128 = 128 * 128;   // [128 rows][64 bf16]
 constexpr int ATOM64 = 64 * 128;     // [64 rows][64 bf16]
@@ -73,61 +73,98 @@ __device__ __forceinline__ void block_coords(const Params& p, int nblk, bool des
   b = pair / p.heads;
 }
 
+// Work item -> (row block, head, batch) for the persistent kernels.  Items go
+// (batch, head)-major, so the items running at once on all SMs cover few pairs
+// and reuse each other's K/V from L2; within a pair the row block index is
+// rotated by the pair index, so a CTA that takes every gridDim-th item meets
+// every row block (and so every amount of causal work) in turn.
+__device__ __forceinline__ void item_coords(const Params& p, int item, bool desc, int& blk,
+                                            int& hd, int& b) {
+  const int pair = item / p.nqb;
+  const int i = (item % p.nqb + pair) % p.nqb;
+  blk = desc ? (p.nqb - 1 - i) : i;
+  hd = pair % p.heads;
+  b = pair / p.heads;
+}
+
 // ============================================================================ forward
-// Per CTA: 128 queries; K/V blocks of 128 keys, double-buffered.
-// smem: Q, K[2], V[2] (NA atoms of 16 KB each), P (2 atoms).  TMEM: S cols
-// 0..127, O cols 128..128+d.
+// Persistent: one CTA per SM walks the (row block, head, batch) work items in
+// item_coords order.  Per item: 128 queries; K/V blocks of 128 keys in a
+// double-buffered ring that runs on across items.  S is double-buffered in
+// TMEM (the MMAs of block j+2 run while the row threads work on block j) and so
+// is O (an item's epilogue overlaps the next item's first MMAs).  Two
+// warpgroups of row threads each take 64 of the 128 key columns; they combine
+// their row maxima through shared memory behind an mbarrier.
+// smem: Q, K[2], V[2] (NA atoms of 16 KB each), P (2 atoms), row-max and row-sum
+// exchange.  TMEM: S[b] cols 128b, O[b] cols 256+128b.
 template <int NA>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(FWD_THREADS, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const Smem sm = smem_aligned(smem_raw);
   constexpr uint32_t TILE = NA * ATOM128;
   const uint32_t sQ = sm.u32, sK0 = sQ + TILE, sV0 = sQ + 3 * TILE, sP = sQ + 5 * TILE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm.base + 5 * TILE + 2 * ATOM128);
+  float* s_mx = reinterpret_cast<float*>(sm.base + 5 * TILE + 2 * ATOM128);  // [2][2][128]
+  float* s_l = s_mx + 512;                                                   // [2][128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm.base + 5 * TILE + 2 * ATOM128 + 3072);
   const uint32_t bar0 = smem_u32(bars);
-  // 0 q_full, 1-2 k_full, 3-4 k_empty, 5-6 v_full, 7-8 v_empty, 9 s_full, 10 p_full, 11 o_done
   auto B = [&](int i) { return bar0 + 8u * i; };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  // barriers
+  constexpr int QFULL = 0, QEMPTY = 1, KFULL = 2, KEMPTY = 4, VFULL = 6, VEMPTY = 8, SFULL = 10,
+                PFULL = 12, ODONE = 13, OFREE = 14, MXB = 16, LXB = 17, NBAR = 18;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  int qb, hd, b;
-  block_coords(p, p.nqb, true, qb, hd, b);
-  const int nkv = qb + 1;
-  const int row0 = b * p.seq + qb * 128;
-  const int colq = hd * 3 * p.d;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_items = p.nqb * p.heads * p.batch;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 12; ++i) mbar_init(B(i), i == 10 ? 128 : 1);
+    for (int i = 0; i < NBAR; ++i) {
+      const bool rows = i == PFULL || i == OFREE || i == OFREE + 1 || i == MXB || i == LXB;
+      mbar_init(B(i), rows ? 256 : 1);
+    }
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_shared();
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 256);
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tO = tmem + 128;
 
   if (warp == 0) {
     if (lane == 0) {
       tma_prefetch_desc(&tm);
-      mbar_arrive_expect_tx(B(0), TILE);
-      for (int a = 0; a < NA; ++a) tma_load_2d(sQ + a * ATOM128, &tm, B(0), colq + 64 * a, row0);
-      for (int j = 0; j < nkv; ++j) {
-        const int s = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        const int krow = b * p.seq + j * 128;
-        if (!mbar_wait_bounded(B(3 + s), ph ^ 1u, p.status, abort_flag)) break;
-        mbar_arrive_expect_tx(B(1 + s), TILE);
+      int g = 0, n = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n) {
+        int qb, hd, b;
+        item_coords(p, item, true, qb, hd, b);
+        const int colq = hd * 3 * p.d;
+        if (!mbar_wait_bounded(B(QEMPTY), (n & 1) ^ 1u, p.status, abort_flag)) break;
+        mbar_arrive_expect_tx(B(QFULL), TILE);
         for (int a = 0; a < NA; ++a)
-          tma_load_2d(sK0 + s * TILE + a * ATOM128, &tm, B(1 + s), colq + p.d + 64 * a, krow);
-        if (!mbar_wait_bounded(B(7 + s), ph ^ 1u, p.status, abort_flag)) break;
-        mbar_arrive_expect_tx(B(5 + s), TILE);
-        for (int a = 0; a < NA; ++a)
-          tma_load_2d(sV0 + s * TILE + a * ATOM128, &tm, B(5 + s), colq + 2 * p.d + 64 * a, krow);
+          tma_load_2d(sQ + a * ATOM128, &tm, B(QFULL), colq + 64 * a, b * p.seq + qb * 128);
+        for (int j = 0; j <= qb; ++j, ++g) {
+          const int s = g & 1;
+          const uint32_t ph = (g >> 1) & 1;
+          const int krow = b * p.seq + j * 128;
+          if (!mbar_wait_bounded(B(KEMPTY + s), ph ^ 1u, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(B(KFULL + s), TILE);
+          for (int a = 0; a < NA; ++a)
+            tma_load_2d(sK0 + s * TILE + a * ATOM128, &tm, B(KFULL + s), colq + p.d + 64 * a, krow);
+          if (!mbar_wait_bounded(B(VEMPTY + s), ph ^ 1u, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(B(VFULL + s), TILE);
+          for (int a = 0; a < NA; ++a)
+            tma_load_2d(sV0 + s * TILE + a * ATOM128, &tm, B(VFULL + s), colq + 2 * p.d + 64 * a,
+                        krow);
+        }
       }
     }
     __syncwarp();
@@ -136,125 +173,171 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);
       const uint32_t id_pv = idesc_bf16_f32(128, p.d, false, true);
       const int ksteps = p.d / 16;
-      bool ok = mbar_wait_bounded(B(0), 0, p.status, abort_flag) &&
-                mbar_wait_bounded(B(1), 0, p.status, abort_flag);
-      if (ok) {
+      int gb = 0, n = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n) {
+        int qb, hd, b;
+        item_coords(p, item, true, qb, hd, b);
+        const int nkv = qb + 1;
+        if (!mbar_wait_bounded(B(QFULL), n & 1, p.status, abort_flag)) break;
         tc_fence_after();
-        for (int kk = 0; kk < ksteps; ++kk)
-          tc_mma_bf16(tS, desc_kmajor(sQ, ATOM128, kk), desc_kmajor(sK0, ATOM128, kk), id_qk,
-                      kk > 0);
-        tc_commit(B(3));
-        tc_commit(B(9));
-      }
-      for (int j = 0; j < nkv && ok; ++j) {
-        if (!mbar_wait_bounded(B(10), j & 1, p.status, abort_flag)) break;
-        tc_fence_after();
-        if (j + 1 < nkv) {
-          const int s1 = (j + 1) & 1;
-          if (!mbar_wait_bounded(B(1 + s1), ((j + 1) >> 1) & 1, p.status, abort_flag)) break;
+        // S(block gg) = Q K(gg)^T into S buffer gg % 2
+        auto issue_qk = [&](int j) -> bool {
+          const int gg = gb + j, s = gg & 1;
+          if (!mbar_wait_bounded(B(KFULL + s), (gg >> 1) & 1, p.status, abort_flag)) return false;
           tc_fence_after();
           for (int kk = 0; kk < ksteps; ++kk)
-            tc_mma_bf16(tS, desc_kmajor(sQ, ATOM128, kk), desc_kmajor(sK0 + s1 * TILE, ATOM128, kk),
-                        id_qk, kk > 0);
-          tc_commit(B(3 + s1));
-          tc_commit(B(9));
+            tc_mma_bf16(tmem + 128 * s, desc_kmajor(sQ, ATOM128, kk),
+                        desc_kmajor(sK0 + s * TILE, ATOM128, kk), id_qk, kk > 0);
+          tc_commit(B(KEMPTY + s));
+          tc_commit(B(SFULL + s));
+          if (j == nkv - 1) tc_commit(B(QEMPTY));
+          return true;
+        };
+        ok = issue_qk(0) && (nkv < 2 || issue_qk(1));
+        const uint32_t tO = tmem + 256 + 128 * (n & 1);
+        for (int j = 0; j < nkv && ok; ++j) {
+          const int gg = gb + j, s = gg & 1;
+          if (!mbar_wait_bounded(B(PFULL), gg & 1, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (j == 0 &&
+              !mbar_wait_bounded(B(OFREE + (n & 1)), ((n >> 1) & 1) ^ 1u, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (!mbar_wait_bounded(B(VFULL + s), (gg >> 1) & 1, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int kk = 0; kk < 8; ++kk)
+            tc_mma_bf16(tO, desc_kmajor(sP, ATOM128, kk), desc_mnmajor(sV0 + s * TILE, ATOM128, kk),
+                        id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(B(VEMPTY + s));
+          tc_commit(B(ODONE));
+          if (j + 2 < nkv && !issue_qk(j + 2)) ok = false;
         }
-        const int s = j & 1;
-        if (!mbar_wait_bounded(B(5 + s), (j >> 1) & 1, p.status, abort_flag)) break;
-        tc_fence_after();
-        for (int kk = 0; kk < 8; ++kk)
-          tc_mma_bf16(tO, desc_kmajor(sP, ATOM128, kk), desc_mnmajor(sV0 + s * TILE, ATOM128, kk),
-                      id_pv, (j > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(B(7 + s));
-        tc_commit(B(11));
+        gb += nkv;
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp >= 4) {
+    const int wg = (warp - 4) >> 2;   // key columns [64 wg, 64 wg + 64) of S
     const int q4 = warp & 3;
-    const int r = q4 * 32 + lane;                       // row in the block = TMEM lane
+    const int r = q4 * 32 + lane;     // row = TMEM lane
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    float m_used = -INFINITY, l = 0.f;
+    int gb = 0, n = 0;
     bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      if (!mbar_wait_bounded(B(9), j & 1, p.status, abort_flag)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float s[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tS + lane_off + c * 32, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]) * p.scale_log2;
-      }
-      if (j == qb) {
-#pragma unroll
-        for (int k = 0; k < 128; ++k)
-          if (k > r) s[k] = -INFINITY;
-      }
-      // 8 independent partial maxima / sums keep the dependent chains short
-      float mxp[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) mxp[q] = s[q];
-#pragma unroll
-      for (int k = 8; k < 128; ++k) mxp[k & 7] = fmaxf(mxp[k & 7], s[k]);
-      const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
-                             fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
-      const float m_new = fmaxf(m_used, mx);
-      // Rescale only when the running maximum grew by more than 2^8: the
-      // exponentials stay below 256 and the final O / l is exact either way.
-      const bool resc = m_new > m_used + 8.0f;
-      const float alpha = resc ? fast_exp2(m_used - m_new) : 1.0f;
-      if (resc) m_used = m_new;
-      float rsp[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) rsp[q] = 0.f;
-#pragma unroll
-      for (int k = 0; k < 128; ++k) {
-        s[k] = fast_exp2(s[k] - m_used);
-        rsp[k & 7] += s[k];
-      }
-      const float rs = ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
-      l = l * alpha + rs;
-      if (j > 0) {
-        if (!mbar_wait_bounded(B(11), (j - 1) & 1, p.status, abort_flag)) {
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n) {
+      int qb, hd, b;
+      item_coords(p, item, true, qb, hd, b);
+      const int nkv = qb + 1;
+      const uint32_t tO = tmem + 256 + 128 * (n & 1);
+      float m_used = -INFINITY, l = 0.f;
+      for (int j = 0; j < nkv; ++j) {
+        const int gg = gb + j;
+        if (!mbar_wait_bounded(B(SFULL + (gg & 1)), (gg >> 1) & 1, p.status, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, resc)) {
-          for (int c = 0; c < p.d; c += 32) {
-            uint32_t v[32];
-            tmem_ld32(tO + lane_off + c, v);
-            tmem_ld_wait();
+        float s[64];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-            tmem_st32(tO + lane_off + c, v);
-          }
-          tmem_st_wait();
+        for (int c = 0; c < 2; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tmem + 128 * (gg & 1) + lane_off + wg * 64 + c * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]) * p.scale_log2;
         }
-      }
-      // P (bf16) -> shared memory, two 64-key boxes
+        if (j == qb) {
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int k = c * 8;
-        const uint32_t addr = sP + (c >> 3) * ATOM128 + sw128_offset(r, c & 7);
-        st_shared_v4(addr, pack_bf16x2(s[k], s[k + 1]), pack_bf16x2(s[k + 2], s[k + 3]),
-                     pack_bf16x2(s[k + 4], s[k + 5]), pack_bf16x2(s[k + 6], s[k + 7]));
+          for (int k = 0; k < 64; ++k)
+            if (wg * 64 + k > r) s[k] = -INFINITY;
+        }
+        float mxp[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) mxp[q] = s[q];
+#pragma unroll
+        for (int k = 8; k < 64; ++k) mxp[k & 7] = fmaxf(mxp[k & 7], s[k]);
+        float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                         fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+        // combine the two halves' maxima (buffer gg % 2; a warpgroup cannot run
+        // two blocks ahead of the other because of this barrier)
+        float* mxs = s_mx + (gg & 1) * 256;
+        mxs[wg * 128 + r] = mx;
+        mbar_arrive(B(MXB));
+        if (!mbar_wait_bounded(B(MXB), gg & 1, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        mx = fmaxf(mxs[r], mxs[128 + r]);
+        const float m_new = fmaxf(m_used, mx);
+        // Rescale only when the running maximum grew by more than 2^8: the
+        // exponentials stay below 256 and the final O / l is exact either way.
+        const bool resc = m_new > m_used + 8.0f;
+        const float alpha = resc ? fast_exp2(m_used - m_new) : 1.0f;
+        if (resc) m_used = m_new;
+        float rsp[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) rsp[q] = 0.f;
+#pragma unroll
+        for (int k = 0; k < 64; ++k) {
+          s[k] = fast_exp2(s[k] - m_used);
+          rsp[k & 7] += s[k];
+        }
+        l = l * alpha + (((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7])));
+        if (j > 0) {
+          if (!mbar_wait_bounded(B(ODONE), (gg - 1) & 1, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, resc)) {
+            for (int c = wg * 32; c < p.d; c += 64) {
+              uint32_t v[32];
+              tmem_ld32(tO + lane_off + c, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+              tmem_st32(tO + lane_off + c, v);
+            }
+            tmem_st_wait();
+          }
+        }
+        // P (bf16) -> shared memory: this half's 64 keys are box `wg`
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int k = c * 8;
+          st_shared_v4(sP + wg * ATOM128 + sw128_offset(r, c), pack_bf16x2(s[k], s[k + 1]),
+                       pack_bf16x2(s[k + 2], s[k + 3]), pack_bf16x2(s[k + 4], s[k + 5]),
+                       pack_bf16x2(s[k + 6], s[k + 7]));
+        }
+        fence_proxy_async_shared();
+        tc_fence_before();
+        mbar_arrive(B(PFULL));
       }
-      fence_proxy_async_shared();
-      tc_fence_before();
-      mbar_arrive(B(10));
-    }
-    if (ok && mbar_wait_bounded(B(11), (nkv - 1) & 1, p.status, abort_flag)) {
+      if (!ok) break;
+      if (!mbar_wait_bounded(B(ODONE), (gb + nkv - 1) & 1, p.status, abort_flag)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
-      const float inv = 1.0f / l;
-      bf16* orow = p.ctx + (size_t)(row0 + r) * p.h + (size_t)hd * p.d;
-      for (int c = 0; c < p.d; c += 32) {
+      // row sum = the two halves' partial sums
+      float* ls = s_l;
+      ls[wg * 128 + r] = l;
+      mbar_arrive(B(LXB));
+      if (!mbar_wait_bounded(B(LXB), n & 1, p.status, abort_flag)) {
+        ok = false;
+        break;
+      }
+      const float lt = ls[r] + ls[128 + r];
+      const float inv = 1.0f / lt;
+      const int row = b * p.seq + qb * 128 + r;
+      bf16* orow = p.ctx + (size_t)row * p.h + (size_t)hd * p.d;
+      for (int c = wg * 32; c < p.d; c += 64) {
         uint32_t v[32];
         tmem_ld32(tO + lane_off + c, v);
         tmem_ld_wait();
@@ -268,7 +351,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           *reinterpret_cast<uint4*>(orow + c + q * 8) = u;
         }
       }
-      p.lse[((size_t)b * p.heads + hd) * p.seq + qb * 128 + r] = (m_used + __log2f(l)) * LN2;
+      if (wg == 0)
+        p.lse[((size_t)b * p.heads + hd) * p.seq + qb * 128 + r] = (m_used + __log2f(lt)) * LN2;
+      tc_fence_before();
+      mbar_arrive(B(OFREE + (n & 1)));
+      gb += nkv;
     }
     __syncwarp();
   }
@@ -280,7 +367,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -728,7 +815,10 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uin
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t fwd_smem(int na) { return (size_t)5 * na * ATOM128 + 2 * ATOM128 + 256 + 1024; }
+size_t fwd_smem(int na) {
+  const size_t need = (size_t)5 * na * ATOM128 + 2 * ATOM128 + 3072 + 256 + 1024;
+  return need < 120 * 1024 ? 120 * 1024 : need;   // one CTA per SM (512 TMEM columns)
+}
 // The backward kernels hold all 512 TMEM columns: their shared memory requests
 // keep them at one CTA per SM so a second CTA never waits in tcgen05.alloc.
 size_t dq_smem(int na) {
@@ -780,19 +870,20 @@ cudaError_t attn_fwd_tc(const void* qkv, void* ctx, float* lse, int batch, int s
   Params p = make_params(batch, seq, heads, d, status);
   p.ctx = static_cast<bf16*>(ctx);
   p.lse = lse;
-  const int grid = p.nqb * heads * batch;
+  const int items = p.nqb * heads * batch;
+  const int grid = items < c.num_sms ? items : c.num_sms;
   const double flops = 2.0 * 2.0 * batch * heads * d * ((double)seq * (seq + 1) / 2.0);
   cudaError_t e;
   if (d == 64) {
     const size_t sm = fwd_smem(1);
     if ((e = set_smem(attn_fwd_tc_kernel<1>, sm)) != cudaSuccess) return e;
     c.before(KK_ATTN_FWD, flops);
-    attn_fwd_tc_kernel<1><<<grid, THREADS, sm, c.stream>>>(tm, p);
+    attn_fwd_tc_kernel<1><<<grid, FWD_THREADS, sm, c.stream>>>(tm, p);
   } else {
     const size_t sm = fwd_smem(2);
     if ((e = set_smem(attn_fwd_tc_kernel<2>, sm)) != cudaSuccess) return e;
     c.before(KK_ATTN_FWD, flops);
-    attn_fwd_tc_kernel<2><<<grid, THREADS, sm, c.stream>>>(tm, p);
+    attn_fwd_tc_kernel<2><<<grid, FWD_THREADS, sm, c.stream>>>(tm, p);
   }
   c.after();
   return cudaGetLastError();
