@@ -60,19 +60,6 @@ __device__ __forceinline__ Smem smem_aligned(uint8_t* raw) {
   return {p, smem_u32(p)};
 }
 
-// Block index -> (row block, head, batch).  Consecutive blocks share a
-// (batch, head) pair, so the CTAs running at once reuse each other's K/V (or
-// Q/dO) tiles from L2; inside a pair the row blocks with the most causal work
-// come first (`desc`: high row blocks are heavy; else low ones are).
-__device__ __forceinline__ void block_coords(const Params& p, int nblk, bool desc, int& blk,
-                                             int& hd, int& b) {
-  const int pair = blockIdx.x / nblk;
-  const int i = blockIdx.x % nblk;
-  blk = desc ? (nblk - 1 - i) : i;
-  hd = pair % p.heads;
-  b = pair / p.heads;
-}
-
 // Work item -> (row block, head, batch) for the persistent kernels.  Items go
 // (batch, head)-major, so the items running at once on all SMs cover few pairs
 // and reuse each other's K/V from L2; within a pair the row block index is
@@ -372,12 +359,16 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
 }
 
 // ============================================================================ dQ
-// Per CTA: 128 queries; K/V blocks of 64 keys in a BWD_STAGES-deep ring.  S and
-// dP are double-buffered in TMEM so the MMAs of block j+2 run while the row
-// threads work on block j; two warpgroups of row threads each take 32 of the 64
-// key columns.  Also writes D_i = sum_c dO_ic O_ic for the dK/dV kernel.
+// Persistent: one CTA per SM walks the query-block work items.  Per item: 128
+// queries; K/V blocks of 64 keys in a BWD_STAGES-deep ring that runs on across
+// items.  S and dP are double-buffered in TMEM (the MMAs of block j+2 run while
+// the row threads work on block j), and so is the dQ accumulator (an item's
+// epilogue overlaps the next item's MMAs).  Two warpgroups of row threads each
+// take 32 of the 64 key columns.  Also writes D_i = sum_c dO_ic O_ic for the
+// dK/dV kernel.
 // smem: Q, dO (NA atoms of 16 KB), K[ST], V[ST] (NA atoms of 8 KB), dS (1 atom
-// of 16 KB).  TMEM: S[b] cols 64b, dP[b] cols 128+64b, dQ cols 256..256+d.
+// of 16 KB), D exchange.  TMEM: S[b] cols 64b, dP[b] cols 128+64b, dQ[b] cols
+// 256+128b.
 template <int NA>
 __global__ void __launch_bounds__(BWD_THREADS, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm128,
@@ -391,25 +382,23 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                  sDS = sV0 + ST * T64;
   float* s_dpart = reinterpret_cast<float*>(sm.base + 2 * T128 + 2 * ST * T64 + ATOM128);
   uint64_t* bars =
-      reinterpret_cast<uint64_t*>(sm.base + 2 * T128 + 2 * ST * T64 + ATOM128 + 1024);
+      reinterpret_cast<uint64_t*>(sm.base + 2 * T128 + 2 * ST * T64 + ATOM128 + 2048);
   const uint32_t bar0 = smem_u32(bars);
-  // 0 q/do full, 1..ST kv_full, ST+1..2ST kv_empty, 2ST+1..2ST+2 s_full[2],
-  // 2ST+3 ds_full, 2ST+4 dq_done
   auto B = [&](int i) { return bar0 + 8u * i; };
-  const int KVF = 1, KVE = 1 + ST, SF = 1 + 2 * ST, DSF = 3 + 2 * ST, DQD = 4 + 2 * ST;
-  const int NBAR = 5 + 2 * ST;
+  // 0 q/do full, 1 q/do empty, 2..ST+1 kv_full, ST+2..2ST+1 kv_empty,
+  // then s_full[2], ds_full, dq_done, dq_free[2], d_exchange
+  const int QF = 0, QE = 1, KVF = 2, KVE = 2 + ST, SF = 2 + 2 * ST, DSF = 4 + 2 * ST,
+            DQD = 5 + 2 * ST, DQFREE = 6 + 2 * ST, DXB = 8 + 2 * ST, NBAR = 9 + 2 * ST;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  int qb, hd, b;
-  block_coords(p, p.nqb, true, qb, hd, b);
-  const int nkv = 2 * qb + 2;   // 64-key blocks up to the diagonal
-  const int row0 = b * p.seq + qb * 128;
-  const int colq = hd * 3 * p.d;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_items = p.nqb * p.heads * p.batch;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NBAR; ++i) mbar_init(B(i), i == DSF ? 256 : 1);
+    for (int i = 0; i < NBAR; ++i) {
+      const bool rows = i == DSF || i == DQFREE || i == DQFREE + 1 || i == DXB;
+      mbar_init(B(i), rows ? 256 : 1);
+    }
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_shared();
@@ -419,27 +408,40 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tDP = tmem + 128, tDQ = tmem + 256;
+  const uint32_t tS = tmem, tDP = tmem + 128;
 
   if (warp == 0) {
     if (lane == 0) {
       tma_prefetch_desc(&tm128);
       tma_prefetch_desc(&tm64);
       tma_prefetch_desc(&tmdo128);
-      mbar_arrive_expect_tx(B(0), 2 * T128);
-      for (int a = 0; a < NA; ++a) {
-        tma_load_2d(sQ + a * ATOM128, &tm128, B(0), colq + 64 * a, row0);
-        tma_load_2d(sDO + a * ATOM128, &tmdo128, B(0), hd * p.d + 64 * a, row0);
-      }
-      for (int j = 0; j < nkv; ++j) {
-        const int s = j % ST;
-        const int krow = b * p.seq + j * 64;
-        if (!mbar_wait_bounded(B(KVE + s), ((j / ST) & 1) ^ 1u, p.status, abort_flag)) break;
-        mbar_arrive_expect_tx(B(KVF + s), 2 * T64);
+      int g = 0, n = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n) {
+        int qb, hd, b;
+        item_coords(p, item, true, qb, hd, b);
+        const int colq = hd * 3 * p.d;
+        const int row0 = b * p.seq + qb * 128;
+        if (!mbar_wait_bounded(B(QE), (n & 1) ^ 1u, p.status, abort_flag)) break;
+        mbar_arrive_expect_tx(B(QF), 2 * T128);
         for (int a = 0; a < NA; ++a) {
-          tma_load_2d(sK0 + s * T64 + a * ATOM64, &tm64, B(KVF + s), colq + p.d + 64 * a, krow);
-          tma_load_2d(sV0 + s * T64 + a * ATOM64, &tm64, B(KVF + s), colq + 2 * p.d + 64 * a,
-                      krow);
+          tma_load_2d(sQ + a * ATOM128, &tm128, B(QF), colq + 64 * a, row0);
+          tma_load_2d(sDO + a * ATOM128, &tmdo128, B(QF), hd * p.d + 64 * a, row0);
+        }
+        const int nkv = 2 * qb + 2;
+        for (int j = 0; j < nkv; ++j, ++g) {
+          const int s = g % ST;
+          const int krow = b * p.seq + j * 64;
+          if (!mbar_wait_bounded(B(KVE + s), ((g / ST) & 1) ^ 1u, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(B(KVF + s), 2 * T64);
+          for (int a = 0; a < NA; ++a) {
+            tma_load_2d(sK0 + s * T64 + a * ATOM64, &tm64, B(KVF + s), colq + p.d + 64 * a, krow);
+            tma_load_2d(sV0 + s * T64 + a * ATOM64, &tm64, B(KVF + s), colq + 2 * p.d + 64 * a,
+                        krow);
+          }
         }
       }
     }
@@ -449,35 +451,53 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const uint32_t id_s = idesc_bf16_f32(128, 64, false, false);
       const uint32_t id_dq = idesc_bf16_f32(128, p.d, false, true);
       const int ksteps = p.d / 16;
-      // S(j), dP(j) into TMEM buffer j % 2
-      auto issue_s = [&](int j) -> bool {
-        const int s = j % ST;
-        if (!mbar_wait_bounded(B(KVF + s), (j / ST) & 1, p.status, abort_flag)) return false;
+      int gb = 0, n = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n) {
+        int qb, hd, b;
+        item_coords(p, item, true, qb, hd, b);
+        const int nkv = 2 * qb + 2;
+        if (!mbar_wait_bounded(B(QF), n & 1, p.status, abort_flag)) break;
         tc_fence_after();
-        const uint32_t bo = (j & 1) * 64;
-        for (int kk = 0; kk < ksteps; ++kk)
-          tc_mma_bf16(tS + bo, desc_kmajor(sQ, ATOM128, kk), desc_kmajor(sK0 + s * T64, ATOM64, kk),
-                      id_s, kk > 0);
-        for (int kk = 0; kk < ksteps; ++kk)
-          tc_mma_bf16(tDP + bo, desc_kmajor(sDO, ATOM128, kk),
-                      desc_kmajor(sV0 + s * T64, ATOM64, kk), id_s, kk > 0);
-        tc_commit(B(SF + (j & 1)));
-        return true;
-      };
-      bool ok = mbar_wait_bounded(B(0), 0, p.status, abort_flag);
-      if (ok) ok = issue_s(0);
-      if (ok && nkv > 1) ok = issue_s(1);
-      for (int j = 0; j < nkv && ok; ++j) {
-        // row threads wrote dS(j) and are done reading buffer j % 2
-        if (!mbar_wait_bounded(B(DSF), j & 1, p.status, abort_flag)) break;
-        tc_fence_after();
-        const int s = j % ST;
-        for (int kk = 0; kk < 4; ++kk)
-          tc_mma_bf16(tDQ, desc_kmajor(sDS, ATOM128, kk), desc_mnmajor(sK0 + s * T64, ATOM64, kk),
-                      id_dq, (j > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(B(KVE + s));
-        tc_commit(B(DQD));
-        if (j + 2 < nkv && !issue_s(j + 2)) break;
+        // S(block gg), dP(block gg) into TMEM buffer gg % 2
+        auto issue_s = [&](int j) -> bool {
+          const int gg = gb + j, s = gg % ST;
+          if (!mbar_wait_bounded(B(KVF + s), (gg / ST) & 1, p.status, abort_flag)) return false;
+          tc_fence_after();
+          const uint32_t bo = (gg & 1) * 64;
+          for (int kk = 0; kk < ksteps; ++kk)
+            tc_mma_bf16(tS + bo, desc_kmajor(sQ, ATOM128, kk),
+                        desc_kmajor(sK0 + s * T64, ATOM64, kk), id_s, kk > 0);
+          for (int kk = 0; kk < ksteps; ++kk)
+            tc_mma_bf16(tDP + bo, desc_kmajor(sDO, ATOM128, kk),
+                        desc_kmajor(sV0 + s * T64, ATOM64, kk), id_s, kk > 0);
+          tc_commit(B(SF + (gg & 1)));
+          if (j == nkv - 1) tc_commit(B(QE));
+          return true;
+        };
+        ok = issue_s(0) && issue_s(1);   // nkv >= 2
+        const uint32_t tDQ = tmem + 256 + 128 * (n & 1);
+        for (int j = 0; j < nkv && ok; ++j) {
+          const int gg = gb + j, s = gg % ST;
+          // row threads wrote dS(gg) and are done reading buffer gg % 2
+          if (!mbar_wait_bounded(B(DSF), gg & 1, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (j == 0 &&
+              !mbar_wait_bounded(B(DQFREE + (n & 1)), ((n >> 1) & 1) ^ 1u, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_bf16(tDQ, desc_kmajor(sDS, ATOM128, kk), desc_mnmajor(sK0 + s * T64, ATOM64, kk),
+                        id_dq, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(B(KVE + s));
+          tc_commit(B(DQD));
+          if (j + 2 < nkv && !issue_s(j + 2)) ok = false;
+        }
+        gb += nkv;
       }
     }
     __syncwarp();
@@ -486,67 +506,87 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    // D_r = dO_r . O_r: each warpgroup sums half of the channels
-    const size_t orow = (size_t)(row0 + r) * p.h + (size_t)hd * p.d;
-    const int half = p.d / 2;
-    float Dp = 0.f;
-    for (int c = wg * half; c < (wg + 1) * half; c += 8) {
-      const uint4 go = *reinterpret_cast<const uint4*>(p.dctx + orow + c);
-      const uint4 oo = *reinterpret_cast<const uint4*>(p.ctx + orow + c);
-      const bf16* g = reinterpret_cast<const bf16*>(&go);
-      const bf16* o = reinterpret_cast<const bf16*>(&oo);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) Dp = fmaf(__bfloat162float(g[e]), __bfloat162float(o[e]), Dp);
-    }
-    s_dpart[wg * 128 + r] = Dp;
-    named_bar_sync(1, 256);   // all 256 row threads reach this before any wait
-    const float Dr = s_dpart[r] + s_dpart[128 + r];
-    const size_t lrow = ((size_t)b * p.heads + hd) * p.seq + qb * 128 + r;
-    if (wg == 0) p.dsum[lrow] = Dr;
-    const float lse2 = p.lse[lrow] * LOG2E;
+    int gb = 0, n = 0;
     bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      if (!mbar_wait_bounded(B(SF + (j & 1)), (j >> 1) & 1, p.status, abort_flag)) {
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n) {
+      int qb, hd, b;
+      item_coords(p, item, true, qb, hd, b);
+      const int nkv = 2 * qb + 2;
+      const int row0 = b * p.seq + qb * 128;
+      const int colq = hd * 3 * p.d;
+      // D_r = dO_r . O_r: each warpgroup sums half of the channels
+      const size_t orow = (size_t)(row0 + r) * p.h + (size_t)hd * p.d;
+      const int half = p.d / 2;
+      float Dp = 0.f;
+      for (int c = wg * half; c < (wg + 1) * half; c += 8) {
+        const uint4 go = *reinterpret_cast<const uint4*>(p.dctx + orow + c);
+        const uint4 oo = *reinterpret_cast<const uint4*>(p.ctx + orow + c);
+        const bf16* gv = reinterpret_cast<const bf16*>(&go);
+        const bf16* ov = reinterpret_cast<const bf16*>(&oo);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) Dp = fmaf(__bfloat162float(gv[e]), __bfloat162float(ov[e]), Dp);
+      }
+      float* dpart = s_dpart + (n & 1) * 256;
+      dpart[wg * 128 + r] = Dp;
+      mbar_arrive(B(DXB));
+      if (!mbar_wait_bounded(B(DXB), n & 1, p.status, abort_flag)) {
+        ok = false;
+        break;
+      }
+      const float Dr = dpart[r] + dpart[128 + r];
+      const size_t lrow = ((size_t)b * p.heads + hd) * p.seq + qb * 128 + r;
+      if (wg == 0) p.dsum[lrow] = Dr;
+      const float lse2 = p.lse[lrow] * LOG2E;
+      const uint32_t tDQ = tmem + 256 + 128 * (n & 1);
+      for (int j = 0; j < nkv; ++j) {
+        const int gg = gb + j;
+        if (!mbar_wait_bounded(B(SF + (gg & 1)), (gg >> 1) & 1, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t col = (gg & 1) * 64 + wg * 32;
+        float ds[32];
+        {
+          uint32_t sv[32], dv[32];
+          tmem_ld32(tS + lane_off + col, sv);
+          tmem_ld32(tDP + lane_off + col, dv);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int key = j * 64 + wg * 32 + i;
+            float pr = fast_exp2(__uint_as_float(sv[i]) * p.scale_log2 - lse2);
+            if (key > qb * 128 + r) pr = 0.f;
+            ds[i] = pr * (__uint_as_float(dv[i]) - Dr);
+          }
+        }
+        if (gg > 0) {
+          // the dQ MMA of the previous block has read the dS buffer
+          if (!mbar_wait_bounded(B(DQD), (gg - 1) & 1, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int k = c * 8;
+          st_shared_v4(sDS + sw128_offset(r, wg * 4 + c), pack_bf16x2(ds[k], ds[k + 1]),
+                       pack_bf16x2(ds[k + 2], ds[k + 3]), pack_bf16x2(ds[k + 4], ds[k + 5]),
+                       pack_bf16x2(ds[k + 6], ds[k + 7]));
+        }
+        fence_proxy_async_shared();
+        tc_fence_before();
+        mbar_arrive(B(DSF));
+      }
+      if (!ok) break;
+      if (!mbar_wait_bounded(B(DQD), (gb + nkv - 1) & 1, p.status, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t col = (j & 1) * 64 + wg * 32;
-      float ds[32];
-      {
-        uint32_t sv[32], dv[32];
-        tmem_ld32(tS + lane_off + col, sv);
-        tmem_ld32(tDP + lane_off + col, dv);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int key = j * 64 + wg * 32 + i;
-          float pr = fast_exp2(__uint_as_float(sv[i]) * p.scale_log2 - lse2);
-          if (key > qb * 128 + r) pr = 0.f;
-          ds[i] = pr * (__uint_as_float(dv[i]) - Dr);
-        }
-      }
-      if (j > 0) {
-        if (!mbar_wait_bounded(B(DQD), (j - 1) & 1, p.status, abort_flag)) {
-          ok = false;
-          break;
-        }
-      }
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int k = c * 8;
-        st_shared_v4(sDS + sw128_offset(r, wg * 4 + c), pack_bf16x2(ds[k], ds[k + 1]),
-                     pack_bf16x2(ds[k + 2], ds[k + 3]), pack_bf16x2(ds[k + 4], ds[k + 5]),
-                     pack_bf16x2(ds[k + 6], ds[k + 7]));
-      }
-      fence_proxy_async_shared();
-      tc_fence_before();
-      mbar_arrive(B(DSF));
-    }
-    if (wg == 0 && ok && mbar_wait_bounded(B(DQD), (nkv - 1) & 1, p.status, abort_flag)) {
-      tc_fence_after();
+      // the two warpgroups store alternate 32-column chunks of dQ
       bf16* dq = p.dqkv + (size_t)(row0 + r) * 3 * p.h + colq;
-      for (int c = 0; c < p.d; c += 32) {
+      for (int c = wg * 32; c < p.d; c += 64) {
         uint32_t v[32];
         tmem_ld32(tDQ + lane_off + c, v);
         tmem_ld_wait();
@@ -560,6 +600,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           *reinterpret_cast<uint4*>(dq + c + q * 8) = u;
         }
       }
+      tc_fence_before();
+      mbar_arrive(B(DQFREE + (n & 1)));
+      gb += nkv;
     }
     __syncwarp();
   }
@@ -576,9 +619,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 }
 
 // ============================================================================ dK, dV
-// Per CTA: 128 keys; query blocks of 64 from the diagonal on, in a
-// BWD_STAGES-deep ring.  S^T and dP^T are double-buffered in TMEM; two
-// warpgroups of row threads each take 32 of the 64 query columns.
+// Persistent: one CTA per SM walks the key-block work items.  Per item: 128
+// keys; query blocks of 64 from the diagonal on, in a BWD_STAGES-deep ring that
+// runs on across items.  S^T and dP^T are double-buffered in TMEM; two
+// warpgroups of row threads each take 32 of the 64 query columns.  The next
+// item's K/V load and first S^T / dP^T MMAs overlap this item's epilogue.
 // smem: K, V (NA atoms of 16 KB), Q[ST], dO[ST] (NA atoms of 8 KB), P^T and dS^T
 // (1 atom of 16 KB each), lse / D per stage.  TMEM: S^T[b] cols 64b, dP^T[b]
 // cols 128+64b, dV 256.., dK 384..
@@ -600,24 +645,18 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm.base + 2 * T128 + 2 * ST * T64 + 2 * ATOM128 +
                                                512 * ST);
   const uint32_t bar0 = smem_u32(bars);
-  // 0 kv_full, 1..ST qdo_full, ST+1..2ST qdo_empty, 2ST+1..2ST+2 st_full[2],
-  // 2ST+3 pt_full, 2ST+4 mm_done
   auto B = [&](int i) { return bar0 + 8u * i; };
-  const int QF = 1, QE = 1 + ST, STF = 1 + 2 * ST, PTF = 3 + 2 * ST, MMD = 4 + 2 * ST;
-  const int NBAR = 5 + 2 * ST;
+  // 0 kv_full, 1 kv_empty, 2..ST+1 qdo_full, ST+2..2ST+1 qdo_empty, then
+  // st_full[2], pt_full, mm_done, acc_free
+  const int KVF = 0, KVE = 1, QF = 2, QE = 2 + ST, STF = 2 + 2 * ST, PTF = 4 + 2 * ST,
+            MMD = 5 + 2 * ST, ACCFREE = 6 + 2 * ST, NBAR = 7 + 2 * ST;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  int kb, hd, b;
-  block_coords(p, p.nqb, false, kb, hd, b);
-  const int first = 2 * kb;               // first 64-query block that sees these keys
-  const int nq = 2 * p.nqb - first;
-  const int krow0 = b * p.seq + kb * 128;
-  const int colq = hd * 3 * p.d;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_items = p.nqb * p.heads * p.batch;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NBAR; ++i) mbar_init(B(i), i == PTF ? 256 : 1);
+    for (int i = 0; i < NBAR; ++i) mbar_init(B(i), (i == PTF || i == ACCFREE) ? 256 : 1);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_shared();
@@ -634,23 +673,36 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       tma_prefetch_desc(&tm128);
       tma_prefetch_desc(&tm64);
       tma_prefetch_desc(&tmdo64);
-      mbar_arrive_expect_tx(B(0), 2 * T128);
-      for (int a = 0; a < NA; ++a) {
-        tma_load_2d(sK + a * ATOM128, &tm128, B(0), colq + p.d + 64 * a, krow0);
-        tma_load_2d(sV + a * ATOM128, &tm128, B(0), colq + 2 * p.d + 64 * a, krow0);
-      }
-      for (int i = 0; i < nq; ++i) {
-        const int s = i % ST;
-        const int qrow = b * p.seq + (first + i) * 64;
-        if (!mbar_wait_bounded(B(QE + s), ((i / ST) & 1) ^ 1u, p.status, abort_flag)) break;
-        mbar_arrive_expect_tx(B(QF + s), 2 * T64 + 512);
+      int g = 0, n = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n) {
+        int kb, hd, b;
+        item_coords(p, item, false, kb, hd, b);
+        const int colq = hd * 3 * p.d;
+        const int first = 2 * kb, nq = 2 * p.nqb - first;
+        if (!mbar_wait_bounded(B(KVE), (n & 1) ^ 1u, p.status, abort_flag)) break;
+        mbar_arrive_expect_tx(B(KVF), 2 * T128);
         for (int a = 0; a < NA; ++a) {
-          tma_load_2d(sQ0 + s * T64 + a * ATOM64, &tm64, B(QF + s), colq + 64 * a, qrow);
-          tma_load_2d(sDO0 + s * T64 + a * ATOM64, &tmdo64, B(QF + s), hd * p.d + 64 * a, qrow);
+          tma_load_2d(sK + a * ATOM128, &tm128, B(KVF), colq + p.d + 64 * a, b * p.seq + kb * 128);
+          tma_load_2d(sV + a * ATOM128, &tm128, B(KVF), colq + 2 * p.d + 64 * a,
+                      b * p.seq + kb * 128);
         }
-        const size_t lo = ((size_t)b * p.heads + hd) * p.seq + (first + i) * 64;
-        bulk_load(s_lse_u32 + s * 256, p.lse + lo, 256, B(QF + s));
-        bulk_load(s_d_u32 + s * 256, p.dsum + lo, 256, B(QF + s));
+        for (int i = 0; i < nq; ++i, ++g) {
+          const int s = g % ST;
+          const int qrow = b * p.seq + (first + i) * 64;
+          if (!mbar_wait_bounded(B(QE + s), ((g / ST) & 1) ^ 1u, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(B(QF + s), 2 * T64 + 512);
+          for (int a = 0; a < NA; ++a) {
+            tma_load_2d(sQ0 + s * T64 + a * ATOM64, &tm64, B(QF + s), colq + 64 * a, qrow);
+            tma_load_2d(sDO0 + s * T64 + a * ATOM64, &tmdo64, B(QF + s), hd * p.d + 64 * a, qrow);
+          }
+          const size_t lo = ((size_t)b * p.heads + hd) * p.seq + (first + i) * 64;
+          bulk_load(s_lse_u32 + s * 256, p.lse + lo, 256, B(QF + s));
+          bulk_load(s_d_u32 + s * 256, p.dsum + lo, 256, B(QF + s));
+        }
       }
     }
     __syncwarp();
@@ -659,38 +711,55 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const uint32_t id_st = idesc_bf16_f32(128, 64, false, false);
       const uint32_t id_acc = idesc_bf16_f32(128, p.d, false, true);
       const int ksteps = p.d / 16;
-      // S^T(i), dP^T(i) into TMEM buffer i % 2
-      auto issue_st = [&](int i) -> bool {
-        const int s = i % ST;
-        if (!mbar_wait_bounded(B(QF + s), (i / ST) & 1, p.status, abort_flag)) return false;
+      int gb = 0, n = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n) {
+        int kb, hd, b;
+        item_coords(p, item, false, kb, hd, b);
+        const int nq = 2 * p.nqb - 2 * kb;
+        if (!mbar_wait_bounded(B(KVF), n & 1, p.status, abort_flag)) break;
         tc_fence_after();
-        const uint32_t bo = (i & 1) * 64;
-        for (int kk = 0; kk < ksteps; ++kk)
-          tc_mma_bf16(tST + bo, desc_kmajor(sK, ATOM128, kk),
-                      desc_kmajor(sQ0 + s * T64, ATOM64, kk), id_st, kk > 0);
-        for (int kk = 0; kk < ksteps; ++kk)
-          tc_mma_bf16(tDPT + bo, desc_kmajor(sV, ATOM128, kk),
-                      desc_kmajor(sDO0 + s * T64, ATOM64, kk), id_st, kk > 0);
-        tc_commit(B(STF + (i & 1)));
-        return true;
-      };
-      bool ok = mbar_wait_bounded(B(0), 0, p.status, abort_flag);
-      if (ok) ok = issue_st(0);
-      if (ok && nq > 1) ok = issue_st(1);
-      for (int i = 0; i < nq && ok; ++i) {
-        // row threads wrote P^T(i), dS^T(i) and are done reading buffer i % 2
-        if (!mbar_wait_bounded(B(PTF), i & 1, p.status, abort_flag)) break;
-        tc_fence_after();
-        const int s = i % ST;
-        for (int kk = 0; kk < 4; ++kk)
-          tc_mma_bf16(tDV, desc_kmajor(sPT, ATOM128, kk), desc_mnmajor(sDO0 + s * T64, ATOM64, kk),
-                      id_acc, (i > 0 || kk > 0) ? 1u : 0u);
-        for (int kk = 0; kk < 4; ++kk)
-          tc_mma_bf16(tDK, desc_kmajor(sDST, ATOM128, kk), desc_mnmajor(sQ0 + s * T64, ATOM64, kk),
-                      id_acc, (i > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(B(QE + s));
-        tc_commit(B(MMD));
-        if (i + 2 < nq && !issue_st(i + 2)) break;
+        // S^T(block gg), dP^T(block gg) into TMEM buffer gg % 2
+        auto issue_st = [&](int i) -> bool {
+          const int gg = gb + i, s = gg % ST;
+          if (!mbar_wait_bounded(B(QF + s), (gg / ST) & 1, p.status, abort_flag)) return false;
+          tc_fence_after();
+          const uint32_t bo = (gg & 1) * 64;
+          for (int kk = 0; kk < ksteps; ++kk)
+            tc_mma_bf16(tST + bo, desc_kmajor(sK, ATOM128, kk),
+                        desc_kmajor(sQ0 + s * T64, ATOM64, kk), id_st, kk > 0);
+          for (int kk = 0; kk < ksteps; ++kk)
+            tc_mma_bf16(tDPT + bo, desc_kmajor(sV, ATOM128, kk),
+                        desc_kmajor(sDO0 + s * T64, ATOM64, kk), id_st, kk > 0);
+          tc_commit(B(STF + (gg & 1)));
+          if (i == nq - 1) tc_commit(B(KVE));
+          return true;
+        };
+        ok = issue_st(0) && issue_st(1);   // nq >= 2
+        for (int i = 0; i < nq && ok; ++i) {
+          const int gg = gb + i, s = gg % ST;
+          // row threads wrote P^T(gg), dS^T(gg) and are done reading buffer gg % 2
+          if (!mbar_wait_bounded(B(PTF), gg & 1, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (i == 0 &&
+              !mbar_wait_bounded(B(ACCFREE), (n & 1) ^ 1u, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_bf16(tDV, desc_kmajor(sPT, ATOM128, kk), desc_mnmajor(sDO0 + s * T64, ATOM64, kk),
+                        id_acc, (i > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_bf16(tDK, desc_kmajor(sDST, ATOM128, kk), desc_mnmajor(sQ0 + s * T64, ATOM64, kk),
+                        id_acc, (i > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(B(QE + s));
+          tc_commit(B(MMD));
+          if (i + 2 < nq && !issue_st(i + 2)) ok = false;
+        }
+        gb += nq;
       }
     }
     __syncwarp();
@@ -699,63 +768,74 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;     // key row
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    const int key = kb * 128 + r;
+    int gb = 0, n = 0;
     bool ok = true;
-    for (int i = 0; i < nq; ++i) {
-      if (!mbar_wait_bounded(B(STF + (i & 1)), (i >> 1) & 1, p.status, abort_flag)) {
-        ok = false;
-        break;
-      }
-      // lse / D of this block arrive with its Q / dO tiles: observe that
-      // barrier's phase too (stage i % ST is not refilled before this
-      // iteration ends: its release follows our arrival below)
-      if (!mbar_wait_bounded(B(QF + i % ST), (i / ST) & 1, p.status, abort_flag)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int q0 = (first + i) * 64 + wg * 32;
-      const float* s_lse = s_lse0 + (i % ST) * 64 + wg * 32;
-      const float* s_d = s_d0 + (i % ST) * 64 + wg * 32;
-      const uint32_t col = (i & 1) * 64 + wg * 32;
-      float pt[32], dst[32];
-      {
-        uint32_t sv[32], dv[32];
-        tmem_ld32(tST + lane_off + col, sv);
-        tmem_ld32(tDPT + lane_off + col, dv);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float pr = fast_exp2(__uint_as_float(sv[e]) * p.scale_log2 - s_lse[e] * LOG2E);
-          if (q0 + e < key) pr = 0.f;
-          pt[e] = pr;
-          dst[e] = pr * (__uint_as_float(dv[e]) - s_d[e]);
-        }
-      }
-      if (i > 0) {
-        if (!mbar_wait_bounded(B(MMD), (i - 1) & 1, p.status, abort_flag)) {
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n) {
+      int kb, hd, b;
+      item_coords(p, item, false, kb, hd, b);
+      const int first = 2 * kb, nq = 2 * p.nqb - first;
+      const int key = kb * 128 + r;
+      for (int i = 0; i < nq; ++i) {
+        const int gg = gb + i;
+        if (!mbar_wait_bounded(B(STF + (gg & 1)), (gg >> 1) & 1, p.status, abort_flag)) {
           ok = false;
           break;
         }
-      }
+        // lse / D of this block arrive with its Q / dO tiles: observe that
+        // barrier's phase too (stage gg % ST is not refilled before this
+        // iteration ends: its release follows our arrival below)
+        if (!mbar_wait_bounded(B(QF + gg % ST), (gg / ST) & 1, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int q0 = (first + i) * 64 + wg * 32;
+        const float* s_lse = s_lse0 + (gg % ST) * 64 + wg * 32;
+        const float* s_d = s_d0 + (gg % ST) * 64 + wg * 32;
+        const uint32_t col = (gg & 1) * 64 + wg * 32;
+        float pt[32], dst[32];
+        {
+          uint32_t sv[32], dv[32];
+          tmem_ld32(tST + lane_off + col, sv);
+          tmem_ld32(tDPT + lane_off + col, dv);
+          tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int k = c * 8;
-        st_shared_v4(sPT + sw128_offset(r, wg * 4 + c), pack_bf16x2(pt[k], pt[k + 1]),
-                     pack_bf16x2(pt[k + 2], pt[k + 3]), pack_bf16x2(pt[k + 4], pt[k + 5]),
-                     pack_bf16x2(pt[k + 6], pt[k + 7]));
-        st_shared_v4(sDST + sw128_offset(r, wg * 4 + c), pack_bf16x2(dst[k], dst[k + 1]),
-                     pack_bf16x2(dst[k + 2], dst[k + 3]), pack_bf16x2(dst[k + 4], dst[k + 5]),
-                     pack_bf16x2(dst[k + 6], dst[k + 7]));
+          for (int e = 0; e < 32; ++e) {
+            float pr = fast_exp2(__uint_as_float(sv[e]) * p.scale_log2 - s_lse[e] * LOG2E);
+            if (q0 + e < key) pr = 0.f;
+            pt[e] = pr;
+            dst[e] = pr * (__uint_as_float(dv[e]) - s_d[e]);
+          }
+        }
+        if (gg > 0) {
+          // the dV / dK MMAs of the previous block have read P^T / dS^T
+          if (!mbar_wait_bounded(B(MMD), (gg - 1) & 1, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int k = c * 8;
+          st_shared_v4(sPT + sw128_offset(r, wg * 4 + c), pack_bf16x2(pt[k], pt[k + 1]),
+                       pack_bf16x2(pt[k + 2], pt[k + 3]), pack_bf16x2(pt[k + 4], pt[k + 5]),
+                       pack_bf16x2(pt[k + 6], pt[k + 7]));
+          st_shared_v4(sDST + sw128_offset(r, wg * 4 + c), pack_bf16x2(dst[k], dst[k + 1]),
+                       pack_bf16x2(dst[k + 2], dst[k + 3]), pack_bf16x2(dst[k + 4], dst[k + 5]),
+                       pack_bf16x2(dst[k + 6], dst[k + 7]));
+        }
+        fence_proxy_async_shared();
+        tc_fence_before();
+        mbar_arrive(B(PTF));
       }
-      fence_proxy_async_shared();
-      tc_fence_before();
-      mbar_arrive(B(PTF));
-    }
-    if (ok && mbar_wait_bounded(B(MMD), (nq - 1) & 1, p.status, abort_flag)) {
+      if (!ok) break;
+      if (!mbar_wait_bounded(B(MMD), (gb + nq - 1) & 1, p.status, abort_flag)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       // warpgroup 0 writes dK (scaled), warpgroup 1 writes dV
-      bf16* out = p.dqkv + (size_t)(krow0 + r) * 3 * p.h + colq;
+      bf16* out = p.dqkv + (size_t)(b * p.seq + kb * 128 + r) * 3 * p.h + hd * 3 * p.d;
       const uint32_t tsrc = wg == 0 ? tDK : tDV;
       const float sc = wg == 0 ? p.scale : 1.0f;
       bf16* dst_row = out + (wg == 0 ? p.d : 2 * p.d);
@@ -773,6 +853,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           *reinterpret_cast<uint4*>(dst_row + c + q * 8) = u;
         }
       }
+      tc_fence_before();
+      mbar_arrive(B(ACCFREE));
+      gb += nq;
     }
     __syncwarp();
   }
@@ -823,7 +906,7 @@ size_t fwd_smem(int na) {
 // keep them at one CTA per SM so a second CTA never waits in tcgen05.alloc.
 size_t dq_smem(int na) {
   const size_t need =
-      (size_t)2 * na * ATOM128 + 2 * BWD_STAGES * na * ATOM64 + ATOM128 + 1024 + 256 + 1024;
+      (size_t)2 * na * ATOM128 + 2 * BWD_STAGES * na * ATOM64 + ATOM128 + 2048 + 256 + 1024;
   return need < 120 * 1024 ? 120 * 1024 : need;
 }
 size_t dkv_smem(int na) {
@@ -907,7 +990,8 @@ cudaError_t attn_bwd_tc(const void* qkv, const void* ctx, const float* lse, cons
   p.dctx = static_cast<const bf16*>(dctx);
   p.dqkv = static_cast<bf16*>(dqkv);
   p.dsum = dsum;
-  const int grid = p.nqb * heads * batch;
+  const int items = p.nqb * heads * batch;
+  const int grid = items < c.num_sms ? items : c.num_sms;
   const double tri = (double)batch * heads * d * ((double)seq * (seq + 1) / 2.0);
   cudaError_t e;
   if (d == 64) {
