@@ -84,7 +84,7 @@ __device__ __forceinline__ void item_coords(const Params& p, int item, bool desc
 // their row maxima through shared memory behind an mbarrier.
 // smem: Q, K[2], V[2] (NA atoms of 16 KB each), P (2 atoms), row-max and row-sum
 // exchange.  TMEM: S[b] cols 128b, O[b] cols 256+128b.
-template <int NA>
+template <int NA, int KS>
 __global__ void __launch_bounds__(FWD_THREADS, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -159,7 +159,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     if (lane == 0) {
       const uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);
       const uint32_t id_pv = idesc_bf16_f32(128, p.d, false, true);
-      const int ksteps = p.d / 16;
+      const uint64_t dQ = desc_kbase(sQ), dK0 = desc_kbase(sK0), dP = desc_kbase(sP);
+      const uint64_t dV0 = desc_mnbase(sV0, ATOM128);
       int gb = 0, n = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n) {
@@ -173,9 +174,11 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
           const int gg = gb + j, s = gg & 1;
           if (!mbar_wait_bounded(B(KFULL + s), (gg >> 1) & 1, p.status, abort_flag)) return false;
           tc_fence_after();
-          for (int kk = 0; kk < ksteps; ++kk)
-            tc_mma_bf16(tmem + 128 * s, desc_kmajor(sQ, ATOM128, kk),
-                        desc_kmajor(sK0 + s * TILE, ATOM128, kk), id_qk, kk > 0);
+          const uint64_t dK = desc_add(dK0, s * TILE);
+#pragma unroll
+          for (int kk = 0; kk < KS; ++kk)
+            tc_mma_bf16(tmem + 128 * s, desc_add(dQ, kmajor_off(kk, ATOM128)),
+                        desc_add(dK, kmajor_off(kk, ATOM128)), id_qk, kk > 0);
           tc_commit(B(KEMPTY + s));
           tc_commit(B(SFULL + s));
           if (j == nkv - 1) tc_commit(B(QEMPTY));
@@ -199,8 +202,10 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             break;
           }
           tc_fence_after();
+          const uint64_t dV = desc_add(dV0, s * TILE);
+#pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            tc_mma_bf16(tO, desc_kmajor(sP, ATOM128, kk), desc_mnmajor(sV0 + s * TILE, ATOM128, kk),
+            tc_mma_bf16(tO, desc_add(dP, kmajor_off(kk, ATOM128)), desc_add(dV, mnmajor_off(kk)),
                         id_pv, (j > 0 || kk > 0) ? 1u : 0u);
           tc_commit(B(VEMPTY + s));
           tc_commit(B(ODONE));
@@ -369,7 +374,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
 // smem: Q, dO (NA atoms of 16 KB), K[ST], V[ST] (NA atoms of 8 KB), dS (1 atom
 // of 16 KB), D exchange.  TMEM: S[b] cols 64b, dP[b] cols 128+64b, dQ[b] cols
 // 256+128b.
-template <int NA>
+template <int NA, int KS>
 __global__ void __launch_bounds__(BWD_THREADS, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm128,
                           const __grid_constant__ CUtensorMap tm64,
@@ -450,7 +455,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16_f32(128, 64, false, false);
       const uint32_t id_dq = idesc_bf16_f32(128, p.d, false, true);
-      const int ksteps = p.d / 16;
+      const uint64_t dQd = desc_kbase(sQ), dDO = desc_kbase(sDO), dK0 = desc_kbase(sK0),
+                     dV0 = desc_kbase(sV0), dDS = desc_kbase(sDS);
+      const uint64_t dKmn0 = desc_mnbase(sK0, ATOM64);
       int gb = 0, n = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n) {
@@ -465,12 +472,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           if (!mbar_wait_bounded(B(KVF + s), (gg / ST) & 1, p.status, abort_flag)) return false;
           tc_fence_after();
           const uint32_t bo = (gg & 1) * 64;
-          for (int kk = 0; kk < ksteps; ++kk)
-            tc_mma_bf16(tS + bo, desc_kmajor(sQ, ATOM128, kk),
-                        desc_kmajor(sK0 + s * T64, ATOM64, kk), id_s, kk > 0);
-          for (int kk = 0; kk < ksteps; ++kk)
-            tc_mma_bf16(tDP + bo, desc_kmajor(sDO, ATOM128, kk),
-                        desc_kmajor(sV0 + s * T64, ATOM64, kk), id_s, kk > 0);
+          const uint64_t dK = desc_add(dK0, s * T64), dV = desc_add(dV0, s * T64);
+#pragma unroll
+          for (int kk = 0; kk < KS; ++kk)
+            tc_mma_bf16(tS + bo, desc_add(dQd, kmajor_off(kk, ATOM128)),
+                        desc_add(dK, kmajor_off(kk, ATOM64)), id_s, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < KS; ++kk)
+            tc_mma_bf16(tDP + bo, desc_add(dDO, kmajor_off(kk, ATOM128)),
+                        desc_add(dV, kmajor_off(kk, ATOM64)), id_s, kk > 0);
           tc_commit(B(SF + (gg & 1)));
           if (j == nkv - 1) tc_commit(B(QE));
           return true;
@@ -490,8 +500,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             break;
           }
           tc_fence_after();
+          const uint64_t dKmn = desc_add(dKmn0, s * T64);
+#pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc_mma_bf16(tDQ, desc_kmajor(sDS, ATOM128, kk), desc_mnmajor(sK0 + s * T64, ATOM64, kk),
+            tc_mma_bf16(tDQ, desc_add(dDS, kmajor_off(kk, ATOM128)), desc_add(dKmn, mnmajor_off(kk)),
                         id_dq, (j > 0 || kk > 0) ? 1u : 0u);
           tc_commit(B(KVE + s));
           tc_commit(B(DQD));
@@ -627,7 +639,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 // smem: K, V (NA atoms of 16 KB), Q[ST], dO[ST] (NA atoms of 8 KB), P^T and dS^T
 // (1 atom of 16 KB each), lse / D per stage.  TMEM: S^T[b] cols 64b, dP^T[b]
 // cols 128+64b, dV 256.., dK 384..
-template <int NA>
+template <int NA, int KS>
 __global__ void __launch_bounds__(BWD_THREADS, 1)
     attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm128,
                            const __grid_constant__ CUtensorMap tm64,
@@ -710,7 +722,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     if (lane == 0) {
       const uint32_t id_st = idesc_bf16_f32(128, 64, false, false);
       const uint32_t id_acc = idesc_bf16_f32(128, p.d, false, true);
-      const int ksteps = p.d / 16;
+      const uint64_t dKd = desc_kbase(sK), dVd = desc_kbase(sV), dQ0 = desc_kbase(sQ0),
+                     dDO0 = desc_kbase(sDO0), dPT = desc_kbase(sPT), dDST = desc_kbase(sDST);
+      const uint64_t dQmn0 = desc_mnbase(sQ0, ATOM64), dDOmn0 = desc_mnbase(sDO0, ATOM64);
       int gb = 0, n = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n) {
@@ -725,12 +739,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           if (!mbar_wait_bounded(B(QF + s), (gg / ST) & 1, p.status, abort_flag)) return false;
           tc_fence_after();
           const uint32_t bo = (gg & 1) * 64;
-          for (int kk = 0; kk < ksteps; ++kk)
-            tc_mma_bf16(tST + bo, desc_kmajor(sK, ATOM128, kk),
-                        desc_kmajor(sQ0 + s * T64, ATOM64, kk), id_st, kk > 0);
-          for (int kk = 0; kk < ksteps; ++kk)
-            tc_mma_bf16(tDPT + bo, desc_kmajor(sV, ATOM128, kk),
-                        desc_kmajor(sDO0 + s * T64, ATOM64, kk), id_st, kk > 0);
+          const uint64_t dQ = desc_add(dQ0, s * T64), dDO = desc_add(dDO0, s * T64);
+#pragma unroll
+          for (int kk = 0; kk < KS; ++kk)
+            tc_mma_bf16(tST + bo, desc_add(dKd, kmajor_off(kk, ATOM128)),
+                        desc_add(dQ, kmajor_off(kk, ATOM64)), id_st, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < KS; ++kk)
+            tc_mma_bf16(tDPT + bo, desc_add(dVd, kmajor_off(kk, ATOM128)),
+                        desc_add(dDO, kmajor_off(kk, ATOM64)), id_st, kk > 0);
           tc_commit(B(STF + (gg & 1)));
           if (i == nq - 1) tc_commit(B(KVE));
           return true;
@@ -749,11 +766,14 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             break;
           }
           tc_fence_after();
+          const uint64_t dDOmn = desc_add(dDOmn0, s * T64), dQmn = desc_add(dQmn0, s * T64);
+#pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc_mma_bf16(tDV, desc_kmajor(sPT, ATOM128, kk), desc_mnmajor(sDO0 + s * T64, ATOM64, kk),
+            tc_mma_bf16(tDV, desc_add(dPT, kmajor_off(kk, ATOM128)), desc_add(dDOmn, mnmajor_off(kk)),
                         id_acc, (i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc_mma_bf16(tDK, desc_kmajor(sDST, ATOM128, kk), desc_mnmajor(sQ0 + s * T64, ATOM64, kk),
+            tc_mma_bf16(tDK, desc_add(dDST, kmajor_off(kk, ATOM128)), desc_add(dQmn, mnmajor_off(kk)),
                         id_acc, (i > 0 || kk > 0) ? 1u : 0u);
           tc_commit(B(QE + s));
           tc_commit(B(MMD));
@@ -957,17 +977,17 @@ cudaError_t attn_fwd_tc(const void* qkv, void* ctx, float* lse, int batch, int s
   const int grid = items < c.num_sms ? items : c.num_sms;
   const double flops = 2.0 * 2.0 * batch * heads * d * ((double)seq * (seq + 1) / 2.0);
   cudaError_t e;
-  if (d == 64) {
-    const size_t sm = fwd_smem(1);
-    if ((e = set_smem(attn_fwd_tc_kernel<1>, sm)) != cudaSuccess) return e;
-    c.before(KK_ATTN_FWD, flops);
-    attn_fwd_tc_kernel<1><<<grid, FWD_THREADS, sm, c.stream>>>(tm, p);
-  } else {
-    const size_t sm = fwd_smem(2);
-    if ((e = set_smem(attn_fwd_tc_kernel<2>, sm)) != cudaSuccess) return e;
-    c.before(KK_ATTN_FWD, flops);
-    attn_fwd_tc_kernel<2><<<grid, FWD_THREADS, sm, c.stream>>>(tm, p);
+#define FWD_CASE(NA_, KS_)                                                          \
+  {                                                                                 \
+    const size_t sm = fwd_smem(NA_);                                                \
+    if ((e = set_smem(attn_fwd_tc_kernel<NA_, KS_>, sm)) != cudaSuccess) return e;  \
+    c.before(KK_ATTN_FWD, flops);                                                   \
+    attn_fwd_tc_kernel<NA_, KS_><<<grid, FWD_THREADS, sm, c.stream>>>(tm, p);       \
   }
+  if (d == 64) FWD_CASE(1, 4)
+  else if (d == 96) FWD_CASE(2, 6)
+  else FWD_CASE(2, 8)
+#undef FWD_CASE
   c.after();
   return cudaGetLastError();
 }
@@ -994,27 +1014,25 @@ cudaError_t attn_bwd_tc(const void* qkv, const void* ctx, const float* lse, cons
   const int grid = items < c.num_sms ? items : c.num_sms;
   const double tri = (double)batch * heads * d * ((double)seq * (seq + 1) / 2.0);
   cudaError_t e;
-  if (d == 64) {
-    if ((e = set_smem(attn_bwd_dq_tc_kernel<1>, dq_smem(1))) != cudaSuccess) return e;
-    if ((e = set_smem(attn_bwd_dkv_tc_kernel<1>, dkv_smem(1))) != cudaSuccess) return e;
-    c.before(KK_ATTN_BWD, 2.0 * 3.0 * tri);
-    attn_bwd_dq_tc_kernel<1><<<grid, BWD_THREADS, dq_smem(1), c.stream>>>(tm128, tm64, tmdo128, p);
-    c.after();
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    c.before(KK_ATTN_BWD, 2.0 * 4.0 * tri);
-    attn_bwd_dkv_tc_kernel<1><<<grid, BWD_THREADS, dkv_smem(1), c.stream>>>(tm128, tm64, tmdo64, p);
-    c.after();
-  } else {
-    if ((e = set_smem(attn_bwd_dq_tc_kernel<2>, dq_smem(2))) != cudaSuccess) return e;
-    if ((e = set_smem(attn_bwd_dkv_tc_kernel<2>, dkv_smem(2))) != cudaSuccess) return e;
-    c.before(KK_ATTN_BWD, 2.0 * 3.0 * tri);
-    attn_bwd_dq_tc_kernel<2><<<grid, BWD_THREADS, dq_smem(2), c.stream>>>(tm128, tm64, tmdo128, p);
-    c.after();
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    c.before(KK_ATTN_BWD, 2.0 * 4.0 * tri);
-    attn_bwd_dkv_tc_kernel<2><<<grid, BWD_THREADS, dkv_smem(2), c.stream>>>(tm128, tm64, tmdo64, p);
-    c.after();
+#define BWD_CASE(NA_, KS_)                                                                    \
+  {                                                                                           \
+    if ((e = set_smem(attn_bwd_dq_tc_kernel<NA_, KS_>, dq_smem(NA_))) != cudaSuccess) return e; \
+    if ((e = set_smem(attn_bwd_dkv_tc_kernel<NA_, KS_>, dkv_smem(NA_))) != cudaSuccess)         \
+      return e;                                                                               \
+    c.before(KK_ATTN_BWD, 2.0 * 3.0 * tri);                                                   \
+    attn_bwd_dq_tc_kernel<NA_, KS_><<<grid, BWD_THREADS, dq_smem(NA_), c.stream>>>(            \
+        tm128, tm64, tmdo128, p);                                                             \
+    c.after();                                                                                \
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;                                    \
+    c.before(KK_ATTN_BWD, 2.0 * 4.0 * tri);                                                   \
+    attn_bwd_dkv_tc_kernel<NA_, KS_><<<grid, BWD_THREADS, dkv_smem(NA_), c.stream>>>(          \
+        tm128, tm64, tmdo64, p);                                                              \
+    c.after();                                                                                \
   }
+  if (d == 64) BWD_CASE(1, 4)
+  else if (d == 96) BWD_CASE(2, 6)
+  else BWD_CASE(2, 8)
+#undef BWD_CASE
   return cudaGetLastError();
 }
 

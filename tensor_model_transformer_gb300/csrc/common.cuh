@@ -277,6 +277,25 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, uint32_t atom_by
   return smem_desc_sw128(base + kk * 2048, atom_bytes, 1024);
 }
 
+// The same descriptors built from a precomputed base: the start address is the
+// low field, so a tile offset is added directly (off >> 4, no carry out of the
+// 14-bit field for shared-memory addresses).  With kk a compile-time constant
+// the offsets fold, so the single MMA-issuing thread spends a couple of integer
+// instructions per MMA instead of rebuilding the descriptor.
+__host__ __device__ constexpr uint32_t kmajor_off(int kk, uint32_t atom_bytes) {
+  return (uint32_t)(kk >> 2) * atom_bytes + (uint32_t)(kk & 3) * 32;
+}
+__host__ __device__ constexpr uint32_t mnmajor_off(int kk) { return (uint32_t)kk * 2048; }
+__device__ __forceinline__ uint64_t desc_kbase(uint32_t base) {
+  return smem_desc_sw128(base, 16, 1024);
+}
+__device__ __forceinline__ uint64_t desc_mnbase(uint32_t base, uint32_t atom_bytes) {
+  return smem_desc_sw128(base, atom_bytes, 1024);
+}
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t byte_off) {
+  return desc + (uint64_t)(byte_off >> 4);
+}
+
 // Byte offset of 16-byte chunk `c` of row `r` inside a [rows][64 bf16] box
 // with 128-byte swizzle (the layout TMA writes and the MMA reads).
 __device__ __forceinline__ uint32_t sw128_offset(int r, int c) {

@@ -327,7 +327,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       // column boxes of BK rows (8 KB apart, the leading byte offset), 8-row
       // K groups 1024 bytes apart; a K step moves 16 rows = 2048 bytes.
       const uint32_t a_lbo = p.a_mn ? BK * 128 : 16, b_lbo = p.b_mn ? BK * 128 : 16;
-      const uint32_t a_kstep = p.a_mn ? 2048 : 32, b_kstep = p.b_mn ? 2048 : 32;
+      // base descriptors of stage 0; a stage or K step only moves the start
+      // address field (in 16-byte units)
+      const uint64_t a_desc0 = smem_desc_sw128(sA0, a_lbo, 1024);
+      const uint64_t b_desc0 = smem_desc_sw128(sB0, b_lbo, 1024);
+      const uint32_t a_kstep16 = p.a_mn ? 2048 / 16 : 32 / 16, b_kstep16 = p.b_mn ? 2048 / 16 : 32 / 16;
       int stage = 0;
       uint32_t phase = 0;
       int unit = 0;
@@ -348,13 +352,12 @@ __global__ void __launch_bounds__(THREADS, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t sa = sA0 + stage * A_BYTES, sb = sB0 + stage * B_BYTES;
+            const uint64_t ad0 = a_desc0 + (uint64_t)(stage * (A_BYTES / 16));
+            const uint64_t bd0 = b_desc0 + (uint64_t)(stage * (B_BYTES / 16));
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
-              const uint64_t ad = smem_desc_sw128(sa + kk * a_kstep, a_lbo, 1024);
-              const uint64_t bd = smem_desc_sw128(sb + kk * b_kstep, b_lbo, 1024);
-              tc_mma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-            }
+            for (int kk = 0; kk < BK / 16; ++kk)
+              tc_mma_bf16(d_tmem, ad0 + kk * a_kstep16, bd0 + kk * b_kstep16, idesc,
+                          (kb > 0 || kk > 0) ? 1u : 0u);
             tc_commit(empty_bar(stage));
             if (++stage == STAGES) {
               stage = 0;
