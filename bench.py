@@ -272,21 +272,54 @@ def main():
     flops = layer_flops(shape)
     value = flops * args.steps * world / (ms / 1e3) / 1e12
 
-    # ---- end to end: host buffers in, results out, every step
+    # ---- end to end: host buffers in, results out, every step.  Each step's x
+    # and dy are copied from pinned host memory and its y and dx are copied
+    # back; a copy stream overlaps step i's copies with step i-1's compute
+    # through double-buffered device inputs and outputs.
     barrier()
     torch.cuda.synchronize()
-    y_h = torch.empty_like(x_h).pin_memory()
-    dx_h = torch.empty_like(x_h).pin_memory()
+    copy = torch.cuda.Stream()
+    xs = [xd, torch.empty_like(xd)]
+    dys = [dyd, torch.empty_like(dyd)]
+    ys = [y, torch.empty_like(y)]
+    dxs = [dx, torch.empty_like(dx)]
+    y_h = [torch.empty_like(x_h).pin_memory() for _ in range(2)]
+    dx_h = [torch.empty_like(x_h).pin_memory() for _ in range(2)]
+    loaded = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
+    drained = [torch.cuda.Event() for _ in range(2)]
+
+    def e2e_step_io(i):
+        b = i % 2
+        with torch.cuda.stream(copy):
+            if i >= 2:
+                copy.wait_event(computed[b])        # step i-2 is done with buffer b
+            xs[b].copy_(x_h, non_blocking=True)
+            dys[b].copy_(dy_h, non_blocking=True)
+            loaded[b].record(copy)
+
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        xd.copy_(x_h, non_blocking=True)
-        dyd.copy_(dy_h, non_blocking=True)
-        step()
-        y_h.copy_(y, non_blocking=True)
-        dx_h.copy_(dx, non_blocking=True)
-    e1.record(stream)
+    copy.wait_event(e0)
+    e2e_step_io(0)
+    for i in range(args.steps):
+        b = i % 2
+        if i + 1 < args.steps:
+            e2e_step_io(i + 1)
+        stream.wait_event(loaded[b])
+        if i >= 2:
+            stream.wait_event(drained[b])           # outputs of step i-2 copied out
+        mtl.layer_fwd(desc, w, xs[b], ys[b], saved, ws, stream)
+        mtl.layer_bwd(desc, w, xs[b], saved, dys[b], dxs[b], grads, ws, stream)
+        computed[b].record(stream)
+        with torch.cuda.stream(copy):
+            copy.wait_event(computed[b])
+            y_h[b].copy_(ys[b], non_blocking=True)
+            dx_h[b].copy_(dxs[b], non_blocking=True)
+            drained[b].record(copy)
+    e1.record(copy)
     e1.synchronize()
+    torch.cuda.synchronize()
     ms_e2e = e0.elapsed_time(e1)
     if world > 1:
         t = torch.tensor([ms_e2e], device="cuda")

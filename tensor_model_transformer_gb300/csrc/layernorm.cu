@@ -302,7 +302,7 @@ cudaError_t ln_fwd_t(const void* x, const void* g, const void* b, void* u, float
         (const T*)x, (const T*)g, (const T*)b, (T*)u, mean, rstd, n, h, eps, rows);          \
     break;
   switch (vpt) {
-    LN_FWD_CASE(1, 4)
+    LN_FWD_CASE(1, 1)
     LN_FWD_CASE(2, 2)
     LN_FWD_CASE(4, 1)
     LN_FWD_CASE(8, 1)
@@ -339,7 +339,7 @@ cudaError_t ln_bwd_t(const float* du, const void* x, const float* mean, const fl
         rows);                                                                              \
     break;
   switch (vpt) {
-    LN_BWD_CASE(1, 4)
+    LN_BWD_CASE(1, 1)
     LN_BWD_CASE(2, 2)
     LN_BWD_CASE(4, 1)
     LN_BWD_CASE(8, 1)
