@@ -43,7 +43,7 @@ constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 128 + 32 * EPI_WARPS;
-constexpr int LAUNCH_REGS = 168, PRODUCER_REGS = 40, EPILOGUE_REGS = 232;
+constexpr int LAUNCH_REGS = 168, PRODUCER_REGS = 56, EPILOGUE_REGS = 224;
 static_assert(PRODUCER_REGS * 128 + EPILOGUE_REGS * 32 * EPI_WARPS == LAUNCH_REGS * THREADS,
               "register split must add up to the launch total");
 constexpr int TMEM_COLS = 2 * BN;
@@ -166,20 +166,26 @@ __device__ __forceinline__ void epi_chunk(const Params& p, int row, int col0, fl
 
 // Epilogue warps 4..11: wait for an accumulator, read it from TMEM (32 columns
 // at a time), add partition partials in order, apply the epilogue, store.
-template <int EPI, bool OUT_F32, bool REDUCE>
-__device__ __forceinline__ void epilogue_role(const Params& p, uint32_t tmem_base, uint32_t bar0,
-                                              volatile int* abort_flag, int warp, int lane) {
-  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
-  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+// tfull0 / tempty0: addresses of tfull[0] and tempty[0] (tempty as a cluster
+// address when PAIR: the epilogue warps of both CTAs of a pair release the
+// accumulator to the leader CTA's barrier).  Tiles tile0, tile0 + tile_step, ...
+// are tile_rows high; this CTA's rows start at row_off inside a tile.
+template <int EPI, bool OUT_F32, bool REDUCE, bool PAIR>
+__device__ __forceinline__ void epilogue_role(const Params& p, uint32_t tmem_base, uint32_t tfull0,
+                                              uint32_t tempty0, volatile int* abort_flag,
+                                              int warp, int lane, int tile0, int tile_step,
+                                              int tile_rows, int row_off) {
+  auto tfull_bar = [&](int b) { return tfull0 + 8u * b; };
+  auto tempty_bar = [&](int b) { return tempty0 + 8u * b; };
   const int ew = warp - 4;
   const int quarter = warp & 3;
   const int chalf = ew >> 2;
   int unit = 0;
   bool ok = true;
-  for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+  for (int tile = tile0; tile < p.num_tiles && ok; tile += tile_step) {
     int mb, nb;
     tile_coords(p, tile, mb, nb);
-    const int row = mb * BM + quarter * 32 + lane;
+    const int row = mb * tile_rows + row_off + quarter * 32 + lane;
     const int colbase = nb * BN + chalf * 128;
     float sum[REDUCE ? 128 : 1];
     for (int u = 0; u < p.units_per_tile; ++u, ++unit) {
@@ -211,7 +217,12 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t tmem_bas
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(buf));
+      if (lane == 0) {
+        if constexpr (PAIR)
+          mbar_arrive_cluster(tempty_bar(buf));
+        else
+          mbar_arrive(tempty_bar(buf));
+      }
     }
     if constexpr (REDUCE) {
       if (ok) {
@@ -278,7 +289,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   if (warp >= 4) {
-    epilogue_role<EPI, OUT_F32, REDUCE>(p, tmem_base, bar0, abort_flag, warp, lane);
+    epilogue_role<EPI, OUT_F32, REDUCE, false>(p, tmem_base, tfull_bar(0), tempty_bar(0),
+                                               abort_flag, warp, lane, blockIdx.x, gridDim.x, BM,
+                                               0);
   } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -386,6 +399,179 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+
+// ============================================================================
+// Pair kernel: a cluster of two CTAs computes 256x256 tiles with cta_group::2
+// MMAs (M = 256 across the pair, N = 256).  Each CTA loads its 128-row half of
+// A and its 128-row half of B; the leader CTA (rank 0) issues every MMA, which
+// reads both CTAs' shared memory and writes each CTA's 128 rows into its own
+// TMEM.  One tcgen05.mma does twice the work of the single-CTA kernel's, so the
+// one issuing thread keeps the tensor pipes busy.  K stages are 128 deep (two
+// 64-wide swizzle boxes), three stages of 64 KB per CTA.
+//   full[s]   leader only: both CTAs' TMA loads complete on it
+//   empty[s]  both CTAs: multicast commit after the stage's MMAs
+//   tfull[b]  both CTAs: multicast commit after a work unit's MMAs
+//   tempty[b] leader only: 16 arrivals, the epilogue warps of both CTAs
+constexpr int P_BK = 128, P_STAGES = 3, P_HALF = 128;
+constexpr int P_A_BYTES = P_HALF * P_BK * 2;
+constexpr int P_B_BYTES = P_HALF * P_BK * 2;
+constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
+constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + BAR_BYTES + 1024;
+constexpr int P_ATOM = P_HALF * 128;   // one [128 rows][64 bf16] box
+
+template <int EPI, bool OUT_F32, bool REDUCE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sA0 = smem_u32(smem);
+  const uint32_t sB0 = sA0 + P_STAGES * P_A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P_STAGES * P_STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * P_STAGES + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (P_STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * P_STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * P_STAGES + 2 + b); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_cta_rank();
+  const int pair_id = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P_STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 2 * EPI_WARPS);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PRODUCER_REGS));
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(EPILOGUE_REGS));
+  }
+
+  if (warp >= 4) {
+    epilogue_role<EPI, OUT_F32, REDUCE, true>(p, tmem_base, tfull_bar(0),
+                                              cluster_map(tempty_bar(0), 0), abort_flag, warp,
+                                              lane, pair_id, npairs, 2 * P_HALF, P_HALF * rank);
+  } else if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      const int kb_per_tile = p.kb_per_unit * p.units_per_tile;
+      bool ok = true;
+      for (int tile = pair_id; tile < p.num_tiles && ok; tile += npairs) {
+        int mb, nb;
+        tile_coords(p, tile, mb, nb);
+        const int m0 = mb * 2 * P_HALF + P_HALF * rank, n0 = nb * 2 * P_HALF + P_HALF * rank;
+        for (int kb = 0; kb < kb_per_tile; ++kb) {
+          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = cluster_map(full_bar(stage), 0);
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * P_STAGE_BYTES);
+          const int k0 = kb * P_BK;
+          const uint32_t sa = sA0 + stage * P_A_BYTES, sb = sB0 + stage * P_B_BYTES;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            if (!p.a_mn)
+              tma_load_2d_pair(sa + j * P_ATOM, &tmA, fb, k0 + 64 * j, m0);
+            else
+              tma_load_2d_pair(sa + j * P_ATOM, &tmA, fb, m0 + 64 * j, k0);
+            if (!p.b_mn)
+              tma_load_2d_pair(sb + j * P_ATOM, &tmB, fb, k0 + 64 * j, n0);
+            else
+              tma_load_2d_pair(sb + j * P_ATOM, &tmB, fb, n0 + 64 * j, k0);
+          }
+          if (++stage == P_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (leader)
+    if (lane == 0 && rank == 0) {
+      const uint32_t idesc = idesc_bf16_f32(2 * P_HALF, BN, p.a_mn != 0, p.b_mn != 0);
+      const uint64_t a_desc0 = p.a_mn ? desc_mnbase(sA0, P_ATOM) : desc_kbase(sA0);
+      const uint64_t b_desc0 = p.b_mn ? desc_mnbase(sB0, P_ATOM) : desc_kbase(sB0);
+      int stage = 0;
+      uint32_t phase = 0;
+      int unit = 0;
+      bool ok = true;
+      for (int tile = pair_id; tile < p.num_tiles && ok; tile += npairs) {
+        for (int u = 0; u < p.units_per_tile && ok; ++u, ++unit) {
+          const int buf = unit & 1;
+          const uint32_t uphase = (unit >> 1) & 1;
+          if (!mbar_wait_bounded_cluster(tempty_bar(buf), uphase ^ 1u, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + buf * BN;
+          for (int kb = 0; kb < p.kb_per_unit; ++kb) {
+            if (!mbar_wait_bounded(full_bar(stage), phase, p.status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t ad0 = a_desc0 + (uint64_t)(stage * (P_A_BYTES / 16));
+            const uint64_t bd0 = b_desc0 + (uint64_t)(stage * (P_B_BYTES / 16));
+#pragma unroll
+            for (int kk = 0; kk < P_BK / 16; ++kk) {
+              const uint32_t ao = p.a_mn ? mnmajor_off(kk) : kmajor_off(kk, P_ATOM);
+              const uint32_t bo = p.b_mn ? mnmajor_off(kk) : kmajor_off(kk, P_ATOM);
+              tc_mma_bf16_pair(d_tmem, desc_add(ad0, ao), desc_add(bd0, bo), idesc,
+                               (kb > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc_commit_pair_mc(empty_bar(stage), 3);
+            if (++stage == P_STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (ok) tc_commit_pair_mc(tfull_bar(buf), 3);
+        }
+      }
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  cluster_sync();
+  if (warp == 1) {
+    if (*abort_flag) {
+      const long long t0 = clock64();
+      while (clock64() - t0 < 2000000LL) {
+      }
+    }
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -437,6 +623,26 @@ KernelFn kernel_ptr() {
   return reinterpret_cast<KernelFn>(gemm_tc_kernel<EPI, F32, RED>);
 }
 
+template <int EPI, bool F32, bool RED>
+KernelFn kernel2_ptr() {
+  return reinterpret_cast<KernelFn>(gemm_tc2_kernel<EPI, F32, RED>);
+}
+
+KernelFn select_kernel2(int epi, bool f32, bool red) {
+#define SEL2(E)                                                                          \
+  if (epi == E) {                                                                        \
+    if (f32) return red ? kernel2_ptr<E, true, true>() : kernel2_ptr<E, true, false>();  \
+    return red ? kernel2_ptr<E, false, true>() : kernel2_ptr<E, false, false>();         \
+  }
+  SEL2(EPI_STORE)
+  SEL2(EPI_BIAS)
+  SEL2(EPI_BIAS_RESID)
+  SEL2(EPI_BIAS_GELU)
+  SEL2(EPI_DGELU)
+#undef SEL2
+  return nullptr;
+}
+
 KernelFn select_kernel(int epi, bool f32, bool red) {
 #define SEL(E)                                                                         \
   if (epi == E) {                                                                      \
@@ -472,21 +678,35 @@ cudaError_t gemm_tc(const GemmArgs& a, const LaunchCtx& c) {
   using namespace tcg;
   if (a.M == 0 || a.N == 0) return cudaSuccess;
   if (!gemm_tc_supported(a)) return cudaErrorInvalidValue;
+  // The pair kernel needs K partitions that are whole 128-deep stages.
+  const bool use_pair = c.num_sms >= 2 && (a.parts == 1 || (a.K / a.parts) % P_BK == 0);
   CUtensorMap ma, mb;
-  if (!make_operand_map(&ma, a.A, a.M, a.K, BM) || !make_operand_map(&mb, a.B, a.N, a.K, BN))
+  if (use_pair) {
+    // every box is 64 wide and 128 deep (K-major: 128 rows of 64 K; MN-major:
+    // 128 K rows of 64 M or N)
+    auto pmap = [](CUtensorMap* m, const GemmOperand& op, int mn, int K) {
+      return op.k_major ? make_map(m, op.ptr, (uint64_t)K, (uint64_t)mn, op.ld, 64, 128)
+                        : make_map(m, op.ptr, (uint64_t)mn, (uint64_t)K, op.ld, 64, 128);
+    };
+    if (!pmap(&ma, a.A, a.M, a.K) || !pmap(&mb, a.B, a.N, a.K)) return cudaErrorInvalidValue;
+  } else if (!make_operand_map(&ma, a.A, a.M, a.K, BM) ||
+             !make_operand_map(&mb, a.B, a.N, a.K, BN)) {
     return cudaErrorInvalidValue;
+  }
   Params p;
   p.M = a.M;
   p.N = a.N;
   p.K = a.K;
   p.parts = a.parts;
   const bool reduce = a.parts > 1;
-  const int nkb = (a.K + BK - 1) / BK;
+  const int bk = use_pair ? P_BK : BK;
+  const int tile_m = use_pair ? 2 * P_HALF : BM;
+  const int nkb = (a.K + bk - 1) / bk;
   p.units_per_tile = reduce ? a.parts : 1;
-  p.kb_per_unit = reduce ? (a.K / a.parts) / BK : nkb;
+  p.kb_per_unit = reduce ? (a.K / a.parts) / bk : nkb;
   p.a_mn = a.A.k_major ? 0 : 1;
   p.b_mn = a.B.k_major ? 0 : 1;
-  p.tiles_m = (a.M + BM - 1) / BM;
+  p.tiles_m = (a.M + tile_m - 1) / tile_m;
   p.tiles_n = (a.N + BN - 1) / BN;
   p.num_tiles = p.tiles_m * p.tiles_n;
   p.bias = static_cast<const bf16*>(a.bias);
@@ -497,10 +717,12 @@ cudaError_t gemm_tc(const GemmArgs& a, const LaunchCtx& c) {
   p.C = a.C;
   p.ldc = a.ldc;
   p.status = a.status;
-  KernelFn fn = select_kernel(a.epi, a.c_f32, reduce);
+  KernelFn fn = use_pair ? select_kernel2(a.epi, a.c_f32, reduce)
+                         : select_kernel(a.epi, a.c_f32, reduce);
   if (!fn) return cudaErrorInvalidValue;
+  const int smem_bytes = use_pair ? P_SMEM_BYTES : SMEM_BYTES;
   cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
   // The warpgroup register split assumes exactly LAUNCH_REGS registers per
   // thread at launch; with fewer, setmaxnreg.inc could never be satisfied.
@@ -512,9 +734,15 @@ cudaError_t gemm_tc(const GemmArgs& a, const LaunchCtx& c) {
     // K == 0: nothing to accumulate; the kernel is not launched
     return cudaErrorInvalidValue;
   }
-  const int grid = p.num_tiles < c.num_sms ? p.num_tiles : c.num_sms;
+  int grid;
+  if (use_pair) {
+    const int pairs = c.num_sms / 2;
+    grid = 2 * (p.num_tiles < pairs ? p.num_tiles : pairs);
+  } else {
+    grid = p.num_tiles < c.num_sms ? p.num_tiles : c.num_sms;
+  }
   c.before(KK_GEMM_TC, 2.0 * a.M * a.N * a.K);
-  fn<<<grid, THREADS, SMEM_BYTES, c.stream>>>(ma, mb, p);
+  fn<<<grid, THREADS, smem_bytes, c.stream>>>(ma, mb, p);
   c.after();
   return cudaGetLastError();
 }
