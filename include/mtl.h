@@ -185,6 +185,13 @@ mtl_status mtl_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, int32_t k_pa
 mtl_status mtl_bias_grad_noalloc(int32_t dtype, const void* dy, int64_t ld, int32_t rows,
                                  int32_t cols, void* out, mtl_stream stream);
 
+/* Failure-detection self-test: launches one CTA that waits, with the same
+ * bounded device wait the pipelined kernels use, on a barrier nothing signals.
+ * After limit_cycles SM cycles (1000 .. 4e9) the wait gives up and records a
+ * timeout in the status word of `workspace` (>= 256 bytes), so a following
+ * mtl_layer_check returns MTL_ERR_TIMEOUT; the GPU context stays usable. */
+mtl_status mtl_selftest_wait_timeout(void* workspace, int64_t limit_cycles, mtl_stream stream);
+
 /* Human-readable name of a status. */
 const char* mtl_status_str(mtl_status s);
 

@@ -126,17 +126,18 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase with parity `parity` of barrier `bar` to complete.  Gives
-// up after kWaitLimitCycles (or at once if *abort is set by another role of the
-// CTA), records the timeout in the status word and sets *abort.  Returns false
-// when it gave up.
+// up after `limit` SM cycles (kWaitLimitCycles by default, or at once if *abort
+// is set by another role of the CTA), records the timeout in the status word
+// and sets *abort.  Returns false when it gave up.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  unsigned* status, volatile int* abort) {
+                                                  unsigned* status, volatile int* abort,
+                                                  long long limit = kWaitLimitCycles) {
   if (mbar_test_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       atomicOr(status, kDevErrTimeout);
       *abort = 1;
       return false;

@@ -487,6 +487,37 @@ mtl_status mtl_layer_check(void* workspace, mtl_stream stream) {
   return MTL_OK;
 }
 
+namespace {
+// One CTA waits, with the same bounded wait the pipelined kernels use, on an
+// mbarrier that nothing will ever arrive at.
+__global__ void selftest_wait_kernel(unsigned* status, long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait_bounded(smem_u32(&bar), 0, status, &abort_flag, limit);
+  __syncthreads();
+}
+}  // namespace
+
+mtl_status mtl_selftest_wait_timeout(void* workspace, int64_t limit_cycles, mtl_stream stream) {
+  g_launches = 0;
+  g_cuda_err[0] = 0;
+  if (!aligned16(workspace)) return MTL_ERR_INVALID_ARG;
+  if (limit_cycles < 1000 || limit_cycles > kWaitLimitCycles) return MTL_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned* status = static_cast<unsigned*>(workspace);
+  MTL_TRY(cudaMemsetAsync(status, 0, kStatusBytes, s), "status reset");
+  selftest_wait_kernel<<<1, 32, 0, s>>>(status, limit_cycles);
+  ++g_launches;
+  MTL_TRY(cudaGetLastError(), "selftest launch");
+  return MTL_OK;
+}
+
 mtl_status mtl_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, int32_t k_parts,
                     const void* A, int64_t lda, int32_t a_k_major, const void* B, int64_t ldb,
                     int32_t b_k_major, int32_t epi, const void* bias, const void* R, int64_t ldr,

@@ -69,6 +69,8 @@ def lib():
         L.mtl_layer_check.argtypes = [vp, vp]
         L.mtl_gemm.argtypes = [i32, i32, i32, i32, i32, vp, i64, i32, vp, i64, i32, i32, vp, vp,
                                i64, vp, i64, vp, i64, i32, vp, sz, vp]
+        L.mtl_selftest_wait_timeout.argtypes = [vp, i64, vp]
+        L.mtl_selftest_wait_timeout.restype = ctypes.c_int
         L.mtl_bias_grad_noalloc.argtypes = [i32, vp, i64, i32, i32, vp, vp]
         L.mtl_bias_grad_noalloc.restype = ctypes.c_int
         L.mtl_status_str.argtypes = [ctypes.c_int]
@@ -162,6 +164,12 @@ def gemm(dtype, M, N, K, parts, A, lda, a_k_major, B, ldb, b_k_major, epi, C, ld
                           ldc, int(c_f32), _ptr(workspace),
                           workspace.numel() * workspace.element_size(), _stream(stream)),
            "mtl_gemm")
+
+
+def selftest_wait_timeout(workspace, limit_cycles, stream=None):
+    """mtl_selftest_wait_timeout: a bounded device wait that is made to run out."""
+    _check(lib().mtl_selftest_wait_timeout(_ptr(workspace), limit_cycles, _stream(stream)),
+           "mtl_selftest_wait_timeout")
 
 
 def bias_grad_noalloc(dtype, dy, ld, rows, cols, out, stream=None):
