@@ -136,6 +136,17 @@ def traffic_record(kernel_file):
         return None
 
 
+def aggregate_over_ranks(ms, flops_per_step, steps, world, dist=None, device=None):
+    """Whole-job throughput of `world` replicas: the slowest rank's time over
+    the units all ranks processed.  Returns (max_ms, TFLOP/s)."""
+    if world > 1 and dist is not None:
+        import torch
+        t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, flops_per_step * steps * world / (ms / 1e3) / 1e12
+
+
 # ---------------------------------------------------------------- reference arm
 
 def run_reference(args, shape, rank, world):
@@ -252,25 +263,23 @@ def main():
     clocks.start()
     barrier()
     torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
+    evs_step = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    evs_step[0].record(stream)
     launches = 0
-    for _ in range(args.steps):
+    for i in range(args.steps):
         launches += step()
-    ev1.record(stream)
-    ev1.synchronize()
+        evs_step[i + 1].record(stream)
+    evs_step[-1].synchronize()
     torch.cuda.synchronize()
     barrier()
-    ms = ev0.elapsed_time(ev1)
+    ms = evs_step[0].elapsed_time(evs_step[-1])
+    per_step = sorted(evs_step[i].elapsed_time(evs_step[i + 1]) for i in range(args.steps))
     clk = clocks.stop()
     mtl.layer_check(ws)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    ms_step = ms / args.steps
     flops = layer_flops(shape)
-    value = flops * args.steps * world / (ms / 1e3) / 1e12
+    ms, value = aggregate_over_ranks(ms, flops, args.steps, world, dist if world > 1 else None,
+                                     "cuda")
+    ms_step = ms / args.steps
 
     # ---- end to end: host buffers in, results out, every step.  Each step's x
     # and dy are copied from pinned host memory and its y and dx are copied
@@ -321,11 +330,8 @@ def main():
     e1.synchronize()
     torch.cuda.synchronize()
     ms_e2e = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms_e2e], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t.item())
-    e2e_value = flops * args.steps * world / (ms_e2e / 1e3) / 1e12
+    ms_e2e, e2e_value = aggregate_over_ranks(ms_e2e, flops, args.steps, world,
+                                             dist if world > 1 else None, "cuda")
     nbytes = x_h.numel() * x_h.element_size()
 
     # ---- per-kernel times: the same steps again with events around every kernel
@@ -383,6 +389,8 @@ def main():
     out = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "step_ms": {"median": per_step[len(per_step) // 2], "min": per_step[0],
+                    "max": per_step[-1]},
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": shape.dtype, "data": "synthetic",
         "config": {"workload": f"{args.config}: {shape.name}, t={args.t}", "h": shape.h,
