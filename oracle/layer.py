@@ -48,6 +48,8 @@ import math
 import numpy as np
 from scipy.special import erf
 
+from . import philox
+
 LN_EPS = 1e-5
 
 
@@ -134,15 +136,22 @@ def attention_head_fwd(q, k, v):
     return p @ v, p, lse
 
 
-def attention_head_bwd(q, k, v, p, o, do):
+def attention_head_bwd(q, k, v, p, o, do, keep_scale=None):
     """Gradients of one causal head given do [s, d].  Returns (dq, dk, dv).
 
     dV = P^T dO; dP = dO V^T; with D_i = sum_j P_ij dP_ij (= sum_c dO_ic O_ic),
     dS = P * (dP - D); dQ = dS K / sqrt(d); dK = dS^T Q / sqrt(d).
+    With attention dropout (keep_scale = keep / (1 - p), o = (P * keep_scale) V):
+    dV = (P * keep_scale)^T dO, dP = (dO V^T) * keep_scale, and D still equals
+    rowsum(dO * O).
     """
     d = q.shape[1]
-    dv = p.T @ do
-    dp = do @ v.T
+    if keep_scale is None:
+        dv = p.T @ do
+        dp = do @ v.T
+    else:
+        dv = (p * keep_scale).T @ do
+        dp = (do @ v.T) * keep_scale
     dsum = (do * o).sum(axis=1, keepdims=True)
     ds = p * (dp - dsum)
     dq = ds @ k / math.sqrt(d)
@@ -161,12 +170,25 @@ def split_qkv_columns(qkv_row_block, n_heads, d):
     return blk[..., 0, :], blk[..., 1, :], blk[..., 2, :]
 
 
-def multihead_fwd(qkv, batch, seq, n_heads, d):
+def attention_keep_scale(b, head, heads_total, seq, drop):
+    """keep / (1 - p) of the attention probabilities of one head, or None."""
+    if not drop or drop.get("p_attn", 0.0) == 0.0:
+        return None
+    p = drop["p_attn"]
+    keep = philox.attention_mask(b, head, heads_total, seq, drop.get("seed", 0), p)
+    return keep / (1.0 - p)
+
+
+def multihead_fwd(qkv, batch, seq, n_heads, d, drop=None, head0=0, heads_total=None):
     """Attention over all heads of a head-interleaved qkv [n, 3 * n_heads * d].
 
     Returns ctx [n, n_heads * d] (column = head * d + channel), lse
-    [batch, n_heads, seq] and the probabilities for the backward.
+    [batch, n_heads, seq] and the probabilities for the backward.  With
+    attention dropout the output is (P * keep / (1 - p)) V; lse and the
+    returned probabilities are those of the undropped softmax.  head0 /
+    heads_total place these heads among the layer's for the dropout mask.
     """
+    heads_total = n_heads if heads_total is None else heads_total
     q, k, v = split_qkv_columns(qkv.reshape(batch, seq, -1), n_heads, d)
     ctx = np.empty((batch, seq, n_heads, d))
     lse = np.empty((batch, n_heads, seq))
@@ -174,22 +196,28 @@ def multihead_fwd(qkv, batch, seq, n_heads, d):
     for b in range(batch):
         for hd in range(n_heads):
             o, p, l = attention_head_fwd(q[b, :, hd], k[b, :, hd], v[b, :, hd])
+            ks = attention_keep_scale(b, head0 + hd, heads_total, seq, drop)
+            if ks is not None:
+                o = (p * ks) @ v[b, :, hd]
             ctx[b, :, hd] = o
             lse[b, hd] = l
             probs[b, hd] = p
     return ctx.reshape(batch * seq, n_heads * d), lse, probs
 
 
-def multihead_bwd(qkv, ctx, probs, dctx, batch, seq, n_heads, d):
+def multihead_bwd(qkv, ctx, probs, dctx, batch, seq, n_heads, d, drop=None, head0=0,
+                  heads_total=None):
     """Gradient of multihead_fwd: dctx [n, n_heads*d] -> dqkv [n, 3*n_heads*d]."""
+    heads_total = n_heads if heads_total is None else heads_total
     q, k, v = split_qkv_columns(qkv.reshape(batch, seq, -1), n_heads, d)
     o = ctx.reshape(batch, seq, n_heads, d)
     do = dctx.reshape(batch, seq, n_heads, d)
     dqkv = np.empty((batch, seq, n_heads, 3, d))
     for b in range(batch):
         for hd in range(n_heads):
+            ks = attention_keep_scale(b, head0 + hd, heads_total, seq, drop)
             dq, dk, dv = attention_head_bwd(q[b, :, hd], k[b, :, hd], v[b, :, hd],
-                                            probs[b, hd], o[b, :, hd], do[b, :, hd])
+                                            probs[b, hd], o[b, :, hd], do[b, :, hd], ks)
             dqkv[b, :, hd, 0] = dq
             dqkv[b, :, hd, 1] = dk
             dqkv[b, :, hd, 2] = dv
@@ -204,29 +232,45 @@ def _f64(a):
     return np.asarray(a, dtype=np.float64)
 
 
-def layer_fwd(params, x, heads, eps=LN_EPS):
+def hidden_keep_scale(n, h, drop, site):
+    """keep / (1 - p) of a hidden-state dropout site, [n, h], or 1.0."""
+    if not drop or drop.get("p_hidden", 0.0) == 0.0:
+        return 1.0
+    p = drop["p_hidden"]
+    return philox.hidden_mask(n, h, drop.get("seed", 0), site, p) / (1.0 - p)
+
+
+def layer_fwd(params, x, heads, eps=LN_EPS, dropout=None):
     """Pre-LN GPT layer forward.  x [batch, seq, h].  Returns (y, cache).
 
     u1 = LN1(x); qkv = u1 W_qkv^T + b_qkv; ctx = causal multi-head attention;
     x1 = x + ctx W_o^T + b_o; u2 = LN2(x1); z = u2 W_fc1^T + b_fc1; a = GeLU(z);
     y = x1 + a W_fc2^T + b_fc2.
+    dropout = dict(p_attn, p_hidden, seed) (optional): attention dropout on the
+    softmax probabilities, and the fused bias + dropout + residual ("Fused
+    Transformer Kernels") after the out-projection and after fc2:
+    x1 = x + drop(ctx W_o^T + b_o), y = x1 + drop(a W_fc2^T + b_fc2); masks as
+    in oracle/philox.py.
     """
     p = {k: _f64(v) for k, v in params.items()}
     x = _f64(x)
     batch, seq, h = x.shape
     d = h // heads
-    xf = x.reshape(batch * seq, h)
+    n = batch * seq
+    xf = x.reshape(n, h)
     u1, mu1, rstd1 = layernorm_fwd(xf, p["ln1_g"], p["ln1_b"], eps)
     qkv = u1 @ p["w_qkv"].T + p["b_qkv"]
-    ctx, lse, probs = multihead_fwd(qkv, batch, seq, heads, d)
-    x1 = xf + ctx @ p["w_o"].T + p["b_o"]
+    ctx, lse, probs = multihead_fwd(qkv, batch, seq, heads, d, dropout)
+    so = hidden_keep_scale(n, h, dropout, philox.SITE_OUT)
+    s2 = hidden_keep_scale(n, h, dropout, philox.SITE_FC2)
+    x1 = xf + (ctx @ p["w_o"].T + p["b_o"]) * so
     u2, mu2, rstd2 = layernorm_fwd(x1, p["ln2_g"], p["ln2_b"], eps)
     z = u2 @ p["w_fc1"].T + p["b_fc1"]
     a = gelu(z)
-    y = x1 + a @ p["w_fc2"].T + p["b_fc2"]
+    y = x1 + (a @ p["w_fc2"].T + p["b_fc2"]) * s2
     cache = dict(x=xf, u1=u1, mu1=mu1, rstd1=rstd1, qkv=qkv, ctx=ctx, lse=lse,
                  probs=probs, x1=x1, u2=u2, mu2=mu2, rstd2=rstd2, z=z, a=a,
-                 batch=batch, seq=seq, heads=heads)
+                 batch=batch, seq=seq, heads=heads, dropout=dropout, so=so, s2=s2)
     return y.reshape(batch, seq, h), cache
 
 
@@ -241,11 +285,13 @@ def layer_bwd(params, cache, dy):
     n, h = c["x"].shape
     d = h // heads
     dy = _f64(dy).reshape(n, h)
+    drop = c.get("dropout")
     g = {}
-    # MLP block: y = x1 + GeLU(u2 W1^T + b1) W2^T + b2
-    g["w_fc2"] = dy.T @ c["a"]
-    g["b_fc2"] = dy.sum(axis=0)
-    da = dy @ p["w_fc2"]
+    # MLP block: y = x1 + drop(GeLU(u2 W1^T + b1) W2^T + b2)
+    g2 = dy * c.get("s2", 1.0)
+    g["w_fc2"] = g2.T @ c["a"]
+    g["b_fc2"] = g2.sum(axis=0)
+    da = g2 @ p["w_fc2"]
     dz = da * gelu_grad(c["z"])
     g["w_fc1"] = dz.T @ c["u2"]
     g["b_fc1"] = dz.sum(axis=0)
@@ -253,11 +299,12 @@ def layer_bwd(params, cache, dy):
     dx1_ln, g["ln2_g"], g["ln2_b"] = layernorm_bwd(du2, c["x1"], c["mu2"], c["rstd2"],
                                                    p["ln2_g"])
     dx1 = dy + dx1_ln
-    # attention block: x1 = x + Attn(u1 W_qkv^T + b_qkv) W_o^T + b_o
-    g["w_o"] = dx1.T @ c["ctx"]
-    g["b_o"] = dx1.sum(axis=0)
-    dctx = dx1 @ p["w_o"]
-    dqkv = multihead_bwd(c["qkv"], c["ctx"], c["probs"], dctx, batch, seq, heads, d)
+    # attention block: x1 = x + drop(Attn(u1 W_qkv^T + b_qkv) W_o^T + b_o)
+    go = dx1 * c.get("so", 1.0)
+    g["w_o"] = go.T @ c["ctx"]
+    g["b_o"] = go.sum(axis=0)
+    dctx = go @ p["w_o"]
+    dqkv = multihead_bwd(c["qkv"], c["ctx"], c["probs"], dctx, batch, seq, heads, d, drop)
     g["w_qkv"] = dqkv.T @ c["u1"]
     g["b_qkv"] = dqkv.sum(axis=0)
     du1 = dqkv @ p["w_qkv"]
@@ -317,7 +364,7 @@ def shard_ranges(h, ffn, heads, t):
     return out
 
 
-def layer_fwd_partitioned(params, x, heads, t, counter, eps=LN_EPS):
+def layer_fwd_partitioned(params, x, heads, t, counter, eps=LN_EPS, dropout=None):
     """Forward with the layer split over t ranks; returns (y, cache).
 
     Each rank holds the replicated input (f forward = identity), computes its
@@ -332,15 +379,19 @@ def layer_fwd_partitioned(params, x, heads, t, counter, eps=LN_EPS):
     ffn = p["w_fc1"].shape[0]
     d = h // heads
     xf = x.reshape(batch * seq, h)
+    n = batch * seq
     ranks = shard_ranges(h, ffn, heads, t)
+    so = hidden_keep_scale(n, h, dropout, philox.SITE_OUT)
+    s2 = hidden_keep_scale(n, h, dropout, philox.SITE_FC2)
     u1, mu1, rstd1 = layernorm_fwd(xf, p["ln1_g"], p["ln1_b"], eps)
     parts, rank_cache = [], []
-    for rk in ranks:
+    for r, rk in enumerate(ranks):
         qkv_r = u1 @ p["w_qkv"][rk["qkv"]].T + p["b_qkv"][rk["qkv"]]
-        ctx_r, lse_r, probs_r = multihead_fwd(qkv_r, batch, seq, rk["heads"], d)
+        ctx_r, lse_r, probs_r = multihead_fwd(qkv_r, batch, seq, rk["heads"], d, dropout,
+                                              r * rk["heads"], heads)
         parts.append(ctx_r @ p["w_o"][:, rk["ctx"]].T)
         rank_cache.append(dict(qkv=qkv_r, ctx=ctx_r, lse=lse_r, probs=probs_r))
-    x1 = xf + g_allreduce(parts, counter) + p["b_o"]
+    x1 = xf + (g_allreduce(parts, counter) + p["b_o"]) * so
     u2, mu2, rstd2 = layernorm_fwd(x1, p["ln2_g"], p["ln2_b"], eps)
     parts = []
     for rk, rc in zip(ranks, rank_cache):
@@ -348,10 +399,10 @@ def layer_fwd_partitioned(params, x, heads, t, counter, eps=LN_EPS):
         a_r = gelu(z_r)
         parts.append(a_r @ p["w_fc2"][:, rk["ffn"]].T)
         rc.update(z=z_r, a=a_r)
-    y = x1 + g_allreduce(parts, counter) + p["b_fc2"]
+    y = x1 + (g_allreduce(parts, counter) + p["b_fc2"]) * s2
     cache = dict(x=xf, u1=u1, mu1=mu1, rstd1=rstd1, x1=x1, u2=u2, mu2=mu2,
                  rstd2=rstd2, ranks=ranks, rank_cache=rank_cache, batch=batch,
-                 seq=seq, heads=heads, t=t)
+                 seq=seq, heads=heads, t=t, dropout=dropout, so=so, s2=s2)
     return y.reshape(batch, seq, h), cache
 
 
@@ -369,13 +420,15 @@ def layer_bwd_partitioned(params, cache, dy, counter):
     ffn = p["w_fc1"].shape[0]
     d = h // heads
     dy = _f64(dy).reshape(n, h)
+    drop = c.get("dropout")
+    g2 = dy * c.get("s2", 1.0)
     g = {k: np.zeros_like(v) for k, v in p.items()}
-    g["b_fc2"] = dy.sum(axis=0)
+    g["b_fc2"] = g2.sum(axis=0)
     parts = []
     for rk, rc in zip(c["ranks"], c["rank_cache"]):
         s = rk["ffn"]
-        g["w_fc2"][:, s] = dy.T @ rc["a"]
-        dz_r = (dy @ p["w_fc2"][:, s]) * gelu_grad(rc["z"])
+        g["w_fc2"][:, s] = g2.T @ rc["a"]
+        dz_r = (g2 @ p["w_fc2"][:, s]) * gelu_grad(rc["z"])
         g["w_fc1"][s] = dz_r.T @ c["u2"]
         g["b_fc1"][s] = dz_r.sum(axis=0)
         parts.append(dz_r @ p["w_fc1"][s])
@@ -383,14 +436,15 @@ def layer_bwd_partitioned(params, cache, dy, counter):
     dx1_ln, g["ln2_g"], g["ln2_b"] = layernorm_bwd(du2, c["x1"], c["mu2"], c["rstd2"],
                                                    p["ln2_g"])
     dx1 = dy + dx1_ln
-    g["b_o"] = dx1.sum(axis=0)
+    go = dx1 * c.get("so", 1.0)
+    g["b_o"] = go.sum(axis=0)
     parts = []
-    for rk, rc in zip(c["ranks"], c["rank_cache"]):
+    for r, (rk, rc) in enumerate(zip(c["ranks"], c["rank_cache"])):
         sc, sq = rk["ctx"], rk["qkv"]
-        g["w_o"][:, sc] = dx1.T @ rc["ctx"]
-        dctx_r = dx1 @ p["w_o"][:, sc]
+        g["w_o"][:, sc] = go.T @ rc["ctx"]
+        dctx_r = go @ p["w_o"][:, sc]
         dqkv_r = multihead_bwd(rc["qkv"], rc["ctx"], rc["probs"], dctx_r, batch, seq,
-                               rk["heads"], d)
+                               rk["heads"], d, drop, r * rk["heads"], heads)
         g["w_qkv"][sq] = dqkv_r.T @ c["u1"]
         g["b_qkv"][sq] = dqkv_r.sum(axis=0)
         parts.append(dqkv_r @ p["w_qkv"][sq])

@@ -408,3 +408,179 @@ def test_gemm_partitioned_pins():
     assert rel_err(c4, full * oracle.gelu_grad(R)) < 1e-14
     with pytest.raises(ValueError):
         oracle.gemm_partitioned(A, B, 5)
+
+
+# ---------------------------------------------------------------- dropout (Philox masks)
+
+def test_philox_known_answers():
+    gold = json.load(open(os.path.join(GOLDEN, "philox_kat.json")))
+    for v in gold["vectors"]:
+        ctr = np.array([int(c, 16) for c in v["counter"]], dtype=np.uint32)
+        key = [int(k, 16) for k in v["key"]]
+        out = oracle.philox.philox4x32(ctr, key)
+        assert [int(o) for o in out] == [int(o, 16) for o in v["out"]]
+
+
+def test_philox_word_layout():
+    """word(e) is lane e mod 4 of the block at counter (e div 4, site); seed splits into the key."""
+    seed = (0x01234567 << 32) | 0x89ABCDEF
+    e = np.arange(4 * 3, dtype=np.uint64) + np.uint64((1 << 34) + 8)
+    w = oracle.philox.words(e, seed, 2)
+    for i, ei in enumerate(e.tolist()):
+        ctr = np.array([(ei >> 2) & 0xFFFFFFFF, ei >> 34, 2, 0], dtype=np.uint32)
+        blk = oracle.philox.philox4x32(ctr, (0x89ABCDEF, 0x01234567))
+        assert int(w[i]) == int(blk[ei & 3])
+
+
+def test_dropout_mask_statistics():
+    """Keep fraction 1 - p within 5 sigma; the words are uniform (mean, decile counts)."""
+    n = 1 << 18
+    e = np.arange(n, dtype=np.uint64)
+    w = oracle.philox.words(e, 1234, 1).astype(np.float64) / 2.0 ** 32
+    assert abs(w.mean() - 0.5) < 5 * math.sqrt(1 / 12 / n)
+    counts = np.histogram(w, bins=10, range=(0, 1))[0]
+    chi2 = float(((counts - n / 10) ** 2 / (n / 10)).sum())
+    assert chi2 < 40.0          # 9 degrees of freedom; P(chi2 > 40) < 1e-5
+    for p in (0.1, 0.5, 0.9):
+        keep = oracle.philox.keep_mask(e, 99, 0, p)
+        assert abs(keep.mean() - (1 - p)) < 5 * math.sqrt(p * (1 - p) / n)
+    # different sites and seeds give different masks
+    a = oracle.philox.keep_mask(e[:4096], 7, 1, 0.5)
+    b = oracle.philox.keep_mask(e[:4096], 7, 2, 0.5)
+    c = oracle.philox.keep_mask(e[:4096], 8, 1, 0.5)
+    assert 0.4 < (a != b).mean() < 0.6 and 0.4 < (a != c).mean() < 0.6
+    assert oracle.philox.threshold(0.0) == 0 and oracle.philox.threshold(0.5) == 1 << 31
+    with pytest.raises(ValueError):
+        oracle.philox.threshold(1.0)
+
+
+def test_dropout_zero_is_the_plain_layer():
+    shp, x, p, dy = small_layer()
+    y0, c0 = oracle.layer_fwd(p, x, shp.heads)
+    dx0, g0, _ = oracle.layer_bwd(p, c0, dy)
+    drop = dict(p_attn=0.0, p_hidden=0.0, seed=5)
+    y1, c1 = oracle.layer_fwd(p, x, shp.heads, dropout=drop)
+    dx1, g1, _ = oracle.layer_bwd(p, c1, dy)
+    assert np.array_equal(y0, y1) and np.array_equal(dx0, dx1)
+    for k in g0:
+        assert np.array_equal(g0[k], g1[k])
+
+
+def test_hidden_dropout_zeroes_and_rescales():
+    """With only hidden dropout, y - x1 is 0 where dropped and (fc2 out) / (1 - p) where kept."""
+    shp, x, p, dy = small_layer()
+    drop = dict(p_attn=0.0, p_hidden=0.3, seed=11)
+    y, c = oracle.layer_fwd(p, x, shp.heads, dropout=drop)
+    n, h = c["x"].shape
+    keep = oracle.philox.hidden_mask(n, h, 11, oracle.philox.SITE_FC2, 0.3)
+    r = y.reshape(n, h) - c["x1"]
+    fc2 = c["a"] @ p["w_fc2"].T + p["b_fc2"]
+    assert np.all(r[~keep] == 0.0)
+    assert np.allclose(r[keep], fc2[keep] / 0.7, rtol=1e-12, atol=1e-12)
+    assert 0.55 < keep.mean() < 0.85
+
+
+def test_attention_dropout_is_unbiased():
+    """Averaged over seeds, dropped attention approaches the undropped output."""
+    rng = np.random.default_rng(0)
+    seq, d, heads = 8, 4, 2
+    qkv = rng.standard_normal((seq, 3 * heads * d))
+    ref, _, _ = oracle.multihead_fwd(qkv, 1, seq, heads, d)
+    runs = 400
+    acc = np.zeros_like(ref)
+    for s in range(runs):
+        out, _, _ = oracle.multihead_fwd(qkv, 1, seq, heads, d, dict(p_attn=0.2, seed=s))
+        acc += out
+    assert np.max(np.abs(acc / runs - ref)) < 0.15
+    one, _, _ = oracle.multihead_fwd(qkv, 1, seq, heads, d, dict(p_attn=0.2, seed=3))
+    assert not np.allclose(one, ref)
+
+
+def _torch_layer_dropout(p, x, heads, mo, m2, ma, p_attn, p_hidden):
+    """Float64 torch forward with the given keep masks (test-only, written independently)."""
+    import torch
+    import torch.nn.functional as F
+    b, s, h = x.shape
+    d = h // heads
+    u1 = F.layer_norm(x, (h,), p["ln1_g"], p["ln1_b"], eps=1e-5)
+    qkv = F.linear(u1, p["w_qkv"], p["b_qkv"]).view(b, s, heads, 3, d)
+    q, k, v = (qkv[:, :, :, i].transpose(1, 2) for i in range(3))
+    sc = q @ k.transpose(-1, -2) / math.sqrt(d)
+    causal = torch.ones(s, s, dtype=torch.bool).tril()
+    prob = torch.softmax(sc.masked_fill(~causal, float("-inf")), dim=-1)
+    o = (prob * ma / (1 - p_attn)) @ v
+    ctx = o.transpose(1, 2).reshape(b, s, h)
+    x1 = x + F.linear(ctx, p["w_o"], p["b_o"]) * mo / (1 - p_hidden)
+    u2 = F.layer_norm(x1, (h,), p["ln2_g"], p["ln2_b"], eps=1e-5)
+    fc2 = F.linear(F.gelu(F.linear(u2, p["w_fc1"], p["b_fc1"])), p["w_fc2"], p["b_fc2"])
+    return x1 + fc2 * m2 / (1 - p_hidden)
+
+
+def test_dropout_layer_matches_torch_autograd():
+    torch = pytest.importorskip("torch")
+    shp, x, p, dy = small_layer(h=32, heads=4, seq=12, batch=2)
+    pa, ph, seed = 0.25, 0.15, 77
+    drop = dict(p_attn=pa, p_hidden=ph, seed=seed)
+    y_ref, cache = oracle.layer_fwd(p, x, shp.heads, dropout=drop)
+    dx_ref, g_ref, _ = oracle.layer_bwd(p, cache, dy)
+    b, s, h = x.shape
+    ph_ = oracle.philox
+    mo = ph_.hidden_mask(b * s, h, seed, ph_.SITE_OUT, ph).reshape(b, s, h)
+    m2 = ph_.hidden_mask(b * s, h, seed, ph_.SITE_FC2, ph).reshape(b, s, h)
+    ma = np.stack([np.stack([ph_.attention_mask(bb, hd, shp.heads, s, seed, pa)
+                             for hd in range(shp.heads)]) for bb in range(b)])
+    T = lambda a: torch.tensor(a, dtype=torch.float64)  # noqa: E731
+    tp = {k: torch.tensor(v, dtype=torch.float64, requires_grad=True) for k, v in p.items()}
+    tx = torch.tensor(x, dtype=torch.float64, requires_grad=True)
+    ty = _torch_layer_dropout(tp, tx, shp.heads, T(mo), T(m2), T(ma), pa, ph)
+    ty.backward(T(dy))
+    assert rel_err(ty.detach().numpy(), y_ref) < 1e-12
+    assert rel_err(tx.grad.numpy(), dx_ref) < 1e-11
+    for k in g_ref:
+        assert rel_err(tp[k].grad.numpy(), g_ref[k]) < 1e-11, k
+
+
+def test_dropout_layer_backward_finite_differences():
+    shp = synthetic.tiny(h=16, heads=4, seq=5, batch=2, ffn=64, dtype="f32",
+                         w_std=0.3, out_std=0.3)
+    x, p, dy = synthetic.make_layer(shp, seed=6, affine=True)
+    x = x.astype(np.float64)
+    p = {k: v.astype(np.float64) for k, v in p.items()}
+    dy = dy.astype(np.float64)
+    drop = dict(p_attn=0.3, p_hidden=0.2, seed=2024)
+    _, cache = oracle.layer_fwd(p, x, shp.heads, dropout=drop)
+    dx, g, _ = oracle.layer_bwd(p, cache, dy)
+
+    def loss():
+        return float((oracle.layer_fwd(p, x, shp.heads, dropout=drop)[0] * dy).sum())
+
+    eps = 1e-6
+    for name, arr, grad in [("x", x, dx), ("w_qkv", p["w_qkv"], g["w_qkv"]),
+                            ("b_o", p["b_o"], g["b_o"]), ("w_fc2", p["w_fc2"], g["w_fc2"]),
+                            ("ln1_g", p["ln1_g"], g["ln1_g"])]:
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            old = arr[idx]
+            arr[idx] = old + eps
+            lp = loss()
+            arr[idx] = old - eps
+            lm = loss()
+            arr[idx] = old
+            fd[idx] = (lp - lm) / (2 * eps)
+        assert rel_err(fd, grad) <= 1e-6, name
+
+
+@pytest.mark.parametrize("t", [1, 2, 4])
+def test_split_identity_with_dropout(t):
+    """The partitioned layer draws the same masks: head masks use the layer-wide head index."""
+    shp = synthetic.tiny(h=64, heads=8, seq=16, batch=2, dtype="f32", w_std=0.1, out_std=0.1)
+    x, p, dy = synthetic.make_layer(shp, seed=1, affine=True)
+    drop = dict(p_attn=0.2, p_hidden=0.1, seed=31337)
+    y_ref, cache = oracle.layer_fwd(p, x, shp.heads, dropout=drop)
+    dx_ref, g_ref, _ = oracle.layer_bwd(p, cache, dy)
+    cnt = oracle.ReductionCounter()
+    y, pc = oracle.layer_fwd_partitioned(p, x, shp.heads, t, cnt, dropout=drop)
+    dx, g = oracle.layer_bwd_partitioned(p, pc, dy, cnt)
+    assert rel_err(y, y_ref) <= 1e-12 and rel_err(dx, dx_ref) <= 1e-12
+    for k in g_ref:
+        assert rel_err(g[k], g_ref[k]) <= 1e-12, (t, k)
