@@ -15,7 +15,7 @@
  *   * "Paper 1: QKV Column-Parallel Splitting in Detail": the fused QKV weight is
  *     head-interleaved, so partition p owns heads [p*H/t, (p+1)*H/t) whole.
  *   * "Fused Transformer Kernels": causal scale-mask-softmax, bias+GeLU and
- *     bias+residual fused into the GEMMs.
+ *     bias+dropout+residual fused into the GEMMs.
  *
  * On one GPU the t partitions are a layout: partition p's shard is a view (a
  * row block of w_qkv / w_fc1, a column block of w_o / w_fc2 and the matching
@@ -40,7 +40,18 @@
  *     OVERWRITTEN, not accumulated.  bf16 math accumulates in fp32.
  *   * GeLU is the exact x*Phi(x) (erf) form; the softmax scale is 1/sqrt(d);
  *     keys after the query are excluded (probability 0); LayerNorm uses the
- *     biased variance with desc.ln_eps inside the square root; dropout is 0.
+ *     biased variance with desc.ln_eps inside the square root.
+ *   * Dropout (desc.p_attn on the attention probabilities, desc.p_hidden after
+ *     the out-projection and after fc2, each before its residual add):
+ *       x1 = x  + drop_1(ctx W_o^T + b_o),   y = x1 + drop_2(a W_fc2^T + b_fc2),
+ *       ctx = (P * keep_0 / (1 - p_attn)) V  (lse stays that of the undropped P).
+ *     keep_s(e) = word_s(e) >= floor(p * 2^32) with word_s(e) = output word
+ *     (e mod 4) of Philox4x32-10 at counter {e/4 mod 2^32, e/4 >> 32, s, 0} and
+ *     key {seed mod 2^32, seed >> 32} (Salmon et al., SC'11).  Site s = 0:
+ *     attention, e = ((b*heads + head)*seq + i)*seq + j for query i, key j;
+ *     s = 1: out-projection output, s = 2: fc2 output, e = token*h + column.
+ *     Masks are recomputed from (seed, e) in the backward, never stored, so
+ *     mtl_layer_bwd must get the desc (seed, p) of the forward it follows.
  *   * Every pointer must be 16-byte aligned.  Validation failures return before
  *     anything is enqueued.  No C++ exception crosses this boundary.  Calls are
  *     reentrant; calls on different streams may run concurrently as long as
@@ -81,9 +92,12 @@ typedef enum { MTL_F32 = 0, MTL_BF16 = 1 } mtl_dtype;
  * CUDA-core kernels and need only h % 4 == 0 and ffn % 4 == 0. */
 typedef struct {
   int32_t h, heads, seq, batch, ffn, t;
-  int32_t dtype;   /* mtl_dtype */
-  float ln_eps;    /* 1e-5 */
-  int32_t causal;  /* 1 */
+  int32_t dtype;     /* mtl_dtype */
+  float ln_eps;      /* 1e-5 */
+  int32_t causal;    /* 1 */
+  float p_attn;      /* attention dropout probability, 0 <= p_attn < 1 */
+  float p_hidden;    /* hidden dropout probability, 0 <= p_hidden < 1 */
+  uint64_t seed;     /* Philox key of the dropout masks */
 } mtl_layer_desc;
 
 typedef struct {
@@ -161,6 +175,28 @@ mtl_status mtl_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, int32_t k_pa
                     int32_t epi, const void* bias, const void* R, int64_t ldr,
                     void* Z, int64_t ldz, void* C, int64_t ldc, int32_t c_f32,
                     void* workspace, size_t ws_bytes, mtl_stream stream);
+
+/* Causal multi-head attention, the layer's attention step on its own (same
+ * kernels, same dropout numbering with site 0):
+ *   qkv [batch*seq][3*heads*d], head-interleaved (column = head*3d +
+ *   {0:Q,1:K,2:V}*d + channel); ctx [batch*seq][heads*d]; lse
+ *   [batch][heads][seq] fp32 (natural log of the undropped softmax normaliser).
+ *   Forward: ctx = (softmax(Q K^T / sqrt d, causal) * keep / (1 - p_attn)) V.
+ *   Backward: dqkv [batch*seq][3*heads*d] (same interleave) from dctx, given
+ *   the forward's qkv, ctx and lse and the same p_attn and seed.
+ * dtype MTL_BF16 (tcgen05 kernels; seq % 128 == 0) or MTL_F32 (CUDA cores;
+ * seq <= 8192); d in {64, 96, 128}; 0 <= p_attn < 1.  Device pointers, 16-byte
+ * aligned.  workspace: >= mtl_attention_ws_bytes (status word and the
+ * backward's row sums D_i = dO_i . O_i); check it with mtl_layer_check.
+ * Errors as for the layer calls. */
+mtl_status mtl_attention_ws_bytes(int32_t batch, int32_t seq, int32_t heads, size_t* bytes);
+mtl_status mtl_attention_fwd(int32_t dtype, int32_t batch, int32_t seq, int32_t heads, int32_t d,
+                             const void* qkv, void* ctx, float* lse, float p_attn, uint64_t seed,
+                             void* workspace, size_t ws_bytes, mtl_stream stream);
+mtl_status mtl_attention_bwd(int32_t dtype, int32_t batch, int32_t seq, int32_t heads, int32_t d,
+                             const void* qkv, const void* ctx, const float* lse, const void* dctx,
+                             void* dqkv, float p_attn, uint64_t seed, void* workspace,
+                             size_t ws_bytes, mtl_stream stream);
 
 /* Bias gradient for callers that cannot allocate device memory:
  *   out[j] = sum_{i < rows} dy[i*ld + j]   (j < cols; fp32, fixed order)

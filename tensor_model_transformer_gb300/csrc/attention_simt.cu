@@ -26,10 +26,17 @@ __device__ __forceinline__ float dot_row(const float* __restrict__ a_smem,
 
 // grid (ceil(seq / rows_per_block), heads, batch); dynamic smem: kWarps*seq
 // floats of scores + kWarps*d floats of query.
+// Attention dropout numbering: element (query i, key j) of head hd, batch b is
+// e = ((b * heads + hd) * seq + i) * seq + j.
+__device__ __forceinline__ unsigned long long drop_index(int b, int hd, int heads, int seq, int i,
+                                                         int j) {
+  return (((unsigned long long)b * heads + hd) * seq + i) * (unsigned long long)seq + j;
+}
+
 template <typename T>
 __global__ void attn_fwd_simt_kernel(const T* __restrict__ qkv, T* __restrict__ ctx,
                                      float* __restrict__ lse, int seq, int heads, int d,
-                                     int rows_per_block) {
+                                     int rows_per_block, Dropout drop) {
   extern __shared__ float sm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float* sc = sm + warp * seq;
@@ -58,6 +65,11 @@ __global__ void attn_fwd_simt_kernel(const T* __restrict__ qkv, T* __restrict__ 
       sum += e;
     }
     sum = warp_sum(sum);
+    if (drop.on) {
+      // O = (P * keep / (1 - p)) V; the row sum stays that of the undropped P
+      for (int j = lane; j <= i; j += 32)
+        sc[j] = drop_keep(drop_index(b, head, heads, seq, i, j), drop) ? sc[j] * drop.scale : 0.f;
+    }
     __syncwarp();
     float o[kMaxDPerLane];
 #pragma unroll
@@ -88,7 +100,7 @@ template <typename T>
 __global__ void attn_bwd_dq_simt_kernel(const T* __restrict__ qkv, const T* __restrict__ ctx,
                                         const float* __restrict__ lse, const T* __restrict__ dctx,
                                         T* __restrict__ dqkv, float* __restrict__ dsum, int seq,
-                                        int heads, int d, int rows_per_block) {
+                                        int heads, int d, int rows_per_block, Dropout drop) {
   extern __shared__ float sm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float* sc = sm + warp * seq;
@@ -116,7 +128,8 @@ __global__ void attn_bwd_dq_simt_kernel(const T* __restrict__ qkv, const T* __re
     for (int j = lane; j <= i; j += 32) {
       const float s = dot_row<T>(qs, base + (size_t)j * ld + d, d) * scale;
       const float p = expf(s - li);
-      const float dp = dot_row<T>(dos, base + (size_t)j * ld + 2 * d, d);
+      float dp = dot_row<T>(dos, base + (size_t)j * ld + 2 * d, d);
+      if (drop.on) dp = drop_keep(drop_index(b, head, heads, seq, i, j), drop) ? dp * drop.scale : 0.f;
       sc[j] = p * (dp - Di);
     }
     __syncwarp();
@@ -148,7 +161,7 @@ template <typename T>
 __global__ void attn_bwd_dkv_simt_kernel(const T* __restrict__ qkv, const float* __restrict__ lse,
                                          const T* __restrict__ dctx, const float* __restrict__ dsum,
                                          T* __restrict__ dqkv, int seq, int heads, int d,
-                                         int rows_per_block) {
+                                         int rows_per_block, Dropout drop) {
   extern __shared__ float sm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float* sp = sm + warp * 2 * seq;
@@ -174,8 +187,14 @@ __global__ void attn_bwd_dkv_simt_kernel(const T* __restrict__ qkv, const float*
     for (int i = j + lane; i < seq; i += 32) {
       const float s = dot_row<T>(ks, base + (size_t)i * ld, d) * scale;
       const float p = expf(s - lrow[i]);
-      const float dp = dot_row<T>(vs, dob + (size_t)i * h, d);
-      sp[i] = p;
+      float dp = dot_row<T>(vs, dob + (size_t)i * h, d);
+      float pd = p;
+      if (drop.on) {
+        const bool kept = drop_keep(drop_index(b, head, heads, seq, i, j), drop);
+        pd = kept ? p * drop.scale : 0.f;
+        dp = kept ? dp * drop.scale : 0.f;
+      }
+      sp[i] = pd;
       sds[i] = p * (dp - drow[i]);
     }
     __syncwarp();
@@ -212,7 +231,7 @@ constexpr int kRowsPerBlock = 16;
 
 template <typename T>
 cudaError_t fwd_t(const void* qkv, void* ctx, float* lse, int batch, int seq, int heads, int d,
-                  const LaunchCtx& c) {
+                  const Dropout& drop, const LaunchCtx& c) {
   dim3 grid((seq + kRowsPerBlock - 1) / kRowsPerBlock, heads, batch);
   const size_t smem = (size_t)kWarps * (seq + d) * sizeof(float);
   if (smem > 48 * 1024) {
@@ -222,7 +241,7 @@ cudaError_t fwd_t(const void* qkv, void* ctx, float* lse, int batch, int seq, in
   }
   c.before(KK_ATTN_FWD, 2.0 * batch * (double)seq * (seq + 1) * heads * d);
   attn_fwd_simt_kernel<T><<<grid, kWarps * 32, smem, c.stream>>>((const T*)qkv, (T*)ctx, lse, seq,
-                                                                 heads, d, kRowsPerBlock);
+                                                                 heads, d, kRowsPerBlock, drop);
   c.after();
   return cudaGetLastError();
 }
@@ -230,7 +249,7 @@ cudaError_t fwd_t(const void* qkv, void* ctx, float* lse, int batch, int seq, in
 template <typename T>
 cudaError_t bwd_t(const void* qkv, const void* ctx, const float* lse, const void* dctx,
                   void* dqkv, float* dsum, int batch, int seq, int heads, int d,
-                  const LaunchCtx& c) {
+                  const Dropout& drop, const LaunchCtx& c) {
   dim3 grid((seq + kRowsPerBlock - 1) / kRowsPerBlock, heads, batch);
   const size_t smem1 = (size_t)kWarps * (seq + 2 * d) * sizeof(float);
   const size_t smem2 = (size_t)kWarps * (2 * seq + 2 * d) * sizeof(float);
@@ -249,11 +268,12 @@ cudaError_t bwd_t(const void* qkv, const void* ctx, const float* lse, const void
   c.before(KK_ATTN_BWD, 2.0 * 2.0 * tri);
   attn_bwd_dq_simt_kernel<T><<<grid, kWarps * 32, smem1, c.stream>>>(
       (const T*)qkv, (const T*)ctx, lse, (const T*)dctx, (T*)dqkv, dsum, seq, heads, d,
-      kRowsPerBlock);
+      kRowsPerBlock, drop);
   c.after();
   c.before(KK_ATTN_BWD, 2.0 * 4.0 * tri);
   attn_bwd_dkv_simt_kernel<T><<<grid, kWarps * 32, smem2, c.stream>>>(
-      (const T*)qkv, lse, (const T*)dctx, dsum, (T*)dqkv, seq, heads, d, kRowsPerBlock);
+      (const T*)qkv, lse, (const T*)dctx, dsum, (T*)dqkv, seq, heads, d, kRowsPerBlock,
+      drop);
   c.after();
   return cudaGetLastError();
 }
@@ -261,18 +281,19 @@ cudaError_t bwd_t(const void* qkv, const void* ctx, const float* lse, const void
 }  // namespace
 
 cudaError_t attn_fwd_simt(int dtype, const void* qkv, void* ctx, float* lse, int batch, int seq,
-                          int heads, int d, const LaunchCtx& c) {
+                          int heads, int d, const Dropout& drop, const LaunchCtx& c) {
   if (batch == 0 || seq == 0) return cudaSuccess;
-  return dtype == kBF16 ? fwd_t<bf16>(qkv, ctx, lse, batch, seq, heads, d, c)
-                        : fwd_t<float>(qkv, ctx, lse, batch, seq, heads, d, c);
+  return dtype == kBF16 ? fwd_t<bf16>(qkv, ctx, lse, batch, seq, heads, d, drop, c)
+                        : fwd_t<float>(qkv, ctx, lse, batch, seq, heads, d, drop, c);
 }
 
 cudaError_t attn_bwd_simt(int dtype, const void* qkv, const void* ctx, const float* lse,
                           const void* dctx, void* dqkv, float* dsum, int batch, int seq,
-                          int heads, int d, const LaunchCtx& c) {
+                          int heads, int d, const Dropout& drop, const LaunchCtx& c) {
   if (batch == 0 || seq == 0) return cudaSuccess;
-  return dtype == kBF16 ? bwd_t<bf16>(qkv, ctx, lse, dctx, dqkv, dsum, batch, seq, heads, d, c)
-                        : bwd_t<float>(qkv, ctx, lse, dctx, dqkv, dsum, batch, seq, heads, d, c);
+  return dtype == kBF16
+             ? bwd_t<bf16>(qkv, ctx, lse, dctx, dqkv, dsum, batch, seq, heads, d, drop, c)
+             : bwd_t<float>(qkv, ctx, lse, dctx, dqkv, dsum, batch, seq, heads, d, drop, c);
 }
 
 }  // namespace mtl

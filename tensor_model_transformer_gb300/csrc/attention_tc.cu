@@ -12,6 +12,10 @@
 //   lse = log sum exp(S) per query row.
 //   Backward: D_i = sum_c dO_ic O_ic;  dS = P * (dO V^T - D);  dQ = dS K / sqrt d;
 //   dK = dS^T Q / sqrt d;  dV = P^T dO.
+// With attention dropout (keep mask M from the Philox stream, scale 1/(1-p)):
+//   O = (P * M / (1-p)) V, lse still that of the undropped P;
+//   dV = (P * M / (1-p))^T dO;  dS = P * ((dO V^T) * M / (1-p) - D).
+// The masks are recomputed in every kernel, never stored.
 //
 // All three kernels: one CTA per 128-row block, 192 threads:
 //   warp 0      TMA producer
@@ -47,7 +51,15 @@ struct Params {
   bf16* dqkv;
   float* dsum;
   unsigned* status;
+  Dropout drop;       // attention dropout: element (query i, key j) of head hd, batch b
+                      // is e = ((b * heads + hd) * seq + i) * seq + j
 };
+
+// First element index of query row i, head hd, batch b in the attention
+// dropout numbering.
+__device__ __forceinline__ unsigned long long drop_row(const Params& p, int b, int hd, int i) {
+  return (((unsigned long long)b * p.heads + hd) * p.seq + i) * (unsigned long long)p.seq;
+}
 
 struct Smem {
   uint8_t* base;
@@ -281,6 +293,16 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
           rsp[k & 7] += s[k];
         }
         l = l * alpha + (((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7])));
+        if (p.drop.on) {
+          // dropped probabilities leave the row sum but not P V
+          const unsigned long long e0 = drop_row(p, b, hd, qb * 128 + r) + j * 128 + wg * 64;
+          const uint32_t lo = drop_bits32(e0, p.drop), hi = drop_bits32(e0 + 32, p.drop);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            if (!((lo >> k) & 1u)) s[k] = 0.f;
+            if (!((hi >> k) & 1u)) s[32 + k] = 0.f;
+          }
+        }
         if (j > 0) {
           if (!mbar_wait_bounded(B(ODONE), (gg - 1) & 1, p.status, abort_flag)) {
             ok = false;
@@ -326,7 +348,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         break;
       }
       const float lt = ls[r] + ls[128 + r];
-      const float inv = 1.0f / lt;
+      const float inv = (p.drop.on ? p.drop.scale : 1.0f) / lt;
       const int row = b * p.seq + qb * 128 + r;
       bf16* orow = p.ctx + (size_t)row * p.h + (size_t)hd * p.d;
       for (int c = wg * 32; c < p.d; c += 64) {
@@ -564,12 +586,17 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           tmem_ld32(tS + lane_off + col, sv);
           tmem_ld32(tDP + lane_off + col, dv);
           tmem_ld_wait();
+          const uint32_t keep =
+              p.drop.on ? drop_bits32(drop_row(p, b, hd, qb * 128 + r) + j * 64 + wg * 32, p.drop)
+                        : 0xffffffffu;
+          const float dsc = p.drop.on ? p.drop.scale : 1.0f;
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int key = j * 64 + wg * 32 + i;
             float pr = fast_exp2(__uint_as_float(sv[i]) * p.scale_log2 - lse2);
             if (key > qb * 128 + r) pr = 0.f;
-            ds[i] = pr * (__uint_as_float(dv[i]) - Dr);
+            const float dp = ((keep >> i) & 1u) ? __uint_as_float(dv[i]) * dsc : 0.f;
+            ds[i] = pr * (dp - Dr);
           }
         }
         if (gg > 0) {
@@ -819,12 +846,29 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           tmem_ld32(tST + lane_off + col, sv);
           tmem_ld32(tDPT + lane_off + col, dv);
           tmem_ld_wait();
+          // Keep bits: query q0+e, this thread's key.  One Philox block covers
+          // 4 consecutive keys of one query, i.e. the 4 lanes of a quad; lane c
+          // of the quad draws the blocks of queries q0 + 4m + c and the quad
+          // trades them, so that every draw is used once.
+          uint32_t qk[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+          const int kq = lane & 3;
+          if (p.drop.on) {
+            uint32_t mine = 0;
+#pragma unroll
+            for (int m = 0; m < 8; ++m)
+              mine |= drop_bits4((drop_row(p, b, hd, q0 + 4 * m + kq) + (key & ~3)) >> 2, p.drop)
+                      << (4 * m);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) qk[c] = __shfl_sync(0xffffffffu, mine, (lane & ~3) | c);
+          }
+          const float dsc = p.drop.on ? p.drop.scale : 1.0f;
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             float pr = fast_exp2(__uint_as_float(sv[e]) * p.scale_log2 - s_lse[e] * LOG2E);
             if (q0 + e < key) pr = 0.f;
-            pt[e] = pr;
-            dst[e] = pr * (__uint_as_float(dv[e]) - s_d[e]);
+            const bool kept = (qk[e & 3] >> (4 * (e >> 2) + kq)) & 1u;
+            pt[e] = kept ? pr * dsc : 0.f;
+            dst[e] = pr * ((kept ? __uint_as_float(dv[e]) * dsc : 0.f) - s_d[e]);
           }
         }
         if (gg > 0) {
@@ -935,8 +979,9 @@ size_t dkv_smem(int na) {
   return need < 120 * 1024 ? 120 * 1024 : need;
 }
 
-Params make_params(int batch, int seq, int heads, int d, unsigned* status) {
+Params make_params(int batch, int seq, int heads, int d, unsigned* status, const Dropout& drop) {
   Params p;
+  p.drop = drop;
   p.batch = batch;
   p.seq = seq;
   p.heads = heads;
@@ -964,13 +1009,13 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 bool attn_tc_supported(int seq, int d) { return seq % 128 == 0 && (d == 64 || d == 96 || d == 128); }
 
 cudaError_t attn_fwd_tc(const void* qkv, void* ctx, float* lse, int batch, int seq, int heads,
-                        int d, unsigned* status, const LaunchCtx& c) {
+                        int d, const Dropout& drop, unsigned* status, const LaunchCtx& c) {
   using namespace attn;
   if (batch == 0) return cudaSuccess;
   if (!attn_tc_supported(seq, d)) return cudaErrorInvalidValue;
   CUtensorMap tm;
   if (!make_map(&tm, qkv, 3ull * heads * d, (uint64_t)batch * seq, 128)) return cudaErrorInvalidValue;
-  Params p = make_params(batch, seq, heads, d, status);
+  Params p = make_params(batch, seq, heads, d, status, drop);
   p.ctx = static_cast<bf16*>(ctx);
   p.lse = lse;
   const int items = p.nqb * heads * batch;
@@ -994,7 +1039,7 @@ cudaError_t attn_fwd_tc(const void* qkv, void* ctx, float* lse, int batch, int s
 
 cudaError_t attn_bwd_tc(const void* qkv, const void* ctx, const float* lse, const void* dctx,
                         void* dqkv, float* dsum, int batch, int seq, int heads, int d,
-                        unsigned* status, const LaunchCtx& c) {
+                        const Dropout& drop, unsigned* status, const LaunchCtx& c) {
   using namespace attn;
   if (batch == 0) return cudaSuccess;
   if (!attn_tc_supported(seq, d)) return cudaErrorInvalidValue;
@@ -1004,7 +1049,7 @@ cudaError_t attn_bwd_tc(const void* qkv, const void* ctx, const float* lse, cons
       !make_map(&tmdo128, dctx, (uint64_t)heads * d, n, 128) ||
       !make_map(&tmdo64, dctx, (uint64_t)heads * d, n, 64))
     return cudaErrorInvalidValue;
-  Params p = make_params(batch, seq, heads, d, status);
+  Params p = make_params(batch, seq, heads, d, status, drop);
   p.ctx = static_cast<bf16*>(const_cast<void*>(ctx));
   p.lse = const_cast<float*>(lse);
   p.dctx = static_cast<const bf16*>(dctx);

@@ -87,6 +87,8 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs a) {
       if (n >= a.N) continue;
       float v = sum[i][j];
       if (EPI == EPI_BIAS || EPI == EPI_BIAS_RESID || EPI == EPI_BIAS_GELU) v += to_f<T>(bias[n]);
+      if (EPI == EPI_BIAS_RESID && a.drop.on)
+        v = drop_keep((unsigned long long)m * a.N + n, a.drop) ? v * a.drop.scale : 0.f;
       if (EPI == EPI_BIAS_RESID) v += to_f<T>(R[(size_t)m * a.ldr + n]);
       if (EPI == EPI_DGELU) v *= gelu_grad_f(to_f<T>(Z[(size_t)m * a.ldz + n]));
       if (EPI == EPI_BIAS_GELU) {

@@ -63,6 +63,7 @@ struct Params {
   void* C;
   int64_t ldc;
   unsigned* status;
+  Dropout drop;   // EPI_BIAS_RESID: C = R + dropout(acc + bias), element e = row * N + col
 };
 
 __device__ __forceinline__ void tile_coords(const Params& p, int tile, int& mb, int& nb) {
@@ -75,9 +76,24 @@ __device__ __forceinline__ void tile_coords(const Params& p, int tile, int& mb, 
   nb = r / gsize;
 }
 
-// Applies the epilogue to 32 consecutive columns [col0, col0+32) of one row.
+// Dropout keep bits of columns [col0, col0+32) of one row (bit e for col0+e),
+// all ones without dropout.
+template <int EPI>
+__device__ __forceinline__ uint32_t chunk_keep(const Params& p, int row, int col0) {
+  if (EPI != EPI_BIAS_RESID || !p.drop.on || row >= p.M) return 0xffffffffu;
+  const unsigned long long e0 = (unsigned long long)row * p.N + col0;
+  if ((p.N & 3) == 0 && col0 + 32 <= p.N) return drop_bits32(e0, p.drop);
+  uint32_t bits = 0;
+#pragma unroll 1
+  for (int e = 0; e < 32 && col0 + e < p.N; ++e) bits |= (drop_keep(e0 + e, p.drop) ? 1u : 0u) << e;
+  return bits;
+}
+
+// Applies the epilogue to 32 consecutive columns [col0, col0+32) of one row;
+// `keep`: dropout bits of EPI_BIAS_RESID (chunk_keep).
 template <int EPI, bool OUT_F32>
-__device__ __forceinline__ void epi_chunk(const Params& p, int row, int col0, float (&v)[32]) {
+__device__ __forceinline__ void epi_chunk(const Params& p, int row, int col0, float (&v)[32],
+                                          uint32_t keep) {
   if (row >= p.M || col0 >= p.N) return;
   const bool full = col0 + 32 <= p.N;
   if (full) {
@@ -90,6 +106,10 @@ __device__ __forceinline__ void epi_chunk(const Params& p, int row, int col0, fl
 #pragma unroll
         for (int e = 0; e < 8; ++e) v[q * 8 + e] += __bfloat162float(hb[e]);
       }
+    }
+    if (EPI == EPI_BIAS_RESID && p.drop.on) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] = ((keep >> e) & 1u) ? v[e] * p.drop.scale : 0.f;
     }
     if (EPI == EPI_BIAS_RESID) {
       const uint4* rp = reinterpret_cast<const uint4*>(p.R + (size_t)row * p.ldr + col0);
@@ -149,6 +169,7 @@ __device__ __forceinline__ void epi_chunk(const Params& p, int row, int col0, fl
         float x = v[e];
         if (EPI == EPI_BIAS || EPI == EPI_BIAS_RESID || EPI == EPI_BIAS_GELU)
           x += __bfloat162float(p.bias[col]);
+        if (EPI == EPI_BIAS_RESID && p.drop.on) x = ((keep >> e) & 1u) ? x * p.drop.scale : 0.f;
         if (EPI == EPI_BIAS_RESID) x += __bfloat162float(p.R[(size_t)row * p.ldr + col]);
         if (EPI == EPI_DGELU) x *= gelu_grad_f(__bfloat162float(p.Z[(size_t)row * p.ldz + col]));
         if (EPI == EPI_BIAS_GELU) {
@@ -199,6 +220,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t tmem_bas
       const uint32_t tb = tmem_base + buf * BN + chalf * 128 + ((uint32_t)(quarter * 32) << 16);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
+        const uint32_t keep = REDUCE ? 0u : chunk_keep<EPI>(p, row, colbase + c * 32);
         uint32_t r[32];
         tmem_ld32(tb + c * 32, r);
         tmem_ld_wait();
@@ -212,7 +234,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t tmem_bas
           float v[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-          epi_chunk<EPI, OUT_F32>(p, row, colbase + c * 32, v);
+          epi_chunk<EPI, OUT_F32>(p, row, colbase + c * 32, v, keep);
         }
       }
       tc_fence_before();
@@ -228,10 +250,11 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t tmem_bas
       if (ok) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
+          const uint32_t keep = chunk_keep<EPI>(p, row, colbase + c * 32);
           float v[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = sum[c * 32 + i];
-          epi_chunk<EPI, OUT_F32>(p, row, colbase + c * 32, v);
+          epi_chunk<EPI, OUT_F32>(p, row, colbase + c * 32, v, keep);
         }
       }
     }
@@ -717,6 +740,7 @@ cudaError_t gemm_tc(const GemmArgs& a, const LaunchCtx& c) {
   p.C = a.C;
   p.ldc = a.ldc;
   p.status = a.status;
+  p.drop = a.drop;
   KernelFn fn = use_pair ? select_kernel2(a.epi, a.c_f32, reduce)
                          : select_kernel(a.epi, a.c_f32, reduce);
   if (!fn) return cudaErrorInvalidValue;

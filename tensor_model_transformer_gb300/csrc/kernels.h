@@ -11,6 +11,19 @@ enum DType { kF32 = 0, kBF16 = 1 };
 // GEMM epilogues (the numbering is the one mtl_gemm exposes).
 enum Epi { EPI_STORE = 0, EPI_BIAS = 1, EPI_BIAS_RESID = 2, EPI_BIAS_GELU = 3, EPI_DGELU = 4 };
 
+// Dropout of one site: element e is kept iff word(e) >= thresh and a kept value
+// is multiplied by scale = 1 / (1 - p).  word(e) is lane e mod 4 of the
+// Philox4x32-10 block at counter (e div 4 as two 32-bit words, site, 0) under
+// the key (seed low word, seed high word).  on == 0: no dropout (p = 0).
+enum DropSite { SITE_ATTN = 0, SITE_OUT = 1, SITE_FC2 = 2 };
+struct Dropout {
+  unsigned long long seed;
+  uint32_t thresh;   // floor(p * 2^32)
+  float scale;       // 1 / (1 - p)
+  uint32_t site;
+  int on;
+};
+
 // A(m,k) = ptr[m*ld + k] when k_major, else ptr[k*ld + m].
 struct GemmOperand {
   const void* ptr;
@@ -32,6 +45,7 @@ struct GemmArgs {
   int64_t ldc;
   bool c_f32;             // C stored as fp32 (else as the operand dtype)
   unsigned* status;       // device status word
+  Dropout drop;           // EPI_BIAS_RESID: C = R + dropout(acc + bias), e = row * N + col
 };
 
 // Kernel kinds reported through the profiling hooks.
@@ -97,6 +111,11 @@ size_t ln_bwd_partial_floats(int n, int h);
 cudaError_t colsum(int dtype, const void* Y, int64_t ld, int n, int N, float* out,
                    float* partial, const LaunchCtx& c);
 size_t colsum_partial_floats(int n, int N);
+// Column sums of the dropped-out Y: Ym = Y * keep / (1 - p) (element e = row * N
+// + col of site drop.site) is written with row pitch ld, out = column sums of Ym
+// (before rounding to the storage type).  N % 4 == 0.
+cudaError_t colsum_dropout(int dtype, const void* Y, void* Ym, int64_t ld, int n, int N,
+                           const Dropout& drop, float* out, float* partial, const LaunchCtx& c);
 
 // Error text for mtl_last_cuda_error, shared by every entry point.
 void record_cuda_error(cudaError_t e, const char* where);
@@ -104,21 +123,22 @@ void clear_cuda_error();
 
 // Causal attention over a head-interleaved qkv [batch*seq][3h] -> ctx
 // [batch*seq][h], lse [batch][heads][seq] (CUDA-core reference kernels).
+// `drop`: attention dropout on the probabilities (site SITE_ATTN).
 cudaError_t attn_fwd_simt(int dtype, const void* qkv, void* ctx, float* lse, int batch, int seq,
-                          int heads, int d, const LaunchCtx& c);
+                          int heads, int d, const Dropout& drop, const LaunchCtx& c);
 // Backward: dctx -> dqkv [batch*seq][3h]; dsum [batch][heads][seq] is scratch.
 cudaError_t attn_bwd_simt(int dtype, const void* qkv, const void* ctx, const float* lse,
                           const void* dctx, void* dqkv, float* dsum, int batch, int seq,
-                          int heads, int d, const LaunchCtx& c);
+                          int heads, int d, const Dropout& drop, const LaunchCtx& c);
 
 // Causal attention on tcgen05 tensor cores (bf16; seq % 128 == 0, d in
 // {64, 96, 128}).  Forward writes ctx and lse; backward writes dqkv and, as
 // scratch, dsum [batch][heads][seq].
 bool attn_tc_supported(int seq, int d);
 cudaError_t attn_fwd_tc(const void* qkv, void* ctx, float* lse, int batch, int seq, int heads,
-                        int d, unsigned* status, const LaunchCtx& c);
+                        int d, const Dropout& drop, unsigned* status, const LaunchCtx& c);
 cudaError_t attn_bwd_tc(const void* qkv, const void* ctx, const float* lse, const void* dctx,
                         void* dqkv, float* dsum, int batch, int seq, int heads, int d,
-                        unsigned* status, const LaunchCtx& c);
+                        const Dropout& drop, unsigned* status, const LaunchCtx& c);
 
 }  // namespace mtl

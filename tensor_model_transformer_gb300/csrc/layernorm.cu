@@ -277,6 +277,37 @@ __global__ void colsum_partial_kernel(const T* __restrict__ Y, int64_t ld, int n
   for (int e = 0; e < E; ++e) part[(size_t)blockIdx.y * N + c0 + e] = acc[e];
 }
 
+// colsum_partial_kernel on Y * keep / (1 - p), also writing that product to Ym.
+template <typename T>
+__global__ void colsum_dropout_partial_kernel(const T* __restrict__ Y, T* __restrict__ Ym,
+                                              int64_t ld, int n, int N, int rows_per_block,
+                                              Dropout drop, float* __restrict__ part) {
+  constexpr int E = Vec<T>::N;   // 8 or 4: whole Philox blocks, N % 4 == 0
+  const int c0 = (blockIdx.x * blockDim.x + threadIdx.x) * E;
+  if (c0 >= N) return;
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  const int r0 = blockIdx.y * rows_per_block;
+  const int r1 = min(n, r0 + rows_per_block);
+  for (int r = r0; r < r1; ++r) {
+    Vec<T> v;
+    v.load(Y + (size_t)r * ld + c0);
+    const unsigned long long blk = ((unsigned long long)r * N + c0) >> 2;
+    uint32_t bits = drop_bits4(blk, drop);
+    if (E == 8) bits |= drop_bits4(blk + 1, drop) << 4;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float x = ((bits >> e) & 1u) ? v.get(e) * drop.scale : 0.f;
+      acc[e] += x;
+      v.set(e, x);
+    }
+    v.store(Ym + (size_t)r * ld + c0);
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) part[(size_t)blockIdx.y * N + c0 + e] = acc[e];
+}
+
 // Vectors per thread and threads per block for a row of h elements.
 template <typename T>
 void row_plan(int h, int* vpt, int* threads) {
@@ -376,6 +407,25 @@ cudaError_t colsum_t(const void* Y, int64_t ld, int n, int N, float* out, float*
   return cudaGetLastError();
 }
 
+template <typename T>
+cudaError_t colsum_dropout_t(const void* Y, void* Ym, int64_t ld, int n, int N,
+                             const Dropout& drop, float* out, float* partial,
+                             const LaunchCtx& c) {
+  constexpr int E = Vec<T>::N;
+  const int nblk = n < kColsumBlocks ? (n > 0 ? n : 1) : kColsumBlocks;
+  const int rows = (n + nblk - 1) / nblk;
+  const int threads = 256;
+  dim3 grid((N / E + threads - 1) / threads, nblk);
+  c.before(KK_COLSUM, 2.0 * n * N * sizeof(T));
+  colsum_dropout_partial_kernel<T><<<grid, threads, 0, c.stream>>>((const T*)Y, (T*)Ym, ld, n, N,
+                                                                   rows, drop, partial);
+  c.after();
+  c.before(KK_FINALIZE, 4.0 * nblk * N);
+  finalize_cols_kernel<<<(N + 31) / 32, kFinWarps * 32, 0, c.stream>>>(partial, nblk, N, out);
+  c.after();
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 size_t ln_bwd_partial_floats(int n, int h) {
@@ -406,6 +456,13 @@ cudaError_t colsum(int dtype, const void* Y, int64_t ld, int n, int N, float* ou
                    float* partial, const LaunchCtx& c) {
   return dtype == kBF16 ? colsum_t<bf16>(Y, ld, n, N, out, partial, c)
                         : colsum_t<float>(Y, ld, n, N, out, partial, c);
+}
+
+cudaError_t colsum_dropout(int dtype, const void* Y, void* Ym, int64_t ld, int n, int N,
+                           const Dropout& drop, float* out, float* partial, const LaunchCtx& c) {
+  if (N % 4) return cudaErrorInvalidValue;
+  return dtype == kBF16 ? colsum_dropout_t<bf16>(Y, Ym, ld, n, N, drop, out, partial, c)
+                        : colsum_dropout_t<float>(Y, Ym, ld, n, N, drop, out, partial, c);
 }
 
 }  // namespace mtl

@@ -11,6 +11,7 @@
 //   y  = x1 + b_fc2 + g( sum_p a[:, F_p] W_fc2[:, F_p]^T )
 // Backward mirrors it; f sums the partitions' partial input gradients of the
 // two column-parallel GEMMs.  g and f are fixed-order sums inside the GEMMs.
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -68,7 +69,21 @@ struct Dims {
   int64_t h, heads, d, seq, batch, n, f, t;
   int dtype;
   size_t esz;
+  float p_attn, p_hidden;
+  unsigned long long seed;
 };
+
+// Dropout of one site: keep iff the Philox word >= floor(p * 2^32), scale 1/(1-p).
+Dropout make_drop(float p, unsigned long long seed, uint32_t site) {
+  Dropout d;
+  d.seed = seed;
+  d.site = site;
+  d.on = p > 0.f ? 1 : 0;
+  const double t = floor((double)p * 4294967296.0);
+  d.thresh = d.on ? (uint32_t)(t > 4294967295.0 ? 4294967295.0 : t) : 0u;
+  d.scale = d.on ? (float)(1.0 / (1.0 - (double)p)) : 1.0f;
+  return d;
+}
 
 mtl_status validate(const mtl_layer_desc* desc, Dims* o) {
   if (!desc) return MTL_ERR_INVALID_ARG;
@@ -77,6 +92,8 @@ mtl_status validate(const mtl_layer_desc* desc, Dims* o) {
     return MTL_ERR_INVALID_ARG;
   if (d.dtype != MTL_F32 && d.dtype != MTL_BF16) return MTL_ERR_INVALID_ARG;
   if (!(d.ln_eps > 0.f)) return MTL_ERR_INVALID_ARG;
+  if (!(d.p_attn >= 0.f && d.p_attn < 1.f) || !(d.p_hidden >= 0.f && d.p_hidden < 1.f))
+    return MTL_ERR_INVALID_ARG;
   if (d.h % d.heads) return MTL_ERR_INVALID_ARG;
   if (d.heads % d.t || d.ffn % d.t) return MTL_ERR_INVALID_ARG;
   const int dh = d.h / d.heads;
@@ -100,6 +117,9 @@ mtl_status validate(const mtl_layer_desc* desc, Dims* o) {
   o->t = d.t;
   o->dtype = d.dtype;
   o->esz = d.dtype == MTL_BF16 ? 2 : 4;
+  o->p_attn = d.p_attn;
+  o->p_hidden = d.p_hidden;
+  o->seed = d.seed;
   return MTL_OK;
 }
 
@@ -130,7 +150,7 @@ mtl_saved_layout saved_layout(const Dims& D) {
 
 // Backward scratch, after the status word.
 struct WsLayout {
-  size_t dz, du, dx1, dctx, dqkv, dsum, partial, total;
+  size_t dz, du, dx1, dctx, dqkv, dsum, gmask, partial, total;
 };
 
 WsLayout ws_layout(const Dims& D) {
@@ -148,6 +168,8 @@ WsLayout ws_layout(const Dims& D) {
   W.dctx = take(nh * D.esz);
   W.dqkv = take(3 * nh * D.esz);
   W.dsum = take((size_t)D.batch * D.heads * D.seq * 4);
+  // dropped-out gradient of the fc2 output, later of the out-proj output
+  W.gmask = take(D.p_hidden > 0.f ? nh * D.esz : 0);
   size_t pf = ln_bwd_partial_floats((int)D.n, (int)D.h);
   const size_t widest = (size_t)(D.f > 3 * D.h ? D.f : 3 * D.h);
   const size_t pc = colsum_partial_floats((int)D.n, (int)widest);
@@ -208,6 +230,21 @@ GemmArgs gemm_args(int M, int N, int K, int parts, const void* A, int64_t lda, b
   g.c_f32 = cf32;
   g.status = status;
   return g;
+}
+
+mtl_status attn_validate(int32_t dtype, int32_t batch, int32_t seq, int32_t heads, int32_t d,
+                         float p_attn) {
+  if (dtype != MTL_F32 && dtype != MTL_BF16) return MTL_ERR_INVALID_ARG;
+  if (batch < 0 || seq <= 0 || heads <= 0) return MTL_ERR_INVALID_ARG;
+  if (!(p_attn >= 0.f && p_attn < 1.f)) return MTL_ERR_INVALID_ARG;
+  if (d != 64 && d != 96 && d != 128) return MTL_ERR_UNSUPPORTED;
+  if ((int64_t)batch * seq > (int64_t)1 << 30) return MTL_ERR_UNSUPPORTED;
+  if (dtype == MTL_BF16 && seq % 128) return MTL_ERR_UNSUPPORTED;
+  if (dtype == MTL_F32 && seq > 8192) return MTL_ERR_UNSUPPORTED;
+  return MTL_OK;
+}
+size_t attn_ws_bytes(int32_t batch, int32_t seq, int32_t heads) {
+  return kStatusBytes + align_up((size_t)batch * heads * seq * 4);
 }
 
 #define MTL_TRY(expr, where)                     \
@@ -296,6 +333,7 @@ mtl_status mtl_layer_fwd(const mtl_layer_desc* desc, const mtl_weights* w, const
   void* z = at<char>(saved, L.z);
   void* a = at<char>(saved, L.a);
   const bool bf = D.dtype == MTL_BF16;
+  const Dropout drop_attn = make_drop(D.p_attn, D.seed, SITE_ATTN);
 
   // F1 LN1
   MTL_TRY(ln_fwd(D.dtype, x, w->ln1_g, w->ln1_b, u1, at<float>(saved, L.mu1),
@@ -311,18 +349,19 @@ mtl_status mtl_layer_fwd(const mtl_layer_desc* desc, const mtl_weights* w, const
   // F3 attention per head
   if (bf) {
     MTL_TRY(attn_fwd_tc(qkv, ctx, at<float>(saved, L.lse), (int)D.batch, (int)D.seq, (int)D.heads,
-                        (int)D.d, status, c),
+                        (int)D.d, drop_attn, status, c),
             "attention fwd");
   } else {
     MTL_TRY(attn_fwd_simt(D.dtype, qkv, ctx, at<float>(saved, L.lse), (int)D.batch, (int)D.seq,
-                          (int)D.heads, (int)D.d, c),
+                          (int)D.heads, (int)D.d, drop_attn, c),
             "attention fwd");
   }
-  // F4 out-proj, row-parallel + g: t partials over K = h, + b_o + x
+  // F4 out-proj, row-parallel + g: t partials over K = h, + b_o, dropout, + x
   {
     GemmArgs g = gemm_args(n, h, h, t, ctx, h, true, w->w_o, h, true, EPI_BIAS_RESID, x1, h,
                            false, status);
     g.bias = w->b_o;
+    g.drop = make_drop(D.p_hidden, D.seed, SITE_OUT);
     g.R = x;
     g.ldr = h;
     MTL_TRY(run_gemm(D, g, c), "out-proj gemm");
@@ -340,11 +379,12 @@ mtl_status mtl_layer_fwd(const mtl_layer_desc* desc, const mtl_weights* w, const
     g.ldz = f;
     MTL_TRY(run_gemm(D, g, c), "fc1 gemm");
   }
-  // F7 fc2, row-parallel + g: t partials over K = ffn, + b_fc2 + x1
+  // F7 fc2, row-parallel + g: t partials over K = ffn, + b_fc2, dropout, + x1
   {
     GemmArgs g = gemm_args(n, h, f, t, a, f, true, w->w_fc2, f, true, EPI_BIAS_RESID, y, h, false,
                            status);
     g.bias = w->b_fc2;
+    g.drop = make_drop(D.p_hidden, D.seed, SITE_FC2);
     g.R = x1;
     g.ldr = h;
     MTL_TRY(run_gemm(D, g, c), "fc2 gemm");
@@ -400,20 +440,33 @@ mtl_status mtl_layer_bwd(const mtl_layer_desc* desc, const mtl_weights* w, const
     return MTL_OK;
   }
 
-  // B1 fc2 dgrad + GeLU': dz = (dy W_fc2) * GeLU'(z)  (column-local, no reduction)
+  const bool hid_drop = D.p_hidden > 0.f;
+  const Dropout drop_attn = make_drop(D.p_attn, D.seed, SITE_ATTN);
+  void* gmask = at<char>(workspace, W.gmask);
+  // B0 gradient at the fc2 output g2 = dy * keep_2 / (1 - p) (dy itself without
+  // dropout) and db2 = sum_rows g2
+  const void* g2 = dy;
+  if (hid_drop) {
+    MTL_TRY(colsum_dropout(D.dtype, dy, gmask, h, n, h, make_drop(D.p_hidden, D.seed, SITE_FC2),
+                           static_cast<float*>(gr->b_fc2), partial, c),
+            "db_fc2");
+    g2 = gmask;
+  } else {
+    MTL_TRY(colsum(D.dtype, dy, h, n, h, static_cast<float*>(gr->b_fc2), partial, c), "db_fc2");
+  }
+  // B1 fc2 dgrad + GeLU': dz = (g2 W_fc2) * GeLU'(z)  (column-local, no reduction)
   {
-    GemmArgs g = gemm_args(n, f, h, 1, dy, h, true, w->w_fc2, f, false, EPI_DGELU, dz, f, false,
+    GemmArgs g = gemm_args(n, f, h, 1, g2, h, true, w->w_fc2, f, false, EPI_DGELU, dz, f, false,
                            status);
     g.Z = const_cast<void*>(z);
     g.ldz = f;
     MTL_TRY(run_gemm(D, g, c), "fc2 dgrad");
   }
-  // B2 fc2 wgrad dW2 = dy^T a, db2 = sum_rows dy
-  MTL_TRY(run_gemm(D, gemm_args(h, f, n, 1, dy, h, false, a, f, false, EPI_STORE, gr->w_fc2, f,
+  // B2 fc2 wgrad dW2 = g2^T a
+  MTL_TRY(run_gemm(D, gemm_args(h, f, n, 1, g2, h, false, a, f, false, EPI_STORE, gr->w_fc2, f,
                                 true, status),
                    c),
           "fc2 wgrad");
-  MTL_TRY(colsum(D.dtype, dy, h, n, h, static_cast<float*>(gr->b_fc2), partial, c), "db_fc2");
   // B3 fc1 dgrad with the f reduction: du2 = sum_p dz[:, F_p] W_fc1[F_p, :]
   MTL_TRY(run_gemm(D, gemm_args(n, h, f, t, dz, f, true, w->w_fc1, h, false, EPI_STORE, du, h,
                                 true, status),
@@ -430,24 +483,33 @@ mtl_status mtl_layer_bwd(const mtl_layer_desc* desc, const mtl_weights* w, const
                  dx1, static_cast<float*>(gr->ln2_g), static_cast<float*>(gr->ln2_b), partial, n,
                  h, c),
           "ln2 bwd");
-  // B6 out-proj dgrad dctx = dx1 W_o, wgrad dW_o = dx1^T ctx, db_o = sum_rows dx1
-  MTL_TRY(run_gemm(D, gemm_args(n, h, h, 1, dx1, h, true, w->w_o, h, false, EPI_STORE, dctx, h,
+  // B6 gradient at the out-proj output go = dx1 * keep_1 / (1 - p) (dx1 without
+  // dropout), db_o = sum_rows go; dgrad dctx = go W_o, wgrad dW_o = go^T ctx
+  const void* go = dx1;
+  if (hid_drop) {
+    MTL_TRY(colsum_dropout(D.dtype, dx1, gmask, h, n, h, make_drop(D.p_hidden, D.seed, SITE_OUT),
+                           static_cast<float*>(gr->b_o), partial, c),
+            "db_o");
+    go = gmask;
+  } else {
+    MTL_TRY(colsum(D.dtype, dx1, h, n, h, static_cast<float*>(gr->b_o), partial, c), "db_o");
+  }
+  MTL_TRY(run_gemm(D, gemm_args(n, h, h, 1, go, h, true, w->w_o, h, false, EPI_STORE, dctx, h,
                                 false, status),
                    c),
           "out-proj dgrad");
-  MTL_TRY(run_gemm(D, gemm_args(h, h, n, 1, dx1, h, false, ctx, h, false, EPI_STORE, gr->w_o, h,
+  MTL_TRY(run_gemm(D, gemm_args(h, h, n, 1, go, h, false, ctx, h, false, EPI_STORE, gr->w_o, h,
                                 true, status),
                    c),
           "out-proj wgrad");
-  MTL_TRY(colsum(D.dtype, dx1, h, n, h, static_cast<float*>(gr->b_o), partial, c), "db_o");
   // B7 attention backward per head
   if (D.dtype == MTL_BF16) {
     MTL_TRY(attn_bwd_tc(qkv, ctx, at<float>(saved, L.lse), dctx, dqkv, dsum, (int)D.batch,
-                        (int)D.seq, (int)D.heads, (int)D.d, status, c),
+                        (int)D.seq, (int)D.heads, (int)D.d, drop_attn, status, c),
             "attention bwd");
   } else {
     MTL_TRY(attn_bwd_simt(D.dtype, qkv, ctx, at<float>(saved, L.lse), dctx, dqkv, dsum,
-                          (int)D.batch, (int)D.seq, (int)D.heads, (int)D.d, c),
+                          (int)D.batch, (int)D.seq, (int)D.heads, (int)D.d, drop_attn, c),
             "attention bwd");
   }
   // B8 QKV wgrad dW_qkv = dqkv^T u1, db_qkv = sum_rows dqkv
@@ -515,6 +577,73 @@ mtl_status mtl_selftest_wait_timeout(void* workspace, int64_t limit_cycles, mtl_
   selftest_wait_kernel<<<1, 32, 0, s>>>(status, limit_cycles);
   ++g_launches;
   MTL_TRY(cudaGetLastError(), "selftest launch");
+  return MTL_OK;
+}
+
+// ---------------------------------------------------------------- attention alone
+
+
+mtl_status mtl_attention_ws_bytes(int32_t batch, int32_t seq, int32_t heads, size_t* bytes) {
+  if (batch < 0 || seq <= 0 || heads <= 0 || !bytes) return MTL_ERR_INVALID_ARG;
+  *bytes = attn_ws_bytes(batch, seq, heads);
+  return MTL_OK;
+}
+
+mtl_status mtl_attention_fwd(int32_t dtype, int32_t batch, int32_t seq, int32_t heads, int32_t d,
+                             const void* qkv, void* ctx, float* lse, float p_attn, uint64_t seed,
+                             void* workspace, size_t ws_bytes, mtl_stream stream) {
+  g_launches = 0;
+  g_cuda_err[0] = 0;
+  mtl_status st = attn_validate(dtype, batch, seq, heads, d, p_attn);
+  if (st != MTL_OK) return st;
+  if (!aligned16(qkv) || !aligned16(ctx) || !aligned16(lse) || !aligned16(workspace) ||
+      qkv == ctx)
+    return MTL_ERR_INVALID_ARG;
+  if (ws_bytes < attn_ws_bytes(batch, seq, heads)) return MTL_ERR_WORKSPACE;
+  const int nsm = device_sm_count();
+  if (nsm <= 0) return cuda_fail(cudaGetLastError(), "device query");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  LaunchCtx c{s, nsm, &g_launches, &g_prof};
+  unsigned* status = static_cast<unsigned*>(workspace);
+  MTL_TRY(cudaMemsetAsync(status, 0, kStatusBytes, s), "status reset");
+  if (batch == 0) return MTL_OK;
+  const Dropout drop = make_drop(p_attn, seed, SITE_ATTN);
+  if (dtype == MTL_BF16) {
+    MTL_TRY(attn_fwd_tc(qkv, ctx, lse, batch, seq, heads, d, drop, status, c), "attention fwd");
+  } else {
+    MTL_TRY(attn_fwd_simt(dtype, qkv, ctx, lse, batch, seq, heads, d, drop, c), "attention fwd");
+  }
+  return MTL_OK;
+}
+
+mtl_status mtl_attention_bwd(int32_t dtype, int32_t batch, int32_t seq, int32_t heads, int32_t d,
+                             const void* qkv, const void* ctx, const float* lse, const void* dctx,
+                             void* dqkv, float p_attn, uint64_t seed, void* workspace,
+                             size_t ws_bytes, mtl_stream stream) {
+  g_launches = 0;
+  g_cuda_err[0] = 0;
+  mtl_status st = attn_validate(dtype, batch, seq, heads, d, p_attn);
+  if (st != MTL_OK) return st;
+  if (!aligned16(qkv) || !aligned16(ctx) || !aligned16(lse) || !aligned16(dctx) ||
+      !aligned16(dqkv) || !aligned16(workspace) || dqkv == qkv || dqkv == dctx)
+    return MTL_ERR_INVALID_ARG;
+  if (ws_bytes < attn_ws_bytes(batch, seq, heads)) return MTL_ERR_WORKSPACE;
+  const int nsm = device_sm_count();
+  if (nsm <= 0) return cuda_fail(cudaGetLastError(), "device query");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  LaunchCtx c{s, nsm, &g_launches, &g_prof};
+  unsigned* status = static_cast<unsigned*>(workspace);
+  MTL_TRY(cudaMemsetAsync(status, 0, kStatusBytes, s), "status reset");
+  if (batch == 0) return MTL_OK;
+  float* dsum = at<float>(workspace, kStatusBytes);
+  const Dropout drop = make_drop(p_attn, seed, SITE_ATTN);
+  if (dtype == MTL_BF16) {
+    MTL_TRY(attn_bwd_tc(qkv, ctx, lse, dctx, dqkv, dsum, batch, seq, heads, d, drop, status, c),
+            "attention bwd");
+  } else {
+    MTL_TRY(attn_bwd_simt(dtype, qkv, ctx, lse, dctx, dqkv, dsum, batch, seq, heads, d, drop, c),
+            "attention bwd");
+  }
   return MTL_OK;
 }
 

@@ -33,7 +33,8 @@ class MtlError(RuntimeError):
 class LayerDesc(ctypes.Structure):
     _fields_ = [("h", ctypes.c_int32), ("heads", ctypes.c_int32), ("seq", ctypes.c_int32),
                 ("batch", ctypes.c_int32), ("ffn", ctypes.c_int32), ("t", ctypes.c_int32),
-                ("dtype", ctypes.c_int32), ("ln_eps", ctypes.c_float), ("causal", ctypes.c_int32)]
+                ("dtype", ctypes.c_int32), ("ln_eps", ctypes.c_float), ("causal", ctypes.c_int32),
+                ("p_attn", ctypes.c_float), ("p_hidden", ctypes.c_float), ("seed", ctypes.c_uint64)]
 
 
 class Weights(ctypes.Structure):
@@ -69,6 +70,11 @@ def lib():
         L.mtl_layer_check.argtypes = [vp, vp]
         L.mtl_gemm.argtypes = [i32, i32, i32, i32, i32, vp, i64, i32, vp, i64, i32, i32, vp, vp,
                                i64, vp, i64, vp, i64, i32, vp, sz, vp]
+        L.mtl_attention_ws_bytes.argtypes = [i32, i32, i32, ctypes.POINTER(sz)]
+        L.mtl_attention_fwd.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, ctypes.c_float,
+                                        ctypes.c_uint64, vp, sz, vp]
+        L.mtl_attention_bwd.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp,
+                                        ctypes.c_float, ctypes.c_uint64, vp, sz, vp]
         L.mtl_selftest_wait_timeout.argtypes = [vp, i64, vp]
         L.mtl_selftest_wait_timeout.restype = ctypes.c_int
         L.mtl_bias_grad_noalloc.argtypes = [i32, vp, i64, i32, i32, vp, vp]
@@ -78,7 +84,8 @@ def lib():
         L.mtl_last_cuda_error.restype = ctypes.c_char_p
         L.mtl_last_launch_count.restype = ctypes.c_int32
         for fn in ("mtl_layer_sizes", "mtl_layer_saved_layout", "mtl_layer_fwd", "mtl_layer_bwd",
-                   "mtl_layer_check", "mtl_gemm"):
+                   "mtl_layer_check", "mtl_gemm", "mtl_attention_ws_bytes", "mtl_attention_fwd",
+                   "mtl_attention_bwd"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -101,9 +108,11 @@ def _stream(stream):
     return getattr(stream, "cuda_stream", stream)
 
 
-def layer_desc(h, heads, seq, batch, ffn, t, dtype, ln_eps=1e-5, causal=1) -> LayerDesc:
+def layer_desc(h, heads, seq, batch, ffn, t, dtype, ln_eps=1e-5, causal=1, p_attn=0.0,
+               p_hidden=0.0, seed=0) -> LayerDesc:
+    """mtl_layer_desc; p_attn / p_hidden / seed: dropout probabilities and Philox seed."""
     dt = {"f32": F32, "bf16": BF16, F32: F32, BF16: BF16}[dtype]
-    return LayerDesc(h, heads, seq, batch, ffn, t, dt, ln_eps, causal)
+    return LayerDesc(h, heads, seq, batch, ffn, t, dt, ln_eps, causal, p_attn, p_hidden, seed)
 
 
 def layer_sizes(desc: LayerDesc):
@@ -164,6 +173,36 @@ def gemm(dtype, M, N, K, parts, A, lda, a_k_major, B, ldb, b_k_major, epi, C, ld
                           ldc, int(c_f32), _ptr(workspace),
                           workspace.numel() * workspace.element_size(), _stream(stream)),
            "mtl_gemm")
+
+
+def attention_ws_bytes(batch, seq, heads) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().mtl_attention_ws_bytes(batch, seq, heads, ctypes.byref(out)),
+           "mtl_attention_ws_bytes")
+    return out.value
+
+
+def _dt(dtype):
+    return {"f32": F32, "bf16": BF16, F32: F32, BF16: BF16}[dtype]
+
+
+def attention_fwd(dtype, batch, seq, heads, d, qkv, ctx, lse, workspace, p_attn=0.0, seed=0,
+                  stream=None):
+    """mtl_attention_fwd on torch tensors."""
+    _check(lib().mtl_attention_fwd(_dt(dtype), batch, seq, heads, d, _ptr(qkv), _ptr(ctx),
+                                   _ptr(lse), p_attn, seed, _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)),
+           "mtl_attention_fwd")
+
+
+def attention_bwd(dtype, batch, seq, heads, d, qkv, ctx, lse, dctx, dqkv, workspace, p_attn=0.0,
+                  seed=0, stream=None):
+    """mtl_attention_bwd on torch tensors."""
+    _check(lib().mtl_attention_bwd(_dt(dtype), batch, seq, heads, d, _ptr(qkv), _ptr(ctx),
+                                   _ptr(lse), _ptr(dctx), _ptr(dqkv), p_attn, seed,
+                                   _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                   _stream(stream)),
+           "mtl_attention_bwd")
 
 
 def selftest_wait_timeout(workspace, limit_cycles, stream=None):

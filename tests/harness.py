@@ -35,12 +35,22 @@ def to_np(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def run_gpu(shape, x, p, dy, t, runs=1, want_saved=True):
-    """Forward + backward through the C ABI.  Returns a dict of float64 arrays."""
+def f32(v):
+    """v rounded to float32: the dropout probabilities cross the C ABI as float."""
+    return float(np.float32(v))
+
+
+def run_gpu(shape, x, p, dy, t, runs=1, want_saved=True, drop=None):
+    """Forward + backward through the C ABI.  Returns a dict of float64 arrays.
+
+    drop: optional dict(p_attn, p_hidden, seed) of float32-exact probabilities."""
     import torch
     from tensor_model_transformer_gb300 import mtl
     b = x.shape[0]
-    desc = mtl.layer_desc(shape.h, shape.heads, shape.seq, b, shape.ffn, t, shape.dtype)
+    drop = drop or {}
+    desc = mtl.layer_desc(shape.h, shape.heads, shape.seq, b, shape.ffn, t, shape.dtype,
+                          p_attn=drop.get("p_attn", 0.0), p_hidden=drop.get("p_hidden", 0.0),
+                          seed=drop.get("seed", 0))
     dev_p = {k: to_device(v, shape.dtype) for k, v in p.items()}
     xd = to_device(x, shape.dtype)
     dyd = to_device(dy, shape.dtype)
@@ -63,9 +73,9 @@ def run_gpu(shape, x, p, dy, t, runs=1, want_saved=True):
     return outs if runs > 1 else outs[0]
 
 
-def run_oracle(shape, x, p, dy):
+def run_oracle(shape, x, p, dy, drop=None):
     """The oracle's outputs and intermediates, keyed like run_gpu."""
-    y, cache = oracle.layer_fwd(p, x, shape.heads)
+    y, cache = oracle.layer_fwd(p, x, shape.heads, dropout=drop)
     dx, g, _ = oracle.layer_bwd(p, cache, dy)
     out = {"y": y, "dx": dx}
     out.update({"d_" + k: v for k, v in g.items()})

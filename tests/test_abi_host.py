@@ -166,3 +166,63 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(m, "_lib", None)
     with pytest.raises(RuntimeError):
         m.lib()
+
+
+def test_dropout_probabilities_validated(mtl):
+    for kw in (dict(p_attn=1.0), dict(p_attn=-0.1), dict(p_hidden=1.0), dict(p_hidden=-1e-3),
+               dict(p_attn=float("nan")), dict(p_hidden=float("nan"))):
+        d = good_desc(mtl, **kw)
+        assert mtl.lib().mtl_layer_sizes(ctypes.byref(d), None, None) == 1, kw
+    d0, d1 = good_desc(mtl), good_desc(mtl, p_attn=0.1, p_hidden=0.1, seed=(1 << 63) + 5)
+    assert d1.seed == (1 << 63) + 5
+    s0, w0 = mtl.layer_sizes(d0)
+    s1, w1 = mtl.layer_sizes(d1)
+    # the saved buffer does not grow (masks are recomputed); the workspace holds
+    # one dropped-out [n][h] gradient
+    assert s1 == s0 and w1 >= w0 + 256 * 256 * 2
+
+
+def test_layer_desc_layout_matches_header(mtl, tmp_path):
+    """The ctypes mirror of mtl_layer_desc has the C struct's size and offsets."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "probe.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "mtl.h"\n'
+                   'int main(void) { printf("%zu %zu %zu %zu %zu\\n", sizeof(mtl_layer_desc),'
+                   ' offsetof(mtl_layer_desc, causal), offsetof(mtl_layer_desc, p_attn),'
+                   ' offsetof(mtl_layer_desc, p_hidden), offsetof(mtl_layer_desc, seed));'
+                   ' return 0; }\n')
+    exe = tmp_path / "probe"
+    subprocess.run([gcc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    D = mtl.LayerDesc
+    assert got == [ctypes.sizeof(D), D.causal.offset, D.p_attn.offset, D.p_hidden.offset,
+                   D.seed.offset]
+
+
+def test_attention_entry_points_reject(mtl):
+    L = mtl.lib()
+    ws = mtl.attention_ws_bytes(2, 256, 4)
+    assert ws >= 256 + 2 * 4 * 256 * 4
+    a = (FAKE, FAKE + 4096, FAKE + 8192)
+    ok = dict(dtype=1, batch=2, seq=256, heads=4, d=64)
+
+    def fwd(**kw):
+        c = dict(ok, p=0.1, ws=ws, qkv=a[0], ctx=a[1], lse=a[2], wsp=FAKE + 16384)
+        c.update(kw)
+        return L.mtl_attention_fwd(c["dtype"], c["batch"], c["seq"], c["heads"], c["d"], c["qkv"],
+                                   c["ctx"], c["lse"], c["p"], 7, c["wsp"], c["ws"], None)
+
+    assert fwd(p=1.0) == 1 and fwd(p=-0.5) == 1 and fwd(dtype=3) == 1 and fwd(heads=0) == 1
+    assert fwd(d=32) == 2 and fwd(seq=200) == 2          # bf16 needs seq % 128 == 0
+    assert fwd(qkv=FAKE + 8) == 1 and fwd(lse=None) == 1 and fwd(ctx=a[0]) == 1
+    assert fwd(ws=ws - 1) == 3
+    assert L.mtl_attention_bwd(1, 2, 256, 4, 64, a[0], a[1], a[2], FAKE + 12288, a[0], 0.0, 0,
+                               FAKE + 16384, ws, None) == 1    # dqkv aliases qkv
+    assert L.mtl_attention_bwd(1, 2, 256, 4, 64, a[0], a[1], a[2], FAKE + 12288, FAKE + 20480,
+                               0.0, 0, FAKE + 16384, 255, None) == 3
