@@ -163,7 +163,7 @@ def run_reference(args, shape, rank, world):
     steps = max(1, min(args.steps, 3))
     for _ in range(steps):
         t0 = time.perf_counter()
-        y, cache = oracle.layer_fwd(p, x, shape.heads)
+        y, cache = oracle.layer_fwd(p, x, shape.heads, dropout=args.drop)
         oracle.layer_bwd(p, cache, dy)
         times.append(time.perf_counter() - t0)
     sec = float(np.mean(times))
@@ -176,7 +176,8 @@ def run_reference(args, shape, rank, world):
            "impl": "reference",
            "config": {"workload": f"{args.config}: {shape.name}, t={args.t}",
                       "h": shape.h, "heads": shape.heads, "seq": shape.seq,
-                      "batch": sample_batch, "ffn": shape.ffn, "t": args.t},
+                      "batch": sample_batch, "ffn": shape.ffn, "t": args.t,
+                      "dropout": args.drop},
            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores,
                             "kind": "oracle", "sample": sample},
            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -184,11 +185,11 @@ def run_reference(args, shape, rank, world):
     print(json.dumps(out), flush=True)
 
 
-def cpu_baseline(shape):
+def cpu_baseline(shape, drop=None):
     import oracle
     x, p, dy = synthetic.make_layer(shape, seed=0, batch=1)
     t0 = time.perf_counter()
-    y, cache = oracle.layer_fwd(p, x, shape.heads)
+    y, cache = oracle.layer_fwd(p, x, shape.heads, dropout=drop)
     oracle.layer_bwd(p, cache, dy)
     sec = time.perf_counter() - t0
     return {"value": layer_flops(shape, 1) / sec / 1e12, "unit": "TFLOP/s",
@@ -208,7 +209,13 @@ def main():
     ap.add_argument("--config", default="D", choices=sorted(synthetic.CONFIGS))
     ap.add_argument("--t", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--p-drop", type=float, default=0.0,
+                    help="dropout probability of the attention and hidden sites (default 0)")
     args = ap.parse_args()
+    args.drop = None
+    if args.p_drop > 0:
+        pd = float(np.float32(args.p_drop))
+        args.drop = {"p_attn": pd, "p_hidden": pd, "seed": 1234}
     shape = synthetic.CONFIGS[args.config]
     if args.t is None:
         args.t = shape.t[0]
@@ -230,8 +237,10 @@ def main():
 
     dt = torch.bfloat16 if shape.dtype == "bf16" else torch.float32
     x, p, dy = synthetic.make_layer(shape, seed=rank)
+    drop = args.drop or {}
     desc = mtl.layer_desc(shape.h, shape.heads, shape.seq, shape.batch, shape.ffn, args.t,
-                          shape.dtype)
+                          shape.dtype, p_attn=drop.get("p_attn", 0.0),
+                          p_hidden=drop.get("p_hidden", 0.0), seed=drop.get("seed", 0))
     w = {k: torch.from_numpy(v).cuda().to(dt) for k, v in p.items()}
     x_h = torch.from_numpy(x).to(dt).pin_memory()
     dy_h = torch.from_numpy(dy).to(dt).pin_memory()
@@ -397,7 +406,8 @@ def main():
                    "heads": shape.heads, "seq": shape.seq, "batch": shape.batch,
                    "ffn": shape.ffn, "t": args.t, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (no flush)",
-                   "flops_per_step": flops, "megatron_flops_per_step": megatron_flops(shape)},
+                   "flops_per_step": flops, "megatron_flops_per_step": megatron_flops(shape),
+                   "dropout": args.drop},
         "pct_of_bf16_peak": 100.0 * value / world / pk["bf16_tflops"],
         "peak_source": pk_src,
         "gpu_launches": launches,
@@ -409,7 +419,7 @@ def main():
     if clk:
         out["clocks"] = clk
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(shape)
+        out["cpu_baseline"] = cpu_baseline(shape, args.drop)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:

@@ -50,8 +50,10 @@
  *     key {seed mod 2^32, seed >> 32} (Salmon et al., SC'11).  Site s = 0:
  *     attention, e = ((b*heads + head)*seq + i)*seq + j for query i, key j;
  *     s = 1: out-projection output, s = 2: fc2 output, e = token*h + column.
- *     Masks are recomputed from (seed, e) in the backward, never stored, so
- *     mtl_layer_bwd must get the desc (seed, p) of the forward it follows.
+ *     The hidden-site masks are redrawn from (seed, e) in the backward; the
+ *     attention mask of a bf16 layer is drawn once by the forward and kept as
+ *     bits in `saved` (fp32 layers redraw it).  mtl_layer_bwd must get the desc
+ *     (seed, p) of the forward it follows.
  *   * Every pointer must be 16-byte aligned.  Validation failures return before
  *     anything is enqueued.  No C++ exception crosses this boundary.  Calls are
  *     reentrant; calls on different streams may run concurrently as long as
@@ -119,6 +121,8 @@ typedef struct {
  * [n][ffn]. */
 typedef struct {
   size_t mu1, rstd1, u1, qkv, ctx, lse, x1, mu2, rstd2, u2, z, a;
+  size_t attn_mask;   /* keep bits of attention dropout (bf16 layers with p_attn > 0;
+                         empty otherwise), see mtl_attention_mask_bytes */
   size_t total;
 } mtl_saved_layout;
 
@@ -186,17 +190,22 @@ mtl_status mtl_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, int32_t k_pa
  *   the forward's qkv, ctx and lse and the same p_attn and seed.
  * dtype MTL_BF16 (tcgen05 kernels; seq % 128 == 0) or MTL_F32 (CUDA cores;
  * seq <= 8192); d in {64, 96, 128}; 0 <= p_attn < 1.  Device pointers, 16-byte
- * aligned.  workspace: >= mtl_attention_ws_bytes (status word and the
- * backward's row sums D_i = dO_i . O_i); check it with mtl_layer_check.
- * Errors as for the layer calls. */
+ * aligned.  mask_bits (mtl_attention_mask_bytes, which is 0 unless dtype is
+ * MTL_BF16 and p_attn > 0; may be NULL then): written by the forward with the
+ * keep bits it drew, read by the backward.  workspace: >=
+ * mtl_attention_ws_bytes (status word and the backward's row sums D_i =
+ * dO_i . O_i); check it with mtl_layer_check.  Errors as for the layer calls. */
 mtl_status mtl_attention_ws_bytes(int32_t batch, int32_t seq, int32_t heads, size_t* bytes);
+mtl_status mtl_attention_mask_bytes(int32_t dtype, int32_t batch, int32_t seq, int32_t heads,
+                                    float p_attn, size_t* bytes);
 mtl_status mtl_attention_fwd(int32_t dtype, int32_t batch, int32_t seq, int32_t heads, int32_t d,
-                             const void* qkv, void* ctx, float* lse, float p_attn, uint64_t seed,
-                             void* workspace, size_t ws_bytes, mtl_stream stream);
+                             const void* qkv, void* ctx, float* lse, void* mask_bits,
+                             float p_attn, uint64_t seed, void* workspace, size_t ws_bytes,
+                             mtl_stream stream);
 mtl_status mtl_attention_bwd(int32_t dtype, int32_t batch, int32_t seq, int32_t heads, int32_t d,
                              const void* qkv, const void* ctx, const float* lse, const void* dctx,
-                             void* dqkv, float p_attn, uint64_t seed, void* workspace,
-                             size_t ws_bytes, mtl_stream stream);
+                             const void* mask_bits, void* dqkv, float p_attn, uint64_t seed,
+                             void* workspace, size_t ws_bytes, mtl_stream stream);
 
 /* Bias gradient for callers that cannot allocate device memory:
  *   out[j] = sum_{i < rows} dy[i*ld + j]   (j < cols; fp32, fixed order)

@@ -15,7 +15,9 @@
 // With attention dropout (keep mask M from the Philox stream, scale 1/(1-p)):
 //   O = (P * M / (1-p)) V, lse still that of the undropped P;
 //   dV = (P * M / (1-p))^T dO;  dS = P * ((dO V^T) * M / (1-p) - D).
-// The masks are recomputed in every kernel, never stored.
+// The forward draws M and stores it as bits (one bit per causal element, an
+// eighth of a bf16 P); the two backward kernels read the bits instead of
+// drawing again, which trades 2 of 3 Philox passes for a few MB of traffic.
 //
 // All three kernels: one CTA per 128-row block, 192 threads:
 //   warp 0      TMA producer
@@ -53,7 +55,32 @@ struct Params {
   unsigned* status;
   Dropout drop;       // attention dropout: element (query i, key j) of head hd, batch b
                       // is e = ((b * heads + hd) * seq + i) * seq + j
+  uint32_t* mask;     // keep bits written by the forward, read by the backward
 };
+
+// Keep bits of the forward, one 2 KB tile per (batch, head, query block qb, key
+// block kb <= qb) of 128 x 128: tiles of a (batch, head) pair in the order
+// qb (qb + 1) / 2 + kb; inside a tile, word w (keys 32w .. 32w+31 of the block,
+// bit = key % 32) of row r sits at w * 128 + r, so a warp's 32 rows are 128
+// contiguous bytes.
+__device__ __forceinline__ uint32_t* mask_tile(const Params& p, int b, int hd, int qb, int kb) {
+  const size_t ntile = (size_t)p.nqb * (p.nqb + 1) / 2;
+  return p.mask + (((size_t)b * p.heads + hd) * ntile + (size_t)qb * (qb + 1) / 2 + kb) * 512;
+}
+
+// 32 x 32 bit transpose across a warp: on entry lane l holds row l (bit k =
+// element (l, k)); on exit lane k holds column k (bit l = element (l, k)).
+// Five exchange stages swap the off-diagonal halves of ever smaller blocks.
+__device__ __forceinline__ uint32_t warp_transpose32(uint32_t w, int lane) {
+#pragma unroll
+  for (int j = 16, i = 0; j >= 1; j >>= 1, ++i) {
+    const uint32_t m = i == 0 ? 0x0000FFFFu : i == 1 ? 0x00FF00FFu : i == 2 ? 0x0F0F0F0Fu
+                     : i == 3 ? 0x33333333u : 0x55555555u;
+    const uint32_t o = __shfl_xor_sync(0xffffffffu, w, j);
+    w = (lane & j) ? ((w & ~m) | ((o >> j) & m)) : ((w & m) | ((o << j) & ~m));
+  }
+  return w;
+}
 
 // First element index of query row i, head hd, batch b in the attention
 // dropout numbering.
@@ -96,7 +123,7 @@ __device__ __forceinline__ void item_coords(const Params& p, int item, bool desc
 // their row maxima through shared memory behind an mbarrier.
 // smem: Q, K[2], V[2] (NA atoms of 16 KB each), P (2 atoms), row-max and row-sum
 // exchange.  TMEM: S[b] cols 128b, O[b] cols 256+128b.
-template <int NA, int KS>
+template <int NA, int KS, bool DROP>
 __global__ void __launch_bounds__(FWD_THREADS, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -242,6 +269,16 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
       float m_used = -INFINITY, l = 0.f;
       for (int j = 0; j < nkv; ++j) {
         const int gg = gb + j;
+        // keep bits of this row's 64 keys, drawn while S is not yet in registers
+        uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
+        if (DROP) {
+          const unsigned long long e0 = drop_row(p, b, hd, qb * 128 + r) + j * 128 + wg * 64;
+          keep_lo = drop_bits32(e0, p.drop);
+          keep_hi = drop_bits32(e0 + 32, p.drop);
+          uint32_t* mt = mask_tile(p, b, hd, qb, j);
+          mt[(2 * wg) * 128 + r] = keep_lo;
+          mt[(2 * wg + 1) * 128 + r] = keep_hi;
+        }
         if (!mbar_wait_bounded(B(SFULL + (gg & 1)), (gg >> 1) & 1, p.status, abort_flag)) {
           ok = false;
           break;
@@ -293,14 +330,12 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
           rsp[k & 7] += s[k];
         }
         l = l * alpha + (((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7])));
-        if (p.drop.on) {
+        if (DROP) {
           // dropped probabilities leave the row sum but not P V
-          const unsigned long long e0 = drop_row(p, b, hd, qb * 128 + r) + j * 128 + wg * 64;
-          const uint32_t lo = drop_bits32(e0, p.drop), hi = drop_bits32(e0 + 32, p.drop);
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
-            if (!((lo >> k) & 1u)) s[k] = 0.f;
-            if (!((hi >> k) & 1u)) s[32 + k] = 0.f;
+            if (!((keep_lo >> k) & 1u)) s[k] = 0.f;
+            if (!((keep_hi >> k) & 1u)) s[32 + k] = 0.f;
           }
         }
         if (j > 0) {
@@ -348,7 +383,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         break;
       }
       const float lt = ls[r] + ls[128 + r];
-      const float inv = (p.drop.on ? p.drop.scale : 1.0f) / lt;
+      const float inv = (DROP ? p.drop.scale : 1.0f) / lt;
       const int row = b * p.seq + qb * 128 + r;
       bf16* orow = p.ctx + (size_t)row * p.h + (size_t)hd * p.d;
       for (int c = wg * 32; c < p.d; c += 64) {
@@ -396,7 +431,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
 // smem: Q, dO (NA atoms of 16 KB), K[ST], V[ST] (NA atoms of 8 KB), dS (1 atom
 // of 16 KB), D exchange.  TMEM: S[b] cols 64b, dP[b] cols 128+64b, dQ[b] cols
 // 256+128b.
-template <int NA, int KS>
+template <int NA, int KS, bool DROP>
 __global__ void __launch_bounds__(BWD_THREADS, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm128,
                           const __grid_constant__ CUtensorMap tm64,
@@ -574,6 +609,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const uint32_t tDQ = tmem + 256 + 128 * (n & 1);
       for (int j = 0; j < nkv; ++j) {
         const int gg = gb + j;
+        // keep bits of this row over the block's 32 keys, loaded before the wait
+        const uint32_t keep =
+            DROP ? mask_tile(p, b, hd, qb, j >> 1)[((j & 1) * 2 + wg) * 128 + r] : 0xffffffffu;
         if (!mbar_wait_bounded(B(SF + (gg & 1)), (gg >> 1) & 1, p.status, abort_flag)) {
           ok = false;
           break;
@@ -586,10 +624,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           tmem_ld32(tS + lane_off + col, sv);
           tmem_ld32(tDP + lane_off + col, dv);
           tmem_ld_wait();
-          const uint32_t keep =
-              p.drop.on ? drop_bits32(drop_row(p, b, hd, qb * 128 + r) + j * 64 + wg * 32, p.drop)
-                        : 0xffffffffu;
-          const float dsc = p.drop.on ? p.drop.scale : 1.0f;
+          const float dsc = DROP ? p.drop.scale : 1.0f;
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int key = j * 64 + wg * 32 + i;
@@ -666,7 +701,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 // smem: K, V (NA atoms of 16 KB), Q[ST], dO[ST] (NA atoms of 8 KB), P^T and dS^T
 // (1 atom of 16 KB each), lse / D per stage.  TMEM: S^T[b] cols 64b, dP^T[b]
 // cols 128+64b, dV 256.., dK 384..
-template <int NA, int KS>
+template <int NA, int KS, bool DROP>
 __global__ void __launch_bounds__(BWD_THREADS, 1)
     attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm128,
                            const __grid_constant__ CUtensorMap tm64,
@@ -824,6 +859,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const int key = kb * 128 + r;
       for (int i = 0; i < nq; ++i) {
         const int gg = gb + i;
+        const int q0 = (first + i) * 64 + wg * 32;
+        // the forward's keep word of query q0+lane over this warp's keys, loaded
+        // before the waits so its latency hides behind them
+        const uint32_t kword =
+            DROP ? mask_tile(p, b, hd, q0 >> 7, kb)[q4 * 128 + (q0 & 127) + lane] : 0u;
         if (!mbar_wait_bounded(B(STF + (gg & 1)), (gg >> 1) & 1, p.status, abort_flag)) {
           ok = false;
           break;
@@ -836,7 +876,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           break;
         }
         tc_fence_after();
-        const int q0 = (first + i) * 64 + wg * 32;
         const float* s_lse = s_lse0 + (gg % ST) * 64 + wg * 32;
         const float* s_d = s_d0 + (gg % ST) * 64 + wg * 32;
         const uint32_t col = (gg & 1) * 64 + wg * 32;
@@ -846,27 +885,16 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           tmem_ld32(tST + lane_off + col, sv);
           tmem_ld32(tDPT + lane_off + col, dv);
           tmem_ld_wait();
-          // Keep bits: query q0+e, this thread's key.  One Philox block covers
-          // 4 consecutive keys of one query, i.e. the 4 lanes of a quad; lane c
-          // of the quad draws the blocks of queries q0 + 4m + c and the quad
-          // trades them, so that every draw is used once.
-          uint32_t qk[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-          const int kq = lane & 3;
-          if (p.drop.on) {
-            uint32_t mine = 0;
-#pragma unroll
-            for (int m = 0; m < 8; ++m)
-              mine |= drop_bits4((drop_row(p, b, hd, q0 + 4 * m + kq) + (key & ~3)) >> 2, p.drop)
-                      << (4 * m);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) qk[c] = __shfl_sync(0xffffffffu, mine, (lane & ~3) | c);
-          }
-          const float dsc = p.drop.on ? p.drop.scale : 1.0f;
+          // Keep bits of queries q0 .. q0+31 for this thread's key: lane l reads
+          // the forward's word of query q0+l over this warp's 32 keys, and a
+          // warp transpose hands lane k the word over queries for key k.
+          const uint32_t keep = DROP ? warp_transpose32(kword, lane) : 0xffffffffu;
+          const float dsc = DROP ? p.drop.scale : 1.0f;
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             float pr = fast_exp2(__uint_as_float(sv[e]) * p.scale_log2 - s_lse[e] * LOG2E);
             if (q0 + e < key) pr = 0.f;
-            const bool kept = (qk[e & 3] >> (4 * (e >> 2) + kq)) & 1u;
+            const bool kept = (keep >> e) & 1u;
             pt[e] = kept ? pr * dsc : 0.f;
             dst[e] = pr * ((kept ? __uint_as_float(dv[e]) * dsc : 0.f) - s_d[e]);
           }
@@ -996,6 +1024,7 @@ Params make_params(int batch, int seq, int heads, int d, unsigned* status, const
   p.dqkv = nullptr;
   p.dsum = nullptr;
   p.status = status;
+  p.mask = nullptr;
   return p;
 }
 
@@ -1008,30 +1037,44 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 
 bool attn_tc_supported(int seq, int d) { return seq % 128 == 0 && (d == 64 || d == 96 || d == 128); }
 
+size_t attn_mask_bytes(int batch, int seq, int heads) {
+  const size_t nqb = (size_t)seq / 128;
+  return (size_t)batch * heads * (nqb * (nqb + 1) / 2) * 2048;
+}
+
 cudaError_t attn_fwd_tc(const void* qkv, void* ctx, float* lse, int batch, int seq, int heads,
-                        int d, const Dropout& drop, unsigned* status, const LaunchCtx& c) {
+                        int d, const Dropout& drop, uint32_t* mask, unsigned* status,
+                        const LaunchCtx& c) {
   using namespace attn;
   if (batch == 0) return cudaSuccess;
   if (!attn_tc_supported(seq, d)) return cudaErrorInvalidValue;
   CUtensorMap tm;
   if (!make_map(&tm, qkv, 3ull * heads * d, (uint64_t)batch * seq, 128)) return cudaErrorInvalidValue;
+  if (drop.on && !mask) return cudaErrorInvalidValue;
   Params p = make_params(batch, seq, heads, d, status, drop);
+  p.mask = mask;
   p.ctx = static_cast<bf16*>(ctx);
   p.lse = lse;
   const int items = p.nqb * heads * batch;
   const int grid = items < c.num_sms ? items : c.num_sms;
   const double flops = 2.0 * 2.0 * batch * heads * d * ((double)seq * (seq + 1) / 2.0);
   cudaError_t e;
-#define FWD_CASE(NA_, KS_)                                                          \
-  {                                                                                 \
-    const size_t sm = fwd_smem(NA_);                                                \
-    if ((e = set_smem(attn_fwd_tc_kernel<NA_, KS_>, sm)) != cudaSuccess) return e;  \
-    c.before(KK_ATTN_FWD, flops);                                                   \
-    attn_fwd_tc_kernel<NA_, KS_><<<grid, FWD_THREADS, sm, c.stream>>>(tm, p);       \
+#define FWD_CASE(NA_, KS_, DR_)                                                          \
+  {                                                                                      \
+    const size_t sm = fwd_smem(NA_);                                                     \
+    if ((e = set_smem(attn_fwd_tc_kernel<NA_, KS_, DR_>, sm)) != cudaSuccess) return e;  \
+    c.before(KK_ATTN_FWD, flops);                                                        \
+    attn_fwd_tc_kernel<NA_, KS_, DR_><<<grid, FWD_THREADS, sm, c.stream>>>(tm, p);       \
   }
-  if (d == 64) FWD_CASE(1, 4)
-  else if (d == 96) FWD_CASE(2, 6)
-  else FWD_CASE(2, 8)
+  if (drop.on) {
+    if (d == 64) FWD_CASE(1, 4, true)
+    else if (d == 96) FWD_CASE(2, 6, true)
+    else FWD_CASE(2, 8, true)
+  } else {
+    if (d == 64) FWD_CASE(1, 4, false)
+    else if (d == 96) FWD_CASE(2, 6, false)
+    else FWD_CASE(2, 8, false)
+  }
 #undef FWD_CASE
   c.after();
   return cudaGetLastError();
@@ -1039,7 +1082,8 @@ cudaError_t attn_fwd_tc(const void* qkv, void* ctx, float* lse, int batch, int s
 
 cudaError_t attn_bwd_tc(const void* qkv, const void* ctx, const float* lse, const void* dctx,
                         void* dqkv, float* dsum, int batch, int seq, int heads, int d,
-                        const Dropout& drop, unsigned* status, const LaunchCtx& c) {
+                        const Dropout& drop, const uint32_t* mask, unsigned* status,
+                        const LaunchCtx& c) {
   using namespace attn;
   if (batch == 0) return cudaSuccess;
   if (!attn_tc_supported(seq, d)) return cudaErrorInvalidValue;
@@ -1049,7 +1093,9 @@ cudaError_t attn_bwd_tc(const void* qkv, const void* ctx, const float* lse, cons
       !make_map(&tmdo128, dctx, (uint64_t)heads * d, n, 128) ||
       !make_map(&tmdo64, dctx, (uint64_t)heads * d, n, 64))
     return cudaErrorInvalidValue;
+  if (drop.on && !mask) return cudaErrorInvalidValue;
   Params p = make_params(batch, seq, heads, d, status, drop);
+  p.mask = const_cast<uint32_t*>(mask);
   p.ctx = static_cast<bf16*>(const_cast<void*>(ctx));
   p.lse = const_cast<float*>(lse);
   p.dctx = static_cast<const bf16*>(dctx);
@@ -1059,24 +1105,31 @@ cudaError_t attn_bwd_tc(const void* qkv, const void* ctx, const float* lse, cons
   const int grid = items < c.num_sms ? items : c.num_sms;
   const double tri = (double)batch * heads * d * ((double)seq * (seq + 1) / 2.0);
   cudaError_t e;
-#define BWD_CASE(NA_, KS_)                                                                    \
-  {                                                                                           \
-    if ((e = set_smem(attn_bwd_dq_tc_kernel<NA_, KS_>, dq_smem(NA_))) != cudaSuccess) return e; \
-    if ((e = set_smem(attn_bwd_dkv_tc_kernel<NA_, KS_>, dkv_smem(NA_))) != cudaSuccess)         \
-      return e;                                                                               \
-    c.before(KK_ATTN_BWD, 2.0 * 3.0 * tri);                                                   \
-    attn_bwd_dq_tc_kernel<NA_, KS_><<<grid, BWD_THREADS, dq_smem(NA_), c.stream>>>(            \
-        tm128, tm64, tmdo128, p);                                                             \
-    c.after();                                                                                \
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;                                    \
-    c.before(KK_ATTN_BWD, 2.0 * 4.0 * tri);                                                   \
-    attn_bwd_dkv_tc_kernel<NA_, KS_><<<grid, BWD_THREADS, dkv_smem(NA_), c.stream>>>(          \
-        tm128, tm64, tmdo64, p);                                                              \
-    c.after();                                                                                \
+#define BWD_CASE(NA_, KS_, DR_)                                                                \
+  {                                                                                            \
+    if ((e = set_smem(attn_bwd_dq_tc_kernel<NA_, KS_, DR_>, dq_smem(NA_))) != cudaSuccess)       \
+      return e;                                                                                \
+    if ((e = set_smem(attn_bwd_dkv_tc_kernel<NA_, KS_, DR_>, dkv_smem(NA_))) != cudaSuccess)     \
+      return e;                                                                                \
+    c.before(KK_ATTN_BWD, 2.0 * 3.0 * tri);                                                    \
+    attn_bwd_dq_tc_kernel<NA_, KS_, DR_><<<grid, BWD_THREADS, dq_smem(NA_), c.stream>>>(        \
+        tm128, tm64, tmdo128, p);                                                              \
+    c.after();                                                                                 \
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;                                     \
+    c.before(KK_ATTN_BWD, 2.0 * 4.0 * tri);                                                    \
+    attn_bwd_dkv_tc_kernel<NA_, KS_, DR_><<<grid, BWD_THREADS, dkv_smem(NA_), c.stream>>>(      \
+        tm128, tm64, tmdo64, p);                                                               \
+    c.after();                                                                                 \
   }
-  if (d == 64) BWD_CASE(1, 4)
-  else if (d == 96) BWD_CASE(2, 6)
-  else BWD_CASE(2, 8)
+  if (drop.on) {
+    if (d == 64) BWD_CASE(1, 4, true)
+    else if (d == 96) BWD_CASE(2, 6, true)
+    else BWD_CASE(2, 8, true)
+  } else {
+    if (d == 64) BWD_CASE(1, 4, false)
+    else if (d == 96) BWD_CASE(2, 6, false)
+    else BWD_CASE(2, 8, false)
+  }
 #undef BWD_CASE
   return cudaGetLastError();
 }

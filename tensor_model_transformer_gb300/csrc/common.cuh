@@ -432,23 +432,23 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // numbers: as easy as 1, 2, 3", SC'11): per round, counter words 0 and 2 are
 // multiplied by the two Philox multipliers; the high halves of the products are
 // XORed with words 1 / 3 and the round key, the low halves move to words 1 / 3;
-// the key advances by the two Weyl increments between rounds.
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+// the key advances by the two Weyl increments between rounds (Dropout::rk holds
+// the ten round keys, precomputed on the host).
+__device__ __forceinline__ uint4 philox4x32_10_rk(uint4 c, const uint32_t (&rk)[20]) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    const uint32_t lo0 = c.x * 0xD2511F53u, hi0 = __umulhi(c.x, 0xD2511F53u);
-    const uint32_t lo1 = c.z * 0xCD9E8D57u, hi1 = __umulhi(c.z, 0xCD9E8D57u);
-    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
-    k0 += 0x9E3779B9u;
-    k1 += 0xBB67AE85u;
+    const unsigned long long p0 = (unsigned long long)c.x * 0xD2511F53u;
+    const unsigned long long p1 = (unsigned long long)c.z * 0xCD9E8D57u;
+    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ rk[2 * r], (uint32_t)p1,
+                   (uint32_t)(p0 >> 32) ^ c.w ^ rk[2 * r + 1], (uint32_t)p0);
   }
   return c;
 }
 
 // Keep bits of elements 4*blk .. 4*blk+3 of a dropout site: bit k for 4*blk+k.
 __device__ __forceinline__ uint32_t drop_bits4(unsigned long long blk, const Dropout& d) {
-  const uint4 w = philox4x32_10(make_uint4((uint32_t)blk, (uint32_t)(blk >> 32), d.site, 0u),
-                                (uint32_t)d.seed, (uint32_t)(d.seed >> 32));
+  const uint4 w =
+      philox4x32_10_rk(make_uint4((uint32_t)blk, (uint32_t)(blk >> 32), d.site, 0u), d.rk);
   return (w.x >= d.thresh ? 1u : 0u) | (w.y >= d.thresh ? 2u : 0u) |
          (w.z >= d.thresh ? 4u : 0u) | (w.w >= d.thresh ? 8u : 0u);
 }

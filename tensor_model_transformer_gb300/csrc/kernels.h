@@ -22,6 +22,10 @@ struct Dropout {
   float scale;       // 1 / (1 - p)
   uint32_t site;
   int on;
+  // Philox round keys: rk[2r], rk[2r+1] = the key of round r (seed words plus
+  // r times the Weyl increments), precomputed so the kernels read them from
+  // parameter space.
+  uint32_t rk[20];
 };
 
 // A(m,k) = ptr[m*ld + k] when k_major, else ptr[k*ld + m].
@@ -116,6 +120,7 @@ size_t colsum_partial_floats(int n, int N);
 // (before rounding to the storage type).  N % 4 == 0.
 cudaError_t colsum_dropout(int dtype, const void* Y, void* Ym, int64_t ld, int n, int N,
                            const Dropout& drop, float* out, float* partial, const LaunchCtx& c);
+size_t colsum_dropout_partial_floats(int n, int N);
 
 // Error text for mtl_last_cuda_error, shared by every entry point.
 void record_cuda_error(cudaError_t e, const char* where);
@@ -135,10 +140,15 @@ cudaError_t attn_bwd_simt(int dtype, const void* qkv, const void* ctx, const flo
 // {64, 96, 128}).  Forward writes ctx and lse; backward writes dqkv and, as
 // scratch, dsum [batch][heads][seq].
 bool attn_tc_supported(int seq, int d);
+// With dropout the forward writes the keep bits to `mask` (attn_mask_bytes) and
+// the backward reads them back.
+size_t attn_mask_bytes(int batch, int seq, int heads);
 cudaError_t attn_fwd_tc(const void* qkv, void* ctx, float* lse, int batch, int seq, int heads,
-                        int d, const Dropout& drop, unsigned* status, const LaunchCtx& c);
+                        int d, const Dropout& drop, uint32_t* mask, unsigned* status,
+                        const LaunchCtx& c);
 cudaError_t attn_bwd_tc(const void* qkv, const void* ctx, const float* lse, const void* dctx,
                         void* dqkv, float* dsum, int batch, int seq, int heads, int d,
-                        const Dropout& drop, unsigned* status, const LaunchCtx& c);
+                        const Dropout& drop, const uint32_t* mask, unsigned* status,
+                        const LaunchCtx& c);
 
 }  // namespace mtl

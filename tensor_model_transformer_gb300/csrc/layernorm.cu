@@ -15,6 +15,7 @@ namespace {
 constexpr int kLnThreadsMax = 512;
 constexpr int kLnBwdBlocks = 512;     // row blocks of the dgamma/dbeta reduction
 constexpr int kColsumBlocks = 128;    // row blocks of the bias-gradient reduction
+constexpr int kColsumDropBlocks = 512;  // the same with dropout (Philox work per element)
 
 // Sums NV values over the block in place; `red` holds NV*32 floats.  Every
 // thread adds the per-warp sums in the same order.
@@ -412,7 +413,7 @@ cudaError_t colsum_dropout_t(const void* Y, void* Ym, int64_t ld, int n, int N,
                              const Dropout& drop, float* out, float* partial,
                              const LaunchCtx& c) {
   constexpr int E = Vec<T>::N;
-  const int nblk = n < kColsumBlocks ? (n > 0 ? n : 1) : kColsumBlocks;
+  const int nblk = n < kColsumDropBlocks ? (n > 0 ? n : 1) : kColsumDropBlocks;
   const int rows = (n + nblk - 1) / nblk;
   const int threads = 256;
   dim3 grid((N / E + threads - 1) / threads, nblk);
@@ -431,6 +432,10 @@ cudaError_t colsum_dropout_t(const void* Y, void* Ym, int64_t ld, int n, int N,
 size_t ln_bwd_partial_floats(int n, int h) {
   const size_t nblk = n < kLnBwdBlocks ? (n > 0 ? n : 1) : kLnBwdBlocks;
   return 2 * nblk * (size_t)h;
+}
+size_t colsum_dropout_partial_floats(int n, int N) {
+  const size_t nblk = n < kColsumDropBlocks ? (n > 0 ? n : 1) : kColsumDropBlocks;
+  return nblk * (size_t)N;
 }
 size_t colsum_partial_floats(int n, int N) {
   const size_t nblk = n < kColsumBlocks ? (n > 0 ? n : 1) : kColsumBlocks;

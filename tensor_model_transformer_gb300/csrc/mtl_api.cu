@@ -82,6 +82,13 @@ Dropout make_drop(float p, unsigned long long seed, uint32_t site) {
   const double t = floor((double)p * 4294967296.0);
   d.thresh = d.on ? (uint32_t)(t > 4294967295.0 ? 4294967295.0 : t) : 0u;
   d.scale = d.on ? (float)(1.0 / (1.0 - (double)p)) : 1.0f;
+  uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+  for (int r = 0; r < 10; ++r) {
+    d.rk[2 * r] = k0;
+    d.rk[2 * r + 1] = k1;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
   return d;
 }
 
@@ -144,6 +151,9 @@ mtl_saved_layout saved_layout(const Dims& D) {
   L.u2 = take(nh);
   L.z = take((size_t)D.n * D.f * D.esz);
   L.a = take((size_t)D.n * D.f * D.esz);
+  L.attn_mask = take(D.dtype == MTL_BF16 && D.p_attn > 0.f
+                         ? attn_mask_bytes((int)D.batch, (int)D.seq, (int)D.heads)
+                         : 0);
   L.total = off;
   return L;
 }
@@ -174,6 +184,8 @@ WsLayout ws_layout(const Dims& D) {
   const size_t widest = (size_t)(D.f > 3 * D.h ? D.f : 3 * D.h);
   const size_t pc = colsum_partial_floats((int)D.n, (int)widest);
   if (pc > pf) pf = pc;
+  const size_t pd = colsum_dropout_partial_floats((int)D.n, (int)D.h);
+  if (pd > pf) pf = pd;
   W.partial = take(pf * 4);
   W.total = off;
   return W;
@@ -349,7 +361,7 @@ mtl_status mtl_layer_fwd(const mtl_layer_desc* desc, const mtl_weights* w, const
   // F3 attention per head
   if (bf) {
     MTL_TRY(attn_fwd_tc(qkv, ctx, at<float>(saved, L.lse), (int)D.batch, (int)D.seq, (int)D.heads,
-                        (int)D.d, drop_attn, status, c),
+                        (int)D.d, drop_attn, at<uint32_t>(saved, L.attn_mask), status, c),
             "attention fwd");
   } else {
     MTL_TRY(attn_fwd_simt(D.dtype, qkv, ctx, at<float>(saved, L.lse), (int)D.batch, (int)D.seq,
@@ -505,7 +517,8 @@ mtl_status mtl_layer_bwd(const mtl_layer_desc* desc, const mtl_weights* w, const
   // B7 attention backward per head
   if (D.dtype == MTL_BF16) {
     MTL_TRY(attn_bwd_tc(qkv, ctx, at<float>(saved, L.lse), dctx, dqkv, dsum, (int)D.batch,
-                        (int)D.seq, (int)D.heads, (int)D.d, drop_attn, status, c),
+                        (int)D.seq, (int)D.heads, (int)D.d, drop_attn,
+                        at<uint32_t>(saved, L.attn_mask), status, c),
             "attention bwd");
   } else {
     MTL_TRY(attn_bwd_simt(D.dtype, qkv, ctx, at<float>(saved, L.lse), dctx, dqkv, dsum,
@@ -589,15 +602,26 @@ mtl_status mtl_attention_ws_bytes(int32_t batch, int32_t seq, int32_t heads, siz
   return MTL_OK;
 }
 
+mtl_status mtl_attention_mask_bytes(int32_t dtype, int32_t batch, int32_t seq, int32_t heads,
+                                    float p_attn, size_t* bytes) {
+  if (!bytes) return MTL_ERR_INVALID_ARG;
+  mtl_status st = attn_validate(dtype, batch, seq, heads, 64, p_attn);
+  if (st != MTL_OK) return st;
+  *bytes = dtype == MTL_BF16 && p_attn > 0.f ? attn_mask_bytes(batch, seq, heads) : 0;
+  return MTL_OK;
+}
+
 mtl_status mtl_attention_fwd(int32_t dtype, int32_t batch, int32_t seq, int32_t heads, int32_t d,
-                             const void* qkv, void* ctx, float* lse, float p_attn, uint64_t seed,
-                             void* workspace, size_t ws_bytes, mtl_stream stream) {
+                             const void* qkv, void* ctx, float* lse, void* mask_bits,
+                             float p_attn, uint64_t seed, void* workspace, size_t ws_bytes,
+                             mtl_stream stream) {
   g_launches = 0;
   g_cuda_err[0] = 0;
   mtl_status st = attn_validate(dtype, batch, seq, heads, d, p_attn);
   if (st != MTL_OK) return st;
+  const bool need_mask = dtype == MTL_BF16 && p_attn > 0.f;
   if (!aligned16(qkv) || !aligned16(ctx) || !aligned16(lse) || !aligned16(workspace) ||
-      qkv == ctx)
+      qkv == ctx || (need_mask && !aligned16(mask_bits)))
     return MTL_ERR_INVALID_ARG;
   if (ws_bytes < attn_ws_bytes(batch, seq, heads)) return MTL_ERR_WORKSPACE;
   const int nsm = device_sm_count();
@@ -609,7 +633,9 @@ mtl_status mtl_attention_fwd(int32_t dtype, int32_t batch, int32_t seq, int32_t 
   if (batch == 0) return MTL_OK;
   const Dropout drop = make_drop(p_attn, seed, SITE_ATTN);
   if (dtype == MTL_BF16) {
-    MTL_TRY(attn_fwd_tc(qkv, ctx, lse, batch, seq, heads, d, drop, status, c), "attention fwd");
+    MTL_TRY(attn_fwd_tc(qkv, ctx, lse, batch, seq, heads, d, drop, static_cast<uint32_t*>(mask_bits),
+                        status, c),
+            "attention fwd");
   } else {
     MTL_TRY(attn_fwd_simt(dtype, qkv, ctx, lse, batch, seq, heads, d, drop, c), "attention fwd");
   }
@@ -618,14 +644,15 @@ mtl_status mtl_attention_fwd(int32_t dtype, int32_t batch, int32_t seq, int32_t 
 
 mtl_status mtl_attention_bwd(int32_t dtype, int32_t batch, int32_t seq, int32_t heads, int32_t d,
                              const void* qkv, const void* ctx, const float* lse, const void* dctx,
-                             void* dqkv, float p_attn, uint64_t seed, void* workspace,
-                             size_t ws_bytes, mtl_stream stream) {
+                             const void* mask_bits, void* dqkv, float p_attn, uint64_t seed,
+                             void* workspace, size_t ws_bytes, mtl_stream stream) {
   g_launches = 0;
   g_cuda_err[0] = 0;
   mtl_status st = attn_validate(dtype, batch, seq, heads, d, p_attn);
   if (st != MTL_OK) return st;
   if (!aligned16(qkv) || !aligned16(ctx) || !aligned16(lse) || !aligned16(dctx) ||
-      !aligned16(dqkv) || !aligned16(workspace) || dqkv == qkv || dqkv == dctx)
+      !aligned16(dqkv) || !aligned16(workspace) || dqkv == qkv || dqkv == dctx ||
+      (dtype == MTL_BF16 && p_attn > 0.f && !aligned16(mask_bits)))
     return MTL_ERR_INVALID_ARG;
   if (ws_bytes < attn_ws_bytes(batch, seq, heads)) return MTL_ERR_WORKSPACE;
   const int nsm = device_sm_count();
@@ -638,7 +665,8 @@ mtl_status mtl_attention_bwd(int32_t dtype, int32_t batch, int32_t seq, int32_t 
   float* dsum = at<float>(workspace, kStatusBytes);
   const Dropout drop = make_drop(p_attn, seed, SITE_ATTN);
   if (dtype == MTL_BF16) {
-    MTL_TRY(attn_bwd_tc(qkv, ctx, lse, dctx, dqkv, dsum, batch, seq, heads, d, drop, status, c),
+    MTL_TRY(attn_bwd_tc(qkv, ctx, lse, dctx, dqkv, dsum, batch, seq, heads, d, drop,
+                        static_cast<const uint32_t*>(mask_bits), status, c),
             "attention bwd");
   } else {
     MTL_TRY(attn_bwd_simt(dtype, qkv, ctx, lse, dctx, dqkv, dsum, batch, seq, heads, d, drop, c),

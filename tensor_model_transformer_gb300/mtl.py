@@ -12,7 +12,8 @@ import os
 
 PARAM_NAMES = ("w_qkv", "b_qkv", "w_o", "b_o", "w_fc1", "b_fc1", "w_fc2", "b_fc2",
                "ln1_g", "ln1_b", "ln2_g", "ln2_b")
-SAVED_NAMES = ("mu1", "rstd1", "u1", "qkv", "ctx", "lse", "x1", "mu2", "rstd2", "u2", "z", "a")
+SAVED_NAMES = ("mu1", "rstd1", "u1", "qkv", "ctx", "lse", "x1", "mu2", "rstd2", "u2", "z", "a",
+               "attn_mask")
 
 F32, BF16 = 0, 1
 STATUS = {0: "MTL_OK", 1: "MTL_ERR_INVALID_ARG", 2: "MTL_ERR_UNSUPPORTED",
@@ -71,9 +72,11 @@ def lib():
         L.mtl_gemm.argtypes = [i32, i32, i32, i32, i32, vp, i64, i32, vp, i64, i32, i32, vp, vp,
                                i64, vp, i64, vp, i64, i32, vp, sz, vp]
         L.mtl_attention_ws_bytes.argtypes = [i32, i32, i32, ctypes.POINTER(sz)]
-        L.mtl_attention_fwd.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, ctypes.c_float,
+        L.mtl_attention_mask_bytes.argtypes = [i32, i32, i32, i32, ctypes.c_float,
+                                               ctypes.POINTER(sz)]
+        L.mtl_attention_fwd.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, ctypes.c_float,
                                         ctypes.c_uint64, vp, sz, vp]
-        L.mtl_attention_bwd.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp,
+        L.mtl_attention_bwd.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp,
                                         ctypes.c_float, ctypes.c_uint64, vp, sz, vp]
         L.mtl_selftest_wait_timeout.argtypes = [vp, i64, vp]
         L.mtl_selftest_wait_timeout.restype = ctypes.c_int
@@ -85,7 +88,7 @@ def lib():
         L.mtl_last_launch_count.restype = ctypes.c_int32
         for fn in ("mtl_layer_sizes", "mtl_layer_saved_layout", "mtl_layer_fwd", "mtl_layer_bwd",
                    "mtl_layer_check", "mtl_gemm", "mtl_attention_ws_bytes", "mtl_attention_fwd",
-                   "mtl_attention_bwd"):
+                   "mtl_attention_bwd", "mtl_attention_mask_bytes"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -186,20 +189,27 @@ def _dt(dtype):
     return {"f32": F32, "bf16": BF16, F32: F32, BF16: BF16}[dtype]
 
 
-def attention_fwd(dtype, batch, seq, heads, d, qkv, ctx, lse, workspace, p_attn=0.0, seed=0,
-                  stream=None):
-    """mtl_attention_fwd on torch tensors."""
+def attention_mask_bytes(dtype, batch, seq, heads, p_attn) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().mtl_attention_mask_bytes(_dt(dtype), batch, seq, heads, p_attn,
+                                          ctypes.byref(out)), "mtl_attention_mask_bytes")
+    return out.value
+
+
+def attention_fwd(dtype, batch, seq, heads, d, qkv, ctx, lse, workspace, mask=None, p_attn=0.0,
+                  seed=0, stream=None):
+    """mtl_attention_fwd on torch tensors; mask: attention_mask_bytes bytes or None."""
     _check(lib().mtl_attention_fwd(_dt(dtype), batch, seq, heads, d, _ptr(qkv), _ptr(ctx),
-                                   _ptr(lse), p_attn, seed, _ptr(workspace),
+                                   _ptr(lse), _ptr(mask), p_attn, seed, _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _stream(stream)),
            "mtl_attention_fwd")
 
 
-def attention_bwd(dtype, batch, seq, heads, d, qkv, ctx, lse, dctx, dqkv, workspace, p_attn=0.0,
-                  seed=0, stream=None):
-    """mtl_attention_bwd on torch tensors."""
+def attention_bwd(dtype, batch, seq, heads, d, qkv, ctx, lse, dctx, dqkv, workspace, mask=None,
+                  p_attn=0.0, seed=0, stream=None):
+    """mtl_attention_bwd on torch tensors (mask: the forward's keep bits)."""
     _check(lib().mtl_attention_bwd(_dt(dtype), batch, seq, heads, d, _ptr(qkv), _ptr(ctx),
-                                   _ptr(lse), _ptr(dctx), _ptr(dqkv), p_attn, seed,
+                                   _ptr(lse), _ptr(dctx), _ptr(mask), _ptr(dqkv), p_attn, seed,
                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
                                    _stream(stream)),
            "mtl_attention_bwd")

@@ -177,9 +177,19 @@ def test_dropout_probabilities_validated(mtl):
     assert d1.seed == (1 << 63) + 5
     s0, w0 = mtl.layer_sizes(d0)
     s1, w1 = mtl.layer_sizes(d1)
-    # the saved buffer does not grow (masks are recomputed); the workspace holds
-    # one dropped-out [n][h] gradient
-    assert s1 == s0 and w1 >= w0 + 256 * 256 * 2
+    # saved grows by the attention keep bits (2 KB per causal 128 x 128 tile of
+    # each (batch, head)); the workspace holds one dropped-out [n][h] gradient
+    tiles = 2 * 4 * 1                       # batch 2, heads 4, seq 128: one tile
+    assert mtl.attention_mask_bytes("bf16", 2, 128, 4, 0.1) == tiles * 2048
+    assert mtl.attention_mask_bytes("bf16", 2, 128, 4, 0.0) == 0
+    assert mtl.attention_mask_bytes("f32", 2, 128, 4, 0.1) == 0
+    assert mtl.attention_mask_bytes("bf16", 1, 512, 1, 0.1) == 10 * 2048
+    lay = mtl.layer_saved_layout(d1)
+    assert lay["total"] - lay["attn_mask"] >= tiles * 2048 and s1 == lay["total"]
+    assert s1 == s0 + tiles * 2048 and w1 >= w0 + 256 * 256 * 2
+    # fp32 layers redraw the attention mask: nothing saved
+    f0, f1 = good_desc(mtl, dtype="f32"), good_desc(mtl, dtype="f32", p_attn=0.1)
+    assert mtl.layer_sizes(f0)[0] == mtl.layer_sizes(f1)[0]
 
 
 def test_layer_desc_layout_matches_header(mtl, tmp_path):
@@ -213,16 +223,21 @@ def test_attention_entry_points_reject(mtl):
     ok = dict(dtype=1, batch=2, seq=256, heads=4, d=64)
 
     def fwd(**kw):
-        c = dict(ok, p=0.1, ws=ws, qkv=a[0], ctx=a[1], lse=a[2], wsp=FAKE + 16384)
+        c = dict(ok, p=0.1, ws=ws, qkv=a[0], ctx=a[1], lse=a[2], mask=FAKE + 24576,
+                 wsp=FAKE + 16384)
         c.update(kw)
         return L.mtl_attention_fwd(c["dtype"], c["batch"], c["seq"], c["heads"], c["d"], c["qkv"],
-                                   c["ctx"], c["lse"], c["p"], 7, c["wsp"], c["ws"], None)
+                                   c["ctx"], c["lse"], c["mask"], c["p"], 7, c["wsp"], c["ws"],
+                                   None)
 
     assert fwd(p=1.0) == 1 and fwd(p=-0.5) == 1 and fwd(dtype=3) == 1 and fwd(heads=0) == 1
     assert fwd(d=32) == 2 and fwd(seq=200) == 2          # bf16 needs seq % 128 == 0
     assert fwd(qkv=FAKE + 8) == 1 and fwd(lse=None) == 1 and fwd(ctx=a[0]) == 1
+    assert fwd(mask=None) == 1                           # bf16 with dropout needs the bits
     assert fwd(ws=ws - 1) == 3
-    assert L.mtl_attention_bwd(1, 2, 256, 4, 64, a[0], a[1], a[2], FAKE + 12288, a[0], 0.0, 0,
-                               FAKE + 16384, ws, None) == 1    # dqkv aliases qkv
-    assert L.mtl_attention_bwd(1, 2, 256, 4, 64, a[0], a[1], a[2], FAKE + 12288, FAKE + 20480,
-                               0.0, 0, FAKE + 16384, 255, None) == 3
+    assert L.mtl_attention_bwd(1, 2, 256, 4, 64, a[0], a[1], a[2], FAKE + 12288, FAKE + 24576,
+                               a[0], 0.0, 0, FAKE + 16384, ws, None) == 1    # dqkv aliases qkv
+    assert L.mtl_attention_bwd(1, 2, 256, 4, 64, a[0], a[1], a[2], FAKE + 12288, None,
+                               FAKE + 20480, 0.1, 0, FAKE + 16384, ws, None) == 1
+    assert L.mtl_attention_bwd(1, 2, 256, 4, 64, a[0], a[1], a[2], FAKE + 12288, None,
+                               FAKE + 20480, 0.0, 0, FAKE + 16384, 255, None) == 3

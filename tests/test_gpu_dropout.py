@@ -107,13 +107,16 @@ def _gpu_attention(dtype, batch, seq, heads, d, qkv, p_attn, seed, dctx=None):
     ctx = torch.empty((batch * seq, heads * d), dtype=tq.dtype, device="cuda")
     lse = torch.empty((batch, heads, seq), dtype=torch.float32, device="cuda")
     ws = torch.empty(mtl.attention_ws_bytes(batch, seq, heads), dtype=torch.uint8, device="cuda")
-    mtl.attention_fwd(dtype, batch, seq, heads, d, tq, ctx, lse, ws, p_attn=p_attn, seed=seed)
+    mb = mtl.attention_mask_bytes(dtype, batch, seq, heads, p_attn)
+    mask = torch.empty(mb, dtype=torch.uint8, device="cuda") if mb else None
+    mtl.attention_fwd(dtype, batch, seq, heads, d, tq, ctx, lse, ws, mask=mask, p_attn=p_attn,
+                      seed=seed)
     mtl.layer_check(ws)
     out = {"ctx": to_np(ctx), "lse": to_np(lse)}
     if dctx is not None:
         tdo = to_device(dctx, dtype)
         dqkv = torch.empty_like(tq)
-        mtl.attention_bwd(dtype, batch, seq, heads, d, tq, ctx, lse, tdo, dqkv, ws,
+        mtl.attention_bwd(dtype, batch, seq, heads, d, tq, ctx, lse, tdo, dqkv, ws, mask=mask,
                           p_attn=p_attn, seed=seed)
         mtl.layer_check(ws)
         out["dqkv"] = to_np(dqkv)
@@ -195,3 +198,39 @@ def test_attention_ds_masks(dtype, seq, d, grad, p_attn):
     if p_attn > 0:
         assert np.max(np.abs(a_r)) > step      # the design is not degenerate
     assert np.max(np.abs(a_g - a_r)) < 0.25 * step
+
+
+@pytest.mark.parametrize("seq,d", [(128, 64), (384, 128)])
+def test_attention_stored_keep_bits(seq, d):
+    """The bits the bf16 forward stores for the backward are the oracle's keep
+    mask: tile (qb, kb <= qb) of each (batch, head), word w of row r at w*128+r."""
+    import torch
+    from tensor_model_transformer_gb300 import mtl
+    from harness import to_device
+    batch, heads, seed, p_attn = 2, 3, 4242, f32(0.4)
+    rng = np.random.default_rng(0)
+    qkv = rng.standard_normal((batch * seq, 3 * heads * d)) * 0.5
+    tq = to_device(qkv, "bf16")
+    ctx = torch.empty((batch * seq, heads * d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((batch, heads, seq), dtype=torch.float32, device="cuda")
+    ws = torch.empty(mtl.attention_ws_bytes(batch, seq, heads), dtype=torch.uint8, device="cuda")
+    mb = mtl.attention_mask_bytes("bf16", batch, seq, heads, p_attn)
+    mask = torch.zeros(mb, dtype=torch.uint8, device="cuda")
+    mtl.attention_fwd("bf16", batch, seq, heads, d, tq, ctx, lse, ws, mask=mask, p_attn=p_attn,
+                      seed=seed)
+    mtl.layer_check(ws)
+    words = mask.cpu().numpy().view(np.uint32)
+    nqb = seq // 128
+    nt = nqb * (nqb + 1) // 2
+    assert words.size == batch * heads * nt * 512
+    bits = ((words[:, None] >> np.arange(32, dtype=np.uint32)[None, :]) & 1).astype(bool)
+    bits = bits.reshape(batch, heads, nt, 4, 128, 32)       # [.., word, row, bit]
+    for b in range(batch):
+        for hd in range(heads):
+            ref = oracle.philox.attention_mask(b, hd, heads, seq, seed, p_attn)
+            for qb in range(nqb):
+                for kb in range(qb + 1):
+                    t = bits[b, hd, qb * (qb + 1) // 2 + kb]          # [4, 128, 32]
+                    got = t.transpose(1, 0, 2).reshape(128, 128)      # [row, key]
+                    want = ref[qb * 128:(qb + 1) * 128, kb * 128:(kb + 1) * 128]
+                    assert np.array_equal(got, want), (b, hd, qb, kb)
