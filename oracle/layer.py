@@ -27,7 +27,8 @@ Readings where the pages are silent (each is also listed in the design notes):
   * LayerNorm uses the biased variance and eps = 1e-5 inside the square root.
   * Row-parallel biases (b_o, b_fc2) are added once, after the partition sum.
   * Activations are [batch, seq, h] row-major; weights are [out, in].
-  * Dropout is 0 (identity) in every workload.
+  * Dropout is the identity unless a dropout dict is given (masks as in
+    ``oracle/philox.py``).
 
 The unpartitioned functions compute the layer the method reaches exactly (in
 exact arithmetic) for any t.  ``layer_fwd_partitioned`` / ``layer_bwd_partitioned``

@@ -53,3 +53,26 @@ def test_full_size(cfg, t):
 @pytest.mark.slow
 def test_full_size_large_layer():
     full_size_check("E", 8)
+
+
+@pytest.mark.parametrize("cfg,t", [("D", 8)])
+def test_full_size_with_dropout(cfg, t):
+    """The headline workload with dropout (bench.py --p-drop 0.1): batch element 0
+    of the full run against the oracle on that element (its masks depend only on
+    its own batch index, 0 in both runs), and every parameter gradient of a
+    batch-1 run against the oracle."""
+    from harness import f32
+    shape = synthetic.CONFIGS[cfg]
+    drop = dict(p_attn=f32(0.1), p_hidden=f32(0.1), seed=1234)
+    x, p, dy = make(shape)
+    full = run_gpu(shape, x, p, dy, t, want_saved=False, drop=drop)
+    one = shape.with_(batch=1)
+    ref0 = run_oracle(one, x[:1], p, dy[:1], drop=drop)
+    errs = {"y[0]": rel_err(full["y"][0], ref0["y"][0]),
+            "dx[0]": rel_err(full["dx"][0], ref0["dx"][0])}
+    assert errs["y[0]"] <= tolerance("y", "bf16"), errs
+    assert errs["dx[0]"] <= tolerance("dx", "bf16"), errs
+    g = run_gpu(one, x[:1], p, dy[:1], t, drop=drop)
+    e0 = compare(g, ref0, "bf16", keys=GRADS + ["y", "dx", "s_ctx", "s_x1"])
+    bad = {k: v for k, v in e0.items() if v > tolerance(k, "bf16")}
+    assert not bad, bad
