@@ -31,7 +31,8 @@ import numpy as np  # noqa: E402
 import synthetic  # noqa: E402
 
 METRIC = "layer fwd+bwd TFLOP/s on 1 GB300 and % of BF16 dense peak; oracle-match"
-KIND_NAMES = {1: "gemm_tc", 2: "gemm_simt", 3: "attn_fwd", 4: "attn_bwd", 5: "ln_fwd",
+KIND_NAMES = {1: "gemm_tc", 2: "gemm_simt", 3: "attn_fwd", 4: "attn_bwd", 5: "ln_fwd", 9: "gemv_tc",
+              10: "attn_decode", 11: "kv_write",
               6: "ln_bwd", 7: "colsum", 8: "finalize"}
 
 

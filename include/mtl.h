@@ -207,6 +207,40 @@ mtl_status mtl_attention_bwd(int32_t dtype, int32_t batch, int32_t seq, int32_t 
                              const void* mask_bits, void* dqkv, float p_attn, uint64_t seed,
                              void* workspace, size_t ws_bytes, mtl_stream stream);
 
+/* ---- Inference: prefill and one-token decode with a head-sharded KV cache
+ * (page "Megatron-LM: GPU-Cluster Training Parallelism", section "Paper 1: QKV
+ * Column-Parallel Splitting in Detail", inference-time behaviour: each
+ * partition appends the new token's K and V of its own heads to its local
+ * cache shard, so the cache divides evenly by t; the row-parallel outputs are
+ * reduced once per token).
+ *   kv_cache: K then V, each [batch][heads][max_seq][d] of desc.dtype, the V
+ *   block starting kv_bytes/2 into the buffer; partition p's shard is heads
+ *   [p*H/t, (p+1)*H/t) of every batch row.  cache_len: DEVICE int32 [batch],
+ *   the number of valid positions of each sequence.
+ *   mtl_layer_prefill: y = layer(x) for prompts x [batch][desc.seq][h] (no
+ *   dropout), K and V of every prompt token written at positions
+ *   0..desc.seq-1, cache_len[b] = desc.seq.  Same shape rules as mtl_layer_fwd;
+ *   desc.seq <= max_seq.
+ *   mtl_layer_decode: one new token per sequence, x_tok / y_tok [batch][h]:
+ *   token b sits at position cache_len[b], its K and V are written there, it
+ *   attends to keys 0..cache_len[b], and cache_len[b] is incremented, so a
+ *   captured CUDA graph of this call can be replayed token after token.
+ *   desc.seq is not used; desc.batch <= 128.  A cache_len outside
+ *   [0, max_seq) makes the step skip that sequence's attention and report
+ *   MTL_ERR_INVALID_ARG through mtl_layer_check (its outputs are undefined).
+ *   The bf16 decode GEMMs read every weight once per step (split-K tcgen05,
+ *   the K slices of a tile summed in slice order: bitwise reproducible).
+ * mtl_infer_sizes: bytes of the cache and of the two calls' workspaces
+ * (prefill's holds the layer's intermediates). */
+mtl_status mtl_infer_sizes(const mtl_layer_desc* desc, int32_t max_seq, size_t* kv_bytes,
+                           size_t* prefill_ws_bytes, size_t* decode_ws_bytes);
+mtl_status mtl_layer_prefill(const mtl_layer_desc* desc, const mtl_weights* w, const void* x,
+                             void* y, void* kv_cache, int32_t max_seq, int32_t* cache_len,
+                             void* workspace, size_t ws_bytes, mtl_stream stream);
+mtl_status mtl_layer_decode(const mtl_layer_desc* desc, const mtl_weights* w, const void* x_tok,
+                            void* y_tok, void* kv_cache, int32_t max_seq, int32_t* cache_len,
+                            void* workspace, size_t ws_bytes, mtl_stream stream);
+
 /* Bias gradient for callers that cannot allocate device memory:
  *   out[j] = sum_{i < rows} dy[i*ld + j]   (j < cols; fp32, fixed order)
  * -- the sum mtl_layer_bwd uses for b_fc2, b_o, b_fc1 and b_qkv, with the same

@@ -55,7 +55,8 @@ struct GemmArgs {
 // Kernel kinds reported through the profiling hooks.
 enum KernelKind {
   KK_GEMM_TC = 1, KK_GEMM_SIMT = 2, KK_ATTN_FWD = 3, KK_ATTN_BWD = 4, KK_LN_FWD = 5,
-  KK_LN_BWD = 6, KK_COLSUM = 7, KK_FINALIZE = 8
+  KK_LN_BWD = 6, KK_COLSUM = 7, KK_FINALIZE = 8, KK_GEMV_TC = 9, KK_ATTN_DECODE = 10,
+  KK_KV_WRITE = 11
 };
 
 // Optional per-launch timing: when set, events[2i] / events[2i+1] are recorded
@@ -150,5 +151,37 @@ cudaError_t attn_bwd_tc(const void* qkv, const void* ctx, const float* lse, cons
                         void* dqkv, float* dsum, int batch, int seq, int heads, int d,
                         const Dropout& drop, const uint32_t* mask, unsigned* status,
                         const LaunchCtx& c);
+
+// ---------------------------------------------------------------- inference
+// Largest token batch of a decode step, and the SM count the decode GEMMs'
+// K split assumes at most (so workspace sizes do not depend on the device).
+constexpr int kDecodeMaxBatch = 128;
+constexpr int kDecodeSmCap = 160;
+
+// Decode GEMM out[b][n] = epi(sum_k W[n][k] X[b][k]) for a few tokens b
+// (tcgen05, weights as the M operand, K split across CTAs, slices summed in
+// order by the last CTA of each output tile).  epi: EPI_BIAS, EPI_BIAS_RESID
+// (+ R[b][n]) or EPI_BIAS_GELU.  part / counters: gemv_tc_partial_floats /
+// gemv_tc_counters; counters zero on entry (left zero).
+bool gemv_tc_supported(int N, int K, int batch);
+size_t gemv_tc_partial_floats(int N, int K, int batch, int num_sms);
+size_t gemv_tc_counters(int N);
+cudaError_t gemv_tc(int epi, int N, int K, int batch, const void* W, const void* X,
+                    const void* bias, const void* R, void* out, float* part, int* counters,
+                    unsigned* status, const LaunchCtx& c);
+// Decode attention: appends each sequence's new K, V (from qkv [batch][3h]) at
+// position cache_len[b] of the [batch][heads][max_seq][d] caches and attends to
+// keys 0..cache_len[b]; ctx [batch][h].  part: batch*heads*attn_decode_splits
+// *(d+2) floats; counters: batch*heads ints, zero on entry.
+int attn_decode_splits(int max_seq);
+cudaError_t attn_decode(int dtype, const void* qkv, void* kcache, void* vcache,
+                        const int* cache_len, void* ctx, float* part, int* counters, int batch,
+                        int heads, int d, int max_seq, double kv_bytes, unsigned* status,
+                        const LaunchCtx& c);
+// Prefill: K, V of every prompt token to cache positions 0..seq-1, lengths = seq.
+cudaError_t kv_write(int dtype, const void* qkv, void* kcache, void* vcache, int* cache_len,
+                     int batch, int seq, int heads, int d, int max_seq, const LaunchCtx& c);
+// cache_len[b] += 1 (lengths outside [0, max_seq) are left alone).
+cudaError_t kv_advance(int* cache_len, int batch, int max_seq, const LaunchCtx& c);
 
 }  // namespace mtl

@@ -265,6 +265,142 @@ size_t attn_ws_bytes(int32_t batch, int32_t seq, int32_t heads) {
     if (_e != cudaSuccess) return cuda_fail(_e, where); \
   } while (0)
 
+// The layer forward after validation (shared by mtl_layer_fwd and prefill):
+// intermediates go to `saved` at saved_layout(D).
+mtl_status forward_core(const Dims& D, float ln_eps, const mtl_weights* w, const void* x, void* y,
+                        void* saved, unsigned* status, const LaunchCtx& c) {
+  const mtl_saved_layout L = saved_layout(D);
+  const int n = (int)D.n, h = (int)D.h, f = (int)D.f, t = (int)D.t;
+  void* u1 = at<char>(saved, L.u1);
+  void* qkv = at<char>(saved, L.qkv);
+  void* ctx = at<char>(saved, L.ctx);
+  void* x1 = at<char>(saved, L.x1);
+  void* u2 = at<char>(saved, L.u2);
+  void* z = at<char>(saved, L.z);
+  void* a = at<char>(saved, L.a);
+  const bool bf = D.dtype == MTL_BF16;
+  const Dropout drop_attn = make_drop(D.p_attn, D.seed, SITE_ATTN);
+
+  // F1 LN1
+  MTL_TRY(ln_fwd(D.dtype, x, w->ln1_g, w->ln1_b, u1, at<float>(saved, L.mu1),
+                 at<float>(saved, L.rstd1), n, h, ln_eps, c),
+          "ln1 fwd");
+  // F2 QKV, column-parallel: partition p = rows [p*3h/t, (p+1)*3h/t) of w_qkv
+  {
+    GemmArgs g = gemm_args(n, 3 * h, h, 1, u1, h, true, w->w_qkv, h, true, EPI_BIAS, qkv, 3 * h,
+                           false, status);
+    g.bias = w->b_qkv;
+    MTL_TRY(run_gemm(D, g, c), "qkv gemm");
+  }
+  // F3 attention per head
+  if (bf) {
+    MTL_TRY(attn_fwd_tc(qkv, ctx, at<float>(saved, L.lse), (int)D.batch, (int)D.seq, (int)D.heads,
+                        (int)D.d, drop_attn, at<uint32_t>(saved, L.attn_mask), status, c),
+            "attention fwd");
+  } else {
+    MTL_TRY(attn_fwd_simt(D.dtype, qkv, ctx, at<float>(saved, L.lse), (int)D.batch, (int)D.seq,
+                          (int)D.heads, (int)D.d, drop_attn, c),
+            "attention fwd");
+  }
+  // F4 out-proj, row-parallel + g: t partials over K = h, + b_o, dropout, + x
+  {
+    GemmArgs g = gemm_args(n, h, h, t, ctx, h, true, w->w_o, h, true, EPI_BIAS_RESID, x1, h,
+                           false, status);
+    g.bias = w->b_o;
+    g.drop = make_drop(D.p_hidden, D.seed, SITE_OUT);
+    g.R = x;
+    g.ldr = h;
+    MTL_TRY(run_gemm(D, g, c), "out-proj gemm");
+  }
+  // F5 LN2
+  MTL_TRY(ln_fwd(D.dtype, x1, w->ln2_g, w->ln2_b, u2, at<float>(saved, L.mu2),
+                 at<float>(saved, L.rstd2), n, h, ln_eps, c),
+          "ln2 fwd");
+  // F6 fc1, column-parallel + bias + GeLU (saves z and a)
+  {
+    GemmArgs g = gemm_args(n, f, h, 1, u2, h, true, w->w_fc1, h, true, EPI_BIAS_GELU, a, f, false,
+                           status);
+    g.bias = w->b_fc1;
+    g.Z = z;
+    g.ldz = f;
+    MTL_TRY(run_gemm(D, g, c), "fc1 gemm");
+  }
+  // F7 fc2, row-parallel + g: t partials over K = ffn, + b_fc2, dropout, + x1
+  {
+    GemmArgs g = gemm_args(n, h, f, t, a, f, true, w->w_fc2, f, true, EPI_BIAS_RESID, y, h, false,
+                           status);
+    g.bias = w->b_fc2;
+    g.drop = make_drop(D.p_hidden, D.seed, SITE_FC2);
+    g.R = x1;
+    g.ldr = h;
+    MTL_TRY(run_gemm(D, g, c), "fc2 gemm");
+  }
+  return MTL_OK;
+}
+
+
+// ---------------------------------------------------------------- inference
+
+// Decode validation: the layer rules that concern a token-batch step (seq is
+// not used), max_seq >= 1, batch <= kDecodeMaxBatch.
+mtl_status validate_decode(const mtl_layer_desc* desc, int32_t max_seq, Dims* o) {
+  if (!desc) return MTL_ERR_INVALID_ARG;
+  mtl_layer_desc d = *desc;
+  if (max_seq <= 0 || d.batch > kDecodeMaxBatch) return max_seq <= 0 ? MTL_ERR_INVALID_ARG
+                                                                     : MTL_ERR_UNSUPPORTED;
+  d.seq = d.dtype == MTL_BF16 ? 128 : 1;   // a valid stand-in: decode has no sequence axis
+  d.p_attn = 0.f;
+  d.p_hidden = 0.f;
+  mtl_status st = validate(&d, o);
+  if (st != MTL_OK) return st;
+  o->seq = 1;
+  o->n = o->batch;
+  return MTL_OK;
+}
+
+size_t kv_cache_bytes(const Dims& D, int32_t max_seq) {
+  return 2 * align_up((size_t)D.batch * D.heads * max_seq * D.d * D.esz);
+}
+
+struct DecWs {
+  size_t c_qkv, c_o, c_fc1, c_fc2, c_att, mean, rstd, u, qkv, ctx, x1, a, z, part, apart, total;
+};
+
+DecWs decode_ws(const Dims& D, int32_t max_seq) {
+  DecWs W;
+  size_t off = kStatusBytes;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align_up(bytes);
+    return at;
+  };
+  const int h = (int)D.h, f = (int)D.f, b = (int)D.batch;
+  W.c_qkv = take(gemv_tc_counters(3 * h) * 4);
+  W.c_o = take(gemv_tc_counters(h) * 4);
+  W.c_fc1 = take(gemv_tc_counters(f) * 4);
+  W.c_fc2 = take(gemv_tc_counters(h) * 4);
+  W.c_att = take((size_t)b * D.heads * 4);
+  W.mean = take((size_t)b * 4);
+  W.rstd = take((size_t)b * 4);
+  W.u = take((size_t)b * h * D.esz);
+  W.qkv = take((size_t)b * 3 * h * D.esz);
+  W.ctx = take((size_t)b * h * D.esz);
+  W.x1 = take((size_t)b * h * D.esz);
+  W.a = take((size_t)b * f * D.esz);
+  W.z = take(D.dtype == MTL_BF16 ? 0 : (size_t)b * f * D.esz);
+  size_t pf = 0;
+  if (D.dtype == MTL_BF16) {
+    const size_t c[4] = {gemv_tc_partial_floats(3 * h, h, b, kDecodeSmCap),
+                         gemv_tc_partial_floats(h, h, b, kDecodeSmCap),
+                         gemv_tc_partial_floats(f, h, b, kDecodeSmCap),
+                         gemv_tc_partial_floats(h, f, b, kDecodeSmCap)};
+    for (size_t v : c) pf = v > pf ? v : pf;
+  }
+  W.part = take(pf * 4);
+  W.apart = take((size_t)b * D.heads * attn_decode_splits(max_seq) * (D.d + 2) * 4);
+  W.total = off;
+  return W;
+}
 }  // namespace
 
 extern "C" {
@@ -335,73 +471,7 @@ mtl_status mtl_layer_fwd(const mtl_layer_desc* desc, const mtl_weights* w, const
   MTL_TRY(cudaMemsetAsync(status, 0, kStatusBytes, s), "status reset");
   if (D.n == 0) return MTL_OK;
 
-  const mtl_saved_layout L = saved_layout(D);
-  const int n = (int)D.n, h = (int)D.h, f = (int)D.f, t = (int)D.t;
-  void* u1 = at<char>(saved, L.u1);
-  void* qkv = at<char>(saved, L.qkv);
-  void* ctx = at<char>(saved, L.ctx);
-  void* x1 = at<char>(saved, L.x1);
-  void* u2 = at<char>(saved, L.u2);
-  void* z = at<char>(saved, L.z);
-  void* a = at<char>(saved, L.a);
-  const bool bf = D.dtype == MTL_BF16;
-  const Dropout drop_attn = make_drop(D.p_attn, D.seed, SITE_ATTN);
-
-  // F1 LN1
-  MTL_TRY(ln_fwd(D.dtype, x, w->ln1_g, w->ln1_b, u1, at<float>(saved, L.mu1),
-                 at<float>(saved, L.rstd1), n, h, desc->ln_eps, c),
-          "ln1 fwd");
-  // F2 QKV, column-parallel: partition p = rows [p*3h/t, (p+1)*3h/t) of w_qkv
-  {
-    GemmArgs g = gemm_args(n, 3 * h, h, 1, u1, h, true, w->w_qkv, h, true, EPI_BIAS, qkv, 3 * h,
-                           false, status);
-    g.bias = w->b_qkv;
-    MTL_TRY(run_gemm(D, g, c), "qkv gemm");
-  }
-  // F3 attention per head
-  if (bf) {
-    MTL_TRY(attn_fwd_tc(qkv, ctx, at<float>(saved, L.lse), (int)D.batch, (int)D.seq, (int)D.heads,
-                        (int)D.d, drop_attn, at<uint32_t>(saved, L.attn_mask), status, c),
-            "attention fwd");
-  } else {
-    MTL_TRY(attn_fwd_simt(D.dtype, qkv, ctx, at<float>(saved, L.lse), (int)D.batch, (int)D.seq,
-                          (int)D.heads, (int)D.d, drop_attn, c),
-            "attention fwd");
-  }
-  // F4 out-proj, row-parallel + g: t partials over K = h, + b_o, dropout, + x
-  {
-    GemmArgs g = gemm_args(n, h, h, t, ctx, h, true, w->w_o, h, true, EPI_BIAS_RESID, x1, h,
-                           false, status);
-    g.bias = w->b_o;
-    g.drop = make_drop(D.p_hidden, D.seed, SITE_OUT);
-    g.R = x;
-    g.ldr = h;
-    MTL_TRY(run_gemm(D, g, c), "out-proj gemm");
-  }
-  // F5 LN2
-  MTL_TRY(ln_fwd(D.dtype, x1, w->ln2_g, w->ln2_b, u2, at<float>(saved, L.mu2),
-                 at<float>(saved, L.rstd2), n, h, desc->ln_eps, c),
-          "ln2 fwd");
-  // F6 fc1, column-parallel + bias + GeLU (saves z and a)
-  {
-    GemmArgs g = gemm_args(n, f, h, 1, u2, h, true, w->w_fc1, h, true, EPI_BIAS_GELU, a, f, false,
-                           status);
-    g.bias = w->b_fc1;
-    g.Z = z;
-    g.ldz = f;
-    MTL_TRY(run_gemm(D, g, c), "fc1 gemm");
-  }
-  // F7 fc2, row-parallel + g: t partials over K = ffn, + b_fc2, dropout, + x1
-  {
-    GemmArgs g = gemm_args(n, h, f, t, a, f, true, w->w_fc2, f, true, EPI_BIAS_RESID, y, h, false,
-                           status);
-    g.bias = w->b_fc2;
-    g.drop = make_drop(D.p_hidden, D.seed, SITE_FC2);
-    g.R = x1;
-    g.ldr = h;
-    MTL_TRY(run_gemm(D, g, c), "fc2 gemm");
-  }
-  return MTL_OK;
+  return forward_core(D, desc->ln_eps, w, x, y, saved, status, c);
 }
 
 mtl_status mtl_layer_bwd(const mtl_layer_desc* desc, const mtl_weights* w, const void* x,
@@ -672,6 +742,134 @@ mtl_status mtl_attention_bwd(int32_t dtype, int32_t batch, int32_t seq, int32_t 
     MTL_TRY(attn_bwd_simt(dtype, qkv, ctx, lse, dctx, dqkv, dsum, batch, seq, heads, d, drop, c),
             "attention bwd");
   }
+  return MTL_OK;
+}
+
+// ---------------------------------------------------------------- inference
+
+mtl_status mtl_infer_sizes(const mtl_layer_desc* desc, int32_t max_seq, size_t* kv_bytes,
+                           size_t* prefill_ws_bytes, size_t* decode_ws_bytes) {
+  Dims D;
+  mtl_status st = validate_decode(desc, max_seq, &D);
+  if (st != MTL_OK) return st;
+  if (kv_bytes) *kv_bytes = kv_cache_bytes(D, max_seq);
+  if (decode_ws_bytes) *decode_ws_bytes = decode_ws(D, max_seq).total;
+  if (prefill_ws_bytes) {
+    Dims P;
+    mtl_layer_desc pd = *desc;
+    pd.p_attn = 0.f;
+    pd.p_hidden = 0.f;
+    st = validate(&pd, &P);
+    if (st != MTL_OK) return st;
+    if (pd.seq > max_seq) return MTL_ERR_INVALID_ARG;
+    *prefill_ws_bytes = kStatusBytes + saved_layout(P).total;
+  }
+  return MTL_OK;
+}
+
+mtl_status mtl_layer_prefill(const mtl_layer_desc* desc, const mtl_weights* w, const void* x,
+                             void* y, void* kv_cache, int32_t max_seq, int32_t* cache_len,
+                             void* workspace, size_t ws_bytes, mtl_stream stream) {
+  g_launches = 0;
+  g_cuda_err[0] = 0;
+  if (!desc) return MTL_ERR_INVALID_ARG;
+  if (desc->p_attn != 0.f || desc->p_hidden != 0.f) return MTL_ERR_INVALID_ARG;
+  Dims D;
+  mtl_status st = validate(desc, &D);
+  if (st != MTL_OK) return st;
+  if (max_seq < desc->seq) return MTL_ERR_INVALID_ARG;
+  if (!weights_ok(w) || !aligned16(x) || !aligned16(y) || !aligned16(kv_cache) ||
+      !aligned16(workspace) || !cache_len || x == y)
+    return MTL_ERR_INVALID_ARG;
+  const size_t need = kStatusBytes + saved_layout(D).total;
+  if (ws_bytes < need) return MTL_ERR_WORKSPACE;
+  const int nsm = device_sm_count();
+  if (nsm <= 0) return cuda_fail(cudaGetLastError(), "device query");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  LaunchCtx c{s, nsm, &g_launches, &g_prof};
+  unsigned* status = static_cast<unsigned*>(workspace);
+  MTL_TRY(cudaMemsetAsync(status, 0, kStatusBytes, s), "status reset");
+  if (D.n == 0) return MTL_OK;
+  void* saved = at<char>(workspace, kStatusBytes);
+  st = forward_core(D, desc->ln_eps, w, x, y, saved, status, c);
+  if (st != MTL_OK) return st;
+  const size_t half = kv_cache_bytes(D, max_seq) / 2;
+  MTL_TRY(kv_write(D.dtype, at<char>(saved, saved_layout(D).qkv), kv_cache,
+                   at<char>(kv_cache, half), cache_len, (int)D.batch, (int)D.seq, (int)D.heads,
+                   (int)D.d, max_seq, c),
+          "kv write");
+  return MTL_OK;
+}
+
+mtl_status mtl_layer_decode(const mtl_layer_desc* desc, const mtl_weights* w, const void* x_tok,
+                            void* y_tok, void* kv_cache, int32_t max_seq, int32_t* cache_len,
+                            void* workspace, size_t ws_bytes, mtl_stream stream) {
+  g_launches = 0;
+  g_cuda_err[0] = 0;
+  Dims D;
+  mtl_status st = validate_decode(desc, max_seq, &D);
+  if (st != MTL_OK) return st;
+  if (!weights_ok(w) || !aligned16(x_tok) || !aligned16(y_tok) || !aligned16(kv_cache) ||
+      !aligned16(workspace) || !cache_len || x_tok == y_tok)
+    return MTL_ERR_INVALID_ARG;
+  const DecWs W = decode_ws(D, max_seq);
+  if (ws_bytes < W.total) return MTL_ERR_WORKSPACE;
+  const int nsm = device_sm_count();
+  if (nsm <= 0) return cuda_fail(cudaGetLastError(), "device query");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  LaunchCtx c{s, nsm, &g_launches, &g_prof};
+  unsigned* status = static_cast<unsigned*>(workspace);
+  // status word and every split-K / split-KV counter
+  MTL_TRY(cudaMemsetAsync(status, 0, W.mean, s), "status reset");
+  if (D.batch == 0) return MTL_OK;
+  const int b = (int)D.batch, h = (int)D.h, f = (int)D.f;
+  const bool bf = D.dtype == MTL_BF16;
+  void* u = at<char>(workspace, W.u);
+  void* qkv = at<char>(workspace, W.qkv);
+  void* ctx = at<char>(workspace, W.ctx);
+  void* x1 = at<char>(workspace, W.x1);
+  void* a = at<char>(workspace, W.a);
+  float* part = at<float>(workspace, W.part);
+  const size_t half = kv_cache_bytes(D, max_seq) / 2;
+  // gemm on the layer's path: the split-K tcgen05 decode GEMM for bf16, the
+  // exact fp32 CUDA-core GEMM for fp32
+  auto dgemm = [&](int epi, int N, int K, const void* Wt, const void* X, const void* bias,
+                   const void* R, void* out, size_t counters) -> cudaError_t {
+    if (bf)
+      return gemv_tc(epi, N, K, b, Wt, X, bias, R, out, part, at<int>(workspace, counters),
+                     status, c);
+    GemmArgs g = gemm_args(b, N, K, 1, X, K, true, Wt, K, true, epi, out, N, false, status);
+    g.bias = bias;
+    g.R = R;
+    g.ldr = N;
+    g.Z = at<char>(workspace, W.z);
+    g.ldz = N;
+    return gemm_simt(kF32, g, c);
+  };
+  // D1 LN1
+  MTL_TRY(ln_fwd(D.dtype, x_tok, w->ln1_g, w->ln1_b, u, at<float>(workspace, W.mean),
+                 at<float>(workspace, W.rstd), b, h, desc->ln_eps, c),
+          "ln1");
+  // D2 QKV (column-parallel)
+  MTL_TRY(dgemm(EPI_BIAS, 3 * h, h, w->w_qkv, u, w->b_qkv, nullptr, qkv, W.c_qkv), "qkv");
+  // D3 attention over the cache; appends K, V
+  double kvb = 0;   // algorithmic bytes are not known on the host (lengths live on the device)
+  MTL_TRY(attn_decode(D.dtype, qkv, kv_cache, at<char>(kv_cache, half), cache_len, ctx,
+                      at<float>(workspace, W.apart), at<int>(workspace, W.c_att), b,
+                      (int)D.heads, (int)D.d, max_seq, kvb, status, c),
+          "attention");
+  // D4 out-proj (row-parallel, ordered K-slice sum) + b_o + x
+  MTL_TRY(dgemm(EPI_BIAS_RESID, h, h, w->w_o, ctx, w->b_o, x_tok, x1, W.c_o), "out-proj");
+  // D5 LN2
+  MTL_TRY(ln_fwd(D.dtype, x1, w->ln2_g, w->ln2_b, u, at<float>(workspace, W.mean),
+                 at<float>(workspace, W.rstd), b, h, desc->ln_eps, c),
+          "ln2");
+  // D6 fc1 + GeLU
+  MTL_TRY(dgemm(EPI_BIAS_GELU, f, h, w->w_fc1, u, w->b_fc1, nullptr, a, W.c_fc1), "fc1");
+  // D7 fc2 (row-parallel) + b_fc2 + x1
+  MTL_TRY(dgemm(EPI_BIAS_RESID, h, f, w->w_fc2, a, w->b_fc2, x1, y_tok, W.c_fc2), "fc2");
+  // D8 cache lengths + 1
+  MTL_TRY(kv_advance(cache_len, b, max_seq, c), "advance");
   return MTL_OK;
 }
 

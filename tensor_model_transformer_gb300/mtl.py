@@ -78,6 +78,12 @@ def lib():
                                         ctypes.c_uint64, vp, sz, vp]
         L.mtl_attention_bwd.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp,
                                         ctypes.c_float, ctypes.c_uint64, vp, sz, vp]
+        L.mtl_infer_sizes.argtypes = [pd, i32, ctypes.POINTER(sz), ctypes.POINTER(sz),
+                                      ctypes.POINTER(sz)]
+        L.mtl_layer_prefill.argtypes = [pd, ctypes.POINTER(Weights), vp, vp, vp, i32, vp, vp, sz,
+                                        vp]
+        L.mtl_layer_decode.argtypes = [pd, ctypes.POINTER(Weights), vp, vp, vp, i32, vp, vp, sz,
+                                       vp]
         L.mtl_selftest_wait_timeout.argtypes = [vp, i64, vp]
         L.mtl_selftest_wait_timeout.restype = ctypes.c_int
         L.mtl_bias_grad_noalloc.argtypes = [i32, vp, i64, i32, i32, vp, vp]
@@ -88,7 +94,8 @@ def lib():
         L.mtl_last_launch_count.restype = ctypes.c_int32
         for fn in ("mtl_layer_sizes", "mtl_layer_saved_layout", "mtl_layer_fwd", "mtl_layer_bwd",
                    "mtl_layer_check", "mtl_gemm", "mtl_attention_ws_bytes", "mtl_attention_fwd",
-                   "mtl_attention_bwd", "mtl_attention_mask_bytes"):
+                   "mtl_attention_bwd", "mtl_attention_mask_bytes", "mtl_infer_sizes",
+                   "mtl_layer_prefill", "mtl_layer_decode"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -213,6 +220,46 @@ def attention_bwd(dtype, batch, seq, heads, d, qkv, ctx, lse, dctx, dqkv, worksp
                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
                                    _stream(stream)),
            "mtl_attention_bwd")
+
+
+def infer_sizes(desc: LayerDesc, max_seq: int):
+    """(kv_cache_bytes, prefill_workspace_bytes, decode_workspace_bytes)."""
+    kv, pw, dw = ctypes.c_size_t(0), ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check(lib().mtl_infer_sizes(ctypes.byref(desc), max_seq, ctypes.byref(kv), ctypes.byref(pw),
+                                 ctypes.byref(dw)), "mtl_infer_sizes")
+    return kv.value, pw.value, dw.value
+
+
+def layer_prefill(desc, weights: dict, x, y, kv_cache, max_seq, cache_len, workspace,
+                  stream=None):
+    """mtl_layer_prefill on torch tensors (cache_len: int32 device tensor [batch])."""
+    wt = _weights(weights)
+    _check(lib().mtl_layer_prefill(ctypes.byref(desc), ctypes.byref(wt), _ptr(x), _ptr(y),
+                                   _ptr(kv_cache), max_seq, _ptr(cache_len), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)),
+           "mtl_layer_prefill")
+
+
+def layer_decode(desc, weights: dict, x_tok, y_tok, kv_cache, max_seq, cache_len, workspace,
+                 stream=None):
+    """mtl_layer_decode on torch tensors: one token per sequence, advances cache_len."""
+    wt = _weights(weights)
+    _check(lib().mtl_layer_decode(ctypes.byref(desc), ctypes.byref(wt), _ptr(x_tok), _ptr(y_tok),
+                                  _ptr(kv_cache), max_seq, _ptr(cache_len), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)),
+           "mtl_layer_decode")
+
+
+def kv_views(desc: LayerDesc, kv_cache, max_seq):
+    """(K, V) views [batch][heads][max_seq][d] of a KV-cache buffer."""
+    dt = torch_dtype(desc)
+    esz = 2 if desc.dtype == BF16 else 4
+    d = desc.h // desc.heads
+    cnt = desc.batch * desc.heads * max_seq * d
+    half = kv_cache.numel() // 2
+    k = kv_cache[:cnt * esz].view(dt).view(desc.batch, desc.heads, max_seq, d)
+    v = kv_cache[half:half + cnt * esz].view(dt).view(desc.batch, desc.heads, max_seq, d)
+    return k, v
 
 
 def selftest_wait_timeout(workspace, limit_cycles, stream=None):

@@ -241,3 +241,30 @@ def test_attention_entry_points_reject(mtl):
                                FAKE + 20480, 0.1, 0, FAKE + 16384, ws, None) == 1
     assert L.mtl_attention_bwd(1, 2, 256, 4, 64, a[0], a[1], a[2], FAKE + 12288, None,
                                FAKE + 20480, 0.0, 0, FAKE + 16384, 255, None) == 3
+
+
+def test_infer_sizes_and_rejects(mtl):
+    d = good_desc(mtl, seq=256, batch=3)
+    kv, pw, dw = mtl.infer_sizes(d, 512)
+    assert kv == 2 * 3 * 4 * 512 * 64 * 2                  # K and V, bf16
+    assert pw >= mtl.layer_sizes(d)[0] and dw > 256
+    s, p, w = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    L = mtl.lib()
+    assert L.mtl_infer_sizes(ctypes.byref(d), 0, ctypes.byref(s), None, None) == 1
+    assert L.mtl_infer_sizes(ctypes.byref(d), 128, None, ctypes.byref(p), None) == 1  # prompt > cache
+    big = good_desc(mtl, batch=129)
+    assert L.mtl_infer_sizes(ctypes.byref(big), 512, ctypes.byref(s), None, None) == 2
+    # decode does not need seq % 128: a bf16 desc with seq = 1 still sizes a decode
+    one = good_desc(mtl, seq=1)
+    assert L.mtl_infer_sizes(ctypes.byref(one), 64, ctypes.byref(s), None, ctypes.byref(w)) == 0
+    wt = _weights(mtl)
+    ok = (FAKE, FAKE + 4096, FAKE + 8192, FAKE + 12288)
+    assert L.mtl_layer_decode(ctypes.byref(one), ctypes.byref(wt), ok[0], ok[1], ok[2], 64, None,
+                              ok[3], w.value, None) == 1              # no cache_len
+    assert L.mtl_layer_decode(ctypes.byref(one), ctypes.byref(wt), ok[0], ok[0], ok[2], 64, FAKE,
+                              ok[3], w.value, None) == 1              # y aliases x
+    assert L.mtl_layer_decode(ctypes.byref(one), ctypes.byref(wt), ok[0], ok[1], ok[2], 64, FAKE,
+                              ok[3], w.value - 1, None) == 3
+    dd = good_desc(mtl, p_attn=0.1)
+    assert L.mtl_layer_prefill(ctypes.byref(dd), ctypes.byref(wt), ok[0], ok[1], ok[2], 512, FAKE,
+                               ok[3], 1 << 30, None) == 1             # no dropout at inference
