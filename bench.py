@@ -199,6 +199,245 @@ def cpu_baseline(shape, drop=None):
                       f"fp64 numpy oracle, {sec:.1f} s"}
 
 
+# ---------------------------------------------------------------- decode workload
+
+DECODE_METRIC = "decode tokens/s on 1 GB300 (one token per sequence per step, KV cache)"
+
+
+def decode_bytes(s, lengths, esz=2):
+    """Algorithmic HBM bytes of one decode step: every weight once, the K and V
+    cache of each sequence up to and including its new position (written once,
+    read once), the small vectors; token-sized activations left out."""
+    weights = (3 * s.h * s.h + s.h * s.h + 2 * s.h * s.ffn) * esz
+    vectors = (3 * s.h + s.h + s.ffn + s.h + 4 * s.h) * esz
+    kv = sum(2 * (int(L) + 1) * s.h * esz for L in lengths)
+    return weights + vectors + kv
+
+
+def decode_flops(s, lengths):
+    g = 2 * (3 * s.h * s.h + s.h * s.h + 2 * s.h * s.ffn) * len(lengths)
+    a = sum(4 * (int(L) + 1) * s.h for L in lengths)
+    return g + a
+
+
+def run_decode_reference(args, shape, rank, world):
+    if rank != 0:
+        return
+    out = decode_cpu_baseline(shape, args.steps)
+    line = {"metric": DECODE_METRIC, "value": out["value"], "unit": "tokens/s", "n_gpus": world,
+            "steps": out["steps"], "warmup": 0, "ms_per_step": out["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": f"decode {args.config}: {shape.name}, batch 1 (of "
+                                   f"{shape.batch}), context {shape.seq}", "h": shape.h,
+                       "heads": shape.heads, "ffn": shape.ffn, "batch": 1, "context": shape.seq},
+            "cpu_baseline": {"value": out["value"], "unit": "tokens/s", "cores": out["cores"],
+                             "kind": "oracle", "sample": out["sample"]},
+            "e2e": {"value": out["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def decode_cpu_baseline(shape, steps):
+    """The oracle's decode step at batch 1 with a random cache of the prompt length."""
+    import oracle
+    d = shape.h // shape.heads
+    _, p, _ = synthetic.make_layer(shape.with_(batch=1, seq=1), seed=0)
+    rng = np.random.default_rng(3)
+    cache = oracle.decode.kv_cache(1, shape.heads, shape.seq + steps + 1, d)
+    cache["k"][:, :, :shape.seq] = rng.standard_normal((1, shape.heads, shape.seq, d))
+    cache["v"][:, :, :shape.seq] = rng.standard_normal((1, shape.heads, shape.seq, d))
+    cache["len"][:] = shape.seq
+    n = max(1, min(steps, 5))
+    t0 = time.perf_counter()
+    for _ in range(n):
+        oracle.decode.decode_step(p, rng.standard_normal((1, shape.h)), shape.heads, cache)
+    sec = (time.perf_counter() - t0) / n
+    return {"value": 1.0 / sec, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle", "steps": n, "ms_per_step": sec * 1e3,
+            "sample": f"{shape.name} at batch 1, context {shape.seq}: {n} decode steps of the "
+                      f"fp64 numpy oracle, {sec:.2f} s each"}
+
+
+def run_decode(args, shape, rank, world, local):
+    import ctypes
+    import torch
+    import torch.distributed as dist
+    from tensor_model_transformer_gb300 import mtl
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dt = torch.bfloat16 if shape.dtype == "bf16" else torch.float32
+    prompt, batch = shape.seq, shape.batch
+    max_seq = prompt + max(args.steps, args.warmup) + 8
+    x, p, _ = synthetic.make_layer(shape, seed=rank)
+    desc = mtl.layer_desc(shape.h, shape.heads, prompt, batch, shape.ffn, args.t, shape.dtype)
+    kvb, pwb, dwb = mtl.infer_sizes(desc, max_seq)
+    w = {k: torch.from_numpy(v).cuda().to(dt) for k, v in p.items()}
+    xd = torch.from_numpy(x).to(dt).cuda()
+    del x
+    yd = torch.empty_like(xd)
+    kv = torch.zeros(kvb, dtype=torch.uint8, device="cuda")
+    pws = torch.empty(pwb, dtype=torch.uint8, device="cuda")
+    dws = torch.empty(dwb, dtype=torch.uint8, device="cuda")
+    lens = torch.zeros(batch, dtype=torch.int32, device="cuda")
+    rng = np.random.default_rng(rank + 11)
+    tok_h = torch.from_numpy(rng.standard_normal((batch, shape.h)).astype(np.float32)).to(dt)
+    tok_h = tok_h.pin_memory()
+    x_in = tok_h.cuda()
+    y_out = torch.empty_like(x_in)
+    stream = torch.cuda.current_stream()
+
+    # prefill (timed once after one warm-up)
+    for _ in range(2):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        mtl.layer_prefill(desc, w, xd, yd, kv, max_seq, lens, pws, stream)
+        e1.record(stream)
+    mtl.layer_check(pws, stream)
+    prefill_ms = e0.elapsed_time(e1)
+    del pws
+
+    def reset():
+        lens.fill_(prompt)
+
+    # eager warm-up, then one decode step captured as a CUDA graph
+    reset()
+    for _ in range(args.warmup):
+        mtl.layer_decode(desc, w, x_in, y_out, kv, max_seq, lens, dws, stream)
+    launches_per_step = mtl.last_launch_count()
+    mtl.layer_check(dws, stream)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side, capture_error_mode="relaxed"):
+            mtl.layer_decode(desc, w, x_in, y_out, kv, max_seq, lens, dws, side)
+    torch.cuda.synchronize()
+
+    # ---- timed region: graph replays, inputs resident in HBM
+    reset()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    evs[0].record(stream)
+    for i in range(args.steps):
+        graph.replay()
+        evs[i + 1].record(stream)
+    evs[-1].synchronize()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms = evs[0].elapsed_time(evs[-1])
+    per_step = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps))
+    clk = clocks.stop()
+    mtl.layer_check(dws, stream)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    lengths = [prompt + i for i in range(args.steps)]
+    total_bytes = sum(decode_bytes(shape, [L] * batch) for L in lengths)
+    total_flops = sum(decode_flops(shape, [L] * batch) for L in lengths)
+    tokens = batch * args.steps * world
+    value = tokens / (ms / 1e3)
+
+    # ---- end to end: each step copies its tokens in from pinned host memory and
+    # its outputs back out
+    reset()
+    y_h = torch.empty_like(tok_h).pin_memory()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        x_in.copy_(tok_h, non_blocking=True)
+        graph.replay()
+        y_h.copy_(y_out, non_blocking=True)
+    e1.record(stream)
+    e1.synchronize()
+    ms_e2e = e0.elapsed_time(e1)
+    e2e_value = tokens / (ms_e2e / 1e3)
+    nbytes = tok_h.numel() * tok_h.element_size()
+
+    # ---- per-kernel times (eager calls with events around every kernel)
+    reset()
+    cap = launches_per_step * args.steps + 16
+    kev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * cap)]
+    for e in kev:
+        e.record(stream)
+    torch.cuda.synchronize()
+    handles = (ctypes.c_void_p * (2 * cap))(*[e.cuda_event for e in kev])
+    kinds = (ctypes.c_int32 * cap)()
+    work = (ctypes.c_double * cap)()
+    mtl.lib().mtl_profile_set(handles, cap, kinds, work)
+    for _ in range(args.steps):
+        mtl.layer_decode(desc, w, x_in, y_out, kv, max_seq, lens, dws, stream)
+    count = mtl.lib().mtl_profile_count()
+    mtl.lib().mtl_profile_set(None, 0, None, None)
+    torch.cuda.synchronize()
+    per_kind = {}
+    for i in range(count):
+        k = KIND_NAMES.get(kinds[i], str(kinds[i]))
+        rec = per_kind.setdefault(k, {"launches": 0, "ms": 0.0, "work": 0.0})
+        rec["launches"] += 1
+        rec["ms"] += kev[2 * i].elapsed_time(kev[2 * i + 1])
+        rec["work"] += work[i]
+    # attention's bytes are known here, not in the library (lengths live on the device)
+    if "attn_decode" in per_kind:
+        per_kind["attn_decode"]["work"] = float(sum(2 * (L + 1) * shape.h * 2 * batch
+                                                    for L in lengths))
+    total_ms = sum(r["ms"] for r in per_kind.values()) or 1.0
+    breakdown = {k: {"launches_per_step": r["launches"] // args.steps,
+                     "ms_per_step": r["ms"] / args.steps, "share": r["ms"] / total_ms,
+                     "gbs": (r["work"] / (r["ms"] / 1e3) / 1e9) if r["work"] else None}
+                 for k, r in sorted(per_kind.items(), key=lambda kv: -kv[1]["ms"])}
+    pk, pk_src = peaks()
+    dom = max(per_kind.items(), key=lambda kv: kv[1]["ms"])[0]
+    r = per_kind[dom]
+    achieved = r["work"] / (r["ms"] / 1e3) / 1e9
+    step_gbs = total_bytes / (ms / 1e3) / 1e9 / world
+    out = {
+        "metric": DECODE_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "step_ms": {"median": per_step[len(per_step) // 2], "min": per_step[0],
+                    "max": per_step[-1]},
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": shape.dtype, "data": "synthetic",
+        "config": {"workload": f"decode {args.config}: {shape.name}, t={args.t}, batch {batch}, "
+                               f"context {prompt}..{prompt + args.steps - 1}",
+                   "h": shape.h, "heads": shape.heads, "ffn": shape.ffn, "t": args.t,
+                   "batch": batch, "prompt": prompt, "max_seq": max_seq,
+                   "parallelism": f"replicas x{world}", "cuda_graph": True,
+                   "l2": "weights and KV cache larger than L2 (no flush)",
+                   "bytes_per_step": total_bytes / args.steps,
+                   "flops_per_step": total_flops / args.steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "step_hbm_gbs": step_gbs, "step_hbm_frac": step_gbs / pk["hbm_gbs"],
+        "prefill": {"ms": prefill_ms, "tflops": layer_flops(shape) / 3 / (prefill_ms / 1e3) / 1e12,
+                    "tokens": batch * prompt},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": nbytes,
+                "d2h_bytes_per_step": nbytes},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": None,
+                     "peak_source": f"{pk_src} hbm"},
+        "kernels": breakdown,
+    }
+    if clk:
+        out["clocks"] = clk
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = decode_cpu_baseline(shape, 3)
+        out["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 # ---------------------------------------------------------------- our arm
 
 def main():
@@ -212,6 +451,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--p-drop", type=float, default=0.0,
                     help="dropout probability of the attention and hidden sites (default 0)")
+    ap.add_argument("--workload", choices=["train", "decode"], default="train",
+                    help="train: fwd+bwd step (default); decode: prefill, then one-token "
+                         "decode steps over the KV cache")
     args = ap.parse_args()
     args.drop = None
     if args.p_drop > 0:
@@ -224,6 +466,12 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
 
+    if args.workload == "decode":
+        if args.impl == "reference":
+            run_decode_reference(args, shape, rank, world)
+        else:
+            run_decode(args, shape, rank, world, local)
+        return
     if args.impl == "reference":
         run_reference(args, shape, rank, world)
         return

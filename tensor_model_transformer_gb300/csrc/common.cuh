@@ -200,6 +200,28 @@ __device__ __forceinline__ void cluster_sync() {
           : "memory");
 }
 
+// Load a float from another CTA's shared memory (address from cluster_map).
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
+
+// ---------------------------------------------------------------- programmatic dependent launch
+// Wait until the kernel this one programmatically depends on has completed and
+// its memory is visible (returns at once when launched without that
+// dependency).  Every kernel that may be launched this way calls it before its
+// first read of a predecessor's output and before its first global write.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Let the next kernel of the stream begin launching once every CTA of this
+// grid has called this or exited (its own griddep_wait still waits for this
+// grid to finish).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" :::);
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

@@ -11,11 +11,15 @@
 // A decode step reads every weight once and the cache up to each sequence's
 // length: it is HBM-bound.  Its GEMMs have M = batch (a few tokens), so they
 // run "swapped": the weight rows are the tcgen05 M dimension (128 output
-// features per CTA) and the tokens the N dimension (batch rounded up to 16);
-// K is split across CTAs until the grid covers the SMs twice over, and the
-// last CTA of an output tile to finish adds the K-slice partials in slice
-// order (deterministic) and applies the epilogue.  The row-parallel GEMMs'
-// partition sum (g) is that ordered sum over K slices.
+// features per CTA) and the tokens the N dimension (batch rounded up to 16).
+// K is split over the CTAs of a thread-block cluster (up to 8) so the grid
+// covers the SMs about twice; each CTA leaves its fp32 partial tile in its own
+// shared memory and the cluster adds the slices in slice order through
+// distributed shared memory (deterministic, no global round trip).  The
+// row-parallel GEMMs' partition sum (g) is that ordered sum over K slices.
+// The decode kernels are chained with programmatic dependent launch: a GEMM
+// starts streaming its weights (which no earlier kernel writes) while the
+// previous kernel finishes, and waits only before touching activations.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -27,6 +31,7 @@ constexpr int BK = 64;           // K per stage (one 128-byte swizzled box)
 constexpr int THREADS = 192;     // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int MAX_STAGES = 8;
 constexpr int A_BYTES = TILE * BK * 2;   // 16 KB of weights per stage
+constexpr int MAX_SPLITS = 8;            // K slices = CTAs of a (portable) cluster
 
 struct GemvParams {
   int N, K, batch, nb;             // nb = batch rounded up to 16 (MMA N)
@@ -34,8 +39,6 @@ struct GemvParams {
   const bf16* bias;
   const bf16* R;                   // residual [batch][N] (EPI_BIAS_RESID)
   bf16* out;                       // [batch][N]
-  float* part;                     // [tiles][splits][batch][TILE] fp32 partials
-  int* counters;                   // [tiles], zero on entry, left zero
   unsigned* status;
 };
 
@@ -47,7 +50,8 @@ __device__ __forceinline__ float gemv_epi(const GemvParams& p, int f, int b, flo
   return v;
 }
 
-// One CTA: output features [128*blockIdx.x, +128) over the K slice blockIdx.y.
+// One CTA: output features [128*blockIdx.x, +128) over K slice blockIdx.y; the
+// p.splits slices of a tile are one cluster.
 template <int EPI>
 __global__ void __launch_bounds__(THREADS) gemv_tc_kernel(const __grid_constant__ CUtensorMap tw,
                                                           const __grid_constant__ CUtensorMap tx,
@@ -65,7 +69,8 @@ __global__ void __launch_bounds__(THREADS) gemv_tc_kernel(const __grid_constant_
   const uint32_t DONE = bar0 + 8u * (2 * MAX_STAGES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * MAX_STAGES + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  // partial tile [batch][128] fp32, over the stage buffers once the MMAs are done
+  float* red = reinterpret_cast<float*>(base);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x, split = blockIdx.y;
   const int kb0 = split * p.kb_per_split;
@@ -78,21 +83,27 @@ __global__ void __launch_bounds__(THREADS) gemv_tc_kernel(const __grid_constant_
     }
     mbar_init(DONE, 1);
     *abort_flag = 0;
-    *last_flag = 0;
     fence_barrier_init();
     fence_proxy_async_shared();
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), ncols);
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
       tma_prefetch_desc(&tw);
       tma_prefetch_desc(&tx);
-      for (int kb = 0; kb < p.kb_per_split; ++kb) {
+      // The weights are never written by an earlier kernel: fill the first
+      // stages with them before waiting for the activations.
+      const int pre = p.kb_per_split < p.stages ? p.kb_per_split : p.stages;
+      for (int kb = 0; kb < pre; ++kb) {
+        mbar_arrive_expect_tx(FULL(kb), stage_bytes);
+        tma_load_2d(sbase + kb * stage_bytes, &tw, FULL(kb), (kb0 + kb) * BK, tile * TILE);
+      }
+      griddep_wait();
+      for (int kb = 0; kb < pre; ++kb)
+        tma_load_2d(sbase + kb * stage_bytes + A_BYTES, &tx, FULL(kb), (kb0 + kb) * BK, 0);
+      for (int kb = pre; kb < p.kb_per_split; ++kb) {
         const int s = kb % p.stages;
         const uint32_t ph = (kb / p.stages) & 1;
         if (!mbar_wait_bounded(EMPTY(s), ph ^ 1u, p.status, abort_flag)) break;
@@ -101,84 +112,95 @@ __global__ void __launch_bounds__(THREADS) gemv_tc_kernel(const __grid_constant_
         tma_load_2d(sa, &tw, FULL(s), (kb0 + kb) * BK, tile * TILE);
         tma_load_2d(sa + A_BYTES, &tx, FULL(s), (kb0 + kb) * BK, 0);
       }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(TILE, p.nb, false, false);
-      bool ok = true;
-      for (int kb = 0; kb < p.kb_per_split && ok; ++kb) {
-        const int s = kb % p.stages;
-        const uint32_t ph = (kb / p.stages) & 1;
-        if (!mbar_wait_bounded(FULL(s), ph, p.status, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t sa = sbase + s * stage_bytes;
-        const uint64_t da = desc_kbase(sa), db = desc_kbase(sa + A_BYTES);
-#pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          tc_mma_bf16(tmem, desc_add(da, kk * 32), desc_add(db, kk * 32), idesc,
-                      (kb > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(EMPTY(s));
-      }
-      if (ok) tc_commit(DONE);
+    } else {
+      griddep_wait();
     }
     __syncwarp();
   } else {
-    // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 = output features
-    const int q4 = warp & 3;
-    const int fl = q4 * 32 + lane;
-    const int f = tile * TILE + fl;
-    const bool ok = mbar_wait_bounded(DONE, 0, p.status, abort_flag);
+    griddep_wait();
+    if (warp == 1) {
+      tmem_alloc(smem_u32(tmem_slot), ncols);
+      tc_fence_before();
+    }
+    named_bar_sync(2, THREADS - 32);   // warps 1..5: the TMEM address is in place
     tc_fence_after();
-    float* mypart = p.part + ((size_t)tile * p.splits + split) * p.batch * TILE;
-    if (ok) {
-      for (int c0 = 0; c0 < p.nb; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + c0, r);
-        tmem_ld_wait();
+    const uint32_t tmem = *tmem_slot;
+    if (warp == 1) {
+      if (lane == 0) {
+        const uint32_t idesc = idesc_bf16_f32(TILE, p.nb, false, false);
+        bool ok = true;
+        for (int kb = 0; kb < p.kb_per_split && ok; ++kb) {
+          const int s = kb % p.stages;
+          const uint32_t ph = (kb / p.stages) & 1;
+          if (!mbar_wait_bounded(FULL(s), ph, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = sbase + s * stage_bytes;
+          const uint64_t da = desc_kbase(sa), db = desc_kbase(sa + A_BYTES);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int b = c0 + i;
-          if (b < p.batch) {
-            const float acc = __uint_as_float(r[i]);
-            if (p.splits == 1) {
-              if (f < p.N) p.out[(size_t)b * p.N + f] = __float2bfloat16_rn(gemv_epi<EPI>(p, f, b, acc));
-            } else {
-              mypart[(size_t)b * TILE + fl] = acc;
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc_mma_bf16(tmem, desc_add(da, kk * 32), desc_add(db, kk * 32), idesc,
+                        (kb > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(EMPTY(s));
+        }
+        if (ok) tc_commit(DONE);
+      }
+      __syncwarp();
+    } else {
+      // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 = output features
+      const int q4 = warp & 3;
+      const int fl = q4 * 32 + lane;
+      const int f = tile * TILE + fl;
+      if (mbar_wait_bounded(DONE, 0, p.status, abort_flag)) {
+        tc_fence_after();
+        for (int c0 = 0; c0 < p.nb; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + c0, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int b = c0 + i;
+            if (b < p.batch) {
+              const float acc = __uint_as_float(r[i]);
+              if (p.splits == 1) {
+                if (f < p.N)
+                  p.out[(size_t)b * p.N + f] = __float2bfloat16_rn(gemv_epi<EPI>(p, f, b, acc));
+              } else {
+                red[b * TILE + fl] = acc;
+              }
             }
           }
         }
       }
     }
-    if (p.splits > 1) {
-      // the last K slice of this tile to finish adds all slices in order
-      __threadfence();
-      named_bar_sync(1, 128);
-      if (warp == 2 && lane == 0) {
-        const int old = ok ? atomicAdd(&p.counters[tile], 1) : -1;
-        *last_flag = (old == p.splits - 1) ? 1 : 0;
-      }
-      named_bar_sync(1, 128);
-      if (*last_flag) {
-        __threadfence();
-        if (f < p.N) {
-          const float* tp = p.part + (size_t)tile * p.splits * p.batch * TILE;
-          for (int b = 0; b < p.batch; ++b) {
-            float acc = __ldcg(tp + (size_t)b * TILE + fl);
-            for (int s = 1; s < p.splits; ++s)
-              acc += __ldcg(tp + ((size_t)s * p.batch + b) * TILE + fl);
-            p.out[(size_t)b * p.N + f] = __float2bfloat16_rn(gemv_epi<EPI>(p, f, b, acc));
-          }
-        }
-        if (warp == 2 && lane == 0) p.counters[tile] = 0;
-      }
-    }
   }
   tc_fence_before();
   __syncthreads();
+  if (p.splits > 1) {
+    // the cluster's slices, added in slice order; CTA `rank` finishes outputs
+    // [rank*per, (rank+1)*per) of the tile's batch x 128
+    cluster_sync();
+    const int rank = (int)cluster_cta_rank();
+    const int total = p.batch * TILE;
+    const int per = (total + p.splits - 1) / p.splits;
+    const int o1 = min(total, (rank + 1) * per);
+    const uint32_t red_u32 = smem_u32(red);
+    for (int o = rank * per + (int)threadIdx.x; o < o1; o += THREADS) {
+      float v[MAX_SPLITS];
+#pragma unroll
+      for (int s = 0; s < MAX_SPLITS; ++s)
+        if (s < p.splits) v[s] = ld_dsmem_f32(cluster_map(red_u32 + 4u * o, s));
+      float acc = v[0];
+#pragma unroll
+      for (int s = 1; s < MAX_SPLITS; ++s)
+        if (s < p.splits) acc += v[s];
+      const int b = o / TILE, f = tile * TILE + o % TILE;
+      if (f < p.N) p.out[(size_t)b * p.N + f] = __float2bfloat16_rn(gemv_epi<EPI>(p, f, b, acc));
+    }
+    cluster_sync();   // no CTA leaves while another may still read its partial
+  }
   if (warp == 1) {
     if (*abort_flag) {
       const long long t0 = clock64();
@@ -186,7 +208,7 @@ __global__ void __launch_bounds__(THREADS) gemv_tc_kernel(const __grid_constant_
       }
     }
     tc_fence_after();
-    tmem_dealloc(tmem, ncols);
+    tmem_dealloc(*tmem_slot, ncols);
   }
 }
 
@@ -232,6 +254,8 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_decode_kernel(const AttnDecP
   const int sp = blockIdx.x, hd = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int d = p.d, h = p.heads * d;
+  griddep_wait();
+  if (tid == 0) griddep_launch_dependents();
   const int L = p.cache_len[b];
   if (L < 0 || L >= p.max_seq) {
     if (tid == 0 && sp == 0 && hd == 0) atomicOr(p.status, kDevErrBadArg);
@@ -376,6 +400,7 @@ __global__ void kv_write_kernel(const T* __restrict__ qkv, T* __restrict__ kc, T
 }
 
 __global__ void kv_advance_kernel(int* cache_len, int batch, int max_seq) {
+  griddep_wait();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b < batch && cache_len[b] >= 0 && cache_len[b] < max_seq) cache_len[b] += 1;
 }
@@ -413,12 +438,13 @@ int round16(int v) { return (v + 15) / 16 * 16; }
 using namespace dec;
 
 // Split of K for a decode GEMM: the largest divisor of the 64-wide K block
-// count that keeps the grid near two CTAs per SM.
+// count, at most one cluster (8), that keeps the grid near two CTAs per SM.
 static int gemv_splits(int N, int K, int num_sms) {
   if (num_sms > kDecodeSmCap) num_sms = kDecodeSmCap;
   const int tiles = (N + TILE - 1) / TILE;
   const int nkb = K / BK;
   int target = (2 * num_sms + tiles - 1) / tiles;
+  if (target > MAX_SPLITS) target = MAX_SPLITS;
   if (target > nkb) target = nkb;
   int s = 1;
   for (int c = 1; c <= target; ++c)
@@ -426,19 +452,13 @@ static int gemv_splits(int N, int K, int num_sms) {
   return s;
 }
 
-size_t gemv_tc_partial_floats(int N, int K, int batch, int num_sms) {
-  const int tiles = (N + TILE - 1) / TILE;
-  return (size_t)tiles * gemv_splits(N, K, num_sms) * batch * TILE;
-}
-size_t gemv_tc_counters(int N) { return (size_t)(N + TILE - 1) / TILE; }
-
 bool gemv_tc_supported(int N, int K, int batch) {
   return batch >= 1 && batch <= kDecodeMaxBatch && K % BK == 0 && K > 0 && N > 0;
 }
 
 cudaError_t gemv_tc(int epi, int N, int K, int batch, const void* W, const void* X,
-                    const void* bias, const void* R, void* out, float* part, int* counters,
-                    unsigned* status, const LaunchCtx& c) {
+                    const void* bias, const void* R, void* out, unsigned* status,
+                    const LaunchCtx& c) {
   if (batch == 0) return cudaSuccess;
   if (!gemv_tc_supported(N, K, batch)) return cudaErrorInvalidValue;
   GemvParams p;
@@ -454,34 +474,31 @@ cudaError_t gemv_tc(int epi, int N, int K, int batch, const void* W, const void*
   p.bias = static_cast<const bf16*>(bias);
   p.R = static_cast<const bf16*>(R);
   p.out = static_cast<bf16*>(out);
-  p.part = part;
-  p.counters = counters;
   p.status = status;
   CUtensorMap tw, tx;
   if (!make_map(&tw, W, (uint64_t)K, (uint64_t)N, TILE) ||
       !make_map(&tx, X, (uint64_t)K, (uint64_t)batch, (uint32_t)p.nb))
     return cudaErrorInvalidValue;
-  const size_t smem = (size_t)p.stages * stage_bytes + 1024 + 256;
+  // the partial tile [batch][128] fp32 reuses the stage buffers
+  size_t smem = (size_t)p.stages * stage_bytes;
+  if (smem < (size_t)batch * TILE * 4) return cudaErrorInvalidValue;
+  smem += 1024 + 256;
   dim3 grid((N + TILE - 1) / TILE, p.splits);
   cudaError_t e;
-#define GEMV_CASE(E)                                                                         \
-  case E:                                                                                    \
-    if ((e = cudaFuncSetAttribute(gemv_tc_kernel<E>,                                         \
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != \
-        cudaSuccess)                                                                         \
-      return e;                                                                              \
-    c.before(KK_GEMV_TC, (double)N * K * 2 + (double)batch * (K + N) * 2);                   \
-    gemv_tc_kernel<E><<<grid, THREADS, smem, c.stream>>>(tw, tx, p);                         \
-    break;
+  void (*fn)(const CUtensorMap, const CUtensorMap, const GemvParams) = nullptr;
   switch (epi) {
-    GEMV_CASE(EPI_BIAS)
-    GEMV_CASE(EPI_BIAS_RESID)
-    GEMV_CASE(EPI_BIAS_GELU)
-    default:
-      return cudaErrorInvalidValue;
+    case EPI_BIAS: fn = gemv_tc_kernel<EPI_BIAS>; break;
+    case EPI_BIAS_RESID: fn = gemv_tc_kernel<EPI_BIAS_RESID>; break;
+    case EPI_BIAS_GELU: fn = gemv_tc_kernel<EPI_BIAS_GELU>; break;
+    default: return cudaErrorInvalidValue;
   }
-#undef GEMV_CASE
+  if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+      cudaSuccess)
+    return e;
+  c.before(KK_GEMV_TC, (double)N * K * 2 + (double)batch * (K + N) * 2);
+  e = launch_ex(c, fn, grid, dim3(THREADS), smem, p.splits, tw, tx, p);
   c.after();
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -509,8 +526,9 @@ static cudaError_t attn_decode_t(const void* qkv, void* kcache, void* vcache, co
   p.status = status;
   dim3 grid(p.splits_max, heads, batch);
   c.before(KK_ATTN_DECODE, kv_bytes);
-  attn_decode_kernel<T><<<grid, ATT_THREADS, 0, c.stream>>>(p);
+  cudaError_t e = launch_ex(c, attn_decode_kernel<T>, grid, dim3(ATT_THREADS), 0, 1, p);
   c.after();
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -546,8 +564,10 @@ cudaError_t kv_write(int dtype, const void* qkv, void* kcache, void* vcache, int
 cudaError_t kv_advance(int* cache_len, int batch, int max_seq, const LaunchCtx& c) {
   if (batch == 0) return cudaSuccess;
   c.before(KK_KV_WRITE, 8.0 * batch);
-  kv_advance_kernel<<<(batch + 127) / 128, 128, 0, c.stream>>>(cache_len, batch, max_seq);
+  cudaError_t e = launch_ex(c, kv_advance_kernel, dim3((batch + 127) / 128), dim3(128), 0, 1,
+                            cache_len, batch, max_seq);
   c.after();
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -75,6 +75,9 @@ struct LaunchCtx {
   int num_sms;
   int* launches;          // incremented per kernel enqueued
   Profiler* prof;         // may be null
+  bool pdl = false;       // launch with programmatic stream serialization (the
+                          // kernels then overlap their start with the previous
+                          // kernel's tail; each calls griddep_wait first)
 
   void before(int kind, double work) const {
     if (prof && prof->events && prof->count < prof->capacity) {
@@ -91,6 +94,36 @@ struct LaunchCtx {
     }
   }
 };
+
+// Launches `kernel` on c.stream with, when c.pdl, programmatic stream
+// serialization and, when cluster_y > 1, a (1, cluster_y, 1) thread-block
+// cluster.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(const LaunchCtx& c, void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                      size_t smem, int cluster_y, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (c.pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_y > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 1;
+    attr[n].val.clusterDim.y = cluster_y;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
 
 // CUDA-core GEMM, exact fp32 math; dtype of operands kF32 or kBF16.
 cudaError_t gemm_simt(int dtype, const GemmArgs& a, const LaunchCtx& c);
@@ -159,16 +192,13 @@ constexpr int kDecodeMaxBatch = 128;
 constexpr int kDecodeSmCap = 160;
 
 // Decode GEMM out[b][n] = epi(sum_k W[n][k] X[b][k]) for a few tokens b
-// (tcgen05, weights as the M operand, K split across CTAs, slices summed in
-// order by the last CTA of each output tile).  epi: EPI_BIAS, EPI_BIAS_RESID
-// (+ R[b][n]) or EPI_BIAS_GELU.  part / counters: gemv_tc_partial_floats /
-// gemv_tc_counters; counters zero on entry (left zero).
+// (tcgen05, weights as the M operand, K split across the CTAs of a cluster,
+// slices summed in order through distributed shared memory).  epi: EPI_BIAS,
+// EPI_BIAS_RESID (+ R[b][n]) or EPI_BIAS_GELU.
 bool gemv_tc_supported(int N, int K, int batch);
-size_t gemv_tc_partial_floats(int N, int K, int batch, int num_sms);
-size_t gemv_tc_counters(int N);
 cudaError_t gemv_tc(int epi, int N, int K, int batch, const void* W, const void* X,
-                    const void* bias, const void* R, void* out, float* part, int* counters,
-                    unsigned* status, const LaunchCtx& c);
+                    const void* bias, const void* R, void* out, unsigned* status,
+                    const LaunchCtx& c);
 // Decode attention: appends each sequence's new K, V (from qkv [batch][3h]) at
 // position cache_len[b] of the [batch][heads][max_seq][d] caches and attends to
 // keys 0..cache_len[b]; ctx [batch][h].  part: batch*heads*attn_decode_splits

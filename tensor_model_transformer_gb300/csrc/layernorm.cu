@@ -48,6 +48,8 @@ __global__ void __launch_bounds__(kLnThreadsMax)
                   int n, int h, float eps, int rows_per_block) {
   constexpr int E = Vec<T>::N;
   __shared__ float red[R * 32];
+  griddep_wait();   // no-op unless launched as a programmatic dependent
+  if (threadIdx.x == 0) griddep_launch_dependents();
   const int nvec = h / E;
   const int r_begin = blockIdx.x * rows_per_block;
   const int r_end = min(n, r_begin + rows_per_block);
@@ -330,9 +332,10 @@ cudaError_t ln_fwd_t(const void* x, const void* g, const void* b, void* u, float
   c.before(KK_LN_FWD, (double)n * h * (2.0 * sizeof(T)) + 8.0 * n);
 #define LN_FWD_CASE(VV, RR)                                                                  \
   case VV:                                                                                   \
-    ln_fwd_kernel<T, VV, RR><<<grid, threads, 0, c.stream>>>(                                \
-        (const T*)x, (const T*)g, (const T*)b, (T*)u, mean, rstd, n, h, eps, rows);          \
+    e = launch_ex(c, ln_fwd_kernel<T, VV, RR>, dim3(grid), dim3(threads), 0, 1, (const T*)x,     \
+                  (const T*)g, (const T*)b, (T*)u, mean, rstd, n, h, eps, rows);             \
     break;
+  cudaError_t e = cudaSuccess;
   switch (vpt) {
     LN_FWD_CASE(1, 1)
     LN_FWD_CASE(2, 2)
@@ -343,6 +346,7 @@ cudaError_t ln_fwd_t(const void* x, const void* g, const void* b, void* u, float
   }
 #undef LN_FWD_CASE
   c.after();
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -363,7 +363,7 @@ size_t kv_cache_bytes(const Dims& D, int32_t max_seq) {
 }
 
 struct DecWs {
-  size_t c_qkv, c_o, c_fc1, c_fc2, c_att, mean, rstd, u, qkv, ctx, x1, a, z, part, apart, total;
+  size_t c_att, mean, rstd, u, qkv, ctx, x1, a, z, apart, total;
 };
 
 DecWs decode_ws(const Dims& D, int32_t max_seq) {
@@ -375,10 +375,6 @@ DecWs decode_ws(const Dims& D, int32_t max_seq) {
     return at;
   };
   const int h = (int)D.h, f = (int)D.f, b = (int)D.batch;
-  W.c_qkv = take(gemv_tc_counters(3 * h) * 4);
-  W.c_o = take(gemv_tc_counters(h) * 4);
-  W.c_fc1 = take(gemv_tc_counters(f) * 4);
-  W.c_fc2 = take(gemv_tc_counters(h) * 4);
   W.c_att = take((size_t)b * D.heads * 4);
   W.mean = take((size_t)b * 4);
   W.rstd = take((size_t)b * 4);
@@ -388,15 +384,6 @@ DecWs decode_ws(const Dims& D, int32_t max_seq) {
   W.x1 = take((size_t)b * h * D.esz);
   W.a = take((size_t)b * f * D.esz);
   W.z = take(D.dtype == MTL_BF16 ? 0 : (size_t)b * f * D.esz);
-  size_t pf = 0;
-  if (D.dtype == MTL_BF16) {
-    const size_t c[4] = {gemv_tc_partial_floats(3 * h, h, b, kDecodeSmCap),
-                         gemv_tc_partial_floats(h, h, b, kDecodeSmCap),
-                         gemv_tc_partial_floats(f, h, b, kDecodeSmCap),
-                         gemv_tc_partial_floats(h, f, b, kDecodeSmCap)};
-    for (size_t v : c) pf = v > pf ? v : pf;
-  }
-  W.part = take(pf * 4);
   W.apart = take((size_t)b * D.heads * attn_decode_splits(max_seq) * (D.d + 2) * 4);
   W.total = off;
   return W;
@@ -818,8 +805,9 @@ mtl_status mtl_layer_decode(const mtl_layer_desc* desc, const mtl_weights* w, co
   if (nsm <= 0) return cuda_fail(cudaGetLastError(), "device query");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   LaunchCtx c{s, nsm, &g_launches, &g_prof};
+  c.pdl = true;   // chain the step's kernels with programmatic dependent launch
   unsigned* status = static_cast<unsigned*>(workspace);
-  // status word and every split-K / split-KV counter
+  // status word and the split-KV counters
   MTL_TRY(cudaMemsetAsync(status, 0, W.mean, s), "status reset");
   if (D.batch == 0) return MTL_OK;
   const int b = (int)D.batch, h = (int)D.h, f = (int)D.f;
@@ -829,15 +817,12 @@ mtl_status mtl_layer_decode(const mtl_layer_desc* desc, const mtl_weights* w, co
   void* ctx = at<char>(workspace, W.ctx);
   void* x1 = at<char>(workspace, W.x1);
   void* a = at<char>(workspace, W.a);
-  float* part = at<float>(workspace, W.part);
   const size_t half = kv_cache_bytes(D, max_seq) / 2;
   // gemm on the layer's path: the split-K tcgen05 decode GEMM for bf16, the
   // exact fp32 CUDA-core GEMM for fp32
   auto dgemm = [&](int epi, int N, int K, const void* Wt, const void* X, const void* bias,
-                   const void* R, void* out, size_t counters) -> cudaError_t {
-    if (bf)
-      return gemv_tc(epi, N, K, b, Wt, X, bias, R, out, part, at<int>(workspace, counters),
-                     status, c);
+                   const void* R, void* out) -> cudaError_t {
+    if (bf) return gemv_tc(epi, N, K, b, Wt, X, bias, R, out, status, c);
     GemmArgs g = gemm_args(b, N, K, 1, X, K, true, Wt, K, true, epi, out, N, false, status);
     g.bias = bias;
     g.R = R;
@@ -851,7 +836,7 @@ mtl_status mtl_layer_decode(const mtl_layer_desc* desc, const mtl_weights* w, co
                  at<float>(workspace, W.rstd), b, h, desc->ln_eps, c),
           "ln1");
   // D2 QKV (column-parallel)
-  MTL_TRY(dgemm(EPI_BIAS, 3 * h, h, w->w_qkv, u, w->b_qkv, nullptr, qkv, W.c_qkv), "qkv");
+  MTL_TRY(dgemm(EPI_BIAS, 3 * h, h, w->w_qkv, u, w->b_qkv, nullptr, qkv), "qkv");
   // D3 attention over the cache; appends K, V
   double kvb = 0;   // algorithmic bytes are not known on the host (lengths live on the device)
   MTL_TRY(attn_decode(D.dtype, qkv, kv_cache, at<char>(kv_cache, half), cache_len, ctx,
@@ -859,15 +844,15 @@ mtl_status mtl_layer_decode(const mtl_layer_desc* desc, const mtl_weights* w, co
                       (int)D.heads, (int)D.d, max_seq, kvb, status, c),
           "attention");
   // D4 out-proj (row-parallel, ordered K-slice sum) + b_o + x
-  MTL_TRY(dgemm(EPI_BIAS_RESID, h, h, w->w_o, ctx, w->b_o, x_tok, x1, W.c_o), "out-proj");
+  MTL_TRY(dgemm(EPI_BIAS_RESID, h, h, w->w_o, ctx, w->b_o, x_tok, x1), "out-proj");
   // D5 LN2
   MTL_TRY(ln_fwd(D.dtype, x1, w->ln2_g, w->ln2_b, u, at<float>(workspace, W.mean),
                  at<float>(workspace, W.rstd), b, h, desc->ln_eps, c),
           "ln2");
   // D6 fc1 + GeLU
-  MTL_TRY(dgemm(EPI_BIAS_GELU, f, h, w->w_fc1, u, w->b_fc1, nullptr, a, W.c_fc1), "fc1");
+  MTL_TRY(dgemm(EPI_BIAS_GELU, f, h, w->w_fc1, u, w->b_fc1, nullptr, a), "fc1");
   // D7 fc2 (row-parallel) + b_fc2 + x1
-  MTL_TRY(dgemm(EPI_BIAS_RESID, h, f, w->w_fc2, a, w->b_fc2, x1, y_tok, W.c_fc2), "fc2");
+  MTL_TRY(dgemm(EPI_BIAS_RESID, h, f, w->w_fc2, a, w->b_fc2, x1, y_tok), "fc2");
   // D8 cache lengths + 1
   MTL_TRY(kv_advance(cache_len, b, max_seq, c), "advance");
   return MTL_OK;
