@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(THREADS) gemv_tc_kernel(const __grid_constant_
 }
 
 // ---------------------------------------------------------------- decode attention
-constexpr int ATT_CHUNK = 256;   // keys per CTA
+constexpr int ATT_CHUNK = 128;   // keys per CTA
 constexpr int ATT_THREADS = 128;
 
 template <typename T>
@@ -231,70 +231,114 @@ struct AttnDecParams {
 };
 
 template <typename T>
-__device__ __forceinline__ void load_vec(const T* p, float (&v)[16 / sizeof(T)]) {
+__device__ __forceinline__ void unpack16(const uint4& u, float (&v)[16 / sizeof(T)]) {
   Vec<T> x;
-  x.load(p);
+  x.raw = *reinterpret_cast<const decltype(x.raw)*>(&u);
 #pragma unroll
   for (int i = 0; i < Vec<T>::N; ++i) v[i] = x.get(i);
 }
 
-// One CTA per (key chunk, head, batch row): scores of the new token's query
-// against the chunk's cached keys (the new key itself for position L), then
-// the chunk's softmax-weighted V; chunks of a (batch, head) combine in chunk
-// order in the last CTA to finish.  The chunk holding position L writes the
-// new K and V into the cache.
+// One CTA per (chunk of 128 keys, head, batch row).  The chunk's cached K and
+// V rows are contiguous in the head-major cache, so one thread starts two bulk
+// copies into shared memory before anything else (the cache rows below the
+// current length were written by earlier steps, so this runs ahead of the
+// programmatic wait on the QKV GEMM).  Scores: four lanes per key, each
+// summing a quarter of the 16-byte chunks of the row (chunk order chosen so
+// the 8 lanes of a shared-memory phase hit 8 different bank groups); the new
+// token's own key and value come from the QKV output.  P V: thread = (16-byte
+// channel chunk, key group).  Chunks of a (batch, head) combine in chunk order
+// in the last CTA to finish; the chunk holding position L writes the new K, V.
 template <typename T>
 __global__ void __launch_bounds__(ATT_THREADS) attn_decode_kernel(const AttnDecParams<T> p) {
   constexpr int VEC = 16 / sizeof(T);
-  __shared__ float s_q[128], s_kn[128], s_vn[128];
+  extern __shared__ __align__(128) uint8_t att_smem[];   // K [CHUNK][d], V [CHUNK][d]
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ float s_q[128];
   __shared__ float s_p[ATT_CHUNK];
   __shared__ float s_red[ATT_THREADS / 32];
-  __shared__ float s_o[ATT_THREADS * VEC];
+  __shared__ float s_o[ATT_THREADS * (VEC + 1)];   // padded: conflict-free stores
   __shared__ int s_last;
+  __shared__ int s_abort;
   const int sp = blockIdx.x, hd = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int d = p.d, h = p.heads * d;
-  griddep_wait();
-  if (tid == 0) griddep_launch_dependents();
+  const int row_bytes = d * (int)sizeof(T);
+  const int nch = row_bytes / 16;                 // 16-byte chunks per row
+  T* sK = reinterpret_cast<T*>(att_smem);
+  T* sV = reinterpret_cast<T*>(att_smem + ATT_CHUNK * row_bytes);
+  // cache lengths are advanced only at the end of a step
   const int L = p.cache_len[b];
   if (L < 0 || L >= p.max_seq) {
+    griddep_wait();
     if (tid == 0 && sp == 0 && hd == 0) atomicOr(p.status, kDevErrBadArg);
     return;
   }
   const int nk = L + 1;
   const int nsplit = (nk + ATT_CHUNK - 1) / ATT_CHUNK;
-  if (sp >= nsplit) return;
-  const int j0 = sp * ATT_CHUNK, j1 = min(nk, j0 + ATT_CHUNK);
-  const T* qrow = p.qkv + (size_t)b * 3 * h + (size_t)hd * 3 * d;
-  const size_t head_off = ((size_t)b * p.heads + hd) * p.max_seq;
-  for (int c = tid; c < d; c += ATT_THREADS) {
-    s_q[c] = to_f<T>(qrow[c]) * p.scale_log2;
-    s_kn[c] = to_f<T>(qrow[d + c]);
-    s_vn[c] = to_f<T>(qrow[2 * d + c]);
+  if (sp >= nsplit) {
+    griddep_wait();
+    return;
   }
-  if (sp == nsplit - 1)
-    for (int c = tid; c < d; c += ATT_THREADS) {
-      p.kc[(head_off + L) * d + c] = qrow[d + c];
-      p.vc[(head_off + L) * d + c] = qrow[2 * d + c];
-    }
+  const int j0 = sp * ATT_CHUNK, j1 = min(nk, j0 + ATT_CHUNK);
+  const int ncached = min(j1, L) - j0;            // rows already in the cache
+  const size_t head_off = ((size_t)b * p.heads + hd) * p.max_seq;
+  if (tid == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    s_abort = 0;
+    fence_barrier_init();
+  }
   __syncthreads();
-  // scores (log2 domain), one key per thread at a time
+  if (tid == 0 && ncached > 0) {
+    const uint32_t bytes = (uint32_t)ncached * row_bytes;
+    mbar_arrive_expect_tx(smem_u32(&bar), 2 * bytes);
+    bulk_load(smem_u32(sK), p.kc + (head_off + j0) * d, bytes, smem_u32(&bar));
+    bulk_load(smem_u32(sV), p.vc + (head_off + j0) * d, bytes, smem_u32(&bar));
+  }
+  griddep_wait();
+  if (tid == 0) griddep_launch_dependents();
+  const T* qrow = p.qkv + (size_t)b * 3 * h + (size_t)hd * 3 * d;
+  for (int c = tid; c < d; c += ATT_THREADS) s_q[c] = to_f<T>(qrow[c]) * p.scale_log2;
+  if (sp == nsplit - 1) {
+    // position L: the new key and value, into the cache and into this chunk
+    for (int c = tid; c < d; c += ATT_THREADS) {
+      const T kv = qrow[d + c], vv = qrow[2 * d + c];
+      p.kc[(head_off + L) * d + c] = kv;
+      p.vc[(head_off + L) * d + c] = vv;
+      sK[(L - j0) * d + c] = kv;
+      sV[(L - j0) * d + c] = vv;
+    }
+  }
+  if (ncached > 0 && !mbar_wait_bounded(smem_u32(&bar), 0, p.status, &s_abort)) {
+    // bulk copy never completed: the status word has the timeout; finish
+    // without trusting the rows
+  }
+  __syncthreads();
+  // scores (log2 domain): lanes 4k..4k+3 of a warp take key 8*pass + k of the warp
+  const int nrows = j1 - j0;
+  const int pp = lane & 3, kk = (lane >> 2) & 1;
+  const int sh = (nch % 8 == 0) ? 4 : 0;
   float mx = -INFINITY;
-  for (int j = j0 + tid; j < j1; j += ATT_THREADS) {
+  for (int r0 = warp * 8; r0 < nrows; r0 += 32) {
+    const int r = r0 + (lane >> 2);
     float s = 0.f;
-    if (j == L) {
-      for (int c = 0; c < d; ++c) s = fmaf(s_q[c], s_kn[c], s);
-    } else {
-      const T* kr = p.kc + (head_off + j) * d;
-      for (int c = 0; c < d; c += VEC) {
+    if (r < nrows) {
+      const uint8_t* krow = reinterpret_cast<const uint8_t*>(sK) + (size_t)r * row_bytes;
+      for (int t = pp; t < nch; t += 4) {
+        int c = t + kk * sh;
+        if (c >= nch) c -= nch;
+        const uint4 u = *reinterpret_cast<const uint4*>(krow + c * 16);
         float kv[VEC];
-        load_vec<T>(kr + c, kv);
+        unpack16<T>(u, kv);
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) s = fmaf(s_q[c + i], kv[i], s);
+        for (int i = 0; i < VEC; ++i) s = fmaf(s_q[c * VEC + i], kv[i], s);
       }
     }
-    s_p[j - j0] = s;
-    mx = fmaxf(mx, s);
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    if (r < nrows) {
+      if (pp == 0) s_p[r] = s;
+      mx = fmaxf(mx, s);
+    }
   }
   mx = warp_max(mx);
   if (lane == 0) s_red[warp] = mx;
@@ -303,9 +347,9 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_decode_kernel(const AttnDecP
   for (int w = 1; w < ATT_THREADS / 32; ++w) mx = fmaxf(mx, s_red[w]);
   __syncthreads();
   float l = 0.f;
-  for (int j = j0 + tid; j < j1; j += ATT_THREADS) {
-    const float e = exp2f(s_p[j - j0] - mx);
-    s_p[j - j0] = e;
+  for (int r = tid; r < nrows; r += ATT_THREADS) {
+    const float e = exp2f(s_p[r] - mx);
+    s_p[r] = e;
     l += e;
   }
   l = warp_sum(l);
@@ -313,36 +357,31 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_decode_kernel(const AttnDecP
   __syncthreads();
   l = 0.f;
   for (int w = 0; w < ATT_THREADS / 32; ++w) l += s_red[w];
-  // o = sum_j p_j v_j: thread = (channel group of VEC, key group)
-  const int cg_n = d / VEC, kg_n = ATT_THREADS / cg_n;
-  const int cg = tid % cg_n, kg = tid / cg_n;
+  // o = sum_r p_r v_r: thread = (channel chunk cg, key group kg)
+  const int kg_n = ATT_THREADS / nch;
+  const int cg = tid % nch, kg = tid / nch;
   float acc[VEC];
 #pragma unroll
   for (int i = 0; i < VEC; ++i) acc[i] = 0.f;
   if (kg < kg_n) {
-    for (int j = j0 + kg; j < j1; j += kg_n) {
-      const float pj = s_p[j - j0];
+    const uint8_t* vbase = reinterpret_cast<const uint8_t*>(sV) + cg * 16;
+    for (int r = kg; r < nrows; r += kg_n) {
+      const float pr = s_p[r];
       float vv[VEC];
-      if (j == L) {
+      unpack16<T>(*reinterpret_cast<const uint4*>(vbase + (size_t)r * row_bytes), vv);
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) vv[i] = s_vn[cg * VEC + i];
-      } else {
-        load_vec<T>(p.vc + (head_off + j) * d + cg * VEC, vv);
-      }
-#pragma unroll
-      for (int i = 0; i < VEC; ++i) acc[i] = fmaf(pj, vv[i], acc[i]);
+      for (int i = 0; i < VEC; ++i) acc[i] = fmaf(pr, vv[i], acc[i]);
     }
   }
 #pragma unroll
-  for (int i = 0; i < VEC; ++i) s_o[tid * VEC + i] = acc[i];
+  for (int i = 0; i < VEC; ++i) s_o[tid * (VEC + 1) + i] = acc[i];
   __syncthreads();
-  // channel c = cg*VEC + i: add the key groups in order
   const int bh = b * p.heads + hd;
   float* mypart = p.part + ((size_t)bh * p.splits_max + sp) * (d + 2);
   for (int c = tid; c < d; c += ATT_THREADS) {
     const int g = c / VEC, i = c % VEC;
     float o = 0.f;
-    for (int k = 0; k < kg_n; ++k) o += s_o[(k * cg_n + g) * VEC + i];
+    for (int k = 0; k < kg_n; ++k) o += s_o[(k * nch + g) * (VEC + 1) + i];
     if (nsplit == 1)
       p.ctx[(size_t)b * h + (size_t)hd * d + c] = from_f<T>(o / l);
     else
@@ -359,16 +398,16 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_decode_kernel(const AttnDecP
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  const float* pp = p.part + (size_t)bh * p.splits_max * (d + 2);
+  const float* pp_ = p.part + (size_t)bh * p.splits_max * (d + 2);
   float M = -INFINITY;
-  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, __ldcg(pp + (size_t)s * (d + 2) + d));
+  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, __ldcg(pp_ + (size_t)s * (d + 2) + d));
   float Lsum = 0.f;
   for (int s = 0; s < nsplit; ++s)
-    Lsum += __ldcg(pp + (size_t)s * (d + 2) + d + 1) * exp2f(__ldcg(pp + (size_t)s * (d + 2) + d) - M);
+    Lsum += __ldcg(pp_ + (size_t)s * (d + 2) + d + 1) * exp2f(__ldcg(pp_ + (size_t)s * (d + 2) + d) - M);
   for (int c = tid; c < d; c += ATT_THREADS) {
     float o = 0.f;
     for (int s = 0; s < nsplit; ++s)
-      o += __ldcg(pp + (size_t)s * (d + 2) + c) * exp2f(__ldcg(pp + (size_t)s * (d + 2) + d) - M);
+      o += __ldcg(pp_ + (size_t)s * (d + 2) + c) * exp2f(__ldcg(pp_ + (size_t)s * (d + 2) + d) - M);
     p.ctx[(size_t)b * h + (size_t)hd * d + c] = from_f<T>(o / Lsum);
   }
   if (tid == 0) p.counters[bh] = 0;
@@ -525,8 +564,12 @@ static cudaError_t attn_decode_t(const void* qkv, void* kcache, void* vcache, co
   p.counters = counters;
   p.status = status;
   dim3 grid(p.splits_max, heads, batch);
+  const size_t smem = 2 * (size_t)ATT_CHUNK * d * sizeof(T);
+  cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<T>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   c.before(KK_ATTN_DECODE, kv_bytes);
-  cudaError_t e = launch_ex(c, attn_decode_kernel<T>, grid, dim3(ATT_THREADS), 0, 1, p);
+  e = launch_ex(c, attn_decode_kernel<T>, grid, dim3(ATT_THREADS), smem, 1, p);
   c.after();
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
