@@ -4,7 +4,7 @@ TEST INFRASTRUCTURE ONLY: imported by the tests, by ``__graft_entry__.smoke()``
 and by the CPU-baseline leg of ``bench.py``, never by the library.  See
 ``oracle/layer.py`` for what it computes and which passages it follows.
 """
-from . import decode, philox
+from . import decode, fp8, philox
 from .layer import (LN_EPS, ReductionCounter, attention_head_bwd, attention_head_fwd,
                     causal_mask, f_allreduce, g_allreduce, gelu, gelu_grad, layer_bwd,
                     layer_bwd_partitioned, layer_flops, layer_fwd, layer_fwd_partitioned,

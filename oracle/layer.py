@@ -241,7 +241,16 @@ def hidden_keep_scale(n, h, drop, site):
     return philox.hidden_mask(n, h, drop.get("seed", 0), site, p) / (1.0 - p)
 
 
-def layer_fwd(params, x, heads, eps=LN_EPS, dropout=None):
+def _lin(u, w, b, fp8, epi=1, R=None):
+    """u w^T + b (+ R): in fp64, or as an FP8 GEMM of per-tensor E4M3 operands."""
+    if not fp8:
+        out = u @ w.T + b
+        return out if R is None else out + R
+    from . import fp8 as _fp8
+    return _fp8.gemm(u, w, "e4m3", "e4m3", epi=epi, bias=b, R=R)[0]
+
+
+def layer_fwd(params, x, heads, eps=LN_EPS, dropout=None, fp8=False):
     """Pre-LN GPT layer forward.  x [batch, seq, h].  Returns (y, cache).
 
     u1 = LN1(x); qkv = u1 W_qkv^T + b_qkv; ctx = causal multi-head attention;
@@ -252,7 +261,12 @@ def layer_fwd(params, x, heads, eps=LN_EPS, dropout=None):
     Transformer Kernels") after the out-projection and after fc2:
     x1 = x + drop(ctx W_o^T + b_o), y = x1 + drop(a W_fc2^T + b_fc2); masks as
     in oracle/philox.py.
+    fp8=True: the four GEMMs take per-tensor E4M3 operands (activation and
+    weight quantized as in oracle/fp8.py); LayerNorm, attention, GeLU, biases
+    and residuals stay in high precision.
     """
+    if fp8 and dropout:
+        raise ValueError("FP8 forward is defined without dropout")
     p = {k: _f64(v) for k, v in params.items()}
     x = _f64(x)
     batch, seq, h = x.shape
@@ -260,15 +274,15 @@ def layer_fwd(params, x, heads, eps=LN_EPS, dropout=None):
     n = batch * seq
     xf = x.reshape(n, h)
     u1, mu1, rstd1 = layernorm_fwd(xf, p["ln1_g"], p["ln1_b"], eps)
-    qkv = u1 @ p["w_qkv"].T + p["b_qkv"]
+    qkv = _lin(u1, p["w_qkv"], p["b_qkv"], fp8)
     ctx, lse, probs = multihead_fwd(qkv, batch, seq, heads, d, dropout)
     so = hidden_keep_scale(n, h, dropout, philox.SITE_OUT)
     s2 = hidden_keep_scale(n, h, dropout, philox.SITE_FC2)
-    x1 = xf + (ctx @ p["w_o"].T + p["b_o"]) * so
+    x1 = xf + _lin(ctx, p["w_o"], p["b_o"], fp8) * so
     u2, mu2, rstd2 = layernorm_fwd(x1, p["ln2_g"], p["ln2_b"], eps)
-    z = u2 @ p["w_fc1"].T + p["b_fc1"]
+    z = _lin(u2, p["w_fc1"], p["b_fc1"], fp8)
     a = gelu(z)
-    y = x1 + (a @ p["w_fc2"].T + p["b_fc2"]) * s2
+    y = x1 + _lin(a, p["w_fc2"], p["b_fc2"], fp8) * s2
     cache = dict(x=xf, u1=u1, mu1=mu1, rstd1=rstd1, qkv=qkv, ctx=ctx, lse=lse,
                  probs=probs, x1=x1, u2=u2, mu2=mu2, rstd2=rstd2, z=z, a=a,
                  batch=batch, seq=seq, heads=heads, dropout=dropout, so=so, s2=s2)
