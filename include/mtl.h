@@ -87,6 +87,9 @@ typedef enum {
 
 typedef enum { MTL_F32 = 0, MTL_BF16 = 1 } mtl_dtype;
 
+/* FP8 formats (OCP 8-bit floating point). */
+typedef enum { MTL_FP8_E4M3 = 0, MTL_FP8_E5M2 = 1 } mtl_fp8_format;
+
 /* One layer.  h = heads * d with d in {64, 96, 128}; t divides heads and ffn;
  * causal must be 1.  bf16 layers (tensor-core path) additionally need
  * seq % 128 == 0, h % 64 == 0, ffn % 64 == 0, (h/t) % 64 == 0, (3h/t) % 64 == 0
@@ -240,6 +243,30 @@ mtl_status mtl_layer_prefill(const mtl_layer_desc* desc, const mtl_weights* w, c
 mtl_status mtl_layer_decode(const mtl_layer_desc* desc, const mtl_weights* w, const void* x_tok,
                             void* y_tok, void* kv_cache, int32_t max_seq, int32_t* cache_len,
                             void* workspace, size_t ws_bytes, mtl_stream stream);
+
+/* ---- FP8 (the pages list FP8 training, "--fp8-hybrid", without a recipe;
+ * read as E4M3 forward operands, E5M2 gradients, per-tensor current scaling).
+ * mtl_fp8_quantize: x [rows][cols] (src_dtype, row pitch ld elements) ->
+ *   amax = max |x| over the whole matrix, *scale = fmt_max / amax (1 if
+ *   amax = 0; fmt_max 448 for E4M3, 57344 for E5M2), q [rows][cols] bytes
+ *   (row pitch ldq) = fp8(float32(x * scale)), rounded to nearest even and
+ *   saturated to +-fmt_max.  scale: a DEVICE float.  cols and ldq multiples of
+ *   16; workspace >= 256 bytes (status word and the amax word).
+ * mtl_gemm_fp8: as mtl_gemm with K-major FP8 operands A [M][K] (lda) and
+ *   B [N][K] (ldb) of formats fmt_a / fmt_b and their DEVICE scales; the
+ *   partition partials (k_parts, each a multiple of 128 deep) are summed in
+ *   order, multiplied by float32(1 / float32(scale_a * scale_b)), then the
+ *   epilogue applies (same epilogue codes and C / R / Z conventions).  lda and
+ *   ldb multiples of 16.  Runs on the 2-CTA tcgen05 kernel (kind::f8f6f4). */
+mtl_status mtl_fp8_quantize(int32_t src_dtype, const void* x, int64_t rows, int64_t cols,
+                            int64_t ld, int32_t fmt, void* q, int64_t ldq, float* scale,
+                            void* workspace, size_t ws_bytes, mtl_stream stream);
+mtl_status mtl_gemm_fp8(int32_t M, int32_t N, int32_t K, int32_t k_parts, const void* A,
+                        int64_t lda, int32_t fmt_a, const float* scale_a, const void* B,
+                        int64_t ldb, int32_t fmt_b, const float* scale_b, int32_t epi,
+                        const void* bias, const void* R, int64_t ldr, void* Z, int64_t ldz,
+                        void* C, int64_t ldc, int32_t c_f32, void* workspace, size_t ws_bytes,
+                        mtl_stream stream);
 
 /* Bias gradient for callers that cannot allocate device memory:
  *   out[j] = sum_{i < rows} dy[i*ld + j]   (j < cols; fp32, fixed order)

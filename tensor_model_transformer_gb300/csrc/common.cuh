@@ -291,6 +291,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
          | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
 
+// Instruction descriptor of tcgen05.mma kind::f8f6f4 with fp32 accumulate and
+// K-major operands; fa / fb: operand formats, 0 = E4M3, 1 = E5M2.
+__host__ __device__ constexpr uint32_t idesc_f8_f32(int M, int N, int fa, int fb) {
+  return (1u << 4)                       // D format: f32
+         | ((uint32_t)fa << 7)           // A format
+         | ((uint32_t)fb << 10)          // B format
+         | ((uint32_t)(N >> 3) << 17)    // N / 8
+         | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -358,6 +368,16 @@ __device__ __forceinline__ void tc_mma_bf16_pair(uint32_t d_tmem, uint64_t adesc
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// The FP8 form (kind::f8f6f4, K = 32 per instruction), issued by the leader.
+__device__ __forceinline__ void tc_mma_f8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }

@@ -1,0 +1,471 @@
+// The tcgen05 GEMM machinery shared by the bf16 kernels (gemm_tc.cu) and the
+// FP8 instantiations of the pair kernel (gemm_fp8.cu): tile raster, fused
+// epilogue, epilogue warp role, the 2-CTA pair kernel and the tensor-map helper.
+#pragma once
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mtl {
+namespace tcg {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 128 + 32 * EPI_WARPS;
+constexpr int LAUNCH_REGS = 168, PRODUCER_REGS = 56, EPILOGUE_REGS = 224;
+static_assert(PRODUCER_REGS * 128 + EPILOGUE_REGS * 32 * EPI_WARPS == LAUNCH_REGS * THREADS,
+              "register split must add up to the launch total");
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int BAR_BYTES = 256;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+constexpr int GROUP_M = 16;   // tile raster: groups of 16 M-blocks sweep all N-blocks
+
+struct Params {
+  int M, N, K, parts, kb_per_unit, units_per_tile;
+  int a_mn, b_mn;
+  int tiles_m, tiles_n, num_tiles;
+  const bf16* bias;
+  const bf16* R;
+  int64_t ldr;
+  bf16* Z;
+  int64_t ldz;
+  void* C;
+  int64_t ldc;
+  unsigned* status;
+  Dropout drop;   // EPI_BIAS_RESID: C = R + dropout(acc + bias), element e = row * N + col
+  // FP8 operands (pair kernel with F8): formats (0 E4M3, 1 E5M2) and the
+  // device-side per-tensor scales; the accumulator is multiplied by
+  // float32(1 / float32(scale_a * scale_b)) before the epilogue.  Null for bf16.
+  int fmt_a, fmt_b;
+  const float* scale_a;
+  const float* scale_b;
+};
+
+__device__ __forceinline__ void tile_coords(const Params& p, int tile, int& mb, int& nb) {
+  const int per_group = GROUP_M * p.tiles_n;
+  const int g = tile / per_group;
+  const int first_m = g * GROUP_M;
+  const int gsize = min(GROUP_M, p.tiles_m - first_m);
+  const int r = tile - g * per_group;
+  mb = first_m + r % gsize;
+  nb = r / gsize;
+}
+
+// Dropout keep bits of columns [col0, col0+32) of one row (bit e for col0+e),
+// all ones without dropout.
+template <int EPI>
+__device__ __forceinline__ uint32_t chunk_keep(const Params& p, int row, int col0) {
+  if (EPI != EPI_BIAS_RESID || !p.drop.on || row >= p.M) return 0xffffffffu;
+  const unsigned long long e0 = (unsigned long long)row * p.N + col0;
+  if ((p.N & 3) == 0 && col0 + 32 <= p.N) return drop_bits32(e0, p.drop);
+  uint32_t bits = 0;
+#pragma unroll 1
+  for (int e = 0; e < 32 && col0 + e < p.N; ++e) bits |= (drop_keep(e0 + e, p.drop) ? 1u : 0u) << e;
+  return bits;
+}
+
+// Applies the epilogue to 32 consecutive columns [col0, col0+32) of one row;
+// `keep`: dropout bits of EPI_BIAS_RESID (chunk_keep).
+template <int EPI, bool OUT_F32>
+__device__ __forceinline__ void epi_chunk(const Params& p, int row, int col0, float (&v)[32],
+                                          uint32_t keep) {
+  if (row >= p.M || col0 >= p.N) return;
+  const bool full = col0 + 32 <= p.N;
+  if (full) {
+    if (EPI == EPI_BIAS || EPI == EPI_BIAS_RESID || EPI == EPI_BIAS_GELU) {
+      const uint4* bp = reinterpret_cast<const uint4*>(p.bias + col0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 u = __ldg(bp + q);
+        const bf16* hb = reinterpret_cast<const bf16*>(&u);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[q * 8 + e] += __bfloat162float(hb[e]);
+      }
+    }
+    if (EPI == EPI_BIAS_RESID && p.drop.on) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] = ((keep >> e) & 1u) ? v[e] * p.drop.scale : 0.f;
+    }
+    if (EPI == EPI_BIAS_RESID) {
+      const uint4* rp = reinterpret_cast<const uint4*>(p.R + (size_t)row * p.ldr + col0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 u = rp[q];
+        const bf16* hb = reinterpret_cast<const bf16*>(&u);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[q * 8 + e] += __bfloat162float(hb[e]);
+      }
+    }
+    if (EPI == EPI_DGELU) {
+      const uint4* zp = reinterpret_cast<const uint4*>(p.Z + (size_t)row * p.ldz + col0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 u = zp[q];
+        const bf16* hb = reinterpret_cast<const bf16*>(&u);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[q * 8 + e] *= gelu_grad_f(__bfloat162float(hb[e]));
+      }
+    }
+    if (EPI == EPI_BIAS_GELU) {
+      uint4* zp = reinterpret_cast<uint4*>(p.Z + (size_t)row * p.ldz + col0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 u;
+        bf16* hb = reinterpret_cast<bf16*>(&u);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          hb[e] = __float2bfloat16_rn(v[q * 8 + e]);
+          v[q * 8 + e] = gelu_f(v[q * 8 + e]);
+        }
+        zp[q] = u;
+      }
+    }
+    if (OUT_F32) {
+      float4* cp = reinterpret_cast<float4*>(static_cast<float*>(p.C) + (size_t)row * p.ldc + col0);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        cp[q] = make_float4(v[q * 4], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
+    } else {
+      uint4* cp = reinterpret_cast<uint4*>(static_cast<bf16*>(p.C) + (size_t)row * p.ldc + col0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 u;
+        bf16* hb = reinterpret_cast<bf16*>(&u);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) hb[e] = __float2bfloat16_rn(v[q * 8 + e]);
+        cp[q] = u;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int col = col0 + e;
+      if (col < p.N) {
+        float x = v[e];
+        if (EPI == EPI_BIAS || EPI == EPI_BIAS_RESID || EPI == EPI_BIAS_GELU)
+          x += __bfloat162float(p.bias[col]);
+        if (EPI == EPI_BIAS_RESID && p.drop.on) x = ((keep >> e) & 1u) ? x * p.drop.scale : 0.f;
+        if (EPI == EPI_BIAS_RESID) x += __bfloat162float(p.R[(size_t)row * p.ldr + col]);
+        if (EPI == EPI_DGELU) x *= gelu_grad_f(__bfloat162float(p.Z[(size_t)row * p.ldz + col]));
+        if (EPI == EPI_BIAS_GELU) {
+          p.Z[(size_t)row * p.ldz + col] = __float2bfloat16_rn(x);
+          x = gelu_f(x);
+        }
+        if (OUT_F32)
+          static_cast<float*>(p.C)[(size_t)row * p.ldc + col] = x;
+        else
+          static_cast<bf16*>(p.C)[(size_t)row * p.ldc + col] = __float2bfloat16_rn(x);
+      }
+    }
+  }
+}
+
+// Epilogue warps 4..11: wait for an accumulator, read it from TMEM (32 columns
+// at a time), add partition partials in order, apply the epilogue, store.
+// tfull0 / tempty0: addresses of tfull[0] and tempty[0] (tempty as a cluster
+// address when PAIR: the epilogue warps of both CTAs of a pair release the
+// accumulator to the leader CTA's barrier).  Tiles tile0, tile0 + tile_step, ...
+// are tile_rows high; this CTA's rows start at row_off inside a tile.
+template <int EPI, bool OUT_F32, bool REDUCE, bool PAIR>
+__device__ __forceinline__ void epilogue_role(const Params& p, uint32_t tmem_base, uint32_t tfull0,
+                                              uint32_t tempty0, volatile int* abort_flag,
+                                              int warp, int lane, int tile0, int tile_step,
+                                              int tile_rows, int row_off) {
+  auto tfull_bar = [&](int b) { return tfull0 + 8u * b; };
+  auto tempty_bar = [&](int b) { return tempty0 + 8u * b; };
+  const int ew = warp - 4;
+  const int quarter = warp & 3;
+  const int chalf = ew >> 2;
+  // FP8 descale (exactly 1 for bf16 operands)
+  const float ds = p.scale_a ? __fdiv_rn(1.0f, __fmul_rn(*p.scale_a, *p.scale_b)) : 1.0f;
+  int unit = 0;
+  bool ok = true;
+  for (int tile = tile0; tile < p.num_tiles && ok; tile += tile_step) {
+    int mb, nb;
+    tile_coords(p, tile, mb, nb);
+    const int row = mb * tile_rows + row_off + quarter * 32 + lane;
+    const int colbase = nb * BN + chalf * 128;
+    float sum[REDUCE ? 128 : 1];
+    for (int u = 0; u < p.units_per_tile; ++u, ++unit) {
+      const int buf = unit & 1;
+      const uint32_t uphase = (unit >> 1) & 1;
+      if (!mbar_wait_bounded(tfull_bar(buf), uphase, p.status, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tb = tmem_base + buf * BN + chalf * 128 + ((uint32_t)(quarter * 32) << 16);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t keep = REDUCE ? 0u : chunk_keep<EPI>(p, row, colbase + c * 32);
+        uint32_t r[32];
+        tmem_ld32(tb + c * 32, r);
+        tmem_ld_wait();
+        if constexpr (REDUCE) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float x = __uint_as_float(r[i]);
+            sum[c * 32 + i] = (u == 0) ? x : sum[c * 32 + i] + x;
+          }
+        } else {
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * ds;
+          epi_chunk<EPI, OUT_F32>(p, row, colbase + c * 32, v, keep);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (PAIR)
+          mbar_arrive_cluster(tempty_bar(buf));
+        else
+          mbar_arrive(tempty_bar(buf));
+      }
+    }
+    if constexpr (REDUCE) {
+      if (ok) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t keep = chunk_keep<EPI>(p, row, colbase + c * 32);
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = sum[c * 32 + i] * ds;
+          epi_chunk<EPI, OUT_F32>(p, row, colbase + c * 32, v, keep);
+        }
+      }
+    }
+  }
+  __syncwarp();
+}
+
+// ============================================================================
+// Pair kernel: a cluster of two CTAs computes 256x256 tiles with cta_group::2
+// MMAs (M = 256 across the pair, N = 256).  Each CTA loads its 128-row half of
+// A and its 128-row half of B; the leader CTA (rank 0) issues every MMA, which
+// reads both CTAs' shared memory and writes each CTA's 128 rows into its own
+// TMEM.  One tcgen05.mma does twice the work of the single-CTA kernel's, so the
+// one issuing thread keeps the tensor pipes busy.  K stages are 128 deep (two
+// 64-wide swizzle boxes), three stages of 64 KB per CTA.  With F8 the operands
+// are FP8 (tcgen05 kind::f8f6f4, K-major only): a 128-deep stage is one
+// 128-byte box per row (32 KB per CTA), six stages, four MMAs of K = 32; the
+// byte layout and descriptor steps are the bf16 ones.
+//   full[s]   leader only: both CTAs' TMA loads complete on it
+//   empty[s]  both CTAs: multicast commit after the stage's MMAs
+//   tfull[b]  both CTAs: multicast commit after a work unit's MMAs
+//   tempty[b] leader only: 16 arrivals, the epilogue warps of both CTAs
+constexpr int P_BK = 128, P_HALF = 128;              // K elements per stage, rows per CTA
+constexpr int P_ATOM = P_HALF * 128;                 // one [128 rows][128 bytes] box
+constexpr int P_SMEM_BYTES = 3 * 2 * 2 * P_ATOM + BAR_BYTES + 1024;   // 192 KB of stages
+
+template <int EPI, bool OUT_F32, bool REDUCE, bool F8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB, const Params p) {
+  constexpr int P_NBOX = F8 ? 1 : 2;                 // 128-byte boxes per row and stage
+  constexpr int P_STAGES = F8 ? 6 : 3;
+  constexpr int P_A_BYTES = P_NBOX * P_ATOM;
+  constexpr int P_B_BYTES = P_NBOX * P_ATOM;
+  constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
+  constexpr int P_KSTEPS = F8 ? P_BK / 32 : P_BK / 16;   // MMAs per stage
+  static_assert(P_STAGES * P_STAGE_BYTES + BAR_BYTES + 1024 <= P_SMEM_BYTES, "stage ring");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sA0 = smem_u32(smem);
+  const uint32_t sB0 = sA0 + P_STAGES * P_A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P_STAGES * P_STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * P_STAGES + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (P_STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * P_STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * P_STAGES + 2 + b); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_cta_rank();
+  const int pair_id = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P_STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 2 * EPI_WARPS);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PRODUCER_REGS));
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(EPILOGUE_REGS));
+  }
+
+  if (warp >= 4) {
+    epilogue_role<EPI, OUT_F32, REDUCE, true>(p, tmem_base, tfull_bar(0),
+                                              cluster_map(tempty_bar(0), 0), abort_flag, warp,
+                                              lane, pair_id, npairs, 2 * P_HALF, P_HALF * rank);
+  } else if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      const int kb_per_tile = p.kb_per_unit * p.units_per_tile;
+      bool ok = true;
+      for (int tile = pair_id; tile < p.num_tiles && ok; tile += npairs) {
+        int mb, nb;
+        tile_coords(p, tile, mb, nb);
+        const int m0 = mb * 2 * P_HALF + P_HALF * rank, n0 = nb * 2 * P_HALF + P_HALF * rank;
+        for (int kb = 0; kb < kb_per_tile; ++kb) {
+          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = cluster_map(full_bar(stage), 0);
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * P_STAGE_BYTES);
+          const int k0 = kb * P_BK;
+          const uint32_t sa = sA0 + stage * P_A_BYTES, sb = sB0 + stage * P_B_BYTES;
+#pragma unroll
+          for (int j = 0; j < P_NBOX; ++j) {
+            if (F8 || !p.a_mn)
+              tma_load_2d_pair(sa + j * P_ATOM, &tmA, fb, k0 + 64 * j, m0);
+            else
+              tma_load_2d_pair(sa + j * P_ATOM, &tmA, fb, m0 + 64 * j, k0);
+            if (F8 || !p.b_mn)
+              tma_load_2d_pair(sb + j * P_ATOM, &tmB, fb, k0 + 64 * j, n0);
+            else
+              tma_load_2d_pair(sb + j * P_ATOM, &tmB, fb, n0 + 64 * j, k0);
+          }
+          if (++stage == P_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (leader)
+    if (lane == 0 && rank == 0) {
+      const uint32_t idesc = F8 ? idesc_f8_f32(2 * P_HALF, BN, p.fmt_a, p.fmt_b)
+                                : idesc_bf16_f32(2 * P_HALF, BN, p.a_mn != 0, p.b_mn != 0);
+      const bool a_mn = !F8 && p.a_mn, b_mn = !F8 && p.b_mn;
+      const uint64_t a_desc0 = a_mn ? desc_mnbase(sA0, P_ATOM) : desc_kbase(sA0);
+      const uint64_t b_desc0 = b_mn ? desc_mnbase(sB0, P_ATOM) : desc_kbase(sB0);
+      int stage = 0;
+      uint32_t phase = 0;
+      int unit = 0;
+      bool ok = true;
+      for (int tile = pair_id; tile < p.num_tiles && ok; tile += npairs) {
+        for (int u = 0; u < p.units_per_tile && ok; ++u, ++unit) {
+          const int buf = unit & 1;
+          const uint32_t uphase = (unit >> 1) & 1;
+          if (!mbar_wait_bounded_cluster(tempty_bar(buf), uphase ^ 1u, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + buf * BN;
+          for (int kb = 0; kb < p.kb_per_unit; ++kb) {
+            if (!mbar_wait_bounded(full_bar(stage), phase, p.status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t ad0 = a_desc0 + (uint64_t)(stage * (P_A_BYTES / 16));
+            const uint64_t bd0 = b_desc0 + (uint64_t)(stage * (P_B_BYTES / 16));
+#pragma unroll
+            for (int kk = 0; kk < P_KSTEPS; ++kk) {
+              const uint32_t ao = a_mn ? mnmajor_off(kk) : kmajor_off(kk, P_ATOM);
+              const uint32_t bo = b_mn ? mnmajor_off(kk) : kmajor_off(kk, P_ATOM);
+              if (F8)
+                tc_mma_f8_pair(d_tmem, desc_add(ad0, ao), desc_add(bd0, bo), idesc,
+                               (kb > 0 || kk > 0) ? 1u : 0u);
+              else
+                tc_mma_bf16_pair(d_tmem, desc_add(ad0, ao), desc_add(bd0, bo), idesc,
+                                 (kb > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc_commit_pair_mc(empty_bar(stage), 3);
+            if (++stage == P_STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (ok) tc_commit_pair_mc(tfull_bar(buf), 3);
+        }
+      }
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  cluster_sync();
+  if (warp == 1) {
+    if (*abort_flag) {
+      const long long t0 = clock64();
+      while (clock64() - t0 < 2000000LL) {
+      }
+    }
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// 2D map over a row-major matrix with `rows` rows of `cols` elements (row pitch
+// ld elements; bf16, or bytes when fp8), box of box_cols x box_rows, 128-byte
+// swizzle, out-of-range elements read as zero.
+inline bool make_map(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, int64_t ld,
+                     uint32_t box_cols, uint32_t box_rows, bool fp8 = false) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * (fp8 ? 1 : 2)};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+             const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace tcg
+}  // namespace mtl

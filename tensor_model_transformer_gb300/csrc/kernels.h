@@ -50,13 +50,18 @@ struct GemmArgs {
   bool c_f32;             // C stored as fp32 (else as the operand dtype)
   unsigned* status;       // device status word
   Dropout drop;           // EPI_BIAS_RESID: C = R + dropout(acc + bias), e = row * N + col
+  // FP8 (gemm_fp8): A and B are bytes of format fmt_a / fmt_b (0 E4M3, 1 E5M2),
+  // K-major; the accumulator is scaled by 1 / (scale_a * scale_b) (device floats).
+  int fmt_a, fmt_b;
+  const float* scale_a;
+  const float* scale_b;
 };
 
 // Kernel kinds reported through the profiling hooks.
 enum KernelKind {
   KK_GEMM_TC = 1, KK_GEMM_SIMT = 2, KK_ATTN_FWD = 3, KK_ATTN_BWD = 4, KK_LN_FWD = 5,
   KK_LN_BWD = 6, KK_COLSUM = 7, KK_FINALIZE = 8, KK_GEMV_TC = 9, KK_ATTN_DECODE = 10,
-  KK_KV_WRITE = 11
+  KK_KV_WRITE = 11, KK_GEMM_FP8 = 12, KK_QUANT = 13
 };
 
 // Optional per-launch timing: when set, events[2i] / events[2i+1] are recorded
@@ -129,6 +134,19 @@ cudaError_t launch_ex(const LaunchCtx& c, void (*kernel)(KArgs...), dim3 grid, d
 cudaError_t gemm_simt(int dtype, const GemmArgs& a, const LaunchCtx& c);
 // tcgen05 / TMEM / TMA GEMM, bf16 operands, fp32 accumulate.
 cudaError_t gemm_tc(const GemmArgs& a, const LaunchCtx& c);
+// FP8 GEMM on the pair kernel (tcgen05 kind::f8f6f4): K-major byte operands,
+// (K / parts) % 128 == 0, lda / ldb multiples of 16, at least 2 SMs.
+bool gemm_fp8_supported(const GemmArgs& a, int num_sms);
+cudaError_t gemm_fp8(const GemmArgs& a, const LaunchCtx& c);
+// Per-tensor FP8 quantization of a bf16 / fp32 matrix [rows][cols] (row pitch
+// ld): amax = max |x| into *amax_bits (as float bits; zeroed first by the
+// caller), then scale = fmt_max / amax (1 if amax = 0) into *scale and
+// q = fp8(x * scale) [rows][cols] with row pitch ldq (RNE, saturating).
+// cols % 16 == 0.
+cudaError_t fp8_quantize(int src_dtype, const void* x, int64_t rows, int64_t cols, int64_t ld,
+                         int fmt, unsigned* amax_bits, float* scale, void* q, int64_t ldq,
+                         const LaunchCtx& c);
+
 // Host check of the shapes gemm_tc accepts.
 bool gemm_tc_supported(const GemmArgs& a);
 

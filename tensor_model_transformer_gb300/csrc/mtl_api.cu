@@ -858,6 +858,74 @@ mtl_status mtl_layer_decode(const mtl_layer_desc* desc, const mtl_weights* w, co
   return MTL_OK;
 }
 
+// ---------------------------------------------------------------- FP8
+
+mtl_status mtl_fp8_quantize(int32_t src_dtype, const void* x, int64_t rows, int64_t cols,
+                            int64_t ld, int32_t fmt, void* q, int64_t ldq, float* scale,
+                            void* workspace, size_t ws_bytes, mtl_stream stream) {
+  g_launches = 0;
+  g_cuda_err[0] = 0;
+  if (src_dtype != MTL_F32 && src_dtype != MTL_BF16) return MTL_ERR_INVALID_ARG;
+  if (fmt != MTL_FP8_E4M3 && fmt != MTL_FP8_E5M2) return MTL_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 0 || ld < cols || ldq < cols || cols % 16 || ldq % 16)
+    return MTL_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(q) || !scale || !aligned16(workspace) || (ld * (src_dtype == MTL_BF16 ? 2 : 4)) % 16)
+    return MTL_ERR_INVALID_ARG;
+  if (ws_bytes < kStatusBytes) return MTL_ERR_WORKSPACE;
+  const int nsm = device_sm_count();
+  if (nsm <= 0) return cuda_fail(cudaGetLastError(), "device query");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  LaunchCtx c{s, nsm, &g_launches, &g_prof};
+  unsigned* status = static_cast<unsigned*>(workspace);
+  MTL_TRY(cudaMemsetAsync(status, 0, kStatusBytes, s), "status reset");
+  // the amax word sits in the status block, after the status word
+  MTL_TRY(fp8_quantize(src_dtype == MTL_BF16 ? kBF16 : kF32, x, rows, cols, ld, fmt, status + 1,
+                       scale, q, ldq, c),
+          "fp8 quantize");
+  return MTL_OK;
+}
+
+mtl_status mtl_gemm_fp8(int32_t M, int32_t N, int32_t K, int32_t k_parts, const void* A,
+                        int64_t lda, int32_t fmt_a, const float* scale_a, const void* B,
+                        int64_t ldb, int32_t fmt_b, const float* scale_b, int32_t epi,
+                        const void* bias, const void* R, int64_t ldr, void* Z, int64_t ldz,
+                        void* C, int64_t ldc, int32_t c_f32, void* workspace, size_t ws_bytes,
+                        mtl_stream stream) {
+  g_launches = 0;
+  g_cuda_err[0] = 0;
+  if (M < 0 || N < 0 || K <= 0 || k_parts < 1 || K % k_parts) return MTL_ERR_INVALID_ARG;
+  if (epi < EPI_STORE || epi > EPI_DGELU) return MTL_ERR_INVALID_ARG;
+  if (lda < K || ldb < K || ldc < N) return MTL_ERR_INVALID_ARG;
+  if ((fmt_a != MTL_FP8_E4M3 && fmt_a != MTL_FP8_E5M2) ||
+      (fmt_b != MTL_FP8_E4M3 && fmt_b != MTL_FP8_E5M2))
+    return MTL_ERR_INVALID_ARG;
+  if (!aligned16(workspace) || !scale_a || !scale_b || !aligned16(A) || !aligned16(B) ||
+      !aligned16(C))
+    return MTL_ERR_INVALID_ARG;
+  if (ws_bytes < kStatusBytes) return MTL_ERR_WORKSPACE;
+  unsigned* status = static_cast<unsigned*>(workspace);
+  GemmArgs g = gemm_args(M, N, K, k_parts, A, lda, true, B, ldb, true, epi, C, ldc, c_f32 != 0,
+                         status);
+  g.bias = bias;
+  g.R = R;
+  g.ldr = ldr;
+  g.Z = Z;
+  g.ldz = ldz;
+  g.fmt_a = fmt_a;
+  g.fmt_b = fmt_b;
+  g.scale_a = scale_a;
+  g.scale_b = scale_b;
+  if (!gemm_fp8_supported(g, 2)) return MTL_ERR_UNSUPPORTED;
+  const int nsm = device_sm_count();
+  if (nsm <= 0) return cuda_fail(cudaGetLastError(), "device query");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  LaunchCtx c{s, nsm, &g_launches, &g_prof};
+  MTL_TRY(cudaMemsetAsync(status, 0, kStatusBytes, s), "status reset");
+  if (M == 0 || N == 0) return MTL_OK;
+  MTL_TRY(gemm_fp8(g, c), "gemm fp8");
+  return MTL_OK;
+}
+
 mtl_status mtl_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, int32_t k_parts,
                     const void* A, int64_t lda, int32_t a_k_major, const void* B, int64_t ldb,
                     int32_t b_k_major, int32_t epi, const void* bias, const void* R, int64_t ldr,

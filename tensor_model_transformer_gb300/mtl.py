@@ -84,6 +84,9 @@ def lib():
                                         vp]
         L.mtl_layer_decode.argtypes = [pd, ctypes.POINTER(Weights), vp, vp, vp, i32, vp, vp, sz,
                                        vp]
+        L.mtl_fp8_quantize.argtypes = [i32, vp, i64, i64, i64, i32, vp, i64, vp, vp, sz, vp]
+        L.mtl_gemm_fp8.argtypes = [i32, i32, i32, i32, vp, i64, i32, vp, vp, i64, i32, vp, i32,
+                                   vp, vp, i64, vp, i64, vp, i64, i32, vp, sz, vp]
         L.mtl_selftest_wait_timeout.argtypes = [vp, i64, vp]
         L.mtl_selftest_wait_timeout.restype = ctypes.c_int
         L.mtl_bias_grad_noalloc.argtypes = [i32, vp, i64, i32, i32, vp, vp]
@@ -95,7 +98,7 @@ def lib():
         for fn in ("mtl_layer_sizes", "mtl_layer_saved_layout", "mtl_layer_fwd", "mtl_layer_bwd",
                    "mtl_layer_check", "mtl_gemm", "mtl_attention_ws_bytes", "mtl_attention_fwd",
                    "mtl_attention_bwd", "mtl_attention_mask_bytes", "mtl_infer_sizes",
-                   "mtl_layer_prefill", "mtl_layer_decode"):
+                   "mtl_layer_prefill", "mtl_layer_decode", "mtl_fp8_quantize", "mtl_gemm_fp8"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -260,6 +263,28 @@ def kv_views(desc: LayerDesc, kv_cache, max_seq):
     k = kv_cache[:cnt * esz].view(dt).view(desc.batch, desc.heads, max_seq, d)
     v = kv_cache[half:half + cnt * esz].view(dt).view(desc.batch, desc.heads, max_seq, d)
     return k, v
+
+
+FP8_FORMATS = {"e4m3": 0, "e5m2": 1}
+
+
+def fp8_quantize(src_dtype, x, rows, cols, ld, fmt, q, ldq, scale, workspace, stream=None):
+    """mtl_fp8_quantize on torch tensors (q: uint8 device tensor, scale: float32 [1])."""
+    _check(lib().mtl_fp8_quantize(_dt(src_dtype), _ptr(x), rows, cols, ld, FP8_FORMATS[fmt],
+                                  _ptr(q), ldq, _ptr(scale), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)),
+           "mtl_fp8_quantize")
+
+
+def gemm_fp8(M, N, K, parts, A, lda, fmt_a, scale_a, B, ldb, fmt_b, scale_b, epi, C, ldc,
+             c_f32, workspace, bias=None, R=None, ldr=0, Z=None, ldz=0, stream=None):
+    """mtl_gemm_fp8 on torch tensors."""
+    _check(lib().mtl_gemm_fp8(M, N, K, parts, _ptr(A), lda, FP8_FORMATS[fmt_a], _ptr(scale_a),
+                              _ptr(B), ldb, FP8_FORMATS[fmt_b], _ptr(scale_b), epi, _ptr(bias),
+                              _ptr(R), ldr, _ptr(Z), ldz, _ptr(C), ldc, int(c_f32),
+                              _ptr(workspace), workspace.numel() * workspace.element_size(),
+                              _stream(stream)),
+           "mtl_gemm_fp8")
 
 
 def selftest_wait_timeout(workspace, limit_cycles, stream=None):

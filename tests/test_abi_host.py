@@ -268,3 +268,28 @@ def test_infer_sizes_and_rejects(mtl):
     dd = good_desc(mtl, p_attn=0.1)
     assert L.mtl_layer_prefill(ctypes.byref(dd), ctypes.byref(wt), ok[0], ok[1], ok[2], 512, FAKE,
                                ok[3], 1 << 30, None) == 1             # no dropout at inference
+
+
+def test_fp8_entry_points_reject(mtl):
+    L = mtl.lib()
+    ok = (FAKE, FAKE + 4096, FAKE + 8192, FAKE + 12288)
+    q = L.mtl_fp8_quantize
+    assert q(1, ok[0], 64, 250, 256, 0, ok[1], 256, ok[2], ok[3], 256, None) == 1   # cols % 16
+    assert q(1, ok[0], 64, 256, 256, 2, ok[1], 256, ok[2], ok[3], 256, None) == 1   # format
+    assert q(1, ok[0], 64, 256, 256, 0, ok[1], 256, None, ok[3], 256, None) == 1    # no scale
+    assert q(1, ok[0], 64, 256, 256, 0, ok[1], 256, ok[2], ok[3], 255, None) == 3
+    g = L.mtl_gemm_fp8
+    args = dict(M=256, N=256, K=512, parts=1, A=ok[0], lda=512, fa=0, sa=ok[2], B=ok[1], ldb=512,
+                fb=0, sb=ok[2], epi=0, C=ok[3], ldc=256)
+
+    def call(**kw):
+        a = dict(args)
+        a.update(kw)
+        return g(a["M"], a["N"], a["K"], a["parts"], a["A"], a["lda"], a["fa"], a["sa"], a["B"],
+                 a["ldb"], a["fb"], a["sb"], a["epi"], None, None, 0, None, 0, a["C"], a["ldc"], 1,
+                 FAKE + 16384, 256, None)
+
+    assert call(fa=3) == 1 and call(sb=None) == 1 and call(K=0) == 1 and call(parts=3) == 1
+    assert call(A=FAKE + 8) == 1
+    assert call(K=576, lda=576, ldb=576, parts=2) == 2        # 288-deep parts: not whole 128s
+    assert call(lda=520) == 2                                  # row pitch not a multiple of 16

@@ -1,0 +1,137 @@
+"""GPU parity of FP8: the per-tensor quantizer (bit-exact: scale and every byte)
+and the tcgen05 kind::f8f6f4 GEMM against the oracle on the same FP8 bytes
+(fp32 outputs within 1e-5 of the largest value: the products of FP8 values are
+exact in fp32, so only the accumulation order differs; bf16 outputs within
+4e-3, their own rounding)."""
+import numpy as np
+import pytest
+
+import oracle
+from harness import rel_err, to_np
+
+pytestmark = pytest.mark.gpu
+FP8 = oracle.fp8
+
+
+def _ws():
+    import torch
+    return torch.empty(1 << 12, dtype=torch.uint8, device="cuda")
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("src", ["bf16", "f32"])
+@pytest.mark.parametrize("case", ["normal", "wide", "zero", "ragged"])
+def test_quantize_bit_exact(fmt, src, case):
+    import torch
+    from tensor_model_transformer_gb300 import mtl
+    rng = np.random.default_rng(hash((fmt, src, case)) % 2**32)
+    rows, cols = {"normal": (256, 512), "wide": (64, 1024), "zero": (8, 32),
+                  "ragged": (301, 144)}[case]
+    x = rng.standard_normal((rows, cols)).astype(np.float32)
+    if case == "wide":   # values spanning many binades, into the subnormal range after scaling
+        x *= np.exp2(rng.uniform(-30, 8, (rows, cols))).astype(np.float32)
+    if case == "zero":
+        x[:] = 0
+    tdt = torch.bfloat16 if src == "bf16" else torch.float32
+    xd = torch.from_numpy(x).to(tdt).cuda()
+    x_used = xd.float().cpu().numpy()            # the values the GPU sees (bf16-rounded)
+    ld = cols + (16 if case == "ragged" else 0)
+    xs = torch.zeros((rows, ld), dtype=tdt, device="cuda")
+    xs[:, :cols] = xd
+    q = torch.full((rows, ld), 0xAB, dtype=torch.uint8, device="cuda")
+    scale = torch.zeros(1, dtype=torch.float32, device="cuda")
+    mtl.fp8_quantize(src, xs, rows, cols, ld, fmt, q, ld, scale, _ws())
+    torch.cuda.synchronize()
+    q_ref, s_ref = FP8.quantize(x_used, fmt)
+    assert scale.item() == float(s_ref)
+    got = FP8.decode(q[:, :cols].cpu().numpy(), fmt)
+    assert np.array_equal(got, q_ref), np.argwhere(got != q_ref)[:5]
+    assert np.all(q[:, cols:].cpu().numpy() == 0xAB)      # padding untouched
+
+
+def _codes(rng, shape, fmt):
+    """Random finite codes of a format."""
+    c = rng.integers(0, 256, shape, dtype=np.uint8)
+    v = FP8.decode(c, fmt)
+    bad = ~np.isfinite(v)
+    c[bad] = 0x38            # a finite code in both formats
+    return c
+
+
+@pytest.mark.parametrize("fmts", [("e4m3", "e4m3"), ("e5m2", "e4m3"), ("e4m3", "e5m2"),
+                                  ("e5m2", "e5m2")])
+@pytest.mark.parametrize("epi,c_f32,parts", [(0, True, 1), (0, True, 4), (1, False, 1),
+                                             (2, False, 2), (3, False, 1), (4, False, 1),
+                                             (2, True, 3)])
+def test_gemm_fp8(fmts, epi, c_f32, parts):
+    import torch
+    from tensor_model_transformer_gb300 import mtl
+    fa, fb = fmts
+    rng = np.random.default_rng(epi * 10 + parts)
+    M, N, K = 300, 320, 384 * parts
+    A = _codes(rng, (M, K), fa)
+    B = _codes(rng, (N, K), fb)
+    if fa == "e5m2":      # keep the products in a moderate range
+        A = np.where(np.abs(FP8.decode(A, fa)) > 64, 0x38, A).astype(np.uint8)
+    if fb == "e5m2":
+        B = np.where(np.abs(FP8.decode(B, fb)) > 64, 0x38, B).astype(np.uint8)
+    sa, sb = np.float32(3.7), np.float32(0.0123)
+    bias = rng.standard_normal(N).astype(np.float32)
+    R = rng.standard_normal((M, N)).astype(np.float32)
+    Zin = rng.standard_normal((M, N)).astype(np.float32)
+    dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dt).cuda()  # noqa: E731
+    Ad, Bd = dev(A, torch.uint8), dev(B, torch.uint8)
+    sad, sbd = dev(np.array([sa]), torch.float32), dev(np.array([sb]), torch.float32)
+    biasd, Rd = dev(bias, torch.bfloat16), dev(R, torch.bfloat16)
+    Zd = dev(Zin, torch.bfloat16)
+    C = torch.zeros((M, N), dtype=torch.float32 if c_f32 else torch.bfloat16, device="cuda")
+    mtl.gemm_fp8(M, N, K, parts, Ad, K, fa, sad, Bd, K, fb, sbd, epi, C, N, c_f32, _ws(),
+                 bias=biasd, R=Rd, ldr=N, Z=Zd, ldz=N)
+    torch.cuda.synchronize()
+    va, vb = FP8.decode(A, fa), FP8.decode(B, fb)
+    kp = K // parts
+    acc = sum(va[:, p * kp:(p + 1) * kp] @ vb[:, p * kp:(p + 1) * kp].T for p in range(parts))
+    acc = acc * FP8.descale(sa, sb)
+    b64 = biasd.float().cpu().numpy().astype(np.float64)
+    r64 = Rd.float().cpu().numpy().astype(np.float64)
+    z64 = Zd.float().cpu().numpy().astype(np.float64)
+    if epi == 0:
+        ref = acc
+    elif epi == 1:
+        ref = acc + b64
+    elif epi == 2:
+        ref = acc + b64 + r64
+    elif epi == 3:
+        ref = oracle.gelu(acc + b64)
+    else:
+        ref = acc * oracle.gelu_grad(z64)
+    tol = 1e-5 if c_f32 else 4e-3
+    assert rel_err(to_np(C), ref) <= tol, rel_err(to_np(C), ref)
+    if epi == 3:   # the pre-activation is written to Z
+        assert rel_err(to_np(Zd), acc + b64) <= 4e-3
+
+
+def test_quantize_then_gemm_is_the_oracle_fp8_gemm():
+    """Quantizer and GEMM together against oracle.fp8.gemm on bf16 inputs."""
+    import torch
+    from tensor_model_transformer_gb300 import mtl
+    rng = np.random.default_rng(9)
+    M, N, K = 512, 256, 768
+    A = rng.standard_normal((M, K)).astype(np.float32)
+    B = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    Ad = torch.from_numpy(A).to(torch.bfloat16).cuda()
+    Bd = torch.from_numpy(B).to(torch.bfloat16).cuda()
+    qa = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+    qb = torch.empty((N, K), dtype=torch.uint8, device="cuda")
+    sa = torch.empty(1, dtype=torch.float32, device="cuda")
+    sb = torch.empty(1, dtype=torch.float32, device="cuda")
+    ws = _ws()
+    mtl.fp8_quantize("bf16", Ad, M, K, K, "e4m3", qa, K, sa, ws)
+    mtl.fp8_quantize("bf16", Bd, N, K, K, "e4m3", qb, K, sb, ws)
+    C = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    mtl.gemm_fp8(M, N, K, 1, qa, K, "e4m3", sa, qb, K, "e4m3", sb, 0, C, N, True, ws)
+    torch.cuda.synchronize()
+    ref, *_ = FP8.gemm(Ad.float().cpu().numpy(), Bd.float().cpu().numpy())
+    assert rel_err(to_np(C), ref) <= 1e-5
+    exact = Ad.float().cpu().numpy().astype(np.float64) @ Bd.float().cpu().numpy().T
+    assert rel_err(to_np(C), exact) <= 0.1                     # FP8 error, not a bug
