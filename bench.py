@@ -32,7 +32,7 @@ import synthetic  # noqa: E402
 
 METRIC = "layer fwd+bwd TFLOP/s on 1 GB300 and % of BF16 dense peak; oracle-match"
 KIND_NAMES = {1: "gemm_tc", 2: "gemm_simt", 3: "attn_fwd", 4: "attn_bwd", 5: "ln_fwd", 9: "gemv_tc",
-              10: "attn_decode", 11: "kv_write",
+              10: "attn_decode", 11: "kv_write", 12: "gemm_fp8", 13: "fp8_quant",
               6: "ln_bwd", 7: "colsum", 8: "finalize"}
 
 
@@ -451,6 +451,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--p-drop", type=float, default=0.0,
                     help="dropout probability of the attention and hidden sites (default 0)")
+    ap.add_argument("--fp8", action="store_true",
+                    help="FP8 (E4M3, per-tensor scaled) forward GEMMs; backward in bf16")
     ap.add_argument("--workload", choices=["train", "decode"], default="train",
                     help="train: fwd+bwd step (default); decode: prefill, then one-token "
                          "decode steps over the KV cache")
@@ -489,7 +491,8 @@ def main():
     drop = args.drop or {}
     desc = mtl.layer_desc(shape.h, shape.heads, shape.seq, shape.batch, shape.ffn, args.t,
                           shape.dtype, p_attn=drop.get("p_attn", 0.0),
-                          p_hidden=drop.get("p_hidden", 0.0), seed=drop.get("seed", 0))
+                          p_hidden=drop.get("p_hidden", 0.0), seed=drop.get("seed", 0),
+                          fp8=1 if args.fp8 else 0)
     w = {k: torch.from_numpy(v).cuda().to(dt) for k, v in p.items()}
     x_h = torch.from_numpy(x).to(dt).pin_memory()
     dy_h = torch.from_numpy(dy).to(dt).pin_memory()
@@ -617,8 +620,11 @@ def main():
         rec["ms"] += dur
         rec["work"] += work[i]
     total_ms = sum(r["ms"] for r in per_kind.values()) or 1.0
+    flop_kinds = ("gemm_tc", "gemm_simt", "attn_fwd", "attn_bwd", "gemm_fp8")
     breakdown = {k: {"launches_per_step": r["launches"] // args.steps,
-                     "ms_per_step": r["ms"] / args.steps, "share": r["ms"] / total_ms}
+                     "ms_per_step": r["ms"] / args.steps, "share": r["ms"] / total_ms,
+                     "tflops" if k in flop_kinds else "gbs":
+                         r["work"] / (r["ms"] / 1e3) / (1e12 if k in flop_kinds else 1e9)}
                  for k, r in sorted(per_kind.items(), key=lambda kv: -kv[1]["ms"])}
 
     pk, pk_src = peaks()
@@ -626,9 +632,11 @@ def main():
     roofline = None
     if dom is not None:
         r = per_kind[dom]
-        if dom in ("gemm_tc", "gemm_simt", "attn_fwd", "attn_bwd"):
+        if dom in ("gemm_tc", "gemm_simt", "attn_fwd", "attn_bwd", "gemm_fp8"):
             achieved = r["work"] / (r["ms"] / 1e3) / 1e12
             peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+            if dom == "gemm_fp8":
+                peak *= 2.0          # dense FP8 : bf16 tensor rate, nominal 4.5 : 2.25
             unit, bound = "TFLOP/s", "tensor"
         else:
             achieved = r["work"] / (r["ms"] / 1e3) / 1e9
@@ -641,8 +649,9 @@ def main():
             traffic = float(tr["dram_bytes_per_launch_full"])
         roofline = {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak,
                     "unit": unit, "frac": achieved / peak, "traffic": traffic,
-                    "peak_source": f"{pk_src} bf16 sustained" if bound == "tensor"
-                    else f"{pk_src} hbm"}
+                    "peak_source": (f"{pk_src} bf16 sustained x 2 (nominal fp8:bf16)"
+                                    if dom == "gemm_fp8" else f"{pk_src} bf16 sustained")
+                    if bound == "tensor" else f"{pk_src} hbm"}
 
     out = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -656,7 +665,8 @@ def main():
                    "ffn": shape.ffn, "t": args.t, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (no flush)",
                    "flops_per_step": flops, "megatron_flops_per_step": megatron_flops(shape),
-                   "dropout": args.drop},
+                   "dropout": args.drop,
+                   "gemm_precision": "fp8 e4m3 forward, bf16 backward" if args.fp8 else "bf16"},
         "pct_of_bf16_peak": 100.0 * value / world / pk["bf16_tflops"],
         "peak_source": pk_src,
         "gpu_launches": launches,

@@ -103,6 +103,9 @@ typedef struct {
   float p_attn;      /* attention dropout probability, 0 <= p_attn < 1 */
   float p_hidden;    /* hidden dropout probability, 0 <= p_hidden < 1 */
   uint64_t seed;     /* Philox key of the dropout masks */
+  int32_t fp8;       /* 1: the forward's four GEMMs take per-tensor E4M3 operands
+                        (bf16 layers without dropout, h, h/t and ffn/t multiples
+                        of 128; the backward and decode stay bf16); 0: bf16 */
 } mtl_layer_desc;
 
 typedef struct {

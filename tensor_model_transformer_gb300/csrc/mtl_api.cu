@@ -71,6 +71,7 @@ struct Dims {
   size_t esz;
   float p_attn, p_hidden;
   unsigned long long seed;
+  int fp8;   // 1: FP8 (E4M3) forward GEMMs
 };
 
 // Dropout of one site: keep iff the Philox word >= floor(p * 2^32), scale 1/(1-p).
@@ -101,6 +102,7 @@ mtl_status validate(const mtl_layer_desc* desc, Dims* o) {
   if (!(d.ln_eps > 0.f)) return MTL_ERR_INVALID_ARG;
   if (!(d.p_attn >= 0.f && d.p_attn < 1.f) || !(d.p_hidden >= 0.f && d.p_hidden < 1.f))
     return MTL_ERR_INVALID_ARG;
+  if (d.fp8 != 0 && d.fp8 != 1) return MTL_ERR_INVALID_ARG;
   if (d.h % d.heads) return MTL_ERR_INVALID_ARG;
   if (d.heads % d.t || d.ffn % d.t) return MTL_ERR_INVALID_ARG;
   const int dh = d.h / d.heads;
@@ -127,6 +129,12 @@ mtl_status validate(const mtl_layer_desc* desc, Dims* o) {
   o->p_attn = d.p_attn;
   o->p_hidden = d.p_hidden;
   o->seed = d.seed;
+  o->fp8 = d.fp8;
+  if (d.fp8) {
+    // FP8 GEMMs: bf16 layers without dropout, K partitions of whole 128s
+    if (d.dtype != MTL_BF16 || d.p_attn > 0.f || d.p_hidden > 0.f) return MTL_ERR_UNSUPPORTED;
+    if (d.h % 128 || (d.h / d.t) % 128 || (d.ffn / d.t) % 128) return MTL_ERR_UNSUPPORTED;
+  }
   return MTL_OK;
 }
 
@@ -158,9 +166,33 @@ mtl_saved_layout saved_layout(const Dims& D) {
   return L;
 }
 
+// FP8 scratch of the forward: amax words and scales of the 8 quantized
+// operands, one activation buffer and one weight buffer (reused GEMM by GEMM).
+struct Fp8Ws {
+  size_t stats, qa, qb, total;
+};
+
+Fp8Ws fp8_ws_layout(const Dims& D) {
+  Fp8Ws F{0, 0, 0, 0};
+  if (!D.fp8) return F;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align_up(bytes);
+    return at;
+  };
+  const size_t wide = (size_t)(D.f > D.h ? D.f : D.h);
+  const size_t wmax = (size_t)(D.f > 3 * D.h ? D.f : 3 * D.h) * D.h;
+  F.stats = take(128);                    // 16 amax words, 16 scales
+  F.qa = take((size_t)D.n * wide);
+  F.qb = take(wmax);
+  F.total = off;
+  return F;
+}
+
 // Backward scratch, after the status word.
 struct WsLayout {
-  size_t dz, du, dx1, dctx, dqkv, dsum, gmask, partial, total;
+  size_t dz, du, dx1, dctx, dqkv, dsum, gmask, partial, fp8, total;
 };
 
 WsLayout ws_layout(const Dims& D) {
@@ -187,6 +219,7 @@ WsLayout ws_layout(const Dims& D) {
   const size_t pd = colsum_dropout_partial_floats((int)D.n, (int)D.h);
   if (pd > pf) pf = pd;
   W.partial = take(pf * 4);
+  W.fp8 = take(fp8_ws_layout(D).total);
   W.total = off;
   return W;
 }
@@ -268,8 +301,36 @@ size_t attn_ws_bytes(int32_t batch, int32_t seq, int32_t heads) {
 // The layer forward after validation (shared by mtl_layer_fwd and prefill):
 // intermediates go to `saved` at saved_layout(D).
 mtl_status forward_core(const Dims& D, float ln_eps, const mtl_weights* w, const void* x, void* y,
-                        void* saved, unsigned* status, const LaunchCtx& c) {
+                        void* saved, void* fp8ws, unsigned* status, const LaunchCtx& c) {
   const mtl_saved_layout L = saved_layout(D);
+  // A GEMM of the forward: bf16 (or fp32) as given, or with FP8 layers each
+  // operand quantized per tensor to E4M3 (own amax / scale slot) and the FP8
+  // pair kernel.
+  const Fp8Ws FW = fp8_ws_layout(D);
+  int slot = 0;
+  if (D.fp8) MTL_TRY(cudaMemsetAsync(at<char>(fp8ws, FW.stats), 0, 128, c.stream), "fp8 stats");
+  auto fwd_gemm = [&](GemmArgs g, const char* where) -> mtl_status {
+    if (!D.fp8) {
+      MTL_TRY(run_gemm(D, g, c), where);
+      return MTL_OK;
+    }
+    unsigned* amax = at<unsigned>(fp8ws, FW.stats) + 2 * slot;
+    float* sc = at<float>(fp8ws, FW.stats + 64) + 2 * slot;
+    ++slot;
+    uint8_t* qa = at<uint8_t>(fp8ws, FW.qa);
+    uint8_t* qb = at<uint8_t>(fp8ws, FW.qb);
+    MTL_TRY(fp8_quantize(kBF16, g.A.ptr, g.M, g.K, g.A.ld, 0, amax, sc, qa, g.K, c), where);
+    MTL_TRY(fp8_quantize(kBF16, g.B.ptr, g.N, g.K, g.B.ld, 0, amax + 1, sc + 1, qb, g.K, c), where);
+    g.A = {qa, g.K, true};
+    g.B = {qb, g.K, true};
+    g.fmt_a = 0;
+    g.fmt_b = 0;
+    g.scale_a = sc;
+    g.scale_b = sc + 1;
+    MTL_TRY(gemm_fp8(g, c), where);
+    return MTL_OK;
+  };
+  mtl_status gst;
   const int n = (int)D.n, h = (int)D.h, f = (int)D.f, t = (int)D.t;
   void* u1 = at<char>(saved, L.u1);
   void* qkv = at<char>(saved, L.qkv);
@@ -290,7 +351,7 @@ mtl_status forward_core(const Dims& D, float ln_eps, const mtl_weights* w, const
     GemmArgs g = gemm_args(n, 3 * h, h, 1, u1, h, true, w->w_qkv, h, true, EPI_BIAS, qkv, 3 * h,
                            false, status);
     g.bias = w->b_qkv;
-    MTL_TRY(run_gemm(D, g, c), "qkv gemm");
+    if ((gst = fwd_gemm(g, "qkv gemm")) != MTL_OK) return gst;
   }
   // F3 attention per head
   if (bf) {
@@ -310,7 +371,7 @@ mtl_status forward_core(const Dims& D, float ln_eps, const mtl_weights* w, const
     g.drop = make_drop(D.p_hidden, D.seed, SITE_OUT);
     g.R = x;
     g.ldr = h;
-    MTL_TRY(run_gemm(D, g, c), "out-proj gemm");
+    if ((gst = fwd_gemm(g, "out-proj gemm")) != MTL_OK) return gst;
   }
   // F5 LN2
   MTL_TRY(ln_fwd(D.dtype, x1, w->ln2_g, w->ln2_b, u2, at<float>(saved, L.mu2),
@@ -323,7 +384,7 @@ mtl_status forward_core(const Dims& D, float ln_eps, const mtl_weights* w, const
     g.bias = w->b_fc1;
     g.Z = z;
     g.ldz = f;
-    MTL_TRY(run_gemm(D, g, c), "fc1 gemm");
+    if ((gst = fwd_gemm(g, "fc1 gemm")) != MTL_OK) return gst;
   }
   // F7 fc2, row-parallel + g: t partials over K = ffn, + b_fc2, dropout, + x1
   {
@@ -333,7 +394,7 @@ mtl_status forward_core(const Dims& D, float ln_eps, const mtl_weights* w, const
     g.drop = make_drop(D.p_hidden, D.seed, SITE_FC2);
     g.R = x1;
     g.ldr = h;
-    MTL_TRY(run_gemm(D, g, c), "fc2 gemm");
+    if ((gst = fwd_gemm(g, "fc2 gemm")) != MTL_OK) return gst;
   }
   return MTL_OK;
 }
@@ -351,6 +412,7 @@ mtl_status validate_decode(const mtl_layer_desc* desc, int32_t max_seq, Dims* o)
   d.seq = d.dtype == MTL_BF16 ? 128 : 1;   // a valid stand-in: decode has no sequence axis
   d.p_attn = 0.f;
   d.p_hidden = 0.f;
+  d.fp8 = 0;                                // decode GEMMs stay bf16
   mtl_status st = validate(&d, o);
   if (st != MTL_OK) return st;
   o->seq = 1;
@@ -458,7 +520,7 @@ mtl_status mtl_layer_fwd(const mtl_layer_desc* desc, const mtl_weights* w, const
   MTL_TRY(cudaMemsetAsync(status, 0, kStatusBytes, s), "status reset");
   if (D.n == 0) return MTL_OK;
 
-  return forward_core(D, desc->ln_eps, w, x, y, saved, status, c);
+  return forward_core(D, desc->ln_eps, w, x, y, saved, at<char>(workspace, W.fp8), status, c);
 }
 
 mtl_status mtl_layer_bwd(const mtl_layer_desc* desc, const mtl_weights* w, const void* x,
@@ -749,7 +811,7 @@ mtl_status mtl_infer_sizes(const mtl_layer_desc* desc, int32_t max_seq, size_t* 
     st = validate(&pd, &P);
     if (st != MTL_OK) return st;
     if (pd.seq > max_seq) return MTL_ERR_INVALID_ARG;
-    *prefill_ws_bytes = kStatusBytes + saved_layout(P).total;
+    *prefill_ws_bytes = kStatusBytes + saved_layout(P).total + fp8_ws_layout(P).total;
   }
   return MTL_OK;
 }
@@ -768,7 +830,7 @@ mtl_status mtl_layer_prefill(const mtl_layer_desc* desc, const mtl_weights* w, c
   if (!weights_ok(w) || !aligned16(x) || !aligned16(y) || !aligned16(kv_cache) ||
       !aligned16(workspace) || !cache_len || x == y)
     return MTL_ERR_INVALID_ARG;
-  const size_t need = kStatusBytes + saved_layout(D).total;
+  const size_t need = kStatusBytes + saved_layout(D).total + fp8_ws_layout(D).total;
   if (ws_bytes < need) return MTL_ERR_WORKSPACE;
   const int nsm = device_sm_count();
   if (nsm <= 0) return cuda_fail(cudaGetLastError(), "device query");
@@ -778,7 +840,8 @@ mtl_status mtl_layer_prefill(const mtl_layer_desc* desc, const mtl_weights* w, c
   MTL_TRY(cudaMemsetAsync(status, 0, kStatusBytes, s), "status reset");
   if (D.n == 0) return MTL_OK;
   void* saved = at<char>(workspace, kStatusBytes);
-  st = forward_core(D, desc->ln_eps, w, x, y, saved, status, c);
+  st = forward_core(D, desc->ln_eps, w, x, y, saved,
+                    at<char>(workspace, kStatusBytes + saved_layout(D).total), status, c);
   if (st != MTL_OK) return st;
   const size_t half = kv_cache_bytes(D, max_seq) / 2;
   MTL_TRY(kv_write(D.dtype, at<char>(saved, saved_layout(D).qkv), kv_cache,

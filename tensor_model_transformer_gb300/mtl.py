@@ -35,7 +35,8 @@ class LayerDesc(ctypes.Structure):
     _fields_ = [("h", ctypes.c_int32), ("heads", ctypes.c_int32), ("seq", ctypes.c_int32),
                 ("batch", ctypes.c_int32), ("ffn", ctypes.c_int32), ("t", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("ln_eps", ctypes.c_float), ("causal", ctypes.c_int32),
-                ("p_attn", ctypes.c_float), ("p_hidden", ctypes.c_float), ("seed", ctypes.c_uint64)]
+                ("p_attn", ctypes.c_float), ("p_hidden", ctypes.c_float), ("seed", ctypes.c_uint64),
+                ("fp8", ctypes.c_int32)]
 
 
 class Weights(ctypes.Structure):
@@ -122,10 +123,12 @@ def _stream(stream):
 
 
 def layer_desc(h, heads, seq, batch, ffn, t, dtype, ln_eps=1e-5, causal=1, p_attn=0.0,
-               p_hidden=0.0, seed=0) -> LayerDesc:
-    """mtl_layer_desc; p_attn / p_hidden / seed: dropout probabilities and Philox seed."""
+               p_hidden=0.0, seed=0, fp8=0) -> LayerDesc:
+    """mtl_layer_desc; p_attn / p_hidden / seed: dropout probabilities and Philox seed;
+    fp8=1: FP8 (E4M3) forward GEMMs."""
     dt = {"f32": F32, "bf16": BF16, F32: F32, BF16: BF16}[dtype]
-    return LayerDesc(h, heads, seq, batch, ffn, t, dt, ln_eps, causal, p_attn, p_hidden, seed)
+    return LayerDesc(h, heads, seq, batch, ffn, t, dt, ln_eps, causal, p_attn, p_hidden, seed,
+                     fp8)
 
 
 def layer_sizes(desc: LayerDesc):

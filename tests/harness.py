@@ -40,7 +40,7 @@ def f32(v):
     return float(np.float32(v))
 
 
-def run_gpu(shape, x, p, dy, t, runs=1, want_saved=True, drop=None):
+def run_gpu(shape, x, p, dy, t, runs=1, want_saved=True, drop=None, fp8=0):
     """Forward + backward through the C ABI.  Returns a dict of float64 arrays.
 
     drop: optional dict(p_attn, p_hidden, seed) of float32-exact probabilities."""
@@ -50,7 +50,7 @@ def run_gpu(shape, x, p, dy, t, runs=1, want_saved=True, drop=None):
     drop = drop or {}
     desc = mtl.layer_desc(shape.h, shape.heads, shape.seq, b, shape.ffn, t, shape.dtype,
                           p_attn=drop.get("p_attn", 0.0), p_hidden=drop.get("p_hidden", 0.0),
-                          seed=drop.get("seed", 0))
+                          seed=drop.get("seed", 0), fp8=fp8)
     dev_p = {k: to_device(v, shape.dtype) for k, v in p.items()}
     xd = to_device(x, shape.dtype)
     dyd = to_device(dy, shape.dtype)
@@ -73,9 +73,9 @@ def run_gpu(shape, x, p, dy, t, runs=1, want_saved=True, drop=None):
     return outs if runs > 1 else outs[0]
 
 
-def run_oracle(shape, x, p, dy, drop=None):
+def run_oracle(shape, x, p, dy, drop=None, fp8=False):
     """The oracle's outputs and intermediates, keyed like run_gpu."""
-    y, cache = oracle.layer_fwd(p, x, shape.heads, dropout=drop)
+    y, cache = oracle.layer_fwd(p, x, shape.heads, dropout=drop, fp8=fp8)
     dx, g, _ = oracle.layer_bwd(p, cache, dy)
     out = {"y": y, "dx": dx}
     out.update({"d_" + k: v for k, v in g.items()})

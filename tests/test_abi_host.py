@@ -201,9 +201,10 @@ def test_layer_desc_layout_matches_header(mtl, tmp_path):
         pytest.skip("no C compiler")
     src = tmp_path / "probe.c"
     src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "mtl.h"\n'
-                   'int main(void) { printf("%zu %zu %zu %zu %zu\\n", sizeof(mtl_layer_desc),'
+                   'int main(void) { printf("%zu %zu %zu %zu %zu %zu\\n", sizeof(mtl_layer_desc),'
                    ' offsetof(mtl_layer_desc, causal), offsetof(mtl_layer_desc, p_attn),'
-                   ' offsetof(mtl_layer_desc, p_hidden), offsetof(mtl_layer_desc, seed));'
+                   ' offsetof(mtl_layer_desc, p_hidden), offsetof(mtl_layer_desc, seed),'
+                   ' offsetof(mtl_layer_desc, fp8));'
                    ' return 0; }\n')
     exe = tmp_path / "probe"
     subprocess.run([gcc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
@@ -212,7 +213,7 @@ def test_layer_desc_layout_matches_header(mtl, tmp_path):
                                           check=True).stdout.split()]
     D = mtl.LayerDesc
     assert got == [ctypes.sizeof(D), D.causal.offset, D.p_attn.offset, D.p_hidden.offset,
-                   D.seed.offset]
+                   D.seed.offset, D.fp8.offset]
 
 
 def test_attention_entry_points_reject(mtl):
@@ -293,3 +294,13 @@ def test_fp8_entry_points_reject(mtl):
     assert call(A=FAKE + 8) == 1
     assert call(K=576, lda=576, ldb=576, parts=2) == 2        # 288-deep parts: not whole 128s
     assert call(lda=520) == 2                                  # row pitch not a multiple of 16
+
+
+def test_fp8_layer_validation(mtl):
+    ok = good_desc(mtl, fp8=1)                                  # h 256, t 2: 128-wide parts
+    assert mtl.layer_sizes(ok)[1] > mtl.layer_sizes(good_desc(mtl))[1]
+    L = mtl.lib()
+    for kw, st in ((dict(fp8=2), 1), (dict(fp8=1, dtype="f32"), 2), (dict(fp8=1, p_attn=0.1), 2),
+                   (dict(fp8=1, t=4), 2)):                      # h/t = 64: not whole 128s
+        d = good_desc(mtl, **kw)
+        assert L.mtl_layer_sizes(ctypes.byref(d), None, None) == st, kw

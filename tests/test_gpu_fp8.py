@@ -135,3 +135,50 @@ def test_quantize_then_gemm_is_the_oracle_fp8_gemm():
     assert rel_err(to_np(C), ref) <= 1e-5
     exact = Ad.float().cpu().numpy().astype(np.float64) @ Bd.float().cpu().numpy().T
     assert rel_err(to_np(C), exact) <= 0.1                     # FP8 error, not a bug
+
+
+# FP8 layer forward.  The GPU quantizes its bf16 activations, the oracle its
+# fp64 ones: the two differ by the bf16 rounding (2^-9 relative), so about 3% of
+# the elements sit close enough to an E4M3 rounding midpoint (spacing 2^-3
+# relative) to land one FP8 step apart, and the per-tensor scales differ by the
+# same 2^-9.  A GEMM output then carries an error of about 0.1 * sqrt(0.03) ~ 2%
+# of a typical output in random sign, under 2% of the largest output: the
+# intermediates are checked at 5e-2; y, dominated by the residual, at the bf16
+# 1.5e-2; the bf16 backward on the FP8 forward's activations at 5e-2.
+FP8_TOL = {"y": 1.5e-2, "s": 5e-2, "d": 5e-2}
+
+FP8_SHAPES = {
+    "d128_t2": (dict(h=256, heads=2, seq=256, batch=2), 2),
+    "d96_t1": (dict(h=384, heads=4, seq=128, batch=2), 1),
+    "d64_t4": (dict(h=512, heads=8, seq=128, batch=1), 4),
+}
+
+
+def _fp8_check(shape, t, keys=None):
+    from harness import compare, make, run_gpu, run_oracle
+    x, p, dy = make(shape, seed=2, affine=True)
+    g8 = run_gpu(shape, x, p, dy, t, fp8=1)
+    ref = run_oracle(shape, x, p, dy, fp8=True)
+    errs = compare(g8, ref, "bf16", keys=keys)
+    tol = lambda k: FP8_TOL["y"] if k == "y" else FP8_TOL["s" if k.startswith("s_") else "d"]  # noqa: E731
+    bad = {k: v for k, v in errs.items() if v > tol(k)}
+    assert not bad, (bad, errs)
+    # the FP8 path ran: its GEMM outputs differ from the bf16 layer's
+    g16 = run_gpu(shape, x, p, dy, t)
+    assert rel_err(g8["s_qkv"], g16["s_qkv"]) > 1e-3
+    return errs
+
+
+@pytest.mark.parametrize("name", sorted(FP8_SHAPES))
+def test_fp8_layer_forward_and_backward(name):
+    import synthetic
+    kw, t = FP8_SHAPES[name]
+    shape = synthetic.tiny(dtype="bf16", w_std=0.02, out_std=0.01, **kw)
+    _fp8_check(shape, t)
+
+
+def test_fp8_layer_headline_shape_batch1():
+    """The 8.3B-shaped layer (h 3072, 32 heads, t = 8) at batch 1, FP8 forward."""
+    import synthetic
+    shape = synthetic.CONFIGS["D"].with_(batch=1)
+    _fp8_check(shape, 8, keys=["y", "s_qkv", "s_ctx", "s_x1", "s_z", "s_a", "d_w_fc2", "dx"])
