@@ -9,4 +9,5 @@ from .layer import (LN_EPS, ReductionCounter, attention_head_bwd, attention_head
                     causal_mask, f_allreduce, g_allreduce, gelu, gelu_grad, layer_bwd,
                     layer_bwd_partitioned, layer_flops, layer_fwd, layer_fwd_partitioned,
                     layernorm_bwd, layernorm_fwd, multihead_bwd, multihead_fwd,
-                    shard_ranges, split_qkv_columns, gemm_partitioned)
+                    shard_ranges, split_qkv_columns, gemm_partitioned,
+                    layer_fwd_post_ln, layer_bwd_post_ln, layer_fwd_post_ln_partitioned)

@@ -331,6 +331,89 @@ def layer_bwd(params, cache, dy):
 
 
 # --------------------------------------------------------------------------
+# Post-LN variant (original BERT)
+# --------------------------------------------------------------------------
+
+def layer_fwd_post_ln(params, x, heads, eps=LN_EPS):
+    """Post-LN layer ("Paper 1: BERT LayerNorm Rearrangement", the original BERT
+    arrangement the Pre-LN layer replaces): LayerNorm after each residual add,
+        h1 = x + Attn(x) W_o^T + b_o,    x1 = LN1(h1),
+        h2 = x1 + GeLU(x1 W_fc1^T + b_fc1) W_fc2^T + b_fc2,    y = LN2(h2),
+    with Attn the same causal multi-head attention over qkv = x W_qkv^T + b_qkv.
+    Returns (y, cache)."""
+    p = {k: _f64(v) for k, v in params.items()}
+    x = _f64(x)
+    batch, seq, h = x.shape
+    d = h // heads
+    xf = x.reshape(batch * seq, h)
+    qkv = xf @ p["w_qkv"].T + p["b_qkv"]
+    ctx, lse, probs = multihead_fwd(qkv, batch, seq, heads, d)
+    h1 = xf + ctx @ p["w_o"].T + p["b_o"]
+    x1, mu1, rstd1 = layernorm_fwd(h1, p["ln1_g"], p["ln1_b"], eps)
+    z = x1 @ p["w_fc1"].T + p["b_fc1"]
+    a = gelu(z)
+    h2 = x1 + a @ p["w_fc2"].T + p["b_fc2"]
+    y, mu2, rstd2 = layernorm_fwd(h2, p["ln2_g"], p["ln2_b"], eps)
+    cache = dict(x=xf, qkv=qkv, ctx=ctx, lse=lse, probs=probs, h1=h1, mu1=mu1, rstd1=rstd1,
+                 x1=x1, z=z, a=a, h2=h2, mu2=mu2, rstd2=rstd2, batch=batch, seq=seq,
+                 heads=heads, post_ln=True)
+    return y.reshape(batch, seq, h), cache
+
+
+def layer_bwd_post_ln(params, cache, dy):
+    """Analytic backward of layer_fwd_post_ln.  Returns (dx, grads, inter)."""
+    p = {k: _f64(v) for k, v in params.items()}
+    c = cache
+    batch, seq, heads = c["batch"], c["seq"], c["heads"]
+    n, h = c["x"].shape
+    d = h // heads
+    dy = _f64(dy).reshape(n, h)
+    g = {}
+    dh2, g["ln2_g"], g["ln2_b"] = layernorm_bwd(dy, c["h2"], c["mu2"], c["rstd2"], p["ln2_g"])
+    g["w_fc2"] = dh2.T @ c["a"]
+    g["b_fc2"] = dh2.sum(axis=0)
+    dz = (dh2 @ p["w_fc2"]) * gelu_grad(c["z"])
+    g["w_fc1"] = dz.T @ c["x1"]
+    g["b_fc1"] = dz.sum(axis=0)
+    dx1 = dh2 + dz @ p["w_fc1"]
+    dh1, g["ln1_g"], g["ln1_b"] = layernorm_bwd(dx1, c["h1"], c["mu1"], c["rstd1"], p["ln1_g"])
+    g["w_o"] = dh1.T @ c["ctx"]
+    g["b_o"] = dh1.sum(axis=0)
+    dctx = dh1 @ p["w_o"]
+    dqkv = multihead_bwd(c["qkv"], c["ctx"], c["probs"], dctx, batch, seq, heads, d)
+    g["w_qkv"] = dqkv.T @ c["x"]
+    g["b_qkv"] = dqkv.sum(axis=0)
+    dx = dh1 + dqkv @ p["w_qkv"]
+    inter = dict(dh2=dh2, dz=dz, dx1=dx1, dh1=dh1, dctx=dctx, dqkv=dqkv)
+    return dx.reshape(batch, seq, h), g, inter
+
+
+def layer_fwd_post_ln_partitioned(params, x, heads, t, counter, eps=LN_EPS):
+    """layer_fwd_post_ln over t simulated ranks: QKV / fc1 split by columns, the
+    out-proj / fc2 partials summed in rank order (g) before the residual add and
+    the LayerNorm, which stay outside the partitions."""
+    p = {k: _f64(v) for k, v in params.items()}
+    x = _f64(x)
+    batch, seq, h = x.shape
+    ffn = p["w_fc1"].shape[0]
+    d = h // heads
+    xf = x.reshape(batch * seq, h)
+    ranks = shard_ranges(h, ffn, heads, t)
+    parts = []
+    for r, rk in enumerate(ranks):
+        qkv_r = xf @ p["w_qkv"][rk["qkv"]].T + p["b_qkv"][rk["qkv"]]
+        ctx_r, _, _ = multihead_fwd(qkv_r, batch, seq, rk["heads"], d)
+        parts.append(ctx_r @ p["w_o"][:, rk["ctx"]].T)
+    h1 = xf + g_allreduce(parts, counter) + p["b_o"]
+    x1, _, _ = layernorm_fwd(h1, p["ln1_g"], p["ln1_b"], eps)
+    parts = [gelu(x1 @ p["w_fc1"][rk["ffn"]].T + p["b_fc1"][rk["ffn"]]) @ p["w_fc2"][:, rk["ffn"]].T
+             for rk in ranks]
+    h2 = x1 + g_allreduce(parts, counter) + p["b_fc2"]
+    y, _, _ = layernorm_fwd(h2, p["ln2_g"], p["ln2_b"], eps)
+    return y.reshape(batch, seq, h)
+
+
+# --------------------------------------------------------------------------
 # The whole layer, partitioned over t simulated ranks
 # --------------------------------------------------------------------------
 
