@@ -106,6 +106,15 @@ typedef struct {
   int32_t fp8;       /* 1: the forward's four GEMMs take per-tensor E4M3 operands
                         (bf16 layers without dropout, h, h/t and ffn/t multiples
                         of 128; the backward and decode stay bf16); 0: bf16 */
+  int32_t post_ln;   /* 1: Post-LN layer (original BERT, page section "Paper 1:
+                        BERT LayerNorm Rearrangement"): h1 = x + Attn(x),
+                        x1 = LN1(h1), h2 = x1 + MLP(x1), y = LN2(h2), with the
+                        QKV GEMM on x; no dropout, no FP8, no decode; 0: Pre-LN */
+  int32_t recompute; /* 1: selective recomputation: the forward does not save the
+                        LayerNorm outputs (Pre-LN u1, u2; Post-LN x1) or
+                        a = GeLU(z); the backward recomputes them from the saved
+                        inputs and statistics (LayerNorm outputs bit for bit).
+                        Smaller `saved`, one elementwise pass each; 0: save all */
 } mtl_layer_desc;
 
 typedef struct {
@@ -129,6 +138,10 @@ typedef struct {
   size_t mu1, rstd1, u1, qkv, ctx, lse, x1, mu2, rstd2, u2, z, a;
   size_t attn_mask;   /* keep bits of attention dropout (bf16 layers with p_attn > 0;
                          empty otherwise), see mtl_attention_mask_bytes */
+  size_t h1, h2;      /* Post-LN: the LayerNorm inputs x + Attn(x) and x1 + MLP(x1)
+                         [n][h] (mu1 / rstd1 and mu2 / rstd2 are their statistics;
+                         u1, u2 are empty); Pre-LN: empty.  With recompute, u1, u2
+                         (Pre-LN), x1 (Post-LN) and a are empty. */
   size_t total;
 } mtl_saved_layout;
 

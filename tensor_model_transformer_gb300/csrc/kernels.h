@@ -147,6 +147,19 @@ cudaError_t fp8_quantize(int src_dtype, const void* x, int64_t rows, int64_t col
                          int fmt, unsigned* amax_bits, float* scale, void* q, int64_t ldq,
                          const LaunchCtx& c);
 
+// LayerNorm backward without a residual: dx = LN_bwd(du + du2) where du (fp32,
+// may be null) and du2 (layer dtype) are the two parts of the upstream
+// gradient (the Post-LN layer).
+cudaError_t ln_bwd_sum(int dtype, const float* du, const void* du2, const void* x,
+                       const float* mean, const float* rstd, const void* g, void* dx,
+                       float* dgamma, float* dbeta, float* partial, int n, int h,
+                       const LaunchCtx& c);
+// Recomputation: u = LN output from saved statistics (bitwise the forward's),
+// a = GeLU(z) elementwise (count a multiple of 8).
+cudaError_t ln_apply(int dtype, const void* x, const float* mean, const float* rstd,
+                     const void* g, const void* b, void* u, int n, int h, const LaunchCtx& c);
+cudaError_t gelu_apply(int dtype, const void* z, void* a, int64_t count, const LaunchCtx& c);
+
 // Host check of the shapes gemm_tc accepts.
 bool gemm_tc_supported(const GemmArgs& a);
 

@@ -122,9 +122,12 @@ __global__ void __launch_bounds__(kLnThreadsMax)
 // Dynamic shared memory: the block's running column sums of du * xhat and du
 // (2 * h floats); thread i owns the same columns in every row, so the sums need
 // no atomics.  R rows per iteration, their loads issued before the reduction.
-template <typename T, int V, int R>
+// MODE 0: du fp32, dx = resid + LN_bwd(du) (Pre-LN);  MODE 1: du = du2 (of type
+// T), dx = LN_bwd(du);  MODE 2: du = du (fp32) + du2 (T), dx = LN_bwd(du) (the
+// Post-LN layer's two LayerNorms).
+template <typename T, int V, int R, int MODE>
 __global__ void __launch_bounds__(kLnThreadsMax)
-    ln_bwd_kernel(const float* __restrict__ du, const T* __restrict__ x,
+    ln_bwd_kernel(const float* __restrict__ du, const T* __restrict__ du2, const T* __restrict__ x,
                   const float* __restrict__ mean_in, const float* __restrict__ rstd_in,
                   const T* __restrict__ gamma, const T* __restrict__ resid, T* __restrict__ dx,
                   float* __restrict__ part_g, float* __restrict__ part_b, int n, int h,
@@ -164,14 +167,23 @@ __global__ void __launch_bounds__(kLnThreadsMax)
         if (live && vi < nvec) {
           const size_t off = (size_t)(r0 + rr) * h + vi * E;
           xv[rr][i].load(x + off);
-          rv[rr][i].load(resid + off);
+          if (MODE == 0) rv[rr][i].load(resid + off);
+          if (MODE != 1) {
 #pragma unroll
-          for (int e = 0; e < E; e += 4) {
-            const float4 q = *reinterpret_cast<const float4*>(du + off + e);
-            dd[rr][i][e] = q.x;
-            dd[rr][i][e + 1] = q.y;
-            dd[rr][i][e + 2] = q.z;
-            dd[rr][i][e + 3] = q.w;
+            for (int e = 0; e < E; e += 4) {
+              const float4 q = *reinterpret_cast<const float4*>(du + off + e);
+              dd[rr][i][e] = q.x;
+              dd[rr][i][e + 1] = q.y;
+              dd[rr][i][e + 2] = q.z;
+              dd[rr][i][e + 3] = q.w;
+            }
+          }
+          if (MODE != 0) {
+            Vec<T> d2;
+            d2.load(du2 + off);
+#pragma unroll
+            for (int e = 0; e < E; ++e)
+              dd[rr][i][e] = (MODE == 2 ? dd[rr][i][e] : 0.f) + d2.get(e);
           }
         }
       }
@@ -213,7 +225,7 @@ __global__ void __launch_bounds__(kLnThreadsMax)
         for (int e = 0; e < E; ++e) {
           const float xh = (xv[rr][i].get(e) - mu[rr]) * rs[rr];
           const float gd = dd[rr][i][e] * tg.get(e);
-          o.set(e, rv[rr][i].get(e) + rs[rr] * (gd - m1 - xh * m2));
+          o.set(e, (MODE == 0 ? rv[rr][i].get(e) : 0.f) + rs[rr] * (gd - m1 - xh * m2));
           ag[e] += dd[rr][i][e] * xh;
           ab[e] += dd[rr][i][e];
         }
@@ -350,10 +362,10 @@ cudaError_t ln_fwd_t(const void* x, const void* g, const void* b, void* u, float
   return cudaGetLastError();
 }
 
-template <typename T>
-cudaError_t ln_bwd_t(const float* du, const void* x, const float* mean, const float* rstd,
-                     const void* g, const void* resid, void* dx, float* dgamma, float* dbeta,
-                     float* partial, int n, int h, const LaunchCtx& c) {
+template <typename T, int MODE>
+cudaError_t ln_bwd_t(const float* du, const void* du2, const void* x, const float* mean,
+                     const float* rstd, const void* g, const void* resid, void* dx, float* dgamma,
+                     float* dbeta, float* partial, int n, int h, const LaunchCtx& c) {
   int vpt, threads;
   row_plan<T>(h, &vpt, &threads);
   const int nblk = n < kLnBwdBlocks ? (n > 0 ? n : 1) : kLnBwdBlocks;
@@ -365,14 +377,14 @@ cudaError_t ln_bwd_t(const float* du, const void* x, const float* mean, const fl
 #define LN_BWD_CASE(VV, RR)                                                                 \
   case VV:                                                                                  \
     if (smem > 48 * 1024) {                                                                 \
-      cudaError_t fe = cudaFuncSetAttribute(ln_bwd_kernel<T, VV, RR>,                       \
+      cudaError_t fe = cudaFuncSetAttribute(ln_bwd_kernel<T, VV, RR, MODE>,                 \
                                             cudaFuncAttributeMaxDynamicSharedMemorySize,    \
                                             (int)smem);                                     \
       if (fe != cudaSuccess) return fe;                                                     \
     }                                                                                       \
-    ln_bwd_kernel<T, VV, RR><<<nblk, threads, smem, c.stream>>>(                            \
-        du, (const T*)x, mean, rstd, (const T*)g, (const T*)resid, (T*)dx, pg, pb, n, h,    \
-        rows);                                                                              \
+    ln_bwd_kernel<T, VV, RR, MODE><<<nblk, threads, smem, c.stream>>>(                      \
+        du, (const T*)du2, (const T*)x, mean, rstd, (const T*)g, (const T*)resid, (T*)dx,   \
+        pg, pb, n, h, rows);                                                                \
     break;
   switch (vpt) {
     LN_BWD_CASE(1, 1)
@@ -456,9 +468,91 @@ cudaError_t ln_bwd(int dtype, const float* du, const void* x, const float* mean,
                    const float* rstd, const void* g, const void* resid, void* dx,
                    float* dgamma, float* dbeta, float* partial, int n, int h,
                    const LaunchCtx& c) {
-  return dtype == kBF16
-             ? ln_bwd_t<bf16>(du, x, mean, rstd, g, resid, dx, dgamma, dbeta, partial, n, h, c)
-             : ln_bwd_t<float>(du, x, mean, rstd, g, resid, dx, dgamma, dbeta, partial, n, h, c);
+  return dtype == kBF16 ? ln_bwd_t<bf16, 0>(du, nullptr, x, mean, rstd, g, resid, dx, dgamma,
+                                            dbeta, partial, n, h, c)
+                        : ln_bwd_t<float, 0>(du, nullptr, x, mean, rstd, g, resid, dx, dgamma,
+                                             dbeta, partial, n, h, c);
+}
+
+cudaError_t ln_bwd_sum(int dtype, const float* du, const void* du2, const void* x,
+                       const float* mean, const float* rstd, const void* g, void* dx,
+                       float* dgamma, float* dbeta, float* partial, int n, int h,
+                       const LaunchCtx& c) {
+  if (!du2) return cudaErrorInvalidValue;
+  if (dtype == kBF16)
+    return du ? ln_bwd_t<bf16, 2>(du, du2, x, mean, rstd, g, nullptr, dx, dgamma, dbeta, partial,
+                                  n, h, c)
+              : ln_bwd_t<bf16, 1>(nullptr, du2, x, mean, rstd, g, nullptr, dx, dgamma, dbeta,
+                                  partial, n, h, c);
+  return du ? ln_bwd_t<float, 2>(du, du2, x, mean, rstd, g, nullptr, dx, dgamma, dbeta, partial,
+                                 n, h, c)
+            : ln_bwd_t<float, 1>(nullptr, du2, x, mean, rstd, g, nullptr, dx, dgamma, dbeta,
+                                 partial, n, h, c);
+}
+
+// ---------------------------------------------------------------- recomputation
+// u = (x - mean) * rstd * gamma + beta from saved statistics: the same
+// arithmetic as ln_fwd_kernel's output, so the values match it bit for bit.
+template <typename T>
+__global__ void ln_apply_kernel(const T* __restrict__ x, const float* __restrict__ mean,
+                                const float* __restrict__ rstd, const T* __restrict__ gamma,
+                                const T* __restrict__ beta, T* __restrict__ u, int n, int h) {
+  constexpr int E = Vec<T>::N;
+  const int nvec = h / E;
+  for (int r = blockIdx.x; r < n; r += gridDim.x) {
+    const float mu = mean[r], rs = rstd[r];
+    for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+      Vec<T> xv, tg, tb, o;
+      xv.load(x + (size_t)r * h + vi * E);
+      tg.load(gamma + vi * E);
+      tb.load(beta + vi * E);
+#pragma unroll
+      for (int e = 0; e < E; ++e) o.set(e, (xv.get(e) - mu) * rs * tg.get(e) + tb.get(e));
+      o.store(u + (size_t)r * h + vi * E);
+    }
+  }
+}
+
+template <typename T>
+__global__ void gelu_apply_kernel(const T* __restrict__ z, T* __restrict__ a, int64_t nvec) {
+  constexpr int E = Vec<T>::N;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    Vec<T> v;
+    v.load(z + i * E);
+#pragma unroll
+    for (int e = 0; e < E; ++e) v.set(e, gelu_f(v.get(e)));
+    v.store(a + i * E);
+  }
+}
+
+cudaError_t ln_apply(int dtype, const void* x, const float* mean, const float* rstd,
+                     const void* g, const void* b, void* u, int n, int h, const LaunchCtx& c) {
+  if (n == 0) return cudaSuccess;
+  const int grid = n < 8 * c.num_sms ? n : 8 * c.num_sms;
+  c.before(KK_LN_FWD, (double)n * h * 2.0 * (dtype == kBF16 ? 2 : 4));
+  if (dtype == kBF16)
+    ln_apply_kernel<bf16><<<grid, 256, 0, c.stream>>>((const bf16*)x, mean, rstd, (const bf16*)g,
+                                                      (const bf16*)b, (bf16*)u, n, h);
+  else
+    ln_apply_kernel<float><<<grid, 256, 0, c.stream>>>((const float*)x, mean, rstd,
+                                                       (const float*)g, (const float*)b,
+                                                       (float*)u, n, h);
+  c.after();
+  return cudaGetLastError();
+}
+
+cudaError_t gelu_apply(int dtype, const void* z, void* a, int64_t count, const LaunchCtx& c) {
+  if (count == 0) return cudaSuccess;
+  const int64_t nvec = count / (dtype == kBF16 ? 8 : 4);
+  const int grid = 8 * c.num_sms;
+  c.before(KK_LN_FWD, (double)count * 2.0 * (dtype == kBF16 ? 2 : 4));
+  if (dtype == kBF16)
+    gelu_apply_kernel<bf16><<<grid, 256, 0, c.stream>>>((const bf16*)z, (bf16*)a, nvec);
+  else
+    gelu_apply_kernel<float><<<grid, 256, 0, c.stream>>>((const float*)z, (float*)a, nvec);
+  c.after();
+  return cudaGetLastError();
 }
 
 cudaError_t colsum(int dtype, const void* Y, int64_t ld, int n, int N, float* out,

@@ -71,7 +71,9 @@ struct Dims {
   size_t esz;
   float p_attn, p_hidden;
   unsigned long long seed;
-  int fp8;   // 1: FP8 (E4M3) forward GEMMs
+  int fp8;        // 1: FP8 (E4M3) forward GEMMs
+  int post_ln;    // 1: Post-LN layer
+  int recompute;  // 1: LayerNorm outputs and GeLU(z) recomputed in the backward
 };
 
 // Dropout of one site: keep iff the Philox word >= floor(p * 2^32), scale 1/(1-p).
@@ -103,6 +105,8 @@ mtl_status validate(const mtl_layer_desc* desc, Dims* o) {
   if (!(d.p_attn >= 0.f && d.p_attn < 1.f) || !(d.p_hidden >= 0.f && d.p_hidden < 1.f))
     return MTL_ERR_INVALID_ARG;
   if (d.fp8 != 0 && d.fp8 != 1) return MTL_ERR_INVALID_ARG;
+  if ((d.post_ln != 0 && d.post_ln != 1) || (d.recompute != 0 && d.recompute != 1))
+    return MTL_ERR_INVALID_ARG;
   if (d.h % d.heads) return MTL_ERR_INVALID_ARG;
   if (d.heads % d.t || d.ffn % d.t) return MTL_ERR_INVALID_ARG;
   const int dh = d.h / d.heads;
@@ -130,6 +134,10 @@ mtl_status validate(const mtl_layer_desc* desc, Dims* o) {
   o->p_hidden = d.p_hidden;
   o->seed = d.seed;
   o->fp8 = d.fp8;
+  o->post_ln = d.post_ln;
+  o->recompute = d.recompute;
+  // the Post-LN variant runs without dropout and with bf16 / fp32 GEMMs
+  if (d.post_ln && (d.p_attn > 0.f || d.p_hidden > 0.f || d.fp8)) return MTL_ERR_UNSUPPORTED;
   if (d.fp8) {
     // FP8 GEMMs: bf16 layers without dropout, K partitions of whole 128s
     if (d.dtype != MTL_BF16 || d.p_attn > 0.f || d.p_hidden > 0.f) return MTL_ERR_UNSUPPORTED;
@@ -147,21 +155,27 @@ mtl_saved_layout saved_layout(const Dims& D) {
     return at;
   };
   const size_t nh = (size_t)D.n * D.h * D.esz;
+  const size_t nf = (size_t)D.n * D.f * D.esz;
+  const bool pre = !D.post_ln, rc = D.recompute != 0;
+  // Pre-LN saves u1, x1, u2 (u1, u2 recomputable); Post-LN saves h1, x1, h2 (x1
+  // recomputable); a = GeLU(z) is recomputable in both.
   L.mu1 = take((size_t)D.n * 4);
   L.rstd1 = take((size_t)D.n * 4);
-  L.u1 = take(nh);
+  L.u1 = take(pre && !rc ? nh : 0);
   L.qkv = take(3 * nh);
   L.ctx = take(nh);
   L.lse = take((size_t)D.batch * D.heads * D.seq * 4);
-  L.x1 = take(nh);
+  L.x1 = take(pre || !rc ? nh : 0);
   L.mu2 = take((size_t)D.n * 4);
   L.rstd2 = take((size_t)D.n * 4);
-  L.u2 = take(nh);
-  L.z = take((size_t)D.n * D.f * D.esz);
-  L.a = take((size_t)D.n * D.f * D.esz);
+  L.u2 = take(pre && !rc ? nh : 0);
+  L.z = take(nf);
+  L.a = take(rc ? 0 : nf);
   L.attn_mask = take(D.dtype == MTL_BF16 && D.p_attn > 0.f
                          ? attn_mask_bytes((int)D.batch, (int)D.seq, (int)D.heads)
                          : 0);
+  L.h1 = take(pre ? 0 : nh);
+  L.h2 = take(pre ? 0 : nh);
   L.total = off;
   return L;
 }
@@ -192,7 +206,7 @@ Fp8Ws fp8_ws_layout(const Dims& D) {
 
 // Backward scratch, after the status word.
 struct WsLayout {
-  size_t dz, du, dx1, dctx, dqkv, dsum, gmask, partial, fp8, total;
+  size_t dz, du, dx1, dctx, dqkv, dsum, gmask, partial, fp8, rc_h, rc_f, zero_h, total;
 };
 
 WsLayout ws_layout(const Dims& D) {
@@ -220,6 +234,11 @@ WsLayout ws_layout(const Dims& D) {
   if (pd > pf) pf = pd;
   W.partial = take(pf * 4);
   W.fp8 = take(fp8_ws_layout(D).total);
+  // recomputed activations ([n][h] and [n][ffn]); the forward keeps the ones it
+  // does not save here too
+  W.rc_h = take(D.recompute ? nh * D.esz : 0);
+  W.rc_f = take(D.recompute ? (size_t)D.n * D.f * D.esz : 0);
+  W.zero_h = take(D.post_ln ? (size_t)D.h * D.esz : 0);   // a zero bias (Post-LN dx GEMM)
   W.total = off;
   return W;
 }
@@ -301,7 +320,8 @@ size_t attn_ws_bytes(int32_t batch, int32_t seq, int32_t heads) {
 // The layer forward after validation (shared by mtl_layer_fwd and prefill):
 // intermediates go to `saved` at saved_layout(D).
 mtl_status forward_core(const Dims& D, float ln_eps, const mtl_weights* w, const void* x, void* y,
-                        void* saved, void* fp8ws, unsigned* status, const LaunchCtx& c) {
+                        void* saved, void* fp8ws, void* rc_h, void* rc_f, unsigned* status,
+                        const LaunchCtx& c) {
   const mtl_saved_layout L = saved_layout(D);
   // A GEMM of the forward: bf16 (or fp32) as given, or with FP8 layers each
   // operand quantized per tensor to E4M3 (own amax / scale slot) and the FP8
@@ -332,15 +352,68 @@ mtl_status forward_core(const Dims& D, float ln_eps, const mtl_weights* w, const
   };
   mtl_status gst;
   const int n = (int)D.n, h = (int)D.h, f = (int)D.f, t = (int)D.t;
-  void* u1 = at<char>(saved, L.u1);
+  // activations the backward recomputes live in the workspace during the forward
+  void* u1 = D.recompute ? rc_h : at<char>(saved, L.u1);
   void* qkv = at<char>(saved, L.qkv);
   void* ctx = at<char>(saved, L.ctx);
-  void* x1 = at<char>(saved, L.x1);
-  void* u2 = at<char>(saved, L.u2);
+  void* x1 = (D.post_ln && D.recompute) ? rc_h : at<char>(saved, L.x1);
+  void* u2 = D.recompute ? rc_h : at<char>(saved, L.u2);
   void* z = at<char>(saved, L.z);
-  void* a = at<char>(saved, L.a);
+  void* a = D.recompute ? rc_f : at<char>(saved, L.a);
   const bool bf = D.dtype == MTL_BF16;
   const Dropout drop_attn = make_drop(D.p_attn, D.seed, SITE_ATTN);
+
+  if (D.post_ln) {
+    // Post-LN: h1 = x + Attn(x); x1 = LN1(h1); h2 = x1 + MLP(x1); y = LN2(h2)
+    void* h1 = at<char>(saved, L.h1);
+    void* h2 = at<char>(saved, L.h2);
+    {
+      GemmArgs g = gemm_args(n, 3 * h, h, 1, x, h, true, w->w_qkv, h, true, EPI_BIAS, qkv, 3 * h,
+                             false, status);
+      g.bias = w->b_qkv;
+      MTL_TRY(run_gemm(D, g, c), "qkv gemm");
+    }
+    if (bf) {
+      MTL_TRY(attn_fwd_tc(qkv, ctx, at<float>(saved, L.lse), (int)D.batch, (int)D.seq,
+                          (int)D.heads, (int)D.d, drop_attn, nullptr, status, c),
+              "attention fwd");
+    } else {
+      MTL_TRY(attn_fwd_simt(D.dtype, qkv, ctx, at<float>(saved, L.lse), (int)D.batch, (int)D.seq,
+                            (int)D.heads, (int)D.d, drop_attn, c),
+              "attention fwd");
+    }
+    {
+      GemmArgs g = gemm_args(n, h, h, t, ctx, h, true, w->w_o, h, true, EPI_BIAS_RESID, h1, h,
+                             false, status);
+      g.bias = w->b_o;
+      g.R = x;
+      g.ldr = h;
+      MTL_TRY(run_gemm(D, g, c), "out-proj gemm");
+    }
+    MTL_TRY(ln_fwd(D.dtype, h1, w->ln1_g, w->ln1_b, x1, at<float>(saved, L.mu1),
+                   at<float>(saved, L.rstd1), n, h, ln_eps, c),
+            "ln1 fwd");
+    {
+      GemmArgs g = gemm_args(n, f, h, 1, x1, h, true, w->w_fc1, h, true, EPI_BIAS_GELU, a, f,
+                             false, status);
+      g.bias = w->b_fc1;
+      g.Z = z;
+      g.ldz = f;
+      MTL_TRY(run_gemm(D, g, c), "fc1 gemm");
+    }
+    {
+      GemmArgs g = gemm_args(n, h, f, t, a, f, true, w->w_fc2, f, true, EPI_BIAS_RESID, h2, h,
+                             false, status);
+      g.bias = w->b_fc2;
+      g.R = x1;
+      g.ldr = h;
+      MTL_TRY(run_gemm(D, g, c), "fc2 gemm");
+    }
+    MTL_TRY(ln_fwd(D.dtype, h2, w->ln2_g, w->ln2_b, y, at<float>(saved, L.mu2),
+                   at<float>(saved, L.rstd2), n, h, ln_eps, c),
+            "ln2 fwd");
+    return MTL_OK;
+  }
 
   // F1 LN1
   MTL_TRY(ln_fwd(D.dtype, x, w->ln1_g, w->ln1_b, u1, at<float>(saved, L.mu1),
@@ -413,6 +486,8 @@ mtl_status validate_decode(const mtl_layer_desc* desc, int32_t max_seq, Dims* o)
   d.p_attn = 0.f;
   d.p_hidden = 0.f;
   d.fp8 = 0;                                // decode GEMMs stay bf16
+  d.recompute = 0;
+  if (d.post_ln) return MTL_ERR_UNSUPPORTED;  // decode runs the Pre-LN layer
   mtl_status st = validate(&d, o);
   if (st != MTL_OK) return st;
   o->seq = 1;
@@ -520,7 +595,8 @@ mtl_status mtl_layer_fwd(const mtl_layer_desc* desc, const mtl_weights* w, const
   MTL_TRY(cudaMemsetAsync(status, 0, kStatusBytes, s), "status reset");
   if (D.n == 0) return MTL_OK;
 
-  return forward_core(D, desc->ln_eps, w, x, y, saved, at<char>(workspace, W.fp8), status, c);
+  return forward_core(D, desc->ln_eps, w, x, y, saved, at<char>(workspace, W.fp8),
+                      at<char>(workspace, W.rc_h), at<char>(workspace, W.rc_f), status, c);
 }
 
 mtl_status mtl_layer_bwd(const mtl_layer_desc* desc, const mtl_weights* w, const void* x,
@@ -552,6 +628,8 @@ mtl_status mtl_layer_bwd(const mtl_layer_desc* desc, const mtl_weights* w, const
   const void* u2 = at<char>(saved, L.u2);
   const void* z = at<char>(saved, L.z);
   const void* a = at<char>(saved, L.a);
+  void* rc_h = at<char>(workspace, W.rc_h);
+  void* rc_f = at<char>(workspace, W.rc_f);
   void* dz = at<char>(workspace, W.dz);
   float* du = at<float>(workspace, W.du);
   void* dx1 = at<char>(workspace, W.dx1);
@@ -568,6 +646,93 @@ mtl_status mtl_layer_bwd(const mtl_layer_desc* desc, const mtl_weights* w, const
                    (size_t)f * h,     (size_t)f,     (size_t)h * f, (size_t)h,
                    (size_t)h,         (size_t)h,     (size_t)h,     (size_t)h};
     for (int i = 0; i < 12; ++i) MTL_TRY(cudaMemsetAsync(zs[i], 0, sz[i] * 4, s), "zero grads");
+    return MTL_OK;
+  }
+
+  if (D.post_ln) {
+    // Post-LN backward.  Buffers: dh2 in dctx (dead once dh1 exists), dh1 in dx1.
+    const void* h1 = at<char>(saved, L.h1);
+    const void* h2 = at<char>(saved, L.h2);
+    void* dh2 = dctx;
+    void* dh1 = dx1;
+    const Dropout no_drop = make_drop(0.f, 0, SITE_ATTN);
+    if (D.recompute) {
+      MTL_TRY(ln_apply(D.dtype, h1, at<float>(saved, L.mu1), at<float>(saved, L.rstd1), w->ln1_g,
+                       w->ln1_b, rc_h, n, h, c),
+              "recompute x1");
+      MTL_TRY(gelu_apply(D.dtype, z, rc_f, (int64_t)n * f, c), "recompute a");
+      x1 = rc_h;
+      a = rc_f;
+    }
+    // P1 dh2 = LN2_bwd(dy); dgamma2, dbeta2
+    MTL_TRY(ln_bwd_sum(D.dtype, nullptr, dy, h2, at<float>(saved, L.mu2),
+                       at<float>(saved, L.rstd2), w->ln2_g, dh2, static_cast<float*>(gr->ln2_g),
+                       static_cast<float*>(gr->ln2_b), partial, n, h, c),
+            "ln2 bwd");
+    // MLP: dz = (dh2 W2) GeLU'(z); dW2 = dh2^T a; db2; du = sum_p dz W1 (f sum);
+    // dW1 = dz^T x1; db1
+    {
+      GemmArgs g = gemm_args(n, f, h, 1, dh2, h, true, w->w_fc2, f, false, EPI_DGELU, dz, f,
+                             false, status);
+      g.Z = const_cast<void*>(z);
+      g.ldz = f;
+      MTL_TRY(run_gemm(D, g, c), "fc2 dgrad");
+    }
+    MTL_TRY(run_gemm(D, gemm_args(h, f, n, 1, dh2, h, false, a, f, false, EPI_STORE, gr->w_fc2,
+                                  f, true, status),
+                     c),
+            "fc2 wgrad");
+    MTL_TRY(colsum(D.dtype, dh2, h, n, h, static_cast<float*>(gr->b_fc2), partial, c), "db_fc2");
+    MTL_TRY(run_gemm(D, gemm_args(n, h, f, t, dz, f, true, w->w_fc1, h, false, EPI_STORE, du, h,
+                                  true, status),
+                     c),
+            "fc1 dgrad");
+    MTL_TRY(run_gemm(D, gemm_args(f, h, n, 1, dz, f, false, x1, h, false, EPI_STORE, gr->w_fc1, h,
+                                  true, status),
+                     c),
+            "fc1 wgrad");
+    MTL_TRY(colsum(D.dtype, dz, f, n, f, static_cast<float*>(gr->b_fc1), partial, c), "db_fc1");
+    // P5 dh1 = LN1_bwd(dh2 + du); dgamma1, dbeta1
+    MTL_TRY(ln_bwd_sum(D.dtype, du, dh2, h1, at<float>(saved, L.mu1), at<float>(saved, L.rstd1),
+                       w->ln1_g, dh1, static_cast<float*>(gr->ln1_g),
+                       static_cast<float*>(gr->ln1_b), partial, n, h, c),
+            "ln1 bwd");
+    // attention block: dW_o = dh1^T ctx; db_o; dctx = dh1 W_o; attention; dW_qkv = dqkv^T x
+    MTL_TRY(colsum(D.dtype, dh1, h, n, h, static_cast<float*>(gr->b_o), partial, c), "db_o");
+    MTL_TRY(run_gemm(D, gemm_args(h, h, n, 1, dh1, h, false, ctx, h, false, EPI_STORE, gr->w_o, h,
+                                  true, status),
+                     c),
+            "out-proj wgrad");
+    MTL_TRY(run_gemm(D, gemm_args(n, h, h, 1, dh1, h, true, w->w_o, h, false, EPI_STORE, dctx, h,
+                                  false, status),
+                     c),
+            "out-proj dgrad");
+    if (D.dtype == MTL_BF16) {
+      MTL_TRY(attn_bwd_tc(qkv, ctx, at<float>(saved, L.lse), dctx, dqkv, dsum, (int)D.batch,
+                          (int)D.seq, (int)D.heads, (int)D.d, no_drop, nullptr, status, c),
+              "attention bwd");
+    } else {
+      MTL_TRY(attn_bwd_simt(D.dtype, qkv, ctx, at<float>(saved, L.lse), dctx, dqkv, dsum,
+                            (int)D.batch, (int)D.seq, (int)D.heads, (int)D.d, no_drop, c),
+              "attention bwd");
+    }
+    MTL_TRY(run_gemm(D, gemm_args(3 * h, h, n, 1, dqkv, 3 * h, false, x, h, false, EPI_STORE,
+                                  gr->w_qkv, h, true, status),
+                     c),
+            "qkv wgrad");
+    MTL_TRY(colsum(D.dtype, dqkv, 3 * h, n, 3 * h, static_cast<float*>(gr->b_qkv), partial, c),
+            "db_qkv");
+    // dx = dh1 + sum_p dqkv[:, Q_p] W_qkv[Q_p, :]  (the f sum, residual in the epilogue)
+    {
+      void* zero_h = at<char>(workspace, W.zero_h);
+      MTL_TRY(cudaMemsetAsync(zero_h, 0, (size_t)h * D.esz, s), "zero bias");
+      GemmArgs g = gemm_args(n, h, 3 * h, t, dqkv, 3 * h, true, w->w_qkv, h, false,
+                             EPI_BIAS_RESID, dx, h, false, status);
+      g.bias = zero_h;
+      g.R = dh1;
+      g.ldr = h;
+      MTL_TRY(run_gemm(D, g, c), "qkv dgrad");
+    }
     return MTL_OK;
   }
 
@@ -593,7 +758,11 @@ mtl_status mtl_layer_bwd(const mtl_layer_desc* desc, const mtl_weights* w, const
     g.ldz = f;
     MTL_TRY(run_gemm(D, g, c), "fc2 dgrad");
   }
-  // B2 fc2 wgrad dW2 = g2^T a
+  // B2 fc2 wgrad dW2 = g2^T a  (a recomputed as GeLU(z) when not saved)
+  if (D.recompute) {
+    MTL_TRY(gelu_apply(D.dtype, z, rc_f, (int64_t)n * f, c), "recompute a");
+    a = rc_f;
+  }
   MTL_TRY(run_gemm(D, gemm_args(h, f, n, 1, g2, h, false, a, f, false, EPI_STORE, gr->w_fc2, f,
                                 true, status),
                    c),
@@ -603,7 +772,14 @@ mtl_status mtl_layer_bwd(const mtl_layer_desc* desc, const mtl_weights* w, const
                                 true, status),
                    c),
           "fc1 dgrad");
-  // B4 fc1 wgrad dW1 = dz^T u2, db1 = sum_rows dz
+  // B4 fc1 wgrad dW1 = dz^T u2, db1 = sum_rows dz  (u2 recomputed from x1 and the
+  // saved statistics when not saved)
+  if (D.recompute) {
+    MTL_TRY(ln_apply(D.dtype, x1, at<float>(saved, L.mu2), at<float>(saved, L.rstd2), w->ln2_g,
+                     w->ln2_b, rc_h, n, h, c),
+            "recompute u2");
+    u2 = rc_h;
+  }
   MTL_TRY(run_gemm(D, gemm_args(f, h, n, 1, dz, f, false, u2, h, false, EPI_STORE, gr->w_fc1, h,
                                 true, status),
                    c),
@@ -644,7 +820,14 @@ mtl_status mtl_layer_bwd(const mtl_layer_desc* desc, const mtl_weights* w, const
                           (int)D.batch, (int)D.seq, (int)D.heads, (int)D.d, drop_attn, c),
             "attention bwd");
   }
-  // B8 QKV wgrad dW_qkv = dqkv^T u1, db_qkv = sum_rows dqkv
+  // B8 QKV wgrad dW_qkv = dqkv^T u1, db_qkv = sum_rows dqkv  (u1 recomputed from x
+  // and the saved statistics when not saved)
+  if (D.recompute) {
+    MTL_TRY(ln_apply(D.dtype, x, at<float>(saved, L.mu1), at<float>(saved, L.rstd1), w->ln1_g,
+                     w->ln1_b, rc_h, n, h, c),
+            "recompute u1");
+    u1 = rc_h;
+  }
   MTL_TRY(run_gemm(D, gemm_args(3 * h, h, n, 1, dqkv, 3 * h, false, u1, h, false, EPI_STORE,
                                 gr->w_qkv, h, true, status),
                    c),
@@ -808,6 +991,7 @@ mtl_status mtl_infer_sizes(const mtl_layer_desc* desc, int32_t max_seq, size_t* 
     mtl_layer_desc pd = *desc;
     pd.p_attn = 0.f;
     pd.p_hidden = 0.f;
+    pd.recompute = 0;
     st = validate(&pd, &P);
     if (st != MTL_OK) return st;
     if (pd.seq > max_seq) return MTL_ERR_INVALID_ARG;
@@ -823,8 +1007,10 @@ mtl_status mtl_layer_prefill(const mtl_layer_desc* desc, const mtl_weights* w, c
   g_cuda_err[0] = 0;
   if (!desc) return MTL_ERR_INVALID_ARG;
   if (desc->p_attn != 0.f || desc->p_hidden != 0.f) return MTL_ERR_INVALID_ARG;
+  mtl_layer_desc pdesc = *desc;
+  pdesc.recompute = 0;   // nothing is kept for a backward
   Dims D;
-  mtl_status st = validate(desc, &D);
+  mtl_status st = validate(&pdesc, &D);
   if (st != MTL_OK) return st;
   if (max_seq < desc->seq) return MTL_ERR_INVALID_ARG;
   if (!weights_ok(w) || !aligned16(x) || !aligned16(y) || !aligned16(kv_cache) ||
@@ -841,7 +1027,8 @@ mtl_status mtl_layer_prefill(const mtl_layer_desc* desc, const mtl_weights* w, c
   if (D.n == 0) return MTL_OK;
   void* saved = at<char>(workspace, kStatusBytes);
   st = forward_core(D, desc->ln_eps, w, x, y, saved,
-                    at<char>(workspace, kStatusBytes + saved_layout(D).total), status, c);
+                    at<char>(workspace, kStatusBytes + saved_layout(D).total), nullptr, nullptr,
+                    status, c);
   if (st != MTL_OK) return st;
   const size_t half = kv_cache_bytes(D, max_seq) / 2;
   MTL_TRY(kv_write(D.dtype, at<char>(saved, saved_layout(D).qkv), kv_cache,

@@ -13,7 +13,7 @@ import os
 PARAM_NAMES = ("w_qkv", "b_qkv", "w_o", "b_o", "w_fc1", "b_fc1", "w_fc2", "b_fc2",
                "ln1_g", "ln1_b", "ln2_g", "ln2_b")
 SAVED_NAMES = ("mu1", "rstd1", "u1", "qkv", "ctx", "lse", "x1", "mu2", "rstd2", "u2", "z", "a",
-               "attn_mask")
+               "attn_mask", "h1", "h2")
 
 F32, BF16 = 0, 1
 STATUS = {0: "MTL_OK", 1: "MTL_ERR_INVALID_ARG", 2: "MTL_ERR_UNSUPPORTED",
@@ -36,7 +36,7 @@ class LayerDesc(ctypes.Structure):
                 ("batch", ctypes.c_int32), ("ffn", ctypes.c_int32), ("t", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("ln_eps", ctypes.c_float), ("causal", ctypes.c_int32),
                 ("p_attn", ctypes.c_float), ("p_hidden", ctypes.c_float), ("seed", ctypes.c_uint64),
-                ("fp8", ctypes.c_int32)]
+                ("fp8", ctypes.c_int32), ("post_ln", ctypes.c_int32), ("recompute", ctypes.c_int32)]
 
 
 class Weights(ctypes.Structure):
@@ -123,12 +123,13 @@ def _stream(stream):
 
 
 def layer_desc(h, heads, seq, batch, ffn, t, dtype, ln_eps=1e-5, causal=1, p_attn=0.0,
-               p_hidden=0.0, seed=0, fp8=0) -> LayerDesc:
+               p_hidden=0.0, seed=0, fp8=0, post_ln=0, recompute=0) -> LayerDesc:
     """mtl_layer_desc; p_attn / p_hidden / seed: dropout probabilities and Philox seed;
-    fp8=1: FP8 (E4M3) forward GEMMs."""
+    fp8=1: FP8 (E4M3) forward GEMMs; post_ln=1: Post-LN layer; recompute=1:
+    selective recomputation of the LayerNorm outputs and GeLU(z)."""
     dt = {"f32": F32, "bf16": BF16, F32: F32, BF16: BF16}[dtype]
     return LayerDesc(h, heads, seq, batch, ffn, t, dt, ln_eps, causal, p_attn, p_hidden, seed,
-                     fp8)
+                     fp8, post_ln, recompute)
 
 
 def layer_sizes(desc: LayerDesc):
@@ -335,14 +336,20 @@ def saved_views(desc: LayerDesc, saved):
     dt = torch_dtype(desc)
     esz = 2 if desc.dtype == BF16 else 4
 
+    # fields are laid out in SAVED_NAMES order: a field's bytes end where the next begins
+    names = SAVED_NAMES + ("total",)
+    size = {k: lay[names[i + 1]] - lay[k] for i, k in enumerate(names[:-1])}
+
     def view(name, shape, dtype, elsize):
         cnt = 1
         for s in shape:
             cnt *= s
         off = lay[name]
+        if size[name] < cnt * elsize:
+            return None                       # not saved in this configuration
         return saved[off:off + cnt * elsize].view(dtype).view(*shape)
 
-    return {
+    views = {
         "mu1": view("mu1", (n,), torch.float32, 4), "rstd1": view("rstd1", (n,), torch.float32, 4),
         "u1": view("u1", (n, h), dt, esz), "qkv": view("qkv", (n, 3 * h), dt, esz),
         "ctx": view("ctx", (n, h), dt, esz),
@@ -350,4 +357,6 @@ def saved_views(desc: LayerDesc, saved):
         "x1": view("x1", (n, h), dt, esz), "mu2": view("mu2", (n,), torch.float32, 4),
         "rstd2": view("rstd2", (n,), torch.float32, 4), "u2": view("u2", (n, h), dt, esz),
         "z": view("z", (n, f), dt, esz), "a": view("a", (n, f), dt, esz),
+        "h1": view("h1", (n, h), dt, esz), "h2": view("h2", (n, h), dt, esz),
     }
+    return {k: v for k, v in views.items() if v is not None}

@@ -40,7 +40,8 @@ def f32(v):
     return float(np.float32(v))
 
 
-def run_gpu(shape, x, p, dy, t, runs=1, want_saved=True, drop=None, fp8=0):
+def run_gpu(shape, x, p, dy, t, runs=1, want_saved=True, drop=None, fp8=0, post_ln=0,
+            recompute=0):
     """Forward + backward through the C ABI.  Returns a dict of float64 arrays.
 
     drop: optional dict(p_attn, p_hidden, seed) of float32-exact probabilities."""
@@ -50,7 +51,8 @@ def run_gpu(shape, x, p, dy, t, runs=1, want_saved=True, drop=None, fp8=0):
     drop = drop or {}
     desc = mtl.layer_desc(shape.h, shape.heads, shape.seq, b, shape.ffn, t, shape.dtype,
                           p_attn=drop.get("p_attn", 0.0), p_hidden=drop.get("p_hidden", 0.0),
-                          seed=drop.get("seed", 0), fp8=fp8)
+                          seed=drop.get("seed", 0), fp8=fp8, post_ln=post_ln,
+                          recompute=recompute)
     dev_p = {k: to_device(v, shape.dtype) for k, v in p.items()}
     xd = to_device(x, shape.dtype)
     dyd = to_device(dy, shape.dtype)
@@ -80,6 +82,17 @@ def run_oracle(shape, x, p, dy, drop=None, fp8=False):
     out = {"y": y, "dx": dx}
     out.update({"d_" + k: v for k, v in g.items()})
     for k in ("u1", "qkv", "ctx", "lse", "x1", "u2", "z", "a", "mu1", "rstd1", "mu2", "rstd2"):
+        out["s_" + k] = cache[k]
+    return out
+
+
+def run_oracle_post_ln(shape, x, p, dy):
+    """The oracle's Post-LN layer, keyed like run_gpu (saved x1 = LN1 output)."""
+    y, cache = oracle.layer_fwd_post_ln(p, x, shape.heads)
+    dx, g, _ = oracle.layer_bwd_post_ln(p, cache, dy)
+    out = {"y": y, "dx": dx}
+    out.update({"d_" + k: v for k, v in g.items()})
+    for k in ("qkv", "ctx", "lse", "x1", "z", "a", "h1", "h2", "mu1", "rstd1", "mu2", "rstd2"):
         out["s_" + k] = cache[k]
     return out
 

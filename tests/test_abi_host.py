@@ -304,3 +304,19 @@ def test_fp8_layer_validation(mtl):
                    (dict(fp8=1, t=4), 2)):                      # h/t = 64: not whole 128s
         d = good_desc(mtl, **kw)
         assert L.mtl_layer_sizes(ctypes.byref(d), None, None) == st, kw
+
+
+def test_variant_validation(mtl):
+    L = mtl.lib()
+    for kw, st in ((dict(post_ln=2), 1), (dict(recompute=-1), 1),
+                   (dict(post_ln=1, p_hidden=0.1), 2), (dict(post_ln=1, fp8=1), 2)):
+        d = good_desc(mtl, **kw)
+        assert L.mtl_layer_sizes(ctypes.byref(d), None, None) == st, kw
+    base, rc = good_desc(mtl), good_desc(mtl, recompute=1)
+    n, h, f = 256, 256, 1024
+    assert mtl.layer_sizes(base)[0] - mtl.layer_sizes(rc)[0] == (2 * n * h + n * f) * 2
+    post = mtl.layer_saved_layout(good_desc(mtl, post_ln=1))
+    assert post["qkv"] == post["u1"] and post["h2"] - post["h1"] >= n * h * 2
+    d = good_desc(mtl, post_ln=1)
+    s = ctypes.c_size_t()
+    assert L.mtl_infer_sizes(ctypes.byref(d), 512, ctypes.byref(s), None, None) == 2  # no decode
