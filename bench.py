@@ -451,8 +451,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--p-drop", type=float, default=0.0,
                     help="dropout probability of the attention and hidden sites (default 0)")
-    ap.add_argument("--fp8", action="store_true",
-                    help="FP8 (E4M3, per-tensor scaled) forward GEMMs; backward in bf16")
+    ap.add_argument("--fp8", nargs="?", const="fwd", choices=["fwd", "hybrid"], default=None,
+                    help="FP8 GEMMs: fwd = E4M3 forward, bf16 backward; hybrid = also the "
+                         "backward in FP8 (E5M2 gradients x E4M3)")
     ap.add_argument("--post-ln", action="store_true", help="Post-LN (original BERT) layer")
     ap.add_argument("--recompute", action="store_true",
                     help="selective recomputation of the LayerNorm outputs and GeLU(z)")
@@ -495,7 +496,8 @@ def main():
     desc = mtl.layer_desc(shape.h, shape.heads, shape.seq, shape.batch, shape.ffn, args.t,
                           shape.dtype, p_attn=drop.get("p_attn", 0.0),
                           p_hidden=drop.get("p_hidden", 0.0), seed=drop.get("seed", 0),
-                          fp8=1 if args.fp8 else 0, post_ln=1 if args.post_ln else 0,
+                          fp8={None: 0, "fwd": 1, "hybrid": 2}[args.fp8],
+                          post_ln=1 if args.post_ln else 0,
                           recompute=1 if args.recompute else 0)
     w = {k: torch.from_numpy(v).cuda().to(dt) for k, v in p.items()}
     x_h = torch.from_numpy(x).to(dt).pin_memory()
@@ -670,7 +672,9 @@ def main():
                    "l2": "inputs larger than L2 (no flush)",
                    "flops_per_step": flops, "megatron_flops_per_step": megatron_flops(shape),
                    "dropout": args.drop,
-                   "gemm_precision": "fp8 e4m3 forward, bf16 backward" if args.fp8 else "bf16",
+                   "gemm_precision": {None: "bf16", "fwd": "fp8 e4m3 forward, bf16 backward",
+                                      "hybrid": "fp8 hybrid: e4m3 forward, e5m2 x e4m3 "
+                                                "backward"}[args.fp8],
                    "layer": "post-ln" if args.post_ln else "pre-ln",
                    "recompute": bool(args.recompute),
                    "saved_bytes": saved.numel()},

@@ -105,7 +105,10 @@ typedef struct {
   uint64_t seed;     /* Philox key of the dropout masks */
   int32_t fp8;       /* 1: the forward's four GEMMs take per-tensor E4M3 operands
                         (bf16 layers without dropout, h, h/t and ffn/t multiples
-                        of 128; the backward and decode stay bf16); 0: bf16 */
+                        of 128; the backward and decode stay bf16); 2: "hybrid",
+                        also the backward's eight GEMMs in FP8, E5M2 gradient x
+                        E4M3 activation or weight ((3h)/t a multiple of 128
+                        too); 0: bf16 */
   int32_t post_ln;   /* 1: Post-LN layer (original BERT, page section "Paper 1:
                         BERT LayerNorm Rearrangement"): h1 = x + Attn(x),
                         x1 = LN1(h1), h2 = x1 + MLP(x1), y = LN2(h2), with the
@@ -142,6 +145,11 @@ typedef struct {
                          [n][h] (mu1 / rstd1 and mu2 / rstd2 are their statistics;
                          u1, u2 are empty); Pre-LN: empty.  With recompute, u1, u2
                          (Pre-LN), x1 (Post-LN) and a are empty. */
+  size_t fp8;         /* FP8 hybrid (desc.fp8 = 2): 16 fp32 scales, then the E4M3
+                         transposes of u1, ctx, u2 [h][n] and a [f][n] and of
+                         W_qkv [h][3h], W_o [h][h], W_fc1 [h][f], W_fc2 [f][h]
+                         (each 256-byte aligned), which the backward reads in
+                         place of u1, u2 and a (then empty); otherwise empty. */
   size_t total;
 } mtl_saved_layout;
 
@@ -266,8 +274,10 @@ mtl_status mtl_layer_decode(const mtl_layer_desc* desc, const mtl_weights* w, co
  *   amax = max |x| over the whole matrix, *scale = fmt_max / amax (1 if
  *   amax = 0; fmt_max 448 for E4M3, 57344 for E5M2), q [rows][cols] bytes
  *   (row pitch ldq) = fp8(float32(x * scale)), rounded to nearest even and
- *   saturated to +-fmt_max.  scale: a DEVICE float.  cols and ldq multiples of
- *   16; workspace >= 256 bytes (status word and the amax word).
+ *   saturated to +-fmt_max, and / or its transpose qT [cols][rows] (row pitch
+ *   ldqT; for a K-major operand of a transposed use).  Either q or qT may be
+ *   NULL, not both.  scale: a DEVICE float.  cols, ldq (and with qT: rows,
+ *   ldqT) multiples of 16; workspace >= 256 bytes (status and amax words).
  * mtl_gemm_fp8: as mtl_gemm with K-major FP8 operands A [M][K] (lda) and
  *   B [N][K] (ldb) of formats fmt_a / fmt_b and their DEVICE scales; the
  *   partition partials (k_parts, each a multiple of 128 deep) are summed in
@@ -275,8 +285,9 @@ mtl_status mtl_layer_decode(const mtl_layer_desc* desc, const mtl_weights* w, co
  *   epilogue applies (same epilogue codes and C / R / Z conventions).  lda and
  *   ldb multiples of 16.  Runs on the 2-CTA tcgen05 kernel (kind::f8f6f4). */
 mtl_status mtl_fp8_quantize(int32_t src_dtype, const void* x, int64_t rows, int64_t cols,
-                            int64_t ld, int32_t fmt, void* q, int64_t ldq, float* scale,
-                            void* workspace, size_t ws_bytes, mtl_stream stream);
+                            int64_t ld, int32_t fmt, void* q, int64_t ldq, void* qT,
+                            int64_t ldqT, float* scale, void* workspace, size_t ws_bytes,
+                            mtl_stream stream);
 mtl_status mtl_gemm_fp8(int32_t M, int32_t N, int32_t K, int32_t k_parts, const void* A,
                         int64_t lda, int32_t fmt_a, const float* scale_a, const void* B,
                         int64_t ldb, int32_t fmt_b, const float* scale_b, int32_t epi,

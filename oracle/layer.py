@@ -261,9 +261,11 @@ def layer_fwd(params, x, heads, eps=LN_EPS, dropout=None, fp8=False):
     Transformer Kernels") after the out-projection and after fc2:
     x1 = x + drop(ctx W_o^T + b_o), y = x1 + drop(a W_fc2^T + b_fc2); masks as
     in oracle/philox.py.
-    fp8=True: the four GEMMs take per-tensor E4M3 operands (activation and
-    weight quantized as in oracle/fp8.py); LayerNorm, attention, GeLU, biases
-    and residuals stay in high precision.
+    fp8=True (or 1): the four GEMMs take per-tensor E4M3 operands (activation
+    and weight quantized as in oracle/fp8.py); LayerNorm, attention, GeLU,
+    biases and residuals stay in high precision.  fp8=2 ("hybrid"): the same
+    forward, and layer_bwd's eight GEMMs take an E5M2 gradient and an E4M3
+    activation or weight.
     """
     if fp8 and dropout:
         raise ValueError("FP8 forward is defined without dropout")
@@ -285,7 +287,8 @@ def layer_fwd(params, x, heads, eps=LN_EPS, dropout=None, fp8=False):
     y = x1 + _lin(a, p["w_fc2"], p["b_fc2"], fp8) * s2
     cache = dict(x=xf, u1=u1, mu1=mu1, rstd1=rstd1, qkv=qkv, ctx=ctx, lse=lse,
                  probs=probs, x1=x1, u2=u2, mu2=mu2, rstd2=rstd2, z=z, a=a,
-                 batch=batch, seq=seq, heads=heads, dropout=dropout, so=so, s2=s2)
+                 batch=batch, seq=seq, heads=heads, dropout=dropout, so=so, s2=s2,
+                 fp8=int(fp8))
     return y.reshape(batch, seq, h), cache
 
 
@@ -301,28 +304,38 @@ def layer_bwd(params, cache, dy):
     d = h // heads
     dy = _f64(dy).reshape(n, h)
     drop = c.get("dropout")
+    hybrid = c.get("fp8", 0) == 2
+
+    def mm(A, Bt):
+        """A Bt^T: in fp64, or (hybrid FP8) with A quantized to E5M2 (the
+        gradient side) and Bt to E4M3, each per tensor."""
+        if not hybrid:
+            return A @ Bt.T
+        from . import fp8 as _fp8
+        return _fp8.gemm(A, Bt, "e5m2", "e4m3")[0]
+
     g = {}
     # MLP block: y = x1 + drop(GeLU(u2 W1^T + b1) W2^T + b2)
     g2 = dy * c.get("s2", 1.0)
-    g["w_fc2"] = g2.T @ c["a"]
+    g["w_fc2"] = mm(g2.T, c["a"].T)
     g["b_fc2"] = g2.sum(axis=0)
-    da = g2 @ p["w_fc2"]
+    da = mm(g2, p["w_fc2"].T)
     dz = da * gelu_grad(c["z"])
-    g["w_fc1"] = dz.T @ c["u2"]
+    g["w_fc1"] = mm(dz.T, c["u2"].T)
     g["b_fc1"] = dz.sum(axis=0)
-    du2 = dz @ p["w_fc1"]
+    du2 = mm(dz, p["w_fc1"].T)
     dx1_ln, g["ln2_g"], g["ln2_b"] = layernorm_bwd(du2, c["x1"], c["mu2"], c["rstd2"],
                                                    p["ln2_g"])
     dx1 = dy + dx1_ln
     # attention block: x1 = x + drop(Attn(u1 W_qkv^T + b_qkv) W_o^T + b_o)
     go = dx1 * c.get("so", 1.0)
-    g["w_o"] = go.T @ c["ctx"]
+    g["w_o"] = mm(go.T, c["ctx"].T)
     g["b_o"] = go.sum(axis=0)
-    dctx = go @ p["w_o"]
+    dctx = mm(go, p["w_o"].T)
     dqkv = multihead_bwd(c["qkv"], c["ctx"], c["probs"], dctx, batch, seq, heads, d, drop)
-    g["w_qkv"] = dqkv.T @ c["u1"]
+    g["w_qkv"] = mm(dqkv.T, c["u1"].T)
     g["b_qkv"] = dqkv.sum(axis=0)
-    du1 = dqkv @ p["w_qkv"]
+    du1 = mm(dqkv, p["w_qkv"].T)
     dx_ln, g["ln1_g"], g["ln1_b"] = layernorm_bwd(du1, c["x"], c["mu1"], c["rstd1"],
                                                   p["ln1_g"])
     dx = dx1 + dx_ln

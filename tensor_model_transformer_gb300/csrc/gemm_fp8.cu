@@ -87,6 +87,71 @@ __global__ void __launch_bounds__(QTHREADS) cast_kernel(const T* __restrict__ x,
   }
 }
 
+// qT = fp8(x * scale) transposed: qT[c][r] for x [rows][cols], and optionally
+// the row-major q from the same read.  A CTA converts a 64 x 64 tile row-wise
+// into a byte tile in shared memory (16 elements per thread; those 16 bytes
+// also go to q), then writes it column-wise: 16 consecutive rows of one column
+// make one 16-byte store of an output row.  rows % 16 == 0.
+constexpr int CT = 64;
+template <typename T, int FMT>
+__global__ void __launch_bounds__(QTHREADS) cast_transpose_kernel(
+    const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
+    const unsigned* __restrict__ amax_bits, float* __restrict__ scale_out,
+    uint8_t* __restrict__ qT, int64_t ldqT, uint8_t* __restrict__ q, int64_t ldq) {
+  constexpr int E = Vec<T>::N;
+  __shared__ __align__(16) uint8_t tile[CT][CT + 16];   // rows of 80 bytes: 16-byte aligned
+  const float amax = __uint_as_float(*amax_bits);
+  const float maxv = FMT == 0 ? 448.0f : 57344.0f;
+  const float scale = amax > 0.f ? __fdiv_rn(maxv, amax) : 1.0f;
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *scale_out = scale;
+  const __nv_fp8_interpretation_t kind = FMT == 0 ? __NV_E4M3 : __NV_E5M2;
+  const int64_t r0 = (int64_t)blockIdx.y * CT, c0 = (int64_t)blockIdx.x * CT;
+  // load: thread -> (row tr, 16 columns from tc)
+  {
+    const int tr = threadIdx.x >> 2, tc = (threadIdx.x & 3) * 16;
+    const int64_t r = r0 + tr, c = c0 + tc;
+    float f[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) f[i] = 0.f;
+    if (r < rows && c < cols) {   // cols % 16 == 0: the 16 columns are all in range
+#pragma unroll
+      for (int j = 0; j < 16 / E; ++j) {
+        Vec<T> v;
+        v.load(x + r * ld + c + j * E);
+#pragma unroll
+        for (int e = 0; e < E; ++e) f[j * E + e] = __fmul_rn(v.get(e), scale);
+      }
+    }
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(f[4 * k], f[4 * k + 1]),
+                                                   __NV_SATFINITE, kind);
+      const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(f[4 * k + 2], f[4 * k + 3]),
+                                                   __NV_SATFINITE, kind);
+      w[k] = (lo & 0xFFFFu) | (hi << 16);
+    }
+    *reinterpret_cast<uint4*>(&tile[tr][tc]) = make_uint4(w[0], w[1], w[2], w[3]);
+    if (q && r < rows && c < cols)
+      *reinterpret_cast<uint4*>(q + r * ldq + c) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  __syncthreads();
+  // store: thread -> (output row oc = tile column, 16 rows from orr)
+  {
+    const int oc = threadIdx.x >> 2, orr = (threadIdx.x & 3) * 16;
+    const int64_t c = c0 + oc, r = r0 + orr;
+    if (c < cols && r < rows) {
+      uint32_t w[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        w[k] = (uint32_t)tile[orr + 4 * k][oc] | ((uint32_t)tile[orr + 4 * k + 1][oc] << 8) |
+               ((uint32_t)tile[orr + 4 * k + 2][oc] << 16) |
+               ((uint32_t)tile[orr + 4 * k + 3][oc] << 24);
+      *reinterpret_cast<uint4*>(qT + c * ldqT + r) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
 }  // namespace f8
 
 namespace tcg {
@@ -178,6 +243,47 @@ cudaError_t gemm_fp8(const GemmArgs& a, const LaunchCtx& c) {
   const int grid = 2 * (p.num_tiles < pairs ? p.num_tiles : pairs);
   c.before(KK_GEMM_FP8, 2.0 * a.M * a.N * a.K);
   fn<<<grid, THREADS, P_SMEM_BYTES, c.stream>>>(ma, mb, p);
+  c.after();
+  return cudaGetLastError();
+}
+
+cudaError_t fp8_quantize2(int src_dtype, const void* x, int64_t rows, int64_t cols, int64_t ld,
+                          int fmt, unsigned* amax_bits, float* scale, void* q, int64_t ldq,
+                          void* qT, int64_t ldqT, const LaunchCtx& c) {
+  using namespace f8;
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  if (cols % 16 || rows % 16 || (fmt != 0 && fmt != 1)) return cudaErrorInvalidValue;
+  cudaError_t e;
+  if (!qT) {
+    // amax, then the row-major cast (which also writes the scale)
+    return fp8_quantize(src_dtype, x, rows, cols, ld, fmt, amax_bits, scale, q, ldq, c);
+  }
+  {
+    const int64_t want = 4LL * c.num_sms;
+    const int grid = (int)(rows < want ? rows : want);
+    c.before(KK_QUANT, (double)rows * cols * (src_dtype == kBF16 ? 2 : 4));
+    if (src_dtype == kBF16)
+      amax_kernel<bf16><<<grid, QTHREADS, 0, c.stream>>>(static_cast<const bf16*>(x), rows, cols,
+                                                         ld, amax_bits);
+    else
+      amax_kernel<float><<<grid, QTHREADS, 0, c.stream>>>(static_cast<const float*>(x), rows,
+                                                          cols, ld, amax_bits);
+    c.after();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  dim3 grid((unsigned)((cols + CT - 1) / CT), (unsigned)((rows + CT - 1) / CT));
+  c.before(KK_QUANT, (double)rows * cols * ((src_dtype == kBF16 ? 2 : 4) + (q ? 2 : 1)));
+  uint8_t* qb = static_cast<uint8_t*>(qT);
+  uint8_t* qr = static_cast<uint8_t*>(q);
+#define CASTT(T, F)                                                                      \
+  cast_transpose_kernel<T, F><<<grid, QTHREADS, 0, c.stream>>>(                          \
+      static_cast<const T*>(x), rows, cols, ld, amax_bits, scale, qb, ldqT, qr, ldq)
+  if (src_dtype == kBF16) {
+    if (fmt == 0) CASTT(bf16, 0); else CASTT(bf16, 1);
+  } else {
+    if (fmt == 0) CASTT(float, 0); else CASTT(float, 1);
+  }
+#undef CASTT
   c.after();
   return cudaGetLastError();
 }

@@ -146,6 +146,12 @@ cudaError_t gemm_fp8(const GemmArgs& a, const LaunchCtx& c);
 cudaError_t fp8_quantize(int src_dtype, const void* x, int64_t rows, int64_t cols, int64_t ld,
                          int fmt, unsigned* amax_bits, float* scale, void* q, int64_t ldq,
                          const LaunchCtx& c);
+// The same with an optional row-major copy q (may be null) and an optional
+// transposed copy qT [cols][rows] (row pitch ldqT; may be null): one amax pass
+// and, with qT, one kernel writing both.  rows % 16 == 0 and cols % 16 == 0.
+cudaError_t fp8_quantize2(int src_dtype, const void* x, int64_t rows, int64_t cols, int64_t ld,
+                          int fmt, unsigned* amax_bits, float* scale, void* q, int64_t ldq,
+                          void* qT, int64_t ldqT, const LaunchCtx& c);
 
 // LayerNorm backward without a residual: dx = LN_bwd(du + du2) where du (fp32,
 // may be null) and du2 (layer dtype) are the two parts of the upstream

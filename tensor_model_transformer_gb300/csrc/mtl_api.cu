@@ -71,7 +71,7 @@ struct Dims {
   size_t esz;
   float p_attn, p_hidden;
   unsigned long long seed;
-  int fp8;        // 1: FP8 (E4M3) forward GEMMs
+  int fp8;        // 1: FP8 (E4M3) forward GEMMs; 2: and E5M2 x E4M3 backward GEMMs
   int post_ln;    // 1: Post-LN layer
   int recompute;  // 1: LayerNorm outputs and GeLU(z) recomputed in the backward
 };
@@ -104,7 +104,7 @@ mtl_status validate(const mtl_layer_desc* desc, Dims* o) {
   if (!(d.ln_eps > 0.f)) return MTL_ERR_INVALID_ARG;
   if (!(d.p_attn >= 0.f && d.p_attn < 1.f) || !(d.p_hidden >= 0.f && d.p_hidden < 1.f))
     return MTL_ERR_INVALID_ARG;
-  if (d.fp8 != 0 && d.fp8 != 1) return MTL_ERR_INVALID_ARG;
+  if (d.fp8 < 0 || d.fp8 > 2) return MTL_ERR_INVALID_ARG;
   if ((d.post_ln != 0 && d.post_ln != 1) || (d.recompute != 0 && d.recompute != 1))
     return MTL_ERR_INVALID_ARG;
   if (d.h % d.heads) return MTL_ERR_INVALID_ARG;
@@ -142,8 +142,41 @@ mtl_status validate(const mtl_layer_desc* desc, Dims* o) {
     // FP8 GEMMs: bf16 layers without dropout, K partitions of whole 128s
     if (d.dtype != MTL_BF16 || d.p_attn > 0.f || d.p_hidden > 0.f) return MTL_ERR_UNSUPPORTED;
     if (d.h % 128 || (d.h / d.t) % 128 || (d.ffn / d.t) % 128) return MTL_ERR_UNSUPPORTED;
+    // hybrid backward: the QKV input-gradient partitions are whole 128s too
+    if (d.fp8 == 2 && ((3 * d.h) / d.t) % 128) return MTL_ERR_UNSUPPORTED;
   }
   return MTL_OK;
+}
+
+// FP8 hybrid: the forward's transposed FP8 copies that the backward's weight-
+// and data-gradient GEMMs read, and their scales.  Scale slot 2i / 2i+1: the
+// activation / weight of forward GEMM i (QKV, out-proj, fc1, fc2).
+struct Fp8Saved {
+  size_t scales, act[4], wt[4], total;
+};
+
+Fp8Saved fp8_saved_layout(const Dims& D) {
+  Fp8Saved F;
+  memset(&F, 0, sizeof(F));
+  if (D.fp8 != 2) return F;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align_up(bytes);
+    return at;
+  };
+  const size_t n = (size_t)D.n, h = (size_t)D.h, f = (size_t)D.f;
+  F.scales = take(16 * 4);
+  F.act[0] = take(h * n);      // u1^T  [h][n]
+  F.act[1] = take(h * n);      // ctx^T [h][n]
+  F.act[2] = take(h * n);      // u2^T  [h][n]
+  F.act[3] = take(f * n);      // a^T   [f][n]
+  F.wt[0] = take(h * 3 * h);   // W_qkv^T [h][3h]
+  F.wt[1] = take(h * h);       // W_o^T   [h][h]
+  F.wt[2] = take(h * f);       // W_fc1^T [h][f]
+  F.wt[3] = take(f * h);       // W_fc2^T [f][h]
+  F.total = off;
+  return F;
 }
 
 mtl_saved_layout saved_layout(const Dims& D) {
@@ -156,7 +189,10 @@ mtl_saved_layout saved_layout(const Dims& D) {
   };
   const size_t nh = (size_t)D.n * D.h * D.esz;
   const size_t nf = (size_t)D.n * D.f * D.esz;
-  const bool pre = !D.post_ln, rc = D.recompute != 0;
+  const bool pre = !D.post_ln;
+  // FP8 hybrid keeps FP8 transposed copies for the backward instead of the
+  // bf16 LayerNorm outputs and GeLU(z): they are dropped as with recomputation
+  const bool rc = D.recompute != 0 || D.fp8 == 2;
   // Pre-LN saves u1, x1, u2 (u1, u2 recomputable); Post-LN saves h1, x1, h2 (x1
   // recomputable); a = GeLU(z) is recomputable in both.
   L.mu1 = take((size_t)D.n * 4);
@@ -176,6 +212,7 @@ mtl_saved_layout saved_layout(const Dims& D) {
                          : 0);
   L.h1 = take(pre ? 0 : nh);
   L.h2 = take(pre ? 0 : nh);
+  L.fp8 = take(fp8_saved_layout(D).total);
   L.total = off;
   return L;
 }
@@ -183,11 +220,11 @@ mtl_saved_layout saved_layout(const Dims& D) {
 // FP8 scratch of the forward: amax words and scales of the 8 quantized
 // operands, one activation buffer and one weight buffer (reused GEMM by GEMM).
 struct Fp8Ws {
-  size_t stats, qa, qb, total;
+  size_t stats, qa, qb, gq, gqT, total;
 };
 
 Fp8Ws fp8_ws_layout(const Dims& D) {
-  Fp8Ws F{0, 0, 0, 0};
+  Fp8Ws F{0, 0, 0, 0, 0, 0};
   if (!D.fp8) return F;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -198,8 +235,11 @@ Fp8Ws fp8_ws_layout(const Dims& D) {
   const size_t wide = (size_t)(D.f > D.h ? D.f : D.h);
   const size_t wmax = (size_t)(D.f > 3 * D.h ? D.f : 3 * D.h) * D.h;
   F.stats = take(128);                    // 16 amax words, 16 scales
-  F.qa = take((size_t)D.n * wide);
-  F.qb = take(wmax);
+  F.qa = take((size_t)D.n * wide);        // activation (forward) / its transpose (backward)
+  F.qb = take(wmax);                      // weight (forward) / its transpose (backward)
+  const size_t gwide = (size_t)(D.f > 3 * D.h ? D.f : 3 * D.h);
+  F.gq = take(D.fp8 == 2 ? (size_t)D.n * gwide : 0);     // gradient, and its transpose
+  F.gqT = take(D.fp8 == 2 ? (size_t)D.n * gwide : 0);
   F.total = off;
   return F;
 }
@@ -236,8 +276,9 @@ WsLayout ws_layout(const Dims& D) {
   W.fp8 = take(fp8_ws_layout(D).total);
   // recomputed activations ([n][h] and [n][ffn]); the forward keeps the ones it
   // does not save here too
-  W.rc_h = take(D.recompute ? nh * D.esz : 0);
-  W.rc_f = take(D.recompute ? (size_t)D.n * D.f * D.esz : 0);
+  const bool rcw = D.recompute || D.fp8 == 2;
+  W.rc_h = take(rcw ? nh * D.esz : 0);
+  W.rc_f = take(rcw ? (size_t)D.n * D.f * D.esz : 0);
   W.zero_h = take(D.post_ln ? (size_t)D.h * D.esz : 0);   // a zero bias (Post-LN dx GEMM)
   W.total = off;
   return W;
@@ -336,11 +377,26 @@ mtl_status forward_core(const Dims& D, float ln_eps, const mtl_weights* w, const
     }
     unsigned* amax = at<unsigned>(fp8ws, FW.stats) + 2 * slot;
     float* sc = at<float>(fp8ws, FW.stats + 64) + 2 * slot;
-    ++slot;
     uint8_t* qa = at<uint8_t>(fp8ws, FW.qa);
     uint8_t* qb = at<uint8_t>(fp8ws, FW.qb);
-    MTL_TRY(fp8_quantize(kBF16, g.A.ptr, g.M, g.K, g.A.ld, 0, amax, sc, qa, g.K, c), where);
-    MTL_TRY(fp8_quantize(kBF16, g.B.ptr, g.N, g.K, g.B.ld, 0, amax + 1, sc + 1, qb, g.K, c), where);
+    if (D.fp8 == 2) {
+      // hybrid: the same passes also write the transposed copies the backward
+      // reads, into `saved` with their scales
+      const Fp8Saved FS = fp8_saved_layout(D);
+      char* fsv = at<char>(saved, L.fp8);
+      sc = at<float>(fsv, FS.scales) + 2 * slot;
+      MTL_TRY(fp8_quantize2(kBF16, g.A.ptr, g.M, g.K, g.A.ld, 0, amax, sc, qa, g.K,
+                            at<uint8_t>(fsv, FS.act[slot]), g.M, c),
+              where);
+      MTL_TRY(fp8_quantize2(kBF16, g.B.ptr, g.N, g.K, g.B.ld, 0, amax + 1, sc + 1, qb, g.K,
+                            at<uint8_t>(fsv, FS.wt[slot]), g.N, c),
+              where);
+    } else {
+      MTL_TRY(fp8_quantize(kBF16, g.A.ptr, g.M, g.K, g.A.ld, 0, amax, sc, qa, g.K, c), where);
+      MTL_TRY(fp8_quantize(kBF16, g.B.ptr, g.N, g.K, g.B.ld, 0, amax + 1, sc + 1, qb, g.K, c),
+              where);
+    }
+    ++slot;
     g.A = {qa, g.K, true};
     g.B = {qb, g.K, true};
     g.fmt_a = 0;
@@ -353,13 +409,14 @@ mtl_status forward_core(const Dims& D, float ln_eps, const mtl_weights* w, const
   mtl_status gst;
   const int n = (int)D.n, h = (int)D.h, f = (int)D.f, t = (int)D.t;
   // activations the backward recomputes live in the workspace during the forward
-  void* u1 = D.recompute ? rc_h : at<char>(saved, L.u1);
+  const bool rcf = D.recompute || D.fp8 == 2;
+  void* u1 = rcf ? rc_h : at<char>(saved, L.u1);
   void* qkv = at<char>(saved, L.qkv);
   void* ctx = at<char>(saved, L.ctx);
   void* x1 = (D.post_ln && D.recompute) ? rc_h : at<char>(saved, L.x1);
-  void* u2 = D.recompute ? rc_h : at<char>(saved, L.u2);
+  void* u2 = rcf ? rc_h : at<char>(saved, L.u2);
   void* z = at<char>(saved, L.z);
-  void* a = D.recompute ? rc_f : at<char>(saved, L.a);
+  void* a = rcf ? rc_f : at<char>(saved, L.a);
   const bool bf = D.dtype == MTL_BF16;
   const Dropout drop_attn = make_drop(D.p_attn, D.seed, SITE_ATTN);
 
@@ -733,6 +790,96 @@ mtl_status mtl_layer_bwd(const mtl_layer_desc* desc, const mtl_weights* w, const
       g.ldr = h;
       MTL_TRY(run_gemm(D, g, c), "qkv dgrad");
     }
+    return MTL_OK;
+  }
+
+  if (D.fp8 == 2) {
+    // FP8 hybrid backward (Pre-LN, no dropout): every GEMM takes an E5M2
+    // gradient and an E4M3 activation or weight, both K-major.  The forward left
+    // the transposed E4M3 copies of its operands (and their scales) in `saved`;
+    // each gradient is quantized once into a row-major and a transposed copy
+    // (one amax pass, one conversion pass).  Bias and LayerNorm gradients and
+    // attention stay bf16 / fp32.
+    const Fp8Ws FW = fp8_ws_layout(D);
+    const Fp8Saved FS = fp8_saved_layout(D);
+    const char* fsv = at<char>(saved, L.fp8);
+    const float* fsc = at<float>(fsv, FS.scales);
+    auto act = [&](int i) { return at<uint8_t>(fsv, FS.act[i]); };
+    auto wtr = [&](int i) { return at<uint8_t>(fsv, FS.wt[i]); };
+    char* fb = at<char>(workspace, W.fp8);
+    unsigned* amax = at<unsigned>(fb, FW.stats);
+    float* gscale = at<float>(fb, FW.stats + 64);
+    uint8_t* gq = at<uint8_t>(fb, FW.gq);
+    uint8_t* gqT = at<uint8_t>(fb, FW.gqT);
+    MTL_TRY(cudaMemsetAsync(amax, 0, 64, s), "fp8 stats");
+    int slot = 0;
+    // the gradient src [rows][cols] to E5M2: gq row-major, gqT transposed
+    auto quant_grad = [&](const void* src, int64_t rows, int64_t cols, const float** scale)
+        -> cudaError_t {
+      *scale = gscale + slot;
+      const cudaError_t e = fp8_quantize2(kBF16, src, rows, cols, cols, MTL_FP8_E5M2,
+                                          amax + slot, gscale + slot, gq, cols, gqT, rows, c);
+      ++slot;
+      return e;
+    };
+    // C = epi(A B^T) with K-major FP8 A [M][K] (E5M2) and B [N][K] (E4M3)
+    auto f8 = [&](int M, int N, int K, int parts, const void* qa, const float* sa, const void* qb,
+                  const float* sbb, int epi, void* C, int64_t ldc, bool cf32,
+                  const void* Z) -> cudaError_t {
+      GemmArgs g = gemm_args(M, N, K, parts, qa, K, true, qb, K, true, epi, C, ldc, cf32, status);
+      g.fmt_a = MTL_FP8_E5M2;
+      g.fmt_b = MTL_FP8_E4M3;
+      g.scale_a = sa;
+      g.scale_b = sbb;
+      g.Z = const_cast<void*>(Z);
+      g.ldz = N;
+      return gemm_fp8(g, c);
+    };
+    const float* s_g;
+    // MLP block
+    MTL_TRY(colsum(D.dtype, dy, h, n, h, static_cast<float*>(gr->b_fc2), partial, c), "db_fc2");
+    MTL_TRY(quant_grad(dy, n, h, &s_g), "fp8 dy");
+    MTL_TRY(f8(n, f, h, 1, gq, s_g, wtr(3), fsc + 7, EPI_DGELU, dz, f, false, z), "fc2 dgrad");
+    MTL_TRY(f8(h, f, n, 1, gqT, s_g, act(3), fsc + 6, EPI_STORE, gr->w_fc2, f, true, nullptr),
+            "fc2 wgrad");
+    MTL_TRY(quant_grad(dz, n, f, &s_g), "fp8 dz");
+    MTL_TRY(f8(n, h, f, t, gq, s_g, wtr(2), fsc + 5, EPI_STORE, du, h, true, nullptr),
+            "fc1 dgrad");
+    MTL_TRY(f8(f, h, n, 1, gqT, s_g, act(2), fsc + 4, EPI_STORE, gr->w_fc1, h, true, nullptr),
+            "fc1 wgrad");
+    MTL_TRY(colsum(D.dtype, dz, f, n, f, static_cast<float*>(gr->b_fc1), partial, c), "db_fc1");
+    MTL_TRY(ln_bwd(D.dtype, du, x1, at<float>(saved, L.mu2), at<float>(saved, L.rstd2), w->ln2_g,
+                   dy, dx1, static_cast<float*>(gr->ln2_g), static_cast<float*>(gr->ln2_b),
+                   partial, n, h, c),
+            "ln2 bwd");
+    // attention block
+    MTL_TRY(colsum(D.dtype, dx1, h, n, h, static_cast<float*>(gr->b_o), partial, c), "db_o");
+    MTL_TRY(quant_grad(dx1, n, h, &s_g), "fp8 dx1");
+    MTL_TRY(f8(n, h, h, 1, gq, s_g, wtr(1), fsc + 3, EPI_STORE, dctx, h, false, nullptr),
+            "out-proj dgrad");
+    MTL_TRY(f8(h, h, n, 1, gqT, s_g, act(1), fsc + 2, EPI_STORE, gr->w_o, h, true, nullptr),
+            "out-proj wgrad");
+    MTL_TRY(attn_bwd_tc(qkv, ctx, at<float>(saved, L.lse), dctx, dqkv, dsum, (int)D.batch,
+                        (int)D.seq, (int)D.heads, (int)D.d, make_drop(0.f, 0, SITE_ATTN),
+                        nullptr, status, c),
+            "attention bwd");
+    MTL_TRY(colsum(D.dtype, dqkv, 3 * h, n, 3 * h, static_cast<float*>(gr->b_qkv), partial, c),
+            "db_qkv");
+    MTL_TRY(quant_grad(dqkv, n, 3 * h, &s_g), "fp8 dqkv");
+    MTL_TRY(f8(3 * h, h, n, 1, gqT, s_g, act(0), fsc + 0, EPI_STORE, gr->w_qkv, h, true,
+               nullptr),
+            "qkv wgrad");
+    MTL_TRY(f8(n, h, 3 * h, t, gq, s_g, wtr(0), fsc + 1, EPI_STORE, du, h, true, nullptr),
+            "qkv dgrad");
+    MTL_TRY(ln_bwd(D.dtype, du, x, at<float>(saved, L.mu1), at<float>(saved, L.rstd1), w->ln1_g,
+                   dx1, dx, static_cast<float*>(gr->ln1_g), static_cast<float*>(gr->ln1_b),
+                   partial, n, h, c),
+            "ln1 bwd");
+    (void)u1;
+    (void)u2;
+    (void)a;
+    (void)rc_h;
+    (void)rc_f;
     return MTL_OK;
   }
 
@@ -1111,15 +1258,18 @@ mtl_status mtl_layer_decode(const mtl_layer_desc* desc, const mtl_weights* w, co
 // ---------------------------------------------------------------- FP8
 
 mtl_status mtl_fp8_quantize(int32_t src_dtype, const void* x, int64_t rows, int64_t cols,
-                            int64_t ld, int32_t fmt, void* q, int64_t ldq, float* scale,
-                            void* workspace, size_t ws_bytes, mtl_stream stream) {
+                            int64_t ld, int32_t fmt, void* q, int64_t ldq, void* qT,
+                            int64_t ldqT, float* scale, void* workspace, size_t ws_bytes,
+                            mtl_stream stream) {
   g_launches = 0;
   g_cuda_err[0] = 0;
   if (src_dtype != MTL_F32 && src_dtype != MTL_BF16) return MTL_ERR_INVALID_ARG;
   if (fmt != MTL_FP8_E4M3 && fmt != MTL_FP8_E5M2) return MTL_ERR_INVALID_ARG;
-  if (rows < 0 || cols < 0 || ld < cols || ldq < cols || cols % 16 || ldq % 16)
-    return MTL_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(q) || !scale || !aligned16(workspace) || (ld * (src_dtype == MTL_BF16 ? 2 : 4)) % 16)
+  if (rows < 0 || cols < 0 || ld < cols || cols % 16 || (!q && !qT)) return MTL_ERR_INVALID_ARG;
+  if (q && (ldq < cols || ldq % 16 || !aligned16(q))) return MTL_ERR_INVALID_ARG;
+  if (qT && (rows % 16 || ldqT < rows || ldqT % 16 || !aligned16(qT))) return MTL_ERR_INVALID_ARG;
+  if (!aligned16(x) || !scale || !aligned16(workspace) ||
+      (ld * (src_dtype == MTL_BF16 ? 2 : 4)) % 16)
     return MTL_ERR_INVALID_ARG;
   if (ws_bytes < kStatusBytes) return MTL_ERR_WORKSPACE;
   const int nsm = device_sm_count();
@@ -1129,9 +1279,15 @@ mtl_status mtl_fp8_quantize(int32_t src_dtype, const void* x, int64_t rows, int6
   unsigned* status = static_cast<unsigned*>(workspace);
   MTL_TRY(cudaMemsetAsync(status, 0, kStatusBytes, s), "status reset");
   // the amax word sits in the status block, after the status word
-  MTL_TRY(fp8_quantize(src_dtype == MTL_BF16 ? kBF16 : kF32, x, rows, cols, ld, fmt, status + 1,
-                       scale, q, ldq, c),
-          "fp8 quantize");
+  if (qT) {
+    MTL_TRY(fp8_quantize2(src_dtype == MTL_BF16 ? kBF16 : kF32, x, rows, cols, ld, fmt, status + 1,
+                          scale, q, ldq, qT, ldqT, c),
+            "fp8 quantize");
+  } else {
+    MTL_TRY(fp8_quantize(src_dtype == MTL_BF16 ? kBF16 : kF32, x, rows, cols, ld, fmt,
+                         status + 1, scale, q, ldq, c),
+            "fp8 quantize");
+  }
   return MTL_OK;
 }
 

@@ -13,7 +13,7 @@ import os
 PARAM_NAMES = ("w_qkv", "b_qkv", "w_o", "b_o", "w_fc1", "b_fc1", "w_fc2", "b_fc2",
                "ln1_g", "ln1_b", "ln2_g", "ln2_b")
 SAVED_NAMES = ("mu1", "rstd1", "u1", "qkv", "ctx", "lse", "x1", "mu2", "rstd2", "u2", "z", "a",
-               "attn_mask", "h1", "h2")
+               "attn_mask", "h1", "h2", "fp8")
 
 F32, BF16 = 0, 1
 STATUS = {0: "MTL_OK", 1: "MTL_ERR_INVALID_ARG", 2: "MTL_ERR_UNSUPPORTED",
@@ -85,7 +85,8 @@ def lib():
                                         vp]
         L.mtl_layer_decode.argtypes = [pd, ctypes.POINTER(Weights), vp, vp, vp, i32, vp, vp, sz,
                                        vp]
-        L.mtl_fp8_quantize.argtypes = [i32, vp, i64, i64, i64, i32, vp, i64, vp, vp, sz, vp]
+        L.mtl_fp8_quantize.argtypes = [i32, vp, i64, i64, i64, i32, vp, i64, vp, i64, vp, vp,
+                                       sz, vp]
         L.mtl_gemm_fp8.argtypes = [i32, i32, i32, i32, vp, i64, i32, vp, vp, i64, i32, vp, i32,
                                    vp, vp, i64, vp, i64, vp, i64, i32, vp, sz, vp]
         L.mtl_selftest_wait_timeout.argtypes = [vp, i64, vp]
@@ -272,10 +273,12 @@ def kv_views(desc: LayerDesc, kv_cache, max_seq):
 FP8_FORMATS = {"e4m3": 0, "e5m2": 1}
 
 
-def fp8_quantize(src_dtype, x, rows, cols, ld, fmt, q, ldq, scale, workspace, stream=None):
-    """mtl_fp8_quantize on torch tensors (q: uint8 device tensor, scale: float32 [1])."""
+def fp8_quantize(src_dtype, x, rows, cols, ld, fmt, q, ldq, scale, workspace, qT=None, ldqT=0,
+                 stream=None):
+    """mtl_fp8_quantize on torch tensors (q / qT: uint8 device tensors or None,
+    scale: float32 [1])."""
     _check(lib().mtl_fp8_quantize(_dt(src_dtype), _ptr(x), rows, cols, ld, FP8_FORMATS[fmt],
-                                  _ptr(q), ldq, _ptr(scale), _ptr(workspace),
+                                  _ptr(q), ldq, _ptr(qT), ldqT, _ptr(scale), _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _stream(stream)),
            "mtl_fp8_quantize")
 

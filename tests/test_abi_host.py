@@ -274,11 +274,17 @@ def test_infer_sizes_and_rejects(mtl):
 def test_fp8_entry_points_reject(mtl):
     L = mtl.lib()
     ok = (FAKE, FAKE + 4096, FAKE + 8192, FAKE + 12288)
-    q = L.mtl_fp8_quantize
+    def q(src, x, rows, cols, ld, fmt, qq, ldq, scale, ws, wsb, st, qT=None, ldqT=0):
+        return L.mtl_fp8_quantize(src, x, rows, cols, ld, fmt, qq, ldq, qT, ldqT, scale, ws, wsb,
+                                  st)
+
     assert q(1, ok[0], 64, 250, 256, 0, ok[1], 256, ok[2], ok[3], 256, None) == 1   # cols % 16
     assert q(1, ok[0], 64, 256, 256, 2, ok[1], 256, ok[2], ok[3], 256, None) == 1   # format
     assert q(1, ok[0], 64, 256, 256, 0, ok[1], 256, None, ok[3], 256, None) == 1    # no scale
     assert q(1, ok[0], 64, 256, 256, 0, ok[1], 256, ok[2], ok[3], 255, None) == 3
+    assert q(1, ok[0], 64, 256, 256, 0, None, 0, ok[2], ok[3], 256, None) == 1      # no output
+    assert q(1, ok[0], 60, 256, 256, 0, None, 0, ok[2], ok[3], 256, None,
+             qT=ok[1], ldqT=64) == 1                                              # rows % 16
     g = L.mtl_gemm_fp8
     args = dict(M=256, N=256, K=512, parts=1, A=ok[0], lda=512, fa=0, sa=ok[2], B=ok[1], ldb=512,
                 fb=0, sb=ok[2], epi=0, C=ok[3], ldc=256)
@@ -298,9 +304,10 @@ def test_fp8_entry_points_reject(mtl):
 
 def test_fp8_layer_validation(mtl):
     ok = good_desc(mtl, fp8=1)                                  # h 256, t 2: 128-wide parts
+    assert mtl.layer_sizes(good_desc(mtl, fp8=2))[1] > mtl.layer_sizes(ok)[1]
     assert mtl.layer_sizes(ok)[1] > mtl.layer_sizes(good_desc(mtl))[1]
     L = mtl.lib()
-    for kw, st in ((dict(fp8=2), 1), (dict(fp8=1, dtype="f32"), 2), (dict(fp8=1, p_attn=0.1), 2),
+    for kw, st in ((dict(fp8=3), 1), (dict(fp8=1, dtype="f32"), 2), (dict(fp8=1, p_attn=0.1), 2),
                    (dict(fp8=1, t=4), 2)):                      # h/t = 64: not whole 128s
         d = good_desc(mtl, **kw)
         assert L.mtl_layer_sizes(ctypes.byref(d), None, None) == st, kw

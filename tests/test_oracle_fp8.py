@@ -137,3 +137,23 @@ def test_fp8_layer_forward():
     y_hand = FP8.gemm(c["a"], P["w_fc2"], epi=2, bias=P["b_fc2"], R=x1)[0]
     assert np.array_equal(y_hand, y8.reshape(-1, shp.h))
     assert 0 < np.max(np.abs(y8 - y)) <= 0.05 * np.max(np.abs(y))
+
+
+def test_fp8_hybrid_backward():
+    """fp8=2: the backward's GEMMs quantize the gradient side to E5M2 and the
+    other side to E4M3 (rebuilt by hand for two of them); the result stays
+    within FP8 error of the high-precision backward of the same forward."""
+    import synthetic
+    shp = synthetic.tiny(h=64, heads=4, seq=16, batch=2, dtype="f32", w_std=0.1, out_std=0.1)
+    x, p, dy = synthetic.make_layer(shp, seed=7, affine=True)
+    _, c2 = oracle.layer_fwd(p, x, shp.heads, fp8=2)
+    _, c1 = oracle.layer_fwd(p, x, shp.heads, fp8=1)
+    dx2, g2, _ = oracle.layer_bwd(p, c2, dy)
+    dx1, g1, _ = oracle.layer_bwd(p, c1, dy)
+    dyf = np.asarray(dy, np.float64).reshape(-1, shp.h)
+    assert np.array_equal(g2["w_fc2"], FP8.gemm(dyf.T, c2["a"].T, "e5m2", "e4m3")[0])
+    assert np.array_equal(g2["b_fc2"], g1["b_fc2"])             # bias gradients unquantized
+    for k in g1:
+        scale = np.max(np.abs(g1[k]))
+        assert np.max(np.abs(g2[k] - g1[k])) <= 0.25 * scale, k
+    assert 0 < np.max(np.abs(dx2 - dx1)) <= 0.25 * np.max(np.abs(dx1))
