@@ -119,7 +119,14 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def traffic_record(kernel_file):
+def gemm_source_sha():
+    """sha256 of the tensor-core GEMM's sources (gemm_core.cuh then gemm_tc.cu)."""
+    csrc = os.path.join(ROOT, "tensor_model_transformer_gb300", "csrc")
+    data = b"".join(open(os.path.join(csrc, f), "rb").read() for f in ("gemm_core.cuh", "gemm_tc.cu"))
+    return hashlib.sha256(data).hexdigest()
+
+
+def traffic_record():
     """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
     or None when absent or taken on a different revision of the kernel source."""
     path = os.path.join(ROOT, "profiles", "gemm_tc_traffic.txt")
@@ -129,8 +136,7 @@ def traffic_record(kernel_file):
             if ":" in ln:
                 k, v = ln.split(":", 1)
                 rec[k.strip()] = v.strip()
-        src = open(kernel_file, "rb").read()
-        if rec.get("source_sha256") != hashlib.sha256(src).hexdigest():
+        if rec.get("source_sha256") != gemm_source_sha():
             return None
         return rec
     except Exception:
@@ -648,8 +654,7 @@ def main():
             achieved = r["work"] / (r["ms"] / 1e3) / 1e9
             peak = pk["hbm_gbs"]
             unit, bound = "GB/s", "hbm"
-        tr = traffic_record(os.path.join(ROOT, "tensor_model_transformer_gb300", "csrc",
-                                         "gemm_tc.cu")) if dom == "gemm_tc" else None
+        tr = traffic_record() if dom == "gemm_tc" else None
         traffic = None
         if tr and "dram_bytes_per_launch_full" in tr:
             traffic = float(tr["dram_bytes_per_launch_full"])
