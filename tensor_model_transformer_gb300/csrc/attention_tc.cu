@@ -19,11 +19,11 @@
 // eighth of a bf16 P); the two backward kernels read the bits instead of
 // drawing again, which trades 2 of 3 Philox passes for a few MB of traffic.
 //
-// All three kernels: one CTA per 128-row block, 192 threads:
+// All three kernels are persistent (one CTA per SM) with warp roles:
 //   warp 0      TMA producer
 //   warp 1      TMEM allocator, MMA issuer
-//   warps 2..5  row threads: thread (warp%4)*32+lane owns TMEM lane = one row of
-//               the block, so row maxima and sums need no cross-thread reduction.
+//   the rest    row threads: thread (warp%4)*32+lane owns TMEM lane = one row of
+//               a 128-row block.
 // Operand tiles are [atoms][rows][64] 128-byte-swizzled boxes straight from TMA;
 // the same box serves as a K-major operand (rows = M/N) or an MN-major one
 // (rows = K), e.g. dO is the K-major B of dO V^T and the MN-major B of P^T dO.
@@ -35,7 +35,7 @@
 namespace mtl {
 namespace attn {
 
-constexpr int FWD_THREADS = 384;   // forward kernel: two warpgroups of row threads
+constexpr int FWD_THREADS = 384;   // forward kernel: 4 control warps, two warpgroups of row threads
 constexpr int BWD_THREADS = 384;   // backward kernels: two warpgroups of row threads
 constexpr int ATOM128 = 128 * 128;   // [128 rows][64 bf16]
 constexpr int ATOM64 = 64 * 128;     // [64 rows][64 bf16]
@@ -56,6 +56,9 @@ struct Params {
   Dropout drop;       // attention dropout: element (query i, key j) of head hd, batch b
                       // is e = ((b * heads + hd) * seq + i) * seq + j
   uint32_t* mask;     // keep bits written by the forward, read by the backward
+  unsigned* sched;    // work counter pair {next item, CTAs done}: zero before the launch,
+                      // reset to zero by the last CTA
+  int chunk;          // (batch, head) pairs per scheduling chunk of the forward
 };
 
 // Keep bits of the forward, one 2 KB tile per (batch, head, query block qb, key
@@ -114,39 +117,117 @@ __device__ __forceinline__ void item_coords(const Params& p, int item, bool desc
 }
 
 // ============================================================================ forward
-// Persistent: one CTA per SM walks the (row block, head, batch) work items in
-// item_coords order.  Per item: 128 queries; K/V blocks of 128 keys in a
-// double-buffered ring that runs on across items.  S is double-buffered in
-// TMEM (the MMAs of block j+2 run while the row threads work on block j) and so
-// is O (an item's epilogue overlaps the next item's first MMAs).  Two
-// warpgroups of row threads each take 64 of the 128 key columns; they combine
-// their row maxima through shared memory behind an mbarrier.
-// smem: Q, K[2], V[2] (NA atoms of 16 KB each), P (2 atoms), row-max and row-sum
-// exchange.  TMEM: S[b] cols 128b, O[b] cols 256+128b.
+// Persistent: one CTA per SM takes (query pair, head, batch) work items from a
+// global counter.  An item is 256 queries as two tiles of 128 rows, A (rows
+// 0..127) and B (rows 128..255).  Each tile has a warpgroup of row threads
+// (a thread owns one query row and all 128 keys of a block, so row maxima and
+// sums stay in registers) and its own P and O in TMEM.  K and V blocks of 128
+// keys stream through one TMA ring that both tiles read.  The S buffer in
+// TMEM serves the tiles in turn, S uses A(0) B(0) A(1) B(1) ...: the next
+// turn's Q K^T runs on the tensor cores while the previous owner computes its
+// exponentials.  A warpgroup writes its bf16 P block into TMEM,
+// where the PV MMA reads it as the A operand; nothing in TMEM is written by
+// an MMA while another MMA may still read it.
+// Causal: tile A of query pair q reads key blocks 0..2q, tile B 0..2q+1 (the
+// last one is the diagonal block of each); with seq % 256 == 128 the last
+// pair has no tile B.
+// Items go longest first within chunks of (batch, head) pairs whose K/V fit
+// in L2 together, so K/V come from HBM about once and the launch ends on
+// short items.
+// Warps: 0 scheduler and TMA producer, 1 TMEM allocator and Q K^T issuer, 2 P V
+// issuer, 3 register donor, 4..7 row threads of tile A, 8..11 of tile B.  The
+// two MMA streams touch disjoint TMEM columns and each commit tracks only its
+// own thread's MMAs, so neither issuer waits on the other's dependencies.
+// smem: Q_A, Q_B, ring[FWD_RING] (NA atoms of 16 KB each), item ids.
+// TMEM: S cols 0..127, P_A 128..191, P_B 192..255, O_A 256.., O_B 384..
+constexpr int FWD_RING = 4;
+static_assert(FWD_RING % 2 == 0, "K and V must keep to their own ring slots");
+constexpr uint32_t TM_S = 0, TM_P = 128, TM_O = 256;
+// Register split: warps 0..3 (producer, MMA issuer, two idle) give registers
+// to the row warps 4..11, which hold a 128-key score row each.  The split is
+// balanced on every SM sub-partition (warp w runs on sub-partition w % 4: one
+// giving warp and two taking warps on each), since setmaxnreg.inc waits, with
+// no bound, for registers released on its own sub-partition.
+constexpr int FWD_LAUNCH_REGS = 168, FWD_LOW_REGS = 56, FWD_ROW_REGS = 224;
+static_assert(FWD_THREADS == 384, "one giving and two taking warps per sub-partition");
+static_assert(FWD_LOW_REGS + 2 * FWD_ROW_REGS <= 3 * FWD_LAUNCH_REGS,
+              "register split exceeds a sub-partition's launch allocation");
+
+struct FwdItem {
+  int qp, hd, b;
+  int n0, n1;   // key blocks of tile A / tile B (0: tile absent)
+  __device__ __forceinline__ int n(int x) const { return x ? n1 : n0; }
+};
+
+__device__ __forceinline__ FwdItem fwd_item(const Params& p, int k) {
+  const int nq2 = (p.nqb + 1) >> 1;
+  const int pairs = p.batch * p.heads;
+  const int per_chunk = p.chunk * nq2;
+  const int c = k / per_chunk;
+  const int cp = min(p.chunk, pairs - c * p.chunk);   // pairs in this chunk
+  const int r = k - c * per_chunk;
+  const int pair = c * p.chunk + r % cp;
+  FwdItem it;
+  it.qp = nq2 - 1 - r / cp;
+  it.hd = pair % p.heads;
+  it.b = pair / p.heads;
+  it.n0 = 2 * it.qp + 1;
+  it.n1 = 2 * it.qp + 1 < p.nqb ? 2 * it.qp + 2 : 0;
+  return it;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// Two fp32 lanes in one instruction: (a0, a1) * (b0, b1) + (c0, c1), and a sum.
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                      float c0, float c1) {
+  unsigned long long ra, rb, rc, rd;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b0), "f"(b1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c0), "f"(c1));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(rd));
+}
+__device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  unsigned long long ra, rb, rd;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b0), "f"(b1));
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(rd));
+}
+
 template <int NA, int KS, bool DROP>
 __global__ void __launch_bounds__(FWD_THREADS, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const Smem sm = smem_aligned(smem_raw);
   constexpr uint32_t TILE = NA * ATOM128;
-  const uint32_t sQ = sm.u32, sK0 = sQ + TILE, sV0 = sQ + 3 * TILE, sP = sQ + 5 * TILE;
-  float* s_mx = reinterpret_cast<float*>(sm.base + 5 * TILE + 2 * ATOM128);  // [2][2][128]
-  float* s_l = s_mx + 512;                                                   // [2][128]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm.base + 5 * TILE + 2 * ATOM128 + 3072);
+  constexpr int D = KS * 16;
+  const uint32_t sQ0 = sm.u32, sR0 = sQ0 + 2 * TILE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm.base + (2 + FWD_RING) * TILE);
   const uint32_t bar0 = smem_u32(bars);
   auto B = [&](int i) { return bar0 + 8u * i; };
-  // barriers
-  constexpr int QFULL = 0, QEMPTY = 1, KFULL = 2, KEMPTY = 4, VFULL = 6, VEMPTY = 8, SFULL = 10,
-                PFULL = 12, ODONE = 13, OFREE = 14, MXB = 16, LXB = 17, NBAR = 18;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBAR);
+  // barriers; per-tile ones come in pairs (A, B), item ones in pairs (slot 0, 1)
+  // (a barrier waited on by several threads at different progress must never
+  // get two completions ahead of any of them: hence S-full per tile)
+  constexpr int QF = 0, QE = 2, RF = 4, RE = RF + FWD_RING, SF = RE + FWD_RING, SE = SF + 2,
+                PF = SE + 1, PE = PF + 2, OF = PE + 2, IF = OF + 2, IE = IF + 2, NBAR = IE + 2;
+  constexpr int ROW_WARPS = FWD_THREADS / 32 - 4;
+  int* s_item = reinterpret_cast<int*>(bars + NBAR);   // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_item + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_items = p.nqb * p.heads * p.batch;
+  const int n_items = ((p.nqb + 1) >> 1) * p.heads * p.batch;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBAR; ++i) {
-      const bool rows = i == PFULL || i == OFREE || i == OFREE + 1 || i == MXB || i == LXB;
-      mbar_init(B(i), rows ? 256 : 1);
+      uint32_t cnt = 1;
+      if (i == SE || i == PF || i == PF + 1 || i == OF || i == OF + 1) cnt = 128;
+      if (i == IE || i == IE + 1) cnt = 2 + ROW_WARPS;   // 2 MMA issuers + a lane per row warp
+      mbar_init(B(i), cnt);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -159,252 +240,308 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
+    // ------------------------------------------------------ scheduler, TMA producer
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(FWD_LOW_REGS));
     if (lane == 0) {
       tma_prefetch_desc(&tm);
-      int g = 0, n = 0;
+      int g = 0, ni = 0, nit0 = 0, nit1 = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n) {
-        int qb, hd, b;
-        item_coords(p, item, true, qb, hd, b);
-        const int colq = hd * 3 * p.d;
-        if (!mbar_wait_bounded(B(QEMPTY), (n & 1) ^ 1u, p.status, abort_flag)) break;
-        mbar_arrive_expect_tx(B(QFULL), TILE);
-        for (int a = 0; a < NA; ++a)
-          tma_load_2d(sQ + a * ATOM128, &tm, B(QFULL), colq + 64 * a, b * p.seq + qb * 128);
-        for (int j = 0; j <= qb; ++j, ++g) {
-          const int s = g & 1;
-          const uint32_t ph = (g >> 1) & 1;
-          const int krow = b * p.seq + j * 128;
-          if (!mbar_wait_bounded(B(KEMPTY + s), ph ^ 1u, p.status, abort_flag)) {
+      while (ok) {
+        const int slot = ni & 1;
+        if (ni >= 2 &&
+            !mbar_wait_bounded(B(IE + slot), ((ni >> 1) - 1) & 1, p.status, abort_flag))
+          break;
+        const int k = (int)atomicAdd(p.sched, 1u);
+        s_item[slot] = k;
+        mbar_arrive(B(IF + slot));
+        ++ni;
+        if (k >= n_items) break;
+        const FwdItem it = fwd_item(p, k);
+        const int colq = it.hd * 3 * p.d, row0 = it.b * p.seq;
+        for (int x = 0; x < 2 && ok; ++x) {
+          if (!it.n(x)) continue;
+          const int nq = x ? nit1++ : nit0++;
+          if (nq > 0 && !mbar_wait_bounded(B(QE + x), (nq - 1) & 1, p.status, abort_flag)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(B(KFULL + s), TILE);
+          mbar_arrive_expect_tx(B(QF + x), TILE);
           for (int a = 0; a < NA; ++a)
-            tma_load_2d(sK0 + s * TILE + a * ATOM128, &tm, B(KFULL + s), colq + p.d + 64 * a, krow);
-          if (!mbar_wait_bounded(B(VEMPTY + s), ph ^ 1u, p.status, abort_flag)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(B(VFULL + s), TILE);
-          for (int a = 0; a < NA; ++a)
-            tma_load_2d(sV0 + s * TILE + a * ATOM128, &tm, B(VFULL + s), colq + 2 * p.d + 64 * a,
-                        krow);
+            tma_load_2d(sQ0 + x * TILE + a * ATOM128, &tm, B(QF + x), colq + 64 * a,
+                        row0 + it.qp * 256 + x * 128);
         }
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);
-      const uint32_t id_pv = idesc_bf16_f32(128, p.d, false, true);
-      const uint64_t dQ = desc_kbase(sQ), dK0 = desc_kbase(sK0), dP = desc_kbase(sP);
-      const uint64_t dV0 = desc_mnbase(sV0, ATOM128);
-      int gb = 0, n = 0;
-      bool ok = true;
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n) {
-        int qb, hd, b;
-        item_coords(p, item, true, qb, hd, b);
-        const int nkv = qb + 1;
-        if (!mbar_wait_bounded(B(QFULL), n & 1, p.status, abort_flag)) break;
-        tc_fence_after();
-        // S(block gg) = Q K(gg)^T into S buffer gg % 2
-        auto issue_qk = [&](int j) -> bool {
-          const int gg = gb + j, s = gg & 1;
-          if (!mbar_wait_bounded(B(KFULL + s), (gg >> 1) & 1, p.status, abort_flag)) return false;
-          tc_fence_after();
-          const uint64_t dK = desc_add(dK0, s * TILE);
-#pragma unroll
-          for (int kk = 0; kk < KS; ++kk)
-            tc_mma_bf16(tmem + 128 * s, desc_add(dQ, kmajor_off(kk, ATOM128)),
-                        desc_add(dK, kmajor_off(kk, ATOM128)), id_qk, kk > 0);
-          tc_commit(B(KEMPTY + s));
-          tc_commit(B(SFULL + s));
-          if (j == nkv - 1) tc_commit(B(QEMPTY));
-          return true;
-        };
-        ok = issue_qk(0) && (nkv < 2 || issue_qk(1));
-        const uint32_t tO = tmem + 256 + 128 * (n & 1);
+        const int nkv = it.n0 > it.n1 ? it.n0 : it.n1;
         for (int j = 0; j < nkv && ok; ++j) {
-          const int gg = gb + j, s = gg & 1;
-          if (!mbar_wait_bounded(B(PFULL), gg & 1, p.status, abort_flag)) {
-            ok = false;
-            break;
+          for (int kv = 0; kv < 2; ++kv, ++g) {
+            const int s = g % FWD_RING, use = g / FWD_RING;
+            if (use > 0 && !mbar_wait_bounded(B(RE + s), (use - 1) & 1, p.status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(B(RF + s), TILE);
+            for (int a = 0; a < NA; ++a)
+              tma_load_2d(sR0 + s * TILE + a * ATOM128, &tm, B(RF + s),
+                          colq + (1 + kv) * p.d + 64 * a, row0 + j * 128);
           }
-          if (j == 0 &&
-              !mbar_wait_bounded(B(OFREE + (n & 1)), ((n >> 1) & 1) ^ 1u, p.status, abort_flag)) {
-            ok = false;
-            break;
-          }
-          if (!mbar_wait_bounded(B(VFULL + s), (gg >> 1) & 1, p.status, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t dV = desc_add(dV0, s * TILE);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            tc_mma_bf16(tO, desc_add(dP, kmajor_off(kk, ATOM128)), desc_add(dV, mnmajor_off(kk)),
-                        id_pv, (j > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(B(VEMPTY + s));
-          tc_commit(B(ODONE));
-          if (j + 2 < nkv && !issue_qk(j + 2)) ok = false;
         }
-        gb += nkv;
+      }
+      // the last CTA out leaves the counters at zero for the next launch
+      __threadfence();
+      if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+        atomicExch(p.sched, 0u);
+        atomicExch(p.sched + 1, 0u);
       }
     }
     __syncwarp();
-  } else if (warp >= 4) {
-    const int wg = (warp - 4) >> 2;   // key columns [64 wg, 64 wg + 64) of S
-    const int q4 = warp & 3;
-    const int r = q4 * 32 + lane;     // row = TMEM lane
-    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    int gb = 0, n = 0;
-    bool ok = true;
-    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n) {
-      int qb, hd, b;
-      item_coords(p, item, true, qb, hd, b);
-      const int nkv = qb + 1;
-      const uint32_t tO = tmem + 256 + 128 * (n & 1);
-      float m_used = -INFINITY, l = 0.f;
-      for (int j = 0; j < nkv; ++j) {
-        const int gg = gb + j;
-        // keep bits of this row's 64 keys, drawn while S is not yet in registers
-        uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
-        if (DROP) {
-          const unsigned long long e0 = drop_row(p, b, hd, qb * 128 + r) + j * 128 + wg * 64;
-          keep_lo = drop_bits32(e0, p.drop);
-          keep_hi = drop_bits32(e0 + 32, p.drop);
-          uint32_t* mt = mask_tile(p, b, hd, qb, j);
-          mt[(2 * wg) * 128 + r] = keep_lo;
-          mt[(2 * wg + 1) * 128 + r] = keep_hi;
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------ MMA issuers: warp 1 Q K^T, warp 2 P V
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(FWD_LOW_REGS));
+    if (lane == 0) {
+      const bool is_qk = warp == 1;
+      const uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);
+      const uint32_t id_pv = idesc_bf16_f32(128, D, false, true);
+      const uint64_t dQ0 = desc_kbase(sQ0), dR0 = desc_kbase(sR0);
+      const uint64_t dRmn0 = desc_mnbase(sR0, ATOM128);
+      int g = 0, su = 0, ni = 0;        // ring loads, S uses and items before this item
+      int npv0 = 0, npv1 = 0, nit0 = 0, nit1 = 0;
+      int ring_seen = -1;               // last ring load this thread waited for
+      bool ok = true;
+      auto wait = [&](int bar, int k) -> bool {   // completion k (0-based) of barrier `bar`
+        if (!mbar_wait_bounded(B(bar), k & 1, p.status, abort_flag)) ok = false;
+        return ok;
+      };
+      // ring load gi (K(j) = g + 2j, V(j) = g + 2j + 1) is in shared memory; with an
+      // even ring each slot only ever holds K or only V, so it has a single waiter
+      auto wait_ring = [&](int gi) -> bool {
+        if (gi <= ring_seen) return true;
+        ring_seen = gi;
+        return wait(RF + gi % FWD_RING, gi / FWD_RING);
+      };
+      while (ok) {
+        const int slot = ni & 1;
+        if (!wait(IF + slot, ni >> 1)) break;
+        const int k = *reinterpret_cast<volatile int*>(&s_item[slot]);
+        mbar_arrive(B(IE + slot));
+        ++ni;
+        if (k >= n_items) break;
+        const FwdItem it = fwd_item(p, k);
+        const int nuse = it.n0 + it.n1;
+        const bool last_b = it.n1 > 0;           // tile B is the last reader of K and V
+        for (int v = 0; v < nuse && ok; ++v) {
+          // S use v -> tile x, key block j: A(0) B(0) A(1) B(1) ... [B(n0)]
+          int x, j;
+          if (!last_b) {
+            x = 0;
+            j = v;
+          } else if (v < 2 * it.n0) {
+            x = v & 1;
+            j = v >> 1;
+          } else {
+            x = 1;
+            j = v - it.n0;
+          }
+          if (is_qk) {
+            // S = Q_X K(j)^T once the previous S use has been read
+            const int gk = g + 2 * j, s = gk % FWD_RING;
+            if (j == 0 && !wait(QF + x, x ? nit1 : nit0)) break;
+            if (!wait_ring(gk)) break;
+            if (su + v > 0 && !wait(SE, su + v - 1)) break;
+            tc_fence_after();
+            const uint64_t dQ = desc_add(dQ0, x * TILE), dK = desc_add(dR0, s * TILE);
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk)
+              tc_mma_bf16(tmem + TM_S, desc_add(dQ, kmajor_off(kk, ATOM128)),
+                          desc_add(dK, kmajor_off(kk, ATOM128)), id_qk, kk > 0);
+            tc_commit(B(SF + x));
+            if (j == it.n(x) - 1) tc_commit(B(QE + x));
+            if (x == 1 || !last_b) tc_commit(B(RE + s));
+          } else {
+            // O_X (+)= P_X V(j), P_X read from TMEM
+            const int gv = g + 2 * j + 1, s = gv % FWD_RING;
+            const int nt = x ? nit1 : nit0;
+            if (!wait(PF + x, x ? npv1 : npv0)) break;
+            if (j == 0 && nt > 0 && !wait(OF + x, nt - 1)) break;
+            if (!wait_ring(gv)) break;
+            tc_fence_after();
+            const uint64_t dV = desc_add(dRmn0, s * TILE);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              tc_mma_bf16_ts(tmem + TM_O + 128 * x, tmem + TM_P + 64 * x + 8 * kk,
+                             desc_add(dV, mnmajor_off(kk)), id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(B(PE + x));
+            if (x) ++npv1; else ++npv0;
+            if (x == 1 || !last_b) tc_commit(B(RE + s));
+          }
         }
-        if (!mbar_wait_bounded(B(SFULL + (gg & 1)), (gg >> 1) & 1, p.status, abort_flag)) {
+        if (!ok) break;
+        g += 2 * (it.n0 > it.n1 ? it.n0 : it.n1);
+        su += nuse;
+        if (it.n0) ++nit0;
+        if (it.n1) ++nit1;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 3) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(FWD_LOW_REGS));
+  } else {
+    // ---------------------------------------------------------------- row threads
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(FWD_ROW_REGS));
+    const int x = (warp - 4) >> 2;                 // tile
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;                  // row = TMEM lane
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    const uint32_t tS = tmem + TM_S + lane_off, tP = tmem + TM_P + 64 * x + lane_off;
+    const uint32_t tO = tmem + TM_O + 128 * x + lane_off;
+    int cnt = 0, ni = 0;           // blocks of this tile so far, items read
+    bool ok = true;
+    while (ok) {
+      const int slot = ni & 1;
+      if (!mbar_wait_bounded(B(IF + slot), (ni >> 1) & 1, p.status, abort_flag)) break;
+      const int k = *reinterpret_cast<volatile int*>(&s_item[slot]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(B(IE + slot));
+      ++ni;
+      if (k >= n_items) break;
+      const FwdItem it = fwd_item(p, k);
+      const int nx = it.n(x);
+      const int qb = 2 * it.qp + x;                // 128-row query block of this tile
+      float m_used = -INFINITY, l = 0.f;
+      for (int j = 0; j < nx; ++j) {
+        uint32_t keep[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+        if (DROP) {
+          // keep bits of this row's 128 keys, drawn before S arrives
+          const unsigned long long e0 = drop_row(p, it.b, it.hd, qb * 128 + r) + j * 128;
+          uint32_t* mt = mask_tile(p, it.b, it.hd, qb, j);
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            keep[w] = drop_bits32(e0 + 32 * w, p.drop);
+            mt[w * 128 + r] = keep[w];
+          }
+        }
+        if (!mbar_wait_bounded(B(SF + x), cnt & 1, p.status, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        float s[64];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tmem + 128 * (gg & 1) + lane_off + wg * 64 + c * 32, v);
+        float s[128];
+        {
+          uint32_t v0[32], v1[32], v2[32], v3[32];
+          tmem_ld32(tS, v0);
+          tmem_ld32(tS + 32, v1);
+          tmem_ld32(tS + 64, v2);
+          tmem_ld32(tS + 96, v3);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]) * p.scale_log2;
+          for (int i = 0; i < 32; ++i) {
+            s[i] = __uint_as_float(v0[i]);
+            s[32 + i] = __uint_as_float(v1[i]);
+            s[64 + i] = __uint_as_float(v2[i]);
+            s[96 + i] = __uint_as_float(v3[i]);
+          }
         }
-        if (j == qb) {
+        tc_fence_before();
+        mbar_arrive(B(SE));                        // the S buffer may take the next turn
+        if (j == nx - 1) {                         // diagonal block: keys after the query
 #pragma unroll
-          for (int k = 0; k < 64; ++k)
-            if (wg * 64 + k > r) s[k] = -INFINITY;
+          for (int c = 0; c < 128; ++c)
+            if (c > r) s[c] = -INFINITY;
         }
-        float mxp[8];
+        float mxa[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) mxp[q] = s[q];
+        for (int q = 0; q < 8; ++q) {
+          float a = fmax3(s[q], s[q + 8], s[q + 16]);
 #pragma unroll
-        for (int k = 8; k < 64; ++k) mxp[k & 7] = fmaxf(mxp[k & 7], s[k]);
-        float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
-                         fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
-        // combine the two halves' maxima (buffer gg % 2; a warpgroup cannot run
-        // two blocks ahead of the other because of this barrier)
-        float* mxs = s_mx + (gg & 1) * 256;
-        mxs[wg * 128 + r] = mx;
-        mbar_arrive(B(MXB));
-        if (!mbar_wait_bounded(B(MXB), gg & 1, p.status, abort_flag)) {
-          ok = false;
-          break;
+          for (int t = 3; t < 15; t += 2) a = fmax3(a, s[q + 8 * t], s[q + 8 * t + 8]);
+          mxa[q] = fmaxf(a, s[q + 120]);
         }
-        mx = fmaxf(mxs[r], mxs[128 + r]);
-        const float m_new = fmaxf(m_used, mx);
+        const float mx = fmax3(fmax3(mxa[0], mxa[1], mxa[2]), fmax3(mxa[3], mxa[4], mxa[5]),
+                               fmaxf(mxa[6], mxa[7]));
+        const float m_new = fmaxf(m_used, mx * p.scale_log2);
         // Rescale only when the running maximum grew by more than 2^8: the
         // exponentials stay below 256 and the final O / l is exact either way.
         const bool resc = m_new > m_used + 8.0f;
         const float alpha = resc ? fast_exp2(m_used - m_new) : 1.0f;
         if (resc) m_used = m_new;
-        float rsp[8];
+        const float neg = -m_used;
+        float rs[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) rsp[q] = 0.f;
+        for (int q = 0; q < 8; ++q) rs[q] = 0.f;
 #pragma unroll
-        for (int k = 0; k < 64; ++k) {
-          s[k] = fast_exp2(s[k] - m_used);
-          rsp[k & 7] += s[k];
+        for (int c = 0; c < 128; c += 2) {
+          ffma2(s[c], s[c + 1], s[c], s[c + 1], p.scale_log2, p.scale_log2, neg, neg);
+          s[c] = fast_exp2(s[c]);
+          s[c + 1] = fast_exp2(s[c + 1]);
+          const int q = (c >> 1) & 3;
+          fadd2(rs[2 * q], rs[2 * q + 1], rs[2 * q], rs[2 * q + 1], s[c], s[c + 1]);
         }
-        l = l * alpha + (((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7])));
+        l = l * alpha + (((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7])));
         if (DROP) {
           // dropped probabilities leave the row sum but not P V
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            if (!((keep_lo >> k) & 1u)) s[k] = 0.f;
-            if (!((keep_hi >> k) & 1u)) s[32 + k] = 0.f;
-          }
+          for (int c = 0; c < 128; ++c)
+            if (!((keep[c >> 5] >> (c & 31)) & 1u)) s[c] = 0.f;
         }
-        if (j > 0) {
-          if (!mbar_wait_bounded(B(ODONE), (gg - 1) & 1, p.status, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          if (__any_sync(0xffffffffu, resc)) {
-            for (int c = wg * 32; c < p.d; c += 64) {
-              uint32_t v[32];
-              tmem_ld32(tO + lane_off + c, v);
-              tmem_ld_wait();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-              tmem_st32(tO + lane_off + c, v);
-            }
-            tmem_st_wait();
-          }
+        // P_X and O_X are free once the previous PV of this tile is done
+        if (cnt > 0 && !mbar_wait_bounded(B(PE + x), (cnt - 1) & 1, p.status, abort_flag)) {
+          ok = false;
+          break;
         }
-        // P (bf16) -> shared memory: this half's 64 keys are box `wg`
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const int k = c * 8;
-          st_shared_v4(sP + wg * ATOM128 + sw128_offset(r, c), pack_bf16x2(s[k], s[k + 1]),
-                       pack_bf16x2(s[k + 2], s[k + 3]), pack_bf16x2(s[k + 4], s[k + 5]),
-                       pack_bf16x2(s[k + 6], s[k + 7]));
-        }
-        fence_proxy_async_shared();
-        tc_fence_before();
-        mbar_arrive(B(PFULL));
-      }
-      if (!ok) break;
-      if (!mbar_wait_bounded(B(ODONE), (gb + nkv - 1) & 1, p.status, abort_flag)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      // row sum = the two halves' partial sums
-      float* ls = s_l;
-      ls[wg * 128 + r] = l;
-      mbar_arrive(B(LXB));
-      if (!mbar_wait_bounded(B(LXB), n & 1, p.status, abort_flag)) {
-        ok = false;
-        break;
-      }
-      const float lt = ls[r] + ls[128 + r];
-      const float inv = (DROP ? p.drop.scale : 1.0f) / lt;
-      const int row = b * p.seq + qb * 128 + r;
-      bf16* orow = p.ctx + (size_t)row * p.h + (size_t)hd * p.d;
-      for (int c = wg * 32; c < p.d; c += 64) {
-        uint32_t v[32];
-        tmem_ld32(tO + lane_off + c, v);
-        tmem_ld_wait();
+        tc_fence_after();
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          uint4 u;
-          u.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]) * inv, __uint_as_float(v[q * 8 + 1]) * inv);
-          u.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]) * inv, __uint_as_float(v[q * 8 + 3]) * inv);
-          u.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]) * inv, __uint_as_float(v[q * 8 + 5]) * inv);
-          u.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]) * inv, __uint_as_float(v[q * 8 + 7]) * inv);
-          *reinterpret_cast<uint4*>(orow + c + q * 8) = u;
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(s[32 * q + 2 * c], s[32 * q + 2 * c + 1]);
+          tmem_st16(tP + 16 * q, pk);
         }
+        if (j > 0 && __any_sync(0xffffffffu, resc)) {
+          // O_X *= alpha before PV_X(j) (rare; P is already out of registers)
+#pragma unroll
+          for (int c = 0; c < D; c += 32) {
+            uint32_t v[32];
+            tmem_ld32(tO + c, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            tmem_st32(tO + c, v);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(B(PF + x));
+        ++cnt;
       }
-      if (wg == 0)
-        p.lse[((size_t)b * p.heads + hd) * p.seq + qb * 128 + r] = (m_used + __log2f(lt)) * LN2;
-      tc_fence_before();
-      mbar_arrive(B(OFREE + (n & 1)));
-      gb += nkv;
+      if (!ok) break;
+      if (nx) {
+        // epilogue: O_X / l once the last PV_X is done
+        if (!mbar_wait_bounded(B(PE + x), (cnt - 1) & 1, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float inv = (DROP ? p.drop.scale : 1.0f) / l;
+        const int row = it.b * p.seq + qb * 128 + r;
+        bf16* orow = p.ctx + (size_t)row * p.h + (size_t)it.hd * D;
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(tO + c, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]) * inv, __uint_as_float(v[q * 8 + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]) * inv, __uint_as_float(v[q * 8 + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]) * inv, __uint_as_float(v[q * 8 + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]) * inv, __uint_as_float(v[q * 8 + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + c + q * 8) = w;
+          }
+        }
+        p.lse[((size_t)it.b * p.heads + it.hd) * p.seq + qb * 128 + r] =
+            (m_used + __log2f(l)) * LN2;
+        tc_fence_before();
+        mbar_arrive(B(OF + x));
+      }
     }
     __syncwarp();
   }
@@ -991,7 +1128,7 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uin
 }
 
 size_t fwd_smem(int na) {
-  const size_t need = (size_t)5 * na * ATOM128 + 2 * ATOM128 + 3072 + 256 + 1024;
+  const size_t need = (size_t)(2 + FWD_RING) * na * ATOM128 + 256 + 1024;
   return need < 120 * 1024 ? 120 * 1024 : need;   // one CTA per SM (512 TMEM columns)
 }
 // The backward kernels hold all 512 TMEM columns: their shared memory requests
@@ -1025,12 +1162,23 @@ Params make_params(int batch, int seq, int heads, int d, unsigned* status, const
   p.dsum = nullptr;
   p.status = status;
   p.mask = nullptr;
+  p.sched = nullptr;
+  p.chunk = 1;
   return p;
 }
 
 template <typename K>
 cudaError_t set_smem(K kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+// A kernel with a setmaxnreg split must start with exactly the registers the
+// split was sized for, or setmaxnreg.inc could never be satisfied.
+template <typename K>
+cudaError_t check_regs(K kernel, int regs) {
+  cudaFuncAttributes fa;
+  const cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+  if (e != cudaSuccess) return e;
+  return fa.numRegs == regs ? cudaSuccess : cudaErrorInvalidConfiguration;
 }
 
 }  // namespace attn
@@ -1055,7 +1203,14 @@ cudaError_t attn_fwd_tc(const void* qkv, void* ctx, float* lse, int batch, int s
   p.mask = mask;
   p.ctx = static_cast<bf16*>(ctx);
   p.lse = lse;
-  const int items = p.nqb * heads * batch;
+  p.sched = status + kSchedFwd;
+  // pairs whose K/V (NA 128-byte boxes per row) fit in about 48 MB of L2
+  {
+    const size_t kv = 2ull * seq * (d > 64 ? 2 : 1) * 128;
+    const size_t c = ((size_t)48 << 20) / kv;
+    p.chunk = c < 1 ? 1 : (c > (size_t)batch * heads ? batch * heads : (int)c);
+  }
+  const int items = ((p.nqb + 1) / 2) * heads * batch;
   const int grid = items < c.num_sms ? items : c.num_sms;
   const double flops = 2.0 * 2.0 * batch * heads * d * ((double)seq * (seq + 1) / 2.0);
   cudaError_t e;
@@ -1063,6 +1218,8 @@ cudaError_t attn_fwd_tc(const void* qkv, void* ctx, float* lse, int batch, int s
   {                                                                                      \
     const size_t sm = fwd_smem(NA_);                                                     \
     if ((e = set_smem(attn_fwd_tc_kernel<NA_, KS_, DR_>, sm)) != cudaSuccess) return e;  \
+    if ((e = check_regs(attn_fwd_tc_kernel<NA_, KS_, DR_>, FWD_LAUNCH_REGS)) != cudaSuccess) \
+      return e;                                                                          \
     c.before(KK_ATTN_FWD, flops);                                                        \
     attn_fwd_tc_kernel<NA_, KS_, DR_><<<grid, FWD_THREADS, sm, c.stream>>>(tm, p);       \
   }
