@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
   // (a barrier waited on by several threads at different progress must never
   // get two completions ahead of any of them: hence S-full per tile)
   constexpr int QF = 0, QE = 2, RF = 4, RE = RF + FWD_RING, SF = RE + FWD_RING, SE = SF + 2,
-                PF = SE + 1, PE = PF + 2, OF = PE + 2, IF = OF + 2, IE = IF + 2, NBAR = IE + 2;
+                PF = SE + 1, PE = PF + 2, IF = PE + 2, IE = IF + 2, NBAR = IE + 2;
   constexpr int ROW_WARPS = FWD_THREADS / 32 - 4;
   int* s_item = reinterpret_cast<int*>(bars + NBAR);   // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_item + 2);
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBAR; ++i) {
       uint32_t cnt = 1;
-      if (i == SE || i == PF || i == PF + 1 || i == OF || i == OF + 1) cnt = 128;
+      if (i == SE || i == PF || i == PF + 1) cnt = 128;
       if (i == IE || i == IE + 1) cnt = 2 + ROW_WARPS;   // 2 MMA issuers + a lane per row warp
       mbar_init(B(i), cnt);
     }
@@ -357,10 +357,9 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             if (x == 1 || !last_b) tc_commit(B(RE + s));
           } else {
             // O_X (+)= P_X V(j), P_X read from TMEM
+            // (PF_X of a tile's first block also means its last epilogue read O_X)
             const int gv = g + 2 * j + 1, s = gv % FWD_RING;
-            const int nt = x ? nit1 : nit0;
             if (!wait(PF + x, x ? npv1 : npv0)) break;
-            if (j == 0 && nt > 0 && !wait(OF + x, nt - 1)) break;
             if (!wait_ring(gv)) break;
             tc_fence_after();
             const uint64_t dV = desc_add(dRmn0, s * TILE);
@@ -393,10 +392,39 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     const uint32_t tS = tmem + TM_S + lane_off, tP = tmem + TM_P + 64 * x + lane_off;
     const uint32_t tO = tmem + TM_O + 128 * x + lane_off;
     int cnt = 0, ni = 0;           // blocks of this tile so far, items read
+    // A tile's epilogue (O / l to ctx, lse) runs when the tile's next item has
+    // its first P block computed: the last PV of the item is done by then, and
+    // PV_X(0) of the next item waits for that P block, so O_X is read first.
+    bool pend = false;
+    float pm = 0.f, pl = 1.f;
+    size_t po = 0, plse = 0;       // ctx offset of the row's head slice, lse index
+    auto epilogue = [&]() {
+      const float inv = (DROP ? p.drop.scale : 1.0f) / pl;
+      bf16* orow = p.ctx + po;
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {   // one 32-column chunk live at a time
+        uint32_t v[32];
+        tmem_ld32(tO + c, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]) * inv, __uint_as_float(v[q * 8 + 1]) * inv);
+          w.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]) * inv, __uint_as_float(v[q * 8 + 3]) * inv);
+          w.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]) * inv, __uint_as_float(v[q * 8 + 5]) * inv);
+          w.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]) * inv, __uint_as_float(v[q * 8 + 7]) * inv);
+          *reinterpret_cast<uint4*>(orow + c + q * 8) = w;
+        }
+      }
+      p.lse[plse] = (pm + __log2f(pl)) * LN2;
+    };
     bool ok = true;
     while (ok) {
       const int slot = ni & 1;
-      if (!mbar_wait_bounded(B(IF + slot), (ni >> 1) & 1, p.status, abort_flag)) break;
+      if (!mbar_wait_bounded(B(IF + slot), (ni >> 1) & 1, p.status, abort_flag)) {
+        ok = false;
+        break;
+      }
       const int k = *reinterpret_cast<volatile int*>(&s_item[slot]);
       __syncwarp();
       if (lane == 0) mbar_arrive(B(IE + slot));
@@ -463,39 +491,45 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         const float alpha = resc ? fast_exp2(m_used - m_new) : 1.0f;
         if (resc) m_used = m_new;
         const float neg = -m_used;
-        float rs[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) rs[q] = 0.f;
-#pragma unroll
-        for (int c = 0; c < 128; c += 2) {
-          ffma2(s[c], s[c + 1], s[c], s[c + 1], p.scale_log2, p.scale_log2, neg, neg);
-          s[c] = fast_exp2(s[c]);
-          s[c + 1] = fast_exp2(s[c + 1]);
-          const int q = (c >> 1) & 3;
-          fadd2(rs[2 * q], rs[2 * q + 1], rs[2 * q], rs[2 * q + 1], s[c], s[c + 1]);
-        }
-        l = l * alpha + (((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7])));
-        if (DROP) {
-          // dropped probabilities leave the row sum but not P V
-#pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (!((keep[c >> 5] >> (c & 31)) & 1u)) s[c] = 0.f;
-        }
         // P_X and O_X are free once the previous PV of this tile is done
         if (cnt > 0 && !mbar_wait_bounded(B(PE + x), (cnt - 1) & 1, p.status, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        if (j == 0 && pend) {
+          epilogue();
+          pend = false;
+        }
+        // exponentials and row sum a 32-key chunk at a time, each chunk's bf16
+        // P stored into TMEM while the next one is computed
+        float rs[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) rs[q] = 0.f;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
+#pragma unroll
+          for (int c = 32 * q; c < 32 * q + 32; c += 2) {
+            ffma2(s[c], s[c + 1], s[c], s[c + 1], p.scale_log2, p.scale_log2, neg, neg);
+            s[c] = fast_exp2(s[c]);
+            s[c + 1] = fast_exp2(s[c + 1]);
+            const int e = (c >> 1) & 3;
+            fadd2(rs[2 * e], rs[2 * e + 1], rs[2 * e], rs[2 * e + 1], s[c], s[c + 1]);
+          }
+          if (DROP) {
+            // dropped probabilities leave the row sum but not P V
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (!((keep[q] >> c) & 1u)) s[32 * q + c] = 0.f;
+          }
           uint32_t pk[16];
 #pragma unroll
           for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(s[32 * q + 2 * c], s[32 * q + 2 * c + 1]);
           tmem_st16(tP + 16 * q, pk);
         }
+        l = l * alpha + (((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7])));
         if (j > 0 && __any_sync(0xffffffffu, resc)) {
-          // O_X *= alpha before PV_X(j) (rare; P is already out of registers)
+          // O_X *= alpha before PV_X(j) (rare)
 #pragma unroll
           for (int c = 0; c < D; c += 32) {
             uint32_t v[32];
@@ -513,34 +547,17 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
       }
       if (!ok) break;
       if (nx) {
-        // epilogue: O_X / l once the last PV_X is done
-        if (!mbar_wait_bounded(B(PE + x), (cnt - 1) & 1, p.status, abort_flag)) {
-          ok = false;
-          break;
-        }
+        pend = true;
+        pm = m_used;
+        pl = l;
+        po = (size_t)(it.b * p.seq + qb * 128 + r) * p.h + (size_t)it.hd * D;
+        plse = ((size_t)it.b * p.heads + it.hd) * p.seq + qb * 128 + r;
+      }
+    }
+    if (ok && pend) {
+      if (mbar_wait_bounded(B(PE + x), (cnt - 1) & 1, p.status, abort_flag)) {
         tc_fence_after();
-        const float inv = (DROP ? p.drop.scale : 1.0f) / l;
-        const int row = it.b * p.seq + qb * 128 + r;
-        bf16* orow = p.ctx + (size_t)row * p.h + (size_t)it.hd * D;
-#pragma unroll
-        for (int c = 0; c < D; c += 32) {
-          uint32_t v[32];
-          tmem_ld32(tO + c, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]) * inv, __uint_as_float(v[q * 8 + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]) * inv, __uint_as_float(v[q * 8 + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]) * inv, __uint_as_float(v[q * 8 + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]) * inv, __uint_as_float(v[q * 8 + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + c + q * 8) = w;
-          }
-        }
-        p.lse[((size_t)it.b * p.heads + it.hd) * p.seq + qb * 128 + r] =
-            (m_used + __log2f(l)) * LN2;
-        tc_fence_before();
-        mbar_arrive(B(OF + x));
+        epilogue();
       }
     }
     __syncwarp();
