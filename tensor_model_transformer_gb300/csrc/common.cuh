@@ -62,6 +62,24 @@ template <> struct Vec<bf16> {
     bf16* h = reinterpret_cast<bf16*>(&raw);
     h[i] = __float2bfloat16_rn(v);
   }
+  // all N elements to / from fp32 (a bf16 is the high half of an fp32 word)
+  __device__ __forceinline__ void unpack(float (&f)[N]) const {
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+  __device__ __forceinline__ void pack(const float (&f)[N]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 v = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t*>(&v);
+    }
+    raw = make_uint4(w[0], w[1], w[2], w[3]);
+  }
 };
 template <> struct Vec<float> {
   static constexpr int N = 4;
@@ -70,6 +88,13 @@ template <> struct Vec<float> {
   __device__ __forceinline__ void store(float* p) const { *reinterpret_cast<float4*>(p) = raw; }
   __device__ __forceinline__ float get(int i) const { return (&raw.x)[i]; }
   __device__ __forceinline__ void set(int i, float v) { (&raw.x)[i] = v; }
+  __device__ __forceinline__ void unpack(float (&f)[N]) const {
+    f[0] = raw.x;
+    f[1] = raw.y;
+    f[2] = raw.z;
+    f[3] = raw.w;
+  }
+  __device__ __forceinline__ void pack(const float (&f)[N]) { raw = make_float4(f[0], f[1], f[2], f[3]); }
 };
 
 __device__ __forceinline__ float warp_sum(float v) {

@@ -13,8 +13,10 @@ namespace mtl {
 namespace {
 
 constexpr int kLnThreadsMax = 512;
-constexpr int kLnBwdBlocks = 512;     // row blocks of the dgamma/dbeta reduction
-constexpr int kColsumBlocks = 128;    // row blocks of the bias-gradient reduction
+constexpr int kLnBwdBlocks = 512;     // most row blocks of the dgamma/dbeta reduction
+constexpr int kLnBwdPerSM = 2;        // LN backward blocks per SM (one wave)
+constexpr int kLnBwdThreadsMax = 512; // threads per row of the LN backward
+constexpr int kColsumThreads = 256;   // threads per block of the bias-gradient column sums
 constexpr int kColsumDropBlocks = 512;  // the same with dropout (Philox work per element)
 
 // Sums NV values over the block in place; `red` holds NV*32 floats.  Every
@@ -40,9 +42,10 @@ __device__ __forceinline__ void block_sum_n(float (&v)[NV], float* red) {
 }
 
 // R rows per iteration: the loads of all R rows are issued before the block
-// reductions, so each thread keeps R*V 16-byte loads in flight.
+// reductions, so each thread keeps R*V 16-byte loads in flight.  Each element
+// is converted to fp32 once; gamma and beta are held as fp32 for all rows.
 template <typename T, int V, int R>
-__global__ void __launch_bounds__(kLnThreadsMax)
+__global__ void __launch_bounds__(kLnThreadsMax, V == 1 ? 4 : 1)   // short rows: 32 registers
     ln_fwd_kernel(const T* __restrict__ x, const T* __restrict__ gamma, const T* __restrict__ beta,
                   T* __restrict__ u, float* __restrict__ mean_out, float* __restrict__ rstd_out,
                   int n, int h, float eps, int rows_per_block) {
@@ -54,8 +57,26 @@ __global__ void __launch_bounds__(kLnThreadsMax)
   const int r_begin = blockIdx.x * rows_per_block;
   const int r_end = min(n, r_begin + rows_per_block);
   const float inv_h = 1.0f / (float)h;
+  // gamma and beta are reloaded (from L1) for every row: holding them in
+  // registers would cost occupancy, which this latency-bound kernel needs more
+  constexpr bool GB_REG = false;
+  constexpr int VG = GB_REG ? V : 1;
+  float gf[VG][E], bf[VG][E];
+  if (GB_REG) {
+#pragma unroll
+    for (int i = 0; i < VG; ++i) {
+      const int vi = threadIdx.x + i * blockDim.x;
+      if (vi < nvec) {
+        Vec<T> tg, tb;
+        tg.load(gamma + vi * E);
+        tb.load(beta + vi * E);
+        tg.unpack(gf[i]);
+        tb.unpack(bf[i]);
+      }
+    }
+  }
   for (int r0 = r_begin; r0 < r_end; r0 += R) {
-    Vec<T> xv[R][V];
+    float xf[R][V][E];
     float s[R];
 #pragma unroll
     for (int rr = 0; rr < R; ++rr) {
@@ -64,9 +85,11 @@ __global__ void __launch_bounds__(kLnThreadsMax)
       for (int i = 0; i < V; ++i) {
         const int vi = threadIdx.x + i * blockDim.x;
         if (r0 + rr < r_end && vi < nvec) {
-          xv[rr][i].load(x + (size_t)(r0 + rr) * h + vi * E);
+          Vec<T> xv;
+          xv.load(x + (size_t)(r0 + rr) * h + vi * E);
+          xv.unpack(xf[rr][i]);
 #pragma unroll
-          for (int e = 0; e < E; ++e) s[rr] += xv[rr][i].get(e);
+          for (int e = 0; e < E; ++e) s[rr] += xf[rr][i][e];
         }
       }
     }
@@ -82,7 +105,7 @@ __global__ void __launch_bounds__(kLnThreadsMax)
         if (r0 + rr < r_end && vi < nvec) {
 #pragma unroll
           for (int e = 0; e < E; ++e) {
-            const float dlt = xv[rr][i].get(e) - mean[rr];
+            const float dlt = xf[rr][i][e] - mean[rr];
             ss[rr] += dlt * dlt;
           }
         }
@@ -90,20 +113,32 @@ __global__ void __launch_bounds__(kLnThreadsMax)
     }
     block_sum_n<R>(ss, red);
 #pragma unroll
-    for (int i = 0; i < V; ++i) {
-      const int vi = threadIdx.x + i * blockDim.x;
-      if (vi >= nvec) continue;
-      Vec<T> tg, tb;
-      tg.load(gamma + vi * E);
-      tb.load(beta + vi * E);
+    for (int rr = 0; rr < R; ++rr) {
+      if (r0 + rr >= r_end) continue;
+      const float rs = 1.0f / sqrtf(ss[rr] * inv_h + eps);
 #pragma unroll
-      for (int rr = 0; rr < R; ++rr) {
-        if (r0 + rr >= r_end) continue;
-        const float rs = 1.0f / sqrtf(ss[rr] * inv_h + eps);
+      for (int i = 0; i < V; ++i) {
+        const int vi = threadIdx.x + i * blockDim.x;
+        if (vi >= nvec) continue;
+        float gv[E], bv[E];
+        if (GB_REG) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            gv[e] = gf[GB_REG ? i : 0][e];
+            bv[e] = bf[GB_REG ? i : 0][e];
+          }
+        } else {
+          Vec<T> tg, tb;
+          tg.load(gamma + vi * E);
+          tb.load(beta + vi * E);
+          tg.unpack(gv);
+          tb.unpack(bv);
+        }
+        float of[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) of[e] = (xf[rr][i][e] - mean[rr]) * rs * gv[e] + bv[e];
         Vec<T> o;
-#pragma unroll
-        for (int e = 0; e < E; ++e)
-          o.set(e, (xv[rr][i].get(e) - mean[rr]) * rs * tg.get(e) + tb.get(e));
+        o.pack(of);
         o.store(u + (size_t)(r0 + rr) * h + vi * E);
       }
     }
@@ -119,9 +154,11 @@ __global__ void __launch_bounds__(kLnThreadsMax)
   }
 }
 
-// Dynamic shared memory: the block's running column sums of du * xhat and du
-// (2 * h floats); thread i owns the same columns in every row, so the sums need
-// no atomics.  R rows per iteration, their loads issued before the reduction.
+// Each block sums du * xhat and du over its rows for the dgamma / dbeta
+// partials; a thread owns the same columns in every row, so the sums need no
+// atomics and keep row order.  Short rows (V <= 2) keep those sums and gamma in
+// registers; longer rows keep the sums in dynamic shared memory (2 * h floats).
+// R rows per iteration, their loads issued before the reduction.
 // MODE 0: du fp32, dx = resid + LN_bwd(du) (Pre-LN);  MODE 1: du = du2 (of type
 // T), dx = LN_bwd(du);  MODE 2: du = du (fp32) + du2 (T), dx = LN_bwd(du) (the
 // Post-LN layer's two LayerNorms).
@@ -133,26 +170,43 @@ __global__ void __launch_bounds__(kLnThreadsMax)
                   float* __restrict__ part_g, float* __restrict__ part_b, int n, int h,
                   int rows_per_block) {
   constexpr int E = Vec<T>::N;
+  constexpr bool ACC_REG = V <= 2;
+  constexpr int VA = ACC_REG ? V : 1;
   extern __shared__ float lsm[];
   float* acc_g = lsm;
   float* acc_b = lsm + h;
   __shared__ float red[2 * R * 32];
   const int nvec = h / E;
-  // accumulator layout [e][vi]: consecutive threads touch consecutive words
-  for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+  float ag[VA][E], ab[VA][E], gf[VA][E];
+  if (ACC_REG) {
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      acc_g[e * nvec + vi] = 0.f;
-      acc_b[e * nvec + vi] = 0.f;
+    for (int i = 0; i < VA; ++i) {
+      const int vi = threadIdx.x + i * blockDim.x;
+#pragma unroll
+      for (int e = 0; e < E; ++e) ag[i][e] = ab[i][e] = gf[i][e] = 0.f;
+      if (vi < nvec) {
+        Vec<T> tg;
+        tg.load(gamma + vi * E);
+        tg.unpack(gf[i]);
+      }
+    }
+  } else {
+    // accumulator layout [e][vi]: consecutive threads touch consecutive words;
+    // each thread reads back only the columns it wrote: no barrier needed
+    for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        acc_g[e * nvec + vi] = 0.f;
+        acc_b[e * nvec + vi] = 0.f;
+      }
     }
   }
-  // each thread reads back only the columns it wrote: no barrier needed
   const int r_begin = blockIdx.x * rows_per_block;
   const int r_end = min(n, r_begin + rows_per_block);
   const float inv_h = 1.0f / (float)h;
   for (int r0 = r_begin; r0 < r_end; r0 += R) {
-    Vec<T> xv[R][V], rv[R][V];
-    float dd[R][V][E];
+    Vec<T> rv[R][V];
+    float xh[R][V][E], dd[R][V][E];
     float mu[R], rs[R], s[2 * R];
 #pragma unroll
     for (int rr = 0; rr < R; ++rr) {
@@ -166,7 +220,9 @@ __global__ void __launch_bounds__(kLnThreadsMax)
         const int vi = threadIdx.x + i * blockDim.x;
         if (live && vi < nvec) {
           const size_t off = (size_t)(r0 + rr) * h + vi * E;
-          xv[rr][i].load(x + off);
+          Vec<T> xv;
+          xv.load(x + off);
+          xv.unpack(xh[rr][i]);
           if (MODE == 0) rv[rr][i].load(resid + off);
           if (MODE != 1) {
 #pragma unroll
@@ -181,9 +237,10 @@ __global__ void __launch_bounds__(kLnThreadsMax)
           if (MODE != 0) {
             Vec<T> d2;
             d2.load(du2 + off);
+            float f2[E];
+            d2.unpack(f2);
 #pragma unroll
-            for (int e = 0; e < E; ++e)
-              dd[rr][i][e] = (MODE == 2 ? dd[rr][i][e] : 0.f) + d2.get(e);
+            for (int e = 0; e < E; ++e) dd[rr][i][e] = (MODE == 2 ? dd[rr][i][e] : 0.f) + f2[e];
           }
         }
       }
@@ -192,17 +249,24 @@ __global__ void __launch_bounds__(kLnThreadsMax)
     for (int i = 0; i < V; ++i) {
       const int vi = threadIdx.x + i * blockDim.x;
       if (vi >= nvec) continue;
-      Vec<T> tg;
-      tg.load(gamma + vi * E);
+      float gv[E];
+      if (ACC_REG) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) gv[e] = gf[ACC_REG ? i : 0][e];
+      } else {
+        Vec<T> tg;
+        tg.load(gamma + vi * E);
+        tg.unpack(gv);
+      }
 #pragma unroll
       for (int rr = 0; rr < R; ++rr) {
         if (r0 + rr >= r_end) continue;
 #pragma unroll
         for (int e = 0; e < E; ++e) {
-          const float xh = (xv[rr][i].get(e) - mu[rr]) * rs[rr];
-          const float gd = dd[rr][i][e] * tg.get(e);
+          xh[rr][i][e] = (xh[rr][i][e] - mu[rr]) * rs[rr];
+          const float gd = dd[rr][i][e] * gv[e];
           s[2 * rr] += gd;
-          s[2 * rr + 1] += gd * xh;
+          s[2 * rr + 1] += gd * xh[rr][i][e];
         }
       }
     }
@@ -211,47 +275,88 @@ __global__ void __launch_bounds__(kLnThreadsMax)
     for (int i = 0; i < V; ++i) {
       const int vi = threadIdx.x + i * blockDim.x;
       if (vi >= nvec) continue;
-      Vec<T> tg;
-      tg.load(gamma + vi * E);
-      float ag[E], ab[E];
+      float gv[E];
+      if (ACC_REG) {
 #pragma unroll
-      for (int e = 0; e < E; ++e) ag[e] = ab[e] = 0.f;
+        for (int e = 0; e < E; ++e) gv[e] = gf[ACC_REG ? i : 0][e];
+      } else {
+        Vec<T> tg;
+        tg.load(gamma + vi * E);
+        tg.unpack(gv);
+      }
+      float sg[E], sb[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) sg[e] = sb[e] = 0.f;
 #pragma unroll
       for (int rr = 0; rr < R; ++rr) {
         if (r0 + rr >= r_end) continue;
         const float m1 = s[2 * rr] * inv_h, m2 = s[2 * rr + 1] * inv_h;
-        Vec<T> o;
+        float rf[E], of[E];
+        if (MODE == 0) rv[rr][i].unpack(rf);
 #pragma unroll
         for (int e = 0; e < E; ++e) {
-          const float xh = (xv[rr][i].get(e) - mu[rr]) * rs[rr];
-          const float gd = dd[rr][i][e] * tg.get(e);
-          o.set(e, (MODE == 0 ? rv[rr][i].get(e) : 0.f) + rs[rr] * (gd - m1 - xh * m2));
-          ag[e] += dd[rr][i][e] * xh;
-          ab[e] += dd[rr][i][e];
+          const float gd = dd[rr][i][e] * gv[e];
+          of[e] = (MODE == 0 ? rf[e] : 0.f) + rs[rr] * (gd - m1 - xh[rr][i][e] * m2);
+          sg[e] += dd[rr][i][e] * xh[rr][i][e];
+          sb[e] += dd[rr][i][e];
         }
+        Vec<T> o;
+        o.pack(of);
         o.store(dx + (size_t)(r0 + rr) * h + vi * E);
       }
+      if (ACC_REG) {
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        acc_g[e * nvec + vi] += ag[e];
-        acc_b[e * nvec + vi] += ab[e];
+        for (int e = 0; e < E; ++e) {
+          ag[ACC_REG ? i : 0][e] += sg[e];
+          ab[ACC_REG ? i : 0][e] += sb[e];
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          acc_g[e * nvec + vi] += sg[e];
+          acc_b[e * nvec + vi] += sb[e];
+        }
       }
     }
   }
-  for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+  if (ACC_REG) {
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      part_g[(size_t)blockIdx.x * h + vi * E + e] = acc_g[e * nvec + vi];
-      part_b[(size_t)blockIdx.x * h + vi * E + e] = acc_b[e * nvec + vi];
+    for (int i = 0; i < VA; ++i) {
+      const int vi = threadIdx.x + i * blockDim.x;
+      if (vi >= nvec) continue;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        part_g[(size_t)blockIdx.x * h + vi * E + e] = ag[i][e];
+        part_b[(size_t)blockIdx.x * h + vi * E + e] = ab[i][e];
+      }
+    }
+  } else {
+    for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        part_g[(size_t)blockIdx.x * h + vi * E + e] = acc_g[e * nvec + vi];
+        part_b[(size_t)blockIdx.x * h + vi * E + e] = acc_b[e * nvec + vi];
+      }
     }
   }
 }
 
+// Row blocks of a column sum over n rows of N columns with E elements a
+// thread: about 1024 blocks in all (several waves on any SM count), between
+// 128 and 512 row blocks; rows_blocks * N stays within 1024 * 2048 floats for
+// N up to 16384.
+int colsum_row_blocks(int n, int N, int E) {
+  const int cb = (N / E + kColsumThreads - 1) / kColsumThreads;
+  int b = 1024 / (cb > 0 ? cb : 1);
+  b = b < 128 ? 128 : (b > 512 ? 512 : b);
+  return n < b ? (n > 0 ? n : 1) : b;
+}
+
 // out[c] = sum over row blocks b = 0..nblk-1 of part[b*N + c].  One CTA per
-// 32 columns: warp w sums the row blocks w, w+8, w+16, ... (coalesced 128-byte
-// rows), then the 8 warp sums are added in warp order: a fixed order for any
-// launch.
-constexpr int kFinWarps = 8;
+// 32 columns: warp w sums the row blocks w, w+32, w+64, ... (coalesced 128-byte
+// rows, several loads in flight), then the 32 warp sums are added in warp
+// order: a fixed order for any launch.
+constexpr int kFinWarps = 32;
 __global__ void __launch_bounds__(kFinWarps * 32)
     finalize_cols_kernel(const float* __restrict__ part, int nblk, int N,
                          float* __restrict__ out) {
@@ -259,8 +364,10 @@ __global__ void __launch_bounds__(kFinWarps * 32)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int c = blockIdx.x * 32 + lane;
   float s = 0.f;
-  if (c < N)
+  if (c < N) {
+#pragma unroll 4
     for (int b = warp; b < nblk; b += kFinWarps) s += part[(size_t)b * N + c];
+  }
   red[warp][lane] = s;
   __syncthreads();
   if (warp == 0 && c < N) {
@@ -282,11 +389,15 @@ __global__ void colsum_partial_kernel(const T* __restrict__ Y, int64_t ld, int n
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   const int r0 = blockIdx.y * rows_per_block;
   const int r1 = min(n, r0 + rows_per_block);
+  // unrolled so that 8 row loads are in flight; the adds keep row order
+#pragma unroll 8
   for (int r = r0; r < r1; ++r) {
     Vec<T> v;
     v.load(Y + (size_t)r * ld + c0);
+    float f[E];
+    v.unpack(f);
 #pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] += v.get(e);
+    for (int e = 0; e < E; ++e) acc[e] += f[e];
   }
 #pragma unroll
   for (int e = 0; e < E; ++e) part[(size_t)blockIdx.y * N + c0 + e] = acc[e];
@@ -325,10 +436,10 @@ __global__ void colsum_dropout_partial_kernel(const T* __restrict__ Y, T* __rest
 
 // Vectors per thread and threads per block for a row of h elements.
 template <typename T>
-void row_plan(int h, int* vpt, int* threads) {
+void row_plan(int h, int* vpt, int* threads, int max_threads = kLnThreadsMax) {
   const int nvec = h / Vec<T>::N;
   int v = 1;
-  while ((nvec + v - 1) / v > kLnThreadsMax) v *= 2;
+  while ((nvec + v - 1) / v > max_threads) v *= 2;
   *vpt = v;
   *threads = (((nvec + v - 1) / v) + 31) / 32 * 32;
 }
@@ -350,7 +461,7 @@ cudaError_t ln_fwd_t(const void* x, const void* g, const void* b, void* u, float
   cudaError_t e = cudaSuccess;
   switch (vpt) {
     LN_FWD_CASE(1, 1)
-    LN_FWD_CASE(2, 2)
+    LN_FWD_CASE(2, 1)
     LN_FWD_CASE(4, 1)
     LN_FWD_CASE(8, 1)
     default:
@@ -367,12 +478,15 @@ cudaError_t ln_bwd_t(const float* du, const void* du2, const void* x, const floa
                      const float* rstd, const void* g, const void* resid, void* dx, float* dgamma,
                      float* dbeta, float* partial, int n, int h, const LaunchCtx& c) {
   int vpt, threads;
-  row_plan<T>(h, &vpt, &threads);
-  const int nblk = n < kLnBwdBlocks ? (n > 0 ? n : 1) : kLnBwdBlocks;
+  row_plan<T>(h, &vpt, &threads, kLnBwdThreadsMax);
+  // one wave of kLnBwdPerSM blocks per SM, at most kLnBwdBlocks (the partial
+  // buffer's rows)
+  const int want = kLnBwdPerSM * c.num_sms < kLnBwdBlocks ? kLnBwdPerSM * c.num_sms : kLnBwdBlocks;
+  const int nblk = n < want ? (n > 0 ? n : 1) : want;
   const int rows = (n + nblk - 1) / nblk;
   float* pg = partial;
   float* pb = partial + (size_t)nblk * h;
-  const size_t smem = 2 * (size_t)h * sizeof(float);
+  const size_t smem = vpt <= 2 ? 0 : 2 * (size_t)h * sizeof(float);
   c.before(KK_LN_BWD, (double)n * h * (3.0 * sizeof(T) + 4.0) + 8.0 * n);
 #define LN_BWD_CASE(VV, RR)                                                                 \
   case VV:                                                                                  \
@@ -388,7 +502,7 @@ cudaError_t ln_bwd_t(const float* du, const void* du2, const void* x, const floa
     break;
   switch (vpt) {
     LN_BWD_CASE(1, 1)
-    LN_BWD_CASE(2, 2)
+    LN_BWD_CASE(2, 1)
     LN_BWD_CASE(4, 1)
     LN_BWD_CASE(8, 1)
     default:
@@ -411,9 +525,9 @@ template <typename T>
 cudaError_t colsum_t(const void* Y, int64_t ld, int n, int N, float* out, float* partial,
                      const LaunchCtx& c) {
   constexpr int E = Vec<T>::N;
-  const int nblk = n < kColsumBlocks ? (n > 0 ? n : 1) : kColsumBlocks;
+  const int nblk = colsum_row_blocks(n, N, E);
   const int rows = (n + nblk - 1) / nblk;
-  const int threads = 256;
+  const int threads = kColsumThreads;
   dim3 grid((N / E + threads - 1) / threads, nblk);
   c.before(KK_COLSUM, (double)n * N * sizeof(T));
   colsum_partial_kernel<T><<<grid, threads, 0, c.stream>>>((const T*)Y, ld, n, N, rows, partial);
@@ -454,8 +568,8 @@ size_t colsum_dropout_partial_floats(int n, int N) {
   return nblk * (size_t)N;
 }
 size_t colsum_partial_floats(int n, int N) {
-  const size_t nblk = n < kColsumBlocks ? (n > 0 ? n : 1) : kColsumBlocks;
-  return nblk * (size_t)N;
+  // the bf16 plan (8 elements a thread) has the most row blocks for a width
+  return (size_t)colsum_row_blocks(n, N, 8) * N;
 }
 
 cudaError_t ln_fwd(int dtype, const void* x, const void* g, const void* b, void* u, float* mean,

@@ -267,9 +267,10 @@ WsLayout ws_layout(const Dims& D) {
   // dropped-out gradient of the fc2 output, later of the out-proj output
   W.gmask = take(D.p_hidden > 0.f ? nh * D.esz : 0);
   size_t pf = ln_bwd_partial_floats((int)D.n, (int)D.h);
-  const size_t widest = (size_t)(D.f > 3 * D.h ? D.f : 3 * D.h);
-  const size_t pc = colsum_partial_floats((int)D.n, (int)widest);
-  if (pc > pf) pf = pc;
+  for (const int64_t N : {D.h, D.f, 3 * D.h}) {   // the bias-gradient widths
+    const size_t pc = colsum_partial_floats((int)D.n, (int)N);
+    if (pc > pf) pf = pc;
+  }
   const size_t pd = colsum_dropout_partial_floats((int)D.n, (int)D.h);
   if (pd > pf) pf = pd;
   W.partial = take(pf * 4);
