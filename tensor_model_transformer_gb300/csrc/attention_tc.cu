@@ -36,10 +36,8 @@ namespace mtl {
 namespace attn {
 
 constexpr int FWD_THREADS = 384;   // forward kernel: 4 control warps, two warpgroups of row threads
-constexpr int BWD_THREADS = 384;   // backward kernels: two warpgroups of row threads
+constexpr int BWD_THREADS = 384;   // backward kernels: 4 control warps, two warpgroups of row threads
 constexpr int ATOM128 = 128 * 128;   // [128 rows][64 bf16]
-constexpr int ATOM64 = 64 * 128;     // [64 rows][64 bf16]
-constexpr int BWD_STAGES = 3;      // TMA ring depth of the backward kernels
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
@@ -100,20 +98,6 @@ __device__ __forceinline__ Smem smem_aligned(uint8_t* raw) {
   uint8_t* p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) &
                                           ~static_cast<uintptr_t>(1023));
   return {p, smem_u32(p)};
-}
-
-// Work item -> (row block, head, batch) for the persistent kernels.  Items go
-// (batch, head)-major, so the items running at once on all SMs cover few pairs
-// and reuse each other's K/V from L2; within a pair the row block index is
-// rotated by the pair index, so a CTA that takes every gridDim-th item meets
-// every row block (and so every amount of causal work) in turn.
-__device__ __forceinline__ void item_coords(const Params& p, int item, bool desc, int& blk,
-                                            int& hd, int& b) {
-  const int pair = item / p.nqb;
-  const int i = (item % p.nqb + pair) % p.nqb;
-  blk = desc ? (p.nqb - 1 - i) : i;
-  hd = pair % p.heads;
-  b = pair / p.heads;
 }
 
 // ============================================================================ forward
@@ -574,46 +558,152 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
   }
 }
 
+// ============================================================================ backward
+// Two persistent kernels, each with the forward's warp roles: warp 0 takes
+// work items from a global counter (longest first within L2-sized chunks of
+// (batch, head) pairs) and drives TMA; warp 1 allocates TMEM and issues the
+// products that make the score-sized blocks; warp 2 issues the accumulating
+// products; warp 3 only gives its registers up; warps 4..11 are two
+// warpgroups of row threads, warpgroup w owning columns 64w..64w+63 of every
+// 128 x 128 block (P comes from the saved lse, not a row maximum, so the two
+// halves never need each other).  A slot of the TMA ring that both issuers
+// read is released by two commits.
+constexpr int BWD_RING = 4;
+static_assert(BWD_RING % 2 == 0, "each ring slot keeps to one operand");
+
+struct BwdItem {
+  int blk, hd, b;
+};
+
+// Work item k -> (128-row block, head, batch); within a chunk of pairs the
+// blocks go by decreasing work: the dQ kernel's query blocks from the last,
+// the dK/dV kernel's key blocks from the first.
+__device__ __forceinline__ BwdItem bwd_item(const Params& p, int k, bool last_first) {
+  const int pairs = p.batch * p.heads;
+  const int per_chunk = p.chunk * p.nqb;
+  const int c = k / per_chunk;
+  const int cp = min(p.chunk, pairs - c * p.chunk);
+  const int r = k - c * per_chunk;
+  const int pair = c * p.chunk + r % cp;
+  const int lvl = r / cp;
+  BwdItem it;
+  it.blk = last_first ? p.nqb - 1 - lvl : lvl;
+  it.hd = pair % p.heads;
+  it.b = pair / p.heads;
+  return it;
+}
+
+// Work-item hand-off through two shared-memory slots: the producer publishes,
+// the MMA issuers and one lane of each row warp acknowledge.
+struct ItemRing {
+  int* slot;
+  uint32_t full, empty;   // barrier addresses of slot 0 (slot 1 follows at +8)
+};
+
+__device__ __forceinline__ bool item_publish(const ItemRing& q, int ni, int k, unsigned* status,
+                                             volatile int* abort_flag) {
+  const int s = ni & 1;
+  if (ni >= 2 && !mbar_wait_bounded(q.empty + 8u * s, ((ni >> 1) - 1) & 1, status, abort_flag))
+    return false;
+  q.slot[s] = k;
+  mbar_arrive(q.full + 8u * s);
+  return true;
+}
+
+// Returns false on abort; k >= n_items means no work is left.
+__device__ __forceinline__ bool item_take(const ItemRing& q, int ni, bool ack, int& k,
+                                          unsigned* status, volatile int* abort_flag) {
+  const int s = ni & 1;
+  if (!mbar_wait_bounded(q.full + 8u * s, (ni >> 1) & 1, status, abort_flag)) return false;
+  k = *reinterpret_cast<volatile int*>(&q.slot[s]);
+  __syncwarp(__activemask());
+  if (ack) mbar_arrive(q.empty + 8u * s);
+  return true;
+}
+
+__device__ __forceinline__ void sched_done(unsigned* sched) {
+  __threadfence();
+  if (atomicAdd(sched + 1, 1u) == gridDim.x - 1) {
+    atomicExch(sched, 0u);
+    atomicExch(sched + 1, 0u);
+  }
+}
+
+// 32 x 32 TMEM columns of an fp32 accumulator, scaled, to 32 bf16 of a row.
+__device__ __forceinline__ void store_acc32(uint32_t taddr, float sc, bf16* dst) {
+  uint32_t v[32];
+  tmem_ld32(taddr, v);
+  tmem_ld_wait();
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 w;
+    w.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]) * sc, __uint_as_float(v[q * 8 + 1]) * sc);
+    w.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]) * sc, __uint_as_float(v[q * 8 + 3]) * sc);
+    w.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]) * sc, __uint_as_float(v[q * 8 + 5]) * sc);
+    w.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]) * sc, __uint_as_float(v[q * 8 + 7]) * sc);
+    *reinterpret_cast<uint4*>(dst + q * 8) = w;
+  }
+}
+
+// 64 bf16 (packed pairs) of a row into 32 TMEM columns.
+__device__ __forceinline__ void store_bf16_64(uint32_t taddr, const float (&v)[64]) {
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(v[32 * q + 2 * c], v[32 * q + 2 * c + 1]);
+    tmem_st16(taddr + 16 * q, pk);
+  }
+}
+
+constexpr int BWD_LAUNCH_REGS = 168, BWD_LOW_REGS = 72, BWD_ROW_REGS = 216;
+static_assert(BWD_THREADS == 384, "one giving and two taking warps per sub-partition");
+static_assert(BWD_LOW_REGS + 2 * BWD_ROW_REGS <= 3 * BWD_LAUNCH_REGS,
+              "register split exceeds a sub-partition's launch allocation");
+
 // ============================================================================ dQ
-// Persistent: one CTA per SM walks the query-block work items.  Per item: 128
-// queries; K/V blocks of 64 keys in a BWD_STAGES-deep ring that runs on across
-// items.  S and dP are double-buffered in TMEM (the MMAs of block j+2 run while
-// the row threads work on block j), and so is the dQ accumulator (an item's
-// epilogue overlaps the next item's MMAs).  Two warpgroups of row threads each
-// take 32 of the 64 key columns.  Also writes D_i = sum_c dO_ic O_ic for the
-// dK/dV kernel.
-// smem: Q, dO (NA atoms of 16 KB), K[ST], V[ST] (NA atoms of 8 KB), dS (1 atom
-// of 16 KB), D exchange.  TMEM: S[b] cols 64b, dP[b] cols 128+64b, dQ[b] cols
-// 256+128b.
+// Item: 128 queries (Q, dO resident) against key blocks j = 0..qb of 128 keys
+// (K(j), V(j) through the ring).  Per block: S = Q K^T and dP = dO V^T (warp
+// 1); the row threads' dS = P * (dP - D) with P = exp2(S log2(e) / sqrt(d) -
+// lse log2(e)) (zero after the query), written to TMEM as bf16; dQ += dS K
+// (warp 2, dS as the A operand).  The row threads also form D_i = sum_c dO_ic
+// O_ic from the dO and O tiles in shared memory and store it for the dK/dV
+// kernel.  An item's dQ is written out when
+// the next item's first dS block is ready (the last dQ product is done by
+// then, and the next one waits for that block).
+// smem: Q, dO, O, ring[BWD_RING] (NA atoms of 16 KB each), item ids.
+// TMEM: S 0..127, dP 128..255, dS 256..319, dQ 384..
+constexpr uint32_t TQ_S = 0, TQ_DP = 128, TQ_DS = 256, TQ_ACC = 384;
+
 template <int NA, int KS, bool DROP>
 __global__ void __launch_bounds__(BWD_THREADS, 1)
-    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm128,
-                          const __grid_constant__ CUtensorMap tm64,
-                          const __grid_constant__ CUtensorMap tmdo128, const Params p) {
+    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm,
+                          const __grid_constant__ CUtensorMap tmdo,
+                          const __grid_constant__ CUtensorMap tmo, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const Smem sm = smem_aligned(smem_raw);
-  constexpr uint32_t T128 = NA * ATOM128, T64 = NA * ATOM64;
-  constexpr int ST = BWD_STAGES;
-  const uint32_t sQ = sm.u32, sDO = sQ + T128, sK0 = sQ + 2 * T128, sV0 = sK0 + ST * T64,
-                 sDS = sV0 + ST * T64;
-  float* s_dpart = reinterpret_cast<float*>(sm.base + 2 * T128 + 2 * ST * T64 + ATOM128);
-  uint64_t* bars =
-      reinterpret_cast<uint64_t*>(sm.base + 2 * T128 + 2 * ST * T64 + ATOM128 + 2048);
+  constexpr uint32_t TILE = NA * ATOM128;
+  constexpr int D = KS * 16;
+  const uint32_t sQ = sm.u32, sDO = sQ + TILE, sO = sQ + 2 * TILE, sR0 = sQ + 3 * TILE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm.base + (3 + BWD_RING) * TILE);
   const uint32_t bar0 = smem_u32(bars);
   auto B = [&](int i) { return bar0 + 8u * i; };
-  // 0 q/do full, 1 q/do empty, 2..ST+1 kv_full, ST+2..2ST+1 kv_empty,
-  // then s_full[2], ds_full, dq_done, dq_free[2], d_exchange
-  const int QF = 0, QE = 1, KVF = 2, KVE = 2 + ST, SF = 2 + 2 * ST, DSF = 4 + 2 * ST,
-            DQD = 5 + 2 * ST, DQFREE = 6 + 2 * ST, DXB = 8 + 2 * ST, NBAR = 9 + 2 * ST;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBAR);
+  constexpr int QF = 0, QE = 1, RF = 2, RE = RF + BWD_RING, SF = RE + BWD_RING, SE = SF + 1,
+                DSF = SE + 1, DQD = DSF + 1, IF = DQD + 1, IE = IF + 2, NBAR = IE + 2;
+  int* s_item = reinterpret_cast<int*>(bars + NBAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_item + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const ItemRing iq{s_item, B(IF), B(IE)};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_items = p.nqb * p.heads * p.batch;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBAR; ++i) {
-      const bool rows = i == DSF || i == DQFREE || i == DQFREE + 1 || i == DXB;
-      mbar_init(B(i), rows ? 256 : 1);
+      uint32_t cnt = 1;
+      if (i == SE || i == DSF) cnt = 256;
+      if (i == IE || i == IE + 1) cnt = 2 + 8;            // two issuers + a lane per row warp
+      if (i >= RE && i < RE + BWD_RING && (i - RE) % 2 == 0) cnt = 2;   // K: both issuers
+      mbar_init(B(i), cnt);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -624,213 +714,215 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tDP = tmem + 128;
 
   if (warp == 0) {
+    // ------------------------------------------------------ scheduler, TMA producer
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(BWD_LOW_REGS));
     if (lane == 0) {
-      tma_prefetch_desc(&tm128);
-      tma_prefetch_desc(&tm64);
-      tma_prefetch_desc(&tmdo128);
-      int g = 0, n = 0;
+      tma_prefetch_desc(&tm);
+      tma_prefetch_desc(&tmdo);
+      tma_prefetch_desc(&tmo);
+      int g = 0, ni = 0, nit = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n) {
-        int qb, hd, b;
-        item_coords(p, item, true, qb, hd, b);
-        const int colq = hd * 3 * p.d;
-        const int row0 = b * p.seq + qb * 128;
-        if (!mbar_wait_bounded(B(QE), (n & 1) ^ 1u, p.status, abort_flag)) break;
-        mbar_arrive_expect_tx(B(QF), 2 * T128);
+      while (ok) {
+        const int k = (int)atomicAdd(p.sched, 1u);
+        if (!item_publish(iq, ni++, k, p.status, abort_flag) || k >= n_items) break;
+        const BwdItem it = bwd_item(p, k, true);
+        const int colq = it.hd * 3 * p.d, row0 = it.b * p.seq;
+        if (nit > 0 && !mbar_wait_bounded(B(QE), (nit - 1) & 1, p.status, abort_flag)) break;
+        ++nit;
+        mbar_arrive_expect_tx(B(QF), 3 * TILE);
         for (int a = 0; a < NA; ++a) {
-          tma_load_2d(sQ + a * ATOM128, &tm128, B(QF), colq + 64 * a, row0);
-          tma_load_2d(sDO + a * ATOM128, &tmdo128, B(QF), hd * p.d + 64 * a, row0);
+          tma_load_2d(sQ + a * ATOM128, &tm, B(QF), colq + 64 * a, row0 + it.blk * 128);
+          tma_load_2d(sDO + a * ATOM128, &tmdo, B(QF), it.hd * p.d + 64 * a, row0 + it.blk * 128);
+          tma_load_2d(sO + a * ATOM128, &tmo, B(QF), it.hd * p.d + 64 * a, row0 + it.blk * 128);
         }
-        const int nkv = 2 * qb + 2;
-        for (int j = 0; j < nkv; ++j, ++g) {
-          const int s = g % ST;
-          const int krow = b * p.seq + j * 64;
-          if (!mbar_wait_bounded(B(KVE + s), ((g / ST) & 1) ^ 1u, p.status, abort_flag)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(B(KVF + s), 2 * T64);
-          for (int a = 0; a < NA; ++a) {
-            tma_load_2d(sK0 + s * T64 + a * ATOM64, &tm64, B(KVF + s), colq + p.d + 64 * a, krow);
-            tma_load_2d(sV0 + s * T64 + a * ATOM64, &tm64, B(KVF + s), colq + 2 * p.d + 64 * a,
-                        krow);
+        for (int j = 0; j <= it.blk && ok; ++j) {
+          for (int kv = 0; kv < 2; ++kv, ++g) {
+            const int s = g % BWD_RING, use = g / BWD_RING;
+            if (use > 0 && !mbar_wait_bounded(B(RE + s), (use - 1) & 1, p.status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(B(RF + s), TILE);
+            for (int a = 0; a < NA; ++a)
+              tma_load_2d(sR0 + s * TILE + a * ATOM128, &tm, B(RF + s),
+                          colq + (1 + kv) * p.d + 64 * a, row0 + j * 128);
           }
         }
       }
+      sched_done(p.sched);
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------ MMA issuers: warp 1 S, dP; warp 2 dQ
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(BWD_LOW_REGS));
     if (lane == 0) {
-      const uint32_t id_s = idesc_bf16_f32(128, 64, false, false);
-      const uint32_t id_dq = idesc_bf16_f32(128, p.d, false, true);
-      const uint64_t dQd = desc_kbase(sQ), dDO = desc_kbase(sDO), dK0 = desc_kbase(sK0),
-                     dV0 = desc_kbase(sV0), dDS = desc_kbase(sDS);
-      const uint64_t dKmn0 = desc_mnbase(sK0, ATOM64);
-      int gb = 0, n = 0;
+      const bool first = warp == 1;
+      const uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
+      const uint32_t id_acc = idesc_bf16_f32(128, D, false, true);
+      const uint64_t dQd = desc_kbase(sQ), dDO = desc_kbase(sDO), dR0 = desc_kbase(sR0);
+      const uint64_t dRmn0 = desc_mnbase(sR0, ATOM128);
+      int g = 0, ni = 0, nit = 0, nb = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n) {
-        int qb, hd, b;
-        item_coords(p, item, true, qb, hd, b);
-        const int nkv = 2 * qb + 2;
-        if (!mbar_wait_bounded(B(QF), n & 1, p.status, abort_flag)) break;
-        tc_fence_after();
-        // S(block gg), dP(block gg) into TMEM buffer gg % 2
-        auto issue_s = [&](int j) -> bool {
-          const int gg = gb + j, s = gg % ST;
-          if (!mbar_wait_bounded(B(KVF + s), (gg / ST) & 1, p.status, abort_flag)) return false;
-          tc_fence_after();
-          const uint32_t bo = (gg & 1) * 64;
-          const uint64_t dK = desc_add(dK0, s * T64), dV = desc_add(dV0, s * T64);
+      auto wait = [&](int bar, int k) -> bool {
+        if (!mbar_wait_bounded(B(bar), k & 1, p.status, abort_flag)) ok = false;
+        return ok;
+      };
+      while (ok) {
+        int k;
+        if (!item_take(iq, ni++, true, k, p.status, abort_flag)) break;
+        if (k >= n_items) break;
+        const BwdItem it = bwd_item(p, k, true);
+        const int nkv = it.blk + 1;
+        for (int j = 0; j < nkv && ok; ++j, ++nb) {
+          const int gk = g + 2 * j, gv = gk + 1;
+          const int sk = gk % BWD_RING, sv = gv % BWD_RING;
+          if (first) {
+            if (j == 0 && !wait(QF, nit)) break;
+            if (!wait(RF + sk, gk / BWD_RING) || !wait(RF + sv, gv / BWD_RING)) break;
+            if (nb > 0 && !wait(SE, nb - 1)) break;   // the row threads hold S, dP of the last block
+            tc_fence_after();
+            const uint64_t dK = desc_add(dR0, sk * TILE), dV = desc_add(dR0, sv * TILE);
 #pragma unroll
-          for (int kk = 0; kk < KS; ++kk)
-            tc_mma_bf16(tS + bo, desc_add(dQd, kmajor_off(kk, ATOM128)),
-                        desc_add(dK, kmajor_off(kk, ATOM64)), id_s, kk > 0);
+            for (int kk = 0; kk < KS; ++kk)
+              tc_mma_bf16(tmem + TQ_S, desc_add(dQd, kmajor_off(kk, ATOM128)),
+                          desc_add(dK, kmajor_off(kk, ATOM128)), id_s, kk > 0);
 #pragma unroll
-          for (int kk = 0; kk < KS; ++kk)
-            tc_mma_bf16(tDP + bo, desc_add(dDO, kmajor_off(kk, ATOM128)),
-                        desc_add(dV, kmajor_off(kk, ATOM64)), id_s, kk > 0);
-          tc_commit(B(SF + (gg & 1)));
-          if (j == nkv - 1) tc_commit(B(QE));
-          return true;
-        };
-        ok = issue_s(0) && issue_s(1);   // nkv >= 2
-        const uint32_t tDQ = tmem + 256 + 128 * (n & 1);
-        for (int j = 0; j < nkv && ok; ++j) {
-          const int gg = gb + j, s = gg % ST;
-          // row threads wrote dS(gg) and are done reading buffer gg % 2
-          if (!mbar_wait_bounded(B(DSF), gg & 1, p.status, abort_flag)) {
-            ok = false;
-            break;
+            for (int kk = 0; kk < KS; ++kk)
+              tc_mma_bf16(tmem + TQ_DP, desc_add(dDO, kmajor_off(kk, ATOM128)),
+                          desc_add(dV, kmajor_off(kk, ATOM128)), id_s, kk > 0);
+            tc_commit(B(SF));
+            tc_commit(B(RE + sk));
+            tc_commit(B(RE + sv));
+            if (j == nkv - 1) tc_commit(B(QE));
+          } else {
+            if (!wait(DSF, nb)) break;                // dS of this block is in TMEM
+            if (!wait(RF + sk, gk / BWD_RING)) break;
+            tc_fence_after();
+            const uint64_t dKmn = desc_add(dRmn0, sk * TILE);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              tc_mma_bf16_ts(tmem + TQ_ACC, tmem + TQ_DS + 8 * kk, desc_add(dKmn, mnmajor_off(kk)),
+                             id_acc, (j > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(B(DQD));
+            tc_commit(B(RE + sk));
           }
-          if (j == 0 &&
-              !mbar_wait_bounded(B(DQFREE + (n & 1)), ((n >> 1) & 1) ^ 1u, p.status, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t dKmn = desc_add(dKmn0, s * T64);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc_mma_bf16(tDQ, desc_add(dDS, kmajor_off(kk, ATOM128)), desc_add(dKmn, mnmajor_off(kk)),
-                        id_dq, (j > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(B(KVE + s));
-          tc_commit(B(DQD));
-          if (j + 2 < nkv && !issue_s(j + 2)) ok = false;
         }
-        gb += nkv;
+        if (!ok) break;
+        g += 2 * nkv;
+        ++nit;
       }
     }
     __syncwarp();
-  } else if (warp >= 4) {
-    const int wg = (warp - 4) >> 2;                 // column half of the 64 keys
+  } else if (warp == 3) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(BWD_LOW_REGS));
+  } else {
+    // ---------------------------------------------------------------- row threads
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(BWD_ROW_REGS));
+    const int wg = (warp - 4) >> 2;            // key columns 64 wg .. 64 wg + 63
     const int q4 = warp & 3;
-    const int r = q4 * 32 + lane;
+    const int r = q4 * 32 + lane;              // query row = TMEM lane
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    int gb = 0, n = 0;
+    const float dsc = DROP ? p.drop.scale : 1.0f;
+    int ni = 0, nb = 0, nit = 0;
+    bool pend = false;
+    bf16* pdq = nullptr;                       // dQ row of the item not yet written out
+    auto epilogue = [&]() {
+      // warpgroup wg writes 32-column chunks wg, wg + 2, ...
+#pragma unroll 1
+      for (int c = 32 * wg; c < D; c += 64) store_acc32(tmem + TQ_ACC + lane_off + c, p.scale, pdq + c);
+    };
     bool ok = true;
-    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n) {
-      int qb, hd, b;
-      item_coords(p, item, true, qb, hd, b);
-      const int nkv = 2 * qb + 2;
-      const int row0 = b * p.seq + qb * 128;
-      const int colq = hd * 3 * p.d;
-      // D_r = dO_r . O_r: each warpgroup sums half of the channels
-      const size_t orow = (size_t)(row0 + r) * p.h + (size_t)hd * p.d;
-      const int half = p.d / 2;
-      float Dp = 0.f;
-      for (int c = wg * half; c < (wg + 1) * half; c += 8) {
-        const uint4 go = *reinterpret_cast<const uint4*>(p.dctx + orow + c);
-        const uint4 oo = *reinterpret_cast<const uint4*>(p.ctx + orow + c);
-        const bf16* gv = reinterpret_cast<const bf16*>(&go);
-        const bf16* ov = reinterpret_cast<const bf16*>(&oo);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) Dp = fmaf(__bfloat162float(gv[e]), __bfloat162float(ov[e]), Dp);
-      }
-      float* dpart = s_dpart + (n & 1) * 256;
-      dpart[wg * 128 + r] = Dp;
-      mbar_arrive(B(DXB));
-      if (!mbar_wait_bounded(B(DXB), n & 1, p.status, abort_flag)) {
+    while (ok) {
+      int k;
+      if (!item_take(iq, ni++, lane == 0, k, p.status, abort_flag)) {
         ok = false;
         break;
       }
-      const float Dr = dpart[r] + dpart[128 + r];
-      const size_t lrow = ((size_t)b * p.heads + hd) * p.seq + qb * 128 + r;
+      if (k >= n_items) break;
+      const BwdItem it = bwd_item(p, k, true);
+      const int qb = it.blk;
+      const int row = it.b * p.seq + qb * 128 + r;
+      // D_r = dO_r . O_r from the tiles in shared memory (the tiles stay until
+      // this item's last S / dP product, which waits for our S loads)
+      if (!mbar_wait_bounded(B(QF), nit & 1, p.status, abort_flag)) {
+        ok = false;
+        break;
+      }
+      ++nit;
+      float Dr = 0.f;
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) {
+        const uint32_t off = (c >> 3) * ATOM128 + sw128_offset(r, c & 7);
+        Vec<bf16> go, oo;
+        go.raw = ld_shared_v4(sDO + off);
+        oo.raw = ld_shared_v4(sO + off);
+        float gf[8], of[8];
+        go.unpack(gf);
+        oo.unpack(of);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) Dr = fmaf(gf[e], of[e], Dr);
+      }
+      const size_t lrow = ((size_t)it.b * p.heads + it.hd) * p.seq + qb * 128 + r;
       if (wg == 0) p.dsum[lrow] = Dr;
       const float lse2 = p.lse[lrow] * LOG2E;
-      const uint32_t tDQ = tmem + 256 + 128 * (n & 1);
-      for (int j = 0; j < nkv; ++j) {
-        const int gg = gb + j;
-        // keep bits of this row over the block's 32 keys, loaded before the wait
-        const uint32_t keep =
-            DROP ? mask_tile(p, b, hd, qb, j >> 1)[((j & 1) * 2 + wg) * 128 + r] : 0xffffffffu;
-        if (!mbar_wait_bounded(B(SF + (gg & 1)), (gg >> 1) & 1, p.status, abort_flag)) {
+      for (int j = 0; j <= qb; ++j, ++nb) {
+        uint32_t keep[2] = {0xffffffffu, 0xffffffffu};
+        if (DROP) {
+          const uint32_t* mt = mask_tile(p, it.b, it.hd, qb, j);
+          keep[0] = mt[(2 * wg) * 128 + r];
+          keep[1] = mt[(2 * wg + 1) * 128 + r];
+        }
+        if (!mbar_wait_bounded(B(SF), nb & 1, p.status, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t col = (gg & 1) * 64 + wg * 32;
-        float ds[32];
+        float ds[64];
         {
-          uint32_t sv[32], dv[32];
-          tmem_ld32(tS + lane_off + col, sv);
-          tmem_ld32(tDP + lane_off + col, dv);
+          uint32_t s0[32], s1[32], d0[32], d1[32];
+          tmem_ld32(tmem + TQ_S + lane_off + 64 * wg, s0);
+          tmem_ld32(tmem + TQ_S + lane_off + 64 * wg + 32, s1);
+          tmem_ld32(tmem + TQ_DP + lane_off + 64 * wg, d0);
+          tmem_ld32(tmem + TQ_DP + lane_off + 64 * wg + 32, d1);
           tmem_ld_wait();
-          const float dsc = DROP ? p.drop.scale : 1.0f;
+          tc_fence_before();
+          mbar_arrive(B(SE));                    // S, dP may take the next block
+          const bool diag = j == qb;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int key = j * 64 + wg * 32 + i;
-            float pr = fast_exp2(__uint_as_float(sv[i]) * p.scale_log2 - lse2);
-            if (key > qb * 128 + r) pr = 0.f;
-            const float dp = ((keep >> i) & 1u) ? __uint_as_float(dv[i]) * dsc : 0.f;
-            ds[i] = pr * (dp - Dr);
+          for (int c = 0; c < 64; ++c) {
+            const float sv = __uint_as_float(c < 32 ? s0[c] : s1[c - 32]);
+            const float dv = __uint_as_float(c < 32 ? d0[c] : d1[c - 32]);
+            float pr = fast_exp2(sv * p.scale_log2 - lse2);
+            if (diag && 64 * wg + c > r) pr = 0.f;
+            const float dp = ((keep[c >> 5] >> (c & 31)) & 1u) ? dv * dsc : 0.f;
+            ds[c] = pr * (dp - Dr);
           }
         }
-        if (gg > 0) {
-          // the dQ MMA of the previous block has read the dS buffer
-          if (!mbar_wait_bounded(B(DQD), (gg - 1) & 1, p.status, abort_flag)) {
-            ok = false;
-            break;
-          }
+        // the previous dQ product has read dS (and, at an item's first block,
+        // finished the previous item's dQ)
+        if (nb > 0 && !mbar_wait_bounded(B(DQD), (nb - 1) & 1, p.status, abort_flag)) {
+          ok = false;
+          break;
         }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int k = c * 8;
-          st_shared_v4(sDS + sw128_offset(r, wg * 4 + c), pack_bf16x2(ds[k], ds[k + 1]),
-                       pack_bf16x2(ds[k + 2], ds[k + 3]), pack_bf16x2(ds[k + 4], ds[k + 5]),
-                       pack_bf16x2(ds[k + 6], ds[k + 7]));
+        tc_fence_after();
+        if (j == 0 && pend) {
+          epilogue();
+          pend = false;
         }
-        fence_proxy_async_shared();
+        store_bf16_64(tmem + TQ_DS + lane_off + 32 * wg, ds);
+        tmem_st_wait();
         tc_fence_before();
         mbar_arrive(B(DSF));
       }
       if (!ok) break;
-      if (!mbar_wait_bounded(B(DQD), (gb + nkv - 1) & 1, p.status, abort_flag)) {
-        ok = false;
-        break;
-      }
+      pend = true;
+      pdq = p.dqkv + (size_t)row * 3 * p.h + (size_t)it.hd * 3 * D;
+    }
+    if (ok && pend && mbar_wait_bounded(B(DQD), (nb - 1) & 1, p.status, abort_flag)) {
       tc_fence_after();
-      // the two warpgroups store alternate 32-column chunks of dQ
-      bf16* dq = p.dqkv + (size_t)(row0 + r) * 3 * p.h + colq;
-      for (int c = wg * 32; c < p.d; c += 64) {
-        uint32_t v[32];
-        tmem_ld32(tDQ + lane_off + c, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 u;
-          u.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]) * p.scale, __uint_as_float(v[q * 8 + 1]) * p.scale);
-          u.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]) * p.scale, __uint_as_float(v[q * 8 + 3]) * p.scale);
-          u.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]) * p.scale, __uint_as_float(v[q * 8 + 5]) * p.scale);
-          u.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]) * p.scale, __uint_as_float(v[q * 8 + 7]) * p.scale);
-          *reinterpret_cast<uint4*>(dq + c + q * 8) = u;
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(B(DQFREE + (n & 1)));
-      gb += nkv;
+      epilogue();
     }
     __syncwarp();
   }
@@ -847,44 +939,51 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 }
 
 // ============================================================================ dK, dV
-// Persistent: one CTA per SM walks the key-block work items.  Per item: 128
-// keys; query blocks of 64 from the diagonal on, in a BWD_STAGES-deep ring that
-// runs on across items.  S^T and dP^T are double-buffered in TMEM; two
-// warpgroups of row threads each take 32 of the 64 query columns.  The next
-// item's K/V load and first S^T / dP^T MMAs overlap this item's epilogue.
-// smem: K, V (NA atoms of 16 KB), Q[ST], dO[ST] (NA atoms of 8 KB), P^T and dS^T
-// (1 atom of 16 KB each), lse / D per stage.  TMEM: S^T[b] cols 64b, dP^T[b]
-// cols 128+64b, dV 256.., dK 384..
+// Item: 128 keys (K, V resident) against query blocks i = kb..nqb-1 (Q(i) with
+// the lse and D of its queries, dO(i): through the ring).  Per block: S^T =
+// K Q^T, then dP^T = V dO^T into the same TMEM columns once the row threads
+// have read S^T (warp 1); the row threads' P^T (with the forward's keep mask
+// and scale) and dS^T = P^T * (dP^T - D), written to TMEM as bf16; dV += P^T
+// dO and dK += dS^T Q (warp 2, A operands from TMEM).  An item's dK and dV are
+// written out when the next item's first P^T block is ready.
+// smem: K, V, ring[BWD_RING] (NA atoms of 16 KB each), lse and D of the two Q
+// slots, item ids.  TMEM: S^T / dP^T 0..127, P^T 128..191, dS^T 192..255,
+// dV 256.., dK 384..
+constexpr uint32_t TK_S = 0, TK_P = 128, TK_DS = 192, TK_DV = 256, TK_DK = 384;
+
 template <int NA, int KS, bool DROP>
 __global__ void __launch_bounds__(BWD_THREADS, 1)
-    attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm128,
-                           const __grid_constant__ CUtensorMap tm64,
-                           const __grid_constant__ CUtensorMap tmdo64, const Params p) {
+    attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm,
+                           const __grid_constant__ CUtensorMap tmdo, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const Smem sm = smem_aligned(smem_raw);
-  constexpr uint32_t T128 = NA * ATOM128, T64 = NA * ATOM64;
-  constexpr int ST = BWD_STAGES;
-  const uint32_t sK = sm.u32, sV = sK + T128, sQ0 = sK + 2 * T128, sDO0 = sQ0 + ST * T64,
-                 sPT = sDO0 + ST * T64, sDST = sPT + ATOM128;
-  // lse and D of the 64-query block of each stage, copied in with its Q / dO
-  float* s_lse0 = reinterpret_cast<float*>(sm.base + 2 * T128 + 2 * ST * T64 + 2 * ATOM128);
-  float* s_d0 = s_lse0 + 64 * ST;
-  const uint32_t s_lse_u32 = smem_u32(s_lse0), s_d_u32 = smem_u32(s_d0);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm.base + 2 * T128 + 2 * ST * T64 + 2 * ATOM128 +
-                                               512 * ST);
+  constexpr uint32_t TILE = NA * ATOM128;
+  constexpr int D = KS * 16;
+  const uint32_t sK = sm.u32, sV = sK + TILE, sR0 = sK + 2 * TILE;
+  // lse, D of the queries in Q slot 2m: 128 + 128 floats at s_ld + 256 m
+  float* s_ld = reinterpret_cast<float*>(sm.base + (2 + BWD_RING) * TILE);
+  const uint32_t s_ld_u32 = smem_u32(s_ld);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_ld + 128 * BWD_RING);
   const uint32_t bar0 = smem_u32(bars);
   auto B = [&](int i) { return bar0 + 8u * i; };
-  // 0 kv_full, 1 kv_empty, 2..ST+1 qdo_full, ST+2..2ST+1 qdo_empty, then
-  // st_full[2], pt_full, mm_done, acc_free
-  const int KVF = 0, KVE = 1, QF = 2, QE = 2 + ST, STF = 2 + 2 * ST, PTF = 4 + 2 * ST,
-            MMD = 5 + 2 * ST, ACCFREE = 6 + 2 * ST, NBAR = 7 + 2 * ST;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBAR);
+  constexpr int KVF = 0, KVE = 1, RF = 2, RE = RF + BWD_RING, SF = RE + BWD_RING, SE = SF + 1,
+                DPF = SE + 1, DPE = DPF + 1, PF = DPE + 1, PE = PF + 1, DSF = PE + 1,
+                DSE = DSF + 1, IF = DSE + 1, IE = IF + 2, NBAR = IE + 2;
+  int* s_item = reinterpret_cast<int*>(bars + NBAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_item + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const ItemRing iq{s_item, B(IF), B(IE)};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_items = p.nqb * p.heads * p.batch;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NBAR; ++i) mbar_init(B(i), (i == PTF || i == ACCFREE) ? 256 : 1);
+    for (int i = 0; i < NBAR; ++i) {
+      uint32_t cnt = 1;
+      if (i == SE || i == DPE || i == PF || i == DSF) cnt = 256;
+      if (i == IE || i == IE + 1) cnt = 2 + 8;
+      if (i >= RE && i < RE + BWD_RING) cnt = 2;           // Q and dO: both issuers
+      mbar_init(B(i), cnt);
+    }
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_shared();
@@ -894,214 +993,280 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tST = tmem, tDPT = tmem + 128, tDV = tmem + 256, tDK = tmem + 384;
 
   if (warp == 0) {
+    // ------------------------------------------------------ scheduler, TMA producer
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(BWD_LOW_REGS));
     if (lane == 0) {
-      tma_prefetch_desc(&tm128);
-      tma_prefetch_desc(&tm64);
-      tma_prefetch_desc(&tmdo64);
-      int g = 0, n = 0;
+      tma_prefetch_desc(&tm);
+      tma_prefetch_desc(&tmdo);
+      int g = 0, ni = 0, nit = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n) {
-        int kb, hd, b;
-        item_coords(p, item, false, kb, hd, b);
-        const int colq = hd * 3 * p.d;
-        const int first = 2 * kb, nq = 2 * p.nqb - first;
-        if (!mbar_wait_bounded(B(KVE), (n & 1) ^ 1u, p.status, abort_flag)) break;
-        mbar_arrive_expect_tx(B(KVF), 2 * T128);
+      while (ok) {
+        const int k = (int)atomicAdd(p.sched, 1u);
+        if (!item_publish(iq, ni++, k, p.status, abort_flag) || k >= n_items) break;
+        const BwdItem it = bwd_item(p, k, false);
+        const int colq = it.hd * 3 * p.d, row0 = it.b * p.seq;
+        if (nit > 0 && !mbar_wait_bounded(B(KVE), (nit - 1) & 1, p.status, abort_flag)) break;
+        ++nit;
+        mbar_arrive_expect_tx(B(KVF), 2 * TILE);
         for (int a = 0; a < NA; ++a) {
-          tma_load_2d(sK + a * ATOM128, &tm128, B(KVF), colq + p.d + 64 * a, b * p.seq + kb * 128);
-          tma_load_2d(sV + a * ATOM128, &tm128, B(KVF), colq + 2 * p.d + 64 * a,
-                      b * p.seq + kb * 128);
+          tma_load_2d(sK + a * ATOM128, &tm, B(KVF), colq + p.d + 64 * a, row0 + it.blk * 128);
+          tma_load_2d(sV + a * ATOM128, &tm, B(KVF), colq + 2 * p.d + 64 * a,
+                      row0 + it.blk * 128);
         }
-        for (int i = 0; i < nq; ++i, ++g) {
-          const int s = g % ST;
-          const int qrow = b * p.seq + (first + i) * 64;
-          if (!mbar_wait_bounded(B(QE + s), ((g / ST) & 1) ^ 1u, p.status, abort_flag)) {
-            ok = false;
-            break;
+        for (int i = it.blk; i < p.nqb && ok; ++i) {
+          for (int qd = 0; qd < 2; ++qd, ++g) {
+            const int s = g % BWD_RING, use = g / BWD_RING;
+            if (use > 0 && !mbar_wait_bounded(B(RE + s), (use - 1) & 1, p.status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            if (qd == 0) {
+              // Q(i) with the lse and D of its queries
+              mbar_arrive_expect_tx(B(RF + s), TILE + 1024);
+              for (int a = 0; a < NA; ++a)
+                tma_load_2d(sR0 + s * TILE + a * ATOM128, &tm, B(RF + s), colq + 64 * a,
+                            row0 + i * 128);
+              const size_t lo = ((size_t)it.b * p.heads + it.hd) * p.seq + (size_t)i * 128;
+              bulk_load(s_ld_u32 + (s >> 1) * 1024, p.lse + lo, 512, B(RF + s));
+              bulk_load(s_ld_u32 + (s >> 1) * 1024 + 512, p.dsum + lo, 512, B(RF + s));
+            } else {
+              mbar_arrive_expect_tx(B(RF + s), TILE);
+              for (int a = 0; a < NA; ++a)
+                tma_load_2d(sR0 + s * TILE + a * ATOM128, &tmdo, B(RF + s), it.hd * p.d + 64 * a,
+                            row0 + i * 128);
+            }
           }
-          mbar_arrive_expect_tx(B(QF + s), 2 * T64 + 512);
-          for (int a = 0; a < NA; ++a) {
-            tma_load_2d(sQ0 + s * T64 + a * ATOM64, &tm64, B(QF + s), colq + 64 * a, qrow);
-            tma_load_2d(sDO0 + s * T64 + a * ATOM64, &tmdo64, B(QF + s), hd * p.d + 64 * a, qrow);
-          }
-          const size_t lo = ((size_t)b * p.heads + hd) * p.seq + (first + i) * 64;
-          bulk_load(s_lse_u32 + s * 256, p.lse + lo, 256, B(QF + s));
-          bulk_load(s_d_u32 + s * 256, p.dsum + lo, 256, B(QF + s));
         }
       }
+      sched_done(p.sched);
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 2) {
+    // ---------------------------------- MMA issuers: warp 1 S^T, dP^T; warp 2 dV, dK
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(BWD_LOW_REGS));
     if (lane == 0) {
-      const uint32_t id_st = idesc_bf16_f32(128, 64, false, false);
-      const uint32_t id_acc = idesc_bf16_f32(128, p.d, false, true);
-      const uint64_t dKd = desc_kbase(sK), dVd = desc_kbase(sV), dQ0 = desc_kbase(sQ0),
-                     dDO0 = desc_kbase(sDO0), dPT = desc_kbase(sPT), dDST = desc_kbase(sDST);
-      const uint64_t dQmn0 = desc_mnbase(sQ0, ATOM64), dDOmn0 = desc_mnbase(sDO0, ATOM64);
-      int gb = 0, n = 0;
+      const bool first = warp == 1;
+      const uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
+      const uint32_t id_acc = idesc_bf16_f32(128, D, false, true);
+      const uint64_t dKd = desc_kbase(sK), dVd = desc_kbase(sV), dR0 = desc_kbase(sR0);
+      const uint64_t dRmn0 = desc_mnbase(sR0, ATOM128);
+      int g = 0, ni = 0, nit = 0, nb = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n) {
-        int kb, hd, b;
-        item_coords(p, item, false, kb, hd, b);
-        const int nq = 2 * p.nqb - 2 * kb;
-        if (!mbar_wait_bounded(B(KVF), n & 1, p.status, abort_flag)) break;
-        tc_fence_after();
-        // S^T(block gg), dP^T(block gg) into TMEM buffer gg % 2
-        auto issue_st = [&](int i) -> bool {
-          const int gg = gb + i, s = gg % ST;
-          if (!mbar_wait_bounded(B(QF + s), (gg / ST) & 1, p.status, abort_flag)) return false;
-          tc_fence_after();
-          const uint32_t bo = (gg & 1) * 64;
-          const uint64_t dQ = desc_add(dQ0, s * T64), dDO = desc_add(dDO0, s * T64);
+      auto wait = [&](int bar, int k) -> bool {
+        if (!mbar_wait_bounded(B(bar), k & 1, p.status, abort_flag)) ok = false;
+        return ok;
+      };
+      while (ok) {
+        int k;
+        if (!item_take(iq, ni++, true, k, p.status, abort_flag)) break;
+        if (k >= n_items) break;
+        const BwdItem it = bwd_item(p, k, false);
+        const int nq = p.nqb - it.blk;
+        for (int i = 0; i < nq && ok; ++i, ++nb) {
+          const int gq = g + 2 * i, gd = gq + 1;
+          const int sq = gq % BWD_RING, sd = gd % BWD_RING;
+          if (first) {
+            if (i == 0 && !wait(KVF, nit)) break;
+            if (!wait(RF + sq, gq / BWD_RING)) break;
+            if (nb > 0 && !wait(DPE, nb - 1)) break;   // the rows hold dP^T of the last block
+            tc_fence_after();
+            const uint64_t dQ = desc_add(dR0, sq * TILE), dDO = desc_add(dR0, sd * TILE);
 #pragma unroll
-          for (int kk = 0; kk < KS; ++kk)
-            tc_mma_bf16(tST + bo, desc_add(dKd, kmajor_off(kk, ATOM128)),
-                        desc_add(dQ, kmajor_off(kk, ATOM64)), id_st, kk > 0);
+            for (int kk = 0; kk < KS; ++kk)
+              tc_mma_bf16(tmem + TK_S, desc_add(dKd, kmajor_off(kk, ATOM128)),
+                          desc_add(dQ, kmajor_off(kk, ATOM128)), id_s, kk > 0);
+            tc_commit(B(SF));
+            tc_commit(B(RE + sq));
+            if (!wait(RF + sd, gd / BWD_RING) || !wait(SE, nb)) break;   // rows read S^T
+            tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < KS; ++kk)
-            tc_mma_bf16(tDPT + bo, desc_add(dVd, kmajor_off(kk, ATOM128)),
-                        desc_add(dDO, kmajor_off(kk, ATOM64)), id_st, kk > 0);
-          tc_commit(B(STF + (gg & 1)));
-          if (i == nq - 1) tc_commit(B(KVE));
-          return true;
-        };
-        ok = issue_st(0) && issue_st(1);   // nq >= 2
-        for (int i = 0; i < nq && ok; ++i) {
-          const int gg = gb + i, s = gg % ST;
-          // row threads wrote P^T(gg), dS^T(gg) and are done reading buffer gg % 2
-          if (!mbar_wait_bounded(B(PTF), gg & 1, p.status, abort_flag)) {
-            ok = false;
-            break;
+            for (int kk = 0; kk < KS; ++kk)
+              tc_mma_bf16(tmem + TK_S, desc_add(dVd, kmajor_off(kk, ATOM128)),
+                          desc_add(dDO, kmajor_off(kk, ATOM128)), id_s, kk > 0);
+            tc_commit(B(DPF));
+            tc_commit(B(RE + sd));
+            if (i == nq - 1) tc_commit(B(KVE));
+          } else {
+            if (!wait(PF, nb) || !wait(RF + sd, gd / BWD_RING)) break;
+            tc_fence_after();
+            const uint64_t dDOmn = desc_add(dRmn0, sd * TILE), dQmn = desc_add(dRmn0, sq * TILE);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              tc_mma_bf16_ts(tmem + TK_DV, tmem + TK_P + 8 * kk, desc_add(dDOmn, mnmajor_off(kk)),
+                             id_acc, (i > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(B(PE));
+            tc_commit(B(RE + sd));
+            if (!wait(DSF, nb) || !wait(RF + sq, gq / BWD_RING)) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              tc_mma_bf16_ts(tmem + TK_DK, tmem + TK_DS + 8 * kk, desc_add(dQmn, mnmajor_off(kk)),
+                             id_acc, (i > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(B(DSE));
+            tc_commit(B(RE + sq));
           }
-          if (i == 0 &&
-              !mbar_wait_bounded(B(ACCFREE), (n & 1) ^ 1u, p.status, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t dDOmn = desc_add(dDOmn0, s * T64), dQmn = desc_add(dQmn0, s * T64);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc_mma_bf16(tDV, desc_add(dPT, kmajor_off(kk, ATOM128)), desc_add(dDOmn, mnmajor_off(kk)),
-                        id_acc, (i > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc_mma_bf16(tDK, desc_add(dDST, kmajor_off(kk, ATOM128)), desc_add(dQmn, mnmajor_off(kk)),
-                        id_acc, (i > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(B(QE + s));
-          tc_commit(B(MMD));
-          if (i + 2 < nq && !issue_st(i + 2)) ok = false;
         }
-        gb += nq;
+        if (!ok) break;
+        g += 2 * nq;
+        ++nit;
       }
     }
     __syncwarp();
-  } else if (warp >= 4) {
-    const int wg = (warp - 4) >> 2;   // column half of the 64 queries
+  } else if (warp == 3) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(BWD_LOW_REGS));
+  } else {
+    // ---------------------------------------------------------------- row threads
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(BWD_ROW_REGS));
+    const int wg = (warp - 4) >> 2;            // query columns 64 wg .. 64 wg + 63
     const int q4 = warp & 3;
-    const int r = q4 * 32 + lane;     // key row
+    const int r = q4 * 32 + lane;              // key row = TMEM lane
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    int gb = 0, n = 0;
+    const float dsc = DROP ? p.drop.scale : 1.0f;
+    int ni = 0, nb = 0, g = 0;
+    bool pend = false;
+    bf16* pout = nullptr;                      // K part of the dqkv row not yet written out
+    auto epilogue = [&]() {
+      // warpgroup 0 writes dK (with the 1/sqrt(d) of S), warpgroup 1 dV
+      const uint32_t src = tmem + (wg == 0 ? TK_DK : TK_DV) + lane_off;
+      bf16* dst = pout + (wg == 0 ? 0 : D);
+      const float sc = wg == 0 ? p.scale : 1.0f;
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) store_acc32(src + c, sc, dst + c);
+    };
     bool ok = true;
-    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n) {
-      int kb, hd, b;
-      item_coords(p, item, false, kb, hd, b);
-      const int first = 2 * kb, nq = 2 * p.nqb - first;
-      const int key = kb * 128 + r;
-      for (int i = 0; i < nq; ++i) {
-        const int gg = gb + i;
-        const int q0 = (first + i) * 64 + wg * 32;
-        // the forward's keep word of query q0+lane over this warp's keys, loaded
-        // before the waits so its latency hides behind them
-        const uint32_t kword =
-            DROP ? mask_tile(p, b, hd, q0 >> 7, kb)[q4 * 128 + (q0 & 127) + lane] : 0u;
-        if (!mbar_wait_bounded(B(STF + (gg & 1)), (gg >> 1) & 1, p.status, abort_flag)) {
-          ok = false;
-          break;
-        }
-        // lse / D of this block arrive with its Q / dO tiles: observe that
-        // barrier's phase too (stage gg % ST is not refilled before this
-        // iteration ends: its release follows our arrival below)
-        if (!mbar_wait_bounded(B(QF + gg % ST), (gg / ST) & 1, p.status, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const float* s_lse = s_lse0 + (gg % ST) * 64 + wg * 32;
-        const float* s_d = s_d0 + (gg % ST) * 64 + wg * 32;
-        const uint32_t col = (gg & 1) * 64 + wg * 32;
-        float pt[32], dst[32];
-        {
-          uint32_t sv[32], dv[32];
-          tmem_ld32(tST + lane_off + col, sv);
-          tmem_ld32(tDPT + lane_off + col, dv);
-          tmem_ld_wait();
-          // Keep bits of queries q0 .. q0+31 for this thread's key: lane l reads
-          // the forward's word of query q0+l over this warp's 32 keys, and a
-          // warp transpose hands lane k the word over queries for key k.
-          const uint32_t keep = DROP ? warp_transpose32(kword, lane) : 0xffffffffu;
-          const float dsc = DROP ? p.drop.scale : 1.0f;
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            float pr = fast_exp2(__uint_as_float(sv[e]) * p.scale_log2 - s_lse[e] * LOG2E);
-            if (q0 + e < key) pr = 0.f;
-            const bool kept = (keep >> e) & 1u;
-            pt[e] = kept ? pr * dsc : 0.f;
-            dst[e] = pr * ((kept ? __uint_as_float(dv[e]) * dsc : 0.f) - s_d[e]);
-          }
-        }
-        if (gg > 0) {
-          // the dV / dK MMAs of the previous block have read P^T / dS^T
-          if (!mbar_wait_bounded(B(MMD), (gg - 1) & 1, p.status, abort_flag)) {
-            ok = false;
-            break;
-          }
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int k = c * 8;
-          st_shared_v4(sPT + sw128_offset(r, wg * 4 + c), pack_bf16x2(pt[k], pt[k + 1]),
-                       pack_bf16x2(pt[k + 2], pt[k + 3]), pack_bf16x2(pt[k + 4], pt[k + 5]),
-                       pack_bf16x2(pt[k + 6], pt[k + 7]));
-          st_shared_v4(sDST + sw128_offset(r, wg * 4 + c), pack_bf16x2(dst[k], dst[k + 1]),
-                       pack_bf16x2(dst[k + 2], dst[k + 3]), pack_bf16x2(dst[k + 4], dst[k + 5]),
-                       pack_bf16x2(dst[k + 6], dst[k + 7]));
-        }
-        fence_proxy_async_shared();
-        tc_fence_before();
-        mbar_arrive(B(PTF));
-      }
-      if (!ok) break;
-      if (!mbar_wait_bounded(B(MMD), (gb + nq - 1) & 1, p.status, abort_flag)) {
+    while (ok) {
+      int k;
+      if (!item_take(iq, ni++, lane == 0, k, p.status, abort_flag)) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      // warpgroup 0 writes dK (scaled), warpgroup 1 writes dV
-      bf16* out = p.dqkv + (size_t)(b * p.seq + kb * 128 + r) * 3 * p.h + hd * 3 * p.d;
-      const uint32_t tsrc = wg == 0 ? tDK : tDV;
-      const float sc = wg == 0 ? p.scale : 1.0f;
-      bf16* dst_row = out + (wg == 0 ? p.d : 2 * p.d);
-      for (int c = 0; c < p.d; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(tsrc + lane_off + c, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 u;
-          u.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]) * sc, __uint_as_float(v[q * 8 + 1]) * sc);
-          u.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]) * sc, __uint_as_float(v[q * 8 + 3]) * sc);
-          u.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]) * sc, __uint_as_float(v[q * 8 + 5]) * sc);
-          u.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]) * sc, __uint_as_float(v[q * 8 + 7]) * sc);
-          *reinterpret_cast<uint4*>(dst_row + c + q * 8) = u;
+      if (k >= n_items) break;
+      const BwdItem it = bwd_item(p, k, false);
+      const int kb = it.blk, nq = p.nqb - kb;
+      for (int i = 0; i < nq; ++i, ++nb) {
+        const int qb = kb + i;
+        const int sq = (g + 2 * i) % BWD_RING;
+        uint32_t kword[2] = {0u, 0u};
+        if (DROP) {
+          // the forward's keep words of queries 64 wg + 32 t + lane over this
+          // warp's 32 keys; a warp transpose hands lane k the word over queries
+          const uint32_t* mt = mask_tile(p, it.b, it.hd, qb, kb);
+          kword[0] = mt[q4 * 128 + 64 * wg + lane];
+          kword[1] = mt[q4 * 128 + 64 * wg + 32 + lane];
         }
+        if (!mbar_wait_bounded(B(SF), nb & 1, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float pr[64];
+        {
+          uint32_t s0[32], s1[32];
+          tmem_ld32(tmem + TK_S + lane_off + 64 * wg, s0);
+          tmem_ld32(tmem + TK_S + lane_off + 64 * wg + 32, s1);
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(B(SE));                    // dP^T may take the S^T columns
+          // lse of this block's queries came with Q(i): observe that load
+          if (!mbar_wait_bounded(B(RF + sq), ((g + 2 * i) / BWD_RING) & 1, p.status,
+                                 abort_flag)) {
+            ok = false;
+            break;
+          }
+          const float* lse = s_ld + (sq >> 1) * 256 + 64 * wg;
+          const bool diag = i == 0;
+#pragma unroll
+          for (int c = 0; c < 64; c += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(lse + c);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int cc = c + e;
+              const float sv = __uint_as_float(cc < 32 ? s0[cc] : s1[cc - 32]);
+              float v = fast_exp2(sv * p.scale_log2 - lv[e] * LOG2E);
+              if (diag && 64 * wg + cc < r) v = 0.f;   // query before the key
+              pr[cc] = v;
+            }
+          }
+        }
+        const uint32_t keep0 = DROP ? warp_transpose32(kword[0], lane) : 0xffffffffu;
+        const uint32_t keep1 = DROP ? warp_transpose32(kword[1], lane) : 0xffffffffu;
+        // P^T (and, at an item's first block, dV) is free once the previous dV
+        // product is done; at an item's first block dK must be done as well
+        if (nb > 0 && !mbar_wait_bounded(B(PE), (nb - 1) & 1, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (i == 0 && pend) {
+          if (!mbar_wait_bounded(B(DSE), (nb - 1) & 1, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          epilogue();
+          pend = false;
+        }
+        tc_fence_after();
+        {
+          float pt[64];
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const bool kept = (((c < 32 ? keep0 : keep1) >> (c & 31)) & 1u) != 0;
+            pt[c] = kept ? pr[c] * dsc : 0.f;
+          }
+          store_bf16_64(tmem + TK_P + lane_off + 32 * wg, pt);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(B(PF));
+        // dP^T
+        if (!mbar_wait_bounded(B(DPF), nb & 1, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        {
+          uint32_t d0[32], d1[32];
+          tmem_ld32(tmem + TK_S + lane_off + 64 * wg, d0);
+          tmem_ld32(tmem + TK_S + lane_off + 64 * wg + 32, d1);
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(B(DPE));                   // S^T / dP^T columns free
+          const float* dsum = s_ld + (sq >> 1) * 256 + 128 + 64 * wg;
+#pragma unroll
+          for (int c = 0; c < 64; c += 4) {
+            const float4 d4 = *reinterpret_cast<const float4*>(dsum + c);
+            const float dvv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int cc = c + e;
+              const bool kept = (((cc < 32 ? keep0 : keep1) >> (cc & 31)) & 1u) != 0;
+              const float dp = kept ? __uint_as_float(cc < 32 ? d0[cc] : d1[cc - 32]) * dsc : 0.f;
+              pr[cc] = pr[cc] * (dp - dvv[e]);   // dS^T
+            }
+          }
+        }
+        if (nb > 0 && !mbar_wait_bounded(B(DSE), (nb - 1) & 1, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        store_bf16_64(tmem + TK_DS + lane_off + 32 * wg, pr);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(B(DSF));
       }
-      tc_fence_before();
-      mbar_arrive(B(ACCFREE));
-      gb += nq;
+      if (!ok) break;
+      g += 2 * nq;
+      pend = true;
+      pout = p.dqkv + (size_t)(it.b * p.seq + kb * 128 + r) * 3 * p.h + (size_t)it.hd * 3 * D + D;
+    }
+    if (ok && pend && mbar_wait_bounded(B(PE), (nb - 1) & 1, p.status, abort_flag) &&
+        mbar_wait_bounded(B(DSE), (nb - 1) & 1, p.status, abort_flag)) {
+      tc_fence_after();
+      epilogue();
     }
     __syncwarp();
   }
@@ -1151,13 +1316,11 @@ size_t fwd_smem(int na) {
 // The backward kernels hold all 512 TMEM columns: their shared memory requests
 // keep them at one CTA per SM so a second CTA never waits in tcgen05.alloc.
 size_t dq_smem(int na) {
-  const size_t need =
-      (size_t)2 * na * ATOM128 + 2 * BWD_STAGES * na * ATOM64 + ATOM128 + 2048 + 256 + 1024;
-  return need < 120 * 1024 ? 120 * 1024 : need;
+  const size_t need = (size_t)(3 + BWD_RING) * na * ATOM128 + 256 + 1024;
+  return need < 120 * 1024 ? 120 * 1024 : need;   // one CTA per SM (512 TMEM columns)
 }
 size_t dkv_smem(int na) {
-  const size_t need = (size_t)2 * na * ATOM128 + 2 * BWD_STAGES * na * ATOM64 + 2 * ATOM128 +
-                      512 * BWD_STAGES + 256 + 1024;
+  const size_t need = (size_t)(2 + BWD_RING) * na * ATOM128 + 2048 + 256 + 1024;
   return need < 120 * 1024 ? 120 * 1024 : need;
 }
 
@@ -1182,6 +1345,15 @@ Params make_params(int batch, int seq, int heads, int d, unsigned* status, const
   p.sched = nullptr;
   p.chunk = 1;
   return p;
+}
+
+// (batch, head) pairs per scheduling chunk: pairs whose two streamed operands
+// (NA 128-byte boxes per row each) fit in about 48 MB of L2 together.
+int l2_chunk(int batch, int seq, int heads, int d) {
+  const size_t per_pair = 2ull * seq * (d > 64 ? 2 : 1) * 128;
+  const size_t c = ((size_t)48 << 20) / per_pair;
+  const size_t pairs = (size_t)batch * heads;
+  return c < 1 ? 1 : (int)(c > pairs ? pairs : c);
 }
 
 template <typename K>
@@ -1221,12 +1393,7 @@ cudaError_t attn_fwd_tc(const void* qkv, void* ctx, float* lse, int batch, int s
   p.ctx = static_cast<bf16*>(ctx);
   p.lse = lse;
   p.sched = status + kSchedFwd;
-  // pairs whose K/V (NA 128-byte boxes per row) fit in about 48 MB of L2
-  {
-    const size_t kv = 2ull * seq * (d > 64 ? 2 : 1) * 128;
-    const size_t c = ((size_t)48 << 20) / kv;
-    p.chunk = c < 1 ? 1 : (c > (size_t)batch * heads ? batch * heads : (int)c);
-  }
+  p.chunk = l2_chunk(batch, seq, heads, d);
   const int items = ((p.nqb + 1) / 2) * heads * batch;
   const int grid = items < c.num_sms ? items : c.num_sms;
   const double flops = 2.0 * 2.0 * batch * heads * d * ((double)seq * (seq + 1) / 2.0);
@@ -1262,10 +1429,10 @@ cudaError_t attn_bwd_tc(const void* qkv, const void* ctx, const float* lse, cons
   if (batch == 0) return cudaSuccess;
   if (!attn_tc_supported(seq, d)) return cudaErrorInvalidValue;
   const uint64_t n = (uint64_t)batch * seq;
-  CUtensorMap tm128, tm64, tmdo128, tmdo64;
-  if (!make_map(&tm128, qkv, 3ull * heads * d, n, 128) || !make_map(&tm64, qkv, 3ull * heads * d, n, 64) ||
-      !make_map(&tmdo128, dctx, (uint64_t)heads * d, n, 128) ||
-      !make_map(&tmdo64, dctx, (uint64_t)heads * d, n, 64))
+  CUtensorMap tm, tmdo, tmo;
+  if (!make_map(&tm, qkv, 3ull * heads * d, n, 128) ||
+      !make_map(&tmdo, dctx, (uint64_t)heads * d, n, 128) ||
+      !make_map(&tmo, ctx, (uint64_t)heads * d, n, 128))
     return cudaErrorInvalidValue;
   if (drop.on && !mask) return cudaErrorInvalidValue;
   Params p = make_params(batch, seq, heads, d, status, drop);
@@ -1275,24 +1442,27 @@ cudaError_t attn_bwd_tc(const void* qkv, const void* ctx, const float* lse, cons
   p.dctx = static_cast<const bf16*>(dctx);
   p.dqkv = static_cast<bf16*>(dqkv);
   p.dsum = dsum;
+  p.chunk = l2_chunk(batch, seq, heads, d);
   const int items = p.nqb * heads * batch;
   const int grid = items < c.num_sms ? items : c.num_sms;
   const double tri = (double)batch * heads * d * ((double)seq * (seq + 1) / 2.0);
   cudaError_t e;
 #define BWD_CASE(NA_, KS_, DR_)                                                                \
   {                                                                                            \
-    if ((e = set_smem(attn_bwd_dq_tc_kernel<NA_, KS_, DR_>, dq_smem(NA_))) != cudaSuccess)       \
-      return e;                                                                                \
-    if ((e = set_smem(attn_bwd_dkv_tc_kernel<NA_, KS_, DR_>, dkv_smem(NA_))) != cudaSuccess)     \
-      return e;                                                                                \
+    auto kq = attn_bwd_dq_tc_kernel<NA_, KS_, DR_>;                                            \
+    auto kk = attn_bwd_dkv_tc_kernel<NA_, KS_, DR_>;                                           \
+    if ((e = set_smem(kq, dq_smem(NA_))) != cudaSuccess) return e;                             \
+    if ((e = set_smem(kk, dkv_smem(NA_))) != cudaSuccess) return e;                            \
+    if ((e = check_regs(kq, BWD_LAUNCH_REGS)) != cudaSuccess) return e;                        \
+    if ((e = check_regs(kk, BWD_LAUNCH_REGS)) != cudaSuccess) return e;                        \
     c.before(KK_ATTN_BWD, 2.0 * 3.0 * tri);                                                    \
-    attn_bwd_dq_tc_kernel<NA_, KS_, DR_><<<grid, BWD_THREADS, dq_smem(NA_), c.stream>>>(        \
-        tm128, tm64, tmdo128, p);                                                              \
+    p.sched = status + kSchedDq;                                                               \
+    kq<<<grid, BWD_THREADS, dq_smem(NA_), c.stream>>>(tm, tmdo, tmo, p);                       \
     c.after();                                                                                 \
     if ((e = cudaGetLastError()) != cudaSuccess) return e;                                     \
     c.before(KK_ATTN_BWD, 2.0 * 4.0 * tri);                                                    \
-    attn_bwd_dkv_tc_kernel<NA_, KS_, DR_><<<grid, BWD_THREADS, dkv_smem(NA_), c.stream>>>(      \
-        tm128, tm64, tmdo64, p);                                                               \
+    p.sched = status + kSchedDkv;                                                              \
+    kk<<<grid, BWD_THREADS, dkv_smem(NA_), c.stream>>>(tm, tmdo, p);                           \
     c.after();                                                                                 \
   }
   if (drop.on) {
