@@ -688,8 +688,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm.base + (3 + BWD_RING) * TILE);
   const uint32_t bar0 = smem_u32(bars);
   auto B = [&](int i) { return bar0 + 8u * i; };
+  // QE: the item's last S / dP product is done with Q and dO; DE: the row
+  // threads are done reading dO and O for D (for a one-block item the product
+  // can finish before the rows get to D, so both gate the next load)
   constexpr int QF = 0, QE = 1, RF = 2, RE = RF + BWD_RING, SF = RE + BWD_RING, SE = SF + 1,
-                DSF = SE + 1, DQD = DSF + 1, IF = DQD + 1, IE = IF + 2, NBAR = IE + 2;
+                DSF = SE + 1, DQD = DSF + 1, DE = DQD + 1, IF = DE + 1, IE = IF + 2, NBAR = IE + 2;
   int* s_item = reinterpret_cast<int*>(bars + NBAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_item + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -700,7 +703,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBAR; ++i) {
       uint32_t cnt = 1;
-      if (i == SE || i == DSF) cnt = 256;
+      if (i == SE || i == DSF || i == DE) cnt = 256;
       if (i == IE || i == IE + 1) cnt = 2 + 8;            // two issuers + a lane per row warp
       if (i >= RE && i < RE + BWD_RING && (i - RE) % 2 == 0) cnt = 2;   // K: both issuers
       mbar_init(B(i), cnt);
@@ -729,7 +732,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         if (!item_publish(iq, ni++, k, p.status, abort_flag) || k >= n_items) break;
         const BwdItem it = bwd_item(p, k, true);
         const int colq = it.hd * 3 * p.d, row0 = it.b * p.seq;
-        if (nit > 0 && !mbar_wait_bounded(B(QE), (nit - 1) & 1, p.status, abort_flag)) break;
+        if (nit > 0 && (!mbar_wait_bounded(B(QE), (nit - 1) & 1, p.status, abort_flag) ||
+                        !mbar_wait_bounded(B(DE), (nit - 1) & 1, p.status, abort_flag)))
+          break;
         ++nit;
         mbar_arrive_expect_tx(B(QF), 3 * TILE);
         for (int a = 0; a < NA; ++a) {
@@ -844,8 +849,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const BwdItem it = bwd_item(p, k, true);
       const int qb = it.blk;
       const int row = it.b * p.seq + qb * 128 + r;
-      // D_r = dO_r . O_r from the tiles in shared memory (the tiles stay until
-      // this item's last S / dP product, which waits for our S loads)
+      // D_r = dO_r . O_r from the tiles in shared memory (they are not reloaded
+      // before every row thread has arrived on DE below)
       if (!mbar_wait_bounded(B(QF), nit & 1, p.status, abort_flag)) {
         ok = false;
         break;
@@ -864,6 +869,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 #pragma unroll
         for (int e = 0; e < 8; ++e) Dr = fmaf(gf[e], of[e], Dr);
       }
+      mbar_arrive(B(DE));
       const size_t lrow = ((size_t)it.b * p.heads + it.hd) * p.seq + qb * 128 + r;
       if (wg == 0) p.dsum[lrow] = Dr;
       const float lse2 = p.lse[lrow] * LOG2E;
@@ -889,29 +895,45 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           tmem_ld_wait();
           tc_fence_before();
           mbar_arrive(B(SE));                    // S, dP may take the next block
+          // the previous dQ product has read dS (and, at an item's first block,
+          // finished the previous item's dQ)
+          if (nb > 0 && !mbar_wait_bounded(B(DQD), (nb - 1) & 1, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (j == 0 && pend) {
+            epilogue();
+            pend = false;
+          }
           const bool diag = j == qb;
+          const float nl = -lse2;
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const float sv = __uint_as_float(c < 32 ? s0[c] : s1[c - 32]);
-            const float dv = __uint_as_float(c < 32 ? d0[c] : d1[c - 32]);
-            float pr = fast_exp2(sv * p.scale_log2 - lse2);
-            if (diag && 64 * wg + c > r) pr = 0.f;
-            const float dp = ((keep[c >> 5] >> (c & 31)) & 1u) ? dv * dsc : 0.f;
-            ds[c] = pr * (dp - Dr);
+          for (int h = 0; h < 2; ++h) {
+            // 32 columns: exponentials, dS, and their bf16 store while the next
+            // half is computed
+#pragma unroll
+            for (int c = 32 * h; c < 32 * h + 32; c += 2) {
+              float x0, x1;
+              ffma2(x0, x1, __uint_as_float(h ? s1[c - 32] : s0[c]),
+                    __uint_as_float(h ? s1[c - 31] : s0[c + 1]), p.scale_log2, p.scale_log2, nl, nl);
+              float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+              if (diag && 64 * wg + c > r) p0 = 0.f;
+              if (diag && 64 * wg + c + 1 > r) p1 = 0.f;
+              const float dv0 = __uint_as_float(h ? d1[c - 32] : d0[c]);
+              const float dv1 = __uint_as_float(h ? d1[c - 31] : d0[c + 1]);
+              const float dp0 = ((keep[h] >> (c & 31)) & 1u) ? dv0 * dsc : 0.f;
+              const float dp1 = ((keep[h] >> ((c + 1) & 31)) & 1u) ? dv1 * dsc : 0.f;
+              ds[c] = p0 * (dp0 - Dr);
+              ds[c + 1] = p1 * (dp1 - Dr);
+            }
+            uint32_t pk[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(ds[32 * h + 2 * c], ds[32 * h + 2 * c + 1]);
+            tmem_st16(tmem + TQ_DS + lane_off + 32 * wg + 16 * h, pk);
           }
         }
-        // the previous dQ product has read dS (and, at an item's first block,
-        // finished the previous item's dQ)
-        if (nb > 0 && !mbar_wait_bounded(B(DQD), (nb - 1) & 1, p.status, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (j == 0 && pend) {
-          epilogue();
-          pend = false;
-        }
-        store_bf16_64(tmem + TQ_DS + lane_off + 32 * wg, ds);
+        if (!ok) break;
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(B(DSF));
@@ -1175,85 +1197,104 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             ok = false;
             break;
           }
+          const uint32_t keep0 = DROP ? warp_transpose32(kword[0], lane) : 0xffffffffu;
+          const uint32_t keep1 = DROP ? warp_transpose32(kword[1], lane) : 0xffffffffu;
+          // P^T (and, at an item's first block, dV) is free once the previous dV
+          // product is done; at an item's first block dK must be done as well
+          if (nb > 0 && !mbar_wait_bounded(B(PE), (nb - 1) & 1, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (i == 0 && pend) {
+            if (!mbar_wait_bounded(B(DSE), (nb - 1) & 1, p.status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            epilogue();
+            pend = false;
+          }
+          tc_fence_after();
           const float* lse = s_ld + (sq >> 1) * 256 + 64 * wg;
           const bool diag = i == 0;
 #pragma unroll
-          for (int c = 0; c < 64; c += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(lse + c);
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          for (int h = 0; h < 2; ++h) {
+            // 32 query columns: P, and the dropped and scaled P^T stored while the
+            // next half is computed
+            const uint32_t keep = h ? keep1 : keep0;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int cc = c + e;
-              const float sv = __uint_as_float(cc < 32 ? s0[cc] : s1[cc - 32]);
-              float v = fast_exp2(sv * p.scale_log2 - lv[e] * LOG2E);
-              if (diag && 64 * wg + cc < r) v = 0.f;   // query before the key
-              pr[cc] = v;
+            for (int c = 32 * h; c < 32 * h + 32; c += 4) {
+              const float4 l4 = *reinterpret_cast<const float4*>(lse + c);
+              float x0, x1, x2, x3;
+              ffma2(x0, x1, __uint_as_float(h ? s1[c - 32] : s0[c]),
+                    __uint_as_float(h ? s1[c - 31] : s0[c + 1]), p.scale_log2, p.scale_log2,
+                    -l4.x * LOG2E, -l4.y * LOG2E);
+              ffma2(x2, x3, __uint_as_float(h ? s1[c - 30] : s0[c + 2]),
+                    __uint_as_float(h ? s1[c - 29] : s0[c + 3]), p.scale_log2, p.scale_log2,
+                    -l4.z * LOG2E, -l4.w * LOG2E);
+              pr[c] = fast_exp2(x0);
+              pr[c + 1] = fast_exp2(x1);
+              pr[c + 2] = fast_exp2(x2);
+              pr[c + 3] = fast_exp2(x3);
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                if (diag && 64 * wg + c + e < r) pr[c + e] = 0.f;   // query before the key
             }
+            uint32_t pk[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const int c0 = 32 * h + 2 * c;
+              const float t0 = ((keep >> (2 * c)) & 1u) ? pr[c0] * dsc : 0.f;
+              const float t1 = ((keep >> (2 * c + 1)) & 1u) ? pr[c0 + 1] * dsc : 0.f;
+              pk[c] = pack_bf16x2(t0, t1);
+            }
+            tmem_st16(tmem + TK_P + lane_off + 32 * wg + 16 * h, pk);
           }
-        }
-        const uint32_t keep0 = DROP ? warp_transpose32(kword[0], lane) : 0xffffffffu;
-        const uint32_t keep1 = DROP ? warp_transpose32(kword[1], lane) : 0xffffffffu;
-        // P^T (and, at an item's first block, dV) is free once the previous dV
-        // product is done; at an item's first block dK must be done as well
-        if (nb > 0 && !mbar_wait_bounded(B(PE), (nb - 1) & 1, p.status, abort_flag)) {
-          ok = false;
-          break;
-        }
-        if (i == 0 && pend) {
-          if (!mbar_wait_bounded(B(DSE), (nb - 1) & 1, p.status, abort_flag)) {
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(B(PF));
+          // dP^T
+          if (!mbar_wait_bounded(B(DPF), nb & 1, p.status, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          epilogue();
-          pend = false;
-        }
-        tc_fence_after();
-        {
-          float pt[64];
-#pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const bool kept = (((c < 32 ? keep0 : keep1) >> (c & 31)) & 1u) != 0;
-            pt[c] = kept ? pr[c] * dsc : 0.f;
-          }
-          store_bf16_64(tmem + TK_P + lane_off + 32 * wg, pt);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(B(PF));
-        // dP^T
-        if (!mbar_wait_bounded(B(DPF), nb & 1, p.status, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        {
           uint32_t d0[32], d1[32];
           tmem_ld32(tmem + TK_S + lane_off + 64 * wg, d0);
           tmem_ld32(tmem + TK_S + lane_off + 64 * wg + 32, d1);
           tmem_ld_wait();
           tc_fence_before();
           mbar_arrive(B(DPE));                   // S^T / dP^T columns free
+          // dS^T is free once the previous dK product is done
+          if (nb > 0 && !mbar_wait_bounded(B(DSE), (nb - 1) & 1, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
           const float* dsum = s_ld + (sq >> 1) * 256 + 128 + 64 * wg;
 #pragma unroll
-          for (int c = 0; c < 64; c += 4) {
-            const float4 d4 = *reinterpret_cast<const float4*>(dsum + c);
-            const float dvv[4] = {d4.x, d4.y, d4.z, d4.w};
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t keep = h ? keep1 : keep0;
+            uint32_t pk[16];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int cc = c + e;
-              const bool kept = (((cc < 32 ? keep0 : keep1) >> (cc & 31)) & 1u) != 0;
-              const float dp = kept ? __uint_as_float(cc < 32 ? d0[cc] : d1[cc - 32]) * dsc : 0.f;
-              pr[cc] = pr[cc] * (dp - dvv[e]);   // dS^T
+            for (int c = 0; c < 32; c += 4) {
+              const float4 d4 = *reinterpret_cast<const float4*>(dsum + 32 * h + c);
+              const float dvv[4] = {d4.x, d4.y, d4.z, d4.w};
+              float v[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int cc = c + e;
+                const bool kept = ((keep >> cc) & 1u) != 0;
+                const float dp = kept ? __uint_as_float(h ? d1[cc] : d0[cc]) * dsc : 0.f;
+                v[e] = pr[32 * h + cc] * (dp - dvv[e]);   // dS^T
+              }
+              pk[c / 2] = pack_bf16x2(v[0], v[1]);
+              pk[c / 2 + 1] = pack_bf16x2(v[2], v[3]);
             }
+            tmem_st16(tmem + TK_DS + lane_off + 32 * wg + 16 * h, pk);
           }
         }
-        if (nb > 0 && !mbar_wait_bounded(B(DSE), (nb - 1) & 1, p.status, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        store_bf16_64(tmem + TK_DS + lane_off + 32 * wg, pr);
+        if (!ok) break;
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(B(DSF));

@@ -1,9 +1,10 @@
 """Causal attention alone through the C ABI against the oracle, on random inputs.
 
 The shapes give the persistent kernels several work items per CTA (so barrier
-phases carry across items), sequences whose last 256-query pair has a single
-128-row tile (seq % 256 == 128), every supported head size, and logits large
-enough that the running row maximum jumps and the accumulator is rescaled.
+phases carry across items, and one-block items run between long ones),
+sequences whose last 256-query pair has a single 128-row tile (seq % 256 ==
+128), every supported head size, and logits large enough that the running row
+maximum jumps and the accumulator is rescaled.
 """
 import numpy as np
 import pytest
@@ -19,6 +20,8 @@ CASES = [
     (1, 1024, 40, 128, 1.0),
     (2, 384, 24, 96, 4.0),
     (1, 256, 160, 64, 2.0),
+    # long items next to one-block items, ~10 items per CTA (the large layer's shape)
+    (1, 2048, 96, 128, 0.02),
 ]
 
 
