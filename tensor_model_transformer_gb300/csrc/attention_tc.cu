@@ -19,15 +19,19 @@
 // eighth of a bf16 P); the two backward kernels read the bits instead of
 // drawing again, which trades 2 of 3 Philox passes for a few MB of traffic.
 //
-// All three kernels are persistent (one CTA per SM) with warp roles:
-//   warp 0      TMA producer
-//   warp 1      TMEM allocator, MMA issuer
-//   the rest    row threads: thread (warp%4)*32+lane owns TMEM lane = one row of
+// All three kernels are persistent (one CTA per SM, work items from a global
+// counter) with warp roles:
+//   warp 0      scheduler and TMA producer
+//   warp 1      TMEM allocator and the MMA issuer of the score-sized products
+//   warp 2      the MMA issuer of the products that read P / dS
+//   warp 3      gives its registers to the row threads
+//   warps 4-11  row threads: thread (warp%4)*32+lane owns TMEM lane = one row of
 //               a 128-row block.
 // Operand tiles are [atoms][rows][64] 128-byte-swizzled boxes straight from TMA;
 // the same box serves as a K-major operand (rows = M/N) or an MN-major one
 // (rows = K), e.g. dO is the K-major B of dO V^T and the MN-major B of P^T dO.
-// P and dS go from registers to shared memory in the same swizzled layout.
+// P, dS, P^T and dS^T go from registers to TMEM as bf16 and are read there as
+// the A operand of the next product.
 // Every wait is bounded; a timeout is recorded in the status word.
 #include "common.cuh"
 #include "kernels.h"
@@ -127,8 +131,8 @@ __device__ __forceinline__ Smem smem_aligned(uint8_t* raw) {
 constexpr int FWD_RING = 4;
 static_assert(FWD_RING % 2 == 0, "K and V must keep to their own ring slots");
 constexpr uint32_t TM_S = 0, TM_P = 128, TM_O = 256;
-// Register split: warps 0..3 (producer, MMA issuer, two idle) give registers
-// to the row warps 4..11, which hold a 128-key score row each.  The split is
+// Register split: warps 0..3 (producer, two MMA issuers, one idle) give
+// registers to the row warps 4..11, which hold a 128-key score row each.  The split is
 // balanced on every SM sub-partition (warp w runs on sub-partition w % 4: one
 // giving warp and two taking warps on each), since setmaxnreg.inc waits, with
 // no bound, for registers released on its own sub-partition.
