@@ -556,11 +556,13 @@ def main():
 
     # ---- end to end: host buffers in, results out, every step.  Each step's x
     # and dy are copied from pinned host memory and its y and dx are copied
-    # back; a copy stream overlaps step i's copies with step i-1's compute
-    # through double-buffered device inputs and outputs.
+    # back; one stream per copy direction overlaps step i's copies with the
+    # neighbouring steps' compute through double-buffered device inputs and
+    # outputs (the two directions run on their own copy engines at once).
     barrier()
     torch.cuda.synchronize()
     copy = torch.cuda.Stream()
+    copy_out = torch.cuda.Stream()
     xs = [xd, torch.empty_like(xd)]
     dys = [dyd, torch.empty_like(dyd)]
     ys = [y, torch.empty_like(y)]
@@ -594,12 +596,12 @@ def main():
         mtl.layer_fwd(desc, w, xs[b], ys[b], saved, ws, stream)
         mtl.layer_bwd(desc, w, xs[b], saved, dys[b], dxs[b], grads, ws, stream)
         computed[b].record(stream)
-        with torch.cuda.stream(copy):
-            copy.wait_event(computed[b])
+        with torch.cuda.stream(copy_out):
+            copy_out.wait_event(computed[b])
             y_h[b].copy_(ys[b], non_blocking=True)
             dx_h[b].copy_(dxs[b], non_blocking=True)
-            drained[b].record(copy)
-    e1.record(copy)
+            drained[b].record(copy_out)
+    e1.record(copy_out)
     e1.synchronize()
     torch.cuda.synchronize()
     ms_e2e = e0.elapsed_time(e1)
