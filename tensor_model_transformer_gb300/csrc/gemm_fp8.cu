@@ -20,6 +20,11 @@ namespace f8 {
 
 constexpr int QTHREADS = 256;
 
+// A thread takes the same column vectors of QROWS rows at once (rows
+// blockIdx.x + k * gridDim.x), so that up to QROWS * ceil(cols / (QTHREADS * E))
+// 16-byte loads are in flight.
+constexpr int QROWS = 4;
+
 // Block-wide max of non-negative floats, then one atomicMax on the bits (for
 // non-negative IEEE floats the unsigned order is the float order).
 template <typename T>
@@ -29,13 +34,21 @@ __global__ void __launch_bounds__(QTHREADS) amax_kernel(const T* __restrict__ x,
   constexpr int E = Vec<T>::N;
   __shared__ float red[QTHREADS / 32];
   float m = 0.f;
-  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-    const T* row = x + r * ld;
+  const int64_t G = gridDim.x;
+  for (int64_t r0 = blockIdx.x; r0 < rows; r0 += QROWS * G) {
     for (int64_t c = (int64_t)threadIdx.x * E; c < cols; c += (int64_t)QTHREADS * E) {
-      Vec<T> v;
-      v.load(row + c);
+      Vec<T> v[QROWS];
 #pragma unroll
-      for (int e = 0; e < E; ++e) m = fmaxf(m, fabsf(v.get(e)));
+      for (int k = 0; k < QROWS; ++k)
+        if (r0 + k * G < rows) v[k].load(x + (r0 + k * G) * ld + c);
+#pragma unroll
+      for (int k = 0; k < QROWS; ++k) {
+        if (r0 + k * G >= rows) continue;
+        float f[E];
+        v[k].unpack(f);
+#pragma unroll
+        for (int e = 0; e < E; ++e) m = fmaxf(m, fabsf(f[e]));
+      }
     }
   }
   m = warp_max(m);
@@ -47,7 +60,23 @@ __global__ void __launch_bounds__(QTHREADS) amax_kernel(const T* __restrict__ x,
   }
 }
 
-// q = fp8(x * scale), 16 elements (16 bytes out) per thread and step.
+// 16 fp32 values -> 16 fp8 bytes (saturating, round to nearest even).
+template <int FMT>
+__device__ __forceinline__ uint4 to_fp8x16(const float (&f)[16]) {
+  const __nv_fp8_interpretation_t kind = FMT == 0 ? __NV_E4M3 : __NV_E5M2;
+  uint32_t w[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t lo =
+        __nv_cvt_float2_to_fp8x2(make_float2(f[4 * k], f[4 * k + 1]), __NV_SATFINITE, kind);
+    const uint32_t hi =
+        __nv_cvt_float2_to_fp8x2(make_float2(f[4 * k + 2], f[4 * k + 3]), __NV_SATFINITE, kind);
+    w[k] = (lo & 0xFFFFu) | (hi << 16);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// q = fp8(x * scale), 16 elements (16 bytes out) per thread, row and step.
 template <typename T, int FMT>
 __global__ void __launch_bounds__(QTHREADS) cast_kernel(const T* __restrict__ x, int64_t rows,
                                                         int64_t cols, int64_t ld,
@@ -59,95 +88,115 @@ __global__ void __launch_bounds__(QTHREADS) cast_kernel(const T* __restrict__ x,
   const float maxv = FMT == 0 ? 448.0f : 57344.0f;
   const float scale = amax > 0.f ? __fdiv_rn(maxv, amax) : 1.0f;
   if (blockIdx.x == 0 && threadIdx.x == 0) *scale_out = scale;
-  const __nv_fp8_interpretation_t kind = FMT == 0 ? __NV_E4M3 : __NV_E5M2;
-  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-    const T* row = x + r * ld;
-    uint8_t* qrow = q + r * ldq;
+  const int64_t G = gridDim.x;
+  for (int64_t r0 = blockIdx.x; r0 < rows; r0 += QROWS * G) {
     for (int64_t c = (int64_t)threadIdx.x * 16; c < cols; c += (int64_t)QTHREADS * 16) {
-      float f[16];
+      Vec<T> v[QROWS][16 / E];
 #pragma unroll
-      for (int j = 0; j < 16 / E; ++j) {
-        Vec<T> v;
-        v.load(row + c + j * E);
+      for (int k = 0; k < QROWS; ++k)
+        if (r0 + k * G < rows) {
 #pragma unroll
-        for (int e = 0; e < E; ++e) f[j * E + e] = __fmul_rn(v.get(e), scale);
+          for (int j = 0; j < 16 / E; ++j) v[k][j].load(x + (r0 + k * G) * ld + c + j * E);
+        }
+#pragma unroll
+      for (int k = 0; k < QROWS; ++k) {
+        if (r0 + k * G >= rows) continue;
+        float f[16];
+#pragma unroll
+        for (int j = 0; j < 16 / E; ++j) {
+          float g[E];
+          v[k][j].unpack(g);
+#pragma unroll
+          for (int e = 0; e < E; ++e) f[j * E + e] = __fmul_rn(g[e], scale);
+        }
+        *reinterpret_cast<uint4*>(q + (r0 + k * G) * ldq + c) = to_fp8x16<FMT>(f);
       }
-      uint4 out;
-      uint32_t* w = reinterpret_cast<uint32_t*>(&out);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(f[4 * k], f[4 * k + 1]),
-                                                     __NV_SATFINITE, kind);
-        const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(f[4 * k + 2], f[4 * k + 3]),
-                                                     __NV_SATFINITE, kind);
-        w[k] = (lo & 0xFFFFu) | (hi << 16);
-      }
-      *reinterpret_cast<uint4*>(qrow + c) = out;
     }
   }
 }
 
 // qT = fp8(x * scale) transposed: qT[c][r] for x [rows][cols], and optionally
-// the row-major q from the same read.  A CTA converts a 64 x 64 tile row-wise
-// into a byte tile in shared memory (16 elements per thread; those 16 bytes
-// also go to q), then writes it column-wise: 16 consecutive rows of one column
-// make one 16-byte store of an output row.  rows % 16 == 0.
-constexpr int CT = 64;
+// the row-major q from the same read.  A CTA takes CTX tiles of 64 x 64 side by
+// side along the columns (all their loads issued first) and converts them
+// row-wise into byte tiles in shared memory, 16 elements per thread and tile
+// (those 16 bytes also go to q).  Then each thread reads a 16 x 4 block (16
+// rows, one 32-bit word each) of one tile, transposes it with byte permutes and
+// stores four 16-byte pieces of output rows.  A tile row is 16 words; rows
+// 16j..16j+15 start 8j words further on, so that the four 16-row groups a warp
+// reads fall on disjoint banks.  rows % 16 == 0.
+constexpr int CT = 64, CTX = 4;
+constexpr int TILE_WORDS = CT * 16 + 32;
+__device__ __forceinline__ int tile_word(int row, int wcol) { return row * 16 + (row >> 4) * 8 + wcol; }
+
 template <typename T, int FMT>
 __global__ void __launch_bounds__(QTHREADS) cast_transpose_kernel(
     const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
     const unsigned* __restrict__ amax_bits, float* __restrict__ scale_out,
     uint8_t* __restrict__ qT, int64_t ldqT, uint8_t* __restrict__ q, int64_t ldq) {
+  static_assert(QTHREADS == CTX * 64, "one thread per 16 x 4 block of each tile");
   constexpr int E = Vec<T>::N;
-  __shared__ __align__(16) uint8_t tile[CT][CT + 16];   // rows of 80 bytes: 16-byte aligned
+  __shared__ __align__(16) uint32_t tile[CTX * TILE_WORDS];
   const float amax = __uint_as_float(*amax_bits);
   const float maxv = FMT == 0 ? 448.0f : 57344.0f;
   const float scale = amax > 0.f ? __fdiv_rn(maxv, amax) : 1.0f;
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *scale_out = scale;
-  const __nv_fp8_interpretation_t kind = FMT == 0 ? __NV_E4M3 : __NV_E5M2;
-  const int64_t r0 = (int64_t)blockIdx.y * CT, c0 = (int64_t)blockIdx.x * CT;
-  // load: thread -> (row tr, 16 columns from tc)
+  const int64_t r0 = (int64_t)blockIdx.y * CT, cb = (int64_t)blockIdx.x * CT * CTX;
+  // convert: thread -> (row tr, 16 columns from tc) of every tile
   {
     const int tr = threadIdx.x >> 2, tc = (threadIdx.x & 3) * 16;
-    const int64_t r = r0 + tr, c = c0 + tc;
-    float f[16];
+    const int64_t r = r0 + tr;
+    Vec<T> v[CTX][16 / E];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) f[i] = 0.f;
-    if (r < rows && c < cols) {   // cols % 16 == 0: the 16 columns are all in range
+    for (int t = 0; t < CTX; ++t) {
+      const int64_t c = cb + t * CT + tc;
+      if (r < rows && c < cols) {   // cols % 16 == 0: the 16 columns are all in range
 #pragma unroll
-      for (int j = 0; j < 16 / E; ++j) {
-        Vec<T> v;
-        v.load(x + r * ld + c + j * E);
-#pragma unroll
-        for (int e = 0; e < E; ++e) f[j * E + e] = __fmul_rn(v.get(e), scale);
+        for (int j = 0; j < 16 / E; ++j) v[t][j].load(x + r * ld + c + j * E);
       }
     }
-    uint32_t w[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(f[4 * k], f[4 * k + 1]),
-                                                   __NV_SATFINITE, kind);
-      const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(f[4 * k + 2], f[4 * k + 3]),
-                                                   __NV_SATFINITE, kind);
-      w[k] = (lo & 0xFFFFu) | (hi << 16);
+    for (int t = 0; t < CTX; ++t) {
+      const int64_t c = cb + t * CT + tc;
+      const bool live = r < rows && c < cols;
+      float f[16];
+#pragma unroll
+      for (int j = 0; j < 16 / E; ++j) {
+        float g[E];
+        if (live) v[t][j].unpack(g);
+#pragma unroll
+        for (int e = 0; e < E; ++e) f[j * E + e] = live ? __fmul_rn(g[e], scale) : 0.f;
+      }
+      const uint4 w = to_fp8x16<FMT>(f);
+      *reinterpret_cast<uint4*>(&tile[t * TILE_WORDS + tile_word(tr, tc / 4)]) = w;
+      if (q && live) *reinterpret_cast<uint4*>(q + r * ldq + c) = w;
     }
-    *reinterpret_cast<uint4*>(&tile[tr][tc]) = make_uint4(w[0], w[1], w[2], w[3]);
-    if (q && r < rows && c < cols)
-      *reinterpret_cast<uint4*>(q + r * ldq + c) = make_uint4(w[0], w[1], w[2], w[3]);
   }
   __syncthreads();
-  // store: thread -> (output row oc = tile column, 16 rows from orr)
+  // transpose: thread -> tile t, 16-row group rg, word column wc (columns 4wc..4wc+3)
   {
-    const int oc = threadIdx.x >> 2, orr = (threadIdx.x & 3) * 16;
-    const int64_t c = c0 + oc, r = r0 + orr;
-    if (c < cols && r < rows) {
-      uint32_t w[4];
+    const int t = threadIdx.x >> 6, l = threadIdx.x & 63;
+    const int rg = l & 3, wc = l >> 2;
+    const int64_t r = r0 + rg * 16, c = cb + t * CT + wc * 4;
+    if (r < rows && c < cols) {   // cols % 16 == 0: the 4 columns are all in range
+      const uint32_t* src = &tile[t * TILE_WORDS];
+      uint32_t w[16];
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        w[k] = (uint32_t)tile[orr + 4 * k][oc] | ((uint32_t)tile[orr + 4 * k + 1][oc] << 8) |
-               ((uint32_t)tile[orr + 4 * k + 2][oc] << 16) |
-               ((uint32_t)tile[orr + 4 * k + 3][oc] << 24);
-      *reinterpret_cast<uint4*>(qT + c * ldqT + r) = make_uint4(w[0], w[1], w[2], w[3]);
+      for (int i = 0; i < 16; ++i) w[i] = src[tile_word(rg * 16 + i, wc)];
+      uint32_t o[4][4];   // o[j][k]: column 4wc+j, rows 4k..4k+3 of the group
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t t0 = __byte_perm(w[4 * k], w[4 * k + 1], 0x5140);
+        const uint32_t t1 = __byte_perm(w[4 * k], w[4 * k + 1], 0x7362);
+        const uint32_t t2 = __byte_perm(w[4 * k + 2], w[4 * k + 3], 0x5140);
+        const uint32_t t3 = __byte_perm(w[4 * k + 2], w[4 * k + 3], 0x7362);
+        o[0][k] = __byte_perm(t0, t2, 0x5410);
+        o[1][k] = __byte_perm(t0, t2, 0x7632);
+        o[2][k] = __byte_perm(t1, t3, 0x5410);
+        o[3][k] = __byte_perm(t1, t3, 0x7632);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4*>(qT + (c + j) * ldqT + r) = make_uint4(o[j][0], o[j][1], o[j][2], o[j][3]);
     }
   }
 }
@@ -271,7 +320,7 @@ cudaError_t fp8_quantize2(int src_dtype, const void* x, int64_t rows, int64_t co
     c.after();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  dim3 grid((unsigned)((cols + CT - 1) / CT), (unsigned)((rows + CT - 1) / CT));
+  dim3 grid((unsigned)((cols + CT * CTX - 1) / (CT * CTX)), (unsigned)((rows + CT - 1) / CT));
   c.before(KK_QUANT, (double)rows * cols * ((src_dtype == kBF16 ? 2 : 4) + (q ? 2 : 1)));
   uint8_t* qb = static_cast<uint8_t*>(qT);
   uint8_t* qr = static_cast<uint8_t*>(q);
