@@ -62,6 +62,10 @@ template <> struct Vec<bf16> {
     bf16* h = reinterpret_cast<bf16*>(&raw);
     h[i] = __float2bfloat16_rn(v);
   }
+  // v rounded to bf16 (round to nearest even), as fp32
+  static __device__ __forceinline__ float round(float v) {
+    return __bfloat162float(__float2bfloat16_rn(v));
+  }
   // all N elements to / from fp32 (a bf16 is the high half of an fp32 word)
   __device__ __forceinline__ void unpack(float (&f)[N]) const {
     const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -88,6 +92,7 @@ template <> struct Vec<float> {
   __device__ __forceinline__ void store(float* p) const { *reinterpret_cast<float4*>(p) = raw; }
   __device__ __forceinline__ float get(int i) const { return (&raw.x)[i]; }
   __device__ __forceinline__ void set(int i, float v) { (&raw.x)[i] = v; }
+  static __device__ __forceinline__ float round(float v) { return v; }
   __device__ __forceinline__ void unpack(float (&f)[N]) const {
     f[0] = raw.x;
     f[1] = raw.y;

@@ -296,57 +296,14 @@ cudaError_t gemm_fp8(const GemmArgs& a, const LaunchCtx& c) {
   return cudaGetLastError();
 }
 
-cudaError_t fp8_quantize2(int src_dtype, const void* x, int64_t rows, int64_t cols, int64_t ld,
-                          int fmt, unsigned* amax_bits, float* scale, void* q, int64_t ldq,
-                          void* qT, int64_t ldqT, const LaunchCtx& c) {
+cudaError_t fp8_amax(int src_dtype, const void* x, int64_t rows, int64_t cols, int64_t ld,
+                     unsigned* amax_bits, const LaunchCtx& c) {
   using namespace f8;
   if (rows == 0 || cols == 0) return cudaSuccess;
-  if (cols % 16 || rows % 16 || (fmt != 0 && fmt != 1)) return cudaErrorInvalidValue;
-  cudaError_t e;
-  if (!qT) {
-    // amax, then the row-major cast (which also writes the scale)
-    return fp8_quantize(src_dtype, x, rows, cols, ld, fmt, amax_bits, scale, q, ldq, c);
-  }
-  {
-    const int64_t want = 4LL * c.num_sms;
-    const int grid = (int)(rows < want ? rows : want);
-    c.before(KK_QUANT, (double)rows * cols * (src_dtype == kBF16 ? 2 : 4));
-    if (src_dtype == kBF16)
-      amax_kernel<bf16><<<grid, QTHREADS, 0, c.stream>>>(static_cast<const bf16*>(x), rows, cols,
-                                                         ld, amax_bits);
-    else
-      amax_kernel<float><<<grid, QTHREADS, 0, c.stream>>>(static_cast<const float*>(x), rows,
-                                                          cols, ld, amax_bits);
-    c.after();
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  dim3 grid((unsigned)((cols + CT * CTX - 1) / (CT * CTX)), (unsigned)((rows + CT - 1) / CT));
-  c.before(KK_QUANT, (double)rows * cols * ((src_dtype == kBF16 ? 2 : 4) + (q ? 2 : 1)));
-  uint8_t* qb = static_cast<uint8_t*>(qT);
-  uint8_t* qr = static_cast<uint8_t*>(q);
-#define CASTT(T, F)                                                                      \
-  cast_transpose_kernel<T, F><<<grid, QTHREADS, 0, c.stream>>>(                          \
-      static_cast<const T*>(x), rows, cols, ld, amax_bits, scale, qb, ldqT, qr, ldq)
-  if (src_dtype == kBF16) {
-    if (fmt == 0) CASTT(bf16, 0); else CASTT(bf16, 1);
-  } else {
-    if (fmt == 0) CASTT(float, 0); else CASTT(float, 1);
-  }
-#undef CASTT
-  c.after();
-  return cudaGetLastError();
-}
-
-cudaError_t fp8_quantize(int src_dtype, const void* x, int64_t rows, int64_t cols, int64_t ld,
-                         int fmt, unsigned* amax_bits, float* scale, void* q, int64_t ldq,
-                         const LaunchCtx& c) {
-  using namespace f8;
-  if (rows == 0 || cols == 0) return cudaSuccess;
-  if (cols % 16 || (fmt != 0 && fmt != 1)) return cudaErrorInvalidValue;
+  if (cols % 16) return cudaErrorInvalidValue;
   const int64_t want = 4LL * c.num_sms;
   const int grid = (int)(rows < want ? rows : want);
-  const double bytes = (double)rows * cols * (src_dtype == kBF16 ? 2 : 4);
-  c.before(KK_QUANT, bytes);
+  c.before(KK_QUANT, (double)rows * cols * (src_dtype == kBF16 ? 2 : 4));
   if (src_dtype == kBF16)
     amax_kernel<bf16><<<grid, QTHREADS, 0, c.stream>>>(static_cast<const bf16*>(x), rows, cols, ld,
                                                        amax_bits);
@@ -354,21 +311,62 @@ cudaError_t fp8_quantize(int src_dtype, const void* x, int64_t rows, int64_t col
     amax_kernel<float><<<grid, QTHREADS, 0, c.stream>>>(static_cast<const float*>(x), rows, cols,
                                                         ld, amax_bits);
   c.after();
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  c.before(KK_QUANT, bytes + (double)rows * cols);
-  uint8_t* qb = static_cast<uint8_t*>(q);
+  return cudaGetLastError();
+}
+
+cudaError_t fp8_cast(int src_dtype, const void* x, int64_t rows, int64_t cols, int64_t ld,
+                     int fmt, const unsigned* amax_bits, float* scale, void* q, int64_t ldq,
+                     void* qT, int64_t ldqT, const LaunchCtx& c) {
+  using namespace f8;
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  if (cols % 16 || (qT && rows % 16) || (fmt != 0 && fmt != 1)) return cudaErrorInvalidValue;
+  const int esz = src_dtype == kBF16 ? 2 : 4;
+  uint8_t* qr = static_cast<uint8_t*>(q);
+  if (qT) {
+    dim3 grid((unsigned)((cols + CT * CTX - 1) / (CT * CTX)), (unsigned)((rows + CT - 1) / CT));
+    c.before(KK_QUANT, (double)rows * cols * (esz + (q ? 2 : 1)));
+    uint8_t* qb = static_cast<uint8_t*>(qT);
+#define CASTT(T, F)                                                                      \
+  cast_transpose_kernel<T, F><<<grid, QTHREADS, 0, c.stream>>>(                          \
+      static_cast<const T*>(x), rows, cols, ld, amax_bits, scale, qb, ldqT, qr, ldq)
+    if (src_dtype == kBF16) {
+      if (fmt == 0) CASTT(bf16, 0); else CASTT(bf16, 1);
+    } else {
+      if (fmt == 0) CASTT(float, 0); else CASTT(float, 1);
+    }
+#undef CASTT
+  } else {
+    const int64_t want = 4LL * c.num_sms;
+    const int grid = (int)(rows < want ? rows : want);
+    c.before(KK_QUANT, (double)rows * cols * (esz + 1));
 #define CAST(T, F)                                                                              \
   cast_kernel<T, F><<<grid, QTHREADS, 0, c.stream>>>(static_cast<const T*>(x), rows, cols, ld, \
-                                                     amax_bits, scale, qb, ldq)
-  if (src_dtype == kBF16) {
-    if (fmt == 0) CAST(bf16, 0); else CAST(bf16, 1);
-  } else {
-    if (fmt == 0) CAST(float, 0); else CAST(float, 1);
-  }
+                                                     amax_bits, scale, qr, ldq)
+    if (src_dtype == kBF16) {
+      if (fmt == 0) CAST(bf16, 0); else CAST(bf16, 1);
+    } else {
+      if (fmt == 0) CAST(float, 0); else CAST(float, 1);
+    }
 #undef CAST
+  }
   c.after();
   return cudaGetLastError();
+}
+
+cudaError_t fp8_quantize2(int src_dtype, const void* x, int64_t rows, int64_t cols, int64_t ld,
+                          int fmt, unsigned* amax_bits, float* scale, void* q, int64_t ldq,
+                          void* qT, int64_t ldqT, const LaunchCtx& c) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  if (cols % 16 || (qT && rows % 16) || (fmt != 0 && fmt != 1)) return cudaErrorInvalidValue;
+  const cudaError_t e = fp8_amax(src_dtype, x, rows, cols, ld, amax_bits, c);
+  if (e != cudaSuccess) return e;
+  return fp8_cast(src_dtype, x, rows, cols, ld, fmt, amax_bits, scale, q, ldq, qT, ldqT, c);
+}
+
+cudaError_t fp8_quantize(int src_dtype, const void* x, int64_t rows, int64_t cols, int64_t ld,
+                         int fmt, unsigned* amax_bits, float* scale, void* q, int64_t ldq,
+                         const LaunchCtx& c) {
+  return fp8_quantize2(src_dtype, x, rows, cols, ld, fmt, amax_bits, scale, q, ldq, nullptr, 0, c);
 }
 
 }  // namespace mtl

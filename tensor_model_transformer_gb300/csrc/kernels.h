@@ -152,6 +152,15 @@ cudaError_t fp8_quantize(int src_dtype, const void* x, int64_t rows, int64_t col
 cudaError_t fp8_quantize2(int src_dtype, const void* x, int64_t rows, int64_t cols, int64_t ld,
                           int fmt, unsigned* amax_bits, float* scale, void* q, int64_t ldq,
                           void* qT, int64_t ldqT, const LaunchCtx& c);
+// The two passes of fp8_quantize2 apart: fp8_amax folds max |x| into
+// *amax_bits (atomicMax on the float bits); fp8_cast takes a finished
+// *amax_bits (from fp8_amax, or from a kernel that read x anyway, such as
+// colsum) and writes the scale, q and / or qT.
+cudaError_t fp8_amax(int src_dtype, const void* x, int64_t rows, int64_t cols, int64_t ld,
+                     unsigned* amax_bits, const LaunchCtx& c);
+cudaError_t fp8_cast(int src_dtype, const void* x, int64_t rows, int64_t cols, int64_t ld,
+                     int fmt, const unsigned* amax_bits, float* scale, void* q, int64_t ldq,
+                     void* qT, int64_t ldqT, const LaunchCtx& c);
 
 // LayerNorm backward without a residual: dx = LN_bwd(du + du2) where du (fp32,
 // may be null) and du2 (layer dtype) are the two parts of the upstream
@@ -169,9 +178,12 @@ cudaError_t gelu_apply(int dtype, const void* z, void* a, int64_t count, const L
 // Host check of the shapes gemm_tc accepts.
 bool gemm_tc_supported(const GemmArgs& a);
 
-// LayerNorm forward of x [n][h] -> u [n][h], mean and rstd [n] (fp32).
+// LayerNorm forward of x [n][h] -> u [n][h], mean and rstd [n] (fp32).  With
+// amax_bits, max |u| (of the stored values) is folded into *amax_bits
+// (atomicMax on the float bits; the caller zeroes it).
 cudaError_t ln_fwd(int dtype, const void* x, const void* gamma, const void* beta, void* u,
-                   float* mean, float* rstd, int n, int h, float eps, const LaunchCtx& c);
+                   float* mean, float* rstd, int n, int h, float eps, const LaunchCtx& c,
+                   unsigned* amax_bits = nullptr);
 // LayerNorm backward plus residual gradient: dx = resid + LN_bwd(du); du fp32.
 // dgamma / dbeta (fp32 [h]) are reduced in a fixed order through `partial`
 // (ln_bwd_partial_floats(n, h) floats).
@@ -182,9 +194,11 @@ cudaError_t ln_bwd(int dtype, const float* du, const void* x, const float* mean,
 size_t ln_bwd_partial_floats(int n, int h);
 
 // out[j] = sum_i Y[i*ld + j] (fp32, fixed order) for j < N, i < n, through
-// `partial` (colsum_partial_floats(n, N) floats).
+// `partial` (colsum_partial_floats(n, N) floats).  With amax_bits, max |Y| over
+// the same elements is also folded into *amax_bits (atomicMax on the float
+// bits; the caller zeroes it).
 cudaError_t colsum(int dtype, const void* Y, int64_t ld, int n, int N, float* out,
-                   float* partial, const LaunchCtx& c);
+                   float* partial, const LaunchCtx& c, unsigned* amax_bits = nullptr);
 size_t colsum_partial_floats(int n, int N);
 // Column sums of the dropped-out Y: Ym = Y * keep / (1 - p) (element e = row * N
 // + col of site drop.site) is written with row pitch ld, out = column sums of Ym

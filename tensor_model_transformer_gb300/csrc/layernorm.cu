@@ -44,13 +44,15 @@ __device__ __forceinline__ void block_sum_n(float (&v)[NV], float* red) {
 // R rows per iteration: the loads of all R rows are issued before the block
 // reductions, so each thread keeps R*V 16-byte loads in flight.  Each element
 // is converted to fp32 once; gamma and beta are held as fp32 for all rows.
-template <typename T, int V, int R>
+// AMAX: also fold max |u| into *amax_bits.
+template <typename T, int V, int R, bool AMAX>
 __global__ void __launch_bounds__(kLnThreadsMax, V == 1 ? 4 : 1)   // short rows: 32 registers
     ln_fwd_kernel(const T* __restrict__ x, const T* __restrict__ gamma, const T* __restrict__ beta,
                   T* __restrict__ u, float* __restrict__ mean_out, float* __restrict__ rstd_out,
-                  int n, int h, float eps, int rows_per_block) {
+                  int n, int h, float eps, int rows_per_block, unsigned* __restrict__ amax_bits) {
   constexpr int E = Vec<T>::N;
   __shared__ float red[R * 32];
+  float umax = 0.f;   // max |u| of this thread's outputs before rounding (AMAX)
   griddep_wait();   // no-op unless launched as a programmatic dependent
   if (threadIdx.x == 0) griddep_launch_dependents();
   const int nvec = h / E;
@@ -136,7 +138,10 @@ __global__ void __launch_bounds__(kLnThreadsMax, V == 1 ? 4 : 1)   // short rows
         }
         float of[E];
 #pragma unroll
-        for (int e = 0; e < E; ++e) of[e] = (xf[rr][i][e] - mean[rr]) * rs * gv[e] + bv[e];
+        for (int e = 0; e < E; ++e) {
+          of[e] = (xf[rr][i][e] - mean[rr]) * rs * gv[e] + bv[e];
+          if (AMAX) umax = fmaxf(umax, fabsf(of[e]));
+        }
         Vec<T> o;
         o.pack(of);
         o.store(u + (size_t)(r0 + rr) * h + vi * E);
@@ -150,6 +155,18 @@ __global__ void __launch_bounds__(kLnThreadsMax, V == 1 ? 4 : 1)   // short rows
           rstd_out[r0 + rr] = 1.0f / sqrtf(ss[rr] * inv_h + eps);
         }
       }
+    }
+  }
+  if (AMAX) {
+    // max |u| of the stored values: rounding to T is monotone and symmetric, so
+    // the rounded maximum is the maximum of the rounded values
+    umax = warp_max(umax);
+    __syncthreads();   // the last block_sum_n's readers of `red` are done
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = umax;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int w = 1; w < (int)(blockDim.x + 31) / 32; ++w) umax = fmaxf(umax, red[w]);
+      atomicMax(amax_bits, __float_as_uint(Vec<T>::round(umax)));
     }
   }
 }
@@ -378,29 +395,47 @@ __global__ void __launch_bounds__(kFinWarps * 32)
   }
 }
 
-template <typename T>
-__global__ void colsum_partial_kernel(const T* __restrict__ Y, int64_t ld, int n, int N,
-                                      int rows_per_block, float* __restrict__ part) {
+// With AMAX, max |Y| of the block's elements also goes to *amax_bits (one
+// atomicMax a block).
+template <typename T, bool AMAX>
+__global__ void __launch_bounds__(kColsumThreads)
+    colsum_partial_kernel(const T* __restrict__ Y, int64_t ld, int n, int N, int rows_per_block,
+                          float* __restrict__ part, unsigned* __restrict__ amax_bits) {
   constexpr int E = Vec<T>::N;
   const int c0 = (blockIdx.x * blockDim.x + threadIdx.x) * E;
-  if (c0 >= N) return;
-  float acc[E];
+  float m = 0.f;
+  if (c0 < N) {
+    float acc[E];
 #pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  const int r0 = blockIdx.y * rows_per_block;
-  const int r1 = min(n, r0 + rows_per_block);
-  // unrolled so that 8 row loads are in flight; the adds keep row order
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    const int r0 = blockIdx.y * rows_per_block;
+    const int r1 = min(n, r0 + rows_per_block);
+    // unrolled so that 8 row loads are in flight; the adds keep row order
 #pragma unroll 8
-  for (int r = r0; r < r1; ++r) {
-    Vec<T> v;
-    v.load(Y + (size_t)r * ld + c0);
-    float f[E];
-    v.unpack(f);
+    for (int r = r0; r < r1; ++r) {
+      Vec<T> v;
+      v.load(Y + (size_t)r * ld + c0);
+      float f[E];
+      v.unpack(f);
 #pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] += f[e];
+      for (int e = 0; e < E; ++e) {
+        acc[e] += f[e];
+        if (AMAX) m = fmaxf(m, fabsf(f[e]));
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) part[(size_t)blockIdx.y * N + c0 + e] = acc[e];
   }
-#pragma unroll
-  for (int e = 0; e < E; ++e) part[(size_t)blockIdx.y * N + c0 + e] = acc[e];
+  if (AMAX) {
+    __shared__ float red[kColsumThreads / 32];
+    m = warp_max(m);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int w = 1; w < kColsumThreads / 32; ++w) m = fmaxf(m, red[w]);
+      atomicMax(amax_bits, __float_as_uint(m));
+    }
+  }
 }
 
 // colsum_partial_kernel on Y * keep / (1 - p), also writing that product to Ym.
@@ -446,7 +481,8 @@ void row_plan(int h, int* vpt, int* threads, int max_threads = kLnThreadsMax) {
 
 template <typename T>
 cudaError_t ln_fwd_t(const void* x, const void* g, const void* b, void* u, float* mean,
-                     float* rstd, int n, int h, float eps, const LaunchCtx& c) {
+                     float* rstd, int n, int h, float eps, const LaunchCtx& c,
+                     unsigned* amax_bits) {
   if (n == 0) return cudaSuccess;
   int vpt, threads;
   row_plan<T>(h, &vpt, &threads);
@@ -455,8 +491,13 @@ cudaError_t ln_fwd_t(const void* x, const void* g, const void* b, void* u, float
   c.before(KK_LN_FWD, (double)n * h * (2.0 * sizeof(T)) + 8.0 * n);
 #define LN_FWD_CASE(VV, RR)                                                                  \
   case VV:                                                                                   \
-    e = launch_ex(c, ln_fwd_kernel<T, VV, RR>, dim3(grid), dim3(threads), 0, 1, (const T*)x,     \
-                  (const T*)g, (const T*)b, (T*)u, mean, rstd, n, h, eps, rows);             \
+    e = amax_bits                                                                            \
+            ? launch_ex(c, ln_fwd_kernel<T, VV, RR, true>, dim3(grid), dim3(threads), 0, 1,  \
+                        (const T*)x, (const T*)g, (const T*)b, (T*)u, mean, rstd, n, h, eps, \
+                        rows, amax_bits)                                                     \
+            : launch_ex(c, ln_fwd_kernel<T, VV, RR, false>, dim3(grid), dim3(threads), 0, 1, \
+                        (const T*)x, (const T*)g, (const T*)b, (T*)u, mean, rstd, n, h, eps, \
+                        rows, amax_bits);                                                    \
     break;
   cudaError_t e = cudaSuccess;
   switch (vpt) {
@@ -523,14 +564,19 @@ cudaError_t ln_bwd_t(const float* du, const void* du2, const void* x, const floa
 
 template <typename T>
 cudaError_t colsum_t(const void* Y, int64_t ld, int n, int N, float* out, float* partial,
-                     const LaunchCtx& c) {
+                     const LaunchCtx& c, unsigned* amax_bits) {
   constexpr int E = Vec<T>::N;
   const int nblk = colsum_row_blocks(n, N, E);
   const int rows = (n + nblk - 1) / nblk;
   const int threads = kColsumThreads;
   dim3 grid((N / E + threads - 1) / threads, nblk);
   c.before(KK_COLSUM, (double)n * N * sizeof(T));
-  colsum_partial_kernel<T><<<grid, threads, 0, c.stream>>>((const T*)Y, ld, n, N, rows, partial);
+  if (amax_bits)
+    colsum_partial_kernel<T, true><<<grid, threads, 0, c.stream>>>((const T*)Y, ld, n, N, rows,
+                                                                   partial, amax_bits);
+  else
+    colsum_partial_kernel<T, false><<<grid, threads, 0, c.stream>>>((const T*)Y, ld, n, N, rows,
+                                                                    partial, nullptr);
   c.after();
   c.before(KK_FINALIZE, 4.0 * nblk * N);
   finalize_cols_kernel<<<(N + 31) / 32, kFinWarps * 32, 0, c.stream>>>(partial, nblk, N, out);
@@ -573,9 +619,9 @@ size_t colsum_partial_floats(int n, int N) {
 }
 
 cudaError_t ln_fwd(int dtype, const void* x, const void* g, const void* b, void* u, float* mean,
-                   float* rstd, int n, int h, float eps, const LaunchCtx& c) {
-  return dtype == kBF16 ? ln_fwd_t<bf16>(x, g, b, u, mean, rstd, n, h, eps, c)
-                        : ln_fwd_t<float>(x, g, b, u, mean, rstd, n, h, eps, c);
+                   float* rstd, int n, int h, float eps, const LaunchCtx& c, unsigned* amax_bits) {
+  return dtype == kBF16 ? ln_fwd_t<bf16>(x, g, b, u, mean, rstd, n, h, eps, c, amax_bits)
+                        : ln_fwd_t<float>(x, g, b, u, mean, rstd, n, h, eps, c, amax_bits);
 }
 
 cudaError_t ln_bwd(int dtype, const float* du, const void* x, const float* mean,
@@ -670,9 +716,9 @@ cudaError_t gelu_apply(int dtype, const void* z, void* a, int64_t count, const L
 }
 
 cudaError_t colsum(int dtype, const void* Y, int64_t ld, int n, int N, float* out,
-                   float* partial, const LaunchCtx& c) {
-  return dtype == kBF16 ? colsum_t<bf16>(Y, ld, n, N, out, partial, c)
-                        : colsum_t<float>(Y, ld, n, N, out, partial, c);
+                   float* partial, const LaunchCtx& c, unsigned* amax_bits) {
+  return dtype == kBF16 ? colsum_t<bf16>(Y, ld, n, N, out, partial, c, amax_bits)
+                        : colsum_t<float>(Y, ld, n, N, out, partial, c, amax_bits);
 }
 
 cudaError_t colsum_dropout(int dtype, const void* Y, void* Ym, int64_t ld, int n, int N,

@@ -371,12 +371,19 @@ mtl_status forward_core(const Dims& D, float ln_eps, const mtl_weights* w, const
   const Fp8Ws FW = fp8_ws_layout(D);
   int slot = 0;
   if (D.fp8) MTL_TRY(cudaMemsetAsync(at<char>(fp8ws, FW.stats), 0, 128, c.stream), "fp8 stats");
-  auto fwd_gemm = [&](GemmArgs g, const char* where) -> mtl_status {
+  // the amax slot of the next FP8 GEMM's A operand, for a kernel that writes
+  // that operand (LayerNorm) to fill in (null without FP8 layers)
+  auto next_amax_a = [&]() -> unsigned* {
+    return D.fp8 ? at<unsigned>(fp8ws, FW.stats) + 2 * slot : nullptr;
+  };
+  // a_amax_done: the producer of A already folded its amax in
+  auto fwd_gemm = [&](GemmArgs g, const char* where, bool a_amax_done = false) -> mtl_status {
     if (!D.fp8) {
       MTL_TRY(run_gemm(D, g, c), where);
       return MTL_OK;
     }
     unsigned* amax = at<unsigned>(fp8ws, FW.stats) + 2 * slot;
+    if (!a_amax_done) MTL_TRY(fp8_amax(kBF16, g.A.ptr, g.M, g.K, g.A.ld, amax, c), where);
     float* sc = at<float>(fp8ws, FW.stats + 64) + 2 * slot;
     uint8_t* qa = at<uint8_t>(fp8ws, FW.qa);
     uint8_t* qb = at<uint8_t>(fp8ws, FW.qb);
@@ -386,14 +393,15 @@ mtl_status forward_core(const Dims& D, float ln_eps, const mtl_weights* w, const
       const Fp8Saved FS = fp8_saved_layout(D);
       char* fsv = at<char>(saved, L.fp8);
       sc = at<float>(fsv, FS.scales) + 2 * slot;
-      MTL_TRY(fp8_quantize2(kBF16, g.A.ptr, g.M, g.K, g.A.ld, 0, amax, sc, qa, g.K,
-                            at<uint8_t>(fsv, FS.act[slot]), g.M, c),
+      MTL_TRY(fp8_cast(kBF16, g.A.ptr, g.M, g.K, g.A.ld, 0, amax, sc, qa, g.K,
+                       at<uint8_t>(fsv, FS.act[slot]), g.M, c),
               where);
       MTL_TRY(fp8_quantize2(kBF16, g.B.ptr, g.N, g.K, g.B.ld, 0, amax + 1, sc + 1, qb, g.K,
                             at<uint8_t>(fsv, FS.wt[slot]), g.N, c),
               where);
     } else {
-      MTL_TRY(fp8_quantize(kBF16, g.A.ptr, g.M, g.K, g.A.ld, 0, amax, sc, qa, g.K, c), where);
+      MTL_TRY(fp8_cast(kBF16, g.A.ptr, g.M, g.K, g.A.ld, 0, amax, sc, qa, g.K, nullptr, 0, c),
+              where);
       MTL_TRY(fp8_quantize(kBF16, g.B.ptr, g.N, g.K, g.B.ld, 0, amax + 1, sc + 1, qb, g.K, c),
               where);
     }
@@ -473,16 +481,16 @@ mtl_status forward_core(const Dims& D, float ln_eps, const mtl_weights* w, const
     return MTL_OK;
   }
 
-  // F1 LN1
+  // F1 LN1 (with FP8 layers also the amax of u1 for the QKV GEMM)
   MTL_TRY(ln_fwd(D.dtype, x, w->ln1_g, w->ln1_b, u1, at<float>(saved, L.mu1),
-                 at<float>(saved, L.rstd1), n, h, ln_eps, c),
+                 at<float>(saved, L.rstd1), n, h, ln_eps, c, next_amax_a()),
           "ln1 fwd");
   // F2 QKV, column-parallel: partition p = rows [p*3h/t, (p+1)*3h/t) of w_qkv
   {
     GemmArgs g = gemm_args(n, 3 * h, h, 1, u1, h, true, w->w_qkv, h, true, EPI_BIAS, qkv, 3 * h,
                            false, status);
     g.bias = w->b_qkv;
-    if ((gst = fwd_gemm(g, "qkv gemm")) != MTL_OK) return gst;
+    if ((gst = fwd_gemm(g, "qkv gemm", true)) != MTL_OK) return gst;
   }
   // F3 attention per head
   if (bf) {
@@ -504,9 +512,9 @@ mtl_status forward_core(const Dims& D, float ln_eps, const mtl_weights* w, const
     g.ldr = h;
     if ((gst = fwd_gemm(g, "out-proj gemm")) != MTL_OK) return gst;
   }
-  // F5 LN2
+  // F5 LN2 (and the amax of u2 for fc1)
   MTL_TRY(ln_fwd(D.dtype, x1, w->ln2_g, w->ln2_b, u2, at<float>(saved, L.mu2),
-                 at<float>(saved, L.rstd2), n, h, ln_eps, c),
+                 at<float>(saved, L.rstd2), n, h, ln_eps, c, next_amax_a()),
           "ln2 fwd");
   // F6 fc1, column-parallel + bias + GeLU (saves z and a)
   {
@@ -515,7 +523,7 @@ mtl_status forward_core(const Dims& D, float ln_eps, const mtl_weights* w, const
     g.bias = w->b_fc1;
     g.Z = z;
     g.ldz = f;
-    if ((gst = fwd_gemm(g, "fc1 gemm")) != MTL_OK) return gst;
+    if ((gst = fwd_gemm(g, "fc1 gemm", true)) != MTL_OK) return gst;
   }
   // F7 fc2, row-parallel + g: t partials over K = ffn, + b_fc2, dropout, + x1
   {
@@ -799,8 +807,9 @@ mtl_status mtl_layer_bwd(const mtl_layer_desc* desc, const mtl_weights* w, const
     // gradient and an E4M3 activation or weight, both K-major.  The forward left
     // the transposed E4M3 copies of its operands (and their scales) in `saved`;
     // each gradient is quantized once into a row-major and a transposed copy
-    // (one amax pass, one conversion pass).  Bias and LayerNorm gradients and
-    // attention stay bf16 / fp32.
+    // (its amax comes from the bias-gradient column sum, which reads the
+    // gradient anyway; then one conversion pass).  Bias and LayerNorm
+    // gradients and attention stay bf16 / fp32.
     const Fp8Ws FW = fp8_ws_layout(D);
     const Fp8Saved FS = fp8_saved_layout(D);
     const char* fsv = at<char>(saved, L.fp8);
@@ -814,12 +823,13 @@ mtl_status mtl_layer_bwd(const mtl_layer_desc* desc, const mtl_weights* w, const
     uint8_t* gqT = at<uint8_t>(fb, FW.gqT);
     MTL_TRY(cudaMemsetAsync(amax, 0, 64, s), "fp8 stats");
     int slot = 0;
-    // the gradient src [rows][cols] to E5M2: gq row-major, gqT transposed
+    // the gradient src [rows][cols] to E5M2: gq row-major, gqT transposed; its
+    // amax is in amax[slot], folded in by the column sum that read src
     auto quant_grad = [&](const void* src, int64_t rows, int64_t cols, const float** scale)
         -> cudaError_t {
       *scale = gscale + slot;
-      const cudaError_t e = fp8_quantize2(kBF16, src, rows, cols, cols, MTL_FP8_E5M2,
-                                          amax + slot, gscale + slot, gq, cols, gqT, rows, c);
+      const cudaError_t e = fp8_cast(kBF16, src, rows, cols, cols, MTL_FP8_E5M2, amax + slot,
+                                     gscale + slot, gq, cols, gqT, rows, c);
       ++slot;
       return e;
     };
@@ -838,23 +848,26 @@ mtl_status mtl_layer_bwd(const mtl_layer_desc* desc, const mtl_weights* w, const
     };
     const float* s_g;
     // MLP block
-    MTL_TRY(colsum(D.dtype, dy, h, n, h, static_cast<float*>(gr->b_fc2), partial, c), "db_fc2");
+    MTL_TRY(colsum(D.dtype, dy, h, n, h, static_cast<float*>(gr->b_fc2), partial, c, amax + slot),
+            "db_fc2");
     MTL_TRY(quant_grad(dy, n, h, &s_g), "fp8 dy");
     MTL_TRY(f8(n, f, h, 1, gq, s_g, wtr(3), fsc + 7, EPI_DGELU, dz, f, false, z), "fc2 dgrad");
     MTL_TRY(f8(h, f, n, 1, gqT, s_g, act(3), fsc + 6, EPI_STORE, gr->w_fc2, f, true, nullptr),
             "fc2 wgrad");
+    MTL_TRY(colsum(D.dtype, dz, f, n, f, static_cast<float*>(gr->b_fc1), partial, c, amax + slot),
+            "db_fc1");
     MTL_TRY(quant_grad(dz, n, f, &s_g), "fp8 dz");
     MTL_TRY(f8(n, h, f, t, gq, s_g, wtr(2), fsc + 5, EPI_STORE, du, h, true, nullptr),
             "fc1 dgrad");
     MTL_TRY(f8(f, h, n, 1, gqT, s_g, act(2), fsc + 4, EPI_STORE, gr->w_fc1, h, true, nullptr),
             "fc1 wgrad");
-    MTL_TRY(colsum(D.dtype, dz, f, n, f, static_cast<float*>(gr->b_fc1), partial, c), "db_fc1");
     MTL_TRY(ln_bwd(D.dtype, du, x1, at<float>(saved, L.mu2), at<float>(saved, L.rstd2), w->ln2_g,
                    dy, dx1, static_cast<float*>(gr->ln2_g), static_cast<float*>(gr->ln2_b),
                    partial, n, h, c),
             "ln2 bwd");
     // attention block
-    MTL_TRY(colsum(D.dtype, dx1, h, n, h, static_cast<float*>(gr->b_o), partial, c), "db_o");
+    MTL_TRY(colsum(D.dtype, dx1, h, n, h, static_cast<float*>(gr->b_o), partial, c, amax + slot),
+            "db_o");
     MTL_TRY(quant_grad(dx1, n, h, &s_g), "fp8 dx1");
     MTL_TRY(f8(n, h, h, 1, gq, s_g, wtr(1), fsc + 3, EPI_STORE, dctx, h, false, nullptr),
             "out-proj dgrad");
@@ -864,7 +877,8 @@ mtl_status mtl_layer_bwd(const mtl_layer_desc* desc, const mtl_weights* w, const
                         (int)D.seq, (int)D.heads, (int)D.d, make_drop(0.f, 0, SITE_ATTN),
                         nullptr, status, c),
             "attention bwd");
-    MTL_TRY(colsum(D.dtype, dqkv, 3 * h, n, 3 * h, static_cast<float*>(gr->b_qkv), partial, c),
+    MTL_TRY(colsum(D.dtype, dqkv, 3 * h, n, 3 * h, static_cast<float*>(gr->b_qkv), partial, c,
+                   amax + slot),
             "db_qkv");
     MTL_TRY(quant_grad(dqkv, n, 3 * h, &s_g), "fp8 dqkv");
     MTL_TRY(f8(3 * h, h, n, 1, gqT, s_g, act(0), fsc + 0, EPI_STORE, gr->w_qkv, h, true,

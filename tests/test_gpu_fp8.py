@@ -236,3 +236,51 @@ def test_fp8_hybrid_layer(name):
     assert all(v <= 0.12 for v in rms1.values()), rms1
     assert max(rms1.values()) > 0.01                       # the backward was quantized
     assert np.array_equal(g["y"], g1["y"])               # same forward
+
+
+def test_fp8_hybrid_scales_follow_planted_outliers():
+    """The A-operand and gradient amax values are folded in by the kernels that
+    write or read those tensors anyway (LayerNorm, the bias-gradient column
+    sums).  An outlier planted in the last token's last feature of x (u1 then
+    peaks there) and of dy (dy, and each gradient after it, then peaks in the
+    last row) must set the scales: the eight forward scales the hybrid layer
+    saves equal fmt_max / max|operand| of the GPU's own bf16 operands exactly,
+    and the backward stays within the hybrid bounds of the oracle (a gradient
+    amax that missed the outlier would clip it to the next largest value: an
+    error of order 1 in the last row's weight gradients)."""
+    import torch
+    import synthetic
+    from harness import compare, make, run_gpu, run_oracle, to_device
+    from tensor_model_transformer_gb300 import mtl
+    kw, t = FP8_SHAPES["d64_t4"]
+    shape = synthetic.tiny(dtype="bf16", w_std=0.02, out_std=0.01, **kw)
+    x, p, dy = make(shape, seed=5, affine=True)
+    x[-1, -1, -1] = 40.0
+    dy[-1, -1, -1] = 100.0
+    g1 = run_gpu(shape, x, p, dy, t, fp8=1)               # saves u1, u2 and a
+    assert np.argmax(np.abs(g1["s_u1"]).ravel()) == g1["s_u1"].size - 1
+    # the hybrid layer, keeping `saved` for its scales
+    desc = mtl.layer_desc(shape.h, shape.heads, shape.seq, x.shape[0], shape.ffn, t, "bf16", fp8=2)
+    dev_p = {k: to_device(v, "bf16") for k, v in p.items()}
+    xd, dyd = to_device(x, "bf16"), to_device(dy, "bf16")
+    saved, ws, grads = mtl.alloc_layer_buffers(desc)
+    y, dx = torch.empty_like(xd), torch.empty_like(xd)
+    mtl.layer_fwd(desc, dev_p, xd, y, saved, ws)
+    mtl.layer_check(ws)
+    mtl.layer_bwd(desc, dev_p, xd, saved, dyd, dx, grads, ws)
+    mtl.layer_check(ws)
+    torch.cuda.synchronize()
+    off = mtl.layer_saved_layout(desc)["fp8"]
+    scales = saved[off:off + 64].view(torch.float32).cpu().numpy()
+    operands = [g1["s_u1"], p["w_qkv"], g1["s_ctx"], p["w_o"], g1["s_u2"], p["w_fc1"],
+                g1["s_a"], p["w_fc2"]]
+    want = [np.float32(448.0) / np.float32(np.max(np.abs(o))) for o in operands]
+    assert np.array_equal(scales[:8], np.array(want, dtype=np.float32)), (scales[:8], want)
+    # the backward against the oracle, at the hybrid layer's bounds
+    g = {"y": to_np(y), "dx": to_np(dx)}
+    g.update({"d_" + k: to_np(v) for k, v in grads.items()})
+    ref = run_oracle(shape, x, p, dy, fp8=2)
+    errs = compare(g, ref, "bf16")
+    bad = {k: v for k, v in errs.items() if v > (FP8_TOL["y"] if k == "y" else 0.15)}
+    assert not bad, (bad, errs)
+    assert np.array_equal(g["y"], g1["y"])
