@@ -28,15 +28,36 @@ constexpr long long kWaitLimitCycles = 4000000000LL;
 using bf16 = __nv_bfloat16;
 
 // ---------------------------------------------------------------- elementwise
+// The standard normal Phi(z) and phi(z) from one exponential.  With
+// x = |z| / sqrt 2: erfc(x) ~ t (a1 + a2 t + ... + a5 t^4) exp(-x^2),
+// t = 1 / (1 + p x), the rational approximation 7.1.26 of Abramowitz and
+// Stegun, Handbook of Mathematical Functions (|error| <= 1.5e-7 on erf, with
+// its published p and a1..a5); Phi(-|z|) = erfc(x) / 2 and
+// phi(z) = exp(-x^2) / sqrt(2 pi).  A GeLU epilogue thus costs one reciprocal
+// and one exp2 per element.
+__device__ __forceinline__ void normal_cdf_pdf(float z, float& cdf, float& pdf) {
+  const float x = fabsf(z) * 0.70710678118654752f;
+  const float t = __fdividef(1.0f, fmaf(0.3275911f, x, 1.0f));
+  float q = fmaf(t, 1.061405429f, -1.453152027f);
+  q = fmaf(t, q, 1.421413741f);
+  q = fmaf(t, q, -0.284496736f);
+  q = fmaf(t, q, 0.254829592f);
+  const float g = exp2f(-0.72134752044448170f * z * z);  // exp(-x^2) = exp(-z^2 / 2)
+  const float tail = 0.5f * t * q * g;                  // Phi(-|z|)
+  cdf = z >= 0.f ? 1.0f - tail : tail;
+  pdf = 0.39894228040143268f * g;
+}
 __device__ __forceinline__ float gelu_f(float z) {
-  // GeLU(z) = z * Phi(z) = 0.5 z (1 + erf(z / sqrt 2))
-  return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
+  // GeLU(z) = z * Phi(z)
+  float cdf, pdf;
+  normal_cdf_pdf(z, cdf, pdf);
+  return z * cdf;
 }
 __device__ __forceinline__ float gelu_grad_f(float z) {
   // d/dz GeLU = Phi(z) + z * phi(z)
-  const float cdf = 0.5f * (1.0f + erff(z * 0.70710678118654752f));
-  const float pdf = 0.39894228040143268f * expf(-0.5f * z * z);
-  return cdf + z * pdf;
+  float cdf, pdf;
+  normal_cdf_pdf(z, cdf, pdf);
+  return fmaf(z, pdf, cdf);
 }
 
 template <typename T> __device__ __forceinline__ float to_f(T v);

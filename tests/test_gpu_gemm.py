@@ -104,3 +104,39 @@ def test_gemm_is_deterministic():
     a = run_case("bf16", 1024, 768, 1024, 4, 1, 0, EPI_STORE, True, seed=3)[0]
     b = run_case("bf16", 1024, 768, 1024, 4, 1, 0, EPI_STORE, True, seed=3)[0]
     assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("epi", [EPI_BIAS_GELU, EPI_DGELU])
+def test_gelu_epilogue_accuracy(epi):
+    """GeLU and GeLU' of the fused epilogues against the exact functions.  The
+    fp32 GEMM with one nonzero product per output (A[:, 0] = 1) puts a known
+    value z into every accumulator (EPI_BIAS_GELU: B[n, 0] = z_n; EPI_DGELU: the
+    product is 1 and Z holds z), so C is the epilogue's function of z alone.
+    Bound: 6e-7 * max(1, |z|) absolute (the erfc approximation's 1.5e-7 on erf,
+    halved for Phi, plus fp32 rounding of a few operations)."""
+    import torch
+    from tensor_model_transformer_gb300 import mtl
+    from scipy.special import erf
+    M, N, K = 64, 4096, 16
+    z = np.concatenate([np.linspace(-9.0, 9.0, N - 8),
+                        [0.0, 1e-3, -1e-3, 0.5, -0.5, 30.0, -30.0, 3.0]]).astype(np.float32)
+    A = np.zeros((M, K), np.float32)
+    A[:, 0] = 1.0
+    B = np.zeros((N, K), np.float32)
+    B[:, 0] = z if epi == EPI_BIAS_GELU else 1.0
+    Zd = torch.from_numpy(np.broadcast_to(z, (M, N)).copy()).cuda()
+    Cd = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    mtl.gemm("f32", M, N, K, 1, _dev(A, "f32"), K, 1, _dev(B, "f32"), K, 1, epi, Cd, N, True, ws,
+             bias=torch.zeros(N, dtype=torch.float32, device="cuda"), Z=Zd, ldz=N)
+    mtl.layer_check(ws)
+    torch.cuda.synchronize()
+    c = _host(Cd)
+    zz = z.astype(np.float64)
+    cdf = 0.5 * (1.0 + erf(zz / np.sqrt(2.0)))
+    pdf = np.exp(-0.5 * zz * zz) / np.sqrt(2.0 * np.pi)
+    want = zz * cdf if epi == EPI_BIAS_GELU else cdf + zz * pdf
+    err = np.abs(c - want[None, :]) / np.maximum(1.0, np.abs(zz))[None, :]
+    assert float(err.max()) <= 6e-7, (float(err.max()), float(zz[np.argmax(err.max(axis=0))]))
+    if epi == EPI_BIAS_GELU:                  # the saved pre-activation is z itself
+        assert np.array_equal(_host(Zd)[0], zz)
