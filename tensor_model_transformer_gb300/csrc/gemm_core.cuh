@@ -22,7 +22,9 @@ static_assert(PRODUCER_REGS * 128 + EPILOGUE_REGS * 32 * EPI_WARPS == LAUNCH_REG
               "register split must add up to the launch total");
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+constexpr int STAGE_OUT_BYTES = 4096;                       // epilogue output staging a warp
+constexpr int OUT_STAGING_BYTES = EPI_WARPS * STAGE_OUT_BYTES;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_STAGING_BYTES + BAR_BYTES + 1024;
 constexpr int GROUP_M = 16;   // tile raster: groups of 16 M-blocks sweep all N-blocks
 
 struct Params {
@@ -165,17 +167,117 @@ __device__ __forceinline__ void epi_chunk(const Params& p, int row, int col0, fl
   }
 }
 
+// Output staging for the TMA stores of the epilogue: each epilogue warp owns
+// STAGE_OUT_BYTES of shared memory (1024-aligned) holding one 32 x 32 chunk of
+// C (bf16: 64-byte rows in the 64-byte swizzle; fp32: 128-byte rows in the
+// 128-byte swizzle) and, for EPI_BIAS_GELU, the chunk of z (bf16) at +2048.
+template <int EPI, bool OUT_F32>
+__host__ __device__ constexpr bool tma_out() {   // fp32 C with z would not fit the warp's staging
+  return !(EPI == EPI_BIAS_GELU && OUT_F32);
+}
+
+// Row r's 16-byte piece q of a 32 x 32 staging chunk with 64-byte rows
+// (64-byte swizzle: q ^ bits 7-8 of the offset) and with 128-byte rows
+// (128-byte swizzle: q ^ bits 7-9).
+__device__ __forceinline__ uint32_t sw64_piece(int r, int q) { return r * 64 + ((q ^ ((r >> 1) & 3)) << 4); }
+__device__ __forceinline__ uint32_t sw128_piece(int r, int q) { return r * 128 + ((q ^ (r & 7)) << 4); }
+
+// epi_chunk for a whole chunk (col0 + 32 <= N) of the warp's 32 rows row0 + lane,
+// written through the warp's staging buffer by TMA stores (rows >= M are
+// computed on zeros and dropped by the tensor map's bounds).  Called by all 32
+// lanes; lane 0 issues the stores.
+// side: the chunk's 32 bf16 of R (EPI_BIAS_RESID) or Z (EPI_DGELU) of this
+// lane's row, loaded ahead by the caller (side_load).
+template <int EPI, bool OUT_F32>
+__device__ __forceinline__ void epi_chunk_tma(const Params& p, int row0, int col0,
+                                              float (&v)[32], uint32_t keep, int lane,
+                                              const uint4 (&side)[4], const CUtensorMap* tmC,
+                                              const CUtensorMap* tmZ, uint32_t stage) {
+  if (EPI == EPI_BIAS || EPI == EPI_BIAS_RESID || EPI == EPI_BIAS_GELU) {
+    const uint4* bp = reinterpret_cast<const uint4*>(p.bias + col0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 u = __ldg(bp + q);
+      const bf16* hb = reinterpret_cast<const bf16*>(&u);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[q * 8 + e] += __bfloat162float(hb[e]);
+    }
+  }
+  if (EPI == EPI_BIAS_RESID && p.drop.on) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[e] = ((keep >> e) & 1u) ? v[e] * p.drop.scale : 0.f;
+  }
+  if (EPI == EPI_BIAS_RESID) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const bf16* hb = reinterpret_cast<const bf16*>(&side[q]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[q * 8 + e] += __bfloat162float(hb[e]);
+    }
+  }
+  if (EPI == EPI_DGELU) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const bf16* hb = reinterpret_cast<const bf16*>(&side[q]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[q * 8 + e] *= gelu_grad_f(__bfloat162float(hb[e]));
+    }
+  }
+  auto pack2 = [](float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  };
+  // the previous chunk's stores have read the staging buffer
+  if (lane == 0) bulk_wait_read0();
+  __syncwarp();
+  if (EPI == EPI_BIAS_GELU) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      st_shared_v4(stage + 2048 + sw64_piece(lane, q), pack2(v[8 * q], v[8 * q + 1]),
+                   pack2(v[8 * q + 2], v[8 * q + 3]), pack2(v[8 * q + 4], v[8 * q + 5]),
+                   pack2(v[8 * q + 6], v[8 * q + 7]));
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[e] = gelu_f(v[e]);
+  }
+  if (OUT_F32) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      st_shared_v4(stage + sw128_piece(lane, q), __float_as_uint(v[4 * q]),
+                   __float_as_uint(v[4 * q + 1]), __float_as_uint(v[4 * q + 2]),
+                   __float_as_uint(v[4 * q + 3]));
+  } else {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      st_shared_v4(stage + sw64_piece(lane, q), pack2(v[8 * q], v[8 * q + 1]),
+                   pack2(v[8 * q + 2], v[8 * q + 3]), pack2(v[8 * q + 4], v[8 * q + 5]),
+                   pack2(v[8 * q + 6], v[8 * q + 7]));
+  }
+  fence_proxy_async_shared();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tmC, stage, col0, row0);
+    if (EPI == EPI_BIAS_GELU) tma_store_2d(tmZ, stage + 2048, col0, row0);
+    bulk_commit();
+  }
+}
+
 // Epilogue warps 4..11: wait for an accumulator, read it from TMEM (32 columns
 // at a time), add partition partials in order, apply the epilogue, store.
 // tfull0 / tempty0: addresses of tfull[0] and tempty[0] (tempty as a cluster
 // address when PAIR: the epilogue warps of both CTAs of a pair release the
 // accumulator to the leader CTA's barrier).  Tiles tile0, tile0 + tile_step, ...
 // are tile_rows high; this CTA's rows start at row_off inside a tile.
-template <int EPI, bool OUT_F32, bool REDUCE, bool PAIR>
+// tmC / tmZ: tensor maps of C and z (32 x 32 boxes) for the TMA stores of
+// whole chunks; out_stage: the shared staging area (OUT_STAGING_BYTES).
+// AHEAD: R / Z of the next chunk are loaded while this one is processed (the
+// FP8 kernels, whose shorter main loop leaves the epilogue exposed; measured
+// slower for bf16).
+template <int EPI, bool OUT_F32, bool REDUCE, bool PAIR, bool AHEAD>
 __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t tmem_base, uint32_t tfull0,
                                               uint32_t tempty0, volatile int* abort_flag,
                                               int warp, int lane, int tile0, int tile_step,
-                                              int tile_rows, int row_off) {
+                                              int tile_rows, int row_off, const CUtensorMap* tmC,
+                                              const CUtensorMap* tmZ, uint32_t out_stage) {
   auto tfull_bar = [&](int b) { return tfull0 + 8u * b; };
   auto tempty_bar = [&](int b) { return tempty0 + 8u * b; };
   const int ew = warp - 4;
@@ -183,6 +285,38 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t tmem_bas
   const int chalf = ew >> 2;
   // FP8 descale (exactly 1 for bf16 operands)
   const float ds = p.scale_a ? __fdiv_rn(1.0f, __fmul_rn(*p.scale_a, *p.scale_b)) : 1.0f;
+  const uint32_t stage = out_stage + ew * STAGE_OUT_BYTES;
+  // one 32 x 32 chunk of the epilogue: whole chunks through TMA stores, ragged
+  // ones (col0 + 32 > N) element by element
+  // R (EPI_BIAS_RESID) or Z (EPI_DGELU) of a whole chunk is read into
+  // registers; with AHEAD one chunk ahead (the first chunk of a tile before its
+  // accumulator is waited for), so the global-load latency overlaps the
+  // previous chunk's work
+  constexpr bool SIDE = tma_out<EPI, OUT_F32>() && (EPI == EPI_BIAS_RESID || EPI == EPI_DGELU);
+  auto side_load = [&](int row, int col0, uint4(&dst)[4]) {
+    if constexpr (SIDE) {
+      if (row < p.M && col0 + 32 <= p.N) {
+        const bf16* src = EPI == EPI_DGELU ? p.Z + (size_t)row * p.ldz + col0
+                                           : p.R + (size_t)row * p.ldr + col0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dst[q] = reinterpret_cast<const uint4*>(src)[q];
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+  };
+  auto chunk = [&](int row, int col0, float(&v)[32], uint32_t keep, const uint4(&side)[4]) {
+    if (col0 >= p.N) return;
+    const int row0 = row - lane;
+    if constexpr (tma_out<EPI, OUT_F32>()) {
+      if (col0 + 32 <= p.N) {
+        if (row0 < p.M) epi_chunk_tma<EPI, OUT_F32>(p, row0, col0, v, keep, lane, side, tmC, tmZ, stage);
+        return;
+      }
+    }
+    epi_chunk<EPI, OUT_F32>(p, row, col0, v, keep);
+  };
   int unit = 0;
   bool ok = true;
   for (int tile = tile0; tile < p.num_tiles && ok; tile += tile_step) {
@@ -190,6 +324,8 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t tmem_bas
     tile_coords(p, tile, mb, nb);
     const int row = mb * tile_rows + row_off + quarter * 32 + lane;
     const int colbase = nb * BN + chalf * 128;
+    uint4 side[4];
+    if (!REDUCE && AHEAD) side_load(row, colbase, side);
     float sum[REDUCE ? 128 : 1];
     for (int u = 0; u < p.units_per_tile; ++u, ++unit) {
       const int buf = unit & 1;
@@ -213,10 +349,17 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t tmem_bas
             sum[c * 32 + i] = (u == 0) ? x : sum[c * 32 + i] + x;
           }
         } else {
+          uint4 next[4];
+          if (AHEAD && c < 3) side_load(row, colbase + (c + 1) * 32, next);
+          if (!AHEAD) side_load(row, colbase + c * 32, side);
           float v[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * ds;
-          epi_chunk<EPI, OUT_F32>(p, row, colbase + c * 32, v, keep);
+          chunk(row, colbase + c * 32, v, keep, side);
+          if (AHEAD && c < 3) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) side[q] = next[q];
+          }
         }
       }
       tc_fence_before();
@@ -233,14 +376,17 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t tmem_bas
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const uint32_t keep = chunk_keep<EPI>(p, row, colbase + c * 32);
+          side_load(row, colbase + c * 32, side);   // (128 partition sums leave no room ahead)
           float v[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = sum[c * 32 + i] * ds;
-          epi_chunk<EPI, OUT_F32>(p, row, colbase + c * 32, v, keep);
+          chunk(row, colbase + c * 32, v, keep, side);
         }
       }
     }
   }
+  __syncwarp();
+  if (lane == 0) bulk_wait0();   // the last stores are written before the kernel ends
   __syncwarp();
 }
 
@@ -261,25 +407,30 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t tmem_bas
 //   tempty[b] leader only: 16 arrivals, the epilogue warps of both CTAs
 constexpr int P_BK = 128, P_HALF = 128;              // K elements per stage, rows per CTA
 constexpr int P_ATOM = P_HALF * 128;                 // one [128 rows][128 bytes] box
-constexpr int P_SMEM_BYTES = 3 * 2 * 2 * P_ATOM + BAR_BYTES + 1024;   // 192 KB of stages
+constexpr int P_SMEM_BYTES = 3 * 2 * 2 * P_ATOM + OUT_STAGING_BYTES + BAR_BYTES + 1024;   // 192 KB of stages
 
 template <int EPI, bool OUT_F32, bool REDUCE, bool F8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
-                    const __grid_constant__ CUtensorMap tmB, const Params p) {
+                    const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmC,
+                    const __grid_constant__ CUtensorMap tmZ, const Params p) {
   constexpr int P_NBOX = F8 ? 1 : 2;                 // 128-byte boxes per row and stage
   constexpr int P_STAGES = F8 ? 6 : 3;
   constexpr int P_A_BYTES = P_NBOX * P_ATOM;
   constexpr int P_B_BYTES = P_NBOX * P_ATOM;
   constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
   constexpr int P_KSTEPS = F8 ? P_BK / 32 : P_BK / 16;   // MMAs per stage
-  static_assert(P_STAGES * P_STAGE_BYTES + BAR_BYTES + 1024 <= P_SMEM_BYTES, "stage ring");
+  static_assert(P_STAGES * P_STAGE_BYTES + OUT_STAGING_BYTES + BAR_BYTES + 1024 <= P_SMEM_BYTES,
+                "stage ring");
+  static_assert(P_SMEM_BYTES <= 232448, "shared memory of one CTA");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sA0 = smem_u32(smem);
   const uint32_t sB0 = sA0 + P_STAGES * P_A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P_STAGES * P_STAGE_BYTES);
+  const uint32_t out_stage = sA0 + P_STAGES * P_STAGE_BYTES;   // 1024-aligned
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P_STAGES * P_STAGE_BYTES + OUT_STAGING_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * P_STAGES + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
@@ -307,6 +458,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmC);
+    if (EPI == EPI_BIAS_GELU) tma_prefetch_desc(&tmZ);
   }
   tc_fence_before();
   cluster_sync();
@@ -320,9 +473,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   }
 
   if (warp >= 4) {
-    epilogue_role<EPI, OUT_F32, REDUCE, true>(p, tmem_base, tfull_bar(0),
+    epilogue_role<EPI, OUT_F32, REDUCE, true, F8>(p, tmem_base, tfull_bar(0),
                                               cluster_map(tempty_bar(0), 0), abort_flag, warp,
-                                              lane, pair_id, npairs, 2 * P_HALF, P_HALF * rank);
+                                              lane, pair_id, npairs, 2 * P_HALF, P_HALF * rank,
+                                              &tmC, &tmZ, out_stage);
   } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
@@ -465,6 +619,33 @@ inline bool make_map(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t ro
              const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor map of a GEMM output for the epilogue's TMA stores: [rows][cols] of
+// bf16 or fp32 with row pitch ld elements, 32 x 32 boxes in the swizzle the
+// staging chunk uses (64-byte rows: 64-byte swizzle; 128-byte rows: 128-byte).
+inline bool make_out_map(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows,
+                         int64_t ld, bool f32) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * (f32 ? 4 : 2)};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+             const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The C and z maps of a GEMM (z: EPI_BIAS_GELU with a bf16 C; otherwise a copy
+// of the C map, never used).
+inline bool make_epilogue_maps(CUtensorMap* mc, CUtensorMap* mz, const GemmArgs& a) {
+  if (!make_out_map(mc, a.C, (uint64_t)a.N, (uint64_t)a.M, a.ldc, a.c_f32)) return false;
+  if (a.epi == EPI_BIAS_GELU && !a.c_f32)
+    return make_out_map(mz, a.Z, (uint64_t)a.N, (uint64_t)a.M, a.ldz, false);
+  *mz = *mc;
+  return true;
 }
 
 }  // namespace tcg

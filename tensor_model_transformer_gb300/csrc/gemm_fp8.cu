@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(QTHREADS) cast_transpose_kernel(
 
 namespace tcg {
 
-typedef void (*KernelFn)(CUtensorMap, CUtensorMap, Params);
+typedef void (*KernelFn)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, Params);
 
 template <int EPI, bool F32, bool RED>
 static KernelFn kernel8_ptr() {
@@ -254,6 +254,8 @@ cudaError_t gemm_fp8(const GemmArgs& a, const LaunchCtx& c) {
   if (!make_map(&ma, a.A.ptr, (uint64_t)a.K, (uint64_t)a.M, a.A.ld, 128, 128, true) ||
       !make_map(&mb, a.B.ptr, (uint64_t)a.K, (uint64_t)a.N, a.B.ld, 128, 128, true))
     return cudaErrorInvalidValue;
+  CUtensorMap mc, mz;
+  if (!make_epilogue_maps(&mc, &mz, a)) return cudaErrorInvalidValue;
   Params p;
   memset(&p, 0, sizeof(p));
   p.M = a.M;
@@ -291,7 +293,7 @@ cudaError_t gemm_fp8(const GemmArgs& a, const LaunchCtx& c) {
   const int pairs = c.num_sms / 2;
   const int grid = 2 * (p.num_tiles < pairs ? p.num_tiles : pairs);
   c.before(KK_GEMM_FP8, 2.0 * a.M * a.N * a.K);
-  fn<<<grid, THREADS, P_SMEM_BYTES, c.stream>>>(ma, mb, p);
+  fn<<<grid, THREADS, P_SMEM_BYTES, c.stream>>>(ma, mb, mc, mz, p);
   c.after();
   return cudaGetLastError();
 }

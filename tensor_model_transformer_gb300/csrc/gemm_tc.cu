@@ -39,13 +39,16 @@ namespace tcg {
 template <int EPI, bool OUT_F32, bool REDUCE>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmZ,
                    const Params p) {
+  static_assert(SMEM_BYTES <= 232448, "shared memory of one CTA");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sA0 = smem_u32(smem);
   const uint32_t sB0 = sA0 + STAGES * A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  const uint32_t out_stage = sA0 + STAGES * STAGE_BYTES;   // 1024-aligned
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + OUT_STAGING_BYTES);
   // bars[0..S): full, [S..2S): empty, [2S..2S+2): tmem full, [2S+2..2S+4): tmem empty
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -73,6 +76,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmC);
+    if (EPI == EPI_BIAS_GELU) tma_prefetch_desc(&tmZ);
   }
   tc_fence_before();
   __syncthreads();
@@ -86,9 +91,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   if (warp >= 4) {
-    epilogue_role<EPI, OUT_F32, REDUCE, false>(p, tmem_base, tfull_bar(0), tempty_bar(0),
+    epilogue_role<EPI, OUT_F32, REDUCE, false, false>(p, tmem_base, tfull_bar(0), tempty_bar(0),
                                                abort_flag, warp, lane, blockIdx.x, gridDim.x, BM,
-                                               0);
+                                               0, &tmC, &tmZ, out_stage);
   } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -204,7 +209,7 @@ bool make_operand_map(CUtensorMap* m, const GemmOperand& op, int mn, int K, int 
   return make_map(m, op.ptr, (uint64_t)mn, (uint64_t)K, op.ld, 64, BK);
 }
 
-typedef void (*KernelFn)(CUtensorMap, CUtensorMap, Params);
+typedef void (*KernelFn)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, Params);
 
 template <int EPI, bool F32, bool RED>
 KernelFn kernel_ptr() {
@@ -281,6 +286,8 @@ cudaError_t gemm_tc(const GemmArgs& a, const LaunchCtx& c) {
              !make_operand_map(&mb, a.B, a.N, a.K, BN)) {
     return cudaErrorInvalidValue;
   }
+  CUtensorMap mc, mz;
+  if (!make_epilogue_maps(&mc, &mz, a)) return cudaErrorInvalidValue;
   Params p;
   memset(&p, 0, sizeof(p));   // no FP8 scales: the epilogue's descale is 1
   p.M = a.M;
@@ -332,7 +339,7 @@ cudaError_t gemm_tc(const GemmArgs& a, const LaunchCtx& c) {
     grid = p.num_tiles < c.num_sms ? p.num_tiles : c.num_sms;
   }
   c.before(KK_GEMM_TC, 2.0 * a.M * a.N * a.K);
-  fn<<<grid, THREADS, smem_bytes, c.stream>>>(ma, mb, p);
+  fn<<<grid, THREADS, smem_bytes, c.stream>>>(ma, mb, mc, mz, p);
   c.after();
   return cudaGetLastError();
 }
