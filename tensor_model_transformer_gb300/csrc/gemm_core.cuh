@@ -187,7 +187,7 @@ __device__ __forceinline__ uint32_t sw128_piece(int r, int q) { return r * 128 +
 // computed on zeros and dropped by the tensor map's bounds).  Called by all 32
 // lanes; lane 0 issues the stores.
 // side: the chunk's 32 bf16 of R (EPI_BIAS_RESID) or Z (EPI_DGELU) of this
-// lane's row, loaded ahead by the caller (side_load).
+// lane's row, read by the caller (side_load).
 template <int EPI, bool OUT_F32>
 __device__ __forceinline__ void epi_chunk_tma(const Params& p, int row0, int col0,
                                               float (&v)[32], uint32_t keep, int lane,
