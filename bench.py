@@ -590,6 +590,8 @@ def main():
             loaded[b].record(copy)
 
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_clocks = ClockSampler(local)
+    e2e_clocks.start()
     e0.record(stream)
     copy.wait_event(e0)
     e2e_step_io(0)
@@ -611,6 +613,7 @@ def main():
     e1.record(copy_out)
     e1.synchronize()
     torch.cuda.synchronize()
+    e2e_clk = e2e_clocks.stop()
     ms_e2e = e0.elapsed_time(e1)
     ms_e2e, e2e_value = aggregate_over_ranks(ms_e2e, flops, args.steps, world,
                                              dist if world > 1 else None, "cuda")
@@ -696,7 +699,7 @@ def main():
         "peak_source": pk_src,
         "gpu_launches": launches,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 2 * nbytes,
-                "d2h_bytes_per_step": 2 * nbytes},
+                "d2h_bytes_per_step": 2 * nbytes, "clocks": e2e_clk},
         "roofline": roofline,
         "kernels": breakdown,
     }
