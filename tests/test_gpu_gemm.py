@@ -92,6 +92,18 @@ def test_epilogues(dtype, epi, parts):
         assert rel(z, zref) < tol(dtype, False)
 
 
+@pytest.mark.parametrize("epi", [EPI_BIAS, EPI_BIAS_RESID, EPI_BIAS_GELU, EPI_DGELU])
+@pytest.mark.parametrize("parts", [1, 2])
+def test_epilogues_fp32_output(epi, parts):
+    # every fused epilogue with an fp32 C on the tensor-core path; N = 336 ends
+    # in a half chunk (whole chunks leave through TMA stores, the last one
+    # element by element) and M = 296 in a partial tile
+    c, ref, z, zref = run_case("bf16", 296, 336, 256, parts, 1, 1, epi, True)
+    assert rel(c, ref) < 2e-6
+    if z is not None:
+        assert rel(z, zref) < tol("bf16", False)
+
+
 def test_many_tiles_per_cta():
     # more tiles than SMs: the persistent loop and the TMEM double buffer cycle
     c, ref, _, _ = run_case("bf16", 4096, 2048, 512, 1, 1, 1, EPI_STORE, True)
