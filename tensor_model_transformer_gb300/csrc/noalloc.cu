@@ -8,7 +8,9 @@
 // until the process exits.  Host code cannot use the array's name as a device
 // address (it names a host-side shadow), so the first call on each device looks
 // the address up with cudaGetSymbolAddress, with that device current, and
-// passes it to the kernels.
+// passes it to the kernels.  Only a successful lookup is kept: a call whose
+// lookup failed (for instance one made during stream capture) returns
+// MTL_ERR_CUDA and the next call on that device tries again.
 #include <mutex>
 
 #include "../../include/mtl.h"
@@ -24,9 +26,22 @@ constexpr size_t kScratchFloats = (size_t)128 * kMaxCols;
 
 __device__ __align__(256) float g_bias_grad_scratch[kScratchFloats];
 
-float* g_scratch_addr[kMaxDevices];
-cudaError_t g_setup_status[kMaxDevices];
-std::once_flag g_setup_once[kMaxDevices];
+float* g_scratch_addr[kMaxDevices];   // non-null once the lookup succeeded
+std::mutex g_setup_mutex;
+
+// The scratch array's device address on device `dev` (current), looked up on
+// the first successful call.
+cudaError_t scratch_address(int dev, float** addr) {
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_bias_grad_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = static_cast<float*>(p);
+  }
+  *addr = g_scratch_addr[dev];
+  return cudaSuccess;
+}
 
 }  // namespace
 
@@ -49,12 +64,11 @@ extern "C" mtl_status mtl_bias_grad_noalloc(int32_t dtype, const void* dy, int64
     return MTL_ERR_CUDA;
   }
   if (dev < 0 || dev >= kMaxDevices) return MTL_ERR_UNSUPPORTED;
-  std::call_once(g_setup_once[dev], [dev]() {
-    g_setup_status[dev] =
-        cudaGetSymbolAddress(reinterpret_cast<void**>(&g_scratch_addr[dev]), g_bias_grad_scratch);
-  });
-  if (g_setup_status[dev] != cudaSuccess) {
-    mtl::record_cuda_error(g_setup_status[dev], "bias grad: scratch address");
+  float* scratch = nullptr;
+  e = scratch_address(dev, &scratch);
+  if (e != cudaSuccess) {
+    cudaGetLastError();   // the failed lookup leaves nothing behind for later calls
+    mtl::record_cuda_error(e, "bias grad: scratch address");
     return MTL_ERR_CUDA;
   }
 
@@ -62,7 +76,7 @@ extern "C" mtl_status mtl_bias_grad_noalloc(int32_t dtype, const void* dy, int64
   mtl::LaunchCtx c{reinterpret_cast<cudaStream_t>(stream), 0, &launches, nullptr};
   // Every partial the second pass reads is written by the first pass of the
   // same call, so the scratch needs no clearing between calls.
-  e = mtl::colsum(dtype, dy, ld, rows, cols, static_cast<float*>(out), g_scratch_addr[dev], c);
+  e = mtl::colsum(dtype, dy, ld, rows, cols, static_cast<float*>(out), scratch, c);
   if (e != cudaSuccess) {
     mtl::record_cuda_error(e, "bias grad");
     return MTL_ERR_CUDA;
