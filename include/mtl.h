@@ -310,7 +310,9 @@ mtl_status mtl_gemm_fp8(int32_t M, int32_t N, int32_t K, int32_t k_parts, const 
  * 16384 return MTL_ERR_UNSUPPORTED.  Nothing is allocated or freed: no
  * cudaMalloc, no cudaFree, no allocating library call.  The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress, with that
- * device current); make that first call before any stream capture.  All calls
+ * device current); make that first call before any stream capture.  A failed
+ * lookup returns MTL_ERR_CUDA and is not kept: the next call on that device
+ * looks the address up again.  All calls
  * on a device share the one array, whose contents persist from the last call:
  * calls that overlap on the GPU (different streams, no ordering) race and give
  * wrong sums, so order them on one stream.  Returns MTL_ERR_INVALID_ARG for
@@ -324,6 +326,14 @@ mtl_status mtl_bias_grad_noalloc(int32_t dtype, const void* dy, int64_t ld, int3
  * timeout in the status word of `workspace` (>= 256 bytes), so a following
  * mtl_layer_check returns MTL_ERR_TIMEOUT; the GPU context stays usable. */
 mtl_status mtl_selftest_wait_timeout(void* workspace, int64_t limit_cycles, mtl_stream stream);
+
+/* Failure-detection self-test of the launch-error path: enqueues an empty
+ * kernel with 2048 threads a block, above the 1024-thread limit of CUDA
+ * devices, so the runtime refuses the launch before anything runs on the GPU.
+ * Returns MTL_ERR_CUDA, with the runtime's error text in mtl_last_cuda_error,
+ * the way every entry point reports a failed launch; the error is not sticky,
+ * so the context stays usable. */
+mtl_status mtl_selftest_launch_error(mtl_stream stream);
 
 /* Human-readable name of a status. */
 const char* mtl_status_str(mtl_status s);

@@ -1057,6 +1057,23 @@ mtl_status mtl_selftest_wait_timeout(void* workspace, int64_t limit_cycles, mtl_
   return MTL_OK;
 }
 
+namespace {
+__global__ void selftest_empty_kernel() {}
+}  // namespace
+
+mtl_status mtl_selftest_launch_error(mtl_stream stream) {
+  g_launches = 0;
+  g_cuda_err[0] = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // 2048 threads a block is above the 1024-thread limit of every CUDA device:
+  // the runtime rejects the launch configuration and nothing reaches the GPU.
+  selftest_empty_kernel<<<1, 2048, 0, s>>>();
+  const cudaError_t e = cudaGetLastError();   // returns and clears the launch error
+  if (e != cudaSuccess) return cuda_fail(e, "selftest launch");
+  ++g_launches;
+  return MTL_OK;
+}
+
 // ---------------------------------------------------------------- attention alone
 
 

@@ -91,6 +91,8 @@ def lib():
                                    vp, vp, i64, vp, i64, vp, i64, i32, vp, sz, vp]
         L.mtl_selftest_wait_timeout.argtypes = [vp, i64, vp]
         L.mtl_selftest_wait_timeout.restype = ctypes.c_int
+        L.mtl_selftest_launch_error.argtypes = [vp]
+        L.mtl_selftest_launch_error.restype = ctypes.c_int
         L.mtl_bias_grad_noalloc.argtypes = [i32, vp, i64, i32, i32, vp, vp]
         L.mtl_bias_grad_noalloc.restype = ctypes.c_int
         L.mtl_status_str.argtypes = [ctypes.c_int]
@@ -294,6 +296,12 @@ def gemm_fp8(M, N, K, parts, A, lda, fmt_a, scale_a, B, ldb, fmt_b, scale_b, epi
            "mtl_gemm_fp8")
 
 
+def selftest_launch_error(stream=None):
+    """mtl_selftest_launch_error: a launch the runtime refuses; raises MtlError
+    with status MTL_ERR_CUDA and the runtime's error text."""
+    _check(lib().mtl_selftest_launch_error(_stream(stream)), "mtl_selftest_launch_error")
+
+
 def selftest_wait_timeout(workspace, limit_cycles, stream=None):
     """mtl_selftest_wait_timeout: a bounded device wait that is made to run out."""
     _check(lib().mtl_selftest_wait_timeout(_ptr(workspace), limit_cycles, _stream(stream)),
@@ -305,7 +313,16 @@ def bias_grad_noalloc(dtype, dy, ld, rows, cols, out, stream=None):
 
     For callers that cannot allocate device memory; its scratch is a static
     array inside the library (see include/mtl.h)."""
+    import torch
     dt = {"f32": F32, "bf16": BF16, F32: F32, BF16: BF16}[dtype]
+    want = torch.bfloat16 if dt == BF16 else torch.float32
+    if dy.dtype != want or out.dtype != torch.float32:
+        raise MtlError(1, "mtl_bias_grad_noalloc", "dy must match dtype and out must be float32")
+    if not (dy.is_cuda and out.is_cuda and out.is_contiguous()):
+        raise MtlError(1, "mtl_bias_grad_noalloc", "dy and out must be contiguous device tensors")
+    if rows < 0 or cols <= 0 or ld < cols or out.numel() < cols or (
+            rows > 0 and dy.numel() < (rows - 1) * ld + cols):
+        raise MtlError(1, "mtl_bias_grad_noalloc", "dy or out is smaller than rows, ld and cols")
     _check(lib().mtl_bias_grad_noalloc(dt, _ptr(dy), ld, rows, cols, _ptr(out), _stream(stream)),
            "mtl_bias_grad_noalloc")
 

@@ -70,3 +70,18 @@ def test_bounded_wait_times_out_and_context_survives():
     # the context still runs a layer correctly
     check(synthetic.tiny(h=128, heads=2, seq=128, batch=1, dtype="bf16", w_std=0.02,
                          out_std=0.01), t=1)
+
+
+def test_launch_failure_maps_to_cuda_error_and_context_survives():
+    """A launch the runtime refuses (a block above the 1024-thread limit, checked
+    on the host before anything runs) comes back as MTL_ERR_CUDA with the
+    runtime's text, and the next layer call runs correctly."""
+    from tensor_model_transformer_gb300 import mtl
+    with pytest.raises(mtl.MtlError) as ei:
+        mtl.selftest_launch_error()
+    assert ei.value.status == 4                # MTL_ERR_CUDA
+    text = mtl.lib().mtl_last_cuda_error().decode()
+    assert text.startswith("selftest launch:") and len(text) > len("selftest launch: "), text
+    check(synthetic.tiny(h=128, heads=2, seq=128, batch=1, dtype="bf16", w_std=0.02,
+                         out_std=0.01), t=1)
+    assert mtl.lib().mtl_last_cuda_error().decode() == ""
