@@ -51,7 +51,7 @@ def _run(batch, seq, heads, d, qkv, dctx):
 
 @pytest.mark.parametrize("batch,seq,heads,d,amp", CASES)
 def test_attention_random(batch, seq, heads, d, amp):
-    from harness import TOL, rel_err
+    from harness import TOL, rel_err, rel_err_qkv
     rng = np.random.default_rng(seq * 7 + d)
     qkv = _bf16(rng.standard_normal((batch * seq, 3 * heads * d)) * np.sqrt(amp))
     dctx = _bf16(rng.standard_normal((batch * seq, heads * d)))
@@ -60,4 +60,6 @@ def test_attention_random(batch, seq, heads, d, amp):
     dqkv_r = oracle.multihead_bwd(qkv, ctx_r, probs, dctx, batch, seq, heads, d)
     assert rel_err(ctx_g.reshape(ctx_r.shape), ctx_r) <= TOL["bf16"]["fwd"]
     assert np.max(np.abs(lse_g.reshape(lse_r.shape) - lse_r) / np.maximum(1.0, np.abs(lse_r))) < 1e-3
-    assert rel_err(dqkv_g.reshape(dqkv_r.shape), dqkv_r) <= TOL["bf16"]["bwd"]
+    # dQ, dK and dV of every head are judged against their own scale: with a
+    # near-uniform softmax (amp 0.02) dQ and dK are ~70x smaller than dV
+    assert rel_err_qkv(dqkv_g.reshape(dqkv_r.shape), dqkv_r, 1, heads) <= TOL["bf16"]["bwd"]

@@ -16,11 +16,11 @@ pytestmark = pytest.mark.gpu
 TOL = {"f32": 1e-5, "bf16": 1.5e-2}
 
 
-def _setup(shape, max_seq, seed=0):
+def _setup(shape, max_seq, seed=0, t=1, affine=True):
     import torch
     from tensor_model_transformer_gb300 import mtl
-    x, p, _ = synthetic.make_layer(shape, seed=seed, affine=True)
-    desc = mtl.layer_desc(shape.h, shape.heads, shape.seq, shape.batch, shape.ffn, 1, shape.dtype)
+    x, p, _ = synthetic.make_layer(shape, seed=seed, affine=affine)
+    desc = mtl.layer_desc(shape.h, shape.heads, shape.seq, shape.batch, shape.ffn, t, shape.dtype)
     kvb, pwb, dwb = mtl.infer_sizes(desc, max_seq)
     dev = {k: to_device(v, shape.dtype) for k, v in p.items()}
     kv = torch.zeros(kvb, dtype=torch.uint8, device="cuda")
@@ -36,33 +36,42 @@ def _tokens(shape, steps, seed):
                                 shape.dtype)
 
 
-def run_case(shape, max_seq, steps, seed=0):
+def run_case(shape, max_seq, steps, seed=0, t=1, check=None, affine=True):
+    """Prefill and `steps` decode steps of every sequence on the GPU; the
+    sequences `check` (default: all) are run through the oracle on their own
+    (sequences are independent) and compared."""
     import torch
     from tensor_model_transformer_gb300 import mtl
-    x, p, desc, dev, kv, pws, dws, lens = _setup(shape, max_seq, seed)
+    x, p, desc, dev, kv, pws, dws, lens = _setup(shape, max_seq, seed, t, affine)
+    sel = list(range(shape.batch)) if check is None else list(check)
     toks = _tokens(shape, steps, seed + 7)
     xd = to_device(x, shape.dtype)
     y = torch.empty_like(xd)
     mtl.layer_prefill(desc, dev, xd, y, kv, max_seq, lens, pws)
     mtl.layer_check(pws)
-    cache = oracle.decode.kv_cache(shape.batch, shape.heads, max_seq, shape.h // shape.heads)
-    y_ref = oracle.decode.prefill(p, x, shape.heads, cache)
+    cache = oracle.decode.kv_cache(len(sel), shape.heads, max_seq, shape.h // shape.heads)
+    y_ref = oracle.decode.prefill(p, x[sel], shape.heads, cache)
     tol = TOL[shape.dtype]
-    assert rel_err(to_np(y), y_ref) <= tol
+    assert rel_err(to_np(y)[sel], y_ref) <= tol
     assert lens.cpu().tolist() == [shape.seq] * shape.batch
     for i in range(steps):
         xt = to_device(toks[i], shape.dtype)
         yt = torch.empty_like(xt)
         mtl.layer_decode(desc, dev, xt, yt, kv, max_seq, lens, dws)
         mtl.layer_check(dws)
-        yr = oracle.decode.decode_step(p, toks[i], shape.heads, cache)
-        assert rel_err(to_np(yt), yr) <= tol, (i, rel_err(to_np(yt), yr))
+        yr = oracle.decode.decode_step(p, toks[i][sel], shape.heads, cache)
+        assert rel_err(to_np(yt)[sel], yr) <= tol, (i, rel_err(to_np(yt)[sel], yr))
     assert lens.cpu().tolist() == [shape.seq + steps] * shape.batch
     k, v = mtl.kv_views(desc, kv, max_seq)
     L = shape.seq + steps
-    assert rel_err(to_np(k)[:, :, :L], cache["k"][:, :, :L]) <= tol
-    assert rel_err(to_np(v)[:, :, :L], cache["v"][:, :, :L]) <= tol
-    assert np.all(to_np(k)[:, :, L:] == 0)
+    k, v = to_np(k), to_np(v)
+    assert rel_err(k[sel][:, :, :L], cache["k"][:, :, :L]) <= tol
+    assert rel_err(v[sel][:, :, :L], cache["v"][:, :, :L]) <= tol
+    assert np.all(k[:, :, L:] == 0)
+    # partition p's shard of the cache: heads [p*H/t, (p+1)*H/t) of every sequence
+    for part in range(t):
+        hs = slice(part * shape.heads // t, (part + 1) * shape.heads // t)
+        assert rel_err(k[sel][:, hs, :L], cache["k"][:, hs, :L]) <= tol, part
 
 
 CASES = {
@@ -86,6 +95,33 @@ CASES = {
 def test_prefill_and_decode(name):
     shape, max_seq, steps = CASES[name]
     run_case(shape, max_seq, steps)
+
+
+# name: (shape, max_seq, decode steps, t)
+SHARDED = {
+    "bf16_d64_t2": (synthetic.tiny(h=256, heads=4, seq=128, batch=3, dtype="bf16", w_std=0.02,
+                                   out_std=0.01), 256, 3, 2),
+    "bf16_d96_t8": (synthetic.tiny(h=768, heads=8, seq=256, batch=4, dtype="bf16", w_std=0.02,
+                                   out_std=0.01), 384, 3, 8),
+    "f32_d64_t2": (synthetic.tiny(h=256, heads=4, seq=100, batch=2, dtype="f32", w_std=0.05,
+                                  out_std=0.05), 160, 2, 2),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SHARDED))
+def test_prefill_and_decode_head_sharded(name):
+    """t > 1: the prefill runs the t-partitioned forward, every partition's heads
+    fill its own shard of the cache, and decode reads the shards."""
+    shape, max_seq, steps, t = SHARDED[name]
+    run_case(shape, max_seq, steps, t=t)
+
+
+def test_decode_at_the_benchmarked_shape():
+    """bench.py --workload decode: the 8.3B-shape layer (h 3072, 32 heads, t = 8),
+    16 sequences with a 1024-token context, the same seeded inputs.  The GPU
+    prefills and decodes all 16; sequences 0, 7 and 15 are checked."""
+    shape = synthetic.CONFIGS["D"]
+    run_case(shape, shape.seq + 8, 2, seed=0, t=8, check=[0, 7, 15], affine=False)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
