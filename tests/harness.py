@@ -136,12 +136,13 @@ def rel_err_qkv(g, r, axis, heads, zero_k_sum=False):
     return worst
 
 
-def compare(gpu, ref, dtype, keys=None, heads=None):
+def compare(gpu, ref, dtype, keys=None, heads=None, per_block=True):
     """{key: rel_err} for the outputs present in both.  The fused-QKV tensors
     (s_qkv, d_w_qkv, d_b_qkv, dqkv) are judged per head and per Q/K/V block
-    (heads from the argument or from the reference's lse)."""
+    (heads from the argument or from the reference's lse) unless per_block is
+    False."""
     keys = keys or [k for k in ref if k in gpu]
-    if heads is None and "s_lse" in ref:
+    if heads is None and "s_lse" in ref and per_block:
         heads = ref["s_lse"].shape[1]
     res = {}
     for k in keys:

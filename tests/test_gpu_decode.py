@@ -101,8 +101,8 @@ def test_prefill_and_decode(name):
 SHARDED = {
     "bf16_d64_t2": (synthetic.tiny(h=256, heads=4, seq=128, batch=3, dtype="bf16", w_std=0.02,
                                    out_std=0.01), 256, 3, 2),
-    "bf16_d96_t8": (synthetic.tiny(h=768, heads=8, seq=256, batch=4, dtype="bf16", w_std=0.02,
-                                   out_std=0.01), 384, 3, 8),
+    "bf16_d96_t8": (synthetic.tiny(h=1536, heads=16, seq=256, batch=4, dtype="bf16",
+                                   w_std=0.02, out_std=0.01), 384, 3, 8),
     "f32_d64_t2": (synthetic.tiny(h=256, heads=4, seq=100, batch=2, dtype="f32", w_std=0.05,
                                   out_std=0.05), 160, 2, 2),
 }
