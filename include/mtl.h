@@ -199,13 +199,24 @@ mtl_status mtl_layer_check(void* workspace, mtl_stream stream);
  * b_k_major.  A, B, bias, R, Z are `dtype`; C is fp32 if c_f32 else `dtype`.
  * Leading dimensions are in elements (C: ldc, R: ldr, Z: ldz).  K must split
  * into k_parts equal parts; bf16 needs (K/k_parts) % 64 == 0 and lda, ldb,
- * ldc, ldr, ldz multiples of 8. */
+ * ldc, ldr, ldz multiples of 8.
+ * workspace: device, 16-byte aligned, at least 256 bytes (the status word).
+ * With mtl_gemm_ws_bytes(M, N) bytes, a bf16 GEMM whose 256 x 256 tiles leave
+ * the last wave over the SM pairs partly empty cuts each tile of that wave into
+ * equal K slices (runs of K-blocks, or of partitions) on separate pairs, whose
+ * fp32 partials are added in slice order before the epilogue -- a fixed order
+ * for a given shape and SM count, so results stay bitwise reproducible. */
 mtl_status mtl_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, int32_t k_parts,
                     const void* A, int64_t lda, int32_t a_k_major,
                     const void* B, int64_t ldb, int32_t b_k_major,
                     int32_t epi, const void* bias, const void* R, int64_t ldr,
                     void* Z, int64_t ldz, void* C, int64_t ldc, int32_t c_f32,
                     void* workspace, size_t ws_bytes, mtl_stream stream);
+
+/* Workspace bytes for mtl_gemm / mtl_gemm_fp8 with an M x N output (any K)
+ * that lets the tiles of the last, partial wave be cut into K slices (at least
+ * 256; the count depends on the current device's SM count). */
+mtl_status mtl_gemm_ws_bytes(int32_t M, int32_t N, size_t* bytes);
 
 /* Causal multi-head attention, the layer's attention step on its own (same
  * kernels, same dropout numbering with site 0):

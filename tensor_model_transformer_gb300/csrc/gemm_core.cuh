@@ -26,6 +26,11 @@ constexpr int STAGE_OUT_BYTES = 4096;                       // epilogue output s
 constexpr int OUT_STAGING_BYTES = EPI_WARPS * STAGE_OUT_BYTES;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_STAGING_BYTES + BAR_BYTES + 1024;
 constexpr int GROUP_M = 16;   // tile raster: groups of 16 M-blocks sweep all N-blocks
+constexpr int RASTER_N_MAX = 16;   // at most this many N-blocks: the raster runs N fastest
+// Split tiles (pair kernel): a region of a tile's output written by one epilogue
+// warp (32 rows x 128 columns, fp32), and the regions of a tile (2 CTAs x 8 warps).
+constexpr int SPLIT_REGION_FLOATS = 32 * 128;
+constexpr int SPLIT_REGIONS = 2 * EPI_WARPS;
 
 struct Params {
   int M, N, K, parts, kb_per_unit, units_per_tile;
@@ -46,9 +51,80 @@ struct Params {
   int fmt_a, fmt_b;
   const float* scale_a;
   const float* scale_b;
+  // Raster: raster_n = 1 runs N fastest (every N-block of an M-block together,
+  // for narrow outputs whose B operand then stays in L2), else groups of
+  // GROUP_M M-blocks sweep the N-blocks.
+  int raster_n;
+  // Work split (pair kernel).  Tiles [0, dp_tiles) of the raster, whole waves
+  // over the pairs, run whole and round-robin.  Each of the remaining tiles
+  // (the last, partial wave) is cut into split_s slices of its granules
+  // (split_g K-blocks each: a partition when the partials are summed, else one
+  // K-block; split_gpt granules a tile), slice j being granules
+  // [j * split_gpt / split_s, (j + 1) * split_gpt / split_s); pair q < tail
+  // tiles x split_s computes slice q % split_s of tail tile q / split_s.  All
+  // slices start together at their own K offset, like the whole waves before
+  // them, so pairs that share an operand block still read it at the same time.
+  // A slice's epilogue warps write their fp32 partial (a running partition
+  // sum, or the slice's K range) to slot j of split_ws and count themselves in
+  // split_cnt; the warp that arrives last adds slots 0..split_s-1 in order and
+  // runs the epilogue.
+  int dp_tiles;
+  int split_s;
+  int split_g, split_gpt;
+  float* split_ws;       // [tail tile][slot][SPLIT_REGIONS][SPLIT_REGION_FLOATS]
+  unsigned* split_cnt;   // [tail tile][SPLIT_REGIONS], zero between launches
 };
 
+// One piece of a pair's work: granules [g0, g1) of tile `tile`; split: slice
+// `slot` of tail tile `sk` (the tile's other slices run on other pairs).
+struct Piece {
+  int tile, g0, g1, sk, slot;
+  bool split;
+};
+
+struct PieceIter {
+  int next, step;
+  bool tail_done;
+};
+
+__device__ __forceinline__ void piece_begin(const Params& p, int pair_id, int npairs,
+                                            PieceIter& it) {
+  it.next = pair_id;
+  it.step = npairs;
+  it.tail_done = false;
+}
+
+__device__ __forceinline__ bool piece_next(const Params& p, PieceIter& it, Piece& pc) {
+  if (it.next < p.dp_tiles) {
+    pc.tile = it.next;
+    pc.g0 = 0;
+    pc.g1 = p.split_gpt;
+    pc.sk = -1;
+    pc.slot = 0;
+    pc.split = false;
+    it.next += it.step;
+    return true;
+  }
+  if (it.tail_done || p.split_s <= 1) return false;
+  it.tail_done = true;
+  // this pair's slice of the tail: pair index = it.next - dp_tiles (whole waves)
+  const int q = (it.next - p.dp_tiles);
+  if (q < 0 || q >= (p.num_tiles - p.dp_tiles) * p.split_s) return false;
+  pc.sk = q / p.split_s;
+  pc.slot = q - pc.sk * p.split_s;
+  pc.tile = p.dp_tiles + pc.sk;
+  pc.g0 = pc.slot * p.split_gpt / p.split_s;
+  pc.g1 = (pc.slot + 1) * p.split_gpt / p.split_s;
+  pc.split = true;
+  return true;
+}
+
 __device__ __forceinline__ void tile_coords(const Params& p, int tile, int& mb, int& nb) {
+  if (p.raster_n) {
+    mb = tile / p.tiles_n;
+    nb = tile - mb * p.tiles_n;
+    return;
+  }
   const int per_group = GROUP_M * p.tiles_n;
   const int g = tile / per_group;
   const int first_m = g * GROUP_M;
@@ -265,14 +341,15 @@ __device__ __forceinline__ void epi_chunk_tma(const Params& p, int row0, int col
 // at a time), add partition partials in order, apply the epilogue, store.
 // tfull0 / tempty0: addresses of tfull[0] and tempty[0] (tempty as a cluster
 // address when PAIR: the epilogue warps of both CTAs of a pair release the
-// accumulator to the leader CTA's barrier).  Tiles tile0, tile0 + tile_step, ...
-// are tile_rows high; this CTA's rows start at row_off inside a tile.
+// accumulator to the leader CTA's barrier).  The work is the pieces of pair (or
+// CTA) tile0 of tile_step (piece_next); tiles are tile_rows high and this
+// CTA's rows start at row_off inside a tile.
 // tmC / tmZ: tensor maps of C and z (32 x 32 boxes) for the TMA stores of
 // whole chunks; out_stage: the shared staging area (OUT_STAGING_BYTES).
 // AHEAD: R / Z of the next chunk are loaded while this one is processed (the
 // FP8 kernels, whose shorter main loop leaves the epilogue exposed; measured
 // slower for bf16).
-template <int EPI, bool OUT_F32, bool REDUCE, bool PAIR, bool AHEAD>
+template <int EPI, bool OUT_F32, bool REDUCE, bool PAIR, bool AHEAD, bool SPLIT>
 __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t tmem_base, uint32_t tfull0,
                                               uint32_t tempty0, volatile int* abort_flag,
                                               int warp, int lane, int tile0, int tile_step,
@@ -317,17 +394,42 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t tmem_bas
     }
     epi_chunk<EPI, OUT_F32>(p, row, col0, v, keep);
   };
+  // A split piece's partial: this warp's 32 rows x 128 columns in slot `slot`
+  // of split tile `sk`, as [column group of 4][row][4] (a warp's float4 stores
+  // cover 512 contiguous bytes).
+  auto split_region = [&](int sk, int slot) -> float* {
+    return p.split_ws + ((size_t)(sk * p.split_s + slot) * SPLIT_REGIONS +
+                         (size_t)row_off / 128 * EPI_WARPS + ew) *
+                            SPLIT_REGION_FLOATS;
+  };
+  auto split_store4 = [&](float* reg, int q, float a, float b, float c, float d) {
+    reinterpret_cast<float4*>(reg)[q * 32 + lane] = make_float4(a, b, c, d);
+  };
   int unit = 0;
   bool ok = true;
-  for (int tile = tile0; tile < p.num_tiles && ok; tile += tile_step) {
+  PieceIter pit;
+  piece_begin(p, tile0, tile_step, pit);
+  Piece pc;
+  while (ok && piece_next(p, pit, pc)) {
     int mb, nb;
-    tile_coords(p, tile, mb, nb);
+    tile_coords(p, pc.tile, mb, nb);
     const int row = mb * tile_rows + row_off + quarter * 32 + lane;
     const int colbase = nb * BN + chalf * 128;
+    const bool split = SPLIT && pc.split;
+    float* sreg = split ? split_region(pc.sk, pc.slot) : nullptr;
     uint4 side[4];
-    if (!REDUCE && AHEAD) side_load(row, colbase, side);
+    if (!REDUCE && AHEAD && !split) side_load(row, colbase, side);
+    // the running partition sum starts at +0 in every piece, so no value of it
+    // lives from one piece into the next (x + 0 = x: the same sums)
     float sum[REDUCE ? 128 : 1];
-    for (int u = 0; u < p.units_per_tile; ++u, ++unit) {
+    if constexpr (REDUCE) {
+#pragma unroll
+      for (int i = 0; i < 128; ++i) sum[i] = 0.f;
+    }
+    // (a run-time unit count in both cases: units_per_tile is 1 without partial
+    // sums; the loop keeps the same shape either way)
+    const int nunits = REDUCE ? pc.g1 - pc.g0 : p.units_per_tile;
+    for (int u = 0; u < nunits; ++u, ++unit) {
       const int buf = unit & 1;
       const uint32_t uphase = (unit >> 1) & 1;
       if (!mbar_wait_bounded(tfull_bar(buf), uphase, p.status, abort_flag)) {
@@ -336,19 +438,33 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t tmem_bas
       }
       tc_fence_after();
       const uint32_t tb = tmem_base + buf * BN + chalf * 128 + ((uint32_t)(quarter * 32) << 16);
+      if constexpr (REDUCE) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint32_t keep = REDUCE ? 0u : chunk_keep<EPI>(p, row, colbase + c * 32);
-        uint32_t r[32];
-        tmem_ld32(tb + c * 32, r);
-        tmem_ld_wait();
-        if constexpr (REDUCE) {
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tb + c * 32, r);
+          tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float x = __uint_as_float(r[i]);
-            sum[c * 32 + i] = (u == 0) ? x : sum[c * 32 + i] + x;
-          }
-        } else {
+          for (int i = 0; i < 32; ++i) sum[c * 32 + i] += __uint_as_float(r[i]);
+        }
+      } else if (split) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tb + c * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            split_store4(sreg, c * 8 + q, __uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                         __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t keep = chunk_keep<EPI>(p, row, colbase + c * 32);
+          uint32_t r[32];
+          tmem_ld32(tb + c * 32, r);
+          tmem_ld_wait();
           uint4 next[4];
           if (AHEAD && c < 3) side_load(row, colbase + (c + 1) * 32, next);
           if (!AHEAD) side_load(row, colbase + c * 32, side);
@@ -371,8 +487,13 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t tmem_bas
           mbar_arrive(tempty_bar(buf));
       }
     }
+    if (!ok) break;
     if constexpr (REDUCE) {
-      if (ok) {
+      if (split) {
+#pragma unroll
+        for (int q = 0; q < 32; ++q)
+          split_store4(sreg, q, sum[4 * q], sum[4 * q + 1], sum[4 * q + 2], sum[4 * q + 3]);
+      } else {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const uint32_t keep = chunk_keep<EPI>(p, row, colbase + c * 32);
@@ -382,6 +503,64 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t tmem_bas
           for (int i = 0; i < 32; ++i) v[i] = sum[c * 32 + i] * ds;
           chunk(row, colbase + c * 32, v, keep, side);
         }
+      }
+    }
+    if (SPLIT && split) {
+      // publish this slice's partial; the warp of the tile's last slice to
+      // arrive adds the slices in slice order and runs the epilogue
+      __threadfence();
+      __syncwarp();
+      unsigned* cnt = p.split_cnt + (size_t)pc.sk * SPLIT_REGIONS + row_off / 128 * EPI_WARPS + ew;
+      unsigned old = 0;
+      if (lane == 0) old = atomicAdd(cnt, 1u);
+      old = __shfl_sync(0xffffffffu, old, 0);
+      if (old == (unsigned)(p.split_s - 1)) {
+        __threadfence();
+        // this lane's row of the tile region, chunk by chunk, summed over the
+        // slices in slot order (slot j is SPLIT_REGIONS regions after slot
+        // j - 1), two slots' loads in flight at a time; one copy of the chunk
+        // epilogue (a rarely taken path: kept small, not unrolled)
+        constexpr int SLOT4 = SPLIT_REGIONS * SPLIT_REGION_FLOATS / 4;
+        const float4* s0 = reinterpret_cast<const float4*>(split_region(pc.sk, 0)) + lane;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t keep = chunk_keep<EPI>(p, row, colbase + c * 32);
+          side_load(row, colbase + c * 32, side);
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          const float4* sc = s0 + c * 8 * 32;
+#pragma unroll 1
+          for (int jj = 0; jj < p.split_s; jj += 2) {
+            const bool two = jj + 1 < p.split_s;
+            float4 a[8], b[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              a[q] = __ldcg(sc + jj * SLOT4 + q * 32);
+              b[q] = two ? __ldcg(sc + (jj + 1) * SLOT4 + q * 32) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              v[4 * q] += a[q].x;
+              v[4 * q + 1] += a[q].y;
+              v[4 * q + 2] += a[q].z;
+              v[4 * q + 3] += a[q].w;
+            }
+            if (two) {
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                v[4 * q] += b[q].x;
+                v[4 * q + 1] += b[q].y;
+                v[4 * q + 2] += b[q].z;
+                v[4 * q + 3] += b[q].w;
+              }
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= ds;
+          chunk(row, colbase + c * 32, v, keep, side);
+        }
+        if (lane == 0) *cnt = 0u;   // ready for the next launch
       }
     }
   }
@@ -409,7 +588,7 @@ constexpr int P_BK = 128, P_HALF = 128;              // K elements per stage, ro
 constexpr int P_ATOM = P_HALF * 128;                 // one [128 rows][128 bytes] box
 constexpr int P_SMEM_BYTES = 3 * 2 * 2 * P_ATOM + OUT_STAGING_BYTES + BAR_BYTES + 1024;   // 192 KB of stages
 
-template <int EPI, bool OUT_F32, bool REDUCE, bool F8>
+template <int EPI, bool OUT_F32, bool REDUCE, bool F8, bool SPLIT = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
@@ -473,7 +652,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   }
 
   if (warp >= 4) {
-    epilogue_role<EPI, OUT_F32, REDUCE, true, F8>(p, tmem_base, tfull_bar(0),
+    epilogue_role<EPI, OUT_F32, REDUCE, true, F8, SPLIT>(p, tmem_base, tfull_bar(0),
                                               cluster_map(tempty_bar(0), 0), abort_flag, warp,
                                               lane, pair_id, npairs, 2 * P_HALF, P_HALF * rank,
                                               &tmC, &tmZ, out_stage);
@@ -482,13 +661,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      const int kb_per_tile = p.kb_per_unit * p.units_per_tile;
       bool ok = true;
-      for (int tile = pair_id; tile < p.num_tiles && ok; tile += npairs) {
+      PieceIter pit;
+      piece_begin(p, pair_id, npairs, pit);
+      Piece pc;
+      while (ok && piece_next(p, pit, pc)) {
         int mb, nb;
-        tile_coords(p, tile, mb, nb);
+        tile_coords(p, pc.tile, mb, nb);
         const int m0 = mb * 2 * P_HALF + P_HALF * rank, n0 = nb * 2 * P_HALF + P_HALF * rank;
-        for (int kb = 0; kb < kb_per_tile; ++kb) {
+        for (int kb = pc.g0 * p.split_g; kb < pc.g1 * p.split_g; ++kb) {
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, p.status, abort_flag)) {
             ok = false;
             break;
@@ -528,8 +709,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       uint32_t phase = 0;
       int unit = 0;
       bool ok = true;
-      for (int tile = pair_id; tile < p.num_tiles && ok; tile += npairs) {
-        for (int u = 0; u < p.units_per_tile && ok; ++u, ++unit) {
+      PieceIter pit;
+      piece_begin(p, pair_id, npairs, pit);
+      Piece pc;
+      while (ok && piece_next(p, pit, pc)) {
+        // a unit is one partition (partials summed) or the piece's whole K range
+        const int nunits = REDUCE ? pc.g1 - pc.g0 : 1;
+        const int kb_unit = REDUCE ? p.kb_per_unit : (pc.g1 - pc.g0) * p.split_g;
+        for (int u = 0; u < nunits && ok; ++u, ++unit) {
           const int buf = unit & 1;
           const uint32_t uphase = (unit >> 1) & 1;
           if (!mbar_wait_bounded_cluster(tempty_bar(buf), uphase ^ 1u, p.status, abort_flag)) {
@@ -538,7 +725,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + buf * BN;
-          for (int kb = 0; kb < p.kb_per_unit; ++kb) {
+          for (int kb = 0; kb < kb_unit; ++kb) {
             if (!mbar_wait_bounded(full_bar(stage), phase, p.status, abort_flag)) {
               ok = false;
               break;
@@ -584,6 +771,63 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 }
 
 // ---------------------------------------------------------------- host side
+
+typedef void (*KernelFn)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, Params);
+
+// The pair kernels with the tail-slice epilogue (gemm_split.cu): bf16 and FP8.
+KernelFn select_kernel2_split(int epi, bool f32, bool red);
+KernelFn select_kernel8_split(int epi, bool f32, bool red);
+
+// Slices per tile of the last, partial wave of num_tiles tiles over npairs
+// pairs (1: no split): as many as give every tail slice its own pair, at most
+// one per granule and at most MAX_SLICES, for tiles of at least
+// SPLIT_MIN_KBLOCKS 128-deep K-blocks (a shorter tile's saved time, ~0.5 us a
+// K-block, does not pay for the slices' write-out and the ordered re-read).
+constexpr int MAX_SLICES = 16;
+constexpr int SPLIT_MIN_KBLOCKS = 48;
+inline int tail_slices(int num_tiles, int npairs, int gpt, int kb_per_tile) {
+  if (npairs < 2 || num_tiles < npairs || kb_per_tile < SPLIT_MIN_KBLOCKS) return 1;
+  const int rem = num_tiles % npairs;
+  if (rem == 0) return 1;
+  int s = npairs / rem;
+  if (s > gpt) s = gpt;
+  if (s > MAX_SLICES) s = MAX_SLICES;
+  return s < 2 ? 1 : s;
+}
+
+// Scratch bound for M x N outputs over npairs pairs (any K): slots for the
+// tail tiles' slices, and counters.
+inline void split_scratch_for(int num_tiles, int npairs, size_t* bytes, size_t* counters) {
+  const int s = tail_slices(num_tiles, npairs, MAX_SLICES, SPLIT_MIN_KBLOCKS);
+  const int rem = s > 1 ? num_tiles % npairs : 0;
+  *bytes = (size_t)rem * s * SPLIT_REGIONS * SPLIT_REGION_FLOATS * sizeof(float);
+  *counters = (size_t)rem * SPLIT_REGIONS;
+}
+
+// Fills the work-split fields of p (granules, raster, tail slices) for a
+// launch over npairs pairs; the tail is split only with enough scratch in a
+// (else every tile runs whole).
+inline void plan_split(Params& p, bool reduce, int npairs, bool pair_kernel, const GemmArgs& a) {
+  p.raster_n = p.tiles_n <= RASTER_N_MAX;
+  p.split_g = reduce ? p.kb_per_unit : 1;
+  p.split_gpt = reduce ? p.units_per_tile : p.kb_per_unit;
+  p.dp_tiles = p.num_tiles;
+  p.split_s = 1;
+  p.split_ws = nullptr;
+  p.split_cnt = nullptr;
+  if (!pair_kernel) return;
+  const int s = tail_slices(p.num_tiles, npairs, p.split_gpt, p.split_gpt * p.split_g);
+  if (s <= 1) return;
+  const int rem = p.num_tiles % npairs;
+  const size_t bytes = (size_t)rem * s * SPLIT_REGIONS * SPLIT_REGION_FLOATS * sizeof(float);
+  if (!a.split_ws || !a.split_cnt || a.split_ws_bytes < bytes ||
+      a.split_cnt_count < (size_t)rem * SPLIT_REGIONS)
+    return;
+  p.dp_tiles = p.num_tiles - rem;
+  p.split_s = s;
+  p.split_ws = a.split_ws;
+  p.split_cnt = a.split_cnt;
+}
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,

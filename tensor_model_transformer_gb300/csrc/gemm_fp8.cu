@@ -205,8 +205,6 @@ __global__ void __launch_bounds__(QTHREADS) cast_transpose_kernel(
 
 namespace tcg {
 
-typedef void (*KernelFn)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, Params);
-
 template <int EPI, bool F32, bool RED>
 static KernelFn kernel8_ptr() {
   return reinterpret_cast<KernelFn>(gemm_tc2_kernel<EPI, F32, RED, true>);
@@ -281,7 +279,9 @@ cudaError_t gemm_fp8(const GemmArgs& a, const LaunchCtx& c) {
   p.fmt_b = a.fmt_b;
   p.scale_a = a.scale_a;
   p.scale_b = a.scale_b;
-  KernelFn fn = select_kernel8(a.epi, a.c_f32, reduce);
+  plan_split(p, reduce, c.num_sms / 2, true, a);
+  KernelFn fn = p.split_s > 1 ? select_kernel8_split(a.epi, a.c_f32, reduce)
+                              : select_kernel8(a.epi, a.c_f32, reduce);
   if (!fn) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);

@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   if (warp >= 4) {
-    epilogue_role<EPI, OUT_F32, REDUCE, false, false>(p, tmem_base, tfull_bar(0), tempty_bar(0),
+    epilogue_role<EPI, OUT_F32, REDUCE, false, false, false>(p, tmem_base, tfull_bar(0), tempty_bar(0),
                                                abort_flag, warp, lane, blockIdx.x, gridDim.x, BM,
                                                0, &tmC, &tmZ, out_stage);
   } else if (warp == 0) {
@@ -209,8 +209,6 @@ bool make_operand_map(CUtensorMap* m, const GemmOperand& op, int mn, int K, int 
   return make_map(m, op.ptr, (uint64_t)mn, (uint64_t)K, op.ld, 64, BK);
 }
 
-typedef void (*KernelFn)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, Params);
-
 template <int EPI, bool F32, bool RED>
 KernelFn kernel_ptr() {
   return reinterpret_cast<KernelFn>(gemm_tc_kernel<EPI, F32, RED>);
@@ -252,6 +250,22 @@ KernelFn select_kernel(int epi, bool f32, bool red) {
 }
 
 }  // namespace tcg
+
+size_t gemm_split_bytes(int M, int N, int num_sms) {
+  using namespace tcg;
+  const int tiles = ((M + 2 * P_HALF - 1) / (2 * P_HALF)) * ((N + BN - 1) / BN);
+  size_t bytes, counters;
+  split_scratch_for(tiles, num_sms / 2, &bytes, &counters);
+  return bytes;
+}
+
+size_t gemm_split_counters(int M, int N, int num_sms) {
+  using namespace tcg;
+  const int tiles = ((M + 2 * P_HALF - 1) / (2 * P_HALF)) * ((N + BN - 1) / BN);
+  size_t bytes, counters;
+  split_scratch_for(tiles, num_sms / 2, &bytes, &counters);
+  return counters;
+}
 
 bool gemm_tc_supported(const GemmArgs& a) {
   if (a.parts < 1 || a.K % a.parts) return false;
@@ -314,8 +328,10 @@ cudaError_t gemm_tc(const GemmArgs& a, const LaunchCtx& c) {
   p.ldc = a.ldc;
   p.status = a.status;
   p.drop = a.drop;
-  KernelFn fn = use_pair ? select_kernel2(a.epi, a.c_f32, reduce)
-                         : select_kernel(a.epi, a.c_f32, reduce);
+  plan_split(p, reduce, use_pair ? c.num_sms / 2 : c.num_sms, use_pair, a);
+  KernelFn fn = !use_pair          ? select_kernel(a.epi, a.c_f32, reduce)
+                : p.split_s > 1    ? select_kernel2_split(a.epi, a.c_f32, reduce)
+                                   : select_kernel2(a.epi, a.c_f32, reduce);
   if (!fn) return cudaErrorInvalidValue;
   const int smem_bytes = use_pair ? P_SMEM_BYTES : SMEM_BYTES;
   cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),

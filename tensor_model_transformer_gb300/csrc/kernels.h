@@ -55,7 +55,21 @@ struct GemmArgs {
   int fmt_a, fmt_b;
   const float* scale_a;
   const float* scale_b;
+  // Scratch of the tensor-core pair GEMM for the K slices of its last,
+  // partial wave of tiles (gemm_split_bytes / gemm_split_counters for the
+  // sizes; the counters must be zero before the launch and are left zero).
+  // Null: every tile runs whole.
+  float* split_ws;
+  size_t split_ws_bytes;
+  unsigned* split_cnt;
+  size_t split_cnt_count;
 };
+
+// Scratch the pair GEMM uses for sliced tail tiles with M x N outputs on
+// num_sms SMs, for any K: partial-tile bytes and arrival counters (0 when the
+// waves are whole).
+size_t gemm_split_bytes(int M, int N, int num_sms);
+size_t gemm_split_counters(int M, int N, int num_sms);
 
 // Kernel kinds reported through the profiling hooks.
 enum KernelKind {

@@ -244,9 +244,50 @@ Fp8Ws fp8_ws_layout(const Dims& D) {
   return F;
 }
 
-// Backward scratch, after the status word.
+// Scratch of the pair GEMM's sliced tail tiles for the GEMMs of the current layer
+// call on this thread (set by the layer entry points for their duration).
+struct SplitScratch {
+  float* ws;
+  size_t bytes;
+  unsigned* cnt;
+  size_t count;
+};
+thread_local SplitScratch g_split = {nullptr, 0, nullptr, 0};
+
+struct SplitScope {
+  explicit SplitScope(const SplitScratch& s) { g_split = s; }
+  ~SplitScope() { g_split = {nullptr, 0, nullptr, 0}; }
+};
+
+// SM count the tail-slice scratch of the layer's GEMMs is sized for: the
+// device's, or a GB300's (152) where no device answers (sizes asked for on a
+// host without a GPU).
+int split_sms() {
+  const int n = device_sm_count();
+  return n > 0 ? n : 152;
+}
+
+// Tail-slice scratch (bytes, counters) that covers every bf16 GEMM of the layer.
+void layer_split_sizes(const Dims& D, size_t* bytes, size_t* counters) {
+  *bytes = 0;
+  *counters = 0;
+  if (D.dtype != MTL_BF16) return;
+  const int n = (int)D.n, h = (int)D.h, f = (int)D.f, nsm = split_sms();
+  const int shapes[7][2] = {{n, 3 * h}, {n, h}, {n, f}, {h, f}, {f, h}, {h, h}, {3 * h, h}};
+  for (const auto& mn : shapes) {
+    const size_t b = gemm_split_bytes(mn[0], mn[1], nsm);
+    const size_t c = gemm_split_counters(mn[0], mn[1], nsm);
+    if (b > *bytes) *bytes = b;
+    if (c > *counters) *counters = c;
+  }
+}
+
+// Backward scratch, after the status word.  The GEMMs' tail-slice counters
+// come first, so that one memset clears them with the status word.
 struct WsLayout {
-  size_t dz, du, dx1, dctx, dqkv, dsum, gmask, partial, fp8, rc_h, rc_f, zero_h, total;
+  size_t split_cnt, dz, du, dx1, dctx, dqkv, dsum, gmask, partial, fp8, rc_h, rc_f, zero_h,
+      split_ws, total;
+  size_t split_bytes, split_count;
 };
 
 WsLayout ws_layout(const Dims& D) {
@@ -257,6 +298,8 @@ WsLayout ws_layout(const Dims& D) {
     off += align_up(bytes);
     return at;
   };
+  layer_split_sizes(D, &W.split_bytes, &W.split_count);
+  W.split_cnt = take(W.split_count * 4);
   const size_t nh = (size_t)D.n * D.h;
   W.dz = take((size_t)D.n * D.f * D.esz);
   W.du = take(nh * 4);
@@ -281,14 +324,37 @@ WsLayout ws_layout(const Dims& D) {
   W.rc_h = take(rcw ? nh * D.esz : 0);
   W.rc_f = take(rcw ? (size_t)D.n * D.f * D.esz : 0);
   W.zero_h = take(D.post_ln ? (size_t)D.h * D.esz : 0);   // a zero bias (Post-LN dx GEMM)
+  W.split_ws = take(W.split_bytes);
   W.total = off;
   return W;
 }
+
 
 template <typename T>
 T* at(void* base, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(base) + off);
 }
+
+SplitScratch layer_split(void* workspace, const WsLayout& W) {
+  return {W.split_bytes ? at<float>(workspace, W.split_ws) : nullptr, W.split_bytes,
+          W.split_count ? at<unsigned>(workspace, W.split_cnt) : nullptr, W.split_count};
+}
+
+// Workspace of a standalone GEMM: the status block, the tail-slice counters,
+// the tail-slice partials.  Returns the bytes to clear at the start of a call.
+size_t standalone_gemm_split(GemmArgs& g, void* workspace, size_t ws_bytes) {
+  const int nsm = split_sms();
+  const size_t cnt = gemm_split_counters(g.M, g.N, nsm);
+  const size_t bytes = gemm_split_bytes(g.M, g.N, nsm);
+  const size_t off_ws = kStatusBytes + align_up(cnt * 4);
+  if (cnt == 0 || ws_bytes < off_ws + bytes) return kStatusBytes;
+  g.split_cnt = at<unsigned>(workspace, kStatusBytes);
+  g.split_cnt_count = cnt;
+  g.split_ws = at<float>(workspace, off_ws);
+  g.split_ws_bytes = bytes;
+  return off_ws;
+}
+
 template <typename T>
 const T* at(const void* base, size_t off) {
   return reinterpret_cast<const T*>(static_cast<const char*>(base) + off);
@@ -324,6 +390,10 @@ GemmArgs gemm_args(int M, int N, int K, int parts, const void* A, int64_t lda, b
                    unsigned* status) {
   GemmArgs g;
   memset(&g, 0, sizeof(g));
+  g.split_ws = g_split.ws;
+  g.split_ws_bytes = g_split.bytes;
+  g.split_cnt = g_split.cnt;
+  g.split_cnt_count = g_split.count;
   g.M = M;
   g.N = N;
   g.K = K;
@@ -658,8 +728,10 @@ mtl_status mtl_layer_fwd(const mtl_layer_desc* desc, const mtl_weights* w, const
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   LaunchCtx c{s, nsm, &g_launches, &g_prof};
   unsigned* status = static_cast<unsigned*>(workspace);
-  MTL_TRY(cudaMemsetAsync(status, 0, kStatusBytes, s), "status reset");
+  // the status word and the GEMMs' tail-slice counters
+  MTL_TRY(cudaMemsetAsync(status, 0, W.dz, s), "status reset");
   if (D.n == 0) return MTL_OK;
+  const SplitScope split(layer_split(workspace, W));
 
   return forward_core(D, desc->ln_eps, w, x, y, saved, at<char>(workspace, W.fp8),
                       at<char>(workspace, W.rc_h), at<char>(workspace, W.rc_f), status, c);
@@ -683,7 +755,9 @@ mtl_status mtl_layer_bwd(const mtl_layer_desc* desc, const mtl_weights* w, const
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   LaunchCtx c{s, nsm, &g_launches, &g_prof};
   unsigned* status = static_cast<unsigned*>(workspace);
-  MTL_TRY(cudaMemsetAsync(status, 0, kStatusBytes, s), "status reset");
+  // the status word and the GEMMs' tail-slice counters
+  MTL_TRY(cudaMemsetAsync(status, 0, W.dz, s), "status reset");
+  const SplitScope split(layer_split(workspace, W));
 
   const mtl_saved_layout L = saved_layout(D);
   const int n = (int)D.n, h = (int)D.h, f = (int)D.f, t = (int)D.t;
@@ -1323,6 +1397,15 @@ mtl_status mtl_fp8_quantize(int32_t src_dtype, const void* x, int64_t rows, int6
   return MTL_OK;
 }
 
+mtl_status mtl_gemm_ws_bytes(int32_t M, int32_t N, size_t* bytes) {
+  if (M < 0 || N < 0 || !bytes) return MTL_ERR_INVALID_ARG;
+  const int nsm = split_sms();
+  const size_t split = gemm_split_bytes(M, N, nsm);
+  *bytes = split ? kStatusBytes + align_up(gemm_split_counters(M, N, nsm) * 4) + split
+                 : kStatusBytes;
+  return MTL_OK;
+}
+
 mtl_status mtl_gemm_fp8(int32_t M, int32_t N, int32_t K, int32_t k_parts, const void* A,
                         int64_t lda, int32_t fmt_a, const float* scale_a, const void* B,
                         int64_t ldb, int32_t fmt_b, const float* scale_b, int32_t epi,
@@ -1357,8 +1440,9 @@ mtl_status mtl_gemm_fp8(int32_t M, int32_t N, int32_t K, int32_t k_parts, const 
   const int nsm = device_sm_count();
   if (nsm <= 0) return cuda_fail(cudaGetLastError(), "device query");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t clear = standalone_gemm_split(g, workspace, ws_bytes);
   LaunchCtx c{s, nsm, &g_launches, &g_prof};
-  MTL_TRY(cudaMemsetAsync(status, 0, kStatusBytes, s), "status reset");
+  MTL_TRY(cudaMemsetAsync(status, 0, clear, s), "status reset");
   if (M == 0 || N == 0) return MTL_OK;
   MTL_TRY(gemm_fp8(g, c), "gemm fp8");
   return MTL_OK;
@@ -1401,8 +1485,10 @@ mtl_status mtl_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, int32_t k_pa
   const int nsm = device_sm_count();
   if (nsm <= 0) return cuda_fail(cudaGetLastError(), "device query");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t clear = dtype == MTL_BF16 ? standalone_gemm_split(g, workspace, ws_bytes)
+                                           : kStatusBytes;
   LaunchCtx c{s, nsm, &g_launches, &g_prof};
-  MTL_TRY(cudaMemsetAsync(status, 0, kStatusBytes, s), "status reset");
+  MTL_TRY(cudaMemsetAsync(status, 0, clear, s), "status reset");
   if (M == 0 || N == 0) return MTL_OK;
   if (dtype == MTL_BF16) {
     MTL_TRY(gemm_tc(g, c), "gemm");

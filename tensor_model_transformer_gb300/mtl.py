@@ -73,6 +73,7 @@ def lib():
         L.mtl_gemm.argtypes = [i32, i32, i32, i32, i32, vp, i64, i32, vp, i64, i32, i32, vp, vp,
                                i64, vp, i64, vp, i64, i32, vp, sz, vp]
         L.mtl_attention_ws_bytes.argtypes = [i32, i32, i32, ctypes.POINTER(sz)]
+        L.mtl_gemm_ws_bytes.argtypes = [i32, i32, ctypes.POINTER(sz)]
         L.mtl_attention_mask_bytes.argtypes = [i32, i32, i32, i32, ctypes.c_float,
                                                ctypes.POINTER(sz)]
         L.mtl_attention_fwd.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, ctypes.c_float,
@@ -102,7 +103,8 @@ def lib():
         for fn in ("mtl_layer_sizes", "mtl_layer_saved_layout", "mtl_layer_fwd", "mtl_layer_bwd",
                    "mtl_layer_check", "mtl_gemm", "mtl_attention_ws_bytes", "mtl_attention_fwd",
                    "mtl_attention_bwd", "mtl_attention_mask_bytes", "mtl_infer_sizes",
-                   "mtl_layer_prefill", "mtl_layer_decode", "mtl_fp8_quantize", "mtl_gemm_fp8"):
+                   "mtl_layer_prefill", "mtl_layer_decode", "mtl_fp8_quantize", "mtl_gemm_fp8",
+                   "mtl_gemm_ws_bytes"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -193,6 +195,13 @@ def gemm(dtype, M, N, K, parts, A, lda, a_k_major, B, ldb, b_k_major, epi, C, ld
                           ldc, int(c_f32), _ptr(workspace),
                           workspace.numel() * workspace.element_size(), _stream(stream)),
            "mtl_gemm")
+
+
+def gemm_ws_bytes(M, N) -> int:
+    """mtl_gemm_ws_bytes: workspace that lets mtl_gemm slice the tiles of its last, partial wave."""
+    out = ctypes.c_size_t(0)
+    _check(lib().mtl_gemm_ws_bytes(M, N, ctypes.byref(out)), "mtl_gemm_ws_bytes")
+    return out.value
 
 
 def attention_ws_bytes(batch, seq, heads) -> int:

@@ -23,7 +23,9 @@ def _host(t):
     return t.float().cpu().numpy().astype(np.float64)
 
 
-def run_case(dtype, M, N, K, parts, a_k, b_k, epi, c_f32, seed=0):
+def run_case(dtype, M, N, K, parts, a_k, b_k, epi, c_f32, seed=0, split=False, raw=False):
+    """split: a workspace that lets the tiles of the last, partial wave be sliced;
+    raw: also return the device output tensor."""
     import torch
     from tensor_model_transformer_gb300 import mtl
     rng = np.random.default_rng(seed)
@@ -39,11 +41,14 @@ def run_case(dtype, M, N, K, parts, a_k, b_k, epi, c_f32, seed=0):
     ldb = K if b_k else N
     Cd = torch.zeros((M, N), dtype=torch.float32 if c_f32 else Ad.dtype, device="cuda")
     Zd = _dev(Zin, dtype) if epi == EPI_DGELU else torch.zeros((M, N), dtype=Ad.dtype, device="cuda")
-    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    nws = mtl.gemm_ws_bytes(M, N) if split else 256
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
     mtl.gemm(dtype, M, N, K, parts, Ad, lda, a_k, Bd, ldb, b_k, epi, Cd, N, c_f32, ws,
              bias=_dev(bias, dtype), R=_dev(R, dtype), ldr=N, Z=Zd, ldz=N)
     mtl.layer_check(ws)
     torch.cuda.synchronize()
+    if raw:
+        return Cd.clone(), Zd.clone()
     if epi == EPI_BIAS_GELU:
         ref, zref = oracle.gemm_partitioned(A, B, parts, epi, bias=bias)
         return _host(Cd), ref, _host(Zd), zref
@@ -152,3 +157,46 @@ def test_gelu_epilogue_accuracy(epi):
     assert float(err.max()) <= 6e-7, (float(err.max()), float(zz[np.argmax(err.max(axis=0))]))
     if epi == EPI_BIAS_GELU:                  # the saved pre-activation is z itself
         assert np.array_equal(_host(Zd)[0], zz)
+
+
+# Tail slices: 90 or 160 output tiles of 256 x 256 leave a partial last wave
+# over the SM pairs, so each of its tiles is cut into equal K slices (runs of
+# K-blocks, or of partitions) computed on separate pairs, whose fp32 partials
+# are added in slice order before the epilogue.  Ragged M and N.
+SPLIT_SHAPES = [
+    # M, N, K, parts (tiles of at least 48 K-blocks of 128 are sliced)
+    (2550, 2296, 6144, 1),    # 14 tail tiles, 5 slices of 9-10 K-blocks
+    (2550, 2304, 6144, 8),    # partition sums: 5 slices of 1-2 partitions
+    (4096, 2560, 6144, 2),    # 160 tiles: two whole waves, then 2 slices
+    (4096, 2560, 8192, 1),    # 8 tail tiles, 9 slices of 7-8 K-blocks
+]
+
+
+@pytest.mark.parametrize("M,N,K,parts", SPLIT_SHAPES)
+@pytest.mark.parametrize("epi,c_f32", [(EPI_STORE, True), (EPI_BIAS, False),
+                                       (EPI_BIAS_RESID, False), (EPI_BIAS_GELU, False),
+                                       (EPI_DGELU, False), (EPI_BIAS_RESID, True)])
+def test_tail_slices(M, N, K, parts, epi, c_f32):
+    import torch
+    from tensor_model_transformer_gb300 import mtl
+    assert mtl.gemm_ws_bytes(M, N) > 256            # this shape slices its tail tiles
+    c, ref, z, zref = run_case("bf16", M, N, K, parts, 1, 1, epi, c_f32, seed=3, split=True)
+    # fp32 outputs: the fp32 accumulation error grows with K (the other tests'
+    # 2e-6 holds up to K = 1024; these shapes go to 8192)
+    t32 = 2e-6 * max(1.0, K / 1024)
+    assert rel(c, ref) < (t32 if c_f32 else tol("bf16", False)), rel(c, ref)
+    if epi == EPI_BIAS_GELU:
+        assert rel(z, zref) < tol("bf16", False)
+    # bitwise reproducible; equal to the unsliced launch up to fp32 rounding
+    c1, _ = run_case("bf16", M, N, K, parts, 1, 1, epi, c_f32, seed=3, split=True, raw=True)
+    c2, _ = run_case("bf16", M, N, K, parts, 1, 1, epi, c_f32, seed=3, split=True, raw=True)
+    assert torch.equal(c1, c2)
+    c0, _ = run_case("bf16", M, N, K, parts, 1, 1, epi, c_f32, seed=3, split=False, raw=True)
+    d = (c1.float() - c0.float()).abs().max().item() / max(c0.float().abs().max().item(), 1e-30)
+    assert d < (t32 if c_f32 else 8e-3), d
+
+
+def test_tail_slices_mn_major():
+    """Both operands MN-major (the weight-gradient form), sliced tail tiles."""
+    c, ref, _, _ = run_case("bf16", 2304, 2560, 6144, 1, 0, 0, EPI_STORE, True, seed=5, split=True)
+    assert rel(c, ref) < 2e-6 * 6144 / 1024
