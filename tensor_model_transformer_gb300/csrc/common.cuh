@@ -564,6 +564,18 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
                : "memory");
   return v;
 }
+// One fp32 / one bf16 (as fp32) from a shared-memory address.
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float ld_shared_bf16(uint32_t addr) {
+  unsigned short b;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(b) : "r"(addr));
+  return __uint_as_float((uint32_t)b << 16);
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),

@@ -68,6 +68,10 @@ struct Params {
   // sum, or the slice's K range) to slot j of split_ws and count themselves in
   // split_cnt; the warp that arrives last adds slots 0..split_s-1 in order and
   // runs the epilogue.
+  // EPI_DGELU: per-warp column sums of the stored output (32 rows each) go to
+  // csum[row / 32][col] (fp32; the bias gradient's partial sums), or nowhere
+  // when null.  Whole 32-column chunks only (N % 32 == 0).
+  float* csum;
   int dp_tiles;
   int split_s;
   int split_g, split_gpt;
@@ -334,6 +338,23 @@ __device__ __forceinline__ void epi_chunk_tma(const Params& p, int row0, int col
     tma_store_2d(tmC, stage, col0, row0);
     if (EPI == EPI_BIAS_GELU) tma_store_2d(tmZ, stage + 2048, col0, row0);
     bulk_commit();
+  }
+  if (EPI == EPI_DGELU && p.csum) {
+    // column sums of the chunk as stored: lane l adds column l over the 32
+    // rows of the staging buffer (rows past M hold zeros: their A rows read
+    // as zero), in row order
+    float cs = 0.f;
+    if (OUT_F32) {
+#pragma unroll
+      for (int r = 0; r < 32; ++r)
+        cs += ld_shared_f32(stage + r * 128 + ((((lane >> 2) ^ (r & 7))) << 4) + (lane & 3) * 4);
+    } else {
+#pragma unroll
+      for (int r = 0; r < 32; ++r)
+        cs += ld_shared_bf16(stage + r * 64 + ((((lane >> 3) ^ ((r >> 1) & 3))) << 4) +
+                             (lane & 7) * 2);
+    }
+    p.csum[(size_t)(row0 >> 5) * p.N + col0 + lane] = cs;
   }
 }
 
@@ -808,6 +829,7 @@ inline void split_scratch_for(int num_tiles, int npairs, size_t* bytes, size_t* 
 // launch over npairs pairs; the tail is split only with enough scratch in a
 // (else every tile runs whole).
 inline void plan_split(Params& p, bool reduce, int npairs, bool pair_kernel, const GemmArgs& a) {
+  p.csum = a.epi == EPI_DGELU && a.N % 32 == 0 ? a.colsum_part : nullptr;
   p.raster_n = p.tiles_n <= RASTER_N_MAX;
   p.split_g = reduce ? p.kb_per_unit : 1;
   p.split_gpt = reduce ? p.units_per_tile : p.kb_per_unit;

@@ -63,6 +63,10 @@ struct GemmArgs {
   size_t split_ws_bytes;
   unsigned* split_cnt;
   size_t split_cnt_count;
+  // EPI_DGELU on the tensor-core path with N % 32 == 0: the column sums of each
+  // 32 rows of C as stored go to colsum_part [ceil(M / 32)][N] (fp32), ready
+  // for a finalize into the bias gradient.  Null: not computed.
+  float* colsum_part;
 };
 
 // Scratch the pair GEMM uses for sliced tail tiles with M x N outputs on
@@ -198,21 +202,41 @@ bool gemm_tc_supported(const GemmArgs& a);
 cudaError_t ln_fwd(int dtype, const void* x, const void* gamma, const void* beta, void* u,
                    float* mean, float* rstd, int n, int h, float eps, const LaunchCtx& c,
                    unsigned* amax_bits = nullptr);
+// Column-sum finalizes collected for one launch (finalize_jobs): job k adds
+// nblk[k] rows of partial sums part[k] [nblk][N] in row order into out[k] [N],
+// the same fixed order a finalize of its own uses.
+struct FinalizeJobs {
+  static constexpr int kMax = 12;
+  int n = 0;
+  const float* part[kMax];
+  float* out[kMax];
+  int nblk[kMax], N[kMax];
+  bool add(const float* p, int nb, int cols, float* o);
+};
+// Launches the collected finalizes (one kernel) and empties the list.
+cudaError_t finalize_jobs(FinalizeJobs& j, const LaunchCtx& c);
+
 // LayerNorm backward plus residual gradient: dx = resid + LN_bwd(du); du fp32.
 // dgamma / dbeta (fp32 [h]) are reduced in a fixed order through `partial`
-// (ln_bwd_partial_floats(n, h) floats).
+// (ln_bwd_partial_floats(n, h, sums) floats); with defer, their finalizes join
+// *defer instead of running now.  With dresid and ddx (ln_bwd_can_sum), the
+// column sums of resid (as read) and of dx (as stored) go to dresid / ddx the
+// same way.
 cudaError_t ln_bwd(int dtype, const float* du, const void* x, const float* mean,
                    const float* rstd, const void* gamma, const void* resid, void* dx,
                    float* dgamma, float* dbeta, float* partial, int n, int h,
-                   const LaunchCtx& c);
-size_t ln_bwd_partial_floats(int n, int h);
+                   const LaunchCtx& c, FinalizeJobs* defer = nullptr, float* dresid = nullptr,
+                   float* ddx = nullptr);
+size_t ln_bwd_partial_floats(int n, int h, bool sums = false);
+bool ln_bwd_can_sum(int dtype, int h);
 
 // out[j] = sum_i Y[i*ld + j] (fp32, fixed order) for j < N, i < n, through
 // `partial` (colsum_partial_floats(n, N) floats).  With amax_bits, max |Y| over
 // the same elements is also folded into *amax_bits (atomicMax on the float
 // bits; the caller zeroes it).
 cudaError_t colsum(int dtype, const void* Y, int64_t ld, int n, int N, float* out,
-                   float* partial, const LaunchCtx& c, unsigned* amax_bits = nullptr);
+                   float* partial, const LaunchCtx& c, unsigned* amax_bits = nullptr,
+                   FinalizeJobs* defer = nullptr);
 size_t colsum_partial_floats(int n, int N);
 // Column sums of the dropped-out Y: Ym = Y * keep / (1 - p) (element e = row * N
 // + col of site drop.site) is written with row pitch ld, out = column sums of Ym

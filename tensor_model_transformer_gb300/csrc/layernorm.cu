@@ -6,6 +6,8 @@
 // with warp shuffles, and written once.  Parameter gradients (dgamma, dbeta) and
 // bias gradients are reduced deterministically: fixed row blocks write partial
 // column sums, then one pass adds the partials in block order.
+#include <cstring>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -16,6 +18,9 @@ constexpr int kLnThreadsMax = 512;
 constexpr int kLnBwdBlocks = 512;     // most row blocks of the dgamma/dbeta reduction
 constexpr int kLnBwdPerSM = 2;        // LN backward blocks per SM (one wave)
 constexpr int kLnBwdThreadsMax = 512; // threads per row of the LN backward
+// With the folded column sums, rows of one vector a thread and at most this
+// many threads, so that two blocks of it fit an SM's registers.
+constexpr int kLnSumsThreadsMax = 384;
 constexpr int kColsumThreads = 256;   // threads per block of the bias-gradient column sums
 constexpr int kColsumDropBlocks = 512;  // the same with dropout (Philox work per element)
 
@@ -179,16 +184,29 @@ __global__ void __launch_bounds__(kLnThreadsMax, V == 1 ? 4 : 1)   // short rows
 // MODE 0: du fp32, dx = resid + LN_bwd(du) (Pre-LN);  MODE 1: du = du2 (of type
 // T), dx = LN_bwd(du);  MODE 2: du = du (fp32) + du2 (T), dx = LN_bwd(du) (the
 // Post-LN layer's two LayerNorms).
-template <typename T, int V, int R, int MODE>
-__global__ void __launch_bounds__(kLnThreadsMax)
-    ln_bwd_kernel(const float* __restrict__ du, const T* __restrict__ du2, const T* __restrict__ x,
-                  const float* __restrict__ mean_in, const float* __restrict__ rstd_in,
-                  const T* __restrict__ gamma, const T* __restrict__ resid, T* __restrict__ dx,
-                  float* __restrict__ part_g, float* __restrict__ part_b, int n, int h,
-                  int rows_per_block) {
+// SUMS (MODE 0, rows of at most two vectors a thread): the block also sums the
+// residual input and the stored output dx column by column into part_r and
+// part_o (the Pre-LN layer's db_fc2 = sum dy and db_o = sum dx1, read here
+// anyway).
+template <typename T, int V, int R, int MODE, bool SUMS>
+__device__ __forceinline__ void ln_bwd_body(
+    const float* __restrict__ du, const T* __restrict__ du2, const T* __restrict__ x,
+    const float* __restrict__ mean_in, const float* __restrict__ rstd_in,
+    const T* __restrict__ gamma, const T* __restrict__ resid, T* __restrict__ dx,
+    float* __restrict__ part_g, float* __restrict__ part_b, int n, int h, int rows_per_block,
+    float* __restrict__ part_r, float* __restrict__ part_o) {
   constexpr int E = Vec<T>::N;
   constexpr bool ACC_REG = V <= 2;
   constexpr int VA = ACC_REG ? V : 1;
+  static_assert(!SUMS || (MODE == 0 && V == 1), "column sums need MODE 0 and one vector a thread");
+  constexpr int VS = SUMS ? VA : 1;
+  float ar[VS][E], ao[VS][E];
+  if (SUMS) {
+#pragma unroll
+    for (int i = 0; i < VS; ++i)
+#pragma unroll
+      for (int e = 0; e < E; ++e) ar[i][e] = ao[i][e] = 0.f;
+  }
   extern __shared__ float lsm[];
   float* acc_g = lsm;
   float* acc_b = lsm + h;
@@ -320,6 +338,16 @@ __global__ void __launch_bounds__(kLnThreadsMax)
         Vec<T> o;
         o.pack(of);
         o.store(dx + (size_t)(r0 + rr) * h + vi * E);
+        if (SUMS) {
+          // the residual as read and the output as stored, row by row
+          float ofr[E];
+          o.unpack(ofr);
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            ar[SUMS ? i : 0][e] += rf[e];
+            ao[SUMS ? i : 0][e] += ofr[e];
+          }
+        }
       }
       if (ACC_REG) {
 #pragma unroll
@@ -345,6 +373,10 @@ __global__ void __launch_bounds__(kLnThreadsMax)
       for (int e = 0; e < E; ++e) {
         part_g[(size_t)blockIdx.x * h + vi * E + e] = ag[i][e];
         part_b[(size_t)blockIdx.x * h + vi * E + e] = ab[i][e];
+        if (SUMS) {
+          part_r[(size_t)blockIdx.x * h + vi * E + e] = ar[SUMS ? i : 0][e];
+          part_o[(size_t)blockIdx.x * h + vi * E + e] = ao[SUMS ? i : 0][e];
+        }
       }
     }
   } else {
@@ -356,6 +388,31 @@ __global__ void __launch_bounds__(kLnThreadsMax)
       }
     }
   }
+}
+
+template <typename T, int V, int R, int MODE>
+__global__ void __launch_bounds__(kLnThreadsMax)
+    ln_bwd_kernel(const float* __restrict__ du, const T* __restrict__ du2, const T* __restrict__ x,
+                  const float* __restrict__ mean_in, const float* __restrict__ rstd_in,
+                  const T* __restrict__ gamma, const T* __restrict__ resid, T* __restrict__ dx,
+                  float* __restrict__ part_g, float* __restrict__ part_b, int n, int h,
+                  int rows_per_block) {
+  ln_bwd_body<T, V, R, MODE, false>(du, du2, x, mean_in, rstd_in, gamma, resid, dx, part_g,
+                                    part_b, n, h, rows_per_block, nullptr, nullptr);
+}
+
+// The Pre-LN form (MODE 0, one vector a thread) with the column sums of the
+// residual and of the output; bounded to two blocks an SM.
+template <typename T>
+__global__ void __launch_bounds__(kLnSumsThreadsMax, kLnBwdPerSM)
+    ln_bwd_sums_kernel(const float* __restrict__ du, const T* __restrict__ x,
+                       const float* __restrict__ mean_in, const float* __restrict__ rstd_in,
+                       const T* __restrict__ gamma, const T* __restrict__ resid,
+                       T* __restrict__ dx, float* __restrict__ part_g, float* __restrict__ part_b,
+                       int n, int h, int rows_per_block, float* __restrict__ part_r,
+                       float* __restrict__ part_o) {
+  ln_bwd_body<T, 1, 1, 0, true>(du, nullptr, x, mean_in, rstd_in, gamma, resid, dx, part_g,
+                                part_b, n, h, rows_per_block, part_r, part_o);
 }
 
 // Row blocks of a column sum over n rows of N columns with E elements a
@@ -374,12 +431,11 @@ int colsum_row_blocks(int n, int N, int E) {
 // rows, several loads in flight), then the 32 warp sums are added in warp
 // order: a fixed order for any launch.
 constexpr int kFinWarps = 32;
-__global__ void __launch_bounds__(kFinWarps * 32)
-    finalize_cols_kernel(const float* __restrict__ part, int nblk, int N,
-                         float* __restrict__ out) {
+__device__ __forceinline__ void finalize_cols(const float* __restrict__ part, int nblk, int N,
+                                              float* __restrict__ out, int cblock) {
   __shared__ float red[kFinWarps][33];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int c = blockIdx.x * 32 + lane;
+  const int c = cblock * 32 + lane;
   float s = 0.f;
   if (c < N) {
 #pragma unroll 4
@@ -393,6 +449,28 @@ __global__ void __launch_bounds__(kFinWarps * 32)
     for (int w = 0; w < kFinWarps; ++w) t += red[w][lane];
     out[c] = t;
   }
+}
+
+__global__ void __launch_bounds__(kFinWarps * 32)
+    finalize_cols_kernel(const float* __restrict__ part, int nblk, int N,
+                         float* __restrict__ out) {
+  finalize_cols(part, nblk, N, out, blockIdx.x);
+}
+
+// Several finalizes in one launch: job k owns the column blocks
+// [first[k], first[k + 1]) of the grid.  Each column is summed exactly as
+// finalize_cols_kernel sums it.
+struct FinalizeArgs {
+  const float* part[FinalizeJobs::kMax];
+  float* out[FinalizeJobs::kMax];
+  int nblk[FinalizeJobs::kMax], N[FinalizeJobs::kMax], first[FinalizeJobs::kMax + 1];
+  int n;
+};
+
+__global__ void __launch_bounds__(kFinWarps * 32) finalize_multi_kernel(const FinalizeArgs a) {
+  int k = 0;
+  while (k + 1 < a.n && (int)blockIdx.x >= a.first[k + 1]) ++k;
+  finalize_cols(a.part[k], a.nblk[k], a.N[k], a.out[k], blockIdx.x - a.first[k]);
 }
 
 // With AMAX, max |Y| of the block's elements also goes to *amax_bits (one
@@ -514,10 +592,23 @@ cudaError_t ln_fwd_t(const void* x, const void* g, const void* b, void* u, float
   return cudaGetLastError();
 }
 
+// One finalize of nblk rows of partial column sums: deferred into *defer when
+// given, else launched now.
+cudaError_t finalize_or_defer(const float* part, int nblk, int N, float* out, const LaunchCtx& c,
+                              FinalizeJobs* defer) {
+  if (defer) return defer->add(part, nblk, N, out) ? cudaSuccess : cudaErrorInvalidValue;
+  c.before(KK_FINALIZE, 4.0 * nblk * N);
+  finalize_cols_kernel<<<(N + 31) / 32, kFinWarps * 32, 0, c.stream>>>(part, nblk, N, out);
+  c.after();
+  return cudaGetLastError();
+}
+
 template <typename T, int MODE>
 cudaError_t ln_bwd_t(const float* du, const void* du2, const void* x, const float* mean,
                      const float* rstd, const void* g, const void* resid, void* dx, float* dgamma,
-                     float* dbeta, float* partial, int n, int h, const LaunchCtx& c) {
+                     float* dbeta, float* partial, int n, int h, const LaunchCtx& c,
+                     FinalizeJobs* defer = nullptr, float* dresid = nullptr,
+                     float* ddx = nullptr) {
   int vpt, threads;
   row_plan<T>(h, &vpt, &threads, kLnBwdThreadsMax);
   // one wave of kLnBwdPerSM blocks per SM, at most kLnBwdBlocks (the partial
@@ -527,6 +618,10 @@ cudaError_t ln_bwd_t(const float* du, const void* du2, const void* x, const floa
   const int rows = (n + nblk - 1) / nblk;
   float* pg = partial;
   float* pb = partial + (size_t)nblk * h;
+  float* pr = partial + 2 * (size_t)nblk * h;
+  float* po = partial + 3 * (size_t)nblk * h;
+  const bool sums = dresid && ddx;
+  if (sums && MODE != 0) return cudaErrorInvalidValue;
   const size_t smem = vpt <= 2 ? 0 : 2 * (size_t)h * sizeof(float);
   c.before(KK_LN_BWD, (double)n * h * (3.0 * sizeof(T) + 4.0) + 8.0 * n);
 #define LN_BWD_CASE(VV, RR)                                                                 \
@@ -541,30 +636,39 @@ cudaError_t ln_bwd_t(const float* du, const void* du2, const void* x, const floa
         du, (const T*)du2, (const T*)x, mean, rstd, (const T*)g, (const T*)resid, (T*)dx,   \
         pg, pb, n, h, rows);                                                                \
     break;
-  switch (vpt) {
-    LN_BWD_CASE(1, 1)
-    LN_BWD_CASE(2, 1)
-    LN_BWD_CASE(4, 1)
-    LN_BWD_CASE(8, 1)
-    default:
-      return cudaErrorInvalidValue;
+  if (sums) {
+    if constexpr (MODE == 0) {
+      if (vpt != 1 || threads > kLnSumsThreadsMax) return cudaErrorInvalidValue;
+      ln_bwd_sums_kernel<T><<<nblk, threads, 0, c.stream>>>(
+          du, (const T*)x, mean, rstd, (const T*)g, (const T*)resid, (T*)dx, pg, pb, n, h, rows,
+          pr, po);
+    }
+  } else {
+    switch (vpt) {
+      LN_BWD_CASE(1, 1)
+      LN_BWD_CASE(2, 1)
+      LN_BWD_CASE(4, 1)
+      LN_BWD_CASE(8, 1)
+      default:
+        return cudaErrorInvalidValue;
+    }
   }
 #undef LN_BWD_CASE
   c.after();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  c.before(KK_FINALIZE, 4.0 * nblk * h);
-  finalize_cols_kernel<<<(h + 31) / 32, kFinWarps * 32, 0, c.stream>>>(pg, nblk, h, dgamma);
-  c.after();
-  c.before(KK_FINALIZE, 4.0 * nblk * h);
-  finalize_cols_kernel<<<(h + 31) / 32, kFinWarps * 32, 0, c.stream>>>(pb, nblk, h, dbeta);
-  c.after();
-  return cudaGetLastError();
+  if ((e = finalize_or_defer(pg, nblk, h, dgamma, c, defer)) != cudaSuccess) return e;
+  if ((e = finalize_or_defer(pb, nblk, h, dbeta, c, defer)) != cudaSuccess) return e;
+  if (sums) {
+    if ((e = finalize_or_defer(pr, nblk, h, dresid, c, defer)) != cudaSuccess) return e;
+    if ((e = finalize_or_defer(po, nblk, h, ddx, c, defer)) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 template <typename T>
 cudaError_t colsum_t(const void* Y, int64_t ld, int n, int N, float* out, float* partial,
-                     const LaunchCtx& c, unsigned* amax_bits) {
+                     const LaunchCtx& c, unsigned* amax_bits, FinalizeJobs* defer) {
   constexpr int E = Vec<T>::N;
   const int nblk = colsum_row_blocks(n, N, E);
   const int rows = (n + nblk - 1) / nblk;
@@ -578,10 +682,9 @@ cudaError_t colsum_t(const void* Y, int64_t ld, int n, int N, float* out, float*
     colsum_partial_kernel<T, false><<<grid, threads, 0, c.stream>>>((const T*)Y, ld, n, N, rows,
                                                                     partial, nullptr);
   c.after();
-  c.before(KK_FINALIZE, 4.0 * nblk * N);
-  finalize_cols_kernel<<<(N + 31) / 32, kFinWarps * 32, 0, c.stream>>>(partial, nblk, N, out);
-  c.after();
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return finalize_or_defer(partial, nblk, N, out, c, defer);
 }
 
 template <typename T>
@@ -605,9 +708,50 @@ cudaError_t colsum_dropout_t(const void* Y, void* Ym, int64_t ld, int n, int N,
 
 }  // namespace
 
-size_t ln_bwd_partial_floats(int n, int h) {
+size_t ln_bwd_partial_floats(int n, int h, bool sums) {
   const size_t nblk = n < kLnBwdBlocks ? (n > 0 ? n : 1) : kLnBwdBlocks;
-  return 2 * nblk * (size_t)h;
+  return (sums ? 4 : 2) * nblk * (size_t)h;
+}
+
+bool ln_bwd_can_sum(int dtype, int h) {
+  // one vector a thread (the sums stay in registers) and a block small enough
+  // for two a SM
+  return h / (dtype == kBF16 ? 8 : 4) <= kLnSumsThreadsMax;
+}
+
+bool FinalizeJobs::add(const float* p, int nb, int cols, float* o) {
+  if (n >= kMax) return false;
+  part[n] = p;
+  nblk[n] = nb;
+  N[n] = cols;
+  out[n] = o;
+  ++n;
+  return true;
+}
+
+cudaError_t finalize_jobs(FinalizeJobs& j, const LaunchCtx& c) {
+  if (j.n == 0) return cudaSuccess;
+  FinalizeArgs a;
+  memset(&a, 0, sizeof(a));
+  a.n = j.n;
+  int blocks = 0;
+  double bytes = 0;
+  for (int k = 0; k < j.n; ++k) {
+    a.part[k] = j.part[k];
+    a.out[k] = j.out[k];
+    a.nblk[k] = j.nblk[k];
+    a.N[k] = j.N[k];
+    a.first[k] = blocks;
+    blocks += (j.N[k] + 31) / 32;
+    bytes += 4.0 * j.nblk[k] * j.N[k];
+  }
+  a.first[j.n] = blocks;
+  j.n = 0;
+  if (blocks == 0) return cudaSuccess;
+  c.before(KK_FINALIZE, bytes);
+  finalize_multi_kernel<<<blocks, kFinWarps * 32, 0, c.stream>>>(a);
+  c.after();
+  return cudaGetLastError();
 }
 size_t colsum_dropout_partial_floats(int n, int N) {
   const size_t nblk = n < kColsumDropBlocks ? (n > 0 ? n : 1) : kColsumDropBlocks;
@@ -627,11 +771,11 @@ cudaError_t ln_fwd(int dtype, const void* x, const void* g, const void* b, void*
 cudaError_t ln_bwd(int dtype, const float* du, const void* x, const float* mean,
                    const float* rstd, const void* g, const void* resid, void* dx,
                    float* dgamma, float* dbeta, float* partial, int n, int h,
-                   const LaunchCtx& c) {
+                   const LaunchCtx& c, FinalizeJobs* defer, float* dresid, float* ddx) {
   return dtype == kBF16 ? ln_bwd_t<bf16, 0>(du, nullptr, x, mean, rstd, g, resid, dx, dgamma,
-                                            dbeta, partial, n, h, c)
+                                            dbeta, partial, n, h, c, defer, dresid, ddx)
                         : ln_bwd_t<float, 0>(du, nullptr, x, mean, rstd, g, resid, dx, dgamma,
-                                             dbeta, partial, n, h, c);
+                                             dbeta, partial, n, h, c, defer, dresid, ddx);
 }
 
 cudaError_t ln_bwd_sum(int dtype, const float* du, const void* du2, const void* x,
@@ -716,9 +860,9 @@ cudaError_t gelu_apply(int dtype, const void* z, void* a, int64_t count, const L
 }
 
 cudaError_t colsum(int dtype, const void* Y, int64_t ld, int n, int N, float* out,
-                   float* partial, const LaunchCtx& c, unsigned* amax_bits) {
-  return dtype == kBF16 ? colsum_t<bf16>(Y, ld, n, N, out, partial, c, amax_bits)
-                        : colsum_t<float>(Y, ld, n, N, out, partial, c, amax_bits);
+                   float* partial, const LaunchCtx& c, unsigned* amax_bits, FinalizeJobs* defer) {
+  return dtype == kBF16 ? colsum_t<bf16>(Y, ld, n, N, out, partial, c, amax_bits, defer)
+                        : colsum_t<float>(Y, ld, n, N, out, partial, c, amax_bits, defer);
 }
 
 cudaError_t colsum_dropout(int dtype, const void* Y, void* Ym, int64_t ld, int n, int N,

@@ -282,6 +282,37 @@ void layer_split_sizes(const Dims& D, size_t* bytes, size_t* counters) {
   }
 }
 
+// Partial column sums of the Pre-LN backward, all kept until its one finalize
+// launch at the end (float offsets into the workspace's partial region): LN2
+// (dgamma2, dbeta2 and, folded in, db_fc2 and db_o), LN1 (dgamma1, dbeta1),
+// db_fc1 (from the fc2-dgrad epilogue, or a column sum of dz), db_qkv, db_fc2
+// and db_o when not folded, and the dropout column sums (finalized at once).
+struct PartialLayout {
+  size_t ln2, ln1, dz, qkv, b2, bo, drop, total;
+};
+
+PartialLayout partial_layout(const Dims& D) {
+  PartialLayout P;
+  size_t off = 0;
+  auto take = [&](size_t floats) {
+    const size_t at = off;
+    off += (floats + 63) / 64 * 64;
+    return at;
+  };
+  const int n = (int)D.n, h = (int)D.h, f = (int)D.f;
+  P.ln2 = take(ln_bwd_partial_floats(n, h, true));
+  P.ln1 = take(ln_bwd_partial_floats(n, h, false));
+  const size_t dz_epi = (size_t)((n + 31) / 32) * f;
+  const size_t dz_col = colsum_partial_floats(n, f);
+  P.dz = take(dz_epi > dz_col ? dz_epi : dz_col);
+  P.qkv = take(colsum_partial_floats(n, 3 * h));
+  P.b2 = take(colsum_partial_floats(n, h));
+  P.bo = take(colsum_partial_floats(n, h));
+  P.drop = take(colsum_dropout_partial_floats(n, h));
+  P.total = off;
+  return P;
+}
+
 // Backward scratch, after the status word.  The GEMMs' tail-slice counters
 // come first, so that one memset clears them with the status word.
 struct WsLayout {
@@ -316,7 +347,8 @@ WsLayout ws_layout(const Dims& D) {
   }
   const size_t pd = colsum_dropout_partial_floats((int)D.n, (int)D.h);
   if (pd > pf) pf = pd;
-  W.partial = take(pf * 4);
+  const size_t pl = partial_layout(D).total;   // the Pre-LN backward's deferred finalizes
+  W.partial = take((pl > pf ? pl : pf) * 4);
   W.fp8 = take(fp8_ws_layout(D).total);
   // recomputed activations ([n][h] and [n][ffn]); the forward keeps the ones it
   // does not save here too
@@ -975,16 +1007,26 @@ mtl_status mtl_layer_bwd(const mtl_layer_desc* desc, const mtl_weights* w, const
   const bool hid_drop = D.p_hidden > 0.f;
   const Dropout drop_attn = make_drop(D.p_attn, D.seed, SITE_ATTN);
   void* gmask = at<char>(workspace, W.gmask);
+  // Bias, gamma and beta gradients: every partial column sum stays in its own
+  // region and one launch at the end adds them up (finalize_jobs).  db_fc2 and
+  // db_o ride the LN2 backward (it reads dy and writes dx1 anyway) and db_fc1
+  // the fc2-dgrad epilogue (it holds every dz) where they can.
+  const PartialLayout P = partial_layout(D);
+  FinalizeJobs fin;
+  const bool fold_ln2 = !hid_drop && ln_bwd_can_sum(D.dtype, h);
+  const bool fold_dz = D.dtype == MTL_BF16 && f % 32 == 0;
   // B0 gradient at the fc2 output g2 = dy * keep_2 / (1 - p) (dy itself without
   // dropout) and db2 = sum_rows g2
   const void* g2 = dy;
   if (hid_drop) {
     MTL_TRY(colsum_dropout(D.dtype, dy, gmask, h, n, h, make_drop(D.p_hidden, D.seed, SITE_FC2),
-                           static_cast<float*>(gr->b_fc2), partial, c),
+                           static_cast<float*>(gr->b_fc2), partial + P.drop, c),
             "db_fc2");
     g2 = gmask;
-  } else {
-    MTL_TRY(colsum(D.dtype, dy, h, n, h, static_cast<float*>(gr->b_fc2), partial, c), "db_fc2");
+  } else if (!fold_ln2) {
+    MTL_TRY(colsum(D.dtype, dy, h, n, h, static_cast<float*>(gr->b_fc2), partial + P.b2, c,
+                   nullptr, &fin),
+            "db_fc2");
   }
   // B1 fc2 dgrad + GeLU': dz = (g2 W_fc2) * GeLU'(z)  (column-local, no reduction)
   {
@@ -992,7 +1034,10 @@ mtl_status mtl_layer_bwd(const mtl_layer_desc* desc, const mtl_weights* w, const
                            status);
     g.Z = const_cast<void*>(z);
     g.ldz = f;
+    if (fold_dz) g.colsum_part = partial + P.dz;
     MTL_TRY(run_gemm(D, g, c), "fc2 dgrad");
+    if (fold_dz && !fin.add(partial + P.dz, (n + 31) / 32, f, static_cast<float*>(gr->b_fc1)))
+      return cuda_fail(cudaErrorInvalidValue, "finalize list");
   }
   // B2 fc2 wgrad dW2 = g2^T a  (a recomputed as GeLU(z) when not saved)
   if (D.recompute) {
@@ -1020,22 +1065,30 @@ mtl_status mtl_layer_bwd(const mtl_layer_desc* desc, const mtl_weights* w, const
                                 true, status),
                    c),
           "fc1 wgrad");
-  MTL_TRY(colsum(D.dtype, dz, f, n, f, static_cast<float*>(gr->b_fc1), partial, c), "db_fc1");
-  // B5 LN2 backward + residual: dx1 = dy + LN2_bwd(du2)
+  if (!fold_dz)
+    MTL_TRY(colsum(D.dtype, dz, f, n, f, static_cast<float*>(gr->b_fc1), partial + P.dz, c,
+                   nullptr, &fin),
+            "db_fc1");
+  // B5 LN2 backward + residual: dx1 = dy + LN2_bwd(du2); with the fold also
+  // db_fc2 = sum_rows dy and db_o = sum_rows dx1
   MTL_TRY(ln_bwd(D.dtype, du, x1, at<float>(saved, L.mu2), at<float>(saved, L.rstd2), w->ln2_g, dy,
-                 dx1, static_cast<float*>(gr->ln2_g), static_cast<float*>(gr->ln2_b), partial, n,
-                 h, c),
+                 dx1, static_cast<float*>(gr->ln2_g), static_cast<float*>(gr->ln2_b),
+                 partial + P.ln2, n, h, c, &fin,
+                 fold_ln2 ? static_cast<float*>(gr->b_fc2) : nullptr,
+                 fold_ln2 ? static_cast<float*>(gr->b_o) : nullptr),
           "ln2 bwd");
   // B6 gradient at the out-proj output go = dx1 * keep_1 / (1 - p) (dx1 without
   // dropout), db_o = sum_rows go; dgrad dctx = go W_o, wgrad dW_o = go^T ctx
   const void* go = dx1;
   if (hid_drop) {
     MTL_TRY(colsum_dropout(D.dtype, dx1, gmask, h, n, h, make_drop(D.p_hidden, D.seed, SITE_OUT),
-                           static_cast<float*>(gr->b_o), partial, c),
+                           static_cast<float*>(gr->b_o), partial + P.drop, c),
             "db_o");
     go = gmask;
-  } else {
-    MTL_TRY(colsum(D.dtype, dx1, h, n, h, static_cast<float*>(gr->b_o), partial, c), "db_o");
+  } else if (!fold_ln2) {
+    MTL_TRY(colsum(D.dtype, dx1, h, n, h, static_cast<float*>(gr->b_o), partial + P.bo, c,
+                   nullptr, &fin),
+            "db_o");
   }
   MTL_TRY(run_gemm(D, gemm_args(n, h, h, 1, go, h, true, w->w_o, h, false, EPI_STORE, dctx, h,
                                 false, status),
@@ -1068,7 +1121,8 @@ mtl_status mtl_layer_bwd(const mtl_layer_desc* desc, const mtl_weights* w, const
                                 gr->w_qkv, h, true, status),
                    c),
           "qkv wgrad");
-  MTL_TRY(colsum(D.dtype, dqkv, 3 * h, n, 3 * h, static_cast<float*>(gr->b_qkv), partial, c),
+  MTL_TRY(colsum(D.dtype, dqkv, 3 * h, n, 3 * h, static_cast<float*>(gr->b_qkv), partial + P.qkv,
+                 c, nullptr, &fin),
           "db_qkv");
   // B9 QKV dgrad with the f reduction: du1 = sum_p dqkv[:, Q_p] W_qkv[Q_p, :]
   MTL_TRY(run_gemm(D, gemm_args(n, h, 3 * h, t, dqkv, 3 * h, true, w->w_qkv, h, false, EPI_STORE,
@@ -1078,8 +1132,10 @@ mtl_status mtl_layer_bwd(const mtl_layer_desc* desc, const mtl_weights* w, const
   // B10 LN1 backward + residual: dx = dx1 + LN1_bwd(du1)
   MTL_TRY(ln_bwd(D.dtype, du, x, at<float>(saved, L.mu1), at<float>(saved, L.rstd1), w->ln1_g,
                  dx1, dx, static_cast<float*>(gr->ln1_g), static_cast<float*>(gr->ln1_b),
-                 partial, n, h, c),
+                 partial + P.ln1, n, h, c, &fin),
           "ln1 bwd");
+  // every deferred bias / gamma / beta finalize in one launch
+  MTL_TRY(finalize_jobs(fin, c), "finalize");
   return MTL_OK;
 }
 
