@@ -49,6 +49,9 @@ def megatron_flops(s):
     return 72 * n * s.h * s.h + 12 * s.batch * s.seq * s.seq * s.h
 
 
+# Idle seconds before the end-to-end pass, so that it starts from the same
+# rested clock state as the device-only pass.
+REST_S = 1.5
 # Nominal dense (no 2:4 sparsity) tensor rates of a GB300, TFLOP/s.
 NOMINAL_TFLOPS = {"bf16": 2250.0, "fp8": 4500.0}
 # Below this timed-region length a kernel is timed as a burst, so the burst
@@ -82,7 +85,11 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs.
+
+    The nvidia-smi process is started before the warm-up and left running:
+    starting it inside a timed region stalls the host's kernel launches for
+    milliseconds while it initialises."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -109,7 +116,17 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def window(self, t0, t1):
+        """Statistics of the samples taken in [t0, t1 + 0.15] (monotonic seconds;
+        a sample is printed up to one period after it is taken), or of the
+        first sample after t0 when none falls inside."""
+        time.sleep(0.2)
+        inside = [ln for t, ln in list(self.lines) if t0 <= t <= t1 + 0.15]
+        if not inside:
+            inside = [ln for t, ln in list(self.lines) if t >= t0][:1]
+        return self._stats(inside)
 
     def stop(self):
         if self.proc is None:
@@ -122,9 +139,14 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
+        return self._stats([ln for _, ln in self.lines])
+
+    def _stats(self, lines):
+        if self.proc is None:
+            return None
         sm, mx, reasons = [], 0.0, set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for ln in self.lines:
+        for ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 8:
                 continue
@@ -556,16 +578,17 @@ def main():
         if world > 1:
             dist.barrier()
 
+    clocks = ClockSampler(local)
+    clocks.start()
     for _ in range(args.warmup):
         launches_per_step = step()
     mtl.layer_check(ws)
     torch.cuda.synchronize()
 
     # ---- timed region: inputs resident in HBM
-    clocks = ClockSampler(local)
-    clocks.start()
     barrier()
     torch.cuda.synchronize()
+    t_dev = time.monotonic()
     evs_step = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     evs_step[0].record(stream)
     launches = 0
@@ -577,7 +600,7 @@ def main():
     barrier()
     ms = evs_step[0].elapsed_time(evs_step[-1])
     per_step = sorted(evs_step[i].elapsed_time(evs_step[i + 1]) for i in range(args.steps))
-    clk = clocks.stop()
+    clk = clocks.window(t_dev, time.monotonic())
     mtl.layer_check(ws)
     flops = layer_flops(shape)
     ms, value = aggregate_over_ranks(ms, flops, args.steps, world, dist if world > 1 else None,
@@ -589,8 +612,15 @@ def main():
     # back; one stream per copy direction overlaps step i's copies with the
     # neighbouring steps' compute through double-buffered device inputs and
     # outputs (the two directions run on their own copy engines at once).
+    # Both timed passes start from a rested GPU: under seconds of sustained
+    # load the power limit lowers the clock (a step measured at 7.0 ms after
+    # rest took 7.8 ms half a second into a run), which would otherwise be
+    # charged to whichever pass runs second.  After the rest a few untimed
+    # steps of the same pipeline wake the host and the GPU up (the first
+    # launches after an idle second were measured arriving milliseconds late).
     barrier()
     torch.cuda.synchronize()
+    time.sleep(REST_S)
     copy = torch.cuda.Stream()
     copy_out = torch.cuda.Stream()
     xs = [xd, torch.empty_like(xd)]
@@ -603,41 +633,72 @@ def main():
     computed = [torch.cuda.Event() for _ in range(2)]
     drained = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step_io(i):
-        b = i % 2
-        with torch.cuda.stream(copy):
-            if i >= 2:
-                copy.wait_event(computed[b])        # step i-2 is done with buffer b
-            xs[b].copy_(x_h, non_blocking=True)
-            dys[b].copy_(dy_h, non_blocking=True)
-            loaded[b].record(copy)
+    def e2e_pass(nsteps):
+        """nsteps pipelined steps; (ms from start to the last copy out, per-step
+        event intervals on the compute, copy-in and copy-out streams)."""
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        tev = {k: [torch.cuda.Event(enable_timing=True) for _ in range(nsteps)]
+               for k in ("c0", "c1", "i0", "i1", "o0", "o1")}
+        torch.cuda.synchronize()
+        e0.record(stream)
+        copy.wait_event(e0)
+        copy_out.wait_event(e0)
 
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_clocks = ClockSampler(local)
-    e2e_clocks.start()
-    e0.record(stream)
-    copy.wait_event(e0)
-    e2e_step_io(0)
-    for i in range(args.steps):
-        b = i % 2
-        if i + 1 < args.steps:
-            e2e_step_io(i + 1)
-        stream.wait_event(loaded[b])
-        if i >= 2:
-            stream.wait_event(drained[b])           # outputs of step i-2 copied out
-        mtl.layer_fwd(desc, w, xs[b], ys[b], saved, ws, stream)
-        mtl.layer_bwd(desc, w, xs[b], saved, dys[b], dxs[b], grads, ws, stream)
-        computed[b].record(stream)
-        with torch.cuda.stream(copy_out):
-            copy_out.wait_event(computed[b])
-            y_h[b].copy_(ys[b], non_blocking=True)
-            dx_h[b].copy_(dxs[b], non_blocking=True)
-            drained[b].record(copy_out)
-    e1.record(copy_out)
-    e1.synchronize()
-    torch.cuda.synchronize()
-    e2e_clk = e2e_clocks.stop()
-    ms_e2e = e0.elapsed_time(e1)
+        def io_in(i):
+            b = i % 2
+            with torch.cuda.stream(copy):
+                if i >= 2:
+                    copy.wait_event(computed[b])    # step i-2 is done with buffer b
+                tev["i0"][i].record(copy)
+                xs[b].copy_(x_h, non_blocking=True)
+                dys[b].copy_(dy_h, non_blocking=True)
+                tev["i1"][i].record(copy)
+                loaded[b].record(copy)
+
+        io_in(0)
+        for i in range(nsteps):
+            b = i % 2
+            if i + 1 < nsteps:
+                io_in(i + 1)
+            stream.wait_event(loaded[b])
+            if i >= 2:
+                stream.wait_event(drained[b])       # outputs of step i-2 copied out
+            tev["c0"][i].record(stream)
+            mtl.layer_fwd(desc, w, xs[b], ys[b], saved, ws, stream)
+            mtl.layer_bwd(desc, w, xs[b], saved, dys[b], dxs[b], grads, ws, stream)
+            tev["c1"][i].record(stream)
+            computed[b].record(stream)
+            with torch.cuda.stream(copy_out):
+                copy_out.wait_event(computed[b])
+                tev["o0"][i].record(copy_out)
+                y_h[b].copy_(ys[b], non_blocking=True)
+                dx_h[b].copy_(dxs[b], non_blocking=True)
+                tev["o1"][i].record(copy_out)
+                drained[b].record(copy_out)
+        e1.record(copy_out)
+        e1.synchronize()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1), tev, e0
+
+    e2e_pass(3)                                      # untimed: wake up after the rest
+    barrier()
+    t_e2e = time.monotonic()
+    ms_e2e, tev, e0 = e2e_pass(args.steps)
+    e2e_clk = clocks.window(t_e2e, time.monotonic())
+    med = lambda v: sorted(v)[len(v) // 2]  # noqa: E731
+    span = lambda a, b: [tev[a][i].elapsed_time(tev[b][i]) for i in range(args.steps)]  # noqa: E731
+    comp_ms = span("c0", "c1")
+    gaps = [tev["c1"][i - 1].elapsed_time(tev["c0"][i]) for i in range(1, args.steps)]
+    e2e_timeline = {
+        "compute_ms_median": med(comp_ms), "h2d_ms_median": med(span("i0", "i1")),
+        "d2h_ms_median": med(span("o0", "o1")),
+        # time per step not covered by compute: copies or waits on the compute stream
+        "exposed_ms_per_step": (ms_e2e - sum(comp_ms)) / args.steps,
+        "first_compute_start_ms": e0.elapsed_time(tev["c0"][0]),
+        "gap_ms_max": max(gaps) if gaps else 0.0,
+        "gap_ms_mean": sum(gaps) / len(gaps) if gaps else 0.0,
+        "device_only_step_ms_median": per_step[len(per_step) // 2],
+    }
     ms_e2e, e2e_value = aggregate_over_ranks(ms_e2e, flops, args.steps, world,
                                              dist if world > 1 else None, "cuda")
     nbytes = x_h.numel() * x_h.element_size()
@@ -726,10 +787,11 @@ def main():
         "peak_source": step_peak_src,
         "gpu_launches": launches,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 2 * nbytes,
-                "d2h_bytes_per_step": 2 * nbytes, "clocks": e2e_clk},
+                "d2h_bytes_per_step": 2 * nbytes, "clocks": e2e_clk, "timeline": e2e_timeline},
         "roofline": roofline,
         "kernels": breakdown,
     }
+    clocks.stop()
     if clk:
         out["clocks"] = clk
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
