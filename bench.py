@@ -165,11 +165,12 @@ class ClockSampler:
 
 
 def gemm_source_sha():
-    """sha256 of the tensor-core GEMM's sources (gemm_core.cuh, gemm_tc.cu, then
-    common.cuh, which holds the epilogue's helpers and GeLU)."""
+    """sha256 of the tensor-core GEMM's sources (gemm_core.cuh, gemm_tc.cu, the
+    tail-slice instantiations gemm_split.cu, then common.cuh, which holds the
+    epilogue's helpers and GeLU)."""
     csrc = os.path.join(ROOT, "tensor_model_transformer_gb300", "csrc")
     data = b"".join(open(os.path.join(csrc, f), "rb").read()
-                    for f in ("gemm_core.cuh", "gemm_tc.cu", "common.cuh"))
+                    for f in ("gemm_core.cuh", "gemm_tc.cu", "gemm_split.cu", "common.cuh"))
     return hashlib.sha256(data).hexdigest()
 
 
