@@ -163,6 +163,20 @@ mtl_status mtl_layer_sizes(const mtl_layer_desc* desc, size_t* saved_bytes,
 /* Offsets of each saved activation inside `saved` (see mtl_saved_layout). */
 mtl_status mtl_layer_saved_layout(const mtl_layer_desc* desc, mtl_saved_layout* out);
 
+/* Byte offsets, inside the caller's `workspace`, of the backward's
+ * intermediates, which stay there after mtl_layer_bwd (stream-ordered) until
+ * the next call using that workspace -- for inspection.  n = batch*seq.
+ * Pre-LN layer: dz [n][ffn] (desc.dtype) = (g2 W_fc2) * GeLU'(z); du [n][h]
+ * fp32 = the f-summed gradient at the LN1 output (du1; the LN2 one, du2, is
+ * written first and overwritten); dx1 [n][h] (desc.dtype), the gradient at
+ * the attention block's output; dctx [n][h] (desc.dtype) = go W_o; dqkv
+ * [n][3h] (desc.dtype, head-interleaved columns).  Post-LN layer: dctx holds
+ * the LN2 input gradient dh2 and dx1 the LN1 input gradient dh1. */
+typedef struct {
+  size_t dz, du, dx1, dctx, dqkv, total;
+} mtl_workspace_layout;
+mtl_status mtl_layer_workspace_layout(const mtl_layer_desc* desc, mtl_workspace_layout* out);
+
 /* Forward pass: y = layer(x).  x, y [batch][seq][h] of desc.dtype; `saved`
  * (>= saved_bytes) receives the activations for the backward; `workspace`
  * (>= workspace_bytes, contents not preserved) is scratch.  y must not alias x

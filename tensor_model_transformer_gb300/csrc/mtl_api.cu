@@ -742,6 +742,21 @@ mtl_status mtl_layer_saved_layout(const mtl_layer_desc* desc, mtl_saved_layout* 
   return MTL_OK;
 }
 
+mtl_status mtl_layer_workspace_layout(const mtl_layer_desc* desc, mtl_workspace_layout* out) {
+  Dims D;
+  mtl_status st = validate(desc, &D);
+  if (st != MTL_OK) return st;
+  if (!out) return MTL_ERR_INVALID_ARG;
+  const WsLayout W = ws_layout(D);
+  out->dz = W.dz;
+  out->du = W.du;
+  out->dx1 = W.dx1;
+  out->dctx = W.dctx;
+  out->dqkv = W.dqkv;
+  out->total = W.total;
+  return MTL_OK;
+}
+
 mtl_status mtl_layer_fwd(const mtl_layer_desc* desc, const mtl_weights* w, const void* x,
                          void* y, void* saved, void* workspace, size_t ws_bytes,
                          mtl_stream stream) {

@@ -47,6 +47,10 @@ class Grads(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in PARAM_NAMES]
 
 
+class WorkspaceLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in ("dz", "du", "dx1", "dctx", "dqkv", "total")]
+
+
 class SavedLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in SAVED_NAMES] + [("total", ctypes.c_size_t)]
 
@@ -66,6 +70,7 @@ def lib():
         pd = ctypes.POINTER(LayerDesc)
         L.mtl_layer_sizes.argtypes = [pd, ctypes.POINTER(sz), ctypes.POINTER(sz)]
         L.mtl_layer_saved_layout.argtypes = [pd, ctypes.POINTER(SavedLayout)]
+        L.mtl_layer_workspace_layout.argtypes = [pd, ctypes.POINTER(WorkspaceLayout)]
         L.mtl_layer_fwd.argtypes = [pd, ctypes.POINTER(Weights), vp, vp, vp, vp, sz, vp]
         L.mtl_layer_bwd.argtypes = [pd, ctypes.POINTER(Weights), vp, vp, vp, vp,
                                     ctypes.POINTER(Grads), vp, sz, vp]
@@ -104,7 +109,7 @@ def lib():
                    "mtl_layer_check", "mtl_gemm", "mtl_attention_ws_bytes", "mtl_attention_fwd",
                    "mtl_attention_bwd", "mtl_attention_mask_bytes", "mtl_infer_sizes",
                    "mtl_layer_prefill", "mtl_layer_decode", "mtl_fp8_quantize", "mtl_gemm_fp8",
-                   "mtl_gemm_ws_bytes"):
+                   "mtl_gemm_ws_bytes", "mtl_layer_workspace_layout"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -355,6 +360,26 @@ def alloc_layer_buffers(desc: LayerDesc, device="cuda"):
     ws = torch.empty(max(ws_b, 256), dtype=torch.uint8, device=device)
     grads = {k: torch.empty(v, dtype=torch.float32, device=device) for k, v in shapes.items()}
     return saved, ws, grads
+
+
+def workspace_views(desc: LayerDesc, workspace) -> dict:
+    """Typed views of the backward's intermediates left in `workspace` after
+    mtl_layer_bwd (dz, du, dx1, dctx, dqkv; see mtl_workspace_layout)."""
+    import torch
+    out = WorkspaceLayout()
+    _check(lib().mtl_layer_workspace_layout(ctypes.byref(desc), ctypes.byref(out)),
+           "mtl_layer_workspace_layout")
+    n, h, f = desc.batch * desc.seq, desc.h, desc.ffn
+    dt = torch_dtype(desc)
+    esz = 2 if desc.dtype == BF16 else 4
+
+    def view(off, shape, dtype, elsize):
+        cnt = shape[0] * shape[1]
+        return workspace[off:off + cnt * elsize].view(dtype).view(*shape)
+
+    return {"dz": view(out.dz, (n, f), dt, esz), "du": view(out.du, (n, h), torch.float32, 4),
+            "dx1": view(out.dx1, (n, h), dt, esz), "dctx": view(out.dctx, (n, h), dt, esz),
+            "dqkv": view(out.dqkv, (n, 3 * h), dt, esz)}
 
 
 def saved_views(desc: LayerDesc, saved):

@@ -292,3 +292,62 @@ def test_fp8_hybrid_scales_follow_planted_outliers():
     bad = {k: v for k, v in errs.items() if v > (FP8_TOL["y"] if k == "y" else 0.15)}
     assert not bad, (bad, errs)
     assert np.array_equal(g["y"], g1["y"])
+
+
+@pytest.mark.parametrize("name", sorted(FP8_SHAPES))
+def test_fp8_hybrid_backward_gemms_on_the_same_operands(name):
+    """Each backward GEMM of the hybrid layer against oracle.fp8.gemm on the
+    operands the GPU quantized: the gradient operands (dy, and dz, dx1, dqkv as
+    the GPU left them in the workspace) in E5M2, the forward activations (u1,
+    ctx, u2, a as the bf16 forward saves them, the same forward as the hybrid
+    one's) and the weights in E4M3, each with its per-tensor scale.  Both sides
+    multiply identical FP8 values, so they agree to fp32 accumulation order
+    (1e-5 for fp32 outputs) or bf16 rounding of a stored output (4e-3); a
+    swapped operand, orientation, scale slot or partition count gives an error
+    of order 1."""
+    import torch
+    import synthetic
+    from harness import make, run_gpu, to_device
+    from tensor_model_transformer_gb300 import mtl
+    kw, t = FP8_SHAPES[name]
+    shape = synthetic.tiny(dtype="bf16", w_std=0.02, out_std=0.01, **kw)
+    x, p, dy = make(shape, seed=2, affine=True)
+    f1 = run_gpu(shape, x, p, dy, t, fp8=1)              # the forward's saved bf16 activations
+    desc = mtl.layer_desc(shape.h, shape.heads, shape.seq, x.shape[0], shape.ffn, t, "bf16", fp8=2)
+    dev_p = {k: to_device(v, "bf16") for k, v in p.items()}
+    xd, dyd = to_device(x, "bf16"), to_device(dy, "bf16")
+    saved, ws, grads = mtl.alloc_layer_buffers(desc)
+    y, dx = torch.empty_like(xd), torch.empty_like(xd)
+    mtl.layer_fwd(desc, dev_p, xd, y, saved, ws)
+    mtl.layer_bwd(desc, dev_p, xd, saved, dyd, dx, grads, ws)
+    mtl.layer_check(ws)
+    torch.cuda.synchronize()
+    inter = {k: to_np(v) for k, v in mtl.workspace_views(desc, ws).items()}
+    g = {k: to_np(v) for k, v in grads.items()}
+    n = x.shape[0] * shape.seq
+    dyf = dy.reshape(n, shape.h).astype(np.float64)
+    W = {k: p[k].astype(np.float64) for k in ("w_qkv", "w_o", "w_fc1", "w_fc2")}
+    act = {k: f1["s_" + k] for k in ("u1", "ctx", "u2", "a", "z")}
+    E5, E4 = "e5m2", "e4m3"
+
+    def fp8(A, B, parts=1):
+        return FP8.gemm(A, B, E5, E4, parts=parts)[0]
+
+    def bf16(v):
+        return to_np(torch.from_numpy(np.asarray(v, dtype=np.float32)).to(torch.bfloat16))
+
+    checks = {
+        # weight gradients (fp32 out): dW = G^T X
+        "d_w_fc2": (g["w_fc2"], fp8(dyf.T, act["a"].T), 1e-5),
+        "d_w_fc1": (g["w_fc1"], fp8(inter["dz"].T, act["u2"].T), 1e-5),
+        "d_w_o": (g["w_o"], fp8(inter["dx1"].T, act["ctx"].T), 1e-5),
+        "d_w_qkv": (g["w_qkv"], fp8(inter["dqkv"].T, act["u1"].T), 1e-5),
+        # input gradients: dz = (dy W_fc2) GeLU'(z) and dctx = dx1 W_o stored in
+        # bf16; du1 = sum_p dqkv[:, Q_p] W_qkv[Q_p, :] in fp32
+        "dz": (inter["dz"], bf16(fp8(dyf, W["w_fc2"].T) * oracle.gelu_grad(act["z"])), 4e-3),
+        "dctx": (inter["dctx"], bf16(fp8(inter["dx1"], W["w_o"].T)), 4e-3),
+        "du1": (inter["du"], fp8(inter["dqkv"], W["w_qkv"].T, parts=t), 1e-5),
+    }
+    errs = {k: rel_err(got.reshape(want.shape), want) for k, (got, want, _) in checks.items()}
+    bad = {k: v for k, v in errs.items() if v > checks[k][2]}
+    assert not bad, (bad, errs)
