@@ -15,6 +15,7 @@ replica (the layer is not sharded across GPUs).
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -586,9 +587,13 @@ def main():
     mtl.layer_check(ws)
     torch.cuda.synchronize()
 
-    # ---- timed region: inputs resident in HBM
+    # ---- timed region: inputs resident in HBM.  Python's garbage collector is
+    # off inside the timed regions: a full collection pauses the launching
+    # thread for milliseconds, which the GPU sees as an idle gap.
     barrier()
     torch.cuda.synchronize()
+    gc.collect()
+    gc.disable()
     t_dev = time.monotonic()
     evs_step = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     evs_step[0].record(stream)
@@ -601,6 +606,7 @@ def main():
     barrier()
     ms = evs_step[0].elapsed_time(evs_step[-1])
     per_step = sorted(evs_step[i].elapsed_time(evs_step[i + 1]) for i in range(args.steps))
+    gc.enable()
     clk = clocks.window(t_dev, time.monotonic())
     mtl.layer_check(ws)
     flops = layer_flops(shape)
@@ -657,7 +663,9 @@ def main():
                 loaded[b].record(copy)
 
         io_in(0)
+        host = []
         for i in range(nsteps):
+            host.append(time.perf_counter())
             b = i % 2
             if i + 1 < nsteps:
                 io_in(i + 1)
@@ -676,15 +684,21 @@ def main():
                 dx_h[b].copy_(dxs[b], non_blocking=True)
                 tev["o1"][i].record(copy_out)
                 drained[b].record(copy_out)
+        host.append(time.perf_counter())
         e1.record(copy_out)
         e1.synchronize()
         torch.cuda.synchronize()
-        return e0.elapsed_time(e1), tev, e0
+        # longest host time to enqueue one step
+        host_ms = max(1e3 * (host[i + 1] - host[i]) for i in range(nsteps))
+        return e0.elapsed_time(e1), tev, e0, host_ms
 
     e2e_pass(3)                                      # untimed: wake up after the rest
     barrier()
+    gc.collect()
+    gc.disable()
     t_e2e = time.monotonic()
-    ms_e2e, tev, e0 = e2e_pass(args.steps)
+    ms_e2e, tev, e0, host_ms = e2e_pass(args.steps)
+    gc.enable()
     e2e_clk = clocks.window(t_e2e, time.monotonic())
     med = lambda v: sorted(v)[len(v) // 2]  # noqa: E731
     span = lambda a, b: [tev[a][i].elapsed_time(tev[b][i]) for i in range(args.steps)]  # noqa: E731
@@ -699,6 +713,7 @@ def main():
         "gap_ms_max": max(gaps) if gaps else 0.0,
         "gap_ms_mean": sum(gaps) / len(gaps) if gaps else 0.0,
         "device_only_step_ms_median": per_step[len(per_step) // 2],
+        "host_enqueue_ms_max": host_ms,
     }
     ms_e2e, e2e_value = aggregate_over_ranks(ms_e2e, flops, args.steps, world,
                                              dist if world > 1 else None, "cuda")

@@ -62,7 +62,10 @@
  *     MTL_ERR_UNSUPPORTED (valid layer outside what the kernels implement),
  *     MTL_ERR_WORKSPACE (ws_bytes too small), MTL_ERR_CUDA (a CUDA call or launch
  *     failed; see mtl_last_cuda_error), MTL_ERR_TIMEOUT (a device-side bounded
- *     wait gave up; reported by mtl_layer_check).
+ *     wait gave up; reported by mtl_layer_check), MTL_ERR_BOUNDS (a library
+ *     built with MTL_DEBUG found a computed TMA coordinate or output index
+ *     outside its tensor and skipped that access; reported by mtl_layer_check,
+ *     with the fault and call site in mtl_last_cuda_error).
  */
 #ifndef MTL_H_
 #define MTL_H_
@@ -82,7 +85,8 @@ typedef enum {
   MTL_ERR_UNSUPPORTED = 2,
   MTL_ERR_WORKSPACE = 3,
   MTL_ERR_CUDA = 4,
-  MTL_ERR_TIMEOUT = 5
+  MTL_ERR_TIMEOUT = 5,
+  MTL_ERR_BOUNDS = 6
 } mtl_status;
 
 typedef enum { MTL_F32 = 0, MTL_BF16 = 1 } mtl_dtype;

@@ -93,6 +93,16 @@ __device__ __forceinline__ unsigned long long drop_row(const Params& p, int b, i
   return (((unsigned long long)b * p.heads + hd) * p.seq + i) * (unsigned long long)p.seq;
 }
 
+// A TMA load of one 64 x 128 box of a bf16 activation with `cols` x `rows`
+// elements (qkv: 3h x n; ctx and dctx: h x n), its coordinates checked in
+// MTL_DEBUG builds.
+__device__ __forceinline__ void load_box(uint32_t dst, const CUtensorMap* m, uint32_t bar, int x,
+                                         int y, int64_t cols, int64_t rows, unsigned* status,
+                                         uint32_t site) {
+  const bounds::Box2 b = {cols, rows, 64, 128, 2};
+  if (MTL_CHECKED(status, bounds::check_tma_load(b, x, y), site)) tma_load_2d(dst, m, bar, x, y);
+}
+
 struct Smem {
   uint8_t* base;
   uint32_t u32;
@@ -255,8 +265,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
           }
           mbar_arrive_expect_tx(B(QF + x), TILE);
           for (int a = 0; a < NA; ++a)
-            tma_load_2d(sQ0 + x * TILE + a * ATOM128, &tm, B(QF + x), colq + 64 * a,
-                        row0 + it.qp * 256 + x * 128);
+            load_box(sQ0 + x * TILE + a * ATOM128, &tm, B(QF + x), colq + 64 * a,
+                     row0 + it.qp * 256 + x * 128, 3 * (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnFwdQ);
         }
         const int nkv = it.n0 > it.n1 ? it.n0 : it.n1;
         for (int j = 0; j < nkv && ok; ++j) {
@@ -268,8 +278,9 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             }
             mbar_arrive_expect_tx(B(RF + s), TILE);
             for (int a = 0; a < NA; ++a)
-              tma_load_2d(sR0 + s * TILE + a * ATOM128, &tm, B(RF + s),
-                          colq + (1 + kv) * p.d + 64 * a, row0 + j * 128);
+              load_box(sR0 + s * TILE + a * ATOM128, &tm, B(RF + s),
+                       colq + (1 + kv) * p.d + 64 * a, row0 + j * 128, 3 * (int64_t)p.h, (int64_t)p.batch * p.seq, p.status,
+                       bounds::kSiteAttnFwdKV);
           }
         }
       }
@@ -389,6 +400,12 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     auto epilogue = [&]() {
       const float inv = (DROP ? p.drop.scale : 1.0f) / pl;
       bf16* orow = p.ctx + po;
+      // the row's head slice lies inside ctx [n][h], its lse inside [batch][heads][seq]
+      if (!MTL_CHECKED(p.status,
+                       bounds::check_index((int64_t)(po + D - 1), (int64_t)p.batch * p.seq * p.h) |
+                           bounds::check_index((int64_t)plse, (int64_t)p.batch * p.heads * p.seq),
+                       bounds::kSiteAttnFwdOut))
+        return;
 #pragma unroll 1
       for (int c = 0; c < D; c += 32) {   // one 32-column chunk live at a time
         uint32_t v[32];
@@ -742,9 +759,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         ++nit;
         mbar_arrive_expect_tx(B(QF), 3 * TILE);
         for (int a = 0; a < NA; ++a) {
-          tma_load_2d(sQ + a * ATOM128, &tm, B(QF), colq + 64 * a, row0 + it.blk * 128);
-          tma_load_2d(sDO + a * ATOM128, &tmdo, B(QF), it.hd * p.d + 64 * a, row0 + it.blk * 128);
-          tma_load_2d(sO + a * ATOM128, &tmo, B(QF), it.hd * p.d + 64 * a, row0 + it.blk * 128);
+          load_box(sQ + a * ATOM128, &tm, B(QF), colq + 64 * a, row0 + it.blk * 128, 3 * (int64_t)p.h, (int64_t)p.batch * p.seq, p.status,
+                   bounds::kSiteAttnDqLoad);
+          load_box(sDO + a * ATOM128, &tmdo, B(QF), it.hd * p.d + 64 * a, row0 + it.blk * 128,
+                   (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnDqLoad);
+          load_box(sO + a * ATOM128, &tmo, B(QF), it.hd * p.d + 64 * a, row0 + it.blk * 128,
+                   (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnDqLoad);
         }
         for (int j = 0; j <= it.blk && ok; ++j) {
           for (int kv = 0; kv < 2; ++kv, ++g) {
@@ -755,8 +775,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             }
             mbar_arrive_expect_tx(B(RF + s), TILE);
             for (int a = 0; a < NA; ++a)
-              tma_load_2d(sR0 + s * TILE + a * ATOM128, &tm, B(RF + s),
-                          colq + (1 + kv) * p.d + 64 * a, row0 + j * 128);
+              load_box(sR0 + s * TILE + a * ATOM128, &tm, B(RF + s),
+                       colq + (1 + kv) * p.d + 64 * a, row0 + j * 128, 3 * (int64_t)p.h, (int64_t)p.batch * p.seq, p.status,
+                       bounds::kSiteAttnDqKV);
           }
         }
       }
@@ -838,7 +859,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     bool pend = false;
     bf16* pdq = nullptr;                       // dQ row of the item not yet written out
     auto epilogue = [&]() {
-      // warpgroup wg writes 32-column chunks wg, wg + 2, ...
+      // warpgroup wg writes 32-column chunks wg, wg + 2, ... of the row's dQ,
+      // inside dqkv [n][3h]
+      if (!MTL_CHECKED(p.status,
+                       bounds::check_index((int64_t)(pdq - p.dqkv) + D - 1,
+                                           (int64_t)p.batch * p.seq * 3 * p.h),
+                       bounds::kSiteAttnDqOut))
+        return;
 #pragma unroll 1
       for (int c = 32 * wg; c < D; c += 64) store_acc32(tmem + TQ_ACC + lane_off + c, p.scale, pdq + c);
     };
@@ -1037,9 +1064,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         ++nit;
         mbar_arrive_expect_tx(B(KVF), 2 * TILE);
         for (int a = 0; a < NA; ++a) {
-          tma_load_2d(sK + a * ATOM128, &tm, B(KVF), colq + p.d + 64 * a, row0 + it.blk * 128);
-          tma_load_2d(sV + a * ATOM128, &tm, B(KVF), colq + 2 * p.d + 64 * a,
-                      row0 + it.blk * 128);
+          load_box(sK + a * ATOM128, &tm, B(KVF), colq + p.d + 64 * a, row0 + it.blk * 128,
+                   3 * (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnDkvLoad);
+          load_box(sV + a * ATOM128, &tm, B(KVF), colq + 2 * p.d + 64 * a, row0 + it.blk * 128,
+                   3 * (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnDkvLoad);
         }
         for (int i = it.blk; i < p.nqb && ok; ++i) {
           for (int qd = 0; qd < 2; ++qd, ++g) {
@@ -1052,16 +1080,16 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
               // Q(i) with the lse and D of its queries
               mbar_arrive_expect_tx(B(RF + s), TILE + 1024);
               for (int a = 0; a < NA; ++a)
-                tma_load_2d(sR0 + s * TILE + a * ATOM128, &tm, B(RF + s), colq + 64 * a,
-                            row0 + i * 128);
+                load_box(sR0 + s * TILE + a * ATOM128, &tm, B(RF + s), colq + 64 * a,
+                         row0 + i * 128, 3 * (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnDkvQ);
               const size_t lo = ((size_t)it.b * p.heads + it.hd) * p.seq + (size_t)i * 128;
               bulk_load(s_ld_u32 + (s >> 1) * 1024, p.lse + lo, 512, B(RF + s));
               bulk_load(s_ld_u32 + (s >> 1) * 1024 + 512, p.dsum + lo, 512, B(RF + s));
             } else {
               mbar_arrive_expect_tx(B(RF + s), TILE);
               for (int a = 0; a < NA; ++a)
-                tma_load_2d(sR0 + s * TILE + a * ATOM128, &tmdo, B(RF + s), it.hd * p.d + 64 * a,
-                            row0 + i * 128);
+                load_box(sR0 + s * TILE + a * ATOM128, &tmdo, B(RF + s), it.hd * p.d + 64 * a,
+                         row0 + i * 128, (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnDkvQ);
             }
           }
         }
@@ -1158,6 +1186,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const uint32_t src = tmem + (wg == 0 ? TK_DK : TK_DV) + lane_off;
       bf16* dst = pout + (wg == 0 ? 0 : D);
       const float sc = wg == 0 ? p.scale : 1.0f;
+      if (!MTL_CHECKED(p.status,
+                       bounds::check_index((int64_t)(dst - p.dqkv) + D - 1,
+                                           (int64_t)p.batch * p.seq * 3 * p.h),
+                       bounds::kSiteAttnDkvOut))
+        return;
 #pragma unroll 1
       for (int c = 0; c < D; c += 32) store_acc32(src + c, sc, dst + c);
     };

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "bounds.h"
 #include "kernels.h"
 
 namespace mtl {
@@ -16,6 +17,24 @@ namespace mtl {
 // codes into it, the host reads it in mtl_layer_check.
 constexpr unsigned kDevErrTimeout = 1u;
 constexpr unsigned kDevErrBadArg = 2u;
+constexpr unsigned kDevErrBounds = bounds::kStatusBoundsFlag;   // MTL_DEBUG builds
+
+// Coordinate checks of builds with MTL_DEBUG: MTL_CHECKED(status, fault, site)
+// records a failed check (fault != 0) in the status word and is false, so the
+// caller skips the access; without MTL_DEBUG it is `true` and the check is not
+// compiled.
+__device__ __forceinline__ bool dcheck(unsigned* status, uint32_t fault, uint32_t site) {
+  if (fault != bounds::kOk) {
+    atomicOr(status, bounds::status_bits(fault, site));
+    return false;
+  }
+  return true;
+}
+#ifdef MTL_DEBUG
+#define MTL_CHECKED(status, fault, site) ::mtl::dcheck((status), (fault), (site))
+#else
+#define MTL_CHECKED(status, fault, site) true
+#endif
 // Words of the same 256-byte status block (zeroed by every API call) that the
 // persistent attention kernels use as work counters {next item, CTAs done};
 // the last CTA of a launch sets its pair back to zero.

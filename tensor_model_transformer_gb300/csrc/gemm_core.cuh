@@ -335,8 +335,13 @@ __device__ __forceinline__ void epi_chunk_tma(const Params& p, int row0, int col
   fence_proxy_async_shared();
   __syncwarp();
   if (lane == 0) {
-    tma_store_2d(tmC, stage, col0, row0);
-    if (EPI == EPI_BIAS_GELU) tma_store_2d(tmZ, stage + 2048, col0, row0);
+    const bounds::Box2 boxc = {p.N, p.M, 32, 32, OUT_F32 ? 4 : 2};
+    if (MTL_CHECKED(p.status, bounds::check_tma_store(boxc, col0, row0), bounds::kSiteGemmC))
+      tma_store_2d(tmC, stage, col0, row0);
+    const bounds::Box2 boxz = {p.N, p.M, 32, 32, 2};
+    if (EPI == EPI_BIAS_GELU &&
+        MTL_CHECKED(p.status, bounds::check_tma_store(boxz, col0, row0), bounds::kSiteGemmZ))
+      tma_store_2d(tmZ, stage + 2048, col0, row0);
     bulk_commit();
   }
   if (EPI == EPI_DGELU && p.csum) {
@@ -701,14 +706,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           const uint32_t sa = sA0 + stage * P_A_BYTES, sb = sB0 + stage * P_B_BYTES;
 #pragma unroll
           for (int j = 0; j < P_NBOX; ++j) {
-            if (F8 || !p.a_mn)
-              tma_load_2d_pair(sa + j * P_ATOM, &tmA, fb, k0 + 64 * j, m0);
-            else
-              tma_load_2d_pair(sa + j * P_ATOM, &tmA, fb, m0 + 64 * j, k0);
-            if (F8 || !p.b_mn)
-              tma_load_2d_pair(sb + j * P_ATOM, &tmB, fb, k0 + 64 * j, n0);
-            else
-              tma_load_2d_pair(sb + j * P_ATOM, &tmB, fb, n0 + 64 * j, k0);
+            // K-major boxes: 64 K (128 bytes of FP8) x 128 rows; MN-major: 64 M
+            // or N x 128 K
+            const bool ak = F8 || !p.a_mn, bk = F8 || !p.b_mn;
+            const int ax = ak ? k0 + 64 * j : m0 + 64 * j, ay = ak ? m0 : k0;
+            const int bx = bk ? k0 + 64 * j : n0 + 64 * j, by = bk ? n0 : k0;
+            const bounds::Box2 boxa = {ak ? p.K : p.M, ak ? p.M : p.K, F8 ? 128 : 64, 128,
+                                       F8 ? 1 : 2};
+            const bounds::Box2 boxb = {bk ? p.K : p.N, bk ? p.N : p.K, F8 ? 128 : 64, 128,
+                                       F8 ? 1 : 2};
+            if (MTL_CHECKED(p.status, bounds::check_tma_load(boxa, ax, ay), bounds::kSiteGemmA))
+              tma_load_2d_pair(sa + j * P_ATOM, &tmA, fb, ax, ay);
+            if (MTL_CHECKED(p.status, bounds::check_tma_load(boxb, bx, by), bounds::kSiteGemmB))
+              tma_load_2d_pair(sb + j * P_ATOM, &tmB, fb, bx, by);
           }
           if (++stage == P_STAGES) {
             stage = 0;

@@ -113,17 +113,32 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
           const int k0 = kb * BK;
           const uint32_t sa = sA0 + stage * A_BYTES, sb = sB0 + stage * B_BYTES;
+          // K-major: one 64 (K) x BM / BN box; MN-major: 64 x 64 (K) boxes
           if (!p.a_mn) {
-            tma_load_2d(sa, &tmA, fb, k0, mb * BM);
+            const bounds::Box2 b = {p.K, p.M, BK, BM, 2};
+            if (MTL_CHECKED(p.status, bounds::check_tma_load(b, k0, mb * BM), bounds::kSiteGemmA))
+              tma_load_2d(sa, &tmA, fb, k0, mb * BM);
           } else {
 #pragma unroll
-            for (int j = 0; j < BM / 64; ++j) tma_load_2d(sa + j * (BK * 128), &tmA, fb, mb * BM + 64 * j, k0);
+            for (int j = 0; j < BM / 64; ++j) {
+              const bounds::Box2 b = {p.M, p.K, 64, BK, 2};
+              if (MTL_CHECKED(p.status, bounds::check_tma_load(b, mb * BM + 64 * j, k0),
+                              bounds::kSiteGemmA))
+                tma_load_2d(sa + j * (BK * 128), &tmA, fb, mb * BM + 64 * j, k0);
+            }
           }
           if (!p.b_mn) {
-            tma_load_2d(sb, &tmB, fb, k0, nb * BN);
+            const bounds::Box2 b = {p.K, p.N, BK, BN, 2};
+            if (MTL_CHECKED(p.status, bounds::check_tma_load(b, k0, nb * BN), bounds::kSiteGemmB))
+              tma_load_2d(sb, &tmB, fb, k0, nb * BN);
           } else {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * (BK * 128), &tmB, fb, nb * BN + 64 * j, k0);
+            for (int j = 0; j < BN / 64; ++j) {
+              const bounds::Box2 b = {p.N, p.K, 64, BK, 2};
+              if (MTL_CHECKED(p.status, bounds::check_tma_load(b, nb * BN + 64 * j, k0),
+                              bounds::kSiteGemmB))
+                tma_load_2d(sb + j * (BK * 128), &tmB, fb, nb * BN + 64 * j, k0);
+            }
           }
           if (++stage == STAGES) {
             stage = 0;

@@ -705,6 +705,7 @@ const char* mtl_status_str(mtl_status s) {
     case MTL_ERR_WORKSPACE: return "workspace too small";
     case MTL_ERR_CUDA: return "CUDA error";
     case MTL_ERR_TIMEOUT: return "device wait timed out";
+    case MTL_ERR_BOUNDS: return "device bounds check failed";
   }
   return "unknown status";
 }
@@ -1165,6 +1166,13 @@ mtl_status mtl_layer_check(void* workspace, mtl_stream stream) {
   if (word) {
     unsigned zero = 0;
     cudaMemcpy(workspace, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+  }
+  if (word & kDevErrBounds) {
+    // a skipped access usually also leaves a bounded wait to time out: the
+    // bounds fault is the cause, so it is reported first
+    snprintf(g_cuda_err, sizeof(g_cuda_err), "bounds check: fault %u at site %u (word 0x%08x)",
+             (word >> 8) & 0xFu, (word >> 16) & 0xFFu, word);
+    return MTL_ERR_BOUNDS;
   }
   if (word & kDevErrTimeout) return MTL_ERR_TIMEOUT;
   if (word) return MTL_ERR_INVALID_ARG;

@@ -17,9 +17,12 @@ SAVED_NAMES = ("mu1", "rstd1", "u1", "qkv", "ctx", "lse", "x1", "mu2", "rstd2", 
 
 F32, BF16 = 0, 1
 STATUS = {0: "MTL_OK", 1: "MTL_ERR_INVALID_ARG", 2: "MTL_ERR_UNSUPPORTED",
-          3: "MTL_ERR_WORKSPACE", 4: "MTL_ERR_CUDA", 5: "MTL_ERR_TIMEOUT"}
+          3: "MTL_ERR_WORKSPACE", 4: "MTL_ERR_CUDA", 5: "MTL_ERR_TIMEOUT", 6: "MTL_ERR_BOUNDS"}
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmtl.so")
+# The library to load: the in-tree build, or another build of it named by
+# MTL_LIBRARY (e.g. the MTL_DEBUG build, libmtl_debug.so).
+LIB_PATH = os.environ.get("MTL_LIBRARY") or os.path.join(
+    os.path.dirname(os.path.abspath(__file__)), "libmtl.so")
 
 
 class MtlError(RuntimeError):
@@ -117,7 +120,7 @@ def lib():
 
 def _check(status: int, where: str):
     if status != 0:
-        detail = lib().mtl_last_cuda_error().decode() if status == 4 else ""
+        detail = lib().mtl_last_cuda_error().decode() if status in (4, 6) else ""
         raise MtlError(status, where, detail)
 
 

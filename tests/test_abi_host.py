@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(mtl):
 
 
 def test_status_strings(mtl):
-    for s in range(6):
+    for s in range(7):
         assert mtl.lib().mtl_status_str(s)
 
 
