@@ -176,6 +176,93 @@ __global__ void __launch_bounds__(kLnThreadsMax, V == 1 ? 4 : 1)   // short rows
   }
 }
 
+// One warp per row, for rows of at most kLnWarpMaxVec 16-byte vectors a lane:
+// lane l holds vectors l, l + 32, ... of the row (each load instruction of the
+// warp covers 512 contiguous bytes), so a whole row's loads are in flight at
+// once and both reductions are warp shuffles, with no block barrier.  The
+// arithmetic per element is ln_fwd_kernel's: the mean, then the centred second
+// moment, and the output expression ln_apply_kernel uses to rebuild u bit for
+// bit from the saved statistics.
+constexpr int kLnWarpMaxVec = 16;
+constexpr int kLnWarpThreads = 256;
+template <typename T, int VL, bool AMAX>
+__global__ void __launch_bounds__(kLnWarpThreads)
+    ln_fwd_warp_kernel(const T* __restrict__ x, const T* __restrict__ gamma,
+                       const T* __restrict__ beta, T* __restrict__ u, float* __restrict__ mean_out,
+                       float* __restrict__ rstd_out, int n, int h, float eps,
+                       unsigned* __restrict__ amax_bits) {
+  constexpr int E = Vec<T>::N;
+  griddep_wait();   // no-op unless launched as a programmatic dependent
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  const int nvec = h / E;
+  const float inv_h = 1.0f / (float)h;
+  float umax = 0.f;
+  for (int r = blockIdx.x * wpb + (threadIdx.x >> 5); r < n; r += gridDim.x * wpb) {
+    Vec<T> xv[VL];
+#pragma unroll
+    for (int i = 0; i < VL; ++i)
+      if (lane + 32 * i < nvec) xv[i].load(x + (size_t)r * h + (lane + 32 * i) * E);
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < VL; ++i) {
+      if (lane + 32 * i < nvec) {
+        float f[E];
+        xv[i].unpack(f);
+#pragma unroll
+        for (int e = 0; e < E; ++e) s += f[e];
+      }
+    }
+    const float mean = warp_sum(s) * inv_h;
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < VL; ++i) {
+      if (lane + 32 * i < nvec) {
+        float f[E];
+        xv[i].unpack(f);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const float dlt = f[e] - mean;
+          ss += dlt * dlt;
+        }
+      }
+    }
+    ss = warp_sum(ss);
+    const float rs = 1.0f / sqrtf(ss * inv_h + eps);
+#pragma unroll
+    for (int i = 0; i < VL; ++i) {
+      const int vi = lane + 32 * i;
+      if (vi >= nvec) continue;
+      float f[E], gv[E], bv[E], of[E];
+      xv[i].unpack(f);
+      Vec<T> tg, tb;
+      tg.load(gamma + vi * E);
+      tb.load(beta + vi * E);
+      tg.unpack(gv);
+      tb.unpack(bv);
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        of[e] = (f[e] - mean) * rs * gv[e] + bv[e];
+        if (AMAX) umax = fmaxf(umax, fabsf(of[e]));
+      }
+      Vec<T> o;
+      o.pack(of);
+      o.store(u + (size_t)r * h + vi * E);
+    }
+    if (lane == 0) {
+      mean_out[r] = mean;
+      rstd_out[r] = rs;
+    }
+  }
+  if (AMAX) {
+    // max |u| of the stored values: rounding to T is monotone and symmetric,
+    // so the rounded maximum is the maximum of the rounded values
+    umax = warp_max(umax);
+    if (lane == 0) atomicMax(amax_bits, __float_as_uint(Vec<T>::round(umax)));
+  }
+}
+
 // Each block sums du * xhat and du over its rows for the dgamma / dbeta
 // partials; a thread owns the same columns in every row, so the sums need no
 // atomics and keep row order.  Short rows (V <= 2) keep those sums and gamma in
@@ -562,6 +649,33 @@ cudaError_t ln_fwd_t(const void* x, const void* g, const void* b, void* u, float
                      float* rstd, int n, int h, float eps, const LaunchCtx& c,
                      unsigned* amax_bits) {
   if (n == 0) return cudaSuccess;
+  const int vl = (h / Vec<T>::N + 31) / 32;   // vectors a lane with one warp a row
+  if (vl <= kLnWarpMaxVec) {
+    const int wpb = kLnWarpThreads / 32;
+    const int wgrid = (n + wpb - 1) / wpb;
+    c.before(KK_LN_FWD, (double)n * h * (2.0 * sizeof(T)) + 8.0 * n);
+    cudaError_t we = cudaSuccess;
+#define LN_FWD_WARP(VV)                                                                       \
+  if (vl <= VV) {                                                                           \
+    we = amax_bits ? launch_ex(c, ln_fwd_warp_kernel<T, VV, true>, dim3(wgrid),               \
+                               dim3(kLnWarpThreads), 0, 1, (const T*)x, (const T*)g,          \
+                               (const T*)b, (T*)u, mean, rstd, n, h, eps, amax_bits)          \
+                   : launch_ex(c, ln_fwd_warp_kernel<T, VV, false>, dim3(wgrid),              \
+                               dim3(kLnWarpThreads), 0, 1, (const T*)x, (const T*)g,          \
+                               (const T*)b, (T*)u, mean, rstd, n, h, eps, amax_bits);         \
+  } else
+    LN_FWD_WARP(1)
+    LN_FWD_WARP(2)
+    LN_FWD_WARP(4)
+    LN_FWD_WARP(8)
+    LN_FWD_WARP(12)
+    LN_FWD_WARP(16)
+    {}
+#undef LN_FWD_WARP
+    c.after();
+    if (we != cudaSuccess) return we;
+    return cudaGetLastError();
+  }
   int vpt, threads;
   row_plan<T>(h, &vpt, &threads);
   const int rows = n >= 4 * c.num_sms * 4 ? 4 : 1;
