@@ -345,21 +345,36 @@ __device__ __forceinline__ void epi_chunk_tma(const Params& p, int row0, int col
     bulk_commit();
   }
   if (EPI == EPI_DGELU && p.csum) {
-    // column sums of the chunk as stored: lane l adds column l over the 32
-    // rows of the staging buffer (rows past M hold zeros: their A rows read
-    // as zero), in row order
-    float cs = 0.f;
+    // column sums of the chunk as stored, from the staging buffer (rows past M
+    // hold zeros: their A rows read as zero)
     if (OUT_F32) {
+      // lane l adds column l over the 32 rows, in row order
+      float cs = 0.f;
 #pragma unroll
       for (int r = 0; r < 32; ++r)
         cs += ld_shared_f32(stage + r * 128 + ((((lane >> 2) ^ (r & 7))) << 4) + (lane & 3) * 4);
+      p.csum[(size_t)(row0 >> 5) * p.N + col0 + lane] = cs;
     } else {
+      // lane l adds the column pair cp = l % 16 (one 32-bit word of two bf16)
+      // over the even rows (l < 16) or the odd rows (l >= 16), in row order --
+      // an even and an odd row of the 64-byte-swizzled staging tile lie in
+      // opposite halves of the banks -- then the two halves are added
+      const int cp = lane & 15, odd = lane >> 4;
+      float c0 = 0.f, c1 = 0.f;
 #pragma unroll
-      for (int r = 0; r < 32; ++r)
-        cs += ld_shared_bf16(stage + r * 64 + ((((lane >> 3) ^ ((r >> 1) & 3))) << 4) +
-                             (lane & 7) * 2);
+      for (int i = 0; i < 16; ++i) {
+        const int r = 2 * i + odd;
+        const uint32_t w =
+            ld_shared_u32(stage + r * 64 + (((cp >> 2) ^ ((r >> 1) & 3)) << 4) + (cp & 3) * 4);
+        c0 += __uint_as_float(w << 16);
+        c1 += __uint_as_float(w & 0xffff0000u);
+      }
+      c0 += __shfl_xor_sync(0xffffffffu, c0, 16);
+      c1 += __shfl_xor_sync(0xffffffffu, c1, 16);
+      if (!odd)
+        *reinterpret_cast<float2*>(p.csum + (size_t)(row0 >> 5) * p.N + col0 + 2 * cp) =
+            make_float2(c0, c1);
     }
-    p.csum[(size_t)(row0 >> 5) * p.N + col0 + lane] = cs;
   }
 }
 
