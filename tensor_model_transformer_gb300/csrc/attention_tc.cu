@@ -256,33 +256,37 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         if (k >= n_items) break;
         const FwdItem it = fwd_item(p, k);
         const int colq = it.hd * 3 * p.d, row0 = it.b * p.seq;
-        for (int x = 0; x < 2 && ok; ++x) {
-          if (!it.n(x)) continue;
+        const int64_t cols = 3 * (int64_t)p.h, rows = (int64_t)p.batch * p.seq;
+        auto load_q = [&](int x) -> bool {
           const int nq = x ? nit1++ : nit0++;
-          if (nq > 0 && !mbar_wait_bounded(B(QE + x), (nq - 1) & 1, p.status, abort_flag)) {
-            ok = false;
-            break;
-          }
+          if (nq > 0 && !mbar_wait_bounded(B(QE + x), (nq - 1) & 1, p.status, abort_flag))
+            return false;
           mbar_arrive_expect_tx(B(QF + x), TILE);
           for (int a = 0; a < NA; ++a)
             load_box(sQ0 + x * TILE + a * ATOM128, &tm, B(QF + x), colq + 64 * a,
-                     row0 + it.qp * 256 + x * 128, 3 * (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnFwdQ);
-        }
-        const int nkv = it.n0 > it.n1 ? it.n0 : it.n1;
-        for (int j = 0; j < nkv && ok; ++j) {
+                     row0 + it.qp * 256 + x * 128, cols, rows, p.status, bounds::kSiteAttnFwdQ);
+          return true;
+        };
+        auto load_kv = [&](int j) -> bool {   // K(j) and V(j) into the next two ring slots
           for (int kv = 0; kv < 2; ++kv, ++g) {
             const int s = g % FWD_RING, use = g / FWD_RING;
-            if (use > 0 && !mbar_wait_bounded(B(RE + s), (use - 1) & 1, p.status, abort_flag)) {
-              ok = false;
-              break;
-            }
+            if (use > 0 && !mbar_wait_bounded(B(RE + s), (use - 1) & 1, p.status, abort_flag))
+              return false;
             mbar_arrive_expect_tx(B(RF + s), TILE);
             for (int a = 0; a < NA; ++a)
               load_box(sR0 + s * TILE + a * ATOM128, &tm, B(RF + s),
-                       colq + (1 + kv) * p.d + 64 * a, row0 + j * 128, 3 * (int64_t)p.h, (int64_t)p.batch * p.seq, p.status,
+                       colq + (1 + kv) * p.d + 64 * a, row0 + j * 128, cols, rows, p.status,
                        bounds::kSiteAttnFwdKV);
           }
-        }
+          return true;
+        };
+        // Tile A's Q, the first K / V block, then tile B's Q: the previous
+        // item's last Q K^T (tile B's) frees B's Q buffer only at the end of
+        // that item, and this item's first product (tile A's) needs just Q_A
+        // and K(0), which thus load while the previous item finishes.
+        const int nkv = it.n0 > it.n1 ? it.n0 : it.n1;
+        ok = load_q(0) && load_kv(0) && (!it.n1 || load_q(1));
+        for (int j = 1; j < nkv && ok; ++j) ok = load_kv(j);
       }
       // the last CTA out leaves the counters at zero for the next launch
       __threadfence();
