@@ -100,6 +100,7 @@ __device__ __forceinline__ void load_box(uint32_t dst, const CUtensorMap* m, uin
                                          int y, int64_t cols, int64_t rows, unsigned* status,
                                          uint32_t site) {
   const bounds::Box2 b = {cols, rows, 64, 128, 2};
+  (void)b;
   if (MTL_CHECKED(status, bounds::check_tma_load(b, x, y), site)) tma_load_2d(dst, m, bar, x, y);
 }
 
@@ -112,6 +113,43 @@ __device__ __forceinline__ Smem smem_aligned(uint8_t* raw) {
   uint8_t* p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) &
                                           ~static_cast<uintptr_t>(1023));
   return {p, smem_u32(p)};
+}
+
+// Epilogue stores.  A warp's 32 rows (lane = row) of an output tile go to
+// global memory 32 columns at a time through 2 KB of shared memory per warp:
+// each lane writes its row's 64 bytes there, then a store instruction takes
+// 8 rows x 64 contiguous bytes (lane -> row 8q + lane / 4, 16-byte piece
+// lane % 4), a quarter of the cache lines a lane-per-row store touches.  The
+// pieces are swizzled by row (piece ^ ((row / 2) % 4)) so that both the
+// row-wise writes and the piece-wise reads take four shared-memory wavefronts.
+constexpr uint32_t STAGE_WARP_BYTES = 32 * 64;
+constexpr uint32_t STAGE_BYTES = 8 * STAGE_WARP_BYTES;   // the eight row warps
+
+__device__ __forceinline__ uint32_t stage_off(int row, int piece) {
+  return (uint32_t)(row * 64 + ((piece ^ ((row >> 1) & 3)) << 4));
+}
+
+// 32 fp32 TMEM columns at taddr (this lane's row), times sc, as bf16 to
+// dst0 + r * ld for the warp's rows r = 0..31 (dst0: the warp's first row).
+__device__ __forceinline__ void store_acc32_staged(uint32_t taddr, float sc, bf16* dst0, size_t ld,
+                                                   uint32_t stage, int lane) {
+  uint32_t v[32];
+  tmem_ld32(taddr, v);
+  tmem_ld_wait();
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    st_shared_v4(stage + stage_off(lane, q),
+                 pack_bf16x2(__uint_as_float(v[q * 8 + 0]) * sc, __uint_as_float(v[q * 8 + 1]) * sc),
+                 pack_bf16x2(__uint_as_float(v[q * 8 + 2]) * sc, __uint_as_float(v[q * 8 + 3]) * sc),
+                 pack_bf16x2(__uint_as_float(v[q * 8 + 4]) * sc, __uint_as_float(v[q * 8 + 5]) * sc),
+                 pack_bf16x2(__uint_as_float(v[q * 8 + 6]) * sc, __uint_as_float(v[q * 8 + 7]) * sc));
+  __syncwarp();
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int rr = 8 * q + (lane >> 2), pc = lane & 3;
+    *reinterpret_cast<uint4*>(dst0 + (size_t)rr * ld + pc * 8) = ld_shared_v4(stage + stage_off(rr, pc));
+  }
+  __syncwarp();   // the buffer is free for the next chunk
 }
 
 // ============================================================================ forward
@@ -214,6 +252,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
   constexpr int QF = 0, QE = 2, RF = 4, RE = RF + FWD_RING, SF = RE + FWD_RING, SE = SF + 2,
                 PF = SE + 1, PE = PF + 2, IF = PE + 2, IE = IF + 2, NBAR = IE + 2;
   constexpr int ROW_WARPS = FWD_THREADS / 32 - 4;
+  const uint32_t sStage = smem_u32(bars) + 256;          // epilogue staging, 2 KB a row warp
   int* s_item = reinterpret_cast<int*>(bars + NBAR);   // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_item + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -401,30 +440,20 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     bool pend = false;
     float pm = 0.f, pl = 1.f;
     size_t po = 0, plse = 0;       // ctx offset of the row's head slice, lse index
+    const uint32_t stage = sStage + (warp - 4) * STAGE_WARP_BYTES;
     auto epilogue = [&]() {
       const float inv = (DROP ? p.drop.scale : 1.0f) / pl;
-      bf16* orow = p.ctx + po;
       // the row's head slice lies inside ctx [n][h], its lse inside [batch][heads][seq]
-      if (!MTL_CHECKED(p.status,
-                       bounds::check_index((int64_t)(po + D - 1), (int64_t)p.batch * p.seq * p.h) |
-                           bounds::check_index((int64_t)plse, (int64_t)p.batch * p.heads * p.seq),
-                       bounds::kSiteAttnFwdOut))
+      // (the warp stores its rows together: it skips them all if one fails)
+      if (!__all_sync(0xffffffffu,
+                      MTL_CHECKED(p.status,
+                                  bounds::check_index((int64_t)(po + D - 1), (int64_t)p.batch * p.seq * p.h) |
+                                      bounds::check_index((int64_t)plse, (int64_t)p.batch * p.heads * p.seq),
+                                  bounds::kSiteAttnFwdOut)))
         return;
+      bf16* orow0 = p.ctx + po - (size_t)lane * p.h;   // the warp's first row
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) {   // one 32-column chunk live at a time
-        uint32_t v[32];
-        tmem_ld32(tO + c, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]) * inv, __uint_as_float(v[q * 8 + 1]) * inv);
-          w.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]) * inv, __uint_as_float(v[q * 8 + 3]) * inv);
-          w.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]) * inv, __uint_as_float(v[q * 8 + 5]) * inv);
-          w.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]) * inv, __uint_as_float(v[q * 8 + 7]) * inv);
-          *reinterpret_cast<uint4*>(orow + c + q * 8) = w;
-        }
-      }
+      for (int c = 0; c < D; c += 32) store_acc32_staged(tO + c, inv, orow0 + c, p.h, stage, lane);
       p.lse[plse] = (pm + __log2f(pl)) * LN2;
     };
     bool ok = true;
@@ -654,22 +683,6 @@ __device__ __forceinline__ void sched_done(unsigned* sched) {
   }
 }
 
-// 32 x 32 TMEM columns of an fp32 accumulator, scaled, to 32 bf16 of a row.
-__device__ __forceinline__ void store_acc32(uint32_t taddr, float sc, bf16* dst) {
-  uint32_t v[32];
-  tmem_ld32(taddr, v);
-  tmem_ld_wait();
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 w;
-    w.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]) * sc, __uint_as_float(v[q * 8 + 1]) * sc);
-    w.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]) * sc, __uint_as_float(v[q * 8 + 3]) * sc);
-    w.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]) * sc, __uint_as_float(v[q * 8 + 5]) * sc);
-    w.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]) * sc, __uint_as_float(v[q * 8 + 7]) * sc);
-    *reinterpret_cast<uint4*>(dst + q * 8) = w;
-  }
-}
-
 // 64 bf16 (packed pairs) of a row into 32 TMEM columns.
 __device__ __forceinline__ void store_bf16_64(uint32_t taddr, const float (&v)[64]) {
 #pragma unroll
@@ -862,16 +875,22 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     int ni = 0, nb = 0, nit = 0;
     bool pend = false;
     bf16* pdq = nullptr;                       // dQ row of the item not yet written out
+    // the epilogue stages its stores in the O tile, which is free from the
+    // moment every row thread has formed D until the rows arrive on DE
+    const uint32_t stage = sO + (warp - 4) * STAGE_WARP_BYTES;
     auto epilogue = [&]() {
       // warpgroup wg writes 32-column chunks wg, wg + 2, ... of the row's dQ,
       // inside dqkv [n][3h]
-      if (!MTL_CHECKED(p.status,
-                       bounds::check_index((int64_t)(pdq - p.dqkv) + D - 1,
-                                           (int64_t)p.batch * p.seq * 3 * p.h),
-                       bounds::kSiteAttnDqOut))
+      if (!__all_sync(0xffffffffu,
+                      MTL_CHECKED(p.status,
+                                  bounds::check_index((int64_t)(pdq - p.dqkv) + D - 1,
+                                                      (int64_t)p.batch * p.seq * 3 * p.h),
+                                  bounds::kSiteAttnDqOut)))
         return;
+      bf16* dq0 = pdq - (size_t)lane * 3 * p.h;   // the warp's first row
 #pragma unroll 1
-      for (int c = 32 * wg; c < D; c += 64) store_acc32(tmem + TQ_ACC + lane_off + c, p.scale, pdq + c);
+      for (int c = 32 * wg; c < D; c += 64)
+        store_acc32_staged(tmem + TQ_ACC + lane_off + c, p.scale, dq0 + c, 3 * (size_t)p.h, stage, lane);
     };
     bool ok = true;
     while (ok) {
@@ -885,7 +904,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const int qb = it.blk;
       const int row = it.b * p.seq + qb * 128 + r;
       // D_r = dO_r . O_r from the tiles in shared memory (they are not reloaded
-      // before every row thread has arrived on DE below)
+      // before every row thread has arrived on DE, after the first block's
+      // epilogue)
       if (!mbar_wait_bounded(B(QF), nit & 1, p.status, abort_flag)) {
         ok = false;
         break;
@@ -904,7 +924,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 #pragma unroll
         for (int e = 0; e < 8; ++e) Dr = fmaf(gf[e], of[e], Dr);
       }
-      mbar_arrive(B(DE));
+      named_bar_sync(1, 256);                  // every row is done with the O tile
       const size_t lrow = ((size_t)it.b * p.heads + it.hd) * p.seq + qb * 128 + r;
       if (wg == 0) p.dsum[lrow] = Dr;
       const float lse2 = p.lse[lrow] * LOG2E;
@@ -937,9 +957,14 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             break;
           }
           tc_fence_after();
-          if (j == 0 && pend) {
-            epilogue();
-            pend = false;
+          if (j == 0) {
+            if (pend) {
+              epilogue();
+              pend = false;
+            }
+            // the next item's Q, dO and O may load over the staged stores
+            fence_proxy_async_shared();
+            mbar_arrive(B(DE));
           }
           const bool diag = j == qb;
           const float nl = -lse2;
@@ -1022,6 +1047,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   const uint32_t s_ld_u32 = smem_u32(s_ld);
   uint64_t* bars = reinterpret_cast<uint64_t*>(s_ld + 128 * BWD_RING);
   const uint32_t bar0 = smem_u32(bars);
+  const uint32_t sStage = bar0 + 256;          // epilogue staging, 2 KB a row warp
   auto B = [&](int i) { return bar0 + 8u * i; };
   constexpr int KVF = 0, KVE = 1, RF = 2, RE = RF + BWD_RING, SF = RE + BWD_RING, SE = SF + 1,
                 DPF = SE + 1, DPE = DPF + 1, PF = DPE + 1, PE = PF + 1, DSF = PE + 1,
@@ -1185,18 +1211,21 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     int ni = 0, nb = 0, g = 0;
     bool pend = false;
     bf16* pout = nullptr;                      // K part of the dqkv row not yet written out
+    const uint32_t stage = sStage + (warp - 4) * STAGE_WARP_BYTES;
     auto epilogue = [&]() {
       // warpgroup 0 writes dK (with the 1/sqrt(d) of S), warpgroup 1 dV
       const uint32_t src = tmem + (wg == 0 ? TK_DK : TK_DV) + lane_off;
       bf16* dst = pout + (wg == 0 ? 0 : D);
       const float sc = wg == 0 ? p.scale : 1.0f;
-      if (!MTL_CHECKED(p.status,
-                       bounds::check_index((int64_t)(dst - p.dqkv) + D - 1,
-                                           (int64_t)p.batch * p.seq * 3 * p.h),
-                       bounds::kSiteAttnDkvOut))
+      if (!__all_sync(0xffffffffu,
+                      MTL_CHECKED(p.status,
+                                  bounds::check_index((int64_t)(dst - p.dqkv) + D - 1,
+                                                      (int64_t)p.batch * p.seq * 3 * p.h),
+                                  bounds::kSiteAttnDkvOut)))
         return;
+      bf16* dst0 = dst - (size_t)lane * 3 * p.h;   // the warp's first row
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) store_acc32(src + c, sc, dst + c);
+      for (int c = 0; c < D; c += 32) store_acc32_staged(src + c, sc, dst0 + c, 3 * (size_t)p.h, stage, lane);
     };
     bool ok = true;
     while (ok) {
@@ -1392,7 +1421,7 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uin
 }
 
 size_t fwd_smem(int na) {
-  const size_t need = (size_t)(2 + FWD_RING) * na * ATOM128 + 256 + 1024;
+  const size_t need = (size_t)(2 + FWD_RING) * na * ATOM128 + 256 + STAGE_BYTES + 1024;
   return need < 120 * 1024 ? 120 * 1024 : need;   // one CTA per SM (512 TMEM columns)
 }
 // The backward kernels hold all 512 TMEM columns: their shared memory requests
@@ -1402,7 +1431,7 @@ size_t dq_smem(int na) {
   return need < 120 * 1024 ? 120 * 1024 : need;   // one CTA per SM (512 TMEM columns)
 }
 size_t dkv_smem(int na) {
-  const size_t need = (size_t)(2 + BWD_RING) * na * ATOM128 + 2048 + 256 + 1024;
+  const size_t need = (size_t)(2 + BWD_RING) * na * ATOM128 + 2048 + 256 + STAGE_BYTES + 1024;
   return need < 120 * 1024 ? 120 * 1024 : need;
 }
 
