@@ -115,13 +115,16 @@ __device__ __forceinline__ Smem smem_aligned(uint8_t* raw) {
   return {p, smem_u32(p)};
 }
 
-// Epilogue stores.  A warp's 32 rows (lane = row) of an output tile go to
-// global memory 32 columns at a time through 2 KB of shared memory per warp:
-// each lane writes its row's 64 bytes there, then a store instruction takes
-// 8 rows x 64 contiguous bytes (lane -> row 8q + lane / 4, 16-byte piece
-// lane % 4), a quarter of the cache lines a lane-per-row store touches.  The
-// pieces are swizzled by row (piece ^ ((row / 2) % 4)) so that both the
-// row-wise writes and the piece-wise reads take four shared-memory wavefronts.
+// Epilogue stores.  A warp's 32 rows (lane = row) of an output tile leave 32
+// columns at a time as TMA tensor stores of a 32 x 32 box: each lane writes
+// its row's 64 bytes into the warp's 2 KB staging buffer, in the 64-byte
+// swizzle the tensor map names (16-byte piece p of row r at r * 64 + ((p ^
+// ((r / 2) % 4)) * 16), which also keeps the row-wise writes at four
+// shared-memory wavefronts), and one lane issues the store.  The copy engine
+// writes global memory while the rows go on; a lane-per-row store of 16 bytes
+// from registers touched 32 cache lines per instruction and held the rows for
+// thousands of cycles an item.  Before a buffer is rewritten its previous
+// store must have read it (cp.async.bulk.wait_group.read).
 constexpr uint32_t STAGE_WARP_BYTES = 32 * 64;
 constexpr uint32_t STAGE_BYTES = 8 * STAGE_WARP_BYTES;   // the eight row warps
 
@@ -129,13 +132,16 @@ __device__ __forceinline__ uint32_t stage_off(int row, int piece) {
   return (uint32_t)(row * 64 + ((piece ^ ((row >> 1) & 3)) << 4));
 }
 
-// 32 fp32 TMEM columns at taddr (this lane's row), times sc, as bf16 to
-// dst0 + r * ld for the warp's rows r = 0..31 (dst0: the warp's first row).
-__device__ __forceinline__ void store_acc32_staged(uint32_t taddr, float sc, bf16* dst0, size_t ld,
-                                                   uint32_t stage, int lane) {
+// 32 fp32 TMEM columns at taddr (this lane's row), times sc, as bf16 to the
+// box of 32 columns x 32 rows at (x, y) of the tensor map m (y: the warp's
+// first row).  `stage` is the warp's buffer (1024-byte aligned pattern base).
+__device__ __forceinline__ void store_acc32_tma(uint32_t taddr, float sc, const CUtensorMap* m, int x,
+                                                int y, uint32_t stage, int lane) {
   uint32_t v[32];
   tmem_ld32(taddr, v);
   tmem_ld_wait();
+  if (lane == 0) bulk_wait_read0();   // the buffer's previous store has read it
+  __syncwarp();
 #pragma unroll
   for (int q = 0; q < 4; ++q)
     st_shared_v4(stage + stage_off(lane, q),
@@ -143,13 +149,23 @@ __device__ __forceinline__ void store_acc32_staged(uint32_t taddr, float sc, bf1
                  pack_bf16x2(__uint_as_float(v[q * 8 + 2]) * sc, __uint_as_float(v[q * 8 + 3]) * sc),
                  pack_bf16x2(__uint_as_float(v[q * 8 + 4]) * sc, __uint_as_float(v[q * 8 + 5]) * sc),
                  pack_bf16x2(__uint_as_float(v[q * 8 + 6]) * sc, __uint_as_float(v[q * 8 + 7]) * sc));
+  fence_proxy_async_shared();         // the generic writes, before the copy engine reads them
   __syncwarp();
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int rr = 8 * q + (lane >> 2), pc = lane & 3;
-    *reinterpret_cast<uint4*>(dst0 + (size_t)rr * ld + pc * 8) = ld_shared_v4(stage + stage_off(rr, pc));
+  if (lane == 0) {
+    tma_store_2d(m, stage, x, y);
+    bulk_commit();
   }
-  __syncwarp();   // the buffer is free for the next chunk
+}
+
+// In MTL_DEBUG builds: the 32 x 32 store box at (x, y) of a cols x rows bf16
+// tensor starts inside it on a 16-byte boundary.
+__device__ __forceinline__ bool store_box_ok(unsigned* status, int x, int y, int64_t cols, int64_t rows,
+                                             uint32_t site) {
+  const bounds::Box2 b = {cols, rows, 32, 32, 2};
+  (void)b;
+  (void)status;
+  (void)site;
+  return MTL_CHECKED(status, bounds::check_tma_store(b, x, y), site);
 }
 
 // ============================================================================ forward
@@ -237,13 +253,15 @@ __device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1, 
 
 template <int NA, int KS, bool DROP>
 __global__ void __launch_bounds__(FWD_THREADS, 1)
-    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const Params p) {
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ CUtensorMap tmc,
+                       const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const Smem sm = smem_aligned(smem_raw);
   constexpr uint32_t TILE = NA * ATOM128;
   constexpr int D = KS * 16;
   const uint32_t sQ0 = sm.u32, sR0 = sQ0 + 2 * TILE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm.base + (2 + FWD_RING) * TILE);
+  const uint32_t sStage = sQ0 + (2 + FWD_RING) * TILE;   // epilogue staging, 2 KB a row warp
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm.base + (2 + FWD_RING) * TILE + STAGE_BYTES);
   const uint32_t bar0 = smem_u32(bars);
   auto B = [&](int i) { return bar0 + 8u * i; };
   // barriers; per-tile ones come in pairs (A, B), item ones in pairs (slot 0, 1)
@@ -252,7 +270,6 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
   constexpr int QF = 0, QE = 2, RF = 4, RE = RF + FWD_RING, SF = RE + FWD_RING, SE = SF + 2,
                 PF = SE + 1, PE = PF + 2, IF = PE + 2, IE = IF + 2, NBAR = IE + 2;
   constexpr int ROW_WARPS = FWD_THREADS / 32 - 4;
-  const uint32_t sStage = smem_u32(bars) + 256;          // epilogue staging, 2 KB a row warp
   int* s_item = reinterpret_cast<int*>(bars + NBAR);   // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_item + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -439,21 +456,22 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     // PV_X(0) of the next item waits for that P block, so O_X is read first.
     bool pend = false;
     float pm = 0.f, pl = 1.f;
-    size_t po = 0, plse = 0;       // ctx offset of the row's head slice, lse index
+    size_t plse = 0;               // lse index of the row
+    int px = 0, py = 0;            // ctx column of the head slice, the warp's first row
     const uint32_t stage = sStage + (warp - 4) * STAGE_WARP_BYTES;
     auto epilogue = [&]() {
       const float inv = (DROP ? p.drop.scale : 1.0f) / pl;
-      // the row's head slice lies inside ctx [n][h], its lse inside [batch][heads][seq]
-      // (the warp stores its rows together: it skips them all if one fails)
+      // the warp's rows of the head slice lie inside ctx [n][h], the row's lse
+      // inside [batch][heads][seq] (the warp stores its rows together: it
+      // skips them all if one check fails)
       if (!__all_sync(0xffffffffu,
                       MTL_CHECKED(p.status,
-                                  bounds::check_index((int64_t)(po + D - 1), (int64_t)p.batch * p.seq * p.h) |
-                                      bounds::check_index((int64_t)plse, (int64_t)p.batch * p.heads * p.seq),
-                                  bounds::kSiteAttnFwdOut)))
+                                  bounds::check_index((int64_t)plse, (int64_t)p.batch * p.heads * p.seq),
+                                  bounds::kSiteAttnFwdOut)) ||
+          !store_box_ok(p.status, px, py, p.h, (int64_t)p.batch * p.seq, bounds::kSiteAttnFwdOut))
         return;
-      bf16* orow0 = p.ctx + po - (size_t)lane * p.h;   // the warp's first row
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) store_acc32_staged(tO + c, inv, orow0 + c, p.h, stage, lane);
+      for (int c = 0; c < D; c += 32) store_acc32_tma(tO + c, inv, &tmc, px + c, py, stage, lane);
       p.lse[plse] = (pm + __log2f(pl)) * LN2;
     };
     bool ok = true;
@@ -588,8 +606,9 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         pend = true;
         pm = m_used;
         pl = l;
-        po = (size_t)(it.b * p.seq + qb * 128 + r) * p.h + (size_t)it.hd * D;
         plse = ((size_t)it.b * p.heads + it.hd) * p.seq + qb * 128 + r;
+        px = it.hd * D;
+        py = it.b * p.seq + qb * 128 + q4 * 32;
       }
     }
     if (ok && pend) {
@@ -598,6 +617,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         epilogue();
       }
     }
+    if (lane == 0) bulk_wait0();   // this warp's stores are done before shared memory goes
     __syncwarp();
   }
   __syncthreads();
@@ -717,7 +737,8 @@ template <int NA, int KS, bool DROP>
 __global__ void __launch_bounds__(BWD_THREADS, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm,
                           const __grid_constant__ CUtensorMap tmdo,
-                          const __grid_constant__ CUtensorMap tmo, const Params p) {
+                          const __grid_constant__ CUtensorMap tmo,
+                          const __grid_constant__ CUtensorMap tmdq, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const Smem sm = smem_aligned(smem_raw);
   constexpr uint32_t TILE = NA * ATOM128;
@@ -874,23 +895,18 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const float dsc = DROP ? p.drop.scale : 1.0f;
     int ni = 0, nb = 0, nit = 0;
     bool pend = false;
-    bf16* pdq = nullptr;                       // dQ row of the item not yet written out
+    int px = 0, py = 0;                        // dqkv column of the pending dQ, the warp's first row
     // the epilogue stages its stores in the O tile, which is free from the
     // moment every row thread has formed D until the rows arrive on DE
     const uint32_t stage = sO + (warp - 4) * STAGE_WARP_BYTES;
     auto epilogue = [&]() {
-      // warpgroup wg writes 32-column chunks wg, wg + 2, ... of the row's dQ,
+      // warpgroup wg writes 32-column chunks wg, wg + 2, ... of the rows' dQ,
       // inside dqkv [n][3h]
-      if (!__all_sync(0xffffffffu,
-                      MTL_CHECKED(p.status,
-                                  bounds::check_index((int64_t)(pdq - p.dqkv) + D - 1,
-                                                      (int64_t)p.batch * p.seq * 3 * p.h),
-                                  bounds::kSiteAttnDqOut)))
+      if (!store_box_ok(p.status, px, py, 3 * (int64_t)p.h, (int64_t)p.batch * p.seq, bounds::kSiteAttnDqOut))
         return;
-      bf16* dq0 = pdq - (size_t)lane * 3 * p.h;   // the warp's first row
 #pragma unroll 1
       for (int c = 32 * wg; c < D; c += 64)
-        store_acc32_staged(tmem + TQ_ACC + lane_off + c, p.scale, dq0 + c, 3 * (size_t)p.h, stage, lane);
+        store_acc32_tma(tmem + TQ_ACC + lane_off + c, p.scale, &tmdq, px + c, py, stage, lane);
     };
     bool ok = true;
     while (ok) {
@@ -902,7 +918,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       if (k >= n_items) break;
       const BwdItem it = bwd_item(p, k, true);
       const int qb = it.blk;
-      const int row = it.b * p.seq + qb * 128 + r;
       // D_r = dO_r . O_r from the tiles in shared memory (they are not reloaded
       // before every row thread has arrived on DE, after the first block's
       // epilogue)
@@ -962,8 +977,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
               epilogue();
               pend = false;
             }
-            // the next item's Q, dO and O may load over the staged stores
-            fence_proxy_async_shared();
+            // the next item's Q, dO and O may load once the stores have read
+            // their staging buffers
+            if (lane == 0) bulk_wait_read0();
+            __syncwarp();
             mbar_arrive(B(DE));
           }
           const bool diag = j == qb;
@@ -1000,12 +1017,14 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
       if (!ok) break;
       pend = true;
-      pdq = p.dqkv + (size_t)row * 3 * p.h + (size_t)it.hd * 3 * D;
+      px = it.hd * 3 * D;
+      py = it.b * p.seq + qb * 128 + q4 * 32;
     }
     if (ok && pend && mbar_wait_bounded(B(DQD), (nb - 1) & 1, p.status, abort_flag)) {
       tc_fence_after();
       epilogue();
     }
+    if (lane == 0) bulk_wait0();   // this warp's stores are done before shared memory goes
     __syncwarp();
   }
   __syncthreads();
@@ -1036,18 +1055,19 @@ constexpr uint32_t TK_S = 0, TK_P = 128, TK_DS = 192, TK_DV = 256, TK_DK = 384;
 template <int NA, int KS, bool DROP>
 __global__ void __launch_bounds__(BWD_THREADS, 1)
     attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm,
-                           const __grid_constant__ CUtensorMap tmdo, const Params p) {
+                           const __grid_constant__ CUtensorMap tmdo,
+                           const __grid_constant__ CUtensorMap tmdq, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const Smem sm = smem_aligned(smem_raw);
   constexpr uint32_t TILE = NA * ATOM128;
   constexpr int D = KS * 16;
   const uint32_t sK = sm.u32, sV = sK + TILE, sR0 = sK + 2 * TILE;
+  const uint32_t sStage = sK + (2 + BWD_RING) * TILE;   // epilogue staging, 2 KB a row warp
   // lse, D of the queries in Q slot 2m: 128 + 128 floats at s_ld + 256 m
-  float* s_ld = reinterpret_cast<float*>(sm.base + (2 + BWD_RING) * TILE);
+  float* s_ld = reinterpret_cast<float*>(sm.base + (2 + BWD_RING) * TILE + STAGE_BYTES);
   const uint32_t s_ld_u32 = smem_u32(s_ld);
   uint64_t* bars = reinterpret_cast<uint64_t*>(s_ld + 128 * BWD_RING);
   const uint32_t bar0 = smem_u32(bars);
-  const uint32_t sStage = bar0 + 256;          // epilogue staging, 2 KB a row warp
   auto B = [&](int i) { return bar0 + 8u * i; };
   constexpr int KVF = 0, KVE = 1, RF = 2, RE = RF + BWD_RING, SF = RE + BWD_RING, SE = SF + 1,
                 DPF = SE + 1, DPE = DPF + 1, PF = DPE + 1, PE = PF + 1, DSF = PE + 1,
@@ -1210,22 +1230,17 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const float dsc = DROP ? p.drop.scale : 1.0f;
     int ni = 0, nb = 0, g = 0;
     bool pend = false;
-    bf16* pout = nullptr;                      // K part of the dqkv row not yet written out
+    int px = 0, py = 0;                        // dqkv column of the pending dK, the warp's first row
     const uint32_t stage = sStage + (warp - 4) * STAGE_WARP_BYTES;
     auto epilogue = [&]() {
       // warpgroup 0 writes dK (with the 1/sqrt(d) of S), warpgroup 1 dV
       const uint32_t src = tmem + (wg == 0 ? TK_DK : TK_DV) + lane_off;
-      bf16* dst = pout + (wg == 0 ? 0 : D);
       const float sc = wg == 0 ? p.scale : 1.0f;
-      if (!__all_sync(0xffffffffu,
-                      MTL_CHECKED(p.status,
-                                  bounds::check_index((int64_t)(dst - p.dqkv) + D - 1,
-                                                      (int64_t)p.batch * p.seq * 3 * p.h),
-                                  bounds::kSiteAttnDkvOut)))
+      const int x = px + (wg == 0 ? 0 : D);
+      if (!store_box_ok(p.status, x, py, 3 * (int64_t)p.h, (int64_t)p.batch * p.seq, bounds::kSiteAttnDkvOut))
         return;
-      bf16* dst0 = dst - (size_t)lane * 3 * p.h;   // the warp's first row
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) store_acc32_staged(src + c, sc, dst0 + c, 3 * (size_t)p.h, stage, lane);
+      for (int c = 0; c < D; c += 32) store_acc32_tma(src + c, sc, &tmdq, x + c, py, stage, lane);
     };
     bool ok = true;
     while (ok) {
@@ -1372,13 +1387,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       if (!ok) break;
       g += 2 * nq;
       pend = true;
-      pout = p.dqkv + (size_t)(it.b * p.seq + kb * 128 + r) * 3 * p.h + (size_t)it.hd * 3 * D + D;
+      px = it.hd * 3 * D + D;
+      py = it.b * p.seq + kb * 128 + q4 * 32;
     }
     if (ok && pend && mbar_wait_bounded(B(PE), (nb - 1) & 1, p.status, abort_flag) &&
         mbar_wait_bounded(B(DSE), (nb - 1) & 1, p.status, abort_flag)) {
       tc_fence_after();
       epilogue();
     }
+    if (lane == 0) bulk_wait0();   // this warp's stores are done before shared memory goes
     __syncwarp();
   }
   __syncthreads();
@@ -1400,7 +1417,11 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-bool make_map(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+// A bf16 [rows][cols] tensor in boxes of box_cols x box_rows (64 x box_rows
+// with 128-byte swizzle for the operand loads; 32 x 32 with 64-byte swizzle
+// for the epilogue stores).
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint32_t box_rows,
+              uint32_t box_cols = 64, CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B) {
   static EncodeTiledFn enc = nullptr;
   if (!enc) {
     void* fp = nullptr;
@@ -1413,15 +1434,15 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uin
   }
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 size_t fwd_smem(int na) {
-  const size_t need = (size_t)(2 + FWD_RING) * na * ATOM128 + 256 + STAGE_BYTES + 1024;
+  const size_t need = (size_t)(2 + FWD_RING) * na * ATOM128 + STAGE_BYTES + 256 + 1024;
   return need < 120 * 1024 ? 120 * 1024 : need;   // one CTA per SM (512 TMEM columns)
 }
 // The backward kernels hold all 512 TMEM columns: their shared memory requests
@@ -1431,7 +1452,7 @@ size_t dq_smem(int na) {
   return need < 120 * 1024 ? 120 * 1024 : need;   // one CTA per SM (512 TMEM columns)
 }
 size_t dkv_smem(int na) {
-  const size_t need = (size_t)(2 + BWD_RING) * na * ATOM128 + 2048 + 256 + STAGE_BYTES + 1024;
+  const size_t need = (size_t)(2 + BWD_RING) * na * ATOM128 + STAGE_BYTES + 2048 + 256 + 1024;
   return need < 120 * 1024 ? 120 * 1024 : need;
 }
 
@@ -1496,8 +1517,10 @@ cudaError_t attn_fwd_tc(const void* qkv, void* ctx, float* lse, int batch, int s
   using namespace attn;
   if (batch == 0) return cudaSuccess;
   if (!attn_tc_supported(seq, d)) return cudaErrorInvalidValue;
-  CUtensorMap tm;
-  if (!make_map(&tm, qkv, 3ull * heads * d, (uint64_t)batch * seq, 128)) return cudaErrorInvalidValue;
+  CUtensorMap tm, tmc;
+  if (!make_map(&tm, qkv, 3ull * heads * d, (uint64_t)batch * seq, 128) ||
+      !make_map(&tmc, ctx, (uint64_t)heads * d, (uint64_t)batch * seq, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
   if (drop.on && !mask) return cudaErrorInvalidValue;
   Params p = make_params(batch, seq, heads, d, status, drop);
   p.mask = mask;
@@ -1516,7 +1539,7 @@ cudaError_t attn_fwd_tc(const void* qkv, void* ctx, float* lse, int batch, int s
     if ((e = check_regs(attn_fwd_tc_kernel<NA_, KS_, DR_>, FWD_LAUNCH_REGS)) != cudaSuccess) \
       return e;                                                                          \
     c.before(KK_ATTN_FWD, flops);                                                        \
-    attn_fwd_tc_kernel<NA_, KS_, DR_><<<grid, FWD_THREADS, sm, c.stream>>>(tm, p);       \
+    attn_fwd_tc_kernel<NA_, KS_, DR_><<<grid, FWD_THREADS, sm, c.stream>>>(tm, tmc, p);  \
   }
   if (drop.on) {
     if (d == 64) FWD_CASE(1, 4, true)
@@ -1540,10 +1563,11 @@ cudaError_t attn_bwd_tc(const void* qkv, const void* ctx, const float* lse, cons
   if (batch == 0) return cudaSuccess;
   if (!attn_tc_supported(seq, d)) return cudaErrorInvalidValue;
   const uint64_t n = (uint64_t)batch * seq;
-  CUtensorMap tm, tmdo, tmo;
+  CUtensorMap tm, tmdo, tmo, tmdq;
   if (!make_map(&tm, qkv, 3ull * heads * d, n, 128) ||
       !make_map(&tmdo, dctx, (uint64_t)heads * d, n, 128) ||
-      !make_map(&tmo, ctx, (uint64_t)heads * d, n, 128))
+      !make_map(&tmo, ctx, (uint64_t)heads * d, n, 128) ||
+      !make_map(&tmdq, dqkv, 3ull * heads * d, n, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   if (drop.on && !mask) return cudaErrorInvalidValue;
   Params p = make_params(batch, seq, heads, d, status, drop);
@@ -1568,12 +1592,12 @@ cudaError_t attn_bwd_tc(const void* qkv, const void* ctx, const float* lse, cons
     if ((e = check_regs(kk, BWD_LAUNCH_REGS)) != cudaSuccess) return e;                        \
     c.before(KK_ATTN_BWD, 2.0 * 3.0 * tri);                                                    \
     p.sched = status + kSchedDq;                                                               \
-    kq<<<grid, BWD_THREADS, dq_smem(NA_), c.stream>>>(tm, tmdo, tmo, p);                       \
+    kq<<<grid, BWD_THREADS, dq_smem(NA_), c.stream>>>(tm, tmdo, tmo, tmdq, p);                 \
     c.after();                                                                                 \
     if ((e = cudaGetLastError()) != cudaSuccess) return e;                                     \
     c.before(KK_ATTN_BWD, 2.0 * 4.0 * tri);                                                    \
     p.sched = status + kSchedDkv;                                                              \
-    kk<<<grid, BWD_THREADS, dkv_smem(NA_), c.stream>>>(tm, tmdo, p);                           \
+    kk<<<grid, BWD_THREADS, dkv_smem(NA_), c.stream>>>(tm, tmdo, tmdq, p);                     \
     c.after();                                                                                 \
   }
   if (drop.on) {
