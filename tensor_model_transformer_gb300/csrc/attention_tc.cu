@@ -729,9 +729,15 @@ static_assert(BWD_LOW_REGS + 2 * BWD_ROW_REGS <= 3 * BWD_LAUNCH_REGS,
 // kernel.  An item's dQ is written out when
 // the next item's first dS block is ready (the last dQ product is done by
 // then, and the next one waits for that block).
-// smem: Q, dO, O, ring[BWD_RING] (NA atoms of 16 KB each), item ids.
+// smem: Q, dO, O, ring[BWD_RING] (NA atoms of 16 KB each), item ids.  Of the
+// ring, DQ_KSLOTS slots hold K blocks and one holds V: K(j) stays until dQ +=
+// dS K(j) has read it, about a block after S, so K is loaded up to two blocks
+// ahead; V(j) is free once dP(j) is done, and V(j + 1) loads while the rows
+// work on block j.  (With K and V alternating in the four slots, K(j + 2)
+// waited for dQ(j) and the next S = Q K^T for the load.)
 // TMEM: S 0..127, dP 128..255, dS 256..319, dQ 384..
 constexpr uint32_t TQ_S = 0, TQ_DP = 128, TQ_DS = 256, TQ_ACC = 384;
+constexpr int DQ_KSLOTS = BWD_RING - 1, DQ_VSLOT = BWD_RING - 1;
 
 template <int NA, int KS, bool DROP>
 __global__ void __launch_bounds__(BWD_THREADS, 1)
@@ -764,7 +770,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       uint32_t cnt = 1;
       if (i == SE || i == DSF || i == DE) cnt = 256;
       if (i == IE || i == IE + 1) cnt = 2 + 8;            // two issuers + a lane per row warp
-      if (i >= RE && i < RE + BWD_RING && (i - RE) % 2 == 0) cnt = 2;   // K: both issuers
+      if (i >= RE && i < RE + DQ_KSLOTS) cnt = 2;   // K slots: read by both issuers
       mbar_init(B(i), cnt);
     }
     *abort_flag = 0;
@@ -784,7 +790,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       tma_prefetch_desc(&tm);
       tma_prefetch_desc(&tmdo);
       tma_prefetch_desc(&tmo);
-      int g = 0, ni = 0, nit = 0;
+      int g = 0, ni = 0, nit = 0, ksl = 0, kuse = 0;   // K slot and its use count
       bool ok = true;
       while (ok) {
         const int k = (int)atomicAdd(p.sched, 1u);
@@ -804,9 +810,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           load_box(sO + a * ATOM128, &tmo, B(QF), it.hd * p.d + 64 * a, row0 + it.blk * 128,
                    (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnDqLoad);
         }
-        for (int j = 0; j <= it.blk && ok; ++j) {
-          for (int kv = 0; kv < 2; ++kv, ++g) {
-            const int s = g % BWD_RING, use = g / BWD_RING;
+        for (int j = 0; j <= it.blk && ok; ++j, ++g) {   // g: blocks so far
+          for (int kv = 0; kv < 2; ++kv) {
+            const int s = kv ? DQ_VSLOT : ksl, use = kv ? g : kuse;
             if (use > 0 && !mbar_wait_bounded(B(RE + s), (use - 1) & 1, p.status, abort_flag)) {
               ok = false;
               break;
@@ -816,6 +822,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
               load_box(sR0 + s * TILE + a * ATOM128, &tm, B(RF + s),
                        colq + (1 + kv) * p.d + 64 * a, row0 + j * 128, 3 * (int64_t)p.h, (int64_t)p.batch * p.seq, p.status,
                        bounds::kSiteAttnDqKV);
+          }
+          if (++ksl == DQ_KSLOTS) {
+            ksl = 0;
+            ++kuse;
           }
         }
       }
@@ -831,7 +841,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const uint32_t id_acc = idesc_bf16_f32(128, D, false, true);
       const uint64_t dQd = desc_kbase(sQ), dDO = desc_kbase(sDO), dR0 = desc_kbase(sR0);
       const uint64_t dRmn0 = desc_mnbase(sR0, ATOM128);
-      int g = 0, ni = 0, nit = 0, nb = 0;
+      int ni = 0, nit = 0, nb = 0;      // nb: blocks so far
+      int sk = 0, kuse = 0;             // K slot of this block and its use count
       bool ok = true;
       auto wait = [&](int bar, int k) -> bool {
         if (!mbar_wait_bounded(B(bar), k & 1, p.status, abort_flag)) ok = false;
@@ -844,29 +855,30 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         const BwdItem it = bwd_item(p, k, true);
         const int nkv = it.blk + 1;
         for (int j = 0; j < nkv && ok; ++j, ++nb) {
-          const int gk = g + 2 * j, gv = gk + 1;
-          const int sk = gk % BWD_RING, sv = gv % BWD_RING;
           if (first) {
             if (j == 0 && !wait(QF, nit)) break;
-            if (!wait(RF + sk, gk / BWD_RING) || !wait(RF + sv, gv / BWD_RING)) break;
+            if (!wait(RF + sk, kuse)) break;
             if (nb > 0 && !wait(SE, nb - 1)) break;   // the row threads hold S, dP of the last block
             tc_fence_after();
-            const uint64_t dK = desc_add(dR0, sk * TILE), dV = desc_add(dR0, sv * TILE);
+            const uint64_t dK = desc_add(dR0, sk * TILE), dV = desc_add(dR0, DQ_VSLOT * TILE);
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk)
               tc_mma_bf16(tmem + TQ_S, desc_add(dQd, kmajor_off(kk, ATOM128)),
                           desc_add(dK, kmajor_off(kk, ATOM128)), id_s, kk > 0);
+            // V(j) may land after S is under way
+            if (!wait(RF + DQ_VSLOT, nb)) break;
+            tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk)
               tc_mma_bf16(tmem + TQ_DP, desc_add(dDO, kmajor_off(kk, ATOM128)),
                           desc_add(dV, kmajor_off(kk, ATOM128)), id_s, kk > 0);
             tc_commit(B(SF));
             tc_commit(B(RE + sk));
-            tc_commit(B(RE + sv));
+            tc_commit(B(RE + DQ_VSLOT));
             if (j == nkv - 1) tc_commit(B(QE));
           } else {
             if (!wait(DSF, nb)) break;                // dS of this block is in TMEM
-            if (!wait(RF + sk, gk / BWD_RING)) break;
+            if (!wait(RF + sk, kuse)) break;
             tc_fence_after();
             const uint64_t dKmn = desc_add(dRmn0, sk * TILE);
 #pragma unroll
@@ -876,9 +888,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             tc_commit(B(DQD));
             tc_commit(B(RE + sk));
           }
+          if (++sk == DQ_KSLOTS) {
+            sk = 0;
+            ++kuse;
+          }
         }
         if (!ok) break;
-        g += 2 * nkv;
         ++nit;
       }
     }
