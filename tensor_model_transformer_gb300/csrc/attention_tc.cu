@@ -451,9 +451,9 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     const uint32_t tS = tmem + TM_S + lane_off, tP = tmem + TM_P + 64 * x + lane_off;
     const uint32_t tO = tmem + TM_O + 128 * x + lane_off;
     int cnt = 0, ni = 0;           // blocks of this tile so far, items read
-    // A tile's epilogue (O / l to ctx, lse) runs when the tile's next item has
-    // its first P block computed: the last PV of the item is done by then, and
-    // PV_X(0) of the next item waits for that P block, so O_X is read first.
+    // A tile's epilogue (O / l to ctx, lse) runs when the tile has taken its
+    // next item, once the item's last PV is done; PV_X(0) of the next item
+    // waits for that item's first P block, so O_X is read first.
     bool pend = false;
     float pm = 0.f, pl = 1.f;
     size_t plse = 0;               // lse index of the row
@@ -489,6 +489,18 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
       const FwdItem it = fwd_item(p, k);
       const int nx = it.n(x);
       const int qb = 2 * it.qp + x;                // 128-row query block of this tile
+      // The previous item's O / l leave while this item's first S is on its
+      // way (tile A's first block waits for tile B's extra diagonal block of
+      // the previous item); PV_X(0) of this item waits for its first P block.
+      if (pend) {
+        if (!mbar_wait_bounded(B(PE + x), (cnt - 1) & 1, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        epilogue();
+        pend = false;
+      }
       float m_used = -INFINITY, l = 0.f;
       for (int j = 0; j < nx; ++j) {
         uint32_t keep[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
@@ -553,10 +565,6 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
           break;
         }
         tc_fence_after();
-        if (j == 0 && pend) {
-          epilogue();
-          pend = false;
-        }
         // exponentials and row sum a 32-key chunk at a time, each chunk's bf16
         // P stored into TMEM while the next one is computed
         float rs[8];
@@ -726,9 +734,9 @@ static_assert(BWD_LOW_REGS + 2 * BWD_ROW_REGS <= 3 * BWD_LAUNCH_REGS,
 // lse log2(e)) (zero after the query), written to TMEM as bf16; dQ += dS K
 // (warp 2, dS as the A operand).  The row threads also form D_i = sum_c dO_ic
 // O_ic from the dO and O tiles in shared memory and store it for the dK/dV
-// kernel.  An item's dQ is written out when
-// the next item's first dS block is ready (the last dQ product is done by
-// then, and the next one waits for that block).
+// kernel.  An item's dQ is written out when the rows have formed the next
+// item's D (its last dQ product done), while that item's first S and dP are
+// on their way; the first dQ product of the next item waits for its dS.
 // smem: Q, dO, O, ring[BWD_RING] (NA atoms of 16 KB each), item ids.  Of the
 // ring, DQ_KSLOTS slots hold K blocks and one holds V: K(j) stays until dQ +=
 // dS K(j) has read it, about a block after S, so K is loaded up to two blocks
@@ -758,6 +766,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   // can finish before the rows get to D, so both gate the next load)
   constexpr int QF = 0, QE = 1, RF = 2, RE = RF + BWD_RING, SF = RE + BWD_RING, SE = SF + 1,
                 DSF = SE + 1, DQD = DSF + 1, DE = DQD + 1, IF = DE + 1, IE = IF + 2, NBAR = IE + 2;
+  // the two warpgroups' halves of D for the item's 128 rows
+  volatile float* s_dhalf = reinterpret_cast<volatile float*>(sm.base + (3 + BWD_RING) * TILE + 256);
   int* s_item = reinterpret_cast<int*>(bars + NBAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_item + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -934,16 +944,19 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const BwdItem it = bwd_item(p, k, true);
       const int qb = it.blk;
       // D_r = dO_r . O_r from the tiles in shared memory (they are not reloaded
-      // before every row thread has arrived on DE, after the first block's
-      // epilogue)
+      // before every row thread has arrived on DE, after the previous item's
+      // epilogue below)
       if (!mbar_wait_bounded(B(QF), nit & 1, p.status, abort_flag)) {
         ok = false;
         break;
       }
       ++nit;
-      float Dr = 0.f;
+      // warpgroup wg sums columns wg D/2 .. (wg + 1) D/2 - 1; both then add
+      // the two halves in the same order
+      float Dp = 0.f;
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
+      for (int i = 0; i < D / 16; ++i) {
+        const int c = wg * (D / 16) + i;
         const uint32_t off = (c >> 3) * ATOM128 + sw128_offset(r, c & 7);
         Vec<bf16> go, oo;
         go.raw = ld_shared_v4(sDO + off);
@@ -952,9 +965,27 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         go.unpack(gf);
         oo.unpack(of);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) Dr = fmaf(gf[e], of[e], Dr);
+        for (int e = 0; e < 8; ++e) Dp = fmaf(gf[e], of[e], Dp);
       }
+      s_dhalf[wg * 128 + r] = Dp;
       named_bar_sync(1, 256);                  // every row is done with the O tile
+      const float Dr = s_dhalf[r] + s_dhalf[128 + r];
+      // the previous item's dQ leaves now, staged in the O tile, while this
+      // item's first S and dP are on their way (its last dQ product is done)
+      if (pend) {
+        if (!mbar_wait_bounded(B(DQD), (nb - 1) & 1, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        epilogue();
+        pend = false;
+      }
+      // the next item's Q, dO and O may load once the stores have read their
+      // staging buffers
+      if (lane == 0) bulk_wait_read0();
+      __syncwarp();
+      mbar_arrive(B(DE));
       const size_t lrow = ((size_t)it.b * p.heads + it.hd) * p.seq + qb * 128 + r;
       if (wg == 0) p.dsum[lrow] = Dr;
       const float lse2 = p.lse[lrow] * LOG2E;
@@ -987,17 +1018,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             break;
           }
           tc_fence_after();
-          if (j == 0) {
-            if (pend) {
-              epilogue();
-              pend = false;
-            }
-            // the next item's Q, dO and O may load once the stores have read
-            // their staging buffers
-            if (lane == 0) bulk_wait_read0();
-            __syncwarp();
-            mbar_arrive(B(DE));
-          }
           const bool diag = j == qb;
           const float nl = -lse2;
 #pragma unroll
@@ -1061,7 +1081,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 // have read S^T (warp 1); the row threads' P^T (with the forward's keep mask
 // and scale) and dS^T = P^T * (dP^T - D), written to TMEM as bf16; dV += P^T
 // dO and dK += dS^T Q (warp 2, A operands from TMEM).  An item's dK and dV are
-// written out when the next item's first P^T block is ready.
+// written out when the rows take the next item (its last dV and dK products
+// done), while that item's K, V and first S^T are on their way.
 // smem: K, V, ring[BWD_RING] (NA atoms of 16 KB each), lse and D of the two Q
 // slots, item ids.  TMEM: S^T / dP^T 0..127, P^T 128..191, dS^T 192..255,
 // dV 256.., dK 384..
@@ -1267,6 +1288,18 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       if (k >= n_items) break;
       const BwdItem it = bwd_item(p, k, false);
       const int kb = it.blk, nq = p.nqb - kb;
+      // the previous item's dK and dV leave while this item's K and V load
+      // and its first S^T is computed: its last dV and dK products are done
+      if (pend) {
+        if (!mbar_wait_bounded(B(PE), (nb - 1) & 1, p.status, abort_flag) ||
+            !mbar_wait_bounded(B(DSE), (nb - 1) & 1, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        epilogue();
+        pend = false;
+      }
       for (int i = 0; i < nq; ++i, ++nb) {
         const int qb = kb + i;
         const int sq = (g + 2 * i) % BWD_RING;
@@ -1299,20 +1332,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           }
           const uint32_t keep0 = DROP ? warp_transpose32(kword[0], lane) : 0xffffffffu;
           const uint32_t keep1 = DROP ? warp_transpose32(kword[1], lane) : 0xffffffffu;
-          // P^T (and, at an item's first block, dV) is free once the previous dV
-          // product is done; at an item's first block dK must be done as well
+          // P^T is free once the previous dV product is done
           if (nb > 0 && !mbar_wait_bounded(B(PE), (nb - 1) & 1, p.status, abort_flag)) {
             ok = false;
             break;
-          }
-          if (i == 0 && pend) {
-            if (!mbar_wait_bounded(B(DSE), (nb - 1) & 1, p.status, abort_flag)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            epilogue();
-            pend = false;
           }
           tc_fence_after();
           const float* lse = s_ld + (sq >> 1) * 256 + 64 * wg;
@@ -1463,7 +1486,7 @@ size_t fwd_smem(int na) {
 // The backward kernels hold all 512 TMEM columns: their shared memory requests
 // keep them at one CTA per SM so a second CTA never waits in tcgen05.alloc.
 size_t dq_smem(int na) {
-  const size_t need = (size_t)(3 + BWD_RING) * na * ATOM128 + 256 + 1024;
+  const size_t need = (size_t)(3 + BWD_RING) * na * ATOM128 + 256 + 1024 + 1024;
   return need < 120 * 1024 ? 120 * 1024 : need;   // one CTA per SM (512 TMEM columns)
 }
 size_t dkv_smem(int na) {
