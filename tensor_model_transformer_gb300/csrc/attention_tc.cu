@@ -41,7 +41,6 @@ namespace attn {
 
 constexpr int FWD_THREADS = 384;   // forward kernel: 4 control warps, two warpgroups of row threads
 constexpr int BWD_THREADS = 384;   // backward kernels: 4 control warps, two warpgroups of row threads
-constexpr int ATOM128 = 128 * 128;   // [128 rows][64 bf16]
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
@@ -98,11 +97,46 @@ __device__ __forceinline__ unsigned long long drop_row(const Params& p, int b, i
 // MTL_DEBUG builds.
 __device__ __forceinline__ void load_box(uint32_t dst, const CUtensorMap* m, uint32_t bar, int x,
                                          int y, int64_t cols, int64_t rows, unsigned* status,
-                                         uint32_t site) {
-  const bounds::Box2 b = {cols, rows, 64, 128, 2};
+                                         uint32_t site, int box_cols = 64) {
+  const bounds::Box2 b = {cols, rows, box_cols, 128, 2};
   (void)b;
   if (MTL_CHECKED(status, bounds::check_tma_load(b, x, y), site)) tma_load_2d(dst, m, bar, x, y);
 }
+
+// Shared-memory layout of a 128-row bf16 operand tile of d = 16 KS columns:
+// atoms of 128 rows x ACOLS columns, each the box of one TMA load, swizzled as
+// the tensor map says.  d = 64 and 128: 64-column atoms with 128-byte swizzle;
+// d = 96: three 32-column atoms with 64-byte swizzle (24 KB a tile, where two
+// 64-column atoms take 32 KB with a quarter of it unused).
+template <int KS>
+struct Fmt {
+  static constexpr int D = KS * 16;
+  static constexpr bool SW64 = D % 64 != 0;
+  static constexpr int ACOLS = SW64 ? 32 : 64;
+  static constexpr int ATOMS = D / ACOLS;
+  static constexpr uint32_t ROWB = ACOLS * 2;           // bytes of an atom row
+  static constexpr uint32_t ATOM = 128 * ROWB;
+  static constexpr uint32_t TILE = ATOMS * ATOM;
+  static constexpr int KPA = ACOLS / 16;                // 16-column k-steps per atom
+  static constexpr uint32_t MODE = SW64 ? kDescSw64 : kDescSw128;
+  static_assert(D % ACOLS == 0, "a tile is whole atoms");
+  // K-major operand: k-step kk at byte 32 (kk % KPA) of the rows of atom kk / KPA;
+  // 8-row groups ROWB * 8 bytes apart
+  __host__ __device__ static constexpr uint32_t koff(int kk) {
+    return (uint32_t)(kk / KPA) * ATOM + (uint32_t)(kk % KPA) * 32;
+  }
+  __device__ static uint64_t kdesc(uint32_t a) { return smem_desc(a, 16, 8 * ROWB, MODE); }
+  // MN-major operand (the tile's rows are the K dimension): k-step kk is rows
+  // 16 kk .. 16 kk + 15; the N atoms are ATOM bytes apart
+  __host__ __device__ static constexpr uint32_t mnoff(int kk) { return (uint32_t)kk * 16 * ROWB; }
+  __device__ static uint64_t mndesc(uint32_t a) { return smem_desc(a, ATOM, 8 * ROWB, MODE); }
+  // byte offset of 16-byte chunk c (columns 8c .. 8c + 7) of row r
+  __device__ static uint32_t chunk(int r, int c) {
+    constexpr int CPA = ACOLS / 8;
+    const int sw = SW64 ? ((r >> 1) & 3) : (r & 7);
+    return (uint32_t)(c / CPA) * ATOM + (uint32_t)r * ROWB + ((uint32_t)((c % CPA) ^ sw) << 4);
+  }
+};
 
 struct Smem {
   uint8_t* base;
@@ -190,7 +224,7 @@ __device__ __forceinline__ bool store_box_ok(unsigned* status, int x, int y, int
 // issuer, 3 register donor, 4..7 row threads of tile A, 8..11 of tile B.  The
 // two MMA streams touch disjoint TMEM columns and each commit tracks only its
 // own thread's MMAs, so neither issuer waits on the other's dependencies.
-// smem: Q_A, Q_B, ring[FWD_RING] (NA atoms of 16 KB each), item ids.
+// smem: Q_A, Q_B, ring[FWD_RING] (tiles in the Fmt layout), item ids.
 // TMEM: S cols 0..127, P_A 128..191, P_B 192..255, O_A 256.., O_B 384..
 constexpr int FWD_RING = 4;
 static_assert(FWD_RING % 2 == 0, "K and V must keep to their own ring slots");
@@ -251,13 +285,14 @@ __device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1, 
   asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(rd));
 }
 
-template <int NA, int KS, bool DROP>
+template <int KS, bool DROP>
 __global__ void __launch_bounds__(FWD_THREADS, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ CUtensorMap tmc,
                        const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const Smem sm = smem_aligned(smem_raw);
-  constexpr uint32_t TILE = NA * ATOM128;
+  using F = Fmt<KS>;
+  constexpr uint32_t TILE = F::TILE;
   constexpr int D = KS * 16;
   const uint32_t sQ0 = sm.u32, sR0 = sQ0 + 2 * TILE;
   const uint32_t sStage = sQ0 + (2 + FWD_RING) * TILE;   // epilogue staging, 2 KB a row warp
@@ -318,9 +353,9 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
           if (nq > 0 && !mbar_wait_bounded(B(QE + x), (nq - 1) & 1, p.status, abort_flag))
             return false;
           mbar_arrive_expect_tx(B(QF + x), TILE);
-          for (int a = 0; a < NA; ++a)
-            load_box(sQ0 + x * TILE + a * ATOM128, &tm, B(QF + x), colq + 64 * a,
-                     row0 + it.qp * 256 + x * 128, cols, rows, p.status, bounds::kSiteAttnFwdQ);
+          for (int a = 0; a < F::ATOMS; ++a)
+            load_box(sQ0 + x * TILE + a * F::ATOM, &tm, B(QF + x), colq + F::ACOLS * a,
+                     row0 + it.qp * 256 + x * 128, cols, rows, p.status, bounds::kSiteAttnFwdQ, F::ACOLS);
           return true;
         };
         auto load_kv = [&](int j) -> bool {   // K(j) and V(j) into the next two ring slots
@@ -329,10 +364,10 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             if (use > 0 && !mbar_wait_bounded(B(RE + s), (use - 1) & 1, p.status, abort_flag))
               return false;
             mbar_arrive_expect_tx(B(RF + s), TILE);
-            for (int a = 0; a < NA; ++a)
-              load_box(sR0 + s * TILE + a * ATOM128, &tm, B(RF + s),
-                       colq + (1 + kv) * p.d + 64 * a, row0 + j * 128, cols, rows, p.status,
-                       bounds::kSiteAttnFwdKV);
+            for (int a = 0; a < F::ATOMS; ++a)
+              load_box(sR0 + s * TILE + a * F::ATOM, &tm, B(RF + s),
+                       colq + (1 + kv) * p.d + F::ACOLS * a, row0 + j * 128, cols, rows, p.status,
+                       bounds::kSiteAttnFwdKV, F::ACOLS);
           }
           return true;
         };
@@ -359,8 +394,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
       const bool is_qk = warp == 1;
       const uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);
       const uint32_t id_pv = idesc_bf16_f32(128, D, false, true);
-      const uint64_t dQ0 = desc_kbase(sQ0), dR0 = desc_kbase(sR0);
-      const uint64_t dRmn0 = desc_mnbase(sR0, ATOM128);
+      const uint64_t dQ0 = F::kdesc(sQ0), dR0 = F::kdesc(sR0);
+      const uint64_t dRmn0 = F::mndesc(sR0);
       int g = 0, su = 0, ni = 0;        // ring loads, S uses and items before this item
       int npv0 = 0, npv1 = 0, nit0 = 0, nit1 = 0;
       int ring_seen = -1;               // last ring load this thread waited for
@@ -409,8 +444,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             const uint64_t dQ = desc_add(dQ0, x * TILE), dK = desc_add(dR0, s * TILE);
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk)
-              tc_mma_bf16(tmem + TM_S, desc_add(dQ, kmajor_off(kk, ATOM128)),
-                          desc_add(dK, kmajor_off(kk, ATOM128)), id_qk, kk > 0);
+              tc_mma_bf16(tmem + TM_S, desc_add(dQ, F::koff(kk)), desc_add(dK, F::koff(kk)), id_qk,
+                          kk > 0);
             tc_commit(B(SF + x));
             if (j == it.n(x) - 1) tc_commit(B(QE + x));
             if (x == 1 || !last_b) tc_commit(B(RE + s));
@@ -425,7 +460,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
               tc_mma_bf16_ts(tmem + TM_O + 128 * x, tmem + TM_P + 64 * x + 8 * kk,
-                             desc_add(dV, mnmajor_off(kk)), id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                             desc_add(dV, F::mnoff(kk)), id_pv, (j > 0 || kk > 0) ? 1u : 0u);
             tc_commit(B(PE + x));
             if (x) ++npv1; else ++npv0;
             if (x == 1 || !last_b) tc_commit(B(RE + s));
@@ -737,7 +772,7 @@ static_assert(BWD_LOW_REGS + 2 * BWD_ROW_REGS <= 3 * BWD_LAUNCH_REGS,
 // kernel.  An item's dQ is written out when the rows have formed the next
 // item's D (its last dQ product done), while that item's first S and dP are
 // on their way; the first dQ product of the next item waits for its dS.
-// smem: Q, dO, O, ring[BWD_RING] (NA atoms of 16 KB each), item ids.  Of the
+// smem: Q, dO, O, ring[BWD_RING] (tiles in the Fmt layout), item ids.  Of the
 // ring, DQ_KSLOTS slots hold K blocks and one holds V: K(j) stays until dQ +=
 // dS K(j) has read it, about a block after S, so K is loaded up to two blocks
 // ahead; V(j) is free once dP(j) is done, and V(j + 1) loads while the rows
@@ -747,7 +782,7 @@ static_assert(BWD_LOW_REGS + 2 * BWD_ROW_REGS <= 3 * BWD_LAUNCH_REGS,
 constexpr uint32_t TQ_S = 0, TQ_DP = 128, TQ_DS = 256, TQ_ACC = 384;
 constexpr int DQ_KSLOTS = BWD_RING - 1, DQ_VSLOT = BWD_RING - 1;
 
-template <int NA, int KS, bool DROP>
+template <int KS, bool DROP>
 __global__ void __launch_bounds__(BWD_THREADS, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm,
                           const __grid_constant__ CUtensorMap tmdo,
@@ -755,7 +790,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                           const __grid_constant__ CUtensorMap tmdq, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const Smem sm = smem_aligned(smem_raw);
-  constexpr uint32_t TILE = NA * ATOM128;
+  using F = Fmt<KS>;
+  constexpr uint32_t TILE = F::TILE;
   constexpr int D = KS * 16;
   const uint32_t sQ = sm.u32, sDO = sQ + TILE, sO = sQ + 2 * TILE, sR0 = sQ + 3 * TILE;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm.base + (3 + BWD_RING) * TILE);
@@ -812,13 +848,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           break;
         ++nit;
         mbar_arrive_expect_tx(B(QF), 3 * TILE);
-        for (int a = 0; a < NA; ++a) {
-          load_box(sQ + a * ATOM128, &tm, B(QF), colq + 64 * a, row0 + it.blk * 128, 3 * (int64_t)p.h, (int64_t)p.batch * p.seq, p.status,
-                   bounds::kSiteAttnDqLoad);
-          load_box(sDO + a * ATOM128, &tmdo, B(QF), it.hd * p.d + 64 * a, row0 + it.blk * 128,
-                   (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnDqLoad);
-          load_box(sO + a * ATOM128, &tmo, B(QF), it.hd * p.d + 64 * a, row0 + it.blk * 128,
-                   (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnDqLoad);
+        for (int a = 0; a < F::ATOMS; ++a) {
+          load_box(sQ + a * F::ATOM, &tm, B(QF), colq + F::ACOLS * a, row0 + it.blk * 128,
+                   3 * (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnDqLoad, F::ACOLS);
+          load_box(sDO + a * F::ATOM, &tmdo, B(QF), it.hd * p.d + F::ACOLS * a, row0 + it.blk * 128,
+                   (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnDqLoad, F::ACOLS);
+          load_box(sO + a * F::ATOM, &tmo, B(QF), it.hd * p.d + F::ACOLS * a, row0 + it.blk * 128,
+                   (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnDqLoad, F::ACOLS);
         }
         for (int j = 0; j <= it.blk && ok; ++j, ++g) {   // g: blocks so far
           for (int kv = 0; kv < 2; ++kv) {
@@ -828,10 +864,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
               break;
             }
             mbar_arrive_expect_tx(B(RF + s), TILE);
-            for (int a = 0; a < NA; ++a)
-              load_box(sR0 + s * TILE + a * ATOM128, &tm, B(RF + s),
-                       colq + (1 + kv) * p.d + 64 * a, row0 + j * 128, 3 * (int64_t)p.h, (int64_t)p.batch * p.seq, p.status,
-                       bounds::kSiteAttnDqKV);
+            for (int a = 0; a < F::ATOMS; ++a)
+              load_box(sR0 + s * TILE + a * F::ATOM, &tm, B(RF + s), colq + (1 + kv) * p.d + F::ACOLS * a,
+                       row0 + j * 128, 3 * (int64_t)p.h, (int64_t)p.batch * p.seq, p.status,
+                       bounds::kSiteAttnDqKV, F::ACOLS);
           }
           if (++ksl == DQ_KSLOTS) {
             ksl = 0;
@@ -849,8 +885,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const bool first = warp == 1;
       const uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
       const uint32_t id_acc = idesc_bf16_f32(128, D, false, true);
-      const uint64_t dQd = desc_kbase(sQ), dDO = desc_kbase(sDO), dR0 = desc_kbase(sR0);
-      const uint64_t dRmn0 = desc_mnbase(sR0, ATOM128);
+      const uint64_t dQd = F::kdesc(sQ), dDO = F::kdesc(sDO), dR0 = F::kdesc(sR0);
+      const uint64_t dRmn0 = F::mndesc(sR0);
       int ni = 0, nit = 0, nb = 0;      // nb: blocks so far
       int sk = 0, kuse = 0;             // K slot of this block and its use count
       bool ok = true;
@@ -873,15 +909,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             const uint64_t dK = desc_add(dR0, sk * TILE), dV = desc_add(dR0, DQ_VSLOT * TILE);
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk)
-              tc_mma_bf16(tmem + TQ_S, desc_add(dQd, kmajor_off(kk, ATOM128)),
-                          desc_add(dK, kmajor_off(kk, ATOM128)), id_s, kk > 0);
+              tc_mma_bf16(tmem + TQ_S, desc_add(dQd, F::koff(kk)), desc_add(dK, F::koff(kk)), id_s,
+                          kk > 0);
             // V(j) may land after S is under way
             if (!wait(RF + DQ_VSLOT, nb)) break;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk)
-              tc_mma_bf16(tmem + TQ_DP, desc_add(dDO, kmajor_off(kk, ATOM128)),
-                          desc_add(dV, kmajor_off(kk, ATOM128)), id_s, kk > 0);
+              tc_mma_bf16(tmem + TQ_DP, desc_add(dDO, F::koff(kk)), desc_add(dV, F::koff(kk)), id_s,
+                          kk > 0);
             tc_commit(B(SF));
             tc_commit(B(RE + sk));
             tc_commit(B(RE + DQ_VSLOT));
@@ -893,7 +929,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             const uint64_t dKmn = desc_add(dRmn0, sk * TILE);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              tc_mma_bf16_ts(tmem + TQ_ACC, tmem + TQ_DS + 8 * kk, desc_add(dKmn, mnmajor_off(kk)),
+              tc_mma_bf16_ts(tmem + TQ_ACC, tmem + TQ_DS + 8 * kk, desc_add(dKmn, F::mnoff(kk)),
                              id_acc, (j > 0 || kk > 0) ? 1u : 0u);
             tc_commit(B(DQD));
             tc_commit(B(RE + sk));
@@ -957,7 +993,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 #pragma unroll
       for (int i = 0; i < D / 16; ++i) {
         const int c = wg * (D / 16) + i;
-        const uint32_t off = (c >> 3) * ATOM128 + sw128_offset(r, c & 7);
+        const uint32_t off = F::chunk(r, c);
         Vec<bf16> go, oo;
         go.raw = ld_shared_v4(sDO + off);
         oo.raw = ld_shared_v4(sO + off);
@@ -1083,19 +1119,20 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 // dO and dK += dS^T Q (warp 2, A operands from TMEM).  An item's dK and dV are
 // written out when the rows take the next item (its last dV and dK products
 // done), while that item's K, V and first S^T are on their way.
-// smem: K, V, ring[BWD_RING] (NA atoms of 16 KB each), lse and D of the two Q
+// smem: K, V, ring[BWD_RING] (tiles in the Fmt layout), lse and D of the two Q
 // slots, item ids.  TMEM: S^T / dP^T 0..127, P^T 128..191, dS^T 192..255,
 // dV 256.., dK 384..
 constexpr uint32_t TK_S = 0, TK_P = 128, TK_DS = 192, TK_DV = 256, TK_DK = 384;
 
-template <int NA, int KS, bool DROP>
+template <int KS, bool DROP>
 __global__ void __launch_bounds__(BWD_THREADS, 1)
     attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm,
                            const __grid_constant__ CUtensorMap tmdo,
                            const __grid_constant__ CUtensorMap tmdq, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const Smem sm = smem_aligned(smem_raw);
-  constexpr uint32_t TILE = NA * ATOM128;
+  using F = Fmt<KS>;
+  constexpr uint32_t TILE = F::TILE;
   constexpr int D = KS * 16;
   const uint32_t sK = sm.u32, sV = sK + TILE, sR0 = sK + 2 * TILE;
   const uint32_t sStage = sK + (2 + BWD_RING) * TILE;   // epilogue staging, 2 KB a row warp
@@ -1149,11 +1186,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         if (nit > 0 && !mbar_wait_bounded(B(KVE), (nit - 1) & 1, p.status, abort_flag)) break;
         ++nit;
         mbar_arrive_expect_tx(B(KVF), 2 * TILE);
-        for (int a = 0; a < NA; ++a) {
-          load_box(sK + a * ATOM128, &tm, B(KVF), colq + p.d + 64 * a, row0 + it.blk * 128,
-                   3 * (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnDkvLoad);
-          load_box(sV + a * ATOM128, &tm, B(KVF), colq + 2 * p.d + 64 * a, row0 + it.blk * 128,
-                   3 * (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnDkvLoad);
+        for (int a = 0; a < F::ATOMS; ++a) {
+          load_box(sK + a * F::ATOM, &tm, B(KVF), colq + p.d + F::ACOLS * a, row0 + it.blk * 128,
+                   3 * (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnDkvLoad, F::ACOLS);
+          load_box(sV + a * F::ATOM, &tm, B(KVF), colq + 2 * p.d + F::ACOLS * a, row0 + it.blk * 128,
+                   3 * (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnDkvLoad, F::ACOLS);
         }
         for (int i = it.blk; i < p.nqb && ok; ++i) {
           for (int qd = 0; qd < 2; ++qd, ++g) {
@@ -1165,17 +1202,18 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             if (qd == 0) {
               // Q(i) with the lse and D of its queries
               mbar_arrive_expect_tx(B(RF + s), TILE + 1024);
-              for (int a = 0; a < NA; ++a)
-                load_box(sR0 + s * TILE + a * ATOM128, &tm, B(RF + s), colq + 64 * a,
-                         row0 + i * 128, 3 * (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnDkvQ);
+              for (int a = 0; a < F::ATOMS; ++a)
+                load_box(sR0 + s * TILE + a * F::ATOM, &tm, B(RF + s), colq + F::ACOLS * a, row0 + i * 128,
+                         3 * (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnDkvQ, F::ACOLS);
               const size_t lo = ((size_t)it.b * p.heads + it.hd) * p.seq + (size_t)i * 128;
               bulk_load(s_ld_u32 + (s >> 1) * 1024, p.lse + lo, 512, B(RF + s));
               bulk_load(s_ld_u32 + (s >> 1) * 1024 + 512, p.dsum + lo, 512, B(RF + s));
             } else {
               mbar_arrive_expect_tx(B(RF + s), TILE);
-              for (int a = 0; a < NA; ++a)
-                load_box(sR0 + s * TILE + a * ATOM128, &tmdo, B(RF + s), it.hd * p.d + 64 * a,
-                         row0 + i * 128, (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnDkvQ);
+              for (int a = 0; a < F::ATOMS; ++a)
+                load_box(sR0 + s * TILE + a * F::ATOM, &tmdo, B(RF + s), it.hd * p.d + F::ACOLS * a,
+                         row0 + i * 128, (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnDkvQ,
+                         F::ACOLS);
             }
           }
         }
@@ -1190,8 +1228,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const bool first = warp == 1;
       const uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
       const uint32_t id_acc = idesc_bf16_f32(128, D, false, true);
-      const uint64_t dKd = desc_kbase(sK), dVd = desc_kbase(sV), dR0 = desc_kbase(sR0);
-      const uint64_t dRmn0 = desc_mnbase(sR0, ATOM128);
+      const uint64_t dKd = F::kdesc(sK), dVd = F::kdesc(sV), dR0 = F::kdesc(sR0);
+      const uint64_t dRmn0 = F::mndesc(sR0);
       int g = 0, ni = 0, nit = 0, nb = 0;
       bool ok = true;
       auto wait = [&](int bar, int k) -> bool {
@@ -1215,16 +1253,16 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             const uint64_t dQ = desc_add(dR0, sq * TILE), dDO = desc_add(dR0, sd * TILE);
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk)
-              tc_mma_bf16(tmem + TK_S, desc_add(dKd, kmajor_off(kk, ATOM128)),
-                          desc_add(dQ, kmajor_off(kk, ATOM128)), id_s, kk > 0);
+              tc_mma_bf16(tmem + TK_S, desc_add(dKd, F::koff(kk)), desc_add(dQ, F::koff(kk)), id_s,
+                          kk > 0);
             tc_commit(B(SF));
             tc_commit(B(RE + sq));
             if (!wait(RF + sd, gd / BWD_RING) || !wait(SE, nb)) break;   // rows read S^T
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk)
-              tc_mma_bf16(tmem + TK_S, desc_add(dVd, kmajor_off(kk, ATOM128)),
-                          desc_add(dDO, kmajor_off(kk, ATOM128)), id_s, kk > 0);
+              tc_mma_bf16(tmem + TK_S, desc_add(dVd, F::koff(kk)), desc_add(dDO, F::koff(kk)), id_s,
+                          kk > 0);
             tc_commit(B(DPF));
             tc_commit(B(RE + sd));
             if (i == nq - 1) tc_commit(B(KVE));
@@ -1234,7 +1272,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             const uint64_t dDOmn = desc_add(dRmn0, sd * TILE), dQmn = desc_add(dRmn0, sq * TILE);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              tc_mma_bf16_ts(tmem + TK_DV, tmem + TK_P + 8 * kk, desc_add(dDOmn, mnmajor_off(kk)),
+              tc_mma_bf16_ts(tmem + TK_DV, tmem + TK_P + 8 * kk, desc_add(dDOmn, F::mnoff(kk)),
                              id_acc, (i > 0 || kk > 0) ? 1u : 0u);
             tc_commit(B(PE));
             tc_commit(B(RE + sd));
@@ -1242,7 +1280,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              tc_mma_bf16_ts(tmem + TK_DK, tmem + TK_DS + 8 * kk, desc_add(dQmn, mnmajor_off(kk)),
+              tc_mma_bf16_ts(tmem + TK_DK, tmem + TK_DS + 8 * kk, desc_add(dQmn, F::mnoff(kk)),
                              id_acc, (i > 0 || kk > 0) ? 1u : 0u);
             tc_commit(B(DSE));
             tc_commit(B(RE + sq));
@@ -1479,18 +1517,18 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uin
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t fwd_smem(int na) {
-  const size_t need = (size_t)(2 + FWD_RING) * na * ATOM128 + STAGE_BYTES + 256 + 1024;
+size_t fwd_smem(uint32_t tile) {
+  const size_t need = (size_t)(2 + FWD_RING) * tile + STAGE_BYTES + 256 + 1024;
   return need < 120 * 1024 ? 120 * 1024 : need;   // one CTA per SM (512 TMEM columns)
 }
 // The backward kernels hold all 512 TMEM columns: their shared memory requests
 // keep them at one CTA per SM so a second CTA never waits in tcgen05.alloc.
-size_t dq_smem(int na) {
-  const size_t need = (size_t)(3 + BWD_RING) * na * ATOM128 + 256 + 1024 + 1024;
+size_t dq_smem(uint32_t tile) {
+  const size_t need = (size_t)(3 + BWD_RING) * tile + 256 + 1024 + 1024;
   return need < 120 * 1024 ? 120 * 1024 : need;   // one CTA per SM (512 TMEM columns)
 }
-size_t dkv_smem(int na) {
-  const size_t need = (size_t)(2 + BWD_RING) * na * ATOM128 + STAGE_BYTES + 2048 + 256 + 1024;
+size_t dkv_smem(uint32_t tile) {
+  const size_t need = (size_t)(2 + BWD_RING) * tile + STAGE_BYTES + 2048 + 256 + 1024;
   return need < 120 * 1024 ? 120 * 1024 : need;
 }
 
@@ -1518,9 +1556,9 @@ Params make_params(int batch, int seq, int heads, int d, unsigned* status, const
 }
 
 // (batch, head) pairs per scheduling chunk: pairs whose two streamed operands
-// (NA 128-byte boxes per row each) fit in about 48 MB of L2 together.
+// (d bf16 a row each) fit in about 48 MB of L2 together.
 int l2_chunk(int batch, int seq, int heads, int d) {
-  const size_t per_pair = 2ull * seq * (d > 64 ? 2 : 1) * 128;
+  const size_t per_pair = 2ull * seq * d * 2;
   const size_t c = ((size_t)48 << 20) / per_pair;
   const size_t pairs = (size_t)batch * heads;
   return c < 1 ? 1 : (int)(c > pairs ? pairs : c);
@@ -1556,7 +1594,10 @@ cudaError_t attn_fwd_tc(const void* qkv, void* ctx, float* lse, int batch, int s
   if (batch == 0) return cudaSuccess;
   if (!attn_tc_supported(seq, d)) return cudaErrorInvalidValue;
   CUtensorMap tm, tmc;
-  if (!make_map(&tm, qkv, 3ull * heads * d, (uint64_t)batch * seq, 128) ||
+  const bool sw64 = d % 64 != 0;   // the operand tiles' format (Fmt)
+  const uint32_t acols = sw64 ? 32 : 64;
+  const CUtensorMapSwizzle asw = sw64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+  if (!make_map(&tm, qkv, 3ull * heads * d, (uint64_t)batch * seq, 128, acols, asw) ||
       !make_map(&tmc, ctx, (uint64_t)heads * d, (uint64_t)batch * seq, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   if (drop.on && !mask) return cudaErrorInvalidValue;
@@ -1570,23 +1611,23 @@ cudaError_t attn_fwd_tc(const void* qkv, void* ctx, float* lse, int batch, int s
   const int grid = items < c.num_sms ? items : c.num_sms;
   const double flops = 2.0 * 2.0 * batch * heads * d * ((double)seq * (seq + 1) / 2.0);
   cudaError_t e;
-#define FWD_CASE(NA_, KS_, DR_)                                                          \
-  {                                                                                      \
-    const size_t sm = fwd_smem(NA_);                                                     \
-    if ((e = set_smem(attn_fwd_tc_kernel<NA_, KS_, DR_>, sm)) != cudaSuccess) return e;  \
-    if ((e = check_regs(attn_fwd_tc_kernel<NA_, KS_, DR_>, FWD_LAUNCH_REGS)) != cudaSuccess) \
-      return e;                                                                          \
-    c.before(KK_ATTN_FWD, flops);                                                        \
-    attn_fwd_tc_kernel<NA_, KS_, DR_><<<grid, FWD_THREADS, sm, c.stream>>>(tm, tmc, p);  \
+#define FWD_CASE(KS_, DR_)                                                                         \
+  {                                                                                                \
+    const size_t sm = fwd_smem(Fmt<KS_>::TILE);                                                    \
+    if ((e = set_smem(attn_fwd_tc_kernel<KS_, DR_>, sm)) != cudaSuccess) return e;                 \
+    if ((e = check_regs(attn_fwd_tc_kernel<KS_, DR_>, FWD_LAUNCH_REGS)) != cudaSuccess)            \
+      return e;                                                                                    \
+    c.before(KK_ATTN_FWD, flops);                                                                  \
+    attn_fwd_tc_kernel<KS_, DR_><<<grid, FWD_THREADS, sm, c.stream>>>(tm, tmc, p);                 \
   }
   if (drop.on) {
-    if (d == 64) FWD_CASE(1, 4, true)
-    else if (d == 96) FWD_CASE(2, 6, true)
-    else FWD_CASE(2, 8, true)
+    if (d == 64) FWD_CASE(4, true)
+    else if (d == 96) FWD_CASE(6, true)
+    else FWD_CASE(8, true)
   } else {
-    if (d == 64) FWD_CASE(1, 4, false)
-    else if (d == 96) FWD_CASE(2, 6, false)
-    else FWD_CASE(2, 8, false)
+    if (d == 64) FWD_CASE(4, false)
+    else if (d == 96) FWD_CASE(6, false)
+    else FWD_CASE(8, false)
   }
 #undef FWD_CASE
   c.after();
@@ -1602,9 +1643,12 @@ cudaError_t attn_bwd_tc(const void* qkv, const void* ctx, const float* lse, cons
   if (!attn_tc_supported(seq, d)) return cudaErrorInvalidValue;
   const uint64_t n = (uint64_t)batch * seq;
   CUtensorMap tm, tmdo, tmo, tmdq;
-  if (!make_map(&tm, qkv, 3ull * heads * d, n, 128) ||
-      !make_map(&tmdo, dctx, (uint64_t)heads * d, n, 128) ||
-      !make_map(&tmo, ctx, (uint64_t)heads * d, n, 128) ||
+  const bool sw64 = d % 64 != 0;   // the operand tiles' format (Fmt)
+  const uint32_t acols = sw64 ? 32 : 64;
+  const CUtensorMapSwizzle asw = sw64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+  if (!make_map(&tm, qkv, 3ull * heads * d, n, 128, acols, asw) ||
+      !make_map(&tmdo, dctx, (uint64_t)heads * d, n, 128, acols, asw) ||
+      !make_map(&tmo, ctx, (uint64_t)heads * d, n, 128, acols, asw) ||
       !make_map(&tmdq, dqkv, 3ull * heads * d, n, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   if (drop.on && !mask) return cudaErrorInvalidValue;
@@ -1620,32 +1664,32 @@ cudaError_t attn_bwd_tc(const void* qkv, const void* ctx, const float* lse, cons
   const int grid = items < c.num_sms ? items : c.num_sms;
   const double tri = (double)batch * heads * d * ((double)seq * (seq + 1) / 2.0);
   cudaError_t e;
-#define BWD_CASE(NA_, KS_, DR_)                                                                \
-  {                                                                                            \
-    auto kq = attn_bwd_dq_tc_kernel<NA_, KS_, DR_>;                                            \
-    auto kk = attn_bwd_dkv_tc_kernel<NA_, KS_, DR_>;                                           \
-    if ((e = set_smem(kq, dq_smem(NA_))) != cudaSuccess) return e;                             \
-    if ((e = set_smem(kk, dkv_smem(NA_))) != cudaSuccess) return e;                            \
-    if ((e = check_regs(kq, BWD_LAUNCH_REGS)) != cudaSuccess) return e;                        \
-    if ((e = check_regs(kk, BWD_LAUNCH_REGS)) != cudaSuccess) return e;                        \
-    c.before(KK_ATTN_BWD, 2.0 * 3.0 * tri);                                                    \
-    p.sched = status + kSchedDq;                                                               \
-    kq<<<grid, BWD_THREADS, dq_smem(NA_), c.stream>>>(tm, tmdo, tmo, tmdq, p);                 \
-    c.after();                                                                                 \
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;                                     \
-    c.before(KK_ATTN_BWD, 2.0 * 4.0 * tri);                                                    \
-    p.sched = status + kSchedDkv;                                                              \
-    kk<<<grid, BWD_THREADS, dkv_smem(NA_), c.stream>>>(tm, tmdo, tmdq, p);                     \
-    c.after();                                                                                 \
+#define BWD_CASE(KS_, DR_)                                                                         \
+  {                                                                                                \
+    auto kq = attn_bwd_dq_tc_kernel<KS_, DR_>;                                                     \
+    auto kk = attn_bwd_dkv_tc_kernel<KS_, DR_>;                                                    \
+    if ((e = set_smem(kq, dq_smem(Fmt<KS_>::TILE))) != cudaSuccess) return e;                      \
+    if ((e = set_smem(kk, dkv_smem(Fmt<KS_>::TILE))) != cudaSuccess) return e;                     \
+    if ((e = check_regs(kq, BWD_LAUNCH_REGS)) != cudaSuccess) return e;                            \
+    if ((e = check_regs(kk, BWD_LAUNCH_REGS)) != cudaSuccess) return e;                            \
+    c.before(KK_ATTN_BWD, 2.0 * 3.0 * tri);                                                        \
+    p.sched = status + kSchedDq;                                                                   \
+    kq<<<grid, BWD_THREADS, dq_smem(Fmt<KS_>::TILE), c.stream>>>(tm, tmdo, tmo, tmdq, p);          \
+    c.after();                                                                                     \
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;                                         \
+    c.before(KK_ATTN_BWD, 2.0 * 4.0 * tri);                                                        \
+    p.sched = status + kSchedDkv;                                                                  \
+    kk<<<grid, BWD_THREADS, dkv_smem(Fmt<KS_>::TILE), c.stream>>>(tm, tmdo, tmdq, p);              \
+    c.after();                                                                                     \
   }
   if (drop.on) {
-    if (d == 64) BWD_CASE(1, 4, true)
-    else if (d == 96) BWD_CASE(2, 6, true)
-    else BWD_CASE(2, 8, true)
+    if (d == 64) BWD_CASE(4, true)
+    else if (d == 96) BWD_CASE(6, true)
+    else BWD_CASE(8, true)
   } else {
-    if (d == 64) BWD_CASE(1, 4, false)
-    else if (d == 96) BWD_CASE(2, 6, false)
-    else BWD_CASE(2, 8, false)
+    if (d == 64) BWD_CASE(4, false)
+    else if (d == 96) BWD_CASE(6, false)
+    else BWD_CASE(8, false)
   }
 #undef BWD_CASE
   return cudaGetLastError();

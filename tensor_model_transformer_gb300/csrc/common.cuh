@@ -342,15 +342,20 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 // Shared-memory matrix descriptor (tcgen05 form): start address, leading and
 // stride byte offsets (all >> 4), the fixed version bits 46..47 = 1, base
 // offset 0 (tiles are 1024-byte aligned), swizzle mode in bits 61..63
-// (2 = 128-byte swizzle).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+// (2 = 128-byte swizzle, 4 = 64-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t mode) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
   d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
   d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
   d |= 1ull << 46;
-  d |= 2ull << 61;
+  d |= static_cast<uint64_t>(mode & 7u) << 61;
   return d;
+}
+// swizzle modes of the descriptor
+constexpr uint32_t kDescSw128 = 2, kDescSw64 = 4;
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return smem_desc(addr, lbo, sbo, kDescSw128);
 }
 
 // Instruction descriptor of tcgen05.mma kind::f16 with bf16 A/B and fp32
