@@ -686,6 +686,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
 // halves never need each other).  A slot of the TMA ring that both issuers
 // read is released by two commits.
 constexpr int BWD_RING = 4;
+constexpr size_t kSmemMax = 227 * 1024;   // dynamic shared memory a CTA may request
 static_assert(BWD_RING % 2 == 0, "each ring slot keeps to one operand");
 
 struct BwdItem {
@@ -762,6 +763,14 @@ static_assert(BWD_THREADS == 384, "one giving and two taking warps per sub-parti
 static_assert(BWD_LOW_REGS + 2 * BWD_ROW_REGS <= 3 * BWD_LAUNCH_REGS,
               "register split exceeds a sub-partition's launch allocation");
 
+// Shared memory of the dQ kernel with `qb` Q/dO buffer pairs of `tile` bytes.
+__host__ __device__ constexpr size_t dq_need(uint32_t tile, int qb) {
+  return (size_t)(2 * qb + 1 + BWD_RING) * tile + 256 + 1024 + 1024;
+}
+// Q and dO are double-buffered when the tiles leave room (d = 64, 96), so the
+// next item's Q and dO load while the current item runs.
+__host__ __device__ constexpr int dq_q_bufs(uint32_t tile) { return dq_need(tile, 2) <= kSmemMax ? 2 : 1; }
+
 // ============================================================================ dQ
 // Item: 128 queries (Q, dO resident) against key blocks j = 0..qb of 128 keys
 // (K(j), V(j) through the ring).  Per block: S = Q K^T and dP = dO V^T (warp
@@ -793,17 +802,21 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   using F = Fmt<KS>;
   constexpr uint32_t TILE = F::TILE;
   constexpr int D = KS * 16;
-  const uint32_t sQ = sm.u32, sDO = sQ + TILE, sO = sQ + 2 * TILE, sR0 = sQ + 3 * TILE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm.base + (3 + BWD_RING) * TILE);
+  constexpr int NQB = dq_q_bufs(TILE);   // Q/dO buffers: item m uses buffer m % NQB
+  // Q(u) at sQ + 2u TILE with dO(u) after it; then O, then the ring
+  const uint32_t sQ = sm.u32, sO = sQ + 2 * NQB * TILE, sR0 = sO + TILE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm.base + (2 * NQB + 1 + BWD_RING) * TILE);
   const uint32_t bar0 = smem_u32(bars);
   auto B = [&](int i) { return bar0 + 8u * i; };
-  // QE: the item's last S / dP product is done with Q and dO; DE: the row
-  // threads are done reading dO and O for D (for a one-block item the product
-  // can finish before the rows get to D, so both gate the next load)
-  constexpr int QF = 0, QE = 1, RF = 2, RE = RF + BWD_RING, SF = RE + BWD_RING, SE = SF + 1,
+  // QF / QE (one per Q/dO buffer): Q and dO loaded / the item's last S and dP
+  // products done with them; OF: O loaded; DE: the row threads are done with
+  // dO and O for D and with the O tile as staging (for a one-block item the
+  // products can finish before the rows get to D, so the rows gate dO too)
+  constexpr int QF = 0, QE = 2, OF = 4, RF = 5, RE = RF + BWD_RING, SF = RE + BWD_RING, SE = SF + 1,
                 DSF = SE + 1, DQD = DSF + 1, DE = DQD + 1, IF = DE + 1, IE = IF + 2, NBAR = IE + 2;
   // the two warpgroups' halves of D for the item's 128 rows
-  volatile float* s_dhalf = reinterpret_cast<volatile float*>(sm.base + (3 + BWD_RING) * TILE + 256);
+  volatile float* s_dhalf =
+      reinterpret_cast<volatile float*>(sm.base + (2 * NQB + 1 + BWD_RING) * TILE + 256);
   int* s_item = reinterpret_cast<int*>(bars + NBAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_item + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -843,19 +856,27 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         if (!item_publish(iq, ni++, k, p.status, abort_flag) || k >= n_items) break;
         const BwdItem it = bwd_item(p, k, true);
         const int colq = it.hd * 3 * p.d, row0 = it.b * p.seq;
-        if (nit > 0 && (!mbar_wait_bounded(B(QE), (nit - 1) & 1, p.status, abort_flag) ||
-                        !mbar_wait_bounded(B(DE), (nit - 1) & 1, p.status, abort_flag)))
-          break;
-        ++nit;
-        mbar_arrive_expect_tx(B(QF), 3 * TILE);
+        // Q and dO of item nit into buffer u once item nit - NQB is done with
+        // them (its products, and its rows' D: waited on below for the
+        // previous item, before its O load); then O once the rows are done
+        // with the previous item's O
+        const int u = nit % NQB, use = nit / NQB;
+        if (use > 0 && !mbar_wait_bounded(B(QE + u), (use - 1) & 1, p.status, abort_flag)) break;
+        if (NQB == 1 && nit > 0 && !mbar_wait_bounded(B(DE), (nit - 1) & 1, p.status, abort_flag)) break;
+        const uint32_t sQu = sQ + 2 * u * TILE, sDOu = sQu + TILE;
+        mbar_arrive_expect_tx(B(QF + u), 2 * TILE);
         for (int a = 0; a < F::ATOMS; ++a) {
-          load_box(sQ + a * F::ATOM, &tm, B(QF), colq + F::ACOLS * a, row0 + it.blk * 128,
+          load_box(sQu + a * F::ATOM, &tm, B(QF + u), colq + F::ACOLS * a, row0 + it.blk * 128,
                    3 * (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnDqLoad, F::ACOLS);
-          load_box(sDO + a * F::ATOM, &tmdo, B(QF), it.hd * p.d + F::ACOLS * a, row0 + it.blk * 128,
-                   (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnDqLoad, F::ACOLS);
-          load_box(sO + a * F::ATOM, &tmo, B(QF), it.hd * p.d + F::ACOLS * a, row0 + it.blk * 128,
+          load_box(sDOu + a * F::ATOM, &tmdo, B(QF + u), it.hd * p.d + F::ACOLS * a, row0 + it.blk * 128,
                    (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnDqLoad, F::ACOLS);
         }
+        if (NQB == 2 && nit > 0 && !mbar_wait_bounded(B(DE), (nit - 1) & 1, p.status, abort_flag)) break;
+        ++nit;
+        mbar_arrive_expect_tx(B(OF), TILE);
+        for (int a = 0; a < F::ATOMS; ++a)
+          load_box(sO + a * F::ATOM, &tmo, B(OF), it.hd * p.d + F::ACOLS * a, row0 + it.blk * 128,
+                   (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnDqLoad, F::ACOLS);
         for (int j = 0; j <= it.blk && ok; ++j, ++g) {   // g: blocks so far
           for (int kv = 0; kv < 2; ++kv) {
             const int s = kv ? DQ_VSLOT : ksl, use = kv ? g : kuse;
@@ -885,7 +906,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const bool first = warp == 1;
       const uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
       const uint32_t id_acc = idesc_bf16_f32(128, D, false, true);
-      const uint64_t dQd = F::kdesc(sQ), dDO = F::kdesc(sDO), dR0 = F::kdesc(sR0);
+      const uint64_t dQ0 = F::kdesc(sQ), dR0 = F::kdesc(sR0);
       const uint64_t dRmn0 = F::mndesc(sR0);
       int ni = 0, nit = 0, nb = 0;      // nb: blocks so far
       int sk = 0, kuse = 0;             // K slot of this block and its use count
@@ -900,9 +921,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         if (k >= n_items) break;
         const BwdItem it = bwd_item(p, k, true);
         const int nkv = it.blk + 1;
+        const int u = nit % NQB;
+        const uint64_t dQd = desc_add(dQ0, 2 * u * TILE), dDO = desc_add(dQd, TILE);
         for (int j = 0; j < nkv && ok; ++j, ++nb) {
           if (first) {
-            if (j == 0 && !wait(QF, nit)) break;
+            if (j == 0 && !wait(QF + u, nit / NQB)) break;
             if (!wait(RF + sk, kuse)) break;
             if (nb > 0 && !wait(SE, nb - 1)) break;   // the row threads hold S, dP of the last block
             tc_fence_after();
@@ -921,7 +944,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             tc_commit(B(SF));
             tc_commit(B(RE + sk));
             tc_commit(B(RE + DQ_VSLOT));
-            if (j == nkv - 1) tc_commit(B(QE));
+            if (j == nkv - 1) tc_commit(B(QE + u));
           } else {
             if (!wait(DSF, nb)) break;                // dS of this block is in TMEM
             if (!wait(RF + sk, kuse)) break;
@@ -982,7 +1005,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       // D_r = dO_r . O_r from the tiles in shared memory (they are not reloaded
       // before every row thread has arrived on DE, after the previous item's
       // epilogue below)
-      if (!mbar_wait_bounded(B(QF), nit & 1, p.status, abort_flag)) {
+      const int u = nit % NQB;
+      const uint32_t sDO = sQ + (2 * u + 1) * TILE;
+      if (!mbar_wait_bounded(B(QF + u), (nit / NQB) & 1, p.status, abort_flag) ||
+          !mbar_wait_bounded(B(OF), nit & 1, p.status, abort_flag)) {
         ok = false;
         break;
       }
@@ -1110,6 +1136,14 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   }
 }
 
+// Shared memory of the dK/dV kernel with `kvb` K/V buffers of `tile` bytes.
+__host__ __device__ constexpr size_t dkv_need(uint32_t tile, int kvb) {
+  return (size_t)(2 * kvb + BWD_RING) * tile + STAGE_BYTES + 2048 + 256 + 1024;
+}
+// K and V are double-buffered when the tiles leave room (d = 64, 96), so the
+// next item's K and V load while the current item runs.
+__host__ __device__ constexpr int dkv_kv_bufs(uint32_t tile) { return dkv_need(tile, 2) <= kSmemMax ? 2 : 1; }
+
 // ============================================================================ dK, dV
 // Item: 128 keys (K, V resident) against query blocks i = kb..nqb-1 (Q(i) with
 // the lse and D of its queries, dO(i): through the ring).  Per block: S^T =
@@ -1134,15 +1168,17 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   using F = Fmt<KS>;
   constexpr uint32_t TILE = F::TILE;
   constexpr int D = KS * 16;
-  const uint32_t sK = sm.u32, sV = sK + TILE, sR0 = sK + 2 * TILE;
-  const uint32_t sStage = sK + (2 + BWD_RING) * TILE;   // epilogue staging, 2 KB a row warp
+  constexpr int NKV = dkv_kv_bufs(TILE);   // K/V buffers: item m uses buffer m % NKV
+  const uint32_t sK = sm.u32, sR0 = sK + 2 * NKV * TILE;   // K(u) at sK + 2u TILE, V(u) after it
+  const uint32_t sStage = sR0 + BWD_RING * TILE;           // epilogue staging, 2 KB a row warp
   // lse, D of the queries in Q slot 2m: 128 + 128 floats at s_ld + 256 m
-  float* s_ld = reinterpret_cast<float*>(sm.base + (2 + BWD_RING) * TILE + STAGE_BYTES);
+  float* s_ld = reinterpret_cast<float*>(sm.base + (2 * NKV + BWD_RING) * TILE + STAGE_BYTES);
   const uint32_t s_ld_u32 = smem_u32(s_ld);
   uint64_t* bars = reinterpret_cast<uint64_t*>(s_ld + 128 * BWD_RING);
   const uint32_t bar0 = smem_u32(bars);
   auto B = [&](int i) { return bar0 + 8u * i; };
-  constexpr int KVF = 0, KVE = 1, RF = 2, RE = RF + BWD_RING, SF = RE + BWD_RING, SE = SF + 1,
+  // KVF / KVE: one barrier per K/V buffer
+  constexpr int KVF = 0, KVE = 2, RF = 4, RE = RF + BWD_RING, SF = RE + BWD_RING, SE = SF + 1,
                 DPF = SE + 1, DPE = DPF + 1, PF = DPE + 1, PE = PF + 1, DSF = PE + 1,
                 DSE = DSF + 1, IF = DSE + 1, IE = IF + 2, NBAR = IE + 2;
   int* s_item = reinterpret_cast<int*>(bars + NBAR);
@@ -1183,13 +1219,16 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         if (!item_publish(iq, ni++, k, p.status, abort_flag) || k >= n_items) break;
         const BwdItem it = bwd_item(p, k, false);
         const int colq = it.hd * 3 * p.d, row0 = it.b * p.seq;
-        if (nit > 0 && !mbar_wait_bounded(B(KVE), (nit - 1) & 1, p.status, abort_flag)) break;
+        // K and V of item nit into buffer u once item nit - NKV is done with it
+        const int u = nit % NKV, use = nit / NKV;
+        if (use > 0 && !mbar_wait_bounded(B(KVE + u), (use - 1) & 1, p.status, abort_flag)) break;
         ++nit;
-        mbar_arrive_expect_tx(B(KVF), 2 * TILE);
+        const uint32_t sKu = sK + 2 * u * TILE, sVu = sKu + TILE;
+        mbar_arrive_expect_tx(B(KVF + u), 2 * TILE);
         for (int a = 0; a < F::ATOMS; ++a) {
-          load_box(sK + a * F::ATOM, &tm, B(KVF), colq + p.d + F::ACOLS * a, row0 + it.blk * 128,
+          load_box(sKu + a * F::ATOM, &tm, B(KVF + u), colq + p.d + F::ACOLS * a, row0 + it.blk * 128,
                    3 * (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnDkvLoad, F::ACOLS);
-          load_box(sV + a * F::ATOM, &tm, B(KVF), colq + 2 * p.d + F::ACOLS * a, row0 + it.blk * 128,
+          load_box(sVu + a * F::ATOM, &tm, B(KVF + u), colq + 2 * p.d + F::ACOLS * a, row0 + it.blk * 128,
                    3 * (int64_t)p.h, (int64_t)p.batch * p.seq, p.status, bounds::kSiteAttnDkvLoad, F::ACOLS);
         }
         for (int i = it.blk; i < p.nqb && ok; ++i) {
@@ -1228,7 +1267,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const bool first = warp == 1;
       const uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
       const uint32_t id_acc = idesc_bf16_f32(128, D, false, true);
-      const uint64_t dKd = F::kdesc(sK), dVd = F::kdesc(sV), dR0 = F::kdesc(sR0);
+      const uint64_t dK0 = F::kdesc(sK), dR0 = F::kdesc(sR0);
       const uint64_t dRmn0 = F::mndesc(sR0);
       int g = 0, ni = 0, nit = 0, nb = 0;
       bool ok = true;
@@ -1242,11 +1281,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         if (k >= n_items) break;
         const BwdItem it = bwd_item(p, k, false);
         const int nq = p.nqb - it.blk;
+        const int u = nit % NKV;
+        const uint64_t dKd = desc_add(dK0, 2 * u * TILE), dVd = desc_add(dKd, TILE);
         for (int i = 0; i < nq && ok; ++i, ++nb) {
           const int gq = g + 2 * i, gd = gq + 1;
           const int sq = gq % BWD_RING, sd = gd % BWD_RING;
           if (first) {
-            if (i == 0 && !wait(KVF, nit)) break;
+            if (i == 0 && !wait(KVF + u, nit / NKV)) break;
             if (!wait(RF + sq, gq / BWD_RING)) break;
             if (nb > 0 && !wait(DPE, nb - 1)) break;   // the rows hold dP^T of the last block
             tc_fence_after();
@@ -1265,7 +1306,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                           kk > 0);
             tc_commit(B(DPF));
             tc_commit(B(RE + sd));
-            if (i == nq - 1) tc_commit(B(KVE));
+            if (i == nq - 1) tc_commit(B(KVE + u));
           } else {
             if (!wait(PF, nb) || !wait(RF + sd, gd / BWD_RING)) break;
             tc_fence_after();
@@ -1524,11 +1565,11 @@ size_t fwd_smem(uint32_t tile) {
 // The backward kernels hold all 512 TMEM columns: their shared memory requests
 // keep them at one CTA per SM so a second CTA never waits in tcgen05.alloc.
 size_t dq_smem(uint32_t tile) {
-  const size_t need = (size_t)(3 + BWD_RING) * tile + 256 + 1024 + 1024;
+  const size_t need = dq_need(tile, dq_q_bufs(tile));
   return need < 120 * 1024 ? 120 * 1024 : need;   // one CTA per SM (512 TMEM columns)
 }
 size_t dkv_smem(uint32_t tile) {
-  const size_t need = (size_t)(2 + BWD_RING) * tile + STAGE_BYTES + 2048 + 256 + 1024;
+  const size_t need = dkv_need(tile, dkv_kv_bufs(tile));
   return need < 120 * 1024 ? 120 * 1024 : need;
 }
 
