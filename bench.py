@@ -53,6 +53,7 @@ def megatron_flops(s):
 # Idle seconds before the end-to-end pass, so that it starts from the same
 # rested clock state as the device-only pass.
 REST_S = 1.5
+E2E_PASSES = 3   # timed end-to-end passes; the median is reported
 # Nominal dense (no 2:4 sparsity) tensor rates of a GB300, TFLOP/s.
 NOMINAL_TFLOPS = {"bf16": 2250.0, "fp8": 4500.0}
 # Below this timed-region length a kernel is timed as a burst, so the burst
@@ -693,13 +694,21 @@ def main():
         return e0.elapsed_time(e1), tev, e0, host_ms
 
     e2e_pass(3)                                      # untimed: wake up after the rest
-    barrier()
-    gc.collect()
-    gc.disable()
-    t_e2e = time.monotonic()
-    ms_e2e, tev, e0, host_ms = e2e_pass(args.steps)
-    gc.enable()
-    e2e_clk = clocks.window(t_e2e, time.monotonic())
+    # Three timed passes of K steps each; the median one is reported (a single
+    # host stall -- a descheduled enqueue thread -- once delayed the first copy
+    # of a pass by 13 ms), all three are listed in e2e.passes_ms.
+    passes = []
+    for _ in range(E2E_PASSES):
+        barrier()
+        gc.collect()
+        gc.disable()
+        t_e2e = time.monotonic()
+        res = e2e_pass(args.steps)
+        gc.enable()
+        passes.append((res, t_e2e, time.monotonic()))
+    order = sorted(range(len(passes)), key=lambda i: passes[i][0][0])
+    (ms_e2e, tev, e0, host_ms), t_e2e, t_e2e_end = passes[order[len(order) // 2]]
+    e2e_clk = clocks.window(t_e2e, t_e2e_end)
     med = lambda v: sorted(v)[len(v) // 2]  # noqa: E731
     span = lambda a, b: [tev[a][i].elapsed_time(tev[b][i]) for i in range(args.steps)]  # noqa: E731
     comp_ms = span("c0", "c1")
@@ -714,6 +723,7 @@ def main():
         "gap_ms_mean": sum(gaps) / len(gaps) if gaps else 0.0,
         "device_only_step_ms_median": per_step[len(per_step) // 2],
         "host_enqueue_ms_max": host_ms,
+        "passes_ms": [round(p[0][0], 4) for p in passes],
     }
     ms_e2e, e2e_value = aggregate_over_ranks(ms_e2e, flops, args.steps, world,
                                              dist if world > 1 else None, "cuda")
