@@ -35,6 +35,7 @@
 // Every wait is bounded; a timeout is recorded in the status word.
 #include "common.cuh"
 #include "kernels.h"
+#include "tile_layout.h"
 
 namespace mtl {
 namespace attn {
@@ -103,39 +104,15 @@ __device__ __forceinline__ void load_box(uint32_t dst, const CUtensorMap* m, uin
   if (MTL_CHECKED(status, bounds::check_tma_load(b, x, y), site)) tma_load_2d(dst, m, bar, x, y);
 }
 
-// Shared-memory layout of a 128-row bf16 operand tile of d = 16 KS columns:
-// atoms of 128 rows x ACOLS columns, each the box of one TMA load, swizzled as
-// the tensor map says.  d = 64 and 128: 64-column atoms with 128-byte swizzle;
-// d = 96: three 32-column atoms with 64-byte swizzle (24 KB a tile, where two
-// 64-column atoms take 32 KB with a quarter of it unused).
+// The operand tile layout (tile_layout.h) with its tcgen05 descriptors: K-major
+// with 8-row groups ROWB * 8 bytes apart; MN-major with the N atoms ATOM bytes
+// apart.
 template <int KS>
-struct Fmt {
-  static constexpr int D = KS * 16;
-  static constexpr bool SW64 = D % 64 != 0;
-  static constexpr int ACOLS = SW64 ? 32 : 64;
-  static constexpr int ATOMS = D / ACOLS;
-  static constexpr uint32_t ROWB = ACOLS * 2;           // bytes of an atom row
-  static constexpr uint32_t ATOM = 128 * ROWB;
-  static constexpr uint32_t TILE = ATOMS * ATOM;
-  static constexpr int KPA = ACOLS / 16;                // 16-column k-steps per atom
-  static constexpr uint32_t MODE = SW64 ? kDescSw64 : kDescSw128;
-  static_assert(D % ACOLS == 0, "a tile is whole atoms");
-  // K-major operand: k-step kk at byte 32 (kk % KPA) of the rows of atom kk / KPA;
-  // 8-row groups ROWB * 8 bytes apart
-  __host__ __device__ static constexpr uint32_t koff(int kk) {
-    return (uint32_t)(kk / KPA) * ATOM + (uint32_t)(kk % KPA) * 32;
-  }
-  __device__ static uint64_t kdesc(uint32_t a) { return smem_desc(a, 16, 8 * ROWB, MODE); }
-  // MN-major operand (the tile's rows are the K dimension): k-step kk is rows
-  // 16 kk .. 16 kk + 15; the N atoms are ATOM bytes apart
-  __host__ __device__ static constexpr uint32_t mnoff(int kk) { return (uint32_t)kk * 16 * ROWB; }
-  __device__ static uint64_t mndesc(uint32_t a) { return smem_desc(a, ATOM, 8 * ROWB, MODE); }
-  // byte offset of 16-byte chunk c (columns 8c .. 8c + 7) of row r
-  __device__ static uint32_t chunk(int r, int c) {
-    constexpr int CPA = ACOLS / 8;
-    const int sw = SW64 ? ((r >> 1) & 3) : (r & 7);
-    return (uint32_t)(c / CPA) * ATOM + (uint32_t)r * ROWB + ((uint32_t)((c % CPA) ^ sw) << 4);
-  }
+struct Fmt : layout::TileFmt<KS> {
+  using L = layout::TileFmt<KS>;
+  static constexpr uint32_t MODE = L::SW64 ? kDescSw64 : kDescSw128;
+  __device__ static uint64_t kdesc(uint32_t a) { return smem_desc(a, 16, 8 * L::ROWB, MODE); }
+  __device__ static uint64_t mndesc(uint32_t a) { return smem_desc(a, L::ATOM, 8 * L::ROWB, MODE); }
 };
 
 struct Smem {
@@ -162,9 +139,7 @@ __device__ __forceinline__ Smem smem_aligned(uint8_t* raw) {
 constexpr uint32_t STAGE_WARP_BYTES = 32 * 64;
 constexpr uint32_t STAGE_BYTES = 8 * STAGE_WARP_BYTES;   // the eight row warps
 
-__device__ __forceinline__ uint32_t stage_off(int row, int piece) {
-  return (uint32_t)(row * 64 + ((piece ^ ((row >> 1) & 3)) << 4));
-}
+__device__ __forceinline__ uint32_t stage_off(int row, int piece) { return layout::sw64_off(row, piece); }
 
 // 32 fp32 TMEM columns at taddr (this lane's row), times sc, as bf16 to the
 // box of 32 columns x 32 rows at (x, y) of the tensor map m (y: the warp's
