@@ -199,7 +199,8 @@ __device__ __forceinline__ bool store_box_ok(unsigned* status, int x, int y, int
 // issuer, 3 register donor, 4..7 row threads of tile A, 8..11 of tile B.  The
 // two MMA streams touch disjoint TMEM columns and each commit tracks only its
 // own thread's MMAs, so neither issuer waits on the other's dependencies.
-// smem: Q_A, Q_B, ring[FWD_RING] (tiles in the Fmt layout), item ids.
+// smem: Q_A, Q_B, ring[FWD_RING] (tiles in the Fmt layout), the epilogue
+// staging buffers, item ids.
 // TMEM: S cols 0..127, P_A 128..191, P_B 192..255, O_A 256.., O_B 384..
 constexpr int FWD_RING = 4;
 static_assert(FWD_RING % 2 == 0, "K and V must keep to their own ring slots");
@@ -756,7 +757,8 @@ __host__ __device__ constexpr int dq_q_bufs(uint32_t tile) { return dq_need(tile
 // kernel.  An item's dQ is written out when the rows have formed the next
 // item's D (its last dQ product done), while that item's first S and dP are
 // on their way; the first dQ product of the next item waits for its dS.
-// smem: Q, dO, O, ring[BWD_RING] (tiles in the Fmt layout), item ids.  Of the
+// smem: Q and dO (two pairs where they fit: dq_q_bufs), O, ring[BWD_RING]
+// (tiles in the Fmt layout), the halves of D, item ids.  Of the
 // ring, DQ_KSLOTS slots hold K blocks and one holds V: K(j) stays until dQ +=
 // dS K(j) has read it, about a block after S, so K is loaded up to two blocks
 // ahead; V(j) is free once dP(j) is done, and V(j + 1) loads while the rows
@@ -1128,7 +1130,8 @@ __host__ __device__ constexpr int dkv_kv_bufs(uint32_t tile) { return dkv_need(t
 // dO and dK += dS^T Q (warp 2, A operands from TMEM).  An item's dK and dV are
 // written out when the rows take the next item (its last dV and dK products
 // done), while that item's K, V and first S^T are on their way.
-// smem: K, V, ring[BWD_RING] (tiles in the Fmt layout), lse and D of the two Q
+// smem: K and V (two pairs where they fit: dkv_kv_bufs), ring[BWD_RING] (tiles
+// in the Fmt layout), the epilogue staging buffers, lse and D of the two Q
 // slots, item ids.  TMEM: S^T / dP^T 0..127, P^T 128..191, dS^T 192..255,
 // dV 256.., dK 384..
 constexpr uint32_t TK_S = 0, TK_P = 128, TK_DS = 192, TK_DV = 256, TK_DK = 384;
