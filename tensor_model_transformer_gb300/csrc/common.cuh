@@ -297,6 +297,11 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 }
 
 // ---------------------------------------------------------------- TMA
+// Brings the 128-byte line holding `p` into L2 (no register or shared-memory
+// cost; the load that later reads it hits L2).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }

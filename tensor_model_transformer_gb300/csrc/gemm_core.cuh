@@ -458,6 +458,16 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t tmem_bas
     const int colbase = nb * BN + chalf * 128;
     const bool split = SPLIT && pc.split;
     float* sreg = split ? split_region(pc.sk, pc.slot) : nullptr;
+    // R or Z of this lane's row of the piece (two 128-byte lines) into L2 now,
+    // so the epilogue's loads of it, after the piece's products, hit L2
+    if constexpr (SIDE) {
+      if (!split && row < p.M && colbase + 128 <= p.N) {
+        const bf16* src = EPI == EPI_DGELU ? p.Z + (size_t)row * p.ldz + colbase
+                                           : p.R + (size_t)row * p.ldr + colbase;
+        prefetch_l2(src);
+        prefetch_l2(src + 64);
+      }
+    }
     uint4 side[4];
     if (!REDUCE && AHEAD && !split) side_load(row, colbase, side);
     // the running partition sum starts at +0 in every piece, so no value of it
