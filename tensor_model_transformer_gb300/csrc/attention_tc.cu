@@ -723,17 +723,6 @@ __device__ __forceinline__ void sched_done(unsigned* sched) {
   }
 }
 
-// 64 bf16 (packed pairs) of a row into 32 TMEM columns.
-__device__ __forceinline__ void store_bf16_64(uint32_t taddr, const float (&v)[64]) {
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    uint32_t pk[16];
-#pragma unroll
-    for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(v[32 * q + 2 * c], v[32 * q + 2 * c + 1]);
-    tmem_st16(taddr + 16 * q, pk);
-  }
-}
-
 constexpr int BWD_LAUNCH_REGS = 168, BWD_LOW_REGS = 72, BWD_ROW_REGS = 216;
 static_assert(BWD_THREADS == 384, "one giving and two taking warps per sub-partition");
 static_assert(BWD_LOW_REGS + 2 * BWD_ROW_REGS <= 3 * BWD_LAUNCH_REGS,
